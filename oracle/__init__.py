@@ -1,0 +1,281 @@
+"""ctypes binding of the fp64 CPU oracle (``tp_oracle.c``).
+
+TEST INFRASTRUCTURE.  Only the test-suite, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline leg may import this package.  It is independent of the
+CUDA path: it shares no code with it and never imports it.
+
+Inputs are numpy arrays (converted to contiguous float64); results are float64
+numpy arrays.  Layouts follow the C source: row-major, weights ``W[out, in]``.
+Each wrapper cites the passage its C routine follows (see ``tp_oracle.c``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+OK = 0
+ERR_INVALID = 1
+ERR_NOT_DIVISIBLE = 2
+ERR_NOMEM = 3
+
+ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "none": 3}
+
+_lib = None
+_D = C.POINTER(C.c_double)
+_F = C.POINTER(C.c_float)
+_I64 = C.c_int64
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        sig = {
+            "tpo_num_threads": (C.c_int, []),
+            "tpo_gelu_erf": (C.c_double, [C.c_double]),
+            "tpo_gelu_tanh": (C.c_double, [C.c_double]),
+            "tpo_silu": (C.c_double, [C.c_double]),
+            "tpo_round_bf16": (C.c_uint16, [C.c_double]),
+            "tpo_linear": (None, [_D, _I64, _D, _I64, _I64, _I64, _I64, _D, _I64]),
+            "tpo_mlp": (C.c_int, [C.c_int, _I64, _I64, _I64, _D, _D, _D, _D, _D]),
+            "tpo_mlp_sharded": (C.c_int, [C.c_int, _I64, _I64, _I64, _I64, _D, _D, _D, _D, _D, _D]),
+            "tpo_mlp_worked_f32": (C.c_int, [C.c_int, _I64, _I64, _I64, _I64, _F, _F, _F, _F]),
+            "tpo_plan_check": (C.c_int, [_I64] * 6),
+            "tpo_q_head_shard": (_I64, [_I64] * 3),
+            "tpo_q_head_kv": (_I64, [_I64] * 3),
+            "tpo_shard_kv_first": (_I64, [_I64] * 3),
+            "tpo_shard_kv_count": (_I64, [_I64] * 2),
+            "tpo_attention_core": (C.c_int, [_I64] * 5 + [_D, _I64, _D, _D, _I64, _D, _I64]),
+            "tpo_attention": (C.c_int, [_I64] * 6 + [_D] * 7),
+            "tpo_attention_sharded": (C.c_int, [_I64] * 7 + [_D] * 7),
+            "tpo_reduce": (C.c_int, [_I64] * 3 + [_D] * 4),
+            "tpo_rmsnorm": (C.c_int, [_I64, _I64, C.c_double, _D, _D]),
+            "tpo_layer": (C.c_int, [_I64] * 8 + [C.c_int, C.c_double] + [_D] * 9),
+            "tpo_layer_rows": (C.c_int, [_I64] * 7 + [C.c_double] + [_D] * 8
+                               + [_I64, C.POINTER(C.c_int64), _D]),
+            "tpo_attention_rows": (C.c_int, [_I64] * 6 + [_D] * 5
+                                   + [_I64, C.POINTER(C.c_int64), _D]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+class OracleError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code}")
+        self.code = code
+
+
+def _d(a) -> np.ndarray:
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor -> float64 numpy (exact widening of bf16/fp32)
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(_D)
+
+
+def _check(fn, rc):
+    if rc != OK:
+        raise OracleError(fn, rc)
+
+
+def num_threads() -> int:
+    return lib().tpo_num_threads()
+
+
+def gelu_erf(x: float) -> float:
+    return lib().tpo_gelu_erf(float(x))
+
+
+def gelu_tanh(x: float) -> float:
+    return lib().tpo_gelu_tanh(float(x))
+
+
+def silu(x: float) -> float:
+    return lib().tpo_silu(float(x))
+
+
+def round_bf16_bits(values) -> np.ndarray:
+    """bf16 bit patterns (uint16) of values, round-to-nearest-even."""
+    v = np.asarray(values, dtype=np.float64).ravel()
+    L = lib()
+    return np.array([L.tpo_round_bf16(float(x)) for x in v], dtype=np.uint16)
+
+
+def linear(X, W) -> np.ndarray:
+    """Y = X W^T."""
+    X, W = _d(X), _d(W)
+    M, K = X.shape
+    N = W.shape[0]
+    Y = np.empty((M, N))
+    lib().tpo_linear(_p(X), K, _p(W), W.shape[1], M, N, K, _p(Y), N)
+    return Y
+
+
+def mlp(act: str, X, W1, W2, W3=None) -> np.ndarray:
+    """Unsharded MLP: act(X W1^T [(.) X W3^T]) W2^T."""
+    X, W1, W2, W3 = _d(X), _d(W1), _d(W2), _d(W3)
+    M, h = X.shape
+    f = W1.shape[0]
+    Z = np.empty((M, h))
+    _check("tpo_mlp", lib().tpo_mlp(ACT[act], M, h, f, _p(X), _p(W1), _p(W3), _p(W2), _p(Z)))
+    return Z
+
+
+def mlp_sharded(act: str, t: int, X, W1, W2, W3=None, want_partials: bool = False):
+    """Literal t-shard MLP: sum_i act(X W1_i^T [(.) X W3_i^T]) W2_i^T."""
+    X, W1, W2, W3 = _d(X), _d(W1), _d(W2), _d(W3)
+    M, h = X.shape
+    f = W1.shape[0]
+    Z = np.empty((M, h))
+    P = np.empty((t, M, h)) if want_partials else None
+    _check("tpo_mlp_sharded", lib().tpo_mlp_sharded(ACT[act], M, h, f, t, _p(X), _p(W1), _p(W3),
+                                                     _p(W2), _p(P), _p(Z)))
+    return (Z, P) if want_partials else Z
+
+
+def mlp_worked_f32(sharded: bool, t: int, X, A, B) -> np.ndarray:
+    """fp32 restatement of the page's worked example (A[h,f], B[f,h])."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    b, h = X.shape
+    f = A.shape[1]
+    Z = np.empty((b, h), dtype=np.float32)
+    _check("tpo_mlp_worked_f32", lib().tpo_mlp_worked_f32(
+        1 if sharded else 0, b, h, f, t, X.ctypes.data_as(_F), A.ctypes.data_as(_F),
+        B.ctypes.data_as(_F), Z.ctypes.data_as(_F)))
+    return Z
+
+
+def plan_check(h: int, f: int, a: int, k: int, d: int, t: int) -> int:
+    return lib().tpo_plan_check(h, f, a, k, d, t)
+
+
+def q_head_shard(a: int, t: int, j: int) -> int:
+    return lib().tpo_q_head_shard(a, t, j)
+
+
+def q_head_kv(a: int, k: int, j: int) -> int:
+    return lib().tpo_q_head_kv(a, k, j)
+
+
+def shard_kv_first(k: int, t: int, i: int) -> int:
+    return lib().tpo_shard_kv_first(k, t, i)
+
+
+def shard_kv_count(k: int, t: int) -> int:
+    return lib().tpo_shard_kv_count(k, t)
+
+
+def attention_core(batch: int, seq: int, a: int, k: int, d: int, Q, K, V) -> np.ndarray:
+    """Causal GQA attention core: Q[M, a d], K/V[M, k d] -> O[M, a d]."""
+    Q, K, V = _d(Q), _d(K), _d(V)
+    M = batch * seq
+    O = np.empty((M, a * d))
+    _check("tpo_attention_core", lib().tpo_attention_core(
+        batch, seq, a, k, d, _p(Q), Q.shape[1], _p(K), _p(V), K.shape[1], _p(O), a * d))
+    return O
+
+
+def attention(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo,
+              want_O: bool = False):
+    """Unsharded attention block: (causal GQA attn of X Wq^T, X Wk^T, X Wv^T) Wo^T."""
+    X, Wq, Wk, Wv, Wo = map(_d, (X, Wq, Wk, Wv, Wo))
+    M, h = X.shape
+    out = np.empty((M, h))
+    O = np.empty((M, a * d)) if want_O else None
+    _check("tpo_attention", lib().tpo_attention(batch, seq, h, a, k, d, _p(X), _p(Wq), _p(Wk),
+                                                _p(Wv), _p(Wo), _p(O), _p(out)))
+    return (out, O) if want_O else out
+
+
+def attention_sharded(batch: int, seq: int, a: int, k: int, d: int, t: int, X, Wq, Wk, Wv, Wo,
+                      want_partials: bool = False):
+    """Literal head-sharded attention block, out = sum_i O_i Wo_i^T."""
+    X, Wq, Wk, Wv, Wo = map(_d, (X, Wq, Wk, Wv, Wo))
+    M, h = X.shape
+    out = np.empty((M, h))
+    P = np.empty((t, M, h)) if want_partials else None
+    _check("tpo_attention_sharded", lib().tpo_attention_sharded(
+        batch, seq, h, a, k, d, t, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(P), _p(out)))
+    return (out, P) if want_partials else out
+
+
+def reduce(partials, bias=None, residual=None) -> np.ndarray:
+    """g forward: sum_i partials[i] (+ bias once) (+ residual)."""
+    P = _d(partials)
+    t = P.shape[0]
+    h = P.shape[-1]
+    n = int(np.prod(P.shape[1:]))
+    b, r = _d(bias), _d(residual)
+    out = np.empty(P.shape[1:])
+    _check("tpo_reduce", lib().tpo_reduce(t, n, h, _p(P), _p(b), _p(r), _p(out)))
+    return out
+
+
+def rmsnorm(x, eps: float = 1e-5) -> np.ndarray:
+    x = _d(x)
+    M, h = x.shape
+    y = np.empty_like(x)
+    _check("tpo_rmsnorm", lib().tpo_rmsnorm(M, h, float(eps), _p(x), _p(y)))
+    return y
+
+
+def layer(batch: int, seq: int, a: int, k: int, d: int, t: int, X, Wq, Wk, Wv, Wo, W1, W3, W2,
+          sharded: bool = False, eps: float = 1e-5) -> np.ndarray:
+    """Pre-norm layer: h1 = x + Attn(RMSNorm(x)); y = h1 + SwiGLU-MLP(RMSNorm(h1))."""
+    X, Wq, Wk, Wv, Wo, W1, W3, W2 = map(_d, (X, Wq, Wk, Wv, Wo, W1, W3, W2))
+    M, h = X.shape
+    f = W1.shape[0]
+    Y = np.empty((M, h))
+    _check("tpo_layer", lib().tpo_layer(batch, seq, h, a, k, d, f, t, 1 if sharded else 0,
+                                        float(eps), _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo),
+                                        _p(W1), _p(W3), _p(W2), _p(Y)))
+    return Y
+
+
+def _rows(rows: Sequence[int]):
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return r, r.ctypes.data_as(C.POINTER(C.c_int64))
+
+
+def layer_rows(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo, W1, W3, W2,
+               rows: Sequence[int], eps: float = 1e-5) -> np.ndarray:
+    """The layer's output at chosen token rows only (exact same definition)."""
+    X, Wq, Wk, Wv, Wo, W1, W3, W2 = map(_d, (X, Wq, Wk, Wv, Wo, W1, W3, W2))
+    h = X.shape[1]
+    f = W1.shape[0]
+    r, rp = _rows(rows)
+    Y = np.empty((len(r), h))
+    _check("tpo_layer_rows", lib().tpo_layer_rows(batch, seq, h, a, k, d, f, float(eps), _p(X),
+                                                  _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(W1),
+                                                  _p(W3), _p(W2), len(r), rp, _p(Y)))
+    return Y
+
+
+def attention_rows(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo,
+                   rows: Sequence[int]) -> np.ndarray:
+    """The attention block's output at chosen token rows only."""
+    X, Wq, Wk, Wv, Wo = map(_d, (X, Wq, Wk, Wv, Wo))
+    h = X.shape[1]
+    r, rp = _rows(rows)
+    out = np.empty((len(r), h))
+    _check("tpo_attention_rows", lib().tpo_attention_rows(batch, seq, h, a, k, d, _p(X), _p(Wq),
+                                                          _p(Wk), _p(Wv), _p(Wo), len(r), rp,
+                                                          _p(out)))
+    return out

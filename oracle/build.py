@@ -1,0 +1,36 @@
+"""Compile the C oracle into oracle/_build/libtp_oracle.so with gcc.
+
+Test infrastructure: building the checker is not using it.  Plain C11 with
+OpenMP; no architecture-specific flags, so the same source builds on x86_64
+and aarch64 hosts.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "tp_oracle.c")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "libtp_oracle.so")
+
+
+def needs_build() -> bool:
+    return (not os.path.exists(LIB)) or os.path.getmtime(LIB) < os.path.getmtime(SRC)
+
+
+def build(force: bool = False) -> str:
+    if not force and not needs_build():
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,527 @@
+/*
+ * tp_oracle.c -- plain, slow, fp64 CPU oracle of the Megatron-style
+ * tensor-parallel transformer block.
+ *
+ * TEST INFRASTRUCTURE.  Only the test-suite, the smoke check and the bench's
+ * CPU-baseline leg load this library.  The CUDA product path never links,
+ * imports or calls it, and it shares no code, header or table with that path.
+ *
+ * Every routine is the plain definition written out with straightforward
+ * loops in double precision, with no blocking, fusion or reordering beyond
+ * what the definition states.  OpenMP only splits independent output rows
+ * across threads; the arithmetic of every output element is unchanged.
+ *
+ * Sources (web pages; cited by title and section):
+ *  - "텐서 병렬화" (itwiki, Tensor parallelism): sections "행렬 곱 나누기"
+ *    (splitting a matrix product: column- and row-parallel table), "MLP"
+ *    (Z = GeLU(XA)B = sum_i GeLU(X A_i) B_i; SwiGLU form
+ *    W2(SiLU(X W1) (.) X W3)), "셀프 어텐션" (self-attention: heads are
+ *    independent, a/t heads per device, GQA KV heads replicated when fewer
+ *    than t), "통신 연산 f와 g" (f = identity forward, g = all-reduce forward;
+ *    norm, dropout and residual replicated).
+ *  - "추론을 위한 텐서 병렬성" (transformers docs, Tensor parallelism for
+ *    inference), section "설계 구현 / DTensor": a rowwise layer's bias is
+ *    replicated and added once after the reduction.
+ *  - "Tensor 병렬성" (diffusers docs), section "제약 조건 및 검증"
+ *    (constraints and validation): tp_degree must divide the head count.
+ *
+ * Layouts: row-major; weights use the nn.Linear layout W[out][in]; the pages'
+ * A (h x f, Y = XA) is W1 transposed.  Activations are [tokens][features],
+ * tokens = batch * seq with sequence-major order (token = b * seq + p).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define TPO_OK 0
+#define TPO_ERR_INVALID 1
+#define TPO_ERR_NOT_DIVISIBLE 2
+#define TPO_ERR_NOMEM 3
+
+#define TPO_ACT_GELU_ERF 0
+#define TPO_ACT_GELU_TANH 1
+#define TPO_ACT_SWIGLU 2
+#define TPO_ACT_NONE 3
+
+int tpo_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- scalars */
+
+/* GeLU, exact form x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)).  The worked MLP
+ * example ("MLP" section) calls torch's F.gelu, whose default is this form. */
+double tpo_gelu_erf(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/* GeLU, tanh approximation (an option; the pages never name it). */
+double tpo_gelu_tanh(double x) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+/* SiLU(x) = x * sigmoid(x), the gate of the SwiGLU MLP ("MLP" section). */
+double tpo_silu(double x) { return x / (1.0 + exp(-x)); }
+
+static double act_scalar(int act, double x) {
+    switch (act) {
+    case TPO_ACT_GELU_ERF: return tpo_gelu_erf(x);
+    case TPO_ACT_GELU_TANH: return tpo_gelu_tanh(x);
+    case TPO_ACT_SWIGLU: return tpo_silu(x);
+    default: return x;
+    }
+}
+
+/* Round a double to the nearest bf16 (ties to even), returning its bits.
+ * Used only where a test compares a value that is exactly representable in
+ * fp32 (integer-valued data), so rounding straight from double is the same
+ * decision the GPU takes from fp32. */
+uint16_t tpo_round_bf16(double x) {
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)(u >> 16); /* inf/nan */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* ---------------------------------------------------------------- linear */
+
+/* Y[m][n] = sum_k X[m][k] * W[n][k]   (Y = X W^T, nn.Linear without bias).
+ * Row strides ldx, ldw, ldy are in elements. */
+void tpo_linear(const double* X, int64_t ldx, const double* W, int64_t ldw,
+                int64_t M, int64_t N, int64_t K, double* Y, int64_t ldy) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const double* x = X + m * ldx;
+        for (int64_t n = 0; n < N; ++n) {
+            const double* w = W + n * ldw;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += x[k] * w[k];
+            Y[m * ldy + n] = s;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- MLP */
+
+/* Unsharded MLP ("MLP" section):
+ *   GeLU / none :  Z = act(X W1^T) W2^T            (the page's GeLU(XA)B)
+ *   SwiGLU      :  Z = (SiLU(X W1^T) (.) (X W3^T)) W2^T
+ * X[M][h], W1/W3[f][h], W2[h][f], Z[M][h]. */
+int tpo_mlp(int act, int64_t M, int64_t h, int64_t f, const double* X,
+            const double* W1, const double* W3, const double* W2, double* Z) {
+    if (M < 0 || h <= 0 || f <= 0 || !X || !W1 || !W2 || !Z) return TPO_ERR_INVALID;
+    if (act == TPO_ACT_SWIGLU && !W3) return TPO_ERR_INVALID;
+    double* U = (double*)malloc(sizeof(double) * (size_t)(M * f + 1));
+    double* G = NULL;
+    if (!U) return TPO_ERR_NOMEM;
+    tpo_linear(X, h, W1, h, M, f, h, U, f);
+    if (act == TPO_ACT_SWIGLU) {
+        G = (double*)malloc(sizeof(double) * (size_t)(M * f + 1));
+        if (!G) { free(U); return TPO_ERR_NOMEM; }
+        tpo_linear(X, h, W3, h, M, f, h, G, f);
+        for (int64_t e = 0; e < M * f; ++e) U[e] = tpo_silu(U[e]) * G[e];
+    } else {
+        for (int64_t e = 0; e < M * f; ++e) U[e] = act_scalar(act, U[e]);
+    }
+    tpo_linear(U, f, W2, f, M, h, f, Z, h);
+    free(U);
+    free(G);
+    return TPO_OK;
+}
+
+/* Sharded MLP, the literal t-device form ("MLP" section, and the column /
+ * row-parallel table of "행렬 곱 나누기"):
+ *   A_i = columns [i f/t, (i+1) f/t) of A      = rows of W1 (and W3)
+ *   B_i = rows    [i f/t, (i+1) f/t) of B      = columns of W2
+ *   Y_i = act(X A_i)            (no communication: X is replicated, f = id)
+ *   P_i = Y_i B_i               (the partial sum device i holds)
+ *   Z   = sum_{i=0}^{t-1} P_i   (g: the one all-reduce), summed i ascending
+ * Chunks are contiguous and equal, so t must divide f.
+ * partials (nullable) receives P_i as [t][M][h]. */
+int tpo_mlp_sharded(int act, int64_t M, int64_t h, int64_t f, int64_t t,
+                    const double* X, const double* W1, const double* W3,
+                    const double* W2, double* partials, double* Z) {
+    if (M < 0 || h <= 0 || f <= 0 || t <= 0 || !X || !W1 || !W2 || !Z) return TPO_ERR_INVALID;
+    if (act == TPO_ACT_SWIGLU && !W3) return TPO_ERR_INVALID;
+    if (f % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t w = f / t;
+    double* Y = (double*)malloc(sizeof(double) * (size_t)(M * w + 1));
+    double* G = (double*)malloc(sizeof(double) * (size_t)(M * w + 1));
+    double* P = (double*)malloc(sizeof(double) * (size_t)(t * M * h + 1));
+    if (!Y || !G || !P) { free(Y); free(G); free(P); return TPO_ERR_NOMEM; }
+    for (int64_t i = 0; i < t; ++i) {
+        const double* W1_i = W1 + i * w * h;          /* rows of W1 */
+        tpo_linear(X, h, W1_i, h, M, w, h, Y, w);
+        if (act == TPO_ACT_SWIGLU) {
+            const double* W3_i = W3 + i * w * h;
+            tpo_linear(X, h, W3_i, h, M, w, h, G, w);
+            for (int64_t e = 0; e < M * w; ++e) Y[e] = tpo_silu(Y[e]) * G[e];
+        } else {
+            for (int64_t e = 0; e < M * w; ++e) Y[e] = act_scalar(act, Y[e]);
+        }
+        const double* W2_i = W2 + i * w;               /* columns of W2, row stride f */
+        tpo_linear(Y, w, W2_i, f, M, h, w, P + i * M * h, h);
+    }
+    for (int64_t e = 0; e < M * h; ++e) {
+        double s = 0.0;
+        for (int64_t i = 0; i < t; ++i) s += P[i * M * h + e];
+        Z[e] = s;
+    }
+    if (partials) memcpy(partials, P, sizeof(double) * (size_t)(t * M * h));
+    free(Y);
+    free(G);
+    free(P);
+    return TPO_OK;
+}
+
+/* Single-precision restatement of the worked example's two forms (the page's
+ * listing runs in fp32 and compares with atol 1e-4).  A is [h][f] and B is
+ * [f][h] in the page's own orientation (Y = XA).  sharded != 0 selects
+ * sum_i GeLU(X A_i) B_i, else GeLU(XA)B.  Accumulation is float. */
+int tpo_mlp_worked_f32(int sharded, int64_t b, int64_t h, int64_t f, int64_t t,
+                       const float* X, const float* A, const float* B, float* Z) {
+    if (b <= 0 || h <= 0 || f <= 0 || t <= 0 || (f % t)) return TPO_ERR_INVALID;
+    const int64_t nsh = sharded ? t : 1, w = f / nsh;
+    for (int64_t e = 0; e < b * h; ++e) Z[e] = 0.0f;
+    float* Y = (float*)malloc(sizeof(float) * (size_t)(b * w));
+    float* P = (float*)malloc(sizeof(float) * (size_t)(b * h));
+    if (!Y || !P) { free(Y); free(P); return TPO_ERR_NOMEM; }
+    for (int64_t i = 0; i < nsh; ++i) {
+        for (int64_t r = 0; r < b; ++r)
+            for (int64_t c = 0; c < w; ++c) {
+                float s = 0.0f;
+                for (int64_t k = 0; k < h; ++k) s += X[r * h + k] * A[k * f + i * w + c];
+                Y[r * w + c] = 0.5f * s * (1.0f + erff(s / sqrtf(2.0f)));
+            }
+        for (int64_t r = 0; r < b; ++r)
+            for (int64_t c = 0; c < h; ++c) {
+                float s = 0.0f;
+                for (int64_t k = 0; k < w; ++k) s += Y[r * w + k] * B[(i * w + k) * h + c];
+                P[r * h + c] = s;
+            }
+        for (int64_t e = 0; e < b * h; ++e) Z[e] += P[e];
+    }
+    free(Y);
+    free(P);
+    return TPO_OK;
+}
+
+/* ---------------------------------------------------------------- plan */
+
+/* Validation of a t-way split ("제약 조건 및 검증" of the diffusers page:
+ * tp_degree must divide the attention heads; "셀프 어텐션" of the itwiki
+ * page: the head count must divide by t, KV heads are taken into account and
+ * replicated when fewer than t).  Reading for GQA: a % k == 0 (each KV head
+ * serves a/k consecutive query heads); if k >= t then t | k, else k | t.
+ * The MLP's column chunks are equal, so t | f.  Sizes of 0 mean "absent". */
+int tpo_plan_check(int64_t h, int64_t f, int64_t a, int64_t k, int64_t d, int64_t t) {
+    if (h <= 0 || t <= 0 || f < 0 || a < 0 || k < 0 || d < 0) return TPO_ERR_INVALID;
+    if (f > 0 && f % t) return TPO_ERR_NOT_DIVISIBLE;
+    if (a > 0) {
+        if (k <= 0 || d <= 0) return TPO_ERR_INVALID;
+        if (a % t) return TPO_ERR_NOT_DIVISIBLE;
+        if (a % k) return TPO_ERR_NOT_DIVISIBLE;
+        if (k >= t) { if (k % t) return TPO_ERR_NOT_DIVISIBLE; }
+        else if (t % k) return TPO_ERR_NOT_DIVISIBLE;
+    }
+    return TPO_OK;
+}
+
+/* Query head j lives on device floor(j / (a/t)) (a/t heads per device). */
+int64_t tpo_q_head_shard(int64_t a, int64_t t, int64_t j) { return j / (a / t); }
+
+/* Query head j reads KV head floor(j / (a/k)) (consecutive grouping). */
+int64_t tpo_q_head_kv(int64_t a, int64_t k, int64_t j) { return j / (a / k); }
+
+/* First KV head held by device i, and how many it holds: k/t own heads when
+ * k >= t, else one replica of KV head floor(i k / t). */
+int64_t tpo_shard_kv_first(int64_t k, int64_t t, int64_t i) {
+    return (k >= t) ? i * (k / t) : (i * k) / t;
+}
+int64_t tpo_shard_kv_count(int64_t k, int64_t t) { return (k >= t) ? k / t : 1; }
+
+/* ---------------------------------------------------------------- attention */
+
+/* Causal attention of one query row against KV rows 0..p of its sequence
+ * ("셀프 어텐션": per-head softmax attention; causal mask and the 1/sqrt(d)
+ * scale are the standard decoder reading).  q[d]; K/V rows at stride ld;
+ * o[d] receives sum_q softmax_q(q.K_q / sqrt d) V_q.  Softmax subtracts the
+ * row max before exponentiating. */
+static void attend_row(const double* q, const double* K, const double* V, int64_t ld,
+                       int64_t p, int64_t d, double* s, double* o) {
+    const double scale = 1.0 / sqrt((double)d);
+    double mx = -INFINITY;
+    for (int64_t r = 0; r <= p; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += q[c] * K[r * ld + c];
+        s[r] = acc * scale;
+        if (s[r] > mx) mx = s[r];
+    }
+    double sum = 0.0;
+    for (int64_t r = 0; r <= p; ++r) { s[r] = exp(s[r] - mx); sum += s[r]; }
+    for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t r = 0; r <= p; ++r) acc += s[r] * V[r * ld + c];
+        o[c] = acc / sum;
+    }
+}
+
+/* Attention core over all heads: Q[M][a d] (head j at columns j d),
+ * K, V [M][k d]; O[M][a d].  Sequences never attend across each other.
+ * Row strides ldq, ldkv, ldo in elements. */
+int tpo_attention_core(int64_t batch, int64_t seq, int64_t a, int64_t k, int64_t d,
+                       const double* Q, int64_t ldq, const double* K, const double* V,
+                       int64_t ldkv, double* O, int64_t ldo) {
+    if (batch < 0 || seq < 0 || a <= 0 || k <= 0 || d <= 0 || a % k) return TPO_ERR_INVALID;
+    const int64_t M = batch * seq;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(seq + 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t m = 0; m < M; ++m) {
+            const int64_t b = m / seq, p = m % seq;
+            for (int64_t j = 0; j < a; ++j) {
+                const int64_t g = tpo_q_head_kv(a, k, j);
+                attend_row(Q + m * ldq + j * d, K + b * seq * ldkv + g * d,
+                           V + b * seq * ldkv + g * d, ldkv, p, d, s, O + m * ldo + j * d);
+            }
+        }
+        free(s);
+    }
+    return TPO_OK;
+}
+
+/* Unsharded attention block: Q = X Wq^T, K = X Wk^T, V = X Wv^T, causal GQA
+ * attention per head, out = O Wo^T.  X[M][h], Wq[a d][h], Wk/Wv[k d][h],
+ * Wo[h][a d].  O_out (nullable) receives O[M][a d]. */
+int tpo_attention(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                  const double* X, const double* Wq, const double* Wk, const double* Wv,
+                  const double* Wo, double* O_out, double* out) {
+    if (batch < 0 || seq < 0 || h <= 0 || a <= 0 || k <= 0 || d <= 0 || a % k) return TPO_ERR_INVALID;
+    const int64_t M = batch * seq, qw = a * d, kw = k * d;
+    double* Q = (double*)malloc(sizeof(double) * (size_t)(M * qw + 1));
+    double* Kx = (double*)malloc(sizeof(double) * (size_t)(M * kw + 1));
+    double* Vx = (double*)malloc(sizeof(double) * (size_t)(M * kw + 1));
+    double* O = (double*)malloc(sizeof(double) * (size_t)(M * qw + 1));
+    if (!Q || !Kx || !Vx || !O) { free(Q); free(Kx); free(Vx); free(O); return TPO_ERR_NOMEM; }
+    tpo_linear(X, h, Wq, h, M, qw, h, Q, qw);
+    tpo_linear(X, h, Wk, h, M, kw, h, Kx, kw);
+    tpo_linear(X, h, Wv, h, M, kw, h, Vx, kw);
+    tpo_attention_core(batch, seq, a, k, d, Q, qw, Kx, Vx, kw, O, qw);
+    tpo_linear(O, qw, Wo, qw, M, h, qw, out, h);
+    if (O_out) memcpy(O_out, O, sizeof(double) * (size_t)(M * qw));
+    free(Q); free(Kx); free(Vx); free(O);
+    return TPO_OK;
+}
+
+/* Head-sharded attention, the literal t-device form ("셀프 어텐션"):
+ * device i takes query heads [i a/t, (i+1) a/t) -- its column block of Wq --
+ * and the KV heads those read (its own k/t heads, or a replica of one KV head
+ * when k < t), computes attention with no communication, multiplies by its
+ * column block of Wo (row-parallel o_proj) and leaves the partial P_i;
+ * out = sum_i P_i, i ascending (g).  partials (nullable): [t][M][h]. */
+int tpo_attention_sharded(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k,
+                          int64_t d, int64_t t, const double* X, const double* Wq,
+                          const double* Wk, const double* Wv, const double* Wo,
+                          double* partials, double* out) {
+    int rc = tpo_plan_check(h, 0, a, k, d, t);
+    if (rc) return rc;
+    const int64_t M = batch * seq, ap = a / t, kvn = tpo_shard_kv_count(k, t);
+    const int64_t qw = ap * d, kw = kvn * d, ad = a * d;
+    double* Q = (double*)malloc(sizeof(double) * (size_t)(M * qw + 1));
+    double* Kx = (double*)malloc(sizeof(double) * (size_t)(M * kw + 1));
+    double* Vx = (double*)malloc(sizeof(double) * (size_t)(M * kw + 1));
+    double* O = (double*)malloc(sizeof(double) * (size_t)(M * qw + 1));
+    double* P = (double*)malloc(sizeof(double) * (size_t)(t * M * h + 1));
+    if (!Q || !Kx || !Vx || !O || !P) {
+        free(Q); free(Kx); free(Vx); free(O); free(P);
+        return TPO_ERR_NOMEM;
+    }
+    for (int64_t i = 0; i < t; ++i) {
+        const int64_t kv0 = tpo_shard_kv_first(k, t, i);
+        tpo_linear(X, h, Wq + i * qw * h, h, M, qw, h, Q, qw);
+        tpo_linear(X, h, Wk + kv0 * d * h, h, M, kw, h, Kx, kw);
+        tpo_linear(X, h, Wv + kv0 * d * h, h, M, kw, h, Vx, kw);
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)(seq + 1));
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t m = 0; m < M; ++m) {
+                const int64_t b = m / seq, p = m % seq;
+                for (int64_t jl = 0; jl < ap; ++jl) {
+                    const int64_t j = i * ap + jl;
+                    const int64_t gl = tpo_q_head_kv(a, k, j) - kv0; /* local KV slot */
+                    attend_row(Q + m * qw + jl * d, Kx + b * seq * kw + gl * d,
+                               Vx + b * seq * kw + gl * d, kw, p, d, s, O + m * qw + jl * d);
+                }
+            }
+            free(s);
+        }
+        /* Row-parallel o_proj: columns [i a d / t, (i+1) a d / t) of Wo. */
+        tpo_linear(O, qw, Wo + i * qw, ad, M, h, qw, P + i * M * h, h);
+    }
+    for (int64_t e = 0; e < M * h; ++e) {
+        double s = 0.0;
+        for (int64_t i = 0; i < t; ++i) s += P[i * M * h + e];
+        out[e] = s;
+    }
+    if (partials) memcpy(partials, P, sizeof(double) * (size_t)(t * M * h));
+    free(Q); free(Kx); free(Vx); free(O); free(P);
+    return TPO_OK;
+}
+
+/* ---------------------------------------------------------------- g, norm */
+
+/* The g operator's forward on one device's view ("통신 연산 f와 g"): the sum
+ * of the t partials, i ascending; a rowwise bias is replicated and added once
+ * after the reduction (DTensor section of the transformers page); the
+ * replicated residual is added last.  partials[t][n]; bias[h] and residual[n]
+ * nullable; n is a multiple of h (rows of h features). */
+int tpo_reduce(int64_t t, int64_t n, int64_t h, const double* partials, const double* bias,
+               const double* residual, double* out) {
+    if (t <= 0 || n < 0 || h <= 0 || (n % h)) return TPO_ERR_INVALID;
+    for (int64_t e = 0; e < n; ++e) {
+        double s = 0.0;
+        for (int64_t i = 0; i < t; ++i) s += partials[i * n + e];
+        if (bias) s += bias[e % h];
+        if (residual) s += residual[e];
+        out[e] = s;
+    }
+    return TPO_OK;
+}
+
+/* RMSNorm with unit gain: y = x / sqrt(mean_j x_j^2 + eps), per row.  The
+ * norm is replicated on every device ("통신 연산 f와 g"). */
+int tpo_rmsnorm(int64_t M, int64_t h, double eps, const double* x, double* y) {
+    if (M < 0 || h <= 0) return TPO_ERR_INVALID;
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < h; ++j) ss += x[m * h + j] * x[m * h + j];
+        const double r = 1.0 / sqrt(ss / (double)h + eps);
+        for (int64_t j = 0; j < h; ++j) y[m * h + j] = x[m * h + j] * r;
+    }
+    return TPO_OK;
+}
+
+/* ---------------------------------------------------------------- layer */
+
+/* One pre-norm transformer layer ("통신 연산 f와 g": attention then MLP, one
+ * g after each; norm and residual replicated):
+ *   h1 = x + Attn(RMSNorm(x)),  y = h1 + MLP_SwiGLU(RMSNorm(h1)).
+ * sharded != 0 uses the literal t-device forms of both blocks. */
+int tpo_layer(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+              int64_t f, int64_t t, int sharded, double eps, const double* X,
+              const double* Wq, const double* Wk, const double* Wv, const double* Wo,
+              const double* W1, const double* W3, const double* W2, double* Y) {
+    int rc = tpo_plan_check(h, f, a, k, d, t);
+    if (rc) return rc;
+    const int64_t M = batch * seq;
+    double* xn = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    double* at = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    double* h1 = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    if (!xn || !at || !h1) { free(xn); free(at); free(h1); return TPO_ERR_NOMEM; }
+    tpo_rmsnorm(M, h, eps, X, xn);
+    rc = sharded ? tpo_attention_sharded(batch, seq, h, a, k, d, t, xn, Wq, Wk, Wv, Wo, NULL, at)
+                 : tpo_attention(batch, seq, h, a, k, d, xn, Wq, Wk, Wv, Wo, NULL, at);
+    if (!rc) {
+        for (int64_t e = 0; e < M * h; ++e) h1[e] = X[e] + at[e];
+        tpo_rmsnorm(M, h, eps, h1, xn);
+        rc = sharded ? tpo_mlp_sharded(TPO_ACT_SWIGLU, M, h, f, t, xn, W1, W3, W2, NULL, at)
+                     : tpo_mlp(TPO_ACT_SWIGLU, M, h, f, xn, W1, W3, W2, at);
+        if (!rc)
+            for (int64_t e = 0; e < M * h; ++e) Y[e] = h1[e] + at[e];
+    }
+    free(xn); free(at); free(h1);
+    return rc;
+}
+
+/* The same layer evaluated only at chosen tokens.  Causal attention makes
+ * token (b, p) depend on tokens (b, 0..p) alone, so this computes the
+ * normalised inputs and K/V projections of those positions and then the full
+ * definition for each requested token.  rows[] are token indices b*seq+p;
+ * Yrows[nrows][h].  With_mlp == 0 stops after h1 (attention block only) and
+ * returns h1 - x, i.e. the attention block's output, in Yrows. */
+static int layer_rows_impl(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k,
+                           int64_t d, int64_t f, double eps, int prenorm, int with_mlp,
+                           const double* X, const double* Wq, const double* Wk,
+                           const double* Wv, const double* Wo, const double* W1,
+                           const double* W3, const double* W2, int64_t nrows,
+                           const int64_t* rows, double* Yrows) {
+    const int64_t qw = a * d, kw = k * d;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= batch * seq) return TPO_ERR_INVALID;
+    double* xn = (double*)malloc(sizeof(double) * (size_t)(seq * h + 1));
+    double* Kx = (double*)malloc(sizeof(double) * (size_t)(seq * kw + 1));
+    double* Vx = (double*)malloc(sizeof(double) * (size_t)(seq * kw + 1));
+    double* q = (double*)malloc(sizeof(double) * (size_t)(qw + 1));
+    double* o = (double*)malloc(sizeof(double) * (size_t)(qw + 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(seq + 1));
+    double* v = (double*)malloc(sizeof(double) * (size_t)(h + 1));
+    double* vn = (double*)malloc(sizeof(double) * (size_t)(h + 1));
+    double* u = (double*)malloc(sizeof(double) * (size_t)(f + 1));
+    double* gt = (double*)malloc(sizeof(double) * (size_t)(f + 1));
+    int rc = TPO_OK;
+    if (!xn || !Kx || !Vx || !q || !o || !s || !v || !vn || !u || !gt) { rc = TPO_ERR_NOMEM; goto done; }
+    for (int64_t b = 0; b < batch; ++b) {
+        int64_t maxp = -1;
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] / seq == b && rows[r] % seq > maxp) maxp = rows[r] % seq;
+        if (maxp < 0) continue;
+        const double* xb = X + b * seq * h;
+        if (prenorm) tpo_rmsnorm(maxp + 1, h, eps, xb, xn);
+        else memcpy(xn, xb, sizeof(double) * (size_t)((maxp + 1) * h));
+        tpo_linear(xn, h, Wk, h, maxp + 1, kw, h, Kx, kw);
+        tpo_linear(xn, h, Wv, h, maxp + 1, kw, h, Vx, kw);
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (rows[r] / seq != b) continue;
+            const int64_t p = rows[r] % seq;
+            tpo_linear(xn + p * h, h, Wq, h, 1, qw, h, q, qw);
+            for (int64_t j = 0; j < a; ++j) {
+                const int64_t g = tpo_q_head_kv(a, k, j);
+                attend_row(q + j * d, Kx + g * d, Vx + g * d, kw, p, d, s, o + j * d);
+            }
+            tpo_linear(o, qw, Wo, qw, 1, h, qw, v, h);      /* attention output */
+            double* y = Yrows + r * h;
+            if (!with_mlp) { memcpy(y, v, sizeof(double) * (size_t)h); continue; }
+            for (int64_t j = 0; j < h; ++j) v[j] += xb[p * h + j];   /* h1 */
+            tpo_rmsnorm(1, h, eps, v, vn);
+            tpo_linear(vn, h, W1, h, 1, f, h, u, f);
+            tpo_linear(vn, h, W3, h, 1, f, h, gt, f);
+            for (int64_t j = 0; j < f; ++j) u[j] = tpo_silu(u[j]) * gt[j];
+            tpo_linear(u, f, W2, f, 1, h, f, y, h);
+            for (int64_t j = 0; j < h; ++j) y[j] += v[j];            /* y = h1 + mlp */
+        }
+    }
+done:
+    free(xn); free(Kx); free(Vx); free(q); free(o); free(s); free(v); free(vn); free(u); free(gt);
+    return rc;
+}
+
+int tpo_layer_rows(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                   int64_t f, double eps, const double* X, const double* Wq, const double* Wk,
+                   const double* Wv, const double* Wo, const double* W1, const double* W3,
+                   const double* W2, int64_t nrows, const int64_t* rows, double* Yrows) {
+    int rc = tpo_plan_check(h, f, a, k, d, 1);
+    if (rc) return rc;
+    return layer_rows_impl(batch, seq, h, a, k, d, f, eps, 1, 1, X, Wq, Wk, Wv, Wo, W1, W3,
+                           W2, nrows, rows, Yrows);
+}
+
+/* Attention block (no norm, no residual) at chosen tokens: out = O Wo^T. */
+int tpo_attention_rows(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                       const double* X, const double* Wq, const double* Wk, const double* Wv,
+                       const double* Wo, int64_t nrows, const int64_t* rows, double* out_rows) {
+    if (batch < 0 || seq < 0 || h <= 0 || a <= 0 || k <= 0 || d <= 0 || a % k) return TPO_ERR_INVALID;
+    return layer_rows_impl(batch, seq, h, a, k, d, 0, 0.0, 0, 0, X, Wq, Wk, Wv, Wo, NULL, NULL,
+                           NULL, nrows, rows, out_rows);
+}

@@ -1,0 +1,387 @@
+"""Pins of the fp64 CPU oracle to facts fixed outside the oracle itself.
+
+Each test ties one oracle routine to something independent of it: the worked
+example and the statements of the itwiki page "텐서 병렬화" (Tensor
+parallelism), closed forms, exact integer arithmetic, special cases that reduce
+to a library routine (scipy, numpy, torch fp64), or brute force on tiny sizes.
+The cases are chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a mis-grouped KV head) fails one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sp
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def f64(t):
+    return t.detach().double().numpy()
+
+
+# ---------------------------------------------------------------- scalars
+
+@pytest.mark.parametrize("x", [-6.0, -2.5, -1.0, -0.3, 0.0, 0.2, 1.0, 3.7, 8.0])
+def test_gelu_erf_is_x_times_normal_cdf(x):
+    # x * Phi(x) with Phi from scipy's ndtr (independent implementation).
+    assert oracle.gelu_erf(x) == pytest.approx(x * sp.ndtr(x), rel=1e-13, abs=1e-15)
+    # Phi(x) + Phi(-x) = 1  =>  gelu(x) - gelu(-x) = x.
+    assert oracle.gelu_erf(x) - oracle.gelu_erf(-x) == pytest.approx(x, abs=1e-13)
+
+
+def test_gelu_tanh_close_to_exact_but_distinct():
+    xs = np.linspace(-6, 6, 241)
+    diff = np.array([oracle.gelu_tanh(x) - oracle.gelu_erf(x) for x in xs])
+    assert np.abs(diff).max() < 1e-3          # the approximation's known accuracy
+    assert np.abs(diff).max() > 1e-5          # ... and it is a different function
+    assert oracle.gelu_tanh(0.0) == 0.0
+
+
+@pytest.mark.parametrize("x", [-9.0, -1.5, -0.1, 0.0, 0.4, 2.0, 11.0])
+def test_silu_is_x_times_logistic(x):
+    assert oracle.silu(x) == pytest.approx(x * sp.expit(x), rel=1e-13, abs=1e-15)
+    assert oracle.silu(x) - oracle.silu(-x) == pytest.approx(x, abs=1e-12)
+
+
+def test_round_bf16_matches_torch_rounding():
+    vals = np.array([0.0, 1.0, -1.0, 1.00390625, 1.005859375, 257.0, 259.0, 3.0e38, -7.25,
+                     1e-3, 65535.0, 33.0, 513.0, 1027.0])
+    want = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16)
+    want = want.numpy().astype(np.uint16)
+    assert np.array_equal(oracle.round_bf16_bits(vals), want)
+
+
+# ---------------------------------------------------------------- linear / MLP
+
+def test_linear_integer_inputs_exact():
+    rng = np.random.default_rng(5)
+    X = rng.integers(-3, 4, size=(7, 13))
+    W = rng.integers(-3, 4, size=(11, 13))
+    Y = oracle.linear(X, W)
+    assert np.array_equal(Y, (X @ W.T).astype(np.float64))   # X W^T, not W X or X W
+
+
+def test_worked_example_identity_holds_as_the_page_states():
+    g = json.load(open(os.path.join(GOLDEN, "worked_example.json")))
+    w = synth.worked_example()
+    X, A, B = (w[k].numpy() for k in "XAB")
+    assert X.shape == (g["b"], g["h"]) and A.shape == (g["h"], 4 * g["h"])
+    t = g["t"]
+    # fp32, the page's own precision: sum_i GeLU(X A_i) B_i vs GeLU(XA)B.
+    ref32 = oracle.mlp_worked_f32(False, t, X, A, B)
+    out32 = oracle.mlp_worked_f32(True, t, X, A, B)
+    assert np.allclose(out32, ref32, atol=g["atol"], rtol=g["rtol"]) == g["expect_allclose"]
+    # fp64: the identity is exact up to rounding.
+    ref = oracle.mlp("gelu", X, A.T, B.T)
+    out = oracle.mlp_sharded("gelu", t, X, A.T, B.T)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+    # The textbook unsharded MLP via torch fp64 (library gelu, matmul).
+    Xt, At, Bt = (torch.from_numpy(v).double() for v in (X, A, B))
+    tref = F.gelu(Xt @ At) @ Bt
+    assert np.abs(ref - tref.numpy()).max() <= 1e-12 * np.abs(ref).max()
+    # The fp32 restatement tracks fp64 to fp32 rounding.
+    assert np.abs(ref32 - ref).max() < 1e-3
+
+
+def test_worked_example_partials_are_the_per_device_products():
+    w = synth.worked_example()
+    X, A, B = (w[k].double() for k in "XAB")
+    Z, P = oracle.mlp_sharded("gelu", 4, X.numpy(), A.T.numpy(), B.T.numpy(), want_partials=True)
+    # Device i holds A.chunk(4, dim=1)[i] and B.chunk(4, dim=0)[i] (torch's chunk).
+    for i, (Ai, Bi) in enumerate(zip(A.chunk(4, dim=1), B.chunk(4, dim=0))):
+        want = (F.gelu(X @ Ai) @ Bi).numpy()
+        assert np.abs(P[i] - want).max() < 1e-12
+    assert np.abs(P.sum(0) - Z).max() < 1e-12
+
+
+def test_rowwise_split_before_gelu_is_not_an_identity():
+    # The page: GeLU(X1 A1 + X2 A2) != GeLU(X1 A1) + GeLU(X2 A2), so a rowwise A
+    # would need a sync before the nonlinearity.
+    w = synth.worked_example()
+    X, A, B = (w[k].numpy().astype(np.float64) for k in "XAB")
+    gelu = np.vectorize(oracle.gelu_erf)
+    ref = oracle.mlp("gelu", X, A.T, B.T)
+    for parts in (2, 4):
+        Xs = np.split(X, parts, axis=1)
+        As = np.split(A, parts, axis=0)
+        pre = [oracle.linear(Xi, Ai.T) for Xi, Ai in zip(Xs, As)]
+        wrong = sum(gelu(p) for p in pre)
+        right = gelu(sum(pre))
+        assert np.abs(wrong - right).max() > 1e-2
+        # With the sync before GeLU the rowwise split is exact again.
+        assert np.abs(oracle.linear(right, B.T) - ref).max() < 1e-12 * np.abs(ref).max() * 10
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "none"])
+def test_mlp_unsharded_matches_textbook_torch(act):
+    torch.manual_seed(3)
+    M, h, f = 9, 24, 40
+    X = torch.randn(M, h, dtype=torch.float64)
+    W1 = torch.randn(f, h, dtype=torch.float64) * 0.3
+    W3 = torch.randn(f, h, dtype=torch.float64) * 0.3
+    W2 = torch.randn(h, f, dtype=torch.float64) * 0.3
+    U = X @ W1.T
+    if act == "gelu":
+        H = F.gelu(U)
+    elif act == "gelu_tanh":
+        H = F.gelu(U, approximate="tanh")
+    elif act == "swiglu":
+        H = F.silu(U) * (X @ W3.T)
+    else:
+        H = U
+    want = (H @ W2.T).numpy()
+    got = oracle.mlp(act, X.numpy(), W1.numpy(), W2.numpy(), W3.numpy() if act == "swiglu" else None)
+    assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "gelu_tanh"])
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_mlp_sharded_equals_unsharded(act, t):
+    torch.manual_seed(10 + t)
+    M, h, f = 6, 16, 64
+    X = torch.randn(M, h, dtype=torch.float64)
+    W1 = torch.randn(f, h, dtype=torch.float64) * 0.5
+    W3 = torch.randn(f, h, dtype=torch.float64) * 0.5
+    W2 = torch.randn(h, f, dtype=torch.float64) * 0.5
+    w3 = W3.numpy() if act == "swiglu" else None
+    ref = oracle.mlp(act, X.numpy(), W1.numpy(), W2.numpy(), w3)
+    out = oracle.mlp_sharded(act, t, X.numpy(), W1.numpy(), W2.numpy(), w3)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_mlp_sharded_identity_activation_is_exact_integer_product():
+    X = synth.integer_bf16((5, 32), -2, 2, 1).double().numpy()
+    W1 = synth.integer_bf16((48, 32), -2, 2, 2).double().numpy()
+    W2 = synth.integer_bf16((32, 48), -2, 2, 3).double().numpy()
+    Z = oracle.mlp_sharded("none", 4, X, W1, W2)
+    Xi, W1i, W2i = (v.astype(np.int64) for v in (X, W1, W2))
+    assert np.array_equal(Z, ((Xi @ W1i.T) @ W2i.T).astype(np.float64))
+
+
+def test_mlp_sharded_rejects_uneven_chunks():
+    X = np.zeros((2, 8))
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.mlp_sharded("gelu", 3, X, np.zeros((16, 8)), np.zeros((8, 16)))
+    assert e.value.code == oracle.ERR_NOT_DIVISIBLE
+
+
+# ---------------------------------------------------------------- attention
+
+def _qkv(batch, seq, a, k, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    M = batch * seq
+    Q = torch.randn(M, a * d, generator=g, dtype=torch.float64)
+    K = torch.randn(M, k * d, generator=g, dtype=torch.float64)
+    V = torch.randn(M, k * d, generator=g, dtype=torch.float64)
+    return Q, K, V
+
+
+def _torch_attention(batch, seq, a, k, d, Q, K, V):
+    q = Q.view(batch, seq, a, d).transpose(1, 2)
+    kk = K.view(batch, seq, k, d).transpose(1, 2).repeat_interleave(a // k, dim=1)
+    vv = V.view(batch, seq, k, d).transpose(1, 2).repeat_interleave(a // k, dim=1)
+    o = F.scaled_dot_product_attention(q, kk, vv, is_causal=True)
+    return o.transpose(1, 2).reshape(batch * seq, a * d)
+
+
+@pytest.mark.parametrize("batch,seq,a,k,d", [(1, 7, 4, 4, 8), (2, 9, 8, 2, 4), (3, 5, 6, 1, 16)])
+def test_attention_core_matches_torch_sdpa(batch, seq, a, k, d):
+    Q, K, V = _qkv(batch, seq, a, k, d, 7)
+    got = oracle.attention_core(batch, seq, a, k, d, Q.numpy(), K.numpy(), V.numpy())
+    want = _torch_attention(batch, seq, a, k, d, Q, K, V).numpy()
+    assert np.abs(got - want).max() < 1e-12
+
+
+def test_attention_closed_forms():
+    a, k, d = 4, 2, 8
+    # seq = 1: a token attends only to itself -> O = V of its KV head.
+    Q, K, V = _qkv(3, 1, a, k, d, 1)
+    O = oracle.attention_core(3, 1, a, k, d, Q.numpy(), K.numpy(), V.numpy())
+    for j in range(a):
+        g = j // (a // k)
+        assert np.allclose(O[:, j * d:(j + 1) * d], V.numpy()[:, g * d:(g + 1) * d], atol=1e-15)
+    # First position of every sequence -> O = V[0] of that sequence.
+    batch, seq = 2, 6
+    Q, K, V = _qkv(batch, seq, a, k, d, 2)
+    O = oracle.attention_core(batch, seq, a, k, d, Q.numpy(), K.numpy(), V.numpy())
+    for b in range(batch):
+        m = b * seq
+        for j in range(a):
+            g = j // (a // k)
+            assert np.allclose(O[m, j * d:(j + 1) * d], V.numpy()[m, g * d:(g + 1) * d], atol=1e-15)
+    # All keys equal -> uniform weights over the causal prefix: O[p] = mean(V[0..p]).
+    K = torch.ones_like(K)
+    O = oracle.attention_core(batch, seq, a, k, d, Q.numpy(), K.numpy(), V.numpy())
+    Vn = V.numpy()
+    for b in range(batch):
+        for p in range(seq):
+            m = b * seq + p
+            for j in range(a):
+                g = j // (a // k)
+                want = Vn[b * seq:m + 1, g * d:(g + 1) * d].mean(0)
+                assert np.allclose(O[m, j * d:(j + 1) * d], want, atol=1e-13)
+
+
+def test_attention_heads_are_independent():
+    # Heads 4..7 (which read KV head 1 of 2) computed alone equal that slice.
+    batch, seq, a, k, d = 2, 8, 8, 2, 4
+    Q, K, V = _qkv(batch, seq, a, k, d, 3)
+    full = oracle.attention_core(batch, seq, a, k, d, Q.numpy(), K.numpy(), V.numpy())
+    sub = oracle.attention_core(batch, seq, 4, 1, d, Q.numpy()[:, 4 * d:], K.numpy()[:, d:],
+                                V.numpy()[:, d:])
+    assert np.array_equal(sub, full[:, 4 * d:])
+    # Sequences do not see each other: changing sequence 1 leaves sequence 0 alone.
+    K2, V2 = K.clone(), V.clone()
+    K2[seq:] += 1.0
+    V2[seq:] -= 2.0
+    alt = oracle.attention_core(batch, seq, a, k, d, Q.numpy(), K2.numpy(), V2.numpy())
+    assert np.array_equal(alt[:seq], full[:seq])
+    assert not np.allclose(alt[seq:], full[seq:])
+
+
+@pytest.mark.parametrize("a,k,t", [(8, 8, 4), (8, 2, 4), (8, 2, 8), (8, 4, 2), (4, 1, 4), (6, 3, 3)])
+def test_attention_sharded_equals_unsharded(a, k, t):
+    batch, seq, h, d = 2, 5, 12, 4
+    g = torch.Generator().manual_seed(a * 100 + k * 10 + t)
+    X = torch.randn(batch * seq, h, generator=g, dtype=torch.float64)
+    Wq = torch.randn(a * d, h, generator=g, dtype=torch.float64) * 0.4
+    Wk = torch.randn(k * d, h, generator=g, dtype=torch.float64) * 0.4
+    Wv = torch.randn(k * d, h, generator=g, dtype=torch.float64) * 0.4
+    Wo = torch.randn(h, a * d, generator=g, dtype=torch.float64) * 0.4
+    ref, O = oracle.attention(batch, seq, a, k, d, X, Wq, Wk, Wv, Wo, want_O=True)
+    out, P = oracle.attention_sharded(batch, seq, a, k, d, t, X, Wq, Wk, Wv, Wo, want_partials=True)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+    # Device i's partial is its head block of O times its column block of Wo.
+    cols = a * d // t
+    for i in range(t):
+        want = O[:, i * cols:(i + 1) * cols] @ Wo.numpy()[:, i * cols:(i + 1) * cols].T
+        assert np.abs(P[i] - want).max() < 1e-12
+    # The unsharded block against torch (library projections + sdpa).
+    tq, tk, tv = X @ Wq.T, X @ Wk.T, X @ Wv.T
+    tO = _torch_attention(batch, seq, a, k, d, tq, tk, tv)
+    assert np.abs(ref - (tO @ Wo.T).numpy()).max() < 1e-12
+
+
+def test_attention_rows_match_full_block():
+    batch, seq, h, a, k, d = 2, 9, 16, 4, 2, 4
+    g = torch.Generator().manual_seed(11)
+    X = torch.randn(batch * seq, h, generator=g, dtype=torch.float64)
+    Ws = [torch.randn(s, h, generator=g, dtype=torch.float64) * 0.3
+          for s in (a * d, k * d, k * d)]
+    Wo = torch.randn(h, a * d, generator=g, dtype=torch.float64) * 0.3
+    full = oracle.attention(batch, seq, a, k, d, X, *Ws, Wo)
+    rows = [0, 4, 8, 9, 17, 13]
+    part = oracle.attention_rows(batch, seq, a, k, d, X, *Ws, Wo, rows)
+    assert np.abs(part - full[rows]).max() < 1e-13
+
+
+# ---------------------------------------------------------------- plan
+
+def _read_map(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
+@pytest.mark.parametrize("name,a,k,t", [("head_map_a32_k8_t8.txt", 32, 8, 8),
+                                        ("head_map_a8_k2_t4.txt", 8, 2, 4)])
+def test_head_maps_match_golden(name, a, k, t):
+    for shard, q0, nq, kv0, nkv in _read_map(name):
+        heads = [j for j in range(a) if oracle.q_head_shard(a, t, j) == shard]
+        assert heads == list(range(q0, q0 + nq))
+        assert oracle.shard_kv_first(k, t, shard) == kv0
+        assert oracle.shard_kv_count(k, t) == nkv
+        # every query head of the shard reads a KV head the shard holds
+        for j in heads:
+            assert kv0 <= oracle.q_head_kv(a, k, j) < kv0 + nkv
+
+
+@pytest.mark.parametrize("h,f,a,k,d,t,want", [
+    (4096, 14336, 32, 8, 128, 8, oracle.OK),
+    (1024, 4096, 0, 0, 0, 4, oracle.OK),
+    (16, 64, 0, 0, 0, 4, oracle.OK),
+    (4096, 14336, 32, 8, 128, 3, oracle.ERR_NOT_DIVISIBLE),   # t does not divide a or f
+    (64, 60, 8, 8, 8, 8, oracle.ERR_NOT_DIVISIBLE),            # t does not divide f
+    (64, 64, 12, 4, 8, 8, oracle.ERR_NOT_DIVISIBLE),           # t does not divide a
+    (64, 64, 8, 3, 8, 4, oracle.ERR_NOT_DIVISIBLE),            # k does not divide a
+    (64, 64, 16, 8, 8, 16, oracle.OK),                         # k < t, k | t: replicas
+    (64, 64, 24, 6, 8, 4, oracle.ERR_NOT_DIVISIBLE),           # k >= t but t does not divide k
+    (64, 48, 24, 3, 8, 6, oracle.OK),                          # k < t, k | t: replicas
+    (64, 48, 24, 4, 8, 6, oracle.ERR_NOT_DIVISIBLE),           # k < t but k does not divide t
+    (0, 64, 8, 8, 8, 8, oracle.ERR_INVALID),
+    (64, 64, 8, 8, 8, 0, oracle.ERR_INVALID),
+])
+def test_plan_check(h, f, a, k, d, t, want):
+    assert oracle.plan_check(h, f, a, k, d, t) == want
+
+
+# ---------------------------------------------------------------- g, norm, layer
+
+def test_reduce_exact_and_bias_added_once():
+    P = synth.integer_bf16((4, 6, 8), -50, 50, 9).double().numpy()
+    bias = synth.integer_bf16((8,), -3, 3, 10).double().numpy()
+    res = synth.integer_bf16((6, 8), -9, 9, 11).double().numpy()
+    out = oracle.reduce(P, bias, res)
+    Pi = P.astype(np.int64)
+    assert np.array_equal(out, (Pi.sum(0) + bias.astype(np.int64) + res.astype(np.int64)))
+    plain = oracle.reduce(P)
+    assert np.array_equal(out - plain - res, np.broadcast_to(bias, (6, 8)))  # once, not t times
+
+
+def test_rmsnorm_closed_forms():
+    eps = 1e-5
+    for c in (0.0, 0.5, -3.0, 7.0):
+        x = np.full((2, 10), c)
+        y = oracle.rmsnorm(x, eps)
+        assert np.allclose(y, c / math.sqrt(c * c + eps), rtol=1e-14, atol=0)
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(5, 32, generator=g, dtype=torch.float64) * 3
+    want = F.rms_norm(x, (32,), eps=eps).numpy()
+    assert np.abs(oracle.rmsnorm(x.numpy(), eps) - want).max() < 1e-13
+
+
+def _small_layer(seed, batch=2, seq=6, h=16, a=4, k=2, d=4, f=32):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float64)
+    X = r(batch * seq, h)
+    Wq, Wk, Wv = r(a * d, h) * 0.3, r(k * d, h) * 0.3, r(k * d, h) * 0.3
+    Wo = r(h, a * d) * 0.3
+    W1, W3, W2 = r(f, h) * 0.3, r(f, h) * 0.3, r(h, f) * 0.3
+    return (batch, seq, a, k, d), X, (Wq, Wk, Wv, Wo, W1, W3, W2)
+
+
+def test_layer_reduces_to_residual_when_output_projections_vanish():
+    dims, X, (Wq, Wk, Wv, Wo, W1, W3, W2) = _small_layer(1)
+    Y = oracle.layer(*dims, 2, X, Wq, Wk, Wv, torch.zeros_like(Wo), W1, W3, torch.zeros_like(W2))
+    assert np.array_equal(Y, X.numpy())
+
+
+def test_layer_matches_composed_torch_reference_and_sharded_form():
+    dims, X, W = _small_layer(2)
+    batch, seq, a, k, d = dims
+    Wq, Wk, Wv, Wo, W1, W3, W2 = W
+    eps = 1e-5
+    xn = F.rms_norm(X, (X.shape[1],), eps=eps)
+    att = _torch_attention(batch, seq, a, k, d, xn @ Wq.T, xn @ Wk.T, xn @ Wv.T) @ Wo.T
+    h1 = X + att
+    hn = F.rms_norm(h1, (X.shape[1],), eps=eps)
+    want = (h1 + (F.silu(hn @ W1.T) * (hn @ W3.T)) @ W2.T).numpy()
+    Y = oracle.layer(*dims, 2, X, *W)
+    assert np.abs(Y - want).max() < 1e-12
+    for t in (2, 4):
+        Ys = oracle.layer(*dims, t, X, *W, sharded=True)
+        assert np.abs(Ys - Y).max() < 1e-12
+    rows = [0, 5, 6, 11, 7]
+    Yr = oracle.layer_rows(*dims, X, *W, rows)
+    assert np.abs(Yr - Y[rows]).max() < 1e-12
