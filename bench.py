@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-parallel transformer layer on one GB300 (or N
+independent replicas, one per GPU).
+
+A step is one pass of the whole hot path over one batch: tp_layer_forward on
+the full-layer workload (8192 tokens = 4 x 2048, h=4096, 32 query / 8 KV
+heads, d=128, SwiGLU ffn=14336, t=8, bf16), i.e. RMSNorm, the colwise QKV
+GEMM, causal GQA attention, the rowwise o_proj with the g reduction fused in
+its accumulator (+ residual), RMSNorm, the colwise W1/W3 GEMM with the
+SiLU*gate epilogue, and the rowwise W2 with g fused (+ residual).
+
+Printed (rank 0, one JSON line): whole-job TFLOP/s over the timed steps
+(algorithmic FLOPs: GEMMs 2*M*N*K, causal attention core counted as half of
+4*s^2*d*a per sequence), the dominant kernel's roofline measured live with
+CUDA events on the launching stream, the g partial-sum reduce in GB/s
+(PARTIALS-mode [t][M][h] fp32 partials of the same layer), an end-to-end
+figure through the C ABI with host buffers, SM clocks sampled during the
+timed region, and the fp64 oracle timed on the host cores on a bounded
+sample.  ``--impl reference`` times the oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import SHAPES, Shape  # noqa: E402
+
+METRIC = ("sharded-MLP/attn TFLOP/s & % BF16 peak; partial-reduce GB/s & % HBM (1×GB300)")
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ work model
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def attn_core_flops(s: Shape):
+    # QK^T and PV: 2 * 2 * s^2 * d per head and sequence; causal -> half.
+    return 0.5 * 4.0 * s.batch * s.seq * s.seq * s.head_dim * s.heads
+
+
+def layer_kernel_flops(s: Shape):
+    """Algorithmic FLOPs of each kernel of the FUSED layer, in launch order."""
+    M, h, f, a, k, d = s.tokens, s.hidden, s.ffn, s.heads, s.kv_heads, s.head_dim
+    return [
+        ("rmsnorm_attn", 0.0),
+        ("qkv_colwise_gemm", gemm_flops(M, (a + 2 * k) * d, h)),
+        ("attention_core", attn_core_flops(s)),
+        ("o_proj_rowwise_gemm+g", gemm_flops(M, h, a * d)),
+        ("rmsnorm_mlp", 0.0),
+        ("w1w3_colwise_gemm+swiglu", gemm_flops(M, 2 * f, h)),
+        ("w2_rowwise_gemm+g", gemm_flops(M, h, f)),
+    ]
+
+
+def layer_kernel_bytes(s: Shape):
+    """Algorithmic HBM bytes of the two RMSNorm kernels (read x, write xn)."""
+    return {"rmsnorm_attn": 4.0 * s.tokens * s.hidden, "rmsnorm_mlp": 4.0 * s.tokens * s.hidden}
+
+
+def layer_flops(s: Shape):
+    return sum(v for _, v in layer_kernel_flops(s))
+
+
+def reduce_bytes(t, n, partial_bytes=4, residual=True):
+    return t * n * partial_bytes + n * 2 + (n * 2 if residual else 0)
+
+
+# ------------------------------------------------------------------ environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)  # let the first samples arrive
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if self.t0 is None or not (self.t0 - 0.15 <= ts <= self.t1 + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(torch, dev_index: int) -> str:
+    try:
+        props = torch.cuda.get_device_properties(dev_index)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", 0)
+        devid = getattr(props, "pci_device_id", 0)
+        if bus is not None:
+            return f"{dom:08x}:{bus:02x}:{devid:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ------------------------------------------------------------------ distributed glue
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar (the step time) over all ranks."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_step_per_rank: float, world: int, seconds_per_step: float) -> float:
+    """TFLOP/s of all ranks together (each rank runs its own replica)."""
+    return flops_per_step_per_rank * world / seconds_per_step / 1e12
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(s: Shape, inp, tokens: int):
+    """Time the fp64 oracle on the first `tokens` positions of sequence 0 of
+    the layer (causal: identical to the full layer's outputs there)."""
+    import oracle
+    sub = Shape("sample", 1, tokens, s.hidden, ffn=s.ffn, heads=s.heads, kv_heads=s.kv_heads,
+                head_dim=s.head_dim, tp=s.tp, act=s.act)
+    f64 = {k: v.double().numpy() for k, v in inp.items() if k != "X"}
+    X = inp["X"][:tokens].double().numpy()
+    t0 = time.perf_counter()
+    oracle.layer(1, tokens, s.heads, s.kv_heads, s.head_dim, s.tp, X, f64["Wq"], f64["Wk"], f64["Wv"],
+                 f64["Wo"], f64["W1"], f64["W3"], f64["W2"], sharded=True)
+    dt = time.perf_counter() - t0
+    fl = layer_flops(sub)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"layer forward (sharded t={s.tp} form) on the first {tokens} tokens of one "
+                      f"sequence, full h={s.hidden}/ffn={s.ffn} weights, fp64 ({fl / 1e9:.1f} GFLOP)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    s = SHAPES["layer"]
+    import oracle
+    oracle.lib()
+    inp = synth.workload_inputs(s)
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(s, inp, tokens)
+    times = []
+    for _ in range(args.steps):
+        r = oracle_sample(s, inp, tokens)
+        times.append(r["seconds"])
+    sub = Shape("sample", 1, tokens, s.hidden, ffn=s.ffn, heads=s.heads, kv_heads=s.kv_heads,
+                head_dim=s.head_dim, tp=s.tp, act=s.act)
+    per = sum(times) / len(times)
+    value = layer_flops(sub) / per / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, bf16-rounded)",
+        "config": {"workload": "tp_layer_forward, first %d tokens of one 2048-token sequence "
+                               "(fp64 CPU oracle), h=4096, 32q/8kv heads d=128, SwiGLU ffn=14336, "
+                               "t=8" % tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": r["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    import megatron_tensor_transformer_colwise_gb300 as tp
+
+    peaks, peak_src = load_peaks()
+    s = SHAPES["layer"]
+    inp = synth.workload_inputs(s)
+    d = {k: v.to(device) for k, v in inp.items()}
+    plan = tp.Plan(tp.make_config(tokens=s.tokens, hidden=s.hidden, ffn=s.ffn, n_heads=s.heads,
+                                  n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp,
+                                  act=s.act, batch=s.batch, seq=s.seq,
+                                  reduce_mode=tp.TP_REDUCE_FUSED))
+    nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_LAYER)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    Y = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device=device)
+    weights = tp.layer_weights({k: v for k, v in d.items() if k != "X"})
+    stream = torch.cuda.current_stream()
+    kf = layer_kernel_flops(s)
+    nk = len(kf)
+
+    def mk_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # materialise the cudaEvent_t
+        return evs
+
+    warm_events = mk_events(nk + 1)
+    for _ in range(args.warmup):
+        tp.tp_layer_forward_traced(plan, d["X"], weights, Y, ws, nws,
+                                   [e.cuda_event for e in warm_events], stream)
+    torch.cuda.synchronize()
+    assert tp.tp_get_device_status(plan) == tp.TP_OK, tp.tp_last_error()
+
+    step_events = [mk_events(nk + 1) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_for(torch, device.index))
+    sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
+    start.record(stream)
+    for k in range(args.steps):
+        tp.tp_layer_forward_traced(plan, d["X"], weights, Y, ws, nws,
+                                   [e.cuda_event for e in step_events[k]], stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = sampler.stop()
+    status = tp.tp_get_device_status(plan)
+    assert status == tp.TP_OK, tp.tp_last_error()
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, world, device)
+    flops = layer_flops(s)
+    value = whole_job_value(flops, world, ms / 1e3)
+
+    # Per-kernel durations inside the timed region (same stream, live).
+    per_kernel = [0.0] * nk
+    for evs in step_events:
+        for i in range(nk):
+            per_kernel[i] += evs[i].elapsed_time(evs[i + 1])
+    per_kernel = [v / args.steps for v in per_kernel]
+    total_k = sum(per_kernel)
+    kbytes = layer_kernel_bytes(s)
+    kernels = []
+    for (name, fl), msk in zip(kf, per_kernel):
+        row = {"name": name, "us": msk * 1e3, "share": msk / total_k if total_k else None}
+        if fl > 0:
+            row["tflops"] = fl / (msk / 1e3) / 1e12
+            row["frac_bf16_sustained"] = row["tflops"] / peaks["bf16_tflops_sustained"]
+        else:
+            row["gbs"] = kbytes[name] / (msk / 1e3) / 1e9
+            row["frac_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+        kernels.append(row)
+    dom = max(range(nk), key=lambda i: per_kernel[i])
+    dom_name, dom_fl = kf[dom]
+    achieved = dom_fl / (per_kernel[dom] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
+                "algorithmic_flops_per_launch": dom_fl,
+                "traffic": args.dominant_traffic}
+
+    # The g reduction as a PARTIALS-mode kernel over the layer's partials.
+    n = s.tokens * s.hidden
+    P = torch.randn(s.tp, s.tokens, s.hidden, dtype=torch.float32, device=device)
+    res = torch.randn(s.tokens, s.hidden, device=device).to(torch.bfloat16)
+    Zr = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device=device)
+    for _ in range(5):
+        tp.tp_reduce_partials(P, tp.TP_F32, s.tp, n, s.hidden, None, res, Zr, stream)
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 30
+    r0.record(stream)
+    for _ in range(reps):
+        tp.tp_reduce_partials(P, tp.TP_F32, s.tp, n, s.hidden, None, res, Zr, stream)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    red_us = r0.elapsed_time(r1) / reps * 1e3
+    rb = reduce_bytes(s.tp, n, 4, residual=True)
+    red_gbs = rb / (red_us / 1e6) / 1e9
+    reduce_line = {"bound": "hbm", "kernel": "tp_reduce_partials (t=8 fp32 partials + residual)",
+                   "achieved": red_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": red_gbs / peaks["hbm_gbs"], "frac_of_8tbs": red_gbs / 8000.0,
+                   "us": red_us, "bytes_per_launch": rb,
+                   "peak_source": f"{peak_src} hbm_gbs (kernel timed alone)",
+                   "l2": "inputs 1.07 GB > 129 MB L2"}
+    del P
+
+    # End to end through the C ABI with host buffers (pinned): X in, Y out.
+    Xh = inp["X"].pin_memory()
+    Yh = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(d["X"])
+    e2e_steps = max(5, min(args.steps, 50))
+    for _ in range(3):
+        Xd.copy_(Xh, non_blocking=True)
+        tp.tp_layer_forward(plan, Xd, {k: v for k, v in d.items() if k != "X"}, Y, ws, nws, stream)
+        Yh.copy_(Y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        Xd.copy_(Xh, non_blocking=True)
+        tp.tp_layer_forward(plan, Xd, {k: v for k, v in d.items() if k != "X"}, Y, ws, nws, stream)
+        Yh.copy_(Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    e2e = {"value": whole_job_value(flops, world, e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Yh.numel() * 2,
+           "ms_per_step": e2e_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, bf16-rounded)",
+        "config": {"workload": "tp_layer_forward: 8192 tokens (4 x 2048), h=4096, 32 q / 8 kv "
+                               "heads d=128, SwiGLU ffn=14336, t=8, FUSED g, bf16",
+                   "tokens": s.tokens, "tp_degree": s.tp,
+                   "parallelism": f"single-GPU t={s.tp} shards" + (f", {world} replicas" if world > 1 else ""),
+                   "gflop_per_step": flops / 1e9,
+                   "l2": "inputs larger than L2 (436 MB of weights per step)"},
+        "roofline": roofline,
+        "reduce": reduce_line,
+        "kernels": kernels,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": nk * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(s, inp, args.cpu_tokens)
+        del line["cpu_baseline"]["seconds"]
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=96,
+                    help="tokens of the bounded oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=48,
+                    help="tokens of the bounded oracle sample per reference step")
+    ap.add_argument("--dominant-traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,281 @@
+/*
+ * tp.h -- C ABI of the single-GPU (sm_103a) Megatron-style tensor-parallel
+ * transformer block: t-way column-then-row sharded MLP (GeLU / SwiGLU),
+ * head-sharded causal GQA attention, and the g-operator reduction of the t
+ * shard partials.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [wiki]  "텐서 병렬화" (itwiki, Tensor parallelism): "행렬 곱 나누기"
+ *           (column- and row-parallel products), "MLP", "셀프 어텐션"
+ *           (self-attention), "통신 연산 f와 g" (the f and g operators).
+ *   [diff]  "Tensor 병렬성" (diffusers docs, tensor parallelism): "Colwise와
+ *           rowwise" (styles table), "제약 조건 및 검증" (constraints and
+ *           validation), "한계" (limits: errors instead of silent fallbacks).
+ *   [trf]   "추론을 위한 텐서 병렬성" (transformers docs, tensor parallelism for
+ *           inference): "분할 전략" (partitioning strategies), "설계 구현 /
+ *           DTensor" (Shard / Replicate / Partial placements; rowwise bias).
+ *
+ * One process, one GPU: the t "devices" of the pages are shard indices.  A
+ * colwise output that the pages leave sharded on the last dimension is stored
+ * as one row-major [M][t * w] matrix whose column block i is shard i (the
+ * Shard(-1) placement, [trf] "분할 전략").  A rowwise partial awaiting the
+ * all-reduce (the Partial() placement) is an HBM buffer [t][M][h]; the g
+ * operator is a local reduction of it, or is folded into the rowwise GEMM's
+ * accumulator so no separate pass exists.
+ *
+ * Conventions for every call:
+ *  - All tensors are row-major.  Weights use the nn.Linear layout W[out][in]
+ *    ([diff] "Colwise와 rowwise": colwise shards weight dim 0, rowwise dim 1),
+ *    passed whole and unsharded; shards are views (pointer + stride), never
+ *    copies.  bf16 values are passed as their 16-bit patterns (tp_bf16).
+ *  - Device pointers are caller-owned (e.g. allocated by PyTorch), must be
+ *    16-byte aligned and must not alias one another unless stated.  The
+ *    library allocates device memory only in tp_plan_create (a 256-byte
+ *    status word) and never frees caller memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    only enqueue work; nothing synchronises implicitly.
+ *  - Every call returns TP_OK or a TP_ERR_* code, and on error launches
+ *    nothing ([diff] "한계": an error instead of a silent fallback;
+ *    "제약 조건 및 검증": checks happen before any weight is touched).
+ *    tp_last_error() then returns a message naming the failed rule.
+ *  - The library runs only on sm_103a; there is no CPU path.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ error codes */
+#define TP_OK 0
+#define TP_ERR_INVALID_ARG 1    /* null / negative / misaligned / bad enum   */
+#define TP_ERR_NOT_DIVISIBLE 2  /* t does not divide f or a; bad (k, t) pair */
+#define TP_ERR_UNSUPPORTED 3    /* a combination this build does not provide */
+#define TP_ERR_WORKSPACE 4      /* workspace missing or smaller than needed   */
+#define TP_ERR_CUDA 5           /* a CUDA runtime / driver call failed        */
+#define TP_ERR_DEVICE_TIMEOUT 6 /* a bounded device-side wait gave up         */
+
+/* Exported symbols of libtp.so (everything else in the library is hidden). */
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+typedef uint16_t tp_bf16;
+typedef struct tp_plan_s* tp_plan_t;
+
+/* Activation of the colwise MLP projection.  GELU_ERF is the exact
+ * x * Phi(x) form (the default of the [wiki] "MLP" example); SWIGLU is
+ * SiLU(X W1^T) * (X W3^T) with W1 and W3 both colwise ([wiki] "MLP"); NONE is
+ * the identity (a linear MLP, used to check exact integer products). */
+enum { TP_ACT_GELU_ERF = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2, TP_ACT_NONE = 3 };
+
+/* How the rowwise GEMM's t partials are summed (the g operator).
+ * FUSED: shard loop is the outer K loop of one accumulator; no partials
+ *        buffer, no separate pass.
+ * PARTIALS: each shard writes its Partial() [M][h] to a [t][M][h] buffer and
+ *        tp_reduce_partials sums them. */
+enum { TP_REDUCE_FUSED = 0, TP_REDUCE_PARTIALS = 1 };
+
+/* Element type of a partials buffer. */
+enum { TP_F32 = 0, TP_BF16 = 1 };
+
+/* Operations whose workspace size tp_plan_workspace_bytes reports. */
+enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2 };
+
+/* Index tables tp_plan_shard_table exports (int32, row-major):
+ *  FFN_SHARDS  [t][2]: first column of shard i in the ffn dimension, width f/t
+ *  Q_HEAD_SHARD [a]  : shard holding query head j (= j / (a/t))
+ *  Q_HEAD_KV    [a]  : KV head read by query head j (= j / (a/k))
+ *  SHARD_KV    [t][2]: first KV head held by shard i, number held
+ *                      (k/t own heads if k >= t, else 1 replica of head i*k/t)
+ *  QKV_COLUMNS [t][3]: column offsets of Q_i, K_i, V_i in the QKV buffer */
+enum {
+    TP_TABLE_FFN_SHARDS = 0,
+    TP_TABLE_Q_HEAD_SHARD = 1,
+    TP_TABLE_Q_HEAD_KV = 2,
+    TP_TABLE_SHARD_KV = 3,
+    TP_TABLE_QKV_COLUMNS = 4
+};
+
+/* Configuration (plain data; copied by tp_plan_create).  Names follow the
+ * pages: tokens M = batch * seq, hidden h, ffn f (0 = no MLP), n_heads a,
+ * n_kv_heads k, head_dim d (a = 0: no attention), tp_degree t ([diff]
+ * TensorParallelConfig(tp_degree); [trf] DistributedConfig(tp_size)). */
+typedef struct {
+    int64_t tokens;        /* M >= 1                                          */
+    int32_t batch, seq;    /* attention is causal within each sequence;
+                              tokens == batch * seq when n_heads > 0           */
+    int32_t hidden;        /* h, multiple of 8                                */
+    int32_t ffn;           /* f, t | f, (f/t) multiple of 8; 0 = no MLP       */
+    int32_t n_heads;       /* a, t | a; 0 = no attention                      */
+    int32_t n_kv_heads;    /* k, k | a, and t | k (k >= t) or k | t (k < t)    */
+    int32_t head_dim;      /* d in {64, 128}                                  */
+    int32_t tp_degree;     /* t in [1, 64]                                    */
+    int32_t act;           /* TP_ACT_* of the MLP                             */
+    int32_t reduce_mode;   /* TP_REDUCE_*                                     */
+    int32_t partial_dtype; /* TP_F32 or TP_BF16 (PARTIALS mode only)          */
+    float rms_eps;         /* RMSNorm epsilon (layer only), > 0               */
+} tp_config;
+
+/* Weights of one layer, all full nn.Linear matrices [out][in] in bf16:
+ * Wq [a d][h], Wk/Wv [k d][h], Wo [h][a d], W1/W3 [f][h], W2 [h][f]. */
+typedef struct {
+    const tp_bf16 *Wq, *Wk, *Wv, *Wo, *W1, *W3, *W2;
+} tp_layer_weights;
+
+/* ------------------------------------------------------------ plan */
+
+/* Validate a configuration and build the shard layout.  All divisibility and
+ * alignment rules are checked here, before any weight is read ([diff]
+ * "제약 조건 및 검증": tp_degree divides the head count, checked before
+ * loading; [wiki] "셀프 어텐션": KV heads replicated when fewer than t).
+ * Allocates a 256-byte device status word on the current device.
+ * Returns TP_ERR_INVALID_ARG, TP_ERR_NOT_DIVISIBLE, TP_ERR_UNSUPPORTED or
+ * TP_ERR_CUDA on failure, with *out set to NULL. */
+TP_API int tp_plan_create(const tp_config* cfg, tp_plan_t* out);
+
+/* Host-only validation of a configuration: the same rules as
+ * tp_plan_create, with no device work (usable without a GPU). */
+TP_API int tp_config_check(const tp_config* cfg);
+
+/* Host-only form of tp_plan_shard_table for a configuration that passes
+ * tp_config_check (usable without a GPU). */
+TP_API int tp_config_shard_table(const tp_config* cfg, int which, int32_t* out, int64_t cap, int64_t* n);
+
+/* Free a plan (NULL is accepted).  The caller must ensure no launched work
+ * still uses it. */
+TP_API int tp_plan_destroy(tp_plan_t plan);
+
+/* Bytes of caller-provided device workspace the op needs (TP_OP_*). */
+TP_API int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes);
+
+/* Copy index table `which` (TP_TABLE_*) into host array out[cap]; *n gets
+ * the number of int32 entries (also when cap is too small, which returns
+ * TP_ERR_INVALID_ARG).  Host-only; no device work. */
+TP_API int tp_plan_shard_table(tp_plan_t plan, int which, int32_t* out, int64_t cap, int64_t* n);
+
+/* Read and clear the plan's device status word (synchronises `stream`).
+ * TP_OK, or TP_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up. */
+TP_API int tp_get_device_status(tp_plan_t plan, void* stream);
+
+/* Thread-local description of the last error (never NULL). */
+TP_API const char* tp_last_error(void);
+
+/* ------------------------------------------------------------ g operator */
+
+/* out[e] = sum_{i<t} partials[i][e] (+ bias[e % h]) (+ residual[e]), bf16.
+ * The forward of g ([wiki] "통신 연산 f와 g": all-reduce of the partial
+ * sums); bias is the rowwise bias, replicated and added once after the
+ * reduction ([trf] "DTensor"); residual is the replicated residual stream.
+ * partials: device [t][n] of TP_F32 or TP_BF16 (partial_dtype); bias: device
+ * [h] bf16 or NULL; residual, out: device [n] bf16 (residual may be NULL;
+ * out may alias residual).  n % h == 0, h % 8 == 0.  Sums in fp32, shard
+ * order i = 0..t-1. */
+TP_API int tp_reduce_partials(const void* partials, int partial_dtype, int32_t t, int64_t n,
+                       int32_t h, const tp_bf16* bias, const tp_bf16* residual, tp_bf16* out,
+                       void* stream);
+
+/* y = x / sqrt(mean_j x_j^2 + eps) per row of h (unit gain), bf16 in/out,
+ * fp32 arithmetic.  The replicated norm of [wiki] "통신 연산 f와 g".
+ * x, y: device [rows][h]; h % 8 == 0, h <= 8192. */
+TP_API int tp_rmsnorm(const tp_bf16* x, int64_t rows, int32_t h, float eps, tp_bf16* y, void* stream);
+
+/* ------------------------------------------------------------ MLP */
+
+/* Colwise projection with the activation fused ([wiki] "MLP": the first
+ * matrix is split by columns so the nonlinearity needs no sync):
+ *   Y[:, block i] = act(X W1_i^T)              (GeLU / none)
+ *   Y[:, block i] = SiLU(X W1_i^T) * (X W3_i^T) (SwiGLU)
+ * X: device [M][h]; W1, W3: device [f][h] (W3 only for SwiGLU, else NULL);
+ * Y: device [M][f], column block i (width f/t) is shard i.  bf16 in and out,
+ * fp32 accumulation, activation applied to the fp32 accumulator. */
+TP_API int tp_colwise_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                       tp_bf16* Y, void* stream);
+
+/* Rowwise projection of the colwise output ([wiki] "행렬 곱 나누기": row
+ * parallel, Y_i B_i then a sum).  Shard i multiplies column block i of Y by
+ * column block i of W2 (B_i = rows of B = columns of W2).
+ *   FUSED:    Z = sum_i Y_i W2_i^T (+ bias) (+ residual), bf16; partials unused.
+ *   PARTIALS: partials[i] = Y_i W2_i^T as [t][M][h] (plan's partial_dtype);
+ *             Z, bias, residual unused (sum with tp_reduce_partials).
+ * Y: device [M][f]; W2: device [h][f]; bias: [h] or NULL; residual: [M][h]
+ * or NULL (may alias Z). */
+TP_API int tp_rowwise_forward(tp_plan_t plan, const tp_bf16* Y, const tp_bf16* W2, const tp_bf16* bias,
+                       const tp_bf16* residual, void* partials, tp_bf16* Z, void* stream);
+
+/* The whole sharded MLP: Z = sum_i act(X A_i) B_i (+ bias once) (+ residual)
+ * ([wiki] "MLP").  In PARTIALS mode the t partials are written to `partials`
+ * ([t][M][h], required) and then reduced into Z; in FUSED mode `partials`
+ * may be NULL.  workspace: device, >= tp_plan_workspace_bytes(TP_OP_MLP)
+ * (holds the colwise output [M][f] bf16 at offset 0). */
+TP_API int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                   const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
+                   tp_bf16* Z, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ attention */
+
+/* Colwise Q/K/V projection, all shards in one launch ([wiki] "셀프 어텐션":
+ * Q, K, V split by columns, a/t heads per shard).  QKV: device
+ * [M][t * W], W = (a/t + 2 n_kv) d with n_kv the KV heads per shard; column
+ * block i holds [Q_i | K_i | V_i] (offsets from TP_TABLE_QKV_COLUMNS). */
+TP_API int tp_qkv_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                   const tp_bf16* Wv, tp_bf16* QKV, void* stream);
+
+/* Causal GQA attention of every shard's heads, no communication ([wiki]
+ * "셀프 어텐션": heads are independent).  For query head j of shard i and its
+ * KV head g(j) = j / (a/k):  O_j = softmax(Q_j K_g^T / sqrt d + causal) V_g,
+ * fp32 softmax, within each sequence.  QKV as written by tp_qkv_forward;
+ * O: device [M][a d], head j at columns j d (column block i = shard i). */
+TP_API int tp_attn_core_forward(tp_plan_t plan, const tp_bf16* QKV, tp_bf16* O, void* stream);
+
+/* The whole head-sharded attention block: QKV colwise, attention, o_proj
+ * rowwise, g ([wiki] "셀프 어텐션").  out = sum_i O_i Wo_i^T (+ residual).
+ * partials: [t][M][h], required in PARTIALS mode.  workspace >=
+ * tp_plan_workspace_bytes(TP_OP_ATTN). */
+TP_API int tp_attn_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                    const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* residual, void* partials,
+                    tp_bf16* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ layer */
+
+/* One pre-norm layer with two g reductions ([wiki] "통신 연산 f와 g": one
+ * all-reduce after attention and one after the MLP; norm and residual
+ * replicated):  h1 = x + Attn(RMSNorm(x)),  y = h1 + MLP(RMSNorm(h1)).
+ * X, Y: device [M][h] bf16 (may not alias).  Requires act == TP_ACT_SWIGLU
+ * or a GeLU form (W3 NULL then).  workspace >= tp_plan_workspace_bytes(
+ * TP_OP_LAYER); in PARTIALS mode it also holds the [t][M][h] partials. */
+TP_API int tp_layer_forward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, tp_bf16* Y,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* tp_layer_forward that also records caller-created CUDA events (cudaEvent_t
+ * handles) on `stream` at the boundaries of its kernels, for per-kernel
+ * timing on the launching stream: events[0] before the first kernel and
+ * events[i] after kernel i.  FUSED mode launches 7 kernels (RMSNorm, QKV,
+ * attention, o_proj+residual, RMSNorm, W1/W3 colwise, W2+residual) and
+ * needs n_events >= 8; PARTIALS mode launches 8 (RMSNorm, QKV, attention,
+ * o_proj partials, g+RMSNorm, W1/W3 colwise, W2 partials, g) and needs 9.
+ * Fewer events -> TP_ERR_INVALID_ARG before any launch. */
+TP_API int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w,
+                                   tp_bf16* Y, void* workspace, size_t ws_bytes, void* stream,
+                                   void* const* events, int n_events);
+
+/* ------------------------------------------------------------ self test */
+
+/* Failure-detection check: launches one CTA that waits on a shared-memory
+ * barrier nothing ever arrives at, with a wait limit of `timeout_ns`
+ * nanoseconds (1e3 .. 1e9).  The kernel gives up, records
+ * TP_ERR_DEVICE_TIMEOUT in the plan's status word and returns normally, so
+ * the context stays usable; read it with tp_get_device_status. */
+TP_API int tp_selftest_wait_timeout(tp_plan_t plan, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */

@@ -1,0 +1,297 @@
+"""Python binding of libtp.so, the sm_103a tensor-parallel block library.
+
+Argument marshalling only: every function here forwards to the ``extern "C"``
+entry point of the same name declared in ``include/tp.h``; all compute runs
+in the library's CUDA kernels.  Tensors are passed as device pointers
+(``tensor.data_ptr()``), streams as ``cudaStream_t`` handles (default: torch's
+current stream).  PyTorch is used only for memory and streams.
+
+There is no CPU path: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+from . import _build
+
+__all__ = [
+    "TPError", "TPConfig", "TPLayerWeights", "Plan", "lib", "build",
+    "TP_OK", "TP_ERR_INVALID_ARG", "TP_ERR_NOT_DIVISIBLE", "TP_ERR_UNSUPPORTED",
+    "TP_ERR_WORKSPACE", "TP_ERR_CUDA", "TP_ERR_DEVICE_TIMEOUT",
+    "TP_ACT_GELU_ERF", "TP_ACT_GELU_TANH", "TP_ACT_SWIGLU", "TP_ACT_NONE",
+    "TP_REDUCE_FUSED", "TP_REDUCE_PARTIALS", "TP_F32", "TP_BF16",
+    "TP_OP_MLP", "TP_OP_ATTN", "TP_OP_LAYER",
+    "TP_TABLE_FFN_SHARDS", "TP_TABLE_Q_HEAD_SHARD", "TP_TABLE_Q_HEAD_KV",
+    "TP_TABLE_SHARD_KV", "TP_TABLE_QKV_COLUMNS",
+    "tp_plan_create", "tp_plan_destroy", "tp_config_check", "tp_config_shard_table",
+    "tp_plan_workspace_bytes", "tp_plan_shard_table", "tp_get_device_status", "tp_last_error",
+    "tp_reduce_partials", "tp_rmsnorm", "tp_colwise_forward", "tp_rowwise_forward",
+    "tp_mlp_forward", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
+    "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout", "EXPORTED",
+]
+
+TP_OK = 0
+TP_ERR_INVALID_ARG = 1
+TP_ERR_NOT_DIVISIBLE = 2
+TP_ERR_UNSUPPORTED = 3
+TP_ERR_WORKSPACE = 4
+TP_ERR_CUDA = 5
+TP_ERR_DEVICE_TIMEOUT = 6
+
+TP_ACT_GELU_ERF, TP_ACT_GELU_TANH, TP_ACT_SWIGLU, TP_ACT_NONE = 0, 1, 2, 3
+TP_REDUCE_FUSED, TP_REDUCE_PARTIALS = 0, 1
+TP_F32, TP_BF16 = 0, 1
+TP_OP_MLP, TP_OP_ATTN, TP_OP_LAYER = 0, 1, 2
+(TP_TABLE_FFN_SHARDS, TP_TABLE_Q_HEAD_SHARD, TP_TABLE_Q_HEAD_KV, TP_TABLE_SHARD_KV,
+ TP_TABLE_QKV_COLUMNS) = range(5)
+
+ACT_BY_NAME = {"gelu": TP_ACT_GELU_ERF, "gelu_tanh": TP_ACT_GELU_TANH, "swiglu": TP_ACT_SWIGLU,
+               "none": TP_ACT_NONE}
+
+
+class TPError(RuntimeError):
+    """A TP_ERR_* return code with the library's message."""
+
+    def __init__(self, fn: str, code: int, message: str):
+        super().__init__(f"{fn} failed with code {code}: {message}")
+        self.code = code
+        self.fn = fn
+
+
+class TPConfig(C.Structure):
+    _fields_ = [
+        ("tokens", C.c_int64),
+        ("batch", C.c_int32), ("seq", C.c_int32),
+        ("hidden", C.c_int32), ("ffn", C.c_int32),
+        ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+        ("tp_degree", C.c_int32), ("act", C.c_int32), ("reduce_mode", C.c_int32),
+        ("partial_dtype", C.c_int32), ("rms_eps", C.c_float),
+    ]
+
+
+class TPLayerWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")]
+
+
+_VP = C.c_void_p
+_SIGS = {
+    "tp_plan_create": [C.POINTER(TPConfig), C.POINTER(C.c_void_p)],
+    "tp_config_check": [C.POINTER(TPConfig)],
+    "tp_config_shard_table": [C.POINTER(TPConfig), C.c_int, C.POINTER(C.c_int32), C.c_int64,
+                              C.POINTER(C.c_int64)],
+    "tp_plan_destroy": [_VP],
+    "tp_plan_workspace_bytes": [_VP, C.c_int, C.POINTER(C.c_size_t)],
+    "tp_plan_shard_table": [_VP, C.c_int, C.POINTER(C.c_int32), C.c_int64, C.POINTER(C.c_int64)],
+    "tp_get_device_status": [_VP, _VP],
+    "tp_reduce_partials": [_VP, C.c_int, C.c_int32, C.c_int64, C.c_int32, _VP, _VP, _VP, _VP],
+    "tp_rmsnorm": [_VP, C.c_int64, C.c_int32, C.c_float, _VP, _VP],
+    "tp_colwise_forward": [_VP, _VP, _VP, _VP, _VP, _VP],
+    "tp_rowwise_forward": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
+    "tp_mlp_forward": [_VP] * 10 + [C.c_size_t, _VP],
+    "tp_qkv_forward": [_VP] * 7,
+    "tp_attn_core_forward": [_VP] * 4,
+    "tp_attn_forward": [_VP] * 10 + [C.c_size_t, _VP],
+    "tp_layer_forward": [_VP, _VP, C.POINTER(TPLayerWeights), _VP, _VP, C.c_size_t, _VP],
+    "tp_layer_forward_traced": [_VP, _VP, C.POINTER(TPLayerWeights), _VP, _VP, C.c_size_t, _VP,
+                                C.POINTER(C.c_void_p), C.c_int],
+    "tp_selftest_wait_timeout": [_VP, C.c_uint64, _VP],
+}
+EXPORTED = tuple(sorted(list(_SIGS) + ["tp_last_error"]))
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libtp.so for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def lib():
+    """Load libtp.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if _build.needs_build():
+            path = _build.build()
+        L = C.CDLL(path)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = C.c_int
+        L.tp_last_error.argtypes = []
+        L.tp_last_error.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def tp_last_error() -> str:
+    return lib().tp_last_error().decode("utf-8", "replace")
+
+
+def _call(name: str, *args) -> None:
+    rc = getattr(lib(), name)(*args)
+    if rc != TP_OK:
+        raise TPError(name, rc, tp_last_error())
+
+
+def _p(x) -> Optional[int]:
+    """Device pointer of a tensor (or an int / None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream) -> Optional[int]:
+    if stream is None:
+        import torch  # streams come from torch: plumbing only
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_config(tokens: int, hidden: int, ffn: int = 0, n_heads: int = 0, n_kv_heads: int = 0,
+                head_dim: int = 0, tp_degree: int = 1, act="gelu", reduce_mode: int = TP_REDUCE_FUSED,
+                partial_dtype: int = TP_F32, rms_eps: float = 1e-5, batch: int = 1,
+                seq: Optional[int] = None) -> TPConfig:
+    if isinstance(act, str):
+        act = ACT_BY_NAME[act]
+    if seq is None:
+        seq = tokens // max(batch, 1)
+    return TPConfig(tokens, batch, seq, hidden, ffn, n_heads, n_kv_heads, head_dim, tp_degree, act,
+                    reduce_mode, partial_dtype, rms_eps)
+
+
+class Plan:
+    """Owner of a tp_plan_t handle; destroyed with the object."""
+
+    def __init__(self, cfg: TPConfig):
+        h = C.c_void_p()
+        _call("tp_plan_create", C.byref(cfg), C.byref(h))
+        self.handle = h
+        self.cfg = cfg
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+    def close(self):
+        if self.handle:
+            lib().tp_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tp_plan_create(cfg: TPConfig) -> Plan:
+    return Plan(cfg)
+
+
+def tp_plan_destroy(plan: Plan) -> None:
+    plan.close()
+
+
+def tp_config_check(cfg: TPConfig) -> int:
+    """Host-only validation; returns the TP_* code (does not raise)."""
+    return lib().tp_config_check(C.byref(cfg))
+
+
+def _table(fn, target, which: int):
+    n = C.c_int64(0)
+    lib_fn = getattr(lib(), fn)
+    rc = lib_fn(target, which, None, 0, C.byref(n))
+    if rc not in (TP_OK, TP_ERR_INVALID_ARG) or (rc != TP_OK and n.value == 0):
+        raise TPError(fn, rc, tp_last_error())
+    buf = (C.c_int32 * max(n.value, 1))()
+    _call(fn, target, which, buf, n.value, C.byref(n))
+    return [buf[i] for i in range(n.value)]
+
+
+def tp_config_shard_table(cfg: TPConfig, which: int):
+    return _table("tp_config_shard_table", C.byref(cfg), which)
+
+
+def tp_plan_shard_table(plan: Plan, which: int):
+    return _table("tp_plan_shard_table", plan.handle, which)
+
+
+def tp_plan_workspace_bytes(plan: Plan, op: int) -> int:
+    n = C.c_size_t(0)
+    _call("tp_plan_workspace_bytes", plan.handle, op, C.byref(n))
+    return n.value
+
+
+def tp_get_device_status(plan: Plan, stream=None) -> int:
+    """TP_OK or TP_ERR_DEVICE_TIMEOUT (returned, not raised)."""
+    return lib().tp_get_device_status(plan.handle, _s(stream))
+
+
+def tp_reduce_partials(partials, partial_dtype: int, t: int, n: int, h: int, bias, residual, out,
+                       stream=None) -> None:
+    _call("tp_reduce_partials", _p(partials), partial_dtype, t, n, h, _p(bias), _p(residual),
+          _p(out), _s(stream))
+
+
+def tp_rmsnorm(x, rows: int, h: int, eps: float, y, stream=None) -> None:
+    _call("tp_rmsnorm", _p(x), rows, h, eps, _p(y), _s(stream))
+
+
+def tp_colwise_forward(plan: Plan, X, W1, W3, Y, stream=None) -> None:
+    _call("tp_colwise_forward", plan.handle, _p(X), _p(W1), _p(W3), _p(Y), _s(stream))
+
+
+def tp_rowwise_forward(plan: Plan, Y, W2, bias, residual, partials, Z, stream=None) -> None:
+    _call("tp_rowwise_forward", plan.handle, _p(Y), _p(W2), _p(bias), _p(residual), _p(partials),
+          _p(Z), _s(stream))
+
+
+def tp_mlp_forward(plan: Plan, X, W1, W3, W2, b2, residual, partials, Z, workspace,
+                   ws_bytes: int, stream=None) -> None:
+    _call("tp_mlp_forward", plan.handle, _p(X), _p(W1), _p(W3), _p(W2), _p(b2), _p(residual),
+          _p(partials), _p(Z), _p(workspace), ws_bytes, _s(stream))
+
+
+def tp_qkv_forward(plan: Plan, X, Wq, Wk, Wv, QKV, stream=None) -> None:
+    _call("tp_qkv_forward", plan.handle, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(QKV), _s(stream))
+
+
+def tp_attn_core_forward(plan: Plan, QKV, O, stream=None) -> None:
+    _call("tp_attn_core_forward", plan.handle, _p(QKV), _p(O), _s(stream))
+
+
+def tp_attn_forward(plan: Plan, X, Wq, Wk, Wv, Wo, residual, partials, out, workspace,
+                    ws_bytes: int, stream=None) -> None:
+    _call("tp_attn_forward", plan.handle, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(residual),
+          _p(partials), _p(out), _p(workspace), ws_bytes, _s(stream))
+
+
+def tp_layer_forward(plan: Plan, X, weights: dict, Y, workspace, ws_bytes: int,
+                     stream=None) -> None:
+    w = TPLayerWeights(*[_p(weights.get(k)) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")])
+    _call("tp_layer_forward", plan.handle, _p(X), C.byref(w), _p(Y), _p(workspace), ws_bytes,
+          _s(stream))
+
+
+def layer_weights(weights: dict) -> TPLayerWeights:
+    return TPLayerWeights(*[_p(weights.get(k)) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")])
+
+
+def tp_layer_forward_traced(plan: Plan, X, weights, Y, workspace, ws_bytes: int, events,
+                            stream=None) -> None:
+    """``events``: sequence of cudaEvent_t handles (ints) recorded at kernel boundaries."""
+    w = weights if isinstance(weights, TPLayerWeights) else layer_weights(weights)
+    arr = (C.c_void_p * len(events))(*events)
+    _call("tp_layer_forward_traced", plan.handle, _p(X), C.byref(w), _p(Y), _p(workspace),
+          ws_bytes, _s(stream), arr, len(events))
+
+
+def tp_selftest_wait_timeout(plan: Plan, timeout_ns: int, stream=None) -> None:
+    _call("tp_selftest_wait_timeout", plan.handle, timeout_ns, _s(stream))

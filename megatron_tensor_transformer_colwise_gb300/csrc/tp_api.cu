@@ -1,0 +1,671 @@
+// tp_api.cu -- the extern "C" entry points of libtp.so: plan creation and
+// validation, shard tables, workspace layout, and the composition of the
+// kernels into the MLP, attention and layer forwards.
+//
+// Sources: "Tensor 병렬성" (diffusers docs), sections "Colwise와 rowwise"
+// (colwise shards weight dim 0, rowwise weight dim 1, always paired in that
+// order so one all-reduce ends the block) and "제약 조건 및 검증"
+// (tp_degree must divide the head count; checked before any weight is
+// loaded), "한계" (unsupported combinations raise instead of silently
+// falling back); "텐서 병렬화" (itwiki), sections "MLP", "셀프 어텐션",
+// "통신 연산 f와 g"; "추론을 위한 텐서 병렬성" (transformers docs),
+// "DTensor" (rowwise bias replicated and added once after the reduction).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "tp.h"
+#include "tp_internal.h"
+
+struct tp_plan_s {
+    tp_config cfg;
+    int device;
+    unsigned* status;  // device status word (256 bytes allocated)
+    int64_t M, h, f, a, k, d, t;
+    int64_t fw;     // f / t: ffn columns per shard
+    int64_t ap;     // a / t: query heads per shard
+    int64_t kvn;    // KV heads held per shard
+    int64_t qw;     // ap * d
+    int64_t kvw;    // kvn * d
+    int64_t qkv_w;  // per-shard width of the QKV buffer: qw + 2 kvw
+    bool has_mlp, has_attn;
+    uint64_t timeout_ns;
+};
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int fail_str(int code, const std::string& s) {
+    g_last_error = s;
+    return code;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int need_ptr(const void* p, const char* name) {
+    if (!p) return fail(TP_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return fail(TP_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return TP_OK;
+}
+
+int opt_ptr(const void* p, const char* name) {
+    if (p && !aligned16(p)) return fail(TP_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return TP_OK;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int check_device(const tp_plan_s* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return fail(TP_ERR_CUDA, "cudaGetDevice failed");
+    if (dev != p->device)
+        return fail(TP_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev,
+                    p->device);
+    return TP_OK;
+}
+
+int64_t kv_first(int64_t k, int64_t t, int64_t i) { return (k >= t) ? i * (k / t) : (i * k) / t; }
+
+// Workspace regions of each op, in bytes, in order.
+struct Layout {
+    size_t y = 0;        // MLP colwise output [M][f] bf16
+    size_t qkv = 0;      // [M][t * qkv_w] bf16
+    size_t o = 0;        // [M][a d] bf16
+    size_t xn = 0;       // [M][h] bf16 (normalised input of a block)
+    size_t h1 = 0;       // [M][h] bf16 (residual stream after attention)
+    size_t partials = 0; // [t][M][h] fp32 or bf16 (layer in PARTIALS mode)
+};
+
+size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
+
+Layout layout_of(const tp_plan_s* p, int op) {
+    Layout L;
+    const size_t M = static_cast<size_t>(p->M);
+    if (op == TP_OP_MLP || op == TP_OP_LAYER) L.y = p->has_mlp ? align_up(M * p->f * 2) : 0;
+    if (op == TP_OP_ATTN || op == TP_OP_LAYER) {
+        if (p->has_attn) {
+            L.qkv = align_up(M * p->t * p->qkv_w * 2);
+            L.o = align_up(M * p->a * p->d * 2);
+        }
+    }
+    if (op == TP_OP_LAYER) {
+        L.xn = align_up(M * p->h * 2);
+        L.h1 = align_up(M * p->h * 2);
+        if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS)
+            L.partials = align_up(static_cast<size_t>(p->t) * M * p->h * partial_elem_bytes(p));
+    }
+    return L;
+}
+
+size_t layout_total(const Layout& L) { return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials; }
+
+int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
+    const size_t need = layout_total(layout_of(p, op));
+    if (need == 0) return TP_OK;
+    if (!ws) return fail(TP_ERR_WORKSPACE, "workspace is NULL but %zu bytes are needed", need);
+    if (!aligned16(ws)) return fail(TP_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+    if (bytes < need)
+        return fail(TP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, need);
+    return TP_OK;
+}
+
+int run(int rc, const std::string& err) {
+    if (rc != TP_OK) g_last_error = err;
+    return rc;
+}
+
+// ---- building blocks (arguments already validated) ----
+
+int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3, void* Y,
+               cudaStream_t s) {
+    tpi::GemmArgs g;
+    g.mode = (p->cfg.act == TP_ACT_SWIGLU) ? tpi::GEMM_COL_SWIGLU : tpi::GEMM_COL_ACT;
+    g.act = p->cfg.act;
+    g.M = p->M;
+    g.N = p->f;
+    g.A = X;
+    g.K = p->h;
+    g.t = static_cast<int>(p->t);
+    g.B0 = W1;
+    g.B0_rows = p->f;
+    if (g.mode == tpi::GEMM_COL_SWIGLU) {
+        g.B1 = W3;
+        g.B1_rows = p->f;
+    }
+    g.out = Y;
+    g.ldo = p->f;
+    g.status = p->status;
+    g.timeout_ns = p->timeout_ns;
+    std::string err;
+    return run(tpi::gemm_launch(g, s, &err), err);
+}
+
+// Rowwise GEMM of A [M][t*Ks] by B [N][t*Ks]: fused (sum over shards in the
+// accumulator, + bias + residual, bf16 out) or per-shard partials.
+int do_rowwise(const tp_plan_s* p, const void* A, int64_t Ks, const void* B, int64_t N,
+               const void* bias, const void* residual, void* partials, void* out, bool fused,
+               cudaStream_t s) {
+    tpi::GemmArgs g;
+    g.mode = fused ? tpi::GEMM_ROW_FUSED : tpi::GEMM_ROW_PARTIAL;
+    g.M = p->M;
+    g.N = N;
+    g.A = A;
+    g.t = static_cast<int>(p->t);
+    g.Ks = Ks;
+    g.B0 = B;
+    g.B0_rows = N;
+    if (fused) {
+        g.out = out;
+        g.ldo = N;
+        g.bias = bias;
+        g.residual = residual;
+        g.ldr = N;
+    } else {
+        g.out = partials;
+        g.ldo = N;
+        g.out_f32 = p->cfg.partial_dtype == TP_F32 ? 1 : 0;
+    }
+    g.status = p->status;
+    g.timeout_ns = p->timeout_ns;
+    std::string err;
+    return run(tpi::gemm_launch(g, s, &err), err);
+}
+
+int do_reduce(const tp_plan_s* p, const void* partials, const void* bias, const void* residual,
+              void* out, int64_t N, cudaStream_t s) {
+    std::string err;
+    return run(tpi::reduce_launch(partials, p->cfg.partial_dtype == TP_F32 ? 1 : 0,
+                                  static_cast<int>(p->t), p->M * N, static_cast<int>(N), bias,
+                                  residual, out, s, &err),
+               err);
+}
+
+int do_qkv(const tp_plan_s* p, const void* X, const void* Wq, const void* Wk, const void* Wv,
+           void* QKV, cudaStream_t s) {
+    tpi::GemmArgs g;
+    g.mode = tpi::GEMM_COL_QKV;
+    g.M = p->M;
+    g.N = p->t * p->qkv_w;
+    g.A = X;
+    g.K = p->h;
+    g.t = static_cast<int>(p->t);
+    g.B0 = Wq;
+    g.B0_rows = p->a * p->d;
+    g.B1 = Wk;
+    g.B1_rows = p->k * p->d;
+    g.B2 = Wv;
+    g.B2_rows = p->k * p->d;
+    g.qkv_ws = p->qkv_w;
+    g.qkv_qw = p->qw;
+    g.qkv_kvw = p->kvw;
+    g.kv_heads = static_cast<int>(p->k);
+    g.head_dim = static_cast<int>(p->d);
+    g.out = QKV;
+    g.ldo = g.N;
+    g.status = p->status;
+    g.timeout_ns = p->timeout_ns;
+    std::string err;
+    return run(tpi::gemm_launch(g, s, &err), err);
+}
+
+int do_attn_core(const tp_plan_s* p, const void* QKV, void* O, cudaStream_t s) {
+    tpi::AttnArgs a;
+    a.QKV = QKV;
+    a.ld_qkv = p->t * p->qkv_w;
+    a.shard_w = p->qkv_w;
+    a.q_w = p->qw;
+    a.kv_w = p->kvw;
+    a.O = O;
+    a.ld_o = p->a * p->d;
+    a.batch = p->cfg.batch;
+    a.seq = p->cfg.seq;
+    a.heads = static_cast<int>(p->a);
+    a.kv_heads = static_cast<int>(p->k);
+    a.head_dim = static_cast<int>(p->d);
+    a.t = static_cast<int>(p->t);
+    std::string err;
+    return run(tpi::attn_launch(a, s, &err), err);
+}
+
+uint8_t* region(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
+
+// Host-only validation of a configuration and the derived shard geometry
+// ("제약 조건 및 검증": every rule is checked before any device work).
+int derive_plan(const tp_config& cfg, tp_plan_s* p) {
+    const tp_config* pc = &cfg;
+    const tp_config c = *pc;
+    if (c.tokens < 1) return fail(TP_ERR_INVALID_ARG, "tokens must be >= 1 (got %lld)", (long long)c.tokens);
+    if (c.tokens > (int64_t)1 << 30) return fail(TP_ERR_UNSUPPORTED, "tokens above 2^30 are not supported");
+    if (c.tp_degree < 1 || c.tp_degree > 64)
+        return fail(TP_ERR_INVALID_ARG, "tp_degree must be in [1, 64] (got %d)", c.tp_degree);
+    if (c.hidden < 8 || c.hidden % 8)
+        return fail(TP_ERR_INVALID_ARG, "hidden must be a positive multiple of 8 (got %d)", c.hidden);
+    if (c.ffn < 0 || c.n_heads < 0 || c.n_kv_heads < 0 || c.head_dim < 0)
+        return fail(TP_ERR_INVALID_ARG, "sizes must be non-negative");
+    if (c.act < TP_ACT_GELU_ERF || c.act > TP_ACT_NONE)
+        return fail(TP_ERR_INVALID_ARG, "act %d is not one of TP_ACT_GELU_ERF(0), TP_ACT_GELU_TANH(1), "
+                    "TP_ACT_SWIGLU(2), TP_ACT_NONE(3)", c.act);
+    if (c.reduce_mode != TP_REDUCE_FUSED && c.reduce_mode != TP_REDUCE_PARTIALS)
+        return fail(TP_ERR_INVALID_ARG, "reduce_mode %d is not one of TP_REDUCE_FUSED(0), "
+                    "TP_REDUCE_PARTIALS(1)", c.reduce_mode);
+    if (c.partial_dtype != TP_F32 && c.partial_dtype != TP_BF16)
+        return fail(TP_ERR_INVALID_ARG, "partial_dtype %d is not one of TP_F32(0), TP_BF16(1)",
+                    c.partial_dtype);
+    if (c.reduce_mode == TP_REDUCE_FUSED && c.partial_dtype != TP_F32)
+        return fail(TP_ERR_UNSUPPORTED, "bf16 partials only exist in TP_REDUCE_PARTIALS mode");
+    const int64_t t = c.tp_degree;
+    // The pages' divisibility rules first, then this build's alignment rules.
+    if (c.ffn > 0 && c.ffn % t)
+        return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide ffn %d", c.tp_degree, c.ffn);
+    if (c.n_heads > 0) {
+        if (c.n_kv_heads < 1) return fail(TP_ERR_INVALID_ARG, "n_kv_heads must be >= 1 with attention");
+        if (c.n_heads % t)
+            return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide n_heads %d", c.tp_degree,
+                        c.n_heads);
+        if (c.n_heads % c.n_kv_heads)
+            return fail(TP_ERR_NOT_DIVISIBLE, "n_kv_heads %d does not divide n_heads %d", c.n_kv_heads,
+                        c.n_heads);
+        if (c.n_kv_heads >= t && c.n_kv_heads % t)
+            return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide n_kv_heads %d",
+                        c.tp_degree, c.n_kv_heads);
+        if (c.n_kv_heads < t && t % c.n_kv_heads)
+            return fail(TP_ERR_NOT_DIVISIBLE,
+                        "n_kv_heads %d < tp_degree %d must divide it to be replicated evenly",
+                        c.n_kv_heads, c.tp_degree);
+    }
+    if (c.ffn > 0 && (c.ffn / t) % 8)
+        return fail(TP_ERR_INVALID_ARG, "ffn / tp_degree = %lld must be a multiple of 8",
+                    (long long)(c.ffn / t));
+    if (c.n_heads > 0) {
+        if (c.head_dim != 64 && c.head_dim != 128)
+            return fail(TP_ERR_UNSUPPORTED, "head_dim %d: only 64 and 128 are built", c.head_dim);
+        if (c.batch < 1 || c.seq < 1 || (int64_t)c.batch * c.seq != c.tokens)
+            return fail(TP_ERR_INVALID_ARG, "tokens %lld must equal batch %d x seq %d",
+                        (long long)c.tokens, c.batch, c.seq);
+    }
+    if (!(c.rms_eps >= 0.0f)) return fail(TP_ERR_INVALID_ARG, "rms_eps must be >= 0");
+
+    *p = tp_plan_s();
+    p->cfg = c;
+    p->device = -1;
+    p->status = nullptr;
+    p->M = c.tokens;
+    p->h = c.hidden;
+    p->f = c.ffn;
+    p->a = c.n_heads;
+    p->k = c.n_kv_heads;
+    p->d = c.head_dim;
+    p->t = t;
+    p->has_mlp = c.ffn > 0;
+    p->has_attn = c.n_heads > 0;
+    p->fw = p->has_mlp ? p->f / t : 0;
+    if (p->has_attn) {
+        p->ap = p->a / t;
+        p->kvn = (p->k >= t) ? p->k / t : 1;
+        p->qw = p->ap * p->d;
+        p->kvw = p->kvn * p->d;
+        p->qkv_w = p->qw + 2 * p->kvw;
+    }
+    p->timeout_ns = 2000000000ull;  // 2 s per barrier wait
+    return TP_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+const char* tp_last_error(void) { return g_last_error.c_str(); }
+
+int tp_config_check(const tp_config* cfg) {
+    if (!cfg) return fail(TP_ERR_INVALID_ARG, "cfg is NULL");
+    tp_plan_s tmp;
+    return derive_plan(*cfg, &tmp);
+}
+
+int tp_plan_create(const tp_config* cfg, tp_plan_t* out) {
+    if (out) *out = nullptr;
+    if (!cfg || !out) return fail(TP_ERR_INVALID_ARG, "cfg and out must be non-NULL");
+    tp_plan_s tmp;
+    int rc = derive_plan(*cfg, &tmp);
+    if (rc) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(TP_ERR_CUDA, "no CUDA device");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(TP_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                    dev, major, minor);
+    tp_plan_s* p = new (std::nothrow) tp_plan_s(tmp);
+    if (!p) return fail(TP_ERR_CUDA, "out of host memory");
+    p->device = dev;
+    cudaError_t e = cudaMalloc(&p->status, 256);
+    if (e == cudaSuccess) e = cudaMemset(p->status, 0, 256);
+    if (e != cudaSuccess) {
+        delete p;
+        return fail(TP_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    }
+    *out = p;
+    return TP_OK;
+}
+
+int tp_plan_destroy(tp_plan_t plan) {
+    if (!plan) return TP_OK;
+    if (plan->status) cudaFree(plan->status);
+    delete plan;
+    return TP_OK;
+}
+
+int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes) {
+    if (!plan || !bytes) return fail(TP_ERR_INVALID_ARG, "plan and bytes must be non-NULL");
+    if (op < TP_OP_MLP || op > TP_OP_LAYER) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
+    *bytes = layout_total(layout_of(plan, op));
+    return TP_OK;
+}
+
+int tp_plan_shard_table(tp_plan_t plan, int which, int32_t* out, int64_t cap, int64_t* n) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    return tp_config_shard_table(&plan->cfg, which, out, cap, n);
+}
+
+int tp_config_shard_table(const tp_config* cfg, int which, int32_t* out, int64_t cap, int64_t* n) {
+    if (!cfg || !n) return fail(TP_ERR_INVALID_ARG, "cfg and n must be non-NULL");
+    tp_plan_s tmp;
+    int rc = derive_plan(*cfg, &tmp);
+    if (rc) return rc;
+    const tp_plan_s* p = &tmp;
+    int64_t cnt = 0;
+    switch (which) {
+        case TP_TABLE_FFN_SHARDS: cnt = 2 * p->t; break;
+        case TP_TABLE_Q_HEAD_SHARD:
+        case TP_TABLE_Q_HEAD_KV: cnt = p->a; break;
+        case TP_TABLE_SHARD_KV: cnt = p->has_attn ? 2 * p->t : 0; break;
+        case TP_TABLE_QKV_COLUMNS: cnt = p->has_attn ? 3 * p->t : 0; break;
+        default: return fail(TP_ERR_INVALID_ARG, "unknown table %d", which);
+    }
+    *n = cnt;
+    if (cnt > cap || (cnt > 0 && !out))
+        return fail(TP_ERR_INVALID_ARG, "table needs %lld entries, capacity %lld", (long long)cnt,
+                    (long long)cap);
+    for (int64_t i = 0; i < cnt; ++i) {
+        int64_t v = 0;
+        switch (which) {
+            case TP_TABLE_FFN_SHARDS: v = (i & 1) ? p->fw : (i >> 1) * p->fw; break;
+            case TP_TABLE_Q_HEAD_SHARD: v = i / p->ap; break;
+            case TP_TABLE_Q_HEAD_KV: v = i / (p->a / p->k); break;
+            case TP_TABLE_SHARD_KV: v = (i & 1) ? p->kvn : kv_first(p->k, p->t, i >> 1); break;
+            case TP_TABLE_QKV_COLUMNS: {
+                const int64_t s = i / 3, part = i % 3;
+                v = s * p->qkv_w + (part == 0 ? 0 : part == 1 ? p->qw : p->qw + p->kvw);
+                break;
+            }
+        }
+        out[i] = static_cast<int32_t>(v);
+    }
+    return TP_OK;
+}
+
+int tp_get_device_status(tp_plan_t plan, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    unsigned word = 0;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t e = cudaMemcpyAsync(&word, plan->status, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(TP_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (word) {
+        cudaMemsetAsync(plan->status, 0, sizeof(unsigned), s);
+        cudaStreamSynchronize(s);
+        return fail(TP_ERR_DEVICE_TIMEOUT, "a device-side wait exceeded its limit (status 0x%x)", word);
+    }
+    return TP_OK;
+}
+
+int tp_reduce_partials(const void* partials, int partial_dtype, int32_t t, int64_t n, int32_t h,
+                       const tp_bf16* bias, const tp_bf16* residual, tp_bf16* out, void* stream) {
+    int rc;
+    if ((rc = need_ptr(partials, "partials")) || (rc = need_ptr(out, "out")) ||
+        (rc = opt_ptr(bias, "bias")) || (rc = opt_ptr(residual, "residual")))
+        return rc;
+    if (partial_dtype != TP_F32 && partial_dtype != TP_BF16)
+        return fail(TP_ERR_INVALID_ARG, "partial_dtype %d is not TP_F32(0) or TP_BF16(1)", partial_dtype);
+    if (t < 1 || t > 64) return fail(TP_ERR_INVALID_ARG, "t must be in [1, 64]");
+    if (h < 8 || h % 8) return fail(TP_ERR_INVALID_ARG, "h must be a positive multiple of 8");
+    if (n < 0 || n % h) return fail(TP_ERR_INVALID_ARG, "n must be a non-negative multiple of h");
+    std::string err;
+    return run(tpi::reduce_launch(partials, partial_dtype == TP_F32 ? 1 : 0, t, n, h, bias, residual,
+                                  out, as_stream(stream), &err),
+               err);
+}
+
+int tp_rmsnorm(const tp_bf16* x, int64_t rows, int32_t h, float eps, tp_bf16* y, void* stream) {
+    int rc;
+    if ((rc = need_ptr(x, "x")) || (rc = need_ptr(y, "y"))) return rc;
+    if (rows < 0 || rows > (int64_t)1 << 30) return fail(TP_ERR_INVALID_ARG, "rows out of range");
+    if (h < 8 || h % 8 || h > 8192) return fail(TP_ERR_INVALID_ARG, "h must be a multiple of 8 in [8, 8192]");
+    if (!(eps >= 0.0f)) return fail(TP_ERR_INVALID_ARG, "eps must be >= 0");
+    std::string err;
+    return run(tpi::rmsnorm_launch(x, rows, h, eps, y, as_stream(stream), &err), err);
+}
+
+int tp_colwise_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                       tp_bf16* Y, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(W1, "W1")) ||
+        (rc = need_ptr(Y, "Y")))
+        return rc;
+    if (plan->cfg.act == TP_ACT_SWIGLU) {
+        if ((rc = need_ptr(W3, "W3 (SwiGLU)"))) return rc;
+    } else if (W3) {
+        return fail(TP_ERR_INVALID_ARG, "W3 must be NULL unless act is TP_ACT_SWIGLU");
+    }
+    return do_colwise(plan, X, W1, W3, Y, as_stream(stream));
+}
+
+int tp_rowwise_forward(tp_plan_t plan, const tp_bf16* Y, const tp_bf16* W2, const tp_bf16* bias,
+                       const tp_bf16* residual, void* partials, tp_bf16* Z, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(Y, "Y")) || (rc = need_ptr(W2, "W2"))) return rc;
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    if (fused) {
+        if ((rc = need_ptr(Z, "Z")) || (rc = opt_ptr(bias, "bias")) || (rc = opt_ptr(residual, "residual")))
+            return rc;
+    } else if ((rc = need_ptr(partials, "partials"))) {
+        return rc;
+    }
+    return do_rowwise(plan, Y, plan->fw, W2, plan->h, bias, residual, partials, Z, fused,
+                      as_stream(stream));
+}
+
+int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                   const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
+                   tp_bf16* Z, void* workspace, size_t ws_bytes, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(W1, "W1")) ||
+        (rc = need_ptr(W2, "W2")) || (rc = need_ptr(Z, "Z")) || (rc = opt_ptr(b2, "b2")) ||
+        (rc = opt_ptr(residual, "residual")))
+        return rc;
+    if (plan->cfg.act == TP_ACT_SWIGLU) {
+        if ((rc = need_ptr(W3, "W3 (SwiGLU)"))) return rc;
+    } else if (W3) {
+        return fail(TP_ERR_INVALID_ARG, "W3 must be NULL unless act is TP_ACT_SWIGLU");
+    }
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    if (!fused && (rc = need_ptr(partials, "partials"))) return rc;
+    if ((rc = check_ws(plan, TP_OP_MLP, workspace, ws_bytes))) return rc;
+    cudaStream_t s = as_stream(stream);
+    void* Y = workspace;
+    if ((rc = do_colwise(plan, X, W1, W3, Y, s))) return rc;
+    if ((rc = do_rowwise(plan, Y, plan->fw, W2, plan->h, b2, residual, partials, Z, fused, s))) return rc;
+    if (!fused) return do_reduce(plan, partials, b2, residual, Z, plan->h, s);
+    return TP_OK;
+}
+
+int tp_qkv_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                   const tp_bf16* Wv, tp_bf16* QKV, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Wq, "Wq")) ||
+        (rc = need_ptr(Wk, "Wk")) || (rc = need_ptr(Wv, "Wv")) || (rc = need_ptr(QKV, "QKV")))
+        return rc;
+    return do_qkv(plan, X, Wq, Wk, Wv, QKV, as_stream(stream));
+}
+
+int tp_attn_core_forward(tp_plan_t plan, const tp_bf16* QKV, tp_bf16* O, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(QKV, "QKV")) || (rc = need_ptr(O, "O"))) return rc;
+    return do_attn_core(plan, QKV, O, as_stream(stream));
+}
+
+int tp_attn_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                    const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* residual, void* partials,
+                    tp_bf16* out, void* workspace, size_t ws_bytes, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Wq, "Wq")) ||
+        (rc = need_ptr(Wk, "Wk")) || (rc = need_ptr(Wv, "Wv")) || (rc = need_ptr(Wo, "Wo")) ||
+        (rc = need_ptr(out, "out")) || (rc = opt_ptr(residual, "residual")))
+        return rc;
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    if (!fused && (rc = need_ptr(partials, "partials"))) return rc;
+    if ((rc = check_ws(plan, TP_OP_ATTN, workspace, ws_bytes))) return rc;
+    const Layout L = layout_of(plan, TP_OP_ATTN);
+    void* QKV = region(workspace, 0);
+    void* O = region(workspace, L.qkv);
+    cudaStream_t s = as_stream(stream);
+    if ((rc = do_qkv(plan, X, Wq, Wk, Wv, QKV, s))) return rc;
+    if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
+    if ((rc = do_rowwise(plan, O, plan->qw, Wo, plan->h, nullptr, residual, partials, out, fused, s)))
+        return rc;
+    if (!fused) return do_reduce(plan, partials, nullptr, residual, out, plan->h, s);
+    return TP_OK;
+}
+
+int tp_layer_forward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, tp_bf16* Y,
+                     void* workspace, size_t ws_bytes, void* stream) {
+    return tp_layer_forward_traced(plan, X, w, Y, workspace, ws_bytes, stream, nullptr, 0);
+}
+
+int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w,
+                            tp_bf16* Y, void* workspace, size_t ws_bytes, void* stream,
+                            void* const* events, int n_events) {
+    if (!plan || !w) return fail(TP_ERR_INVALID_ARG, "plan and weights must be non-NULL");
+    if (!plan->has_attn || !plan->has_mlp)
+        return fail(TP_ERR_INVALID_ARG, "a layer needs both attention (n_heads > 0) and an MLP (ffn > 0)");
+    if (plan->h > 8192) return fail(TP_ERR_UNSUPPORTED, "layer RMSNorm supports hidden <= 8192");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Y, "Y")) ||
+        (rc = need_ptr(w->Wq, "Wq")) || (rc = need_ptr(w->Wk, "Wk")) || (rc = need_ptr(w->Wv, "Wv")) ||
+        (rc = need_ptr(w->Wo, "Wo")) || (rc = need_ptr(w->W1, "W1")) || (rc = need_ptr(w->W2, "W2")))
+        return rc;
+    if (plan->cfg.act == TP_ACT_SWIGLU) {
+        if ((rc = need_ptr(w->W3, "W3 (SwiGLU)"))) return rc;
+    } else if (w->W3) {
+        return fail(TP_ERR_INVALID_ARG, "W3 must be NULL unless act is TP_ACT_SWIGLU");
+    }
+    if (X == Y) return fail(TP_ERR_INVALID_ARG, "X and Y must not alias");
+    if ((rc = check_ws(plan, TP_OP_LAYER, workspace, ws_bytes))) return rc;
+    const bool fused_mode = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    const int need_events = fused_mode ? 8 : 9;
+    if (events) {
+        if (n_events < need_events)
+            return fail(TP_ERR_INVALID_ARG, "%d events given, %d needed", n_events, need_events);
+        for (int i = 0; i < need_events; ++i)
+            if (!events[i]) return fail(TP_ERR_INVALID_ARG, "event %d is NULL", i);
+    }
+    int ev_i = 0;
+    auto mark = [&](cudaStream_t st) {
+        if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[ev_i++]), st);
+    };
+    const Layout L = layout_of(plan, TP_OP_LAYER);
+    size_t off = 0;
+    void* Yb = region(workspace, off); off += L.y;
+    void* QKV = region(workspace, off); off += L.qkv;
+    void* O = region(workspace, off); off += L.o;
+    void* xn = region(workspace, off); off += L.xn;
+    void* h1 = region(workspace, off); off += L.h1;
+    void* P = L.partials ? region(workspace, off) : nullptr;
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    const float eps = plan->cfg.rms_eps;
+    cudaStream_t s = as_stream(stream);
+    std::string err;
+    // Attention block: h1 = x + sum_i O_i Wo_i^T with O from RMSNorm(x).
+    mark(s);
+    if ((rc = run(tpi::rmsnorm_launch(X, plan->M, (int)plan->h, eps, xn, s, &err), err))) return rc;
+    mark(s);
+    if ((rc = do_qkv(plan, xn, w->Wq, w->Wk, w->Wv, QKV, s))) return rc;
+    mark(s);
+    if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
+    mark(s);
+    if (fused) {
+        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s))) return rc;
+        mark(s);
+        if ((rc = run(tpi::rmsnorm_launch(h1, plan->M, (int)plan->h, eps, xn, s, &err), err))) return rc;
+        mark(s);
+    } else {
+        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, nullptr, P, nullptr, false, s)))
+            return rc;
+        mark(s);
+        // g of the attention block fused with the MLP's RMSNorm.
+        if ((rc = run(tpi::reduce_norm_launch(P, plan->cfg.partial_dtype == TP_F32 ? 1 : 0, (int)plan->t,
+                                              plan->M, (int)plan->h, X, h1, xn, eps, s, &err),
+                      err)))
+            return rc;
+        mark(s);
+    }
+    // MLP block: y = h1 + sum_i act(xn A_i) B_i.
+    if ((rc = do_colwise(plan, xn, w->W1, w->W3, Yb, s))) return rc;
+    mark(s);
+    if (fused) {
+        if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s))) return rc;
+        mark(s);
+        return TP_OK;
+    }
+    if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, nullptr, P, nullptr, false, s)))
+        return rc;
+    mark(s);
+    if ((rc = do_reduce(plan, P, nullptr, h1, Y, plan->h, s))) return rc;
+    mark(s);
+    return TP_OK;
+}
+
+int tp_selftest_wait_timeout(tp_plan_t plan, uint64_t timeout_ns, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (timeout_ns < 1000ull || timeout_ns > 1000000000ull)
+        return fail(TP_ERR_INVALID_ARG, "timeout_ns must be in [1e3, 1e9]");
+    int rc;
+    if ((rc = check_device(plan))) return rc;
+    std::string err;
+    return run(tpi::selftest_timeout_launch(plan->status, timeout_ns, as_stream(stream), &err), err);
+}
+
+}  // extern "C"

@@ -1,0 +1,310 @@
+// tp_elementwise.cu -- HBM-bound kernels of the block: the g-operator
+// reduction of the t shard partials, the replicated RMSNorm, and the
+// reduction fused with the next RMSNorm.
+//
+// Source: "텐서 병렬화" (itwiki, Tensor parallelism), section "통신 연산 f와
+// g": g is an all-reduce of the t partial sums in the forward pass; norm,
+// dropout and residual are replicated.  "추론을 위한 텐서 병렬성"
+// (transformers docs), "설계 구현 / DTensor": a rowwise bias is replicated
+// and added once, after the reduction.
+//
+// The reduction is elementwise over t: every thread owns 8 consecutive
+// outputs, loads them from each of the t partials with 128-bit streaming
+// loads (all issued before the adds), sums in fp32 in shard order
+// i = 0..t-1, adds bias and residual, and stores 8 bf16 with one 128-bit
+// store.  No shuffles, no shared memory; a grid-stride loop over a grid of
+// SM count x 8 CTAs keeps enough loads in flight to saturate HBM.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "tp_device.cuh"
+#include "tp_internal.h"
+
+namespace {
+
+using namespace tpk;
+
+constexpr int RED_THREADS = 256;
+constexpr int MAX_T = 64;
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+    }
+}
+
+// out[e] = sum_i P[i][e] (+ bias[e % h]) (+ residual[e]); T known at compile
+// time (0 = runtime t).
+template <int T, bool F32>
+__global__ void __launch_bounds__(RED_THREADS) reduce_kernel(const void* __restrict__ partials, int t,
+                                                             long long n, int h,
+                                                             const __nv_bfloat16* __restrict__ bias,
+                                                             const __nv_bfloat16* __restrict__ residual,
+                                                             __nv_bfloat16* out) {
+    const int tt = T ? T : t;
+    const long long nvec = n >> 3;
+    for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
+         v += (long long)gridDim.x * blockDim.x) {
+        const long long e0 = v << 3;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        if (F32) {
+            const float* P = reinterpret_cast<const float*>(partials) + e0;
+            if (T) {
+                uint4 lo[T ? T : 1], hi[T ? T : 1];
+#pragma unroll
+                for (int i = 0; i < T; ++i) {
+                    lo[i] = ld_stream(P + i * n);
+                    hi[i] = ld_stream(P + i * n + 4);
+                }
+#pragma unroll
+                for (int i = 0; i < T; ++i) {
+                    acc[0] += __uint_as_float(lo[i].x);
+                    acc[1] += __uint_as_float(lo[i].y);
+                    acc[2] += __uint_as_float(lo[i].z);
+                    acc[3] += __uint_as_float(lo[i].w);
+                    acc[4] += __uint_as_float(hi[i].x);
+                    acc[5] += __uint_as_float(hi[i].y);
+                    acc[6] += __uint_as_float(hi[i].z);
+                    acc[7] += __uint_as_float(hi[i].w);
+                }
+            } else {
+                for (int i = 0; i < tt; ++i) {
+                    const uint4 lo = ld_stream(P + i * n), hi = ld_stream(P + i * n + 4);
+                    acc[0] += __uint_as_float(lo.x);
+                    acc[1] += __uint_as_float(lo.y);
+                    acc[2] += __uint_as_float(lo.z);
+                    acc[3] += __uint_as_float(lo.w);
+                    acc[4] += __uint_as_float(hi.x);
+                    acc[5] += __uint_as_float(hi.y);
+                    acc[6] += __uint_as_float(hi.z);
+                    acc[7] += __uint_as_float(hi.w);
+                }
+            }
+        } else {
+            const __nv_bfloat16* P = reinterpret_cast<const __nv_bfloat16*>(partials) + e0;
+            if (T) {
+                uint4 pv[T ? T : 1];
+#pragma unroll
+                for (int i = 0; i < T; ++i) pv[i] = ld_stream(P + i * n);
+#pragma unroll
+                for (int i = 0; i < T; ++i) add_bf16x8(acc, pv[i]);
+            } else {
+                for (int i = 0; i < tt; ++i) add_bf16x8(acc, ld_stream(P + i * n));
+            }
+        }
+        if (bias) add_bf16x8(acc, *reinterpret_cast<const uint4*>(bias + (e0 % h)));
+        if (residual) add_bf16x8(acc, *reinterpret_cast<const uint4*>(residual + e0));
+        *reinterpret_cast<uint4*>(out + e0) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
+// Row kernel: one CTA per row of h (h/8 vectors spread over the block, at
+// most 4 per thread).  h1 = sum_i P[i][row] + residual[row] (bf16-rounded),
+// then optionally xn = h1 / sqrt(mean(h1^2) + eps) from the rounded h1.
+constexpr int ROW_THREADS = 256;
+constexpr int ROW_VEC = 4;  // vectors of 8 per thread -> h <= 8192
+
+template <bool HAS_P, bool F32>
+__global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict__ partials, int t,
+                                                          long long n, int h,
+                                                          const __nv_bfloat16* __restrict__ src,
+                                                          __nv_bfloat16* h1_out,
+                                                          __nv_bfloat16* xn_out, float eps) {
+    __shared__ float red[ROW_THREADS / 32];
+    const long long row = blockIdx.x;
+    const int nv = h >> 3;
+    float vals[ROW_VEC][8];
+    float ss = 0.0f;
+#pragma unroll
+    for (int j = 0; j < ROW_VEC; ++j) {
+        const int v = threadIdx.x + j * ROW_THREADS;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vals[j][e] = 0.0f;
+        if (v < nv) {
+            const long long e0 = row * h + (long long)v * 8;
+            if (HAS_P) {
+                for (int i = 0; i < t; ++i) {
+                    if (F32) {
+                        const float* P = reinterpret_cast<const float*>(partials) + i * n + e0;
+                        const uint4 lo = ld_stream(P), hi = ld_stream(P + 4);
+                        vals[j][0] += __uint_as_float(lo.x);
+                        vals[j][1] += __uint_as_float(lo.y);
+                        vals[j][2] += __uint_as_float(lo.z);
+                        vals[j][3] += __uint_as_float(lo.w);
+                        vals[j][4] += __uint_as_float(hi.x);
+                        vals[j][5] += __uint_as_float(hi.y);
+                        vals[j][6] += __uint_as_float(hi.z);
+                        vals[j][7] += __uint_as_float(hi.w);
+                    } else {
+                        add_bf16x8(vals[j], ld_stream(reinterpret_cast<const __nv_bfloat16*>(partials) +
+                                                      i * n + e0));
+                    }
+                }
+            }
+            if (src) add_bf16x8(vals[j], *reinterpret_cast<const uint4*>(src + e0));
+            const uint4 packed =
+                make_uint4(pack_bf16x2(vals[j][0], vals[j][1]), pack_bf16x2(vals[j][2], vals[j][3]),
+                           pack_bf16x2(vals[j][4], vals[j][5]), pack_bf16x2(vals[j][6], vals[j][7]));
+            if (h1_out) *reinterpret_cast<uint4*>(h1_out + e0) = packed;
+            // The norm reads the residual stream as stored (bf16).
+            const uint32_t w[4] = {packed.x, packed.y, packed.z, packed.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16x2(w[e]);
+                vals[j][2 * e] = f.x;
+                vals[j][2 * e + 1] = f.y;
+                ss += f.x * f.x + f.y * f.y;
+            }
+        }
+    }
+    if (!xn_out) return;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < ROW_THREADS / 32; ++w) tot += red[w];
+    const float r = rsqrtf(tot / static_cast<float>(h) + eps);
+#pragma unroll
+    for (int j = 0; j < ROW_VEC; ++j) {
+        const int v = threadIdx.x + j * ROW_THREADS;
+        if (v < nv) {
+            const long long e0 = row * h + (long long)v * 8;
+            *reinterpret_cast<uint4*>(xn_out + e0) = make_uint4(
+                pack_bf16x2(vals[j][0] * r, vals[j][1] * r), pack_bf16x2(vals[j][2] * r, vals[j][3] * r),
+                pack_bf16x2(vals[j][4] * r, vals[j][5] * r), pack_bf16x2(vals[j][6] * r, vals[j][7] * r));
+        }
+    }
+}
+
+// Failure-detection self test: wait on a barrier that never completes.
+__global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing arrives: the bounded wait gives up and records a timeout.
+        mbar_wait(smem_u32(&bar), 0, &abort_flag, status, timeout_ns);
+    }
+    __syncthreads();
+}
+
+std::string cuda_msg(const char* what, cudaError_t e) {
+    return std::string(what) + ": " + cudaGetErrorString(e);
+}
+
+int check_launch(const char* what, std::string* err) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        if (err) *err = cuda_msg(what, e);
+        return TP_ERR_CUDA;
+    }
+    return TP_OK;
+}
+
+}  // namespace
+
+namespace tpi {
+
+int device_sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 1;
+    if (!counts[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n > 0 ? n : 1;
+    }
+    return counts[dev];
+}
+
+int reduce_launch(const void* partials, int partial_f32, int t, int64_t n, int h, const void* bias,
+                  const void* residual, void* out, cudaStream_t stream, std::string* err) {
+    if (n == 0) return TP_OK;
+    const long long nvec = n / 8;
+    long long blocks = (nvec + RED_THREADS - 1) / RED_THREADS;
+    blocks = std::min<long long>(blocks, (long long)device_sm_count() * 8);
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(bias);
+    const __nv_bfloat16* r = reinterpret_cast<const __nv_bfloat16*>(residual);
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+#define TP_RED(TT, FF) \
+    reduce_kernel<TT, FF><<<(unsigned)blocks, RED_THREADS, 0, stream>>>(partials, t, n, h, b, r, o)
+    if (partial_f32) {
+        switch (t) {
+            case 1: TP_RED(1, true); break;
+            case 2: TP_RED(2, true); break;
+            case 4: TP_RED(4, true); break;
+            case 8: TP_RED(8, true); break;
+            default: TP_RED(0, true); break;
+        }
+    } else {
+        switch (t) {
+            case 1: TP_RED(1, false); break;
+            case 2: TP_RED(2, false); break;
+            case 4: TP_RED(4, false); break;
+            case 8: TP_RED(8, false); break;
+            default: TP_RED(0, false); break;
+        }
+    }
+#undef TP_RED
+    return check_launch("reduce kernel", err);
+}
+
+int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t rows, int h,
+                       const void* residual, void* h1, void* xn, float eps, cudaStream_t stream,
+                       std::string* err) {
+    if (rows == 0) return TP_OK;
+    const long long n = rows * (long long)h;
+    const __nv_bfloat16* r = reinterpret_cast<const __nv_bfloat16*>(residual);
+    auto* h1p = reinterpret_cast<__nv_bfloat16*>(h1);
+    auto* xnp = reinterpret_cast<__nv_bfloat16*>(xn);
+    if (partial_f32)
+        row_kernel<true, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp, eps);
+    else
+        row_kernel<true, false><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp, eps);
+    return check_launch("reduce+norm kernel", err);
+}
+
+int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaStream_t stream,
+                   std::string* err) {
+    if (rows == 0) return TP_OK;
+    const long long n = rows * (long long)h;
+    row_kernel<false, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(
+        nullptr, 0, n, h, reinterpret_cast<const __nv_bfloat16*>(x), nullptr,
+        reinterpret_cast<__nv_bfloat16*>(y), eps);
+    return check_launch("rmsnorm kernel", err);
+}
+
+int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,
+                            std::string* err) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return check_launch("self-test kernel", err);
+}
+
+}  // namespace tpi

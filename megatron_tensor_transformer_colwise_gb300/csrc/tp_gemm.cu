@@ -1,0 +1,568 @@
+// tp_gemm.cu -- the column- and row-parallel GEMMs of the tensor-parallel
+// block on sm_103a tensor cores (tcgen05 / TMEM), fed by TMA.
+//
+// Source: "텐서 병렬화" (itwiki, Tensor parallelism), sections "행렬 곱
+// 나누기" (column parallel: Y_i = X A_i with X replicated; row parallel:
+// Y_i = X_i A_i, then Y = sum_i Y_i), "MLP" (A colwise with the nonlinearity
+// applied per shard, B rowwise, one sum at the end; SwiGLU with W1 and W3
+// colwise) and "셀프 어텐션" (Q/K/V colwise, a/t heads per shard; o_proj
+// rowwise).
+//
+// One kernel template, one CTA per SM (persistent), 6 warps:
+//   warp 0      TMA producer (one lane): A and B tiles into a 4-stage ring
+//   warp 1      TMEM owner and MMA issuer (one lane): 128x256x16 bf16 UMMAs
+//   warps 2..5  epilogue: TMEM -> registers -> fused op -> global
+// The accumulator is double-buffered in TMEM (2 x 256 fp32 columns) so the
+// epilogue of tile n overlaps the main loop of tile n+1.
+//
+// Shards are grid/loop indices, not devices: a colwise output tile may span
+// shard boundaries (the output is the concatenation of the shards' slices);
+// the rowwise GEMM addresses shard i's K block through a 3-D tensor map
+// (K per shard, shard, rows), so "fused" mode runs the shard loop as the
+// outer K loop of one accumulator -- the g sum happens in TMEM -- and
+// "partial" mode gives every shard its own [M][N] output.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "tp_device.cuh"
+#include "tp_internal.h"
+
+namespace {
+
+using namespace tpk;
+
+constexpr int BM = 128;             // UMMA M (TMEM lanes)
+constexpr int BN = 256;             // UMMA N (TMEM columns per accumulator)
+constexpr int BK = 64;              // one 128-byte swizzle row of bf16
+constexpr int UK = 16;              // K of one kind::f16 UMMA
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_CHUNK_ROWS = 64;
+constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int TMEM_COLS = 2 * BN;               // 512
+constexpr int NUM_THREADS = 192;
+constexpr int GROUP_M = 8;
+constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+
+struct GemmParams {
+    CUtensorMap mapA;
+    CUtensorMap mapB[3];
+    int M, N;
+    int kb_per_shard;  // k-blocks of BK per shard (colwise: per whole K)
+    int k_shards;      // shards walked inside the K loop (ROW_FUSED: t)
+    int m_tiles, n_tiles, grid_shards, num_tiles;
+    int act;
+    int b_rows0;       // rows of B0 (out-of-range chunks read zeros)
+    int qkv_ws, qkv_qw, qkv_kvw, kv_heads, head_dim, tp;
+    void* out;
+    long long ldo;
+    long long shard_stride;  // ROW_PARTIAL: elements between shard outputs
+    int out_f32;
+    const __nv_bfloat16* bias;
+    const __nv_bfloat16* residual;
+    long long ldr;
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& s, int& mb,
+                                            int& nb) {
+    const int per_shard = p.m_tiles * p.n_tiles;
+    s = tile / per_shard;
+    const int r = tile - s * per_shard;
+    const int group_size = GROUP_M * p.n_tiles;
+    const int g = r / group_size;
+    const int first_m = g * GROUP_M;
+    const int gm = min(p.m_tiles - first_m, GROUP_M);
+    const int rr = r - g * group_size;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+// First KV head held by shard i (k/t own heads when k >= t, else a replica
+// of head i*k/t): "셀프 어텐션", GQA KV heads replicated when fewer than t.
+__device__ __forceinline__ int kv_first(int k, int t, int i) {
+    return (k >= t) ? i * (k / t) : (i * k) / t;
+}
+
+__device__ __forceinline__ float act_apply(int act, float v) {
+    if (act == TP_ACT_GELU_ERF) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    if (act == TP_ACT_GELU_TANH)
+        return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * (v + 0.044715f * v * v * v)));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    *reinterpret_cast<uint4*>(ptr) = make_uint4(a, b, c, d);
+}
+
+// Bounded wait used only while draining after an abort (ignores the flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 200000000ull) break;  // 200 ms
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
+                                              volatile int* abort_flag) {
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, last_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int s_grid, mb, nb;
+        decode_tile(p, tile, s_grid, mb, nb);
+        for (int ks = 0; ok && ks < p.k_shards; ++ks) {
+            const int shard = (MODE == tpi::GEMM_ROW_PARTIAL) ? s_grid : ks;
+            for (int kb = 0; kb < p.kb_per_shard; ++kb) {
+                const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+                if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full, STAGE_BYTES);
+                const uint32_t a_dst = base + stage * STAGE_BYTES;
+                const uint32_t b_dst = a_dst + A_BYTES;
+                const int kc = kb * BK;
+                if (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL) {
+                    tma_load_3d(a_dst, &p.mapA, full, kc, shard, mb * BM);
+#pragma unroll
+                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c)
+                        tma_load_3d(b_dst + c * B_CHUNK_BYTES, &p.mapB[0], full, kc, shard,
+                                    nb * BN + c * B_CHUNK_ROWS);
+                } else {
+                    tma_load_2d(a_dst, &p.mapA, full, kc, mb * BM);
+#pragma unroll
+                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c) {
+                        const CUtensorMap* map = &p.mapB[0];
+                        int row;
+                        if (MODE == tpi::GEMM_COL_SWIGLU) {
+                            // rows [0,128) of the tile: W1; rows [128,256): W3,
+                            // both for output columns nb*128 .. nb*128+127.
+                            const int half = c >> 1;
+                            map = &p.mapB[half];
+                            row = nb * (BN / 2) + (c & 1) * B_CHUNK_ROWS;
+                        } else if (MODE == tpi::GEMM_COL_QKV) {
+                            const int col = nb * BN + c * B_CHUNK_ROWS;
+                            if (col >= p.N) {
+                                row = p.b_rows0;  // wholly out of range: zeros
+                            } else {
+                                const int i = col / p.qkv_ws;
+                                const int l = col - i * p.qkv_ws;
+                                if (l < p.qkv_qw) {
+                                    row = i * p.qkv_qw + l;
+                                } else {
+                                    const int kv0 = kv_first(p.kv_heads, p.tp, i) * p.head_dim;
+                                    const int l2 = l - p.qkv_qw;
+                                    if (l2 < p.qkv_kvw) {
+                                        map = &p.mapB[1];
+                                        row = kv0 + l2;
+                                    } else {
+                                        map = &p.mapB[2];
+                                        row = kv0 + (l2 - p.qkv_kvw);
+                                    }
+                                }
+                            }
+                        } else {
+                            row = nb * BN + c * B_CHUNK_ROWS;
+                        }
+                        tma_load_2d(b_dst + c * B_CHUNK_BYTES, map, full, kc, row);
+                    }
+                }
+                issued_mask |= 1u << stage;
+                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (!ok) {
+        // Let every copy this thread started land before the CTA exits.
+        for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s)) drain_wait(bar0 + 8 * s, (last_parity >> s) & 1u);
+    }
+}
+
+__device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
+                                         uint32_t tmem_base, volatile int* abort_flag) {
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    const int kblocks = p.k_shards * p.kb_per_shard;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const uint32_t tfull = bar0 + 8 * (2 * STAGES + acc);
+        const uint32_t tempty = bar0 + 8 * (2 * STAGES + 2 + acc);
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+            if (!mbar_wait(full, phase, abort_flag, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = base + stage * STAGE_BYTES;
+            const uint64_t adesc = sdesc_sw128(a_addr);
+            const uint64_t bdesc = sdesc_sw128(a_addr + A_BYTES);
+#pragma unroll
+            for (int j = 0; j < BK / UK; ++j) {
+                // +32 bytes along K inside the 128-byte swizzle row.
+                umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc,
+                          (kb > 0 || j > 0) ? 1u : 0u);
+            }
+            umma_commit(empty);  // frees the smem stage when these UMMAs finish
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit(tfull);  // accumulator ready for the epilogue
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+        // No UMMA may still write TMEM when it is freed.
+        const uint32_t drain = bar0 + 8 * (2 * STAGES + 4);
+        umma_commit(drain);
+        drain_wait(drain, 0);
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0,
+                                              uint32_t tmem_base, volatile int* abort_flag) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        int s_grid, mb, nb;
+        decode_tile(p, tile, s_grid, mb, nb);
+        const uint32_t tfull = bar0 + 8 * (2 * STAGES + acc);
+        const uint32_t tempty = bar0 + 8 * (2 * STAGES + 2 + acc);
+        const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status, p.timeout_ns);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after();
+        const int row = mb * BM + q * 32 + lane;
+        const bool row_ok = row < p.M;
+        const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t r[32];
+        if (MODE == tpi::GEMM_COL_SWIGLU) {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+            for (int c = 0; c < (BN / 2) / 32; ++c) {
+                if (nb * (BN / 2) + c * 32 >= p.N) break;  // warp-uniform
+                uint32_t u[32];
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);             // gate: X W1^T
+                tmem_ld32(t0 + BN / 2 + c * 32, u);    // up:   X W3^T
+                tmem_ld_wait();
+                const int col0 = nb * (BN / 2) + c * 32;
+                if (row_ok) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = col0 + g * 8;
+                        if (col < p.N) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float g0 = __uint_as_float(r[g * 8 + 2 * e]);
+                                const float g1 = __uint_as_float(r[g * 8 + 2 * e + 1]);
+                                const float u0 = __uint_as_float(u[g * 8 + 2 * e]);
+                                const float u1 = __uint_as_float(u[g * 8 + 2 * e + 1]);
+                                const float h0 = g0 / (1.0f + expf(-g0)) * u0;
+                                const float h1 = g1 / (1.0f + expf(-g1)) * u1;
+                                w[e] = pack_bf16x2(h0, h1);
+                            }
+                            st_v4(out + static_cast<long long>(row) * p.ldo + col, w[0], w[1],
+                                  w[2], w[3]);
+                        }
+                    }
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N) break;  // warp-uniform
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);
+                tmem_ld_wait();
+                if (!row_ok) {
+                } else if (MODE == tpi::GEMM_ROW_PARTIAL && p.out_f32) {
+                    float* out = reinterpret_cast<float*>(p.out) + s_grid * p.shard_stride +
+                                 static_cast<long long>(row) * p.ldo;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int col = col0 + g * 4;
+                        if (col < p.N)
+                            st_v4(out + col, r[g * 4], r[g * 4 + 1], r[g * 4 + 2], r[g * 4 + 3]);
+                    }
+                } else {
+                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+                    if (MODE == tpi::GEMM_ROW_PARTIAL) out += s_grid * p.shard_stride;
+                    out += static_cast<long long>(row) * p.ldo;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = col0 + g * 8;
+                        if (col >= p.N) continue;
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[g * 8 + e]);
+                        if (MODE == tpi::GEMM_COL_ACT) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
+                        }
+                        if (MODE == tpi::GEMM_ROW_FUSED) {
+                            if (p.bias) {
+                                const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col);
+                                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = unpack_bf16x2(bw[e]);
+                                    v[2 * e] += f.x;
+                                    v[2 * e + 1] += f.y;
+                                }
+                            }
+                            if (p.residual) {
+                                const uint4 rr = *reinterpret_cast<const uint4*>(
+                                    p.residual + static_cast<long long>(row) * p.ldr + col);
+                                const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = unpack_bf16x2(rw[e]);
+                                    v[2 * e] += f.x;
+                                    v[2 * e + 1] += f.y;
+                                }
+                            }
+                        }
+                        st_v4(out + col, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8 * s, 1);             // full: producer arrive + tx bytes
+            mbar_init(bar0 + 8 * (STAGES + s), 1);  // empty: one tcgen05.commit
+        }
+        mbar_init(bar0 + 8 * (2 * STAGES + 0), 1);  // tmem full x2: one commit
+        mbar_init(bar0 + 8 * (2 * STAGES + 1), 1);
+        mbar_init(bar0 + 8 * (2 * STAGES + 2), 4);  // tmem empty x2: 4 epilogue warps
+        mbar_init(bar0 + 8 * (2 * STAGES + 3), 4);
+        mbar_init(bar0 + 8 * (2 * STAGES + 4), 1);  // drain
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.mapA);
+        tma_prefetch_desc(&p.mapB[0]);
+        if (MODE == tpi::GEMM_COL_SWIGLU || MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[1]);
+        if (MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[2]);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) producer_loop<MODE>(p, base, bar0, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) mma_loop(p, base, bar0, tmem_base, abort_flag);
+    } else {
+        epilogue_loop<MODE>(p, bar0, tmem_base, abort_flag);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(std::string* err) {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn && err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
+// bytes for dims 1.., box innermost first.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box, std::string* err) {
+    EncodeTiledFn fn = encode_fn(err);
+    if (!fn) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], e[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, s, b, e,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (err) *err = "cuTensorMapEncodeTiled failed with code " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+template <int MODE>
+int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string* err) {
+    auto kern = tp_gemm_kernel<MODE>;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) {
+            if (err) *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+            return TP_ERR_CUDA;
+        }
+        configured[dev] = true;
+    }
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        if (err) *err = std::string("GEMM launch: ") + cudaGetErrorString(e);
+        return TP_ERR_CUDA;
+    }
+    return TP_OK;
+}
+
+}  // namespace
+
+namespace tpi {
+
+int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const bool row = (a.mode == GEMM_ROW_FUSED || a.mode == GEMM_ROW_PARTIAL);
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.act = a.act;
+    p.out = a.out;
+    p.ldo = a.ldo;
+    p.out_f32 = a.out_f32;
+    p.bias = reinterpret_cast<const __nv_bfloat16*>(a.bias);
+    p.residual = reinterpret_cast<const __nv_bfloat16*>(a.residual);
+    p.ldr = a.ldr;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.m_tiles = static_cast<int>((a.M + BM - 1) / BM);
+    const int bn_out = (a.mode == GEMM_COL_SWIGLU) ? BN / 2 : BN;
+    p.n_tiles = static_cast<int>((a.N + bn_out - 1) / bn_out);
+    p.grid_shards = (a.mode == GEMM_ROW_PARTIAL) ? a.t : 1;
+    p.shard_stride = a.M * a.ldo;
+    if (row) {
+        p.kb_per_shard = static_cast<int>((a.Ks + BK - 1) / BK);
+        p.k_shards = (a.mode == GEMM_ROW_FUSED) ? a.t : 1;
+        // A: [M][t*Ks] seen as (Ks, t, M); B: [N][t*Ks] seen as (Ks, t, N).
+        const uint64_t dA[3] = {(uint64_t)a.Ks, (uint64_t)a.t, (uint64_t)a.M};
+        const uint64_t sA[2] = {(uint64_t)a.Ks * 2, (uint64_t)a.t * a.Ks * 2};
+        const uint32_t bA[3] = {BK, 1, BM};
+        if (!make_map(&p.mapA, a.A, 3, dA, sA, bA, err)) return TP_ERR_CUDA;
+        const uint64_t dB[3] = {(uint64_t)a.Ks, (uint64_t)a.t, (uint64_t)a.N};
+        const uint32_t bB[3] = {BK, 1, B_CHUNK_ROWS};
+        if (!make_map(&p.mapB[0], a.B0, 3, dB, sA, bB, err)) return TP_ERR_CUDA;
+    } else {
+        p.kb_per_shard = static_cast<int>((a.K + BK - 1) / BK);
+        p.k_shards = 1;
+        const uint64_t dA[2] = {(uint64_t)a.K, (uint64_t)a.M};
+        const uint64_t sA[1] = {(uint64_t)a.K * 2};
+        const uint32_t bA[2] = {BK, BM};
+        if (!make_map(&p.mapA, a.A, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
+        const void* bs[3] = {a.B0, a.B1, a.B2};
+        const int64_t rows[3] = {a.B0_rows, a.B1_rows, a.B2_rows};
+        const uint32_t bB[2] = {BK, B_CHUNK_ROWS};
+        for (int i = 0; i < 3; ++i) {
+            if (!bs[i]) {
+                p.mapB[i] = p.mapB[0];
+                continue;
+            }
+            const uint64_t dB[2] = {(uint64_t)a.K, (uint64_t)rows[i]};
+            if (!make_map(&p.mapB[i], bs[i], 2, dB, sA, bB, err)) return TP_ERR_CUDA;
+        }
+        p.b_rows0 = static_cast<int>(a.B0_rows);
+        p.qkv_ws = static_cast<int>(a.qkv_ws);
+        p.qkv_qw = static_cast<int>(a.qkv_qw);
+        p.qkv_kvw = static_cast<int>(a.qkv_kvw);
+        p.kv_heads = a.kv_heads;
+        p.head_dim = a.head_dim;
+        p.tp = a.t;
+    }
+    p.num_tiles = p.grid_shards * p.m_tiles * p.n_tiles;
+    if (p.num_tiles == 0) return TP_OK;
+    const int grid = std::min(p.num_tiles, device_sm_count());
+    switch (a.mode) {
+        case GEMM_COL_ACT: return launch_mode<GEMM_COL_ACT>(p, grid, stream, err);
+        case GEMM_COL_SWIGLU: return launch_mode<GEMM_COL_SWIGLU>(p, grid, stream, err);
+        case GEMM_COL_QKV: return launch_mode<GEMM_COL_QKV>(p, grid, stream, err);
+        case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED>(p, grid, stream, err);
+        case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL>(p, grid, stream, err);
+        default:
+            if (err) *err = "unknown GEMM mode";
+            return TP_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace tpi

@@ -1,0 +1,88 @@
+// tp_internal.h -- host-side interfaces shared by the translation units of
+// libtp.so (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace tpi {
+
+// Kinds of GEMM the tcgen05 kernel implements.  D[m][n] = sum_k A[m][k] B[n][k].
+enum GemmMode {
+    GEMM_COL_ACT = 0,     // colwise X W^T with a fused activation, bf16 out
+    GEMM_COL_SWIGLU = 1,  // colwise SiLU(X W1^T) * (X W3^T), bf16 out
+    GEMM_COL_QKV = 2,     // colwise Q|K|V per shard, bf16 out
+    GEMM_ROW_FUSED = 3,   // rowwise, shards summed in the accumulator, + bias + residual
+    GEMM_ROW_PARTIAL = 4  // rowwise, one [M][N] partial per shard (fp32 or bf16)
+};
+
+struct GemmArgs {
+    int mode = GEMM_COL_ACT;
+    int act = 0;  // TP_ACT_* for GEMM_COL_ACT
+    int64_t M = 0;
+    int64_t N = 0;   // output columns (SwiGLU: columns of H)
+    // Colwise: A is [M][K] (K = hidden).  Rowwise: A is [M][t * Ks], shard i
+    // = column block i of width Ks; B is [N][t * Ks] likewise.
+    const void* A = nullptr;
+    int64_t K = 0;   // colwise reduction length
+    int t = 1;       // shards
+    int64_t Ks = 0;  // rowwise reduction length per shard
+    const void* B0 = nullptr;
+    const void* B1 = nullptr;
+    const void* B2 = nullptr;
+    int64_t B0_rows = 0, B1_rows = 0, B2_rows = 0;
+    // QKV column segments of one shard: [q_w | kv_w | kv_w], shard width ws;
+    // KV rows of shard i start at kv_first(i) * d.
+    int64_t qkv_ws = 0, qkv_qw = 0, qkv_kvw = 0;
+    int kv_heads = 0, head_dim = 0;
+    // Output.
+    void* out = nullptr;
+    int64_t ldo = 0;
+    int out_f32 = 0;  // GEMM_ROW_PARTIAL: 1 = fp32 partials, 0 = bf16
+    const void* bias = nullptr;
+    const void* residual = nullptr;
+    int64_t ldr = 0;
+    unsigned* status = nullptr;
+    uint64_t timeout_ns = 2000000000ull;
+};
+
+// Encodes the tensor maps and launches the persistent tcgen05 GEMM on
+// `stream`.  Returns 0 or a TP_ERR_* code with a message in *err.
+int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err);
+
+// Number of kernel launches gemm_launch issues (always 1).
+constexpr int kGemmLaunches = 1;
+
+// Elementwise / row kernels (tp_elementwise.cu).
+int reduce_launch(const void* partials, int partial_f32, int t, int64_t n, int h,
+                  const void* bias, const void* residual, void* out, cudaStream_t stream,
+                  std::string* err);
+// Row-wise reduce of the partials plus residual into h1 (bf16), and also
+// xn = RMSNorm(h1) (unit gain) when xn != nullptr.
+int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t rows, int h,
+                       const void* residual, void* h1, void* xn, float eps, cudaStream_t stream,
+                       std::string* err);
+int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaStream_t stream,
+                   std::string* err);
+
+// Attention core (tp_attn.cu).
+struct AttnArgs {
+    const void* QKV = nullptr;
+    int64_t ld_qkv = 0;
+    int64_t shard_w = 0, q_w = 0, kv_w = 0;  // column layout of one shard
+    void* O = nullptr;
+    int64_t ld_o = 0;
+    int batch = 0, seq = 0, heads = 0, kv_heads = 0, head_dim = 0, t = 1;
+};
+int attn_launch(const AttnArgs& a, cudaStream_t stream, std::string* err);
+
+// Self test: a kernel that waits on a barrier nobody arrives at.
+int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,
+                            std::string* err);
+
+// Device properties cached per device.
+int device_sm_count();
+
+}  // namespace tpi

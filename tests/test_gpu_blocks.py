@@ -1,0 +1,194 @@
+"""GPU parity of the whole blocks (sharded MLP, head-sharded attention, the
+layer) against the fp64 oracle, through the C ABI.
+
+Small shapes are compared element by element over the full output; the
+workloads' full sizes (the configuration the bench times: FUSED reduction)
+are compared on sampled token rows that the oracle computes one by one with
+the same definition (rows are independent in the MLP; a causal attention row
+depends only on its sequence's prefix)."""
+import numpy as np
+import pytest
+import torch
+
+import megatron_tensor_transformer_colwise_gb300 as tp
+import oracle
+import synth
+from synth import SHAPES, Shape
+from gpu_util import assert_close, dev, host64, plan_for, sync_ok, workspace
+
+pytestmark = pytest.mark.gpu
+
+MODES = [tp.TP_REDUCE_FUSED, tp.TP_REDUCE_PARTIALS]
+
+
+def run_mlp(s, inp, mode, partial_dtype=tp.TP_F32, bias=None, residual=None):
+    plan = plan_for(s, reduce_mode=mode, partial_dtype=partial_dtype)
+    ws, nws = workspace(plan, tp.TP_OP_MLP)
+    Z = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+    P = None
+    if mode == tp.TP_REDUCE_PARTIALS:
+        dt = torch.float32 if partial_dtype == tp.TP_F32 else torch.bfloat16
+        P = torch.empty(s.tp, s.tokens, s.hidden, dtype=dt, device="cuda")
+    W3 = dev(inp["W3"]) if s.act == "swiglu" else None
+    tp.tp_mlp_forward(plan, dev(inp["X"]), dev(inp["W1"]), W3, dev(inp["W2"]), bias, residual, P,
+                      Z, ws, nws)
+    sync_ok(plan)
+    return host64(Z)
+
+
+# ---------------------------------------------------------------- MLP
+
+def test_worked_example_shapes_through_the_bf16_path():
+    # The page's worked example (b=4, h=16, t=4, seed 0) rounded to bf16 and
+    # run through the GPU path; compared with the oracle on the same values.
+    w = synth.worked_example()
+    s = SHAPES["worked"]
+    inp = {"X": w["X"].to(torch.bfloat16), "W1": w["A"].T.contiguous().to(torch.bfloat16),
+           "W2": w["B"].T.contiguous().to(torch.bfloat16)}
+    for mode in MODES:
+        Z = run_mlp(s, inp, mode)
+        ref = oracle.mlp("gelu", host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]))
+        assert_close(Z, ref, what="worked example")
+        # and the oracle's own sharded form agrees with its unsharded one
+        refs = oracle.mlp_sharded("gelu", 4, host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]))
+        assert np.abs(refs - ref).max() < 1e-12 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "gelu_tanh"])
+@pytest.mark.parametrize("mode", MODES)
+def test_small_mlp_full_output(act, mode):
+    s = Shape("m", 1, 300, 192, ffn=800, tp=4, act=act, index=21)
+    inp = synth.workload_inputs(s)
+    Z = run_mlp(s, inp, mode)
+    w3 = host64(inp["W3"]) if act == "swiglu" else None
+    ref = oracle.mlp_sharded(act, s.tp, host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]), w3)
+    assert_close(Z, ref, what=f"mlp {act}")
+
+
+def test_mlp_bias_and_residual_added_once():
+    s = Shape("m", 1, 130, 64, ffn=256, tp=4, act="gelu", index=22)
+    inp = synth.workload_inputs(s)
+    bias = synth.normal_bf16((s.hidden,), 1.0, 5)
+    res = synth.normal_bf16((s.tokens, s.hidden), 1.0, 6)
+    ref = oracle.mlp("gelu", host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]))
+    ref = ref + host64(bias)[None, :] + host64(res)
+    for mode in MODES:
+        Z = run_mlp(s, inp, mode, bias=dev(bias), residual=dev(res))
+        assert_close(Z, ref, what="mlp + bias + residual")
+
+
+def test_mlp_bf16_partials_mode():
+    s = Shape("m", 1, 257, 256, ffn=1024, tp=8, act="swiglu", index=23)
+    inp = synth.workload_inputs(s)
+    Z = run_mlp(s, inp, tp.TP_REDUCE_PARTIALS, partial_dtype=tp.TP_BF16)
+    ref = oracle.mlp("swiglu", host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]),
+                     host64(inp["W3"]))
+    assert_close(Z, ref, what="mlp bf16 partials")
+
+
+def _sample_rows(M, n, seed):
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(M, size=n, replace=False).tolist())
+    rows |= {0, M - 1}
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["gpt_mlp", "llama_mlp"])
+def test_full_size_mlp_sampled_rows(name):
+    s = SHAPES[name]
+    inp = synth.workload_inputs(s)
+    Z = run_mlp(s, inp, tp.TP_REDUCE_FUSED)
+    rows = _sample_rows(s.tokens, 14, 7)
+    X = host64(inp["X"][rows])
+    w3 = host64(inp["W3"]) if s.act == "swiglu" else None
+    ref = oracle.mlp(s.act, X, host64(inp["W1"]), host64(inp["W2"]), w3)
+    assert_close(Z[rows], ref, what=f"{name} sampled rows")
+    assert np.isfinite(Z).all()
+
+
+# ---------------------------------------------------------------- attention
+
+def run_attn(s, inp, mode, residual=None):
+    plan = plan_for(s, reduce_mode=mode)
+    ws, nws = workspace(plan, tp.TP_OP_ATTN)
+    out = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+    P = torch.empty(s.tp, s.tokens, s.hidden, dtype=torch.float32, device="cuda") \
+        if mode == tp.TP_REDUCE_PARTIALS else None
+    tp.tp_attn_forward(plan, dev(inp["X"]), dev(inp["Wq"]), dev(inp["Wk"]), dev(inp["Wv"]),
+                       dev(inp["Wo"]), residual, P, out, ws, nws)
+    sync_ok(plan)
+    return host64(out)
+
+
+@pytest.mark.parametrize("a,k,t,d", [(8, 2, 4, 64), (8, 8, 4, 128), (8, 1, 8, 128), (4, 4, 2, 64)])
+@pytest.mark.parametrize("mode", MODES)
+def test_small_attention_block_full_output(a, k, t, d, mode):
+    s = Shape("a", 2, 150, 256, heads=a, kv_heads=k, head_dim=d, tp=t, act="none", index=24)
+    inp = synth.workload_inputs(s)
+    out = run_attn(s, inp, mode)
+    ref = oracle.attention_sharded(s.batch, s.seq, a, k, d, t, *(host64(inp[n]) for n in
+                                                                  ("X", "Wq", "Wk", "Wv", "Wo")))
+    assert_close(out, ref, what="attention block")
+
+
+def test_attention_block_residual():
+    s = Shape("a", 1, 96, 128, heads=4, kv_heads=2, head_dim=64, tp=2, act="none", index=25)
+    inp = synth.workload_inputs(s)
+    res = synth.normal_bf16((s.tokens, s.hidden), 1.0, 9)
+    ref = oracle.attention(s.batch, s.seq, 4, 2, 64, *(host64(inp[n]) for n in
+                                                       ("X", "Wq", "Wk", "Wv", "Wo"))) + host64(res)
+    for mode in MODES:
+        assert_close(run_attn(s, inp, mode, residual=dev(res)), ref, what="attention + residual")
+
+
+def test_full_size_attention_sampled_rows():
+    s = SHAPES["attn"]
+    inp = synth.workload_inputs(s)
+    out = run_attn(s, inp, tp.TP_REDUCE_FUSED)
+    rows = [0, 1, 63, 64, 127, 500, 1023, 1500, 2047]
+    ref = oracle.attention_rows(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim,
+                                *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo")), rows)
+    assert_close(out[rows], ref, what="attention sampled rows")
+    assert np.isfinite(out).all()
+
+
+# ---------------------------------------------------------------- layer
+
+def run_layer(s, inp, mode):
+    plan = plan_for(s, reduce_mode=mode)
+    ws, nws = workspace(plan, tp.TP_OP_LAYER)
+    Y = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+    wd = {k: dev(v) for k, v in inp.items() if k != "X"}
+    tp.tp_layer_forward(plan, dev(inp["X"]), wd, Y, ws, nws)
+    sync_ok(plan)
+    return host64(Y)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_small_layer_full_output(mode):
+    s = Shape("l", 2, 140, 256, ffn=768, heads=8, kv_heads=2, head_dim=64, tp=4, act="swiglu",
+              index=26)
+    inp = synth.workload_inputs(s)
+    Y = run_layer(s, inp, mode)
+    ref = oracle.layer(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, s.tp,
+                       *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")),
+                       sharded=True)
+    assert_close(Y, ref, what="layer")
+    # The residual stream dominates y; check the block contributions too.
+    X = host64(inp["X"])
+    assert_close(Y - X, ref - X, tol=5e-2, what="layer minus residual")
+
+
+def test_full_size_layer_sampled_rows():
+    s = SHAPES["layer"]
+    inp = synth.workload_inputs(s)
+    Y = run_layer(s, inp, tp.TP_REDUCE_FUSED)
+    seq = s.seq
+    rows = [0, 5, 300, 2 * seq + 1, 2 * seq + 700, 3 * seq + 1100, seq - 1]
+    ref = oracle.layer_rows(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim,
+                            *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")),
+                            rows)
+    assert_close(Y[rows], ref, what="layer sampled rows")
+    X = host64(inp["X"])[rows]
+    assert_close(Y[rows] - X, ref - X, tol=5e-2, what="layer sampled rows minus residual")
+    assert np.isfinite(Y).all()
