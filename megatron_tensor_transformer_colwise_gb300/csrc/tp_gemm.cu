@@ -113,15 +113,60 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Tensor map and first row of each 64-row B box of an output tile.  Depends
+// only on the tile, so the producer computes it once per tile, not per
+// k-block (the QKV segment arithmetic would otherwise stall the TMA issue).
+template <int MODE>
+__device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, const CUtensorMap* (&map)[4],
+                                        int (&row)[4]) {
+#pragma unroll
+    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c) {
+        map[c] = &p.mapB[0];
+        if (MODE == tpi::GEMM_COL_SWIGLU) {
+            // rows [0,128) of the tile: W1; rows [128,256): W3, both for
+            // output columns nb*128 .. nb*128+127.
+            map[c] = &p.mapB[c >> 1];
+            row[c] = nb * (BN / 2) + (c & 1) * B_CHUNK_ROWS;
+        } else if (MODE == tpi::GEMM_COL_QKV) {
+            const int col = nb * BN + c * B_CHUNK_ROWS;
+            if (col >= p.N) {
+                row[c] = p.b_rows0;  // wholly out of range: zeros
+            } else {
+                const int i = col / p.qkv_ws;
+                const int l = col - i * p.qkv_ws;
+                if (l < p.qkv_qw) {
+                    row[c] = i * p.qkv_qw + l;
+                } else {
+                    const int kv0 = kv_first(p.kv_heads, p.tp, i) * p.head_dim;
+                    const int l2 = l - p.qkv_qw;
+                    if (l2 < p.qkv_kvw) {
+                        map[c] = &p.mapB[1];
+                        row[c] = kv0 + l2;
+                    } else {
+                        map[c] = &p.mapB[2];
+                        row[c] = kv0 + (l2 - p.qkv_kvw);
+                    }
+                }
+            }
+        } else {
+            row[c] = nb * BN + c * B_CHUNK_ROWS;
+        }
+    }
+}
+
 template <int MODE>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                               volatile int* abort_flag) {
+    constexpr bool ROW = (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int s_grid, mb, nb;
         decode_tile(p, tile, s_grid, mb, nb);
+        const CUtensorMap* bmap[4];
+        int brow[4];
+        if (!ROW) b_boxes<MODE>(p, nb, bmap, brow);
         for (int ks = 0; ok && ks < p.k_shards; ++ks) {
             const int shard = (MODE == tpi::GEMM_ROW_PARTIAL) ? s_grid : ks;
             for (int kb = 0; kb < p.kb_per_shard; ++kb) {
@@ -134,7 +179,7 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                 const uint32_t a_dst = base + stage * STAGE_BYTES;
                 const uint32_t b_dst = a_dst + A_BYTES;
                 const int kc = kb * BK;
-                if (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL) {
+                if (ROW) {
                     tma_load_3d(a_dst, &p.mapA, full, kc, shard, mb * BM);
 #pragma unroll
                     for (int c = 0; c < BN / B_CHUNK_ROWS; ++c)
@@ -143,41 +188,8 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                 } else {
                     tma_load_2d(a_dst, &p.mapA, full, kc, mb * BM);
 #pragma unroll
-                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c) {
-                        const CUtensorMap* map = &p.mapB[0];
-                        int row;
-                        if (MODE == tpi::GEMM_COL_SWIGLU) {
-                            // rows [0,128) of the tile: W1; rows [128,256): W3,
-                            // both for output columns nb*128 .. nb*128+127.
-                            const int half = c >> 1;
-                            map = &p.mapB[half];
-                            row = nb * (BN / 2) + (c & 1) * B_CHUNK_ROWS;
-                        } else if (MODE == tpi::GEMM_COL_QKV) {
-                            const int col = nb * BN + c * B_CHUNK_ROWS;
-                            if (col >= p.N) {
-                                row = p.b_rows0;  // wholly out of range: zeros
-                            } else {
-                                const int i = col / p.qkv_ws;
-                                const int l = col - i * p.qkv_ws;
-                                if (l < p.qkv_qw) {
-                                    row = i * p.qkv_qw + l;
-                                } else {
-                                    const int kv0 = kv_first(p.kv_heads, p.tp, i) * p.head_dim;
-                                    const int l2 = l - p.qkv_qw;
-                                    if (l2 < p.qkv_kvw) {
-                                        map = &p.mapB[1];
-                                        row = kv0 + l2;
-                                    } else {
-                                        map = &p.mapB[2];
-                                        row = kv0 + (l2 - p.qkv_kvw);
-                                    }
-                                }
-                            }
-                        } else {
-                            row = nb * BN + c * B_CHUNK_ROWS;
-                        }
-                        tma_load_2d(b_dst + c * B_CHUNK_BYTES, map, full, kc, row);
-                    }
+                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c)
+                        tma_load_2d(b_dst + c * B_CHUNK_BYTES, bmap[c], full, kc, brow[c]);
                 }
                 issued_mask |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
