@@ -218,6 +218,34 @@ TP_API int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, c
                    const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
                    tp_bf16* Z, void* workspace, size_t ws_bytes, void* stream);
 
+/* tp_mlp_forward without a workspace, for callers that cannot allocate
+ * device memory when they call: e.g. a framework whose memory manager owns
+ * all device memory and forbids allocations behind its back, a plugin that
+ * has no allocator handle, or a latency-critical loop where cudaMalloc's
+ * implicit device synchronisation would stall other streams.  The pages have
+ * no counterpart of this call; it computes exactly what tp_mlp_forward does.
+ *
+ * Scratch (the colwise output [M][f] bf16 and, in PARTIALS mode, the
+ * [t][M][h] partials) lives in one file-scope device array of
+ * TP_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
+ * holds until process exit.  A plan whose scratch needs more returns
+ * TP_ERR_WORKSPACE before any launch.  The call itself allocates nothing
+ * (no cudaMalloc / cudaFree / allocating library routine); the plan is
+ * created beforehand, at set-up time, by tp_plan_create.
+ *
+ * The first call on a device resolves the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: calls that overlap on the GPU (different streams, or different
+ * threads without ordering) race with each other.  Calls on one stream are
+ * ordered and safe.  Every scratch byte read is first written by the same
+ * call, so nothing needs clearing between calls.
+ * Arguments as tp_mlp_forward, minus partials / workspace. */
+#define TP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+TP_API int tp_mlp_forward_noalloc(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1,
+                                  const tp_bf16* W3, const tp_bf16* W2, const tp_bf16* b2,
+                                  const tp_bf16* residual, tp_bf16* Z, void* stream);
+
 /* ------------------------------------------------------------ attention */
 
 /* Colwise Q/K/V projection, all shards in one launch ([wiki] "셀프 어텐션":

@@ -28,7 +28,7 @@ __all__ = [
     "tp_plan_create", "tp_plan_destroy", "tp_config_check", "tp_config_shard_table",
     "tp_plan_workspace_bytes", "tp_plan_shard_table", "tp_get_device_status", "tp_last_error",
     "tp_reduce_partials", "tp_rmsnorm", "tp_colwise_forward", "tp_rowwise_forward",
-    "tp_mlp_forward", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
+    "tp_mlp_forward", "tp_mlp_forward_noalloc", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
     "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout", "EXPORTED",
 ]
 
@@ -90,6 +90,7 @@ _SIGS = {
     "tp_colwise_forward": [_VP, _VP, _VP, _VP, _VP, _VP],
     "tp_rowwise_forward": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
     "tp_mlp_forward": [_VP] * 10 + [C.c_size_t, _VP],
+    "tp_mlp_forward_noalloc": [_VP] * 9,
     "tp_qkv_forward": [_VP] * 7,
     "tp_attn_core_forward": [_VP] * 4,
     "tp_attn_forward": [_VP] * 10 + [C.c_size_t, _VP],
@@ -257,6 +258,13 @@ def tp_mlp_forward(plan: Plan, X, W1, W3, W2, b2, residual, partials, Z, workspa
                    ws_bytes: int, stream=None) -> None:
     _call("tp_mlp_forward", plan.handle, _p(X), _p(W1), _p(W3), _p(W2), _p(b2), _p(residual),
           _p(partials), _p(Z), _p(workspace), ws_bytes, _s(stream))
+
+
+def tp_mlp_forward_noalloc(plan: Plan, X, W1, W3, W2, b2, residual, Z, stream=None) -> None:
+    """tp_mlp_forward with its scratch in the library's built-in device array
+    (no workspace argument; nothing is allocated by the call)."""
+    _call("tp_mlp_forward_noalloc", plan.handle, _p(X), _p(W1), _p(W3), _p(W2), _p(b2),
+          _p(residual), _p(Z), _s(stream))
 
 
 def tp_qkv_forward(plan: Plan, X, Wq, Wk, Wv, QKV, stream=None) -> None:

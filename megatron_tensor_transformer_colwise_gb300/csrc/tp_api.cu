@@ -15,6 +15,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -669,3 +670,73 @@ int tp_selftest_wait_timeout(tp_plan_t plan, uint64_t timeout_ns, void* stream) 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free MLP: scratch in a file-scope device array.
+//
+// For callers that cannot allocate device memory at call time.  The array
+// is sized once (TP_NOALLOC_SCRATCH_BYTES) and lives for the whole process on
+// every GPU that loads this library.  Host code must not pass the array's
+// name to a kernel -- on the host it is only a stand-in symbol -- so its
+// device address is looked up with cudaGetSymbolAddress, once per device,
+// with that device current, and the looked-up pointer is what the kernels
+// receive.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of the scratch array on the current device (first call on
+// a device resolves and caches it).
+int noalloc_scratch(int dev, void** out) {
+    if (dev < 0 || dev >= 64) return fail(TP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr)
+            return fail(TP_ERR_CUDA, "cudaGetSymbolAddress(scratch) failed: %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return TP_OK;
+}
+
+}  // namespace
+
+extern "C" int tp_mlp_forward_noalloc(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1,
+                                      const tp_bf16* W3, const tp_bf16* W2, const tp_bf16* b2,
+                                      const tp_bf16* residual, tp_bf16* Z, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(W1, "W1")) ||
+        (rc = need_ptr(W2, "W2")) || (rc = need_ptr(Z, "Z")) || (rc = opt_ptr(b2, "b2")) ||
+        (rc = opt_ptr(residual, "residual")))
+        return rc;
+    if (plan->cfg.act == TP_ACT_SWIGLU) {
+        if ((rc = need_ptr(W3, "W3 (SwiGLU)"))) return rc;
+    } else if (W3) {
+        return fail(TP_ERR_INVALID_ARG, "W3 must be NULL unless act is TP_ACT_SWIGLU");
+    }
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    const size_t y_bytes = align_up(static_cast<size_t>(plan->M) * plan->f * 2);
+    const size_t p_bytes =
+        fused ? 0 : align_up(static_cast<size_t>(plan->t) * plan->M * plan->h * partial_elem_bytes(plan));
+    if (y_bytes + p_bytes > TP_NOALLOC_SCRATCH_BYTES)
+        return fail(TP_ERR_WORKSPACE,
+                    "this MLP needs %zu bytes of scratch; the built-in scratch array of "
+                    "tp_mlp_forward_noalloc holds %zu bytes (use tp_mlp_forward with a workspace)",
+                    y_bytes + p_bytes, (size_t)TP_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(plan->device, &scratch))) return rc;
+    void* Y = scratch;
+    void* P = fused ? nullptr : static_cast<uint8_t*>(scratch) + y_bytes;
+    cudaStream_t s = as_stream(stream);
+    if ((rc = do_colwise(plan, X, W1, W3, Y, s))) return rc;
+    if ((rc = do_rowwise(plan, Y, plan->fw, W2, plan->h, b2, residual, P, Z, fused, s))) return rc;
+    if (!fused) return do_reduce(plan, P, b2, residual, Z, plan->h, s);
+    return TP_OK;
+}
