@@ -340,6 +340,184 @@ def run_case(args):
     return 0
 
 
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    import megatron_tensor_transformer_colwise_gb300 as tp
+
+    peaks, peak_src = load_peaks()
+    s = SHAPES["layer"]
+    inp = synth.workload_inputs(s)
+    d = {k: v.to(device) for k, v in inp.items()}
+    plan = tp.Plan(tp.make_config(tokens=s.tokens, hidden=s.hidden, ffn=s.ffn, n_heads=s.heads,
+                                  n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp,
+                                  act=s.act, batch=s.batch, seq=s.seq,
+                                  reduce_mode=tp.TP_REDUCE_FUSED))
+    nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_LAYER)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    Y = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device=device)
+    wdict = {k: v for k, v in d.items() if k != "X"}
+    weights = tp.layer_weights(wdict)
+    stream = torch.cuda.current_stream()
+    kf = layer_kernel_flops(s)
+    nk = len(kf)
+
+    def mk_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # materialise the cudaEvent_t
+        return evs
+
+    warm_events = mk_events(nk + 1)
+    for _ in range(args.warmup):
+        tp.tp_layer_forward_traced(plan, d["X"], weights, Y, ws, nws,
+                                   [e.cuda_event for e in warm_events], stream)
+    torch.cuda.synchronize()
+    assert tp.tp_get_device_status(plan) == tp.TP_OK, tp.tp_last_error()
+
+    step_events = [mk_events(nk + 1) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_for(torch, device.index))
+    sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
+    start.record(stream)
+    for k in range(args.steps):
+        tp.tp_layer_forward_traced(plan, d["X"], weights, Y, ws, nws,
+                                   [e.cuda_event for e in step_events[k]], stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = sampler.stop()
+    assert tp.tp_get_device_status(plan) == tp.TP_OK, tp.tp_last_error()
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, world, device)
+    flops = layer_flops(s)
+    value = whole_job_value(flops, world, ms / 1e3)
+
+    # Per-kernel durations inside the timed region (same stream, live).
+    per_kernel = [0.0] * nk
+    for evs in step_events:
+        for i in range(nk):
+            per_kernel[i] += evs[i].elapsed_time(evs[i + 1])
+    per_kernel = [v / args.steps for v in per_kernel]
+    total_k = sum(per_kernel)
+    kbytes = layer_kernel_bytes(s)
+    kernels = []
+    for (name, fl), msk in zip(kf, per_kernel):
+        row = {"name": name, "us": msk * 1e3, "share": msk / total_k if total_k else None}
+        if fl > 0:
+            row["tflops"] = fl / (msk / 1e3) / 1e12
+            row["frac_bf16_sustained"] = row["tflops"] / peaks["bf16_tflops_sustained"]
+        else:
+            row["gbs"] = kbytes[name] / (msk / 1e3) / 1e9
+            row["frac_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+        kernels.append(row)
+    dom = max(range(nk), key=lambda i: per_kernel[i])
+    dom_name, dom_fl = kf[dom]
+    achieved = dom_fl / (per_kernel[dom] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
+                "algorithmic_flops_per_launch": dom_fl,
+                "traffic": args.dominant_traffic}
+
+    # The g reduction as a PARTIALS-mode kernel over the layer's partials.
+    n = s.tokens * s.hidden
+    P = torch.randn(s.tp, s.tokens, s.hidden, dtype=torch.float32, device=device)
+    res = torch.randn(s.tokens, s.hidden, device=device).to(torch.bfloat16)
+    Zr = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device=device)
+    for _ in range(5):
+        tp.tp_reduce_partials(P, tp.TP_F32, s.tp, n, s.hidden, None, res, Zr, stream)
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 30
+    r0.record(stream)
+    for _ in range(reps):
+        tp.tp_reduce_partials(P, tp.TP_F32, s.tp, n, s.hidden, None, res, Zr, stream)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    red_us = r0.elapsed_time(r1) / reps * 1e3
+    rb = reduce_bytes(s.tp, n, 4, residual=True)
+    red_gbs = rb / (red_us / 1e6) / 1e9
+    reduce_line = {"bound": "hbm", "kernel": "tp_reduce_partials (t=8 fp32 partials + residual)",
+                   "achieved": red_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": red_gbs / peaks["hbm_gbs"], "frac_of_8tbs": red_gbs / 8000.0,
+                   "us": red_us, "bytes_per_launch": rb,
+                   "peak_source": f"{peak_src} hbm_gbs (kernel timed alone)",
+                   "l2": "inputs 1.07 GB > 129 MB L2"}
+    del P
+
+    # End to end through the C ABI with host buffers (pinned): X in, Y out.
+    Xh = inp["X"].pin_memory()
+    Yh = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(d["X"])
+    e2e_steps = max(5, min(args.steps, 50))
+    for _ in range(3):
+        Xd.copy_(Xh, non_blocking=True)
+        tp.tp_layer_forward(plan, Xd, wdict, Y, ws, nws, stream)
+        Yh.copy_(Y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        Xd.copy_(Xh, non_blocking=True)
+        tp.tp_layer_forward(plan, Xd, wdict, Y, ws, nws, stream)
+        Yh.copy_(Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    e2e = {"value": whole_job_value(flops, world, e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Yh.numel() * 2,
+           "ms_per_step": e2e_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, bf16-rounded)",
+        "config": {"workload": "tp_layer_forward: 8192 tokens (4 x 2048), h=4096, 32 q / 8 kv "
+                               "heads d=128, SwiGLU ffn=14336, t=8, FUSED g, bf16",
+                   "tokens": s.tokens, "tp_degree": s.tp,
+                   "parallelism": f"single-GPU t={s.tp} shards" + (f", {world} replicas" if world > 1 else ""),
+                   "gflop_per_step": flops / 1e9,
+                   "l2": "inputs larger than L2 (436 MB of weights per step)"},
+        "roofline": roofline,
+        "reduce": reduce_line,
+        "kernels": kernels,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": nk * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(s, inp, args.cpu_tokens)
+        del line["cpu_baseline"]["seconds"]
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)

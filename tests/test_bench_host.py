@@ -22,6 +22,11 @@ def test_layer_flop_model_matches_the_workload_arithmetic():
     assert bench.layer_flops(s) == pytest.approx(3710.9e9, rel=1e-3)
 
 
+def test_bench_entry_points_exist():
+    for name in ("run_ours", "run_reference", "run_case", "main", "oracle_sample"):
+        assert callable(getattr(bench, name)), name
+
+
 def test_reduce_byte_model():
     # t partials in fp32 read once, residual read once, output written once.
     assert bench.reduce_bytes(8, 8192 * 4096, 4, True) == 8 * 8192 * 4096 * 4 + 2 * 8192 * 4096 * 2
