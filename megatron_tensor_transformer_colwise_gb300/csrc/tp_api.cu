@@ -243,6 +243,8 @@ int do_attn_core(const tp_plan_s* p, const void* QKV, void* O, cudaStream_t s) {
     a.kv_heads = static_cast<int>(p->k);
     a.head_dim = static_cast<int>(p->d);
     a.t = static_cast<int>(p->t);
+    a.status = p->status;
+    a.timeout_ns = p->timeout_ns;
     std::string err;
     return run(tpi::attn_launch(a, s, &err), err);
 }

@@ -1,4 +1,5 @@
-// tp_attn.cu -- causal GQA attention of every shard's heads.
+// tp_attn.cu -- causal GQA attention of every shard's heads on sm_103a
+// tensor cores (tcgen05 / TMEM), fed by TMA.
 //
 // Source: "텐서 병렬화" (itwiki, Tensor parallelism), section "셀프 어텐션"
 // (self-attention): heads are independent, so with Q/K/V split by columns
@@ -8,18 +9,28 @@
 //
 // Reading of what the page leaves open: scale 1/sqrt(d), causal mask
 // (key position <= query position) within each sequence, fp32 softmax with
-// the running row maximum subtracted, no dropout, no rotary embedding.
+// a running maximum subtracted, no dropout, no rotary embedding.
 //
-// Kernel: one CTA of 4 warps per (64 query rows, query head, sequence);
-// each warp owns 16 query rows.  K/V tiles of 64 keys stream through a
-// double-buffered, XOR-swizzled shared-memory ring (cp.async); S = Q K^T and
-// O += P V run on bf16 mma.sync tensor-core instructions with fp32
-// accumulators; the softmax is the online (running max / running sum) form,
-// so the 64 x seq score matrix never exists.  Key blocks above the diagonal
-// are skipped; the diagonal block is masked element-wise.
+// One CTA per (128 query rows, query head, sequence), 6 warps:
+//   warp 0      TMA: Q once, then K and V blocks of 128 keys (2-stage rings)
+//               from the shard-blocked QKV buffer (one 2-D tensor map).
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 128, fp32, two
+//               TMEM buffers so S of block j+1 is computed while the softmax
+//               works on block j), then O += P V (V used as an MN-major
+//               operand straight from its [key][d] layout).
+//   warps 2..5  one query row per thread (TMEM lane = row): read the S row,
+//               apply the causal mask, online softmax with exp2, write P
+//               (bf16) to 128-byte-swizzled shared memory for the PV MMA,
+//               rescale the O row in TMEM when its reference maximum moves,
+//               and finally write O / l as bf16.
+// The reference maximum of a row only moves when the block maximum exceeds
+// it by more than 2^8 (in the exp2 domain), so most blocks need no O
+// rescale; P then stays below 256, well inside bf16 and fp32 range.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <string>
 
 #include "tp_device.cuh"
@@ -29,245 +40,375 @@ namespace {
 
 using namespace tpk;
 
-constexpr int ABM = 64;  // query rows per CTA
-constexpr int ABN = 64;  // keys per tile
-constexpr int ATHREADS = 128;
+constexpr int QB = 128;  // query rows per CTA (UMMA M, TMEM lanes)
+constexpr int KB = 128;  // keys per block (UMMA N of S, UMMA K of PV)
+constexpr int NTHREADS = 192;
+constexpr int BOX_BYTES = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (16 KB)
+constexpr int P_BYTES = QB * KB * 2;     // 32 KB
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 of the allowed growth of P
 
-struct AttnParams {
-    const __nv_bfloat16* qkv;
-    long long ld_qkv;
-    int shard_w, q_w, kv_w;
-    __nv_bfloat16* o;
-    long long ld_o;
-    int seq, heads, kv_heads, t, heads_per_shard;
-    float scale_log2;  // log2(e) / sqrt(d)
+enum {
+    B_Q_FULL = 0,
+    B_K_FULL = 1,   // x2
+    B_K_EMPTY = 3,  // x2
+    B_V_FULL = 5,   // x2
+    B_V_EMPTY = 7,  // x2
+    B_S_FULL = 9,   // x2
+    B_S_EMPTY = 11, // x2
+    B_P_FULL = 13,
+    B_P_EMPTY = 14,
+    B_O_FULL = 15,
+    B_DRAIN = 16,
+    NUM_BARS = 17
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Byte offset of 16-byte chunk c of row r in a [64][D] bf16 tile whose
-// chunks are XOR-swizzled by the row's low 3 bits (conflict-free ldmatrix).
 template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return static_cast<uint32_t>(r * (D * 2) + ((c ^ (r & 7)) << 4));
-}
+struct Layout {
+    static constexpr int TILE = QB * D * 2;  // Q, K or V tile bytes
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = TILE;
+    static constexpr int V_OFF = 3 * TILE;
+    static constexpr int P_OFF = 5 * TILE;
+    static constexpr int BAR_OFF = P_OFF + P_BYTES;
+    static constexpr int SMEM = 1024 + BAR_OFF + 8 * NUM_BARS + 16;
+};
 
-// Copy rows [row0, row0+64) x D columns of a strided bf16 matrix into a
-// swizzled tile; rows at or beyond `rows_valid` are zero-filled.
-template <int D>
-__device__ __forceinline__ void load_tile(uint32_t tile, const __nv_bfloat16* g, long long ld,
-                                          int rows_valid) {
-    constexpr int CPR = D / 8;
-#pragma unroll
-    for (int idx = threadIdx.x; idx < ABM * CPR; idx += ATHREADS) {
-        const int r = idx / CPR, c = idx - (idx / CPR) * CPR;
-        const bool ok = r < rows_valid;
-        const __nv_bfloat16* src = ok ? g + static_cast<long long>(r) * ld + c * 8 : g;
-        cp_async16(tile + swz<D>(r, c), src, ok ? 16 : 0);
+struct AttnParams {
+    CUtensorMap map;  // the QKV buffer: dims {t * W, tokens}, box {64, 128}
+    __nv_bfloat16* o;
+    long long ld_o;
+    int seq, heads, kv_heads, t, heads_per_shard, shard_w, q_w, kv_w;
+    float scale_log2;  // log2(e) / sqrt(d)
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 200000000ull) break;  // 200 ms
     }
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(ATHREADS) attn_kernel(const AttnParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int TILE = ABM * D * 2;
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sK = sQ + TILE;          // 2 buffers
-    const uint32_t sV = sQ + 3 * TILE;      // 2 buffers
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + L::Q_OFF, sK = base + L::K_OFF, sV = base + L::V_OFF,
+                   sP = base + L::P_OFF;
+    const uint32_t bar0 = base + L::BAR_OFF;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::BAR_OFF + 8 * NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nqb = (p.seq + ABM - 1) / ABM;
-    const int qb = nqb - 1 - static_cast<int>(blockIdx.x);  // heavy blocks first
-    const int j = blockIdx.y;                                // global query head
-    const int b = blockIdx.z;                                // sequence
+    const int nqb = (p.seq + QB - 1) / QB;
+    const int qb = nqb - 1 - static_cast<int>(blockIdx.x);  // longest rows first
+    const int j = blockIdx.y;
+    const int b = blockIdx.z;
     const int shard = j / p.heads_per_shard;
     const int jl = j - shard * p.heads_per_shard;
-    const int g = j / (p.heads / p.kv_heads);                // KV head read by j
+    const int g = j / (p.heads / p.kv_heads);
     const int kv0 = (p.kv_heads >= p.t) ? shard * (p.kv_heads / p.t) : (shard * p.kv_heads) / p.t;
-    const int gl = g - kv0;                                  // its slot in the shard
-
-    const long long tok0 = static_cast<long long>(b) * p.seq;
-    const __nv_bfloat16* Qg = p.qkv + (tok0 + qb * ABM) * p.ld_qkv + shard * p.shard_w + jl * D;
-    const __nv_bfloat16* Kg = p.qkv + tok0 * p.ld_qkv + shard * p.shard_w + p.q_w + gl * D;
-    const __nv_bfloat16* Vg = Kg + p.kv_w;
-
-    const int q_rows = min(ABM, p.seq - qb * ABM);
-    load_tile<D>(sQ, Qg, p.ld_qkv, q_rows);
+    const int gl = g - kv0;
+    const int qcol = shard * p.shard_w + jl * D;
+    const int kcol = shard * p.shard_w + p.q_w + gl * D;
+    const int vcol = kcol + p.kv_w;
+    const int tok0 = b * p.seq;
     const int nkb = qb + 1;  // causal: key blocks 0..qb
-    load_tile<D>(sK, Kg, p.ld_qkv, min(ABN, p.seq));
-    load_tile<D>(sV, Vg, p.ld_qkv, min(ABN, p.seq));
-    cp_async_commit();
 
-    float o[D / 8][4];
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q_FULL), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_K_FULL + s), 1);
+            mbar_init(bar(B_K_EMPTY + s), 1);
+            mbar_init(bar(B_V_FULL + s), 1);
+            mbar_init(bar(B_V_EMPTY + s), 1);
+            mbar_init(bar(B_S_FULL + s), 1);
+            mbar_init(bar(B_S_EMPTY + s), 4);
+        }
+        mbar_init(bar(B_P_FULL), 4);
+        mbar_init(bar(B_P_EMPTY), 1);
+        mbar_init(bar(B_O_FULL), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.map);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t issued = 0;  // bit per stage and operand: fills not yet known landed
+            uint32_t kpar = 0, vpar = 0;
+            mbar_arrive_expect_tx(bar(B_Q_FULL), L::TILE);
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-    uint32_t qf[D / 16][4];
-
-    const int qrow0 = qb * ABM + warp * 16 + (lane >> 2);  // rows qrow0 and qrow0 + 8
-
-    for (int kb = 0; kb < nkb; ++kb) {
-        cp_async_wait_all();
-        __syncthreads();
-        if (kb == 0) {
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_2d(sQ + c * BOX_BYTES, &p.map, bar(B_Q_FULL), qcol + 64 * c, tok0 + qb * QB);
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int st = kb & 1;
+                const uint32_t ph = (kb >> 1) & 1;
+                const int krow = tok0 + kb * KB;
+                if (!mbar_wait(bar(B_K_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_K_FULL + st), L::TILE);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int c = ks * 2 + (lane >> 4);
-                ldsm_x4(sQ + swz<D>(r, c), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(sK + st * L::TILE + c * BOX_BYTES, &p.map, bar(B_K_FULL + st),
+                                kcol + 64 * c, krow);
+                issued |= 1u << st;
+                kpar = (kpar & ~(1u << st)) | (ph << st);
+                if (!mbar_wait(bar(B_V_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_V_FULL + st), L::TILE);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(sV + st * L::TILE + c * BOX_BYTES, &p.map, bar(B_V_FULL + st),
+                                vcol + 64 * c, krow);
+                issued |= 4u << st;
+                vpar = (vpar & ~(1u << st)) | (ph << st);
             }
-        }
-        if (kb + 1 < nkb) {
-            const int nb = (kb + 1) & 1;
-            const int rows = min(ABN, p.seq - (kb + 1) * ABN);
-            load_tile<D>(sK + nb * TILE, Kg + static_cast<long long>((kb + 1) * ABN) * p.ld_qkv,
-                         p.ld_qkv, rows);
-            load_tile<D>(sV + nb * TILE, Vg + static_cast<long long>((kb + 1) * ABN) * p.ld_qkv,
-                         p.ld_qkv, rows);
-            cp_async_commit();
-        }
-        const uint32_t kt = sK + (kb & 1) * TILE, vt = sV + (kb & 1) * TILE;
-
-        // S = Q K^T for this warp's 16 rows x 64 keys.
-        float s[ABN / 8][4];
-#pragma unroll
-        for (int i = 0; i < ABN / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-            for (int np = 0; np < ABN / 16; ++np) {
-                const int r = np * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int c = ks * 2 + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kt + swz<D>(r, c), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-                mma_bf16_16816(s[2 * np + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-            }
-        }
-        // Causal / length mask (only the diagonal and the ragged last block).
-        const int key0 = kb * ABN;
-        if (kb == qb || key0 + ABN > p.seq) {
-#pragma unroll
-            for (int nt = 0; nt < ABN / 8; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                    const int qpos = qrow0 + (e >> 1) * 8;
-                    if (key > qpos || key >= p.seq) s[nt][e] = -INFINITY;
+            if (!ok) {
+                drain_wait(bar(B_Q_FULL), 0);
+                for (int s = 0; s < 2; ++s) {
+                    if (issued & (1u << s)) drain_wait(bar(B_K_FULL + s), (kpar >> s) & 1u);
+                    if (issued & (4u << s)) drain_wait(bar(B_V_FULL + s), (vpar >> s) & 1u);
                 }
             }
         }
-        // Online softmax.
-        float mx[2] = {m_run[0], m_run[1]};
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(QB, KB);
+            constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(QB, D);
+            bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, p.status, p.timeout_ns);
+            auto issue_s = [&](int kb) -> bool {
+                const int st = kb & 1;
+                const uint32_t use = static_cast<uint32_t>(kb >> 1);
+                if (!mbar_wait(bar(B_S_EMPTY + st), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
+                    return false;
+                if (!mbar_wait(bar(B_K_FULL + st), use & 1u, abort_flag, p.status, p.timeout_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + st * KB;
 #pragma unroll
-        for (int nt = 0; nt < ABN / 8; ++nt) {
-            mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
-            mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * BOX_BYTES + (ks & 3) * 32;
+                    umma_bf16(d_tmem, sdesc_sw128(sQ + off), sdesc_sw128(sK + st * L::TILE + off),
+                              idesc_s, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(B_K_EMPTY + st));
+                umma_commit(bar(B_S_FULL + st));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                if (kb + 1 < nkb && !(ok = issue_s(kb + 1))) break;
+                const int st = kb & 1;
+                if (!mbar_wait(bar(B_P_FULL), kb & 1, abort_flag, p.status, p.timeout_ns) ||
+                    !mbar_wait(bar(B_V_FULL + st), (kb >> 1) & 1, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < KB / 16; ++ks) {
+                    const uint32_t a_off = (ks >> 2) * (P_BYTES / 2) + (ks & 3) * 32;
+                    umma_bf16(tmem + 2 * KB, sdesc_sw128(sP + a_off),
+                              sdesc_sw128_mn(sV + st * L::TILE + ks * 16 * 128, BOX_BYTES, 1024),
+                              idesc_o, (kb > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(bar(B_V_EMPTY + st));
+                umma_commit(bar(B_P_EMPTY));
+            }
+            if (ok) {
+                umma_commit(bar(B_O_FULL));
+            } else {
+                umma_commit(bar(B_DRAIN));
+                drain_wait(bar(B_DRAIN), 0);
+            }
         }
+    } else {
+        // ---------------------------------------------------------- softmax / epilogue
+        const int q = warp & 3;  // TMEM lane quadrant
+        const int r = q * 32 + lane;
+        const int qpos = qb * QB + r;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        float m_ref = -INFINITY, l_sum = 0.0f;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb & 1;
+            const bool got = mbar_wait(bar(B_S_FULL + st), (kb >> 1) & 1, abort_flag, p.status,
+                                       p.timeout_ns);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[KB];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            for (int c = 0; c < KB / 32; ++c)
+                tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + st));
+
+            const int k0 = kb * KB;
+            if (kb == qb || k0 + KB > p.seq) {
+#pragma unroll
+                for (int c = 0; c < KB; ++c) {
+                    const int key = k0 + c;
+                    if (key > qpos || key >= p.seq) s[c] = __float_as_uint(-INFINITY);
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < KB; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            const float mxs = mx * p.scale_log2;
+            float alpha = 1.0f;
+            bool rescale = false;
+            if (mxs > m_ref + RESCALE_THRESHOLD) {
+                alpha = exp2f(m_ref - mxs);  // 0 on the first block
+                m_ref = mxs;
+                rescale = kb > 0;
+            }
+            float sum = 0.0f;
+            uint32_t pk[KB / 2];
+#pragma unroll
+            for (int c = 0; c < KB / 2; ++c) {
+                const float p0 = exp2f(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
+                const float p1 = exp2f(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
+                sum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l_sum = l_sum * alpha + sum;
+
+            // PV of the previous block must be done: O is stable, P is free.
+            const bool got2 = mbar_wait(bar(B_P_EMPTY), (kb & 1) ^ 1, abort_flag, p.status, p.timeout_ns);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got2)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    const uint32_t ta = tmem + lane_off + 2 * KB + c * 32;
+                    tmem_ld32(ta, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(ta, o);
+                }
+                tmem_st_wait();
+            }
+            // P row r: keys 0..63 in the first 16 KB region, 64..127 in the
+            // second; 16-byte chunk c of the row sits at chunk c ^ (r % 8).
+#pragma unroll
+            for (int c8 = 0; c8 < KB / 8; ++c8) {
+                const uint32_t region = static_cast<uint32_t>(c8 >> 3) * (P_BYTES / 2);
+                const uint32_t chunk = static_cast<uint32_t>((c8 & 7) ^ (r & 7));
+                st_shared_v4(sP + region + r * 128 + (chunk << 4), pk[4 * c8], pk[4 * c8 + 1],
+                             pk[4 * c8 + 2], pk[4 * c8 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_P_FULL));
         }
-        float alpha[2], msc[2], rs[2] = {0.0f, 0.0f};
+        if (ok) {
+            const bool got = mbar_wait(bar(B_O_FULL), 0, abort_flag, p.status, p.timeout_ns);
+            __syncwarp();
+            if (__all_sync(0xffffffffu, got)) {
+                tc_fence_after();
+                const float inv = 1.0f / l_sum;
+                __nv_bfloat16* orow = p.o + static_cast<long long>(tok0 + qpos) * p.ld_o +
+                                      static_cast<long long>(j) * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + 2 * KB + c * 32, o);
+                    tmem_ld_wait();
+                    if (qpos < p.seq) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float mref = (mx[h] == -INFINITY) ? 0.0f : mx[h];
-            alpha[h] = exp2f((m_run[h] - mref) * p.scale_log2);
-            msc[h] = mref * p.scale_log2;
-            m_run[h] = mx[h];
-        }
-        uint32_t pf[ABN / 16][4];
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            uint32_t w[4];
 #pragma unroll
-        for (int nt = 0; nt < ABN / 8; ++nt) {
-            const float p0 = exp2f(fmaf(s[nt][0], p.scale_log2, -msc[0]));
-            const float p1 = exp2f(fmaf(s[nt][1], p.scale_log2, -msc[0]));
-            const float p2 = exp2f(fmaf(s[nt][2], p.scale_log2, -msc[1]));
-            const float p3 = exp2f(fmaf(s[nt][3], p.scale_log2, -msc[1]));
-            rs[0] += p0 + p1;
-            rs[1] += p2 + p3;
-            pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-            pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[0];
-            o[i][2] *= alpha[1];
-            o[i][3] *= alpha[1];
-        }
-        // O += P V.  A fragment of P for keys 16ks..16ks+15 comes straight
-        // from the S accumulators of n-tiles 2ks, 2ks+1.
-#pragma unroll
-        for (int ks = 0; ks < ABN / 16; ++ks) {
-            const uint32_t a0 = pf[ks][0], a1 = pf[ks][1], a2 = pf[ks][2], a3 = pf[ks][3];
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int c = dp * 2 + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vt + swz<D>(r, c), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * inv,
+                                                   __uint_as_float(o[g8 * 8 + 2 * e + 1]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c * 32 + g8 * 8) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
             }
         }
     }
-    // Row sums live spread over the 4 lanes of a quad.
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-    }
-    const float inv0 = 1.0f / l_run[0], inv1 = 1.0f / l_run[1];
-    __nv_bfloat16* Og = p.o + (tok0 + qrow0) * p.ld_o + static_cast<long long>(j) * D;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const int col = i * 8 + (lane & 3) * 2;
-        if (qrow0 < p.seq)
-            *reinterpret_cast<uint32_t*>(Og + col) = pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0);
-        if (qrow0 + 8 < p.seq)
-            *reinterpret_cast<uint32_t*>(Og + 8 * p.ld_o + col) =
-                pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1);
-    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 template <int D>
 int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     AttnParams p;
-    p.qkv = reinterpret_cast<const __nv_bfloat16*>(a.QKV);
-    p.ld_qkv = a.ld_qkv;
-    p.shard_w = static_cast<int>(a.shard_w);
-    p.q_w = static_cast<int>(a.q_w);
-    p.kv_w = static_cast<int>(a.kv_w);
+    memset(&p, 0, sizeof(p));
+    void* fn_ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn_ptr, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !fn_ptr) {
+        if (err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+        return TP_ERR_CUDA;
+    }
+    EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(fn_ptr);
+    const long long tokens = static_cast<long long>(a.batch) * a.seq;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.ld_qkv), static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.ld_qkv) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&p.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.QKV), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (err) *err = "cuTensorMapEncodeTiled (attention QKV) failed: " + std::to_string((int)r);
+        return TP_ERR_CUDA;
+    }
     p.o = reinterpret_cast<__nv_bfloat16*>(a.O);
     p.ld_o = a.ld_o;
     p.seq = a.seq;
@@ -275,21 +416,26 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     p.kv_heads = a.kv_heads;
     p.t = a.t;
     p.heads_per_shard = a.heads / a.t;
+    p.shard_w = static_cast<int>(a.shard_w);
+    p.q_w = static_cast<int>(a.q_w);
+    p.kv_w = static_cast<int>(a.kv_w);
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-    const int smem = 5 * ABM * D * 2;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    const int smem = Layout<D>::SMEM;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             if (err) *err = std::string("cudaFuncSetAttribute(attn): ") + cudaGetErrorString(e);
             return TP_ERR_CUDA;
         }
         configured[dev] = true;
     }
-    dim3 grid((a.seq + ABM - 1) / ABM, a.heads, a.batch);
-    attn_kernel<D><<<grid, ATHREADS, smem, stream>>>(p);
+    dim3 grid((a.seq + QB - 1) / QB, a.heads, a.batch);
+    attn_tc_kernel<D><<<grid, NTHREADS, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (err) *err = std::string("attention launch: ") + cudaGetErrorString(e);

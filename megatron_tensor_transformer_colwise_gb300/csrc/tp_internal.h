@@ -75,6 +75,8 @@ struct AttnArgs {
     void* O = nullptr;
     int64_t ld_o = 0;
     int batch = 0, seq = 0, heads = 0, kv_heads = 0, head_dim = 0, t = 1;
+    unsigned* status = nullptr;
+    uint64_t timeout_ns = 2000000000ull;
 };
 int attn_launch(const AttnArgs& a, cudaStream_t stream, std::string* err);
 
