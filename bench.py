@@ -174,6 +174,25 @@ def gpu_id_for(torch, dev_index: int) -> str:
     return str(dev_index)
 
 
+def profiled_traffic(kernel_name: str):
+    """DRAM bytes per launch of `kernel_name` from the committed ncu summary
+    (profiles/dram_traffic.json), or None when the GEMM kernel sources have
+    changed since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as fh:
+            entry = json.load(fh)[kernel_name]
+        h = hashlib.sha256()
+        for f in ("tp_gemm.cu", "tp_device.cuh"):
+            with open(os.path.join(ROOT, "megatron_tensor_transformer_colwise_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != entry["source_sha256_16"]:
+            return None
+        return entry["bytes_per_launch"]
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------------ distributed glue
 
 def dist_env():
@@ -437,7 +456,8 @@ def run_ours(args):
                 "frac": achieved / peaks["bf16_tflops_sustained"],
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
                 "algorithmic_flops_per_launch": dom_fl,
-                "traffic": args.dominant_traffic}
+                "traffic": args.dominant_traffic if args.dominant_traffic is not None
+                else profiled_traffic(dom_name)}
 
     # The g reduction as a PARTIALS-mode kernel over the layer's partials.
     n = s.tokens * s.hidden
