@@ -11,10 +11,13 @@
 // (key position <= query position) within each sequence, fp32 softmax with
 // a running maximum subtracted, no dropout, no rotary embedding.
 //
-// One CTA per (128 query rows, query head, sequence), 6 warps:
-//   warp 0      TMA: Q once, then K and V blocks of 128 keys (2-stage rings)
-//               from the shard-blocked QKV buffer (one 2-D tensor map).
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 128, fp32, two
+// One CTA per (128 query rows, query head, sequence), 6 warps, two CTAs
+// resident per SM (256 TMEM columns and ~97 KB of shared memory each), so
+// one CTA's softmax overlaps the other's tensor-core work:
+//   warp 0      TMA: Q once, then K and V blocks of 64 keys (K in a 2-stage
+//               ring running one block ahead, V single-buffered) from the
+//               shard-blocked QKV buffer.
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 64, fp32, two
 //               TMEM buffers so S of block j+1 is computed while the softmax
 //               works on block j), then O += P V (V used as an MN-major
 //               operand straight from its [key][d] layout).
@@ -41,40 +44,46 @@ namespace {
 using namespace tpk;
 
 constexpr int QB = 128;  // query rows per CTA (UMMA M, TMEM lanes)
-constexpr int KB = 128;  // keys per block (UMMA N of S, UMMA K of PV)
+constexpr int KB = 64;   // keys per block (UMMA N of S, UMMA K of PV)
 constexpr int NTHREADS = 192;
-constexpr int BOX_BYTES = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (16 KB)
-constexpr int P_BYTES = QB * KB * 2;     // 32 KB
+constexpr int QBOX = QB * 128;  // TMA box of Q: 128 rows x 64 bf16 (16 KB)
+constexpr int KBOX = KB * 128;  // TMA box of K or V: 64 rows x 64 bf16 (8 KB)
+constexpr int P_BYTES = QB * KB * 2;       // 16 KB: one 128-byte-swizzle column
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 of the allowed growth of P
 
 enum {
     B_Q_FULL = 0,
-    B_K_FULL = 1,   // x2
+    B_K_FULL = 1,   // x2 (K ring)
     B_K_EMPTY = 3,  // x2
-    B_V_FULL = 5,   // x2
-    B_V_EMPTY = 7,  // x2
-    B_S_FULL = 9,   // x2
-    B_S_EMPTY = 11, // x2
-    B_P_FULL = 13,
-    B_P_EMPTY = 14,
-    B_O_FULL = 15,
-    B_DRAIN = 16,
-    NUM_BARS = 17
+    B_V_FULL = 5,   // V is single-buffered
+    B_V_EMPTY = 6,
+    B_S_FULL = 7,   // x2 (S buffers in TMEM)
+    B_S_EMPTY = 9,  // x2
+    B_P_FULL = 11,
+    B_P_EMPTY = 12,
+    B_O_FULL = 13,
+    B_DRAIN = 14,
+    NUM_BARS = 15
 };
 
+// Shared memory of one CTA (two CTAs share an SM):
+//   Q [128][d] | K ring 2 x [64][d] | V [64][d] | P [128][64] | barriers
 template <int D>
 struct Layout {
-    static constexpr int TILE = QB * D * 2;  // Q, K or V tile bytes
+    static constexpr int QT = QB * D * 2;
+    static constexpr int KT = KB * D * 2;
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = TILE;
-    static constexpr int V_OFF = 3 * TILE;
-    static constexpr int P_OFF = 5 * TILE;
+    static constexpr int K_OFF = QT;
+    static constexpr int V_OFF = K_OFF + 2 * KT;
+    static constexpr int P_OFF = V_OFF + KT;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * NUM_BARS + 16;
+    static constexpr int TMEM_COLS = 2 * KB + D <= 256 ? 256 : 512;  // S0 | S1 | O
 };
 
 struct AttnParams {
-    CUtensorMap map;  // the QKV buffer: dims {t * W, tokens}, box {64, 128}
+    CUtensorMap map_q;   // the QKV buffer: dims {t * W, tokens}, box {64, 128}
+    CUtensorMap map_kv;  // the same buffer, box {64, 64}
     __nv_bfloat16* o;
     long long ld_o;
     int seq, heads, kv_heads, t, heads_per_shard, shard_w, q_w, kv_w;
@@ -90,6 +99,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// 2^x with the SFU's approximate exp2 (PTX ex2.approx.ftz.f32: relative
+// error about 2^-22, -inf -> +0); used for the softmax numerators.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -98,7 +115,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_constant__ AttnParams p) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -125,18 +142,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const int kcol = shard * p.shard_w + p.q_w + gl * D;
     const int vcol = kcol + p.kv_w;
     const int tok0 = b * p.seq;
-    const int nkb = qb + 1;  // causal: key blocks 0..qb
+    const int q0 = qb * QB;
+    // causal: keys 0 .. q0+127, and never past the sequence
+    const int nkb = min((q0 + QB + KB - 1) / KB, (p.seq + KB - 1) / KB);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q_FULL), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
-            mbar_init(bar(B_V_FULL + s), 1);
-            mbar_init(bar(B_V_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
             mbar_init(bar(B_S_EMPTY + s), 4);
         }
+        mbar_init(bar(B_V_FULL), 1);
+        mbar_init(bar(B_V_EMPTY), 1);
         mbar_init(bar(B_P_FULL), 4);
         mbar_init(bar(B_P_EMPTY), 1);
         mbar_init(bar(B_O_FULL), 1);
@@ -144,9 +163,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.map);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.map_q);
+        tma_prefetch_desc(&p.map_kv);
+    }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -156,47 +178,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
+        // Order: Q, K0, then for each block kb: K(kb+1), V(kb).  V is single-
+        // buffered (its load waits for the previous PV), so K runs one block
+        // ahead to keep the S = Q K^T MMAs fed.
         if (lane == 0) {
             bool ok = true;
-            uint32_t issued = 0;  // bit per stage and operand: fills not yet known landed
-            uint32_t kpar = 0, vpar = 0;
-            mbar_arrive_expect_tx(bar(B_Q_FULL), L::TILE);
+            uint32_t kissued = 0, kpar = 0, vissued = 0, vpar = 0;
+            mbar_arrive_expect_tx(bar(B_Q_FULL), L::QT);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-                tma_load_2d(sQ + c * BOX_BYTES, &p.map, bar(B_Q_FULL), qcol + 64 * c, tok0 + qb * QB);
-            for (int kb = 0; kb < nkb && ok; ++kb) {
+                tma_load_2d(sQ + c * QBOX, &p.map_q, bar(B_Q_FULL), qcol + 64 * c, tok0 + q0);
+            auto load_k = [&](int kb) -> bool {
                 const int st = kb & 1;
                 const uint32_t ph = (kb >> 1) & 1;
-                const int krow = tok0 + kb * KB;
-                if (!mbar_wait(bar(B_K_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar(B_K_FULL + st), L::TILE);
+                if (!mbar_wait(bar(B_K_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns))
+                    return false;
+                mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KT);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sK + st * L::TILE + c * BOX_BYTES, &p.map, bar(B_K_FULL + st),
-                                kcol + 64 * c, krow);
-                issued |= 1u << st;
+                    tma_load_2d(sK + st * L::KT + c * KBOX, &p.map_kv, bar(B_K_FULL + st),
+                                kcol + 64 * c, tok0 + kb * KB);
+                kissued |= 1u << st;
                 kpar = (kpar & ~(1u << st)) | (ph << st);
-                if (!mbar_wait(bar(B_V_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                return true;
+            };
+            ok = load_k(0);
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                if (kb + 1 < nkb && !(ok = load_k(kb + 1))) break;
+                const uint32_t ph = kb & 1;
+                if (!mbar_wait(bar(B_V_EMPTY), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(B_V_FULL + st), L::TILE);
+                mbar_arrive_expect_tx(bar(B_V_FULL), L::KT);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sV + st * L::TILE + c * BOX_BYTES, &p.map, bar(B_V_FULL + st),
-                                vcol + 64 * c, krow);
-                issued |= 4u << st;
-                vpar = (vpar & ~(1u << st)) | (ph << st);
+                    tma_load_2d(sV + c * KBOX, &p.map_kv, bar(B_V_FULL), vcol + 64 * c, tok0 + kb * KB);
+                vissued = 1;
+                vpar = ph;
             }
             if (!ok) {
                 drain_wait(bar(B_Q_FULL), 0);
-                for (int s = 0; s < 2; ++s) {
-                    if (issued & (1u << s)) drain_wait(bar(B_K_FULL + s), (kpar >> s) & 1u);
-                    if (issued & (4u << s)) drain_wait(bar(B_V_FULL + s), (vpar >> s) & 1u);
-                }
+                for (int s = 0; s < 2; ++s)
+                    if (kissued & (1u << s)) drain_wait(bar(B_K_FULL + s), (kpar >> s) & 1u);
+                if (vissued) drain_wait(bar(B_V_FULL), vpar);
             }
         }
     } else if (warp == 1) {
@@ -216,8 +241,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 const uint32_t d_tmem = tmem + st * KB;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * BOX_BYTES + (ks & 3) * 32;
-                    umma_bf16(d_tmem, sdesc_sw128(sQ + off), sdesc_sw128(sK + st * L::TILE + off),
+                    const uint32_t a_off = (ks >> 2) * QBOX + (ks & 3) * 32;
+                    const uint32_t b_off = (ks >> 2) * KBOX + (ks & 3) * 32;
+                    umma_bf16(d_tmem, sdesc_sw128(sQ + a_off), sdesc_sw128(sK + st * L::KT + b_off),
                               idesc_s, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_K_EMPTY + st));
@@ -227,21 +253,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             if (ok) ok = issue_s(0);
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 if (kb + 1 < nkb && !(ok = issue_s(kb + 1))) break;
-                const int st = kb & 1;
                 if (!mbar_wait(bar(B_P_FULL), kb & 1, abort_flag, p.status, p.timeout_ns) ||
-                    !mbar_wait(bar(B_V_FULL + st), (kb >> 1) & 1, abort_flag, p.status, p.timeout_ns)) {
+                    !mbar_wait(bar(B_V_FULL), kb & 1, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < KB / 16; ++ks) {
-                    const uint32_t a_off = (ks >> 2) * (P_BYTES / 2) + (ks & 3) * 32;
-                    umma_bf16(tmem + 2 * KB, sdesc_sw128(sP + a_off),
-                              sdesc_sw128_mn(sV + st * L::TILE + ks * 16 * 128, BOX_BYTES, 1024),
-                              idesc_o, (kb > 0 || ks > 0) ? 1u : 0u);
+                    umma_bf16(tmem + 2 * KB, sdesc_sw128(sP + ks * 32),
+                              sdesc_sw128_mn(sV + ks * 16 * 128, KBOX, 1024), idesc_o,
+                              (kb > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(B_V_EMPTY + st));
+                umma_commit(bar(B_V_EMPTY));
                 umma_commit(bar(B_P_EMPTY));
             }
             if (ok) {
@@ -255,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         // ---------------------------------------------------------- softmax / epilogue
         const int q = warp & 3;  // TMEM lane quadrant
         const int r = q * 32 + lane;
-        const int qpos = qb * QB + r;
+        const int qpos = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         float m_ref = -INFINITY, l_sum = 0.0f;
         bool ok = true;
@@ -279,16 +303,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             if (lane == 0) mbar_arrive(bar(B_S_EMPTY + st));
 
             const int k0 = kb * KB;
-            if (kb == qb || k0 + KB > p.seq) {
+            if (k0 + KB - 1 > q0 || k0 + KB > p.seq) {
 #pragma unroll
                 for (int c = 0; c < KB; ++c) {
                     const int key = k0 + c;
                     if (key > qpos || key >= p.seq) s[c] = __float_as_uint(-INFINITY);
                 }
             }
-            float mx = -INFINITY;
+            // Row max with 8 independent chains (one softmax warp per SM
+            // sub-partition and CTA leaves little to hide a serial chain).
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < KB; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+#pragma unroll
+            for (int c = 8; c < KB; c += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[c + e]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float mxs = mx * p.scale_log2;
             float alpha = 1.0f;
             bool rescale = false;
@@ -297,15 +329,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 m_ref = mxs;
                 rescale = kb > 0;
             }
-            float sum = 0.0f;
+            float sum8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
             uint32_t pk[KB / 2];
 #pragma unroll
             for (int c = 0; c < KB / 2; ++c) {
-                const float p0 = exp2f(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
-                const float p1 = exp2f(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
-                sum += p0 + p1;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
+                sum8[c & 7] += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
+            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l_sum = l_sum * alpha + sum;
 
             // PV of the previous block must be done: O is stable, P is free.
@@ -329,14 +365,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 }
                 tmem_st_wait();
             }
-            // P row r: keys 0..63 in the first 16 KB region, 64..127 in the
-            // second; 16-byte chunk c of the row sits at chunk c ^ (r % 8).
+            // P row r: 64 keys = one 128-byte row of a 128-byte-swizzle
+            // column; 16-byte chunk c of the row sits at chunk c ^ (r % 8).
 #pragma unroll
             for (int c8 = 0; c8 < KB / 8; ++c8) {
-                const uint32_t region = static_cast<uint32_t>(c8 >> 3) * (P_BYTES / 2);
-                const uint32_t chunk = static_cast<uint32_t>((c8 & 7) ^ (r & 7));
-                st_shared_v4(sP + region + r * 128 + (chunk << 4), pk[4 * c8], pk[4 * c8 + 1],
-                             pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                const uint32_t chunk = static_cast<uint32_t>(c8 ^ (r & 7));
+                st_shared_v4(sP + r * 128 + (chunk << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
+                             pk[4 * c8 + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -376,7 +411,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -400,14 +435,17 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     const long long tokens = static_cast<long long>(a.batch) * a.seq;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.ld_qkv), static_cast<cuuint64_t>(tokens)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.ld_qkv) * 2};
-    cuuint32_t box[2] = {64, 128};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&p.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.QKV), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (err) *err = "cuTensorMapEncodeTiled (attention QKV) failed: " + std::to_string((int)r);
-        return TP_ERR_CUDA;
+    for (int m = 0; m < 2; ++m) {
+        cuuint32_t box[2] = {64, m == 0 ? static_cast<cuuint32_t>(QB) : static_cast<cuuint32_t>(KB)};
+        CUresult r = encode(m == 0 ? &p.map_q : &p.map_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                            const_cast<void*>(a.QKV), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            if (err) *err = "cuTensorMapEncodeTiled (attention QKV) failed: " + std::to_string((int)r);
+            return TP_ERR_CUDA;
+        }
     }
     p.o = reinterpret_cast<__nv_bfloat16*>(a.O);
     p.ld_o = a.ld_o;
