@@ -8,12 +8,18 @@
 // colwise) and "셀프 어텐션" (Q/K/V colwise, a/t heads per shard; o_proj
 // rowwise).
 //
-// One kernel template, one CTA per SM (persistent), 6 warps:
-//   warp 0      TMA producer (one lane): A and B tiles into a 4-stage ring
-//   warp 1      TMEM owner and MMA issuer (one lane): 128x256x16 bf16 UMMAs
+// One kernel template, one CTA per SM (persistent), CTAs in pairs
+// (clusters of 2) that share a 256 x 256 output tile, 6 warps per CTA:
+//   warp 0      TMA producer (one lane): this CTA's 128 rows of A and half of
+//               the tile's 256 B rows into a 6-stage ring (32 KB stages);
+//               completion is counted on the pair leader's barriers
+//   warp 1      TMEM owner; in the leader CTA also the MMA issuer (one lane):
+//               256x256x16 bf16 UMMAs (tcgen05 cta_group::2) that read both
+//               CTAs' shared memory and accumulate 128 rows in each CTA's TMEM
 //   warps 2..5  epilogue: TMEM -> registers -> fused op -> global
 // The accumulator is double-buffered in TMEM (2 x 256 fp32 columns) so the
-// epilogue of tile n overlaps the main loop of tile n+1.
+// epilogue of tile n overlaps the main loop of tile n+1.  Splitting B over
+// the pair halves each SM's shared-memory operand traffic per FLOP.
 //
 // Shards are grid/loop indices, not devices: a colwise output tile may span
 // shard boundaries (the output is the concatenation of the shards' slices);
@@ -33,24 +39,39 @@
 #include "tp_device.cuh"
 #include "tp_internal.h"
 
+#ifndef TP_GEMM_CTA_PAIR
+#define TP_GEMM_CTA_PAIR 2
+#endif
+
 namespace {
 
 using namespace tpk;
 
-constexpr int BM = 128;             // UMMA M (TMEM lanes)
+constexpr int BM = 128;             // rows of the tile held by one CTA (TMEM lanes)
 constexpr int BN = 256;             // UMMA N (TMEM columns per accumulator)
 constexpr int BK = 64;              // one 128-byte swizzle row of bf16
 constexpr int UK = 16;              // K of one kind::f16 UMMA
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_CHUNK_ROWS = 64;
 constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int TMEM_COLS = 2 * BN;               // 512
 constexpr int NUM_THREADS = 192;
-constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+
+// CG = CTAs per tile.  CG = 1: a 128 x 256 tile per CTA, 4 stages of 48 KB.
+// CG = 2: a 256 x 256 tile per CTA pair (cta_group::2): each CTA loads its
+// 128 rows of A and half of the 256 B rows, 6 stages of 32 KB, and the
+// pair's leader issues 256 x 256 x 16 UMMAs that read both CTAs' shared
+// memory and write 128 accumulator rows into each CTA's TMEM.
+template <int CG>
+struct Cfg {
+    static constexpr int B_BYTES = (BN / CG) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr int CHUNKS = (BN / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int TILE_M = BM * CG;
+};
 
 struct GemmParams {
     CUtensorMap mapA;
@@ -116,106 +137,124 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Tensor map and first row of each 64-row B box of an output tile.  Depends
 // only on the tile, so the producer computes it once per tile, not per
 // k-block (the QKV segment arithmetic would otherwise stall the TMA issue).
-template <int MODE>
-__device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, const CUtensorMap* (&map)[4],
-                                        int (&row)[4]) {
+// Tensor map and first row of the 64-row B boxes [first, first + N) of an
+// output tile (a CTA of a pair loads half of the tile's four boxes).
+// Depends only on the tile, so the producer computes it once per tile, not
+// per k-block (the QKV segment arithmetic would otherwise stall TMA issue).
+template <int MODE, int N>
+__device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, int first,
+                                        const CUtensorMap* (&map)[N], int (&row)[N]) {
 #pragma unroll
-    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c) {
-        map[c] = &p.mapB[0];
+    for (int i = 0; i < N; ++i) {
+        const int c = first + i;
+        map[i] = &p.mapB[0];
         if (MODE == tpi::GEMM_COL_SWIGLU) {
             // rows [0,128) of the tile: W1; rows [128,256): W3, both for
             // output columns nb*128 .. nb*128+127.
-            map[c] = &p.mapB[c >> 1];
-            row[c] = nb * (BN / 2) + (c & 1) * B_CHUNK_ROWS;
+            map[i] = (c >> 1) ? &p.mapB[1] : &p.mapB[0];
+            row[i] = nb * (BN / 2) + (c & 1) * B_CHUNK_ROWS;
         } else if (MODE == tpi::GEMM_COL_QKV) {
             const int col = nb * BN + c * B_CHUNK_ROWS;
             if (col >= p.N) {
-                row[c] = p.b_rows0;  // wholly out of range: zeros
+                row[i] = p.b_rows0;  // wholly out of range: zeros
             } else {
-                const int i = col / p.qkv_ws;
-                const int l = col - i * p.qkv_ws;
+                const int sh = col / p.qkv_ws;
+                const int l = col - sh * p.qkv_ws;
                 if (l < p.qkv_qw) {
-                    row[c] = i * p.qkv_qw + l;
+                    row[i] = sh * p.qkv_qw + l;
                 } else {
-                    const int kv0 = kv_first(p.kv_heads, p.tp, i) * p.head_dim;
+                    const int kv0 = kv_first(p.kv_heads, p.tp, sh) * p.head_dim;
                     const int l2 = l - p.qkv_qw;
                     if (l2 < p.qkv_kvw) {
-                        map[c] = &p.mapB[1];
-                        row[c] = kv0 + l2;
+                        map[i] = &p.mapB[1];
+                        row[i] = kv0 + l2;
                     } else {
-                        map[c] = &p.mapB[2];
-                        row[c] = kv0 + (l2 - p.qkv_kvw);
+                        map[i] = &p.mapB[2];
+                        row[i] = kv0 + (l2 - p.qkv_kvw);
                     }
                 }
             }
         } else {
-            row[c] = nb * BN + c * B_CHUNK_ROWS;
+            row[i] = nb * BN + c * B_CHUNK_ROWS;
         }
     }
 }
 
-template <int MODE>
+template <int MODE, int CG>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
-                                              volatile int* abort_flag) {
+                                              uint32_t rank, volatile int* abort_flag) {
+    using C = Cfg<CG>;
     constexpr bool ROW = (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
         int s_grid, mb, nb;
         decode_tile(p, tile, s_grid, mb, nb);
-        const CUtensorMap* bmap[4];
-        int brow[4];
-        if (!ROW) b_boxes<MODE>(p, nb, bmap, brow);
+        const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
+        const CUtensorMap* bmap[C::CHUNKS];
+        int brow[C::CHUNKS];
+        if (!ROW) b_boxes<MODE, C::CHUNKS>(p, nb, static_cast<int>(rank) * C::CHUNKS, bmap, brow);
         for (int ks = 0; ok && ks < p.k_shards; ++ks) {
             const int shard = (MODE == tpi::GEMM_ROW_PARTIAL) ? s_grid : ks;
             for (int kb = 0; kb < p.kb_per_shard; ++kb) {
-                const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+                const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
                 if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(full, STAGE_BYTES);
-                const uint32_t a_dst = base + stage * STAGE_BYTES;
+                // The leader's full barrier counts the bytes of both CTAs.
+                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
+                const uint32_t full_l = (CG == 2) ? mapa_shared(full, 0) : full;
+                const uint32_t a_dst = base + stage * C::STAGE_BYTES;
                 const uint32_t b_dst = a_dst + A_BYTES;
                 const int kc = kb * BK;
-                if (ROW) {
-                    tma_load_3d(a_dst, &p.mapA, full, kc, shard, mb * BM);
 #pragma unroll
-                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c)
-                        tma_load_3d(b_dst + c * B_CHUNK_BYTES, &p.mapB[0], full, kc, shard,
-                                    nb * BN + c * B_CHUNK_ROWS);
-                } else {
-                    tma_load_2d(a_dst, &p.mapA, full, kc, mb * BM);
-#pragma unroll
-                    for (int c = 0; c < BN / B_CHUNK_ROWS; ++c)
-                        tma_load_2d(b_dst + c * B_CHUNK_BYTES, bmap[c], full, kc, brow[c]);
+                for (int c = -1; c < C::CHUNKS; ++c) {
+                    const int cc = static_cast<int>(rank) * C::CHUNKS + c;  // B box of the tile
+                    const uint32_t dst = c < 0 ? a_dst : b_dst + c * B_CHUNK_BYTES;
+                    if (ROW) {
+                        const CUtensorMap* map = c < 0 ? &p.mapA : &p.mapB[0];
+                        const int r = c < 0 ? arow : nb * BN + cc * B_CHUNK_ROWS;
+                        if (CG == 2) tma_load_3d_pair(dst, map, full_l, kc, shard, r);
+                        else tma_load_3d(dst, map, full_l, kc, shard, r);
+                    } else {
+                        const CUtensorMap* map = c < 0 ? &p.mapA : bmap[c < 0 ? 0 : c];
+                        const int r = c < 0 ? arow : brow[c < 0 ? 0 : c];
+                        if (CG == 2) tma_load_2d_pair(dst, map, full_l, kc, r);
+                        else tma_load_2d(dst, map, full_l, kc, r);
+                    }
                 }
                 issued_mask |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
+                if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
         }
     }
-    if (!ok) {
-        // Let every copy this thread started land before the CTA exits.
-        for (int s = 0; s < STAGES; ++s)
+    if (!ok && rank == 0) {
+        // Let every copy of the pair land before the CTAs exit (the leader's
+        // full barriers count both CTAs' bytes).
+        for (int s = 0; s < C::STAGES; ++s)
             if (issued_mask & (1u << s)) drain_wait(bar0 + 8 * s, (last_parity >> s) & 1u);
     }
 }
 
+template <int CG>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                          uint32_t tmem_base, volatile int* abort_flag) {
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    using C = Cfg<CG>;
+    constexpr uint32_t idesc = idesc_bf16_f32(BM * CG, BN);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     const int kblocks = p.k_shards * p.kb_per_shard;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const uint32_t tfull = bar0 + 8 * (2 * STAGES + acc);
-        const uint32_t tempty = bar0 + 8 * (2 * STAGES + 2 + acc);
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
+        const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
+        const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
         if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -223,56 +262,64 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
-            const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (STAGES + stage);
+            const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
             if (!mbar_wait(full, phase, abort_flag, p.status, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t a_addr = base + stage * STAGE_BYTES;
+            const uint32_t a_addr = base + stage * C::STAGE_BYTES;
             const uint64_t adesc = sdesc_sw128(a_addr);
             const uint64_t bdesc = sdesc_sw128(a_addr + A_BYTES);
 #pragma unroll
             for (int j = 0; j < BK / UK; ++j) {
                 // +32 bytes along K inside the 128-byte swizzle row.
-                umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc,
-                          (kb > 0 || j > 0) ? 1u : 0u);
+                const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+                if (CG == 2) umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, accum);
+                else umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, accum);
             }
-            umma_commit(empty);  // frees the smem stage when these UMMAs finish
-            if (++stage == STAGES) {
+            // Frees the smem stage (of both CTAs) when these UMMAs finish.
+            if (CG == 2) umma_commit_pair(empty, 0x3);
+            else umma_commit(empty);
+            if (++stage == C::STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        umma_commit(tfull);  // accumulator ready for the epilogue
+        // Accumulator ready for the epilogue (of both CTAs).
+        if (CG == 2) umma_commit_pair(tfull, 0x3);
+        else umma_commit(tfull);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
     if (!ok) {
         // No UMMA may still write TMEM when it is freed.
-        const uint32_t drain = bar0 + 8 * (2 * STAGES + 4);
-        umma_commit(drain);
+        const uint32_t drain = bar0 + 8 * (2 * C::STAGES + 4);
+        if (CG == 2) umma_commit_pair(drain, 0x1);
+        else umma_commit(drain);
         drain_wait(drain, 0);
     }
 }
 
-template <int MODE>
-__device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0,
-                                              uint32_t tmem_base, volatile int* abort_flag) {
+template <int MODE, int CG>
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t tmem_base,
+                                              uint32_t rank, volatile int* abort_flag) {
+    using C = Cfg<CG>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    for (int tile = cid; tile < p.num_tiles; tile += ncl) {
         int s_grid, mb, nb;
         decode_tile(p, tile, s_grid, mb, nb);
-        const uint32_t tfull = bar0 + 8 * (2 * STAGES + acc);
-        const uint32_t tempty = bar0 + 8 * (2 * STAGES + 2 + acc);
+        const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
+        const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
         const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status, p.timeout_ns);
         __syncwarp();
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
-        const int row = mb * BM + q * 32 + lane;
+        const int row = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
         const bool row_ok = row < p.M;
         const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
         uint32_t r[32];
@@ -373,33 +420,41 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty);
+        // Release the accumulator: the leader's MMA waits for the epilogue
+        // warps of both CTAs.
+        if (lane == 0) {
+            if (CG == 2) mbar_arrive_cluster(mapa_shared(tempty, 0));
+            else mbar_arrive(tempty);
+        }
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
 }
 
-template <int MODE>
+template <int MODE, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using C = Cfg<CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(gbase + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 5));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar0 + 8 * s, 1);             // full: producer arrive + tx bytes
-            mbar_init(bar0 + 8 * (STAGES + s), 1);  // empty: one tcgen05.commit
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar0 + 8 * s, 1);                // full: leader's arrive + both CTAs' bytes
+            mbar_init(bar0 + 8 * (C::STAGES + s), 1);  // empty: one commit
         }
-        mbar_init(bar0 + 8 * (2 * STAGES + 0), 1);  // tmem full x2: one commit
-        mbar_init(bar0 + 8 * (2 * STAGES + 1), 1);
-        mbar_init(bar0 + 8 * (2 * STAGES + 2), 4);  // tmem empty x2: 4 epilogue warps
-        mbar_init(bar0 + 8 * (2 * STAGES + 3), 4);
-        mbar_init(bar0 + 8 * (2 * STAGES + 4), 1);  // drain
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 0), 1);       // tmem full x2: one commit
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 1), 1);
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 2), 4 * CG);  // tmem empty x2: epilogue warps
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 3), 4 * CG);
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 4), 1);       // drain
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -410,26 +465,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_co
         if (MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[2]);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if (CG == 2) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // Both CTAs' barriers exist before either signals the other's.
+    if (CG == 2) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop<MODE>(p, base, bar0, abort_flag);
+        if (lane == 0) producer_loop<MODE, CG>(p, base, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop(p, base, bar0, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) mma_loop<CG>(p, base, bar0, tmem_base, abort_flag);
     } else {
-        epilogue_loop<MODE>(p, bar0, tmem_base, abort_flag);
+        epilogue_loop<MODE, CG>(p, bar0, tmem_base, rank, abort_flag);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    // Neither CTA leaves while the pair may still touch its shared memory.
+    if (CG == 2) cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) {
+        if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -477,23 +544,36 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     return true;
 }
 
-template <int MODE>
+template <int MODE, int CG>
 int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string* err) {
-    auto kern = tp_gemm_kernel<MODE>;
+    auto kern = tp_gemm_kernel<MODE, CG>;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+                                             Cfg<CG>::SMEM);
         if (e != cudaSuccess) {
             if (err) *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return TP_ERR_CUDA;
         }
         configured[dev] = true;
     }
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (err) *err = std::string("GEMM launch: ") + cudaGetErrorString(e);
         return TP_ERR_CUDA;
@@ -504,6 +584,9 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
 }  // namespace
 
 namespace tpi {
+
+// CTAs per output tile (1: 128 x 256 per CTA; 2: 256 x 256 per CTA pair).
+constexpr int kPairTiles = TP_GEMM_CTA_PAIR;
 
 int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     GemmParams p;
@@ -520,7 +603,8 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     p.ldr = a.ldr;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
-    p.m_tiles = static_cast<int>((a.M + BM - 1) / BM);
+    constexpr int CG = kPairTiles;
+    p.m_tiles = static_cast<int>((a.M + Cfg<CG>::TILE_M - 1) / Cfg<CG>::TILE_M);
     const int bn_out = (a.mode == GEMM_COL_SWIGLU) ? BN / 2 : BN;
     p.n_tiles = static_cast<int>((a.N + bn_out - 1) / bn_out);
     p.grid_shards = (a.mode == GEMM_ROW_PARTIAL) ? a.t : 1;
@@ -564,18 +648,18 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     }
     // Tiles run in groups of group_m m-tiles sweeping all n-tiles, so a wave
     // of SM-count CTAs shares a few weight (B) tiles across many m-tiles.
-    // Measured on GB300 at the layer's shapes: 32 is best for the colwise
-    // GEMMs (W1/W3 1846 vs 1655 TFLOP/s at 8), 16 for the rowwise ones.
-    p.group_m = row ? 16 : 32;
+    // Measured on GB300 at the layer's shapes with 256-row pair tiles: 16
+    // is best (W1/W3 2005 TFLOP/s vs 1941 at 32 and 1884 at 4).
+    p.group_m = 16;
     p.num_tiles = p.grid_shards * p.m_tiles * p.n_tiles;
     if (p.num_tiles == 0) return TP_OK;
-    const int grid = std::min(p.num_tiles, device_sm_count());
+    const int grid = std::min(p.num_tiles, device_sm_count() / CG) * CG;
     switch (a.mode) {
-        case GEMM_COL_ACT: return launch_mode<GEMM_COL_ACT>(p, grid, stream, err);
-        case GEMM_COL_SWIGLU: return launch_mode<GEMM_COL_SWIGLU>(p, grid, stream, err);
-        case GEMM_COL_QKV: return launch_mode<GEMM_COL_QKV>(p, grid, stream, err);
-        case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED>(p, grid, stream, err);
-        case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL>(p, grid, stream, err);
+        case GEMM_COL_ACT: return launch_mode<GEMM_COL_ACT, CG>(p, grid, stream, err);
+        case GEMM_COL_SWIGLU: return launch_mode<GEMM_COL_SWIGLU, CG>(p, grid, stream, err);
+        case GEMM_COL_QKV: return launch_mode<GEMM_COL_QKV, CG>(p, grid, stream, err);
+        case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED, CG>(p, grid, stream, err);
+        case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL, CG>(p, grid, stream, err);
         default:
             if (err) *err = "unknown GEMM mode";
             return TP_ERR_INVALID_ARG;
