@@ -284,10 +284,12 @@ TP_API int tp_layer_forward(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
 /* tp_layer_forward that also records caller-created CUDA events (cudaEvent_t
  * handles) on `stream` at the boundaries of its kernels, for per-kernel
  * timing on the launching stream: events[0] before the first kernel and
- * events[i] after kernel i.  FUSED mode launches 7 kernels (RMSNorm, QKV,
- * attention, o_proj+residual, RMSNorm, W1/W3 colwise, W2+residual) and
- * needs n_events >= 8; PARTIALS mode launches 8 (RMSNorm, QKV, attention,
- * o_proj partials, g+RMSNorm, W1/W3 colwise, W2 partials, g) and needs 9.
+ * events[i] after kernel i.  FUSED mode launches 6 kernels (row sums of
+ * squares of x, QKV with the first RMSNorm folded in, attention,
+ * o_proj + g + residual + row sums of squares of h1, W1/W3 colwise with the
+ * second RMSNorm folded in, W2 + g + residual) and needs n_events >= 7;
+ * PARTIALS mode launches 8 (RMSNorm, QKV, attention, o_proj partials,
+ * g + RMSNorm, W1/W3 colwise, W2 partials, g) and needs 9.
  * Fewer events -> TP_ERR_INVALID_ARG before any launch. */
 TP_API int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w,
                                    tp_bf16* Y, void* workspace, size_t ws_bytes, void* stream,

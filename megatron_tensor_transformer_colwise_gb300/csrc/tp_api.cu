@@ -94,6 +94,7 @@ struct Layout {
     size_t xn = 0;       // [M][h] bf16 (normalised input of a block)
     size_t h1 = 0;       // [M][h] bf16 (residual stream after attention)
     size_t partials = 0; // [t][M][h] fp32 or bf16 (layer in PARTIALS mode)
+    size_t ss = 0;       // 2 x [M] fp32 row sums of squares (layer in FUSED mode)
 };
 
 size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
@@ -109,15 +110,18 @@ Layout layout_of(const tp_plan_s* p, int op) {
         }
     }
     if (op == TP_OP_LAYER) {
-        L.xn = align_up(M * p->h * 2);
         L.h1 = align_up(M * p->h * 2);
-        if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS)
+        if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS) {
+            L.xn = align_up(M * p->h * 2);
             L.partials = align_up(static_cast<size_t>(p->t) * M * p->h * partial_elem_bytes(p));
+        } else {
+            L.ss = align_up(2 * M * sizeof(float));  // folded RMSNorm statistics
+        }
     }
     return L;
 }
 
-size_t layout_total(const Layout& L) { return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials; }
+size_t layout_total(const Layout& L) { return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss; }
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
     const size_t need = layout_total(layout_of(p, op));
@@ -137,7 +141,7 @@ int run(int rc, const std::string& err) {
 // ---- building blocks (arguments already validated) ----
 
 int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3, void* Y,
-               cudaStream_t s) {
+               cudaStream_t s, const float* row_ss = nullptr) {
     tpi::GemmArgs g;
     g.mode = (p->cfg.act == TP_ACT_SWIGLU) ? tpi::GEMM_COL_SWIGLU : tpi::GEMM_COL_ACT;
     g.act = p->cfg.act;
@@ -154,6 +158,9 @@ int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3
     }
     g.out = Y;
     g.ldo = p->f;
+    g.row_ss = row_ss;
+    g.inv_h = 1.0f / static_cast<float>(p->h);
+    g.eps = p->cfg.rms_eps;
     g.status = p->status;
     g.timeout_ns = p->timeout_ns;
     std::string err;
@@ -164,7 +171,7 @@ int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3
 // accumulator, + bias + residual, bf16 out) or per-shard partials.
 int do_rowwise(const tp_plan_s* p, const void* A, int64_t Ks, const void* B, int64_t N,
                const void* bias, const void* residual, void* partials, void* out, bool fused,
-               cudaStream_t s) {
+               cudaStream_t s, float* ss_out = nullptr) {
     tpi::GemmArgs g;
     g.mode = fused ? tpi::GEMM_ROW_FUSED : tpi::GEMM_ROW_PARTIAL;
     g.M = p->M;
@@ -180,6 +187,7 @@ int do_rowwise(const tp_plan_s* p, const void* A, int64_t Ks, const void* B, int
         g.bias = bias;
         g.residual = residual;
         g.ldr = N;
+        g.ss_out = ss_out;
     } else {
         g.out = partials;
         g.ldo = N;
@@ -201,7 +209,7 @@ int do_reduce(const tp_plan_s* p, const void* partials, const void* bias, const 
 }
 
 int do_qkv(const tp_plan_s* p, const void* X, const void* Wq, const void* Wk, const void* Wv,
-           void* QKV, cudaStream_t s) {
+           void* QKV, cudaStream_t s, const float* row_ss = nullptr) {
     tpi::GemmArgs g;
     g.mode = tpi::GEMM_COL_QKV;
     g.M = p->M;
@@ -222,6 +230,9 @@ int do_qkv(const tp_plan_s* p, const void* X, const void* Wq, const void* Wk, co
     g.head_dim = static_cast<int>(p->d);
     g.out = QKV;
     g.ldo = g.N;
+    g.row_ss = row_ss;
+    g.inv_h = 1.0f / static_cast<float>(p->h);
+    g.eps = p->cfg.rms_eps;
     g.status = p->status;
     g.timeout_ns = p->timeout_ns;
     std::string err;
@@ -598,7 +609,7 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     if (X == Y) return fail(TP_ERR_INVALID_ARG, "X and Y must not alias");
     if ((rc = check_ws(plan, TP_OP_LAYER, workspace, ws_bytes))) return rc;
     const bool fused_mode = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
-    const int need_events = fused_mode ? 8 : 9;
+    const int need_events = fused_mode ? 7 : 9;
     if (events) {
         if (n_events < need_events)
             return fail(TP_ERR_INVALID_ARG, "%d events given, %d needed", n_events, need_events);
@@ -616,12 +627,37 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     void* O = region(workspace, off); off += L.o;
     void* xn = region(workspace, off); off += L.xn;
     void* h1 = region(workspace, off); off += L.h1;
-    void* P = L.partials ? region(workspace, off) : nullptr;
-    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    void* P = L.partials ? region(workspace, off) : nullptr; off += L.partials;
+    float* ss1 = L.ss ? reinterpret_cast<float*>(region(workspace, off)) : nullptr;
+    float* ss2 = ss1 ? ss1 + plan->M : nullptr;
     const float eps = plan->cfg.rms_eps;
     cudaStream_t s = as_stream(stream);
     std::string err;
-    // Attention block: h1 = x + sum_i O_i Wo_i^T with O from RMSNorm(x).
+    if (fused_mode) {
+        // RMSNorm is folded into the GEMMs: a unit-gain norm is a per-row
+        // scale, so RMSNorm(x) W^T = rsqrt(mean(x^2) + eps) * (x W^T).  The
+        // row statistic of x comes from one read-only pass, that of h1 from
+        // the o_proj epilogue (which also clears nothing: ss2 is zeroed by
+        // the first pass).
+        mark(s);
+        if ((rc = run(tpi::row_sumsq_launch(X, plan->M, (int)plan->h, ss1, ss2, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = do_qkv(plan, X, w->Wq, w->Wk, w->Wv, QKV, s, ss1))) return rc;
+        mark(s);
+        if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
+        mark(s);
+        // h1 = x + sum_i O_i Wo_i^T (g in the accumulator), and sum h1^2.
+        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s, ss2)))
+            return rc;
+        mark(s);
+        if ((rc = do_colwise(plan, h1, w->W1, w->W3, Yb, s, ss2))) return rc;
+        mark(s);
+        // y = h1 + sum_i act(xn A_i) B_i.
+        if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s))) return rc;
+        mark(s);
+        return TP_OK;
+    }
+    // PARTIALS: the t partials of each block go through HBM and the g reduce.
     mark(s);
     if ((rc = run(tpi::rmsnorm_launch(X, plan->M, (int)plan->h, eps, xn, s, &err), err))) return rc;
     mark(s);
@@ -629,30 +665,17 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     mark(s);
     if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
     mark(s);
-    if (fused) {
-        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s))) return rc;
-        mark(s);
-        if ((rc = run(tpi::rmsnorm_launch(h1, plan->M, (int)plan->h, eps, xn, s, &err), err))) return rc;
-        mark(s);
-    } else {
-        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, nullptr, P, nullptr, false, s)))
-            return rc;
-        mark(s);
-        // g of the attention block fused with the MLP's RMSNorm.
-        if ((rc = run(tpi::reduce_norm_launch(P, plan->cfg.partial_dtype == TP_F32 ? 1 : 0, (int)plan->t,
-                                              plan->M, (int)plan->h, X, h1, xn, eps, s, &err),
-                      err)))
-            return rc;
-        mark(s);
-    }
-    // MLP block: y = h1 + sum_i act(xn A_i) B_i.
+    if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, nullptr, P, nullptr, false, s)))
+        return rc;
+    mark(s);
+    // g of the attention block fused with the MLP's RMSNorm.
+    if ((rc = run(tpi::reduce_norm_launch(P, plan->cfg.partial_dtype == TP_F32 ? 1 : 0, (int)plan->t,
+                                          plan->M, (int)plan->h, X, h1, xn, eps, s, &err),
+                  err)))
+        return rc;
+    mark(s);
     if ((rc = do_colwise(plan, xn, w->W1, w->W3, Yb, s))) return rc;
     mark(s);
-    if (fused) {
-        if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s))) return rc;
-        mark(s);
-        return TP_OK;
-    }
     if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, nullptr, P, nullptr, false, s)))
         return rc;
     mark(s);

@@ -197,6 +197,37 @@ __global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict
     }
 }
 
+// Per-row sum of squares (the statistic of a unit-gain RMSNorm that the next
+// colwise GEMM applies as a per-row scale).  One warp per row; 128-bit
+// streaming loads; also clears the next norm's accumulator row.
+constexpr int SS_WARPS = 8;
+
+__global__ void __launch_bounds__(SS_WARPS * 32) row_sumsq_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                  long long rows, int h, float* ss,
+                                                                  float* zero) {
+    const long long row = static_cast<long long>(blockIdx.x) * SS_WARPS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16* xr = x + row * h;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int v = lane; v < (h >> 3); v += 32) {
+        const uint4 u = *reinterpret_cast<const uint4*>(xr + v * 8);  // kept in L2 for the GEMM
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            acc[e] = fmaf(f.x, f.x, fmaf(f.y, f.y, acc[e]));
+        }
+    }
+    float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) {
+        ss[row] = t;
+        if (zero) zero[row] = 0.0f;
+    }
+}
+
 // Failure-detection self test: wait on a barrier that never completes.
 __global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -299,6 +330,15 @@ int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaS
         nullptr, 0, n, h, reinterpret_cast<const __nv_bfloat16*>(x), nullptr,
         reinterpret_cast<__nv_bfloat16*>(y), eps);
     return check_launch("rmsnorm kernel", err);
+}
+
+int row_sumsq_launch(const void* x, int64_t rows, int h, float* ss, float* zero,
+                     cudaStream_t stream, std::string* err) {
+    if (rows == 0) return TP_OK;
+    const long long blocks = (rows + SS_WARPS - 1) / SS_WARPS;
+    row_sumsq_kernel<<<(unsigned)blocks, SS_WARPS * 32, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), rows, h, ss, zero);
+    return check_launch("row sum-of-squares kernel", err);
 }
 
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,

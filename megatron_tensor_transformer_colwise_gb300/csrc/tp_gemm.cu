@@ -91,6 +91,9 @@ struct GemmParams {
     const __nv_bfloat16* bias;
     const __nv_bfloat16* residual;
     long long ldr;
+    const float* row_ss;  // colwise: scale row by rsqrt(row_ss * inv_h + eps)
+    float* ss_out;        // ROW_FUSED: += sum of squares of the row's bf16 outputs
+    float inv_h, eps;
     unsigned* status;
     unsigned long long timeout_ns;
 };
@@ -321,6 +324,11 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         tc_fence_after();
         const int row = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
         const bool row_ok = row < p.M;
+        // Folded RMSNorm of the A rows (colwise modes): per-row scale.
+        float rs = 1.0f;
+        if (MODE != tpi::GEMM_ROW_FUSED && MODE != tpi::GEMM_ROW_PARTIAL && p.row_ss && row_ok)
+            rs = rsqrtf(p.row_ss[row] * p.inv_h + p.eps);
+        float ssq = 0.0f;
         const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
         uint32_t r[32];
         if (MODE == tpi::GEMM_COL_SWIGLU) {
@@ -342,10 +350,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float g0 = __uint_as_float(r[g * 8 + 2 * e]);
-                                const float g1 = __uint_as_float(r[g * 8 + 2 * e + 1]);
-                                const float u0 = __uint_as_float(u[g * 8 + 2 * e]);
-                                const float u1 = __uint_as_float(u[g * 8 + 2 * e + 1]);
+                                const float g0 = __uint_as_float(r[g * 8 + 2 * e]) * rs;
+                                const float g1 = __uint_as_float(r[g * 8 + 2 * e + 1]) * rs;
+                                const float u0 = __uint_as_float(u[g * 8 + 2 * e]) * rs;
+                                const float u1 = __uint_as_float(u[g * 8 + 2 * e + 1]) * rs;
                                 const float h0 = g0 / (1.0f + expf(-g0)) * u0;
                                 const float h1 = g1 / (1.0f + expf(-g1)) * u1;
                                 w[e] = pack_bf16x2(h0, h1);
@@ -385,6 +393,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                         float v[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[g * 8 + e]);
+                        if (MODE == tpi::GEMM_COL_ACT || MODE == tpi::GEMM_COL_QKV) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] *= rs;
+                        }
                         if (MODE == tpi::GEMM_COL_ACT) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
@@ -412,12 +424,23 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                                 }
                             }
                         }
-                        st_v4(out + col, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                        const uint32_t w0 = pack_bf16x2(v[0], v[1]), w1 = pack_bf16x2(v[2], v[3]);
+                        const uint32_t w2 = pack_bf16x2(v[4], v[5]), w3 = pack_bf16x2(v[6], v[7]);
+                        st_v4(out + col, w0, w1, w2, w3);
+                        if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out) {
+                            // The next norm reads the stored (bf16) values.
+                            const uint32_t ws[4] = {w0, w1, w2, w3};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = unpack_bf16x2(ws[e]);
+                                ssq = fmaf(f.x, f.x, fmaf(f.y, f.y, ssq));
+                            }
+                        }
                     }
                 }
             }
         }
+        if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out && row_ok) atomicAdd(p.ss_out + row, ssq);
         tc_fence_before();
         __syncwarp();
         // Release the accumulator: the leader's MMA waits for the epilogue
@@ -601,6 +624,10 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     p.bias = reinterpret_cast<const __nv_bfloat16*>(a.bias);
     p.residual = reinterpret_cast<const __nv_bfloat16*>(a.residual);
     p.ldr = a.ldr;
+    p.row_ss = a.row_ss;
+    p.ss_out = a.ss_out;
+    p.inv_h = a.inv_h;
+    p.eps = a.eps;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     constexpr int CG = kPairTiles;

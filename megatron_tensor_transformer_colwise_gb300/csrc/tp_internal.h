@@ -44,6 +44,13 @@ struct GemmArgs {
     const void* bias = nullptr;
     const void* residual = nullptr;
     int64_t ldr = 0;
+    // RMSNorm folded into the GEMMs (unit gain): colwise modes scale each
+    // accumulator row by rsqrt(row_ss[row] * inv_h + eps) when row_ss is set;
+    // GEMM_ROW_FUSED adds the sum of squares of each output row's bf16
+    // values to ss_out[row] when ss_out is set.
+    const float* row_ss = nullptr;
+    float* ss_out = nullptr;
+    float inv_h = 0.0f, eps = 0.0f;
     unsigned* status = nullptr;
     uint64_t timeout_ns = 2000000000ull;
 };
@@ -66,6 +73,10 @@ int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t row
                        std::string* err);
 int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaStream_t stream,
                    std::string* err);
+// ss[row] = sum_j x[row][j]^2 (fp32 over the bf16 values); zero[row] = 0
+// when zero != nullptr (clears the next norm's accumulator).
+int row_sumsq_launch(const void* x, int64_t rows, int h, float* ss, float* zero,
+                     cudaStream_t stream, std::string* err);
 
 // Attention core (tp_attn.cu).
 struct AttnArgs {

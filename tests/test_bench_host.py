@@ -14,10 +14,10 @@ from synth import SHAPES
 def test_layer_flop_model_matches_the_workload_arithmetic():
     s = SHAPES["layer"]
     parts = dict(bench.layer_kernel_flops(s))
-    assert parts["qkv_colwise_gemm"] == pytest.approx(412.3e9, rel=1e-3)
+    assert parts["qkv_colwise_gemm+norm"] == pytest.approx(412.3e9, rel=1e-3)
     assert parts["o_proj_rowwise_gemm+g"] == pytest.approx(274.9e9, rel=1e-3)
     assert parts["attention_core"] == pytest.approx(137.4e9, rel=1e-3)
-    mlp = parts["w1w3_colwise_gemm+swiglu"] + parts["w2_rowwise_gemm+g"]
+    mlp = parts["w1w3_colwise_gemm+norm+swiglu"] + parts["w2_rowwise_gemm+g"]
     assert mlp == pytest.approx(2886.2e9, rel=1e-3)
     assert bench.layer_flops(s) == pytest.approx(3710.9e9, rel=1e-3)
 
