@@ -161,7 +161,9 @@ TP_API int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes);
 TP_API int tp_plan_shard_table(tp_plan_t plan, int which, int32_t* out, int64_t cap, int64_t* n);
 
 /* Read and clear the plan's device status word (synchronises `stream`).
- * TP_OK, or TP_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up. */
+ * TP_OK; TP_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up;
+ * TP_ERR_CUDA when a kernel found its shared-memory layout does not fit its
+ * allocation and stopped without computing (its outputs are not written). */
 TP_API int tp_get_device_status(tp_plan_t plan, void* stream);
 
 /* Thread-local description of the last error (never NULL). */

@@ -449,7 +449,10 @@ int tp_get_device_status(tp_plan_t plan, void* stream) {
     if (word) {
         cudaMemsetAsync(plan->status, 0, sizeof(unsigned), s);
         cudaStreamSynchronize(s);
-        return fail(TP_ERR_DEVICE_TIMEOUT, "a device-side wait exceeded its limit (status 0x%x)", word);
+        if (word & 1u)
+            return fail(TP_ERR_DEVICE_TIMEOUT, "a device-side wait exceeded its limit (status 0x%x)", word);
+        return fail(TP_ERR_CUDA, "a kernel found its shared-memory layout does not fit (status 0x%x)",
+                    word);
     }
     return TP_OK;
 }

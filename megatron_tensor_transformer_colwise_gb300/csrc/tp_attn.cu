@@ -14,9 +14,8 @@
 // One CTA per (128 query rows, query head, sequence), 6 warps, two CTAs
 // resident per SM (256 TMEM columns and ~97 KB of shared memory each), so
 // one CTA's softmax overlaps the other's tensor-core work:
-//   warp 0      TMA: Q once, then K and V blocks of 64 keys (K in a 2-stage
-//               ring running one block ahead, V single-buffered) from the
-//               shard-blocked QKV buffer.
+//   warp 0      TMA: Q once, then K and V blocks of 64 keys (2-stage rings,
+//               K one block ahead) from the shard-blocked QKV buffer.
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 64, fp32, two
 //               TMEM buffers so S of block j+1 is computed while the softmax
 //               works on block j), then O += P V (V used as an MN-major
@@ -55,19 +54,28 @@ enum {
     B_Q_FULL = 0,
     B_K_FULL = 1,   // x2 (K ring)
     B_K_EMPTY = 3,  // x2
-    B_V_FULL = 5,   // V is single-buffered
-    B_V_EMPTY = 6,
-    B_S_FULL = 7,   // x2 (S buffers in TMEM)
-    B_S_EMPTY = 9,  // x2
-    B_P_FULL = 11,
-    B_P_EMPTY = 12,
-    B_O_FULL = 13,
-    B_DRAIN = 14,
-    NUM_BARS = 15
+    B_V_FULL = 5,   // x2 (V ring)
+    B_V_EMPTY = 7,  // x2
+    B_S_FULL = 9,   // x2 (S buffers in TMEM)
+    B_S_EMPTY = 11, // x2
+    B_P_FULL = 13,
+    B_P_EMPTY = 14,
+    B_O_FULL = 15,
+    B_DRAIN = 16,
+    NUM_BARS = 17
 };
 
+// Per-CTA dynamic shared memory when two CTAs share an SM: (228 KB - 2 x
+// 1 KB reserved) / 2.
+constexpr int TWO_CTA_SMEM = 115712;
+
 // Shared memory of one CTA (two CTAs share an SM):
-//   Q [128][d] | K ring 2 x [64][d] | V [64][d] | P [128][64] | barriers
+//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | P [128][64] | barriers
+// At d = 128 the data fills 114,840 of the 115,712 bytes two CTAs may each
+// use, leaving 872 bytes to align the data to 1024 bytes; the kernel checks
+// at run time that its layout fits the allocation (it does when the dynamic
+// shared-memory base is 1024-byte aligned) and otherwise stops with an
+// error flag, touching nothing.
 template <int D>
 struct Layout {
     static constexpr int QT = QB * D * 2;
@@ -75,9 +83,10 @@ struct Layout {
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = QT;
     static constexpr int V_OFF = K_OFF + 2 * KT;
-    static constexpr int P_OFF = V_OFF + KT;
+    static constexpr int P_OFF = V_OFF + 2 * KT;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    static constexpr int SMEM = 1024 + BAR_OFF + 8 * NUM_BARS + 16;
+    static constexpr int DATA = BAR_OFF + 8 * NUM_BARS + 16;
+    static constexpr int SMEM = DATA + 1024 <= TWO_CTA_SMEM ? DATA + 1024 : TWO_CTA_SMEM;
     static constexpr int TMEM_COLS = 2 * KB + D <= 256 ? 256 : 512;  // S0 | S1 | O
 };
 
@@ -128,6 +137,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::BAR_OFF + 8 * NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+    if (base - raw + static_cast<uint32_t>(L::DATA) > static_cast<uint32_t>(L::SMEM)) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusLayout);
+        return;  // the aligned layout does not fit: nothing was touched
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqb = (p.seq + QB - 1) / QB;
     const int qb = nqb - 1 - static_cast<int>(blockIdx.x);  // longest rows first
@@ -153,9 +166,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             mbar_init(bar(B_K_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
             mbar_init(bar(B_S_EMPTY + s), 4);
+            mbar_init(bar(B_V_FULL + s), 1);
+            mbar_init(bar(B_V_EMPTY + s), 1);
         }
-        mbar_init(bar(B_V_FULL), 1);
-        mbar_init(bar(B_V_EMPTY), 1);
         mbar_init(bar(B_P_FULL), 4);
         mbar_init(bar(B_P_EMPTY), 1);
         mbar_init(bar(B_O_FULL), 1);
@@ -178,9 +191,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // Order: Q, K0, then for each block kb: K(kb+1), V(kb).  V is single-
-        // buffered (its load waits for the previous PV), so K runs one block
-        // ahead to keep the S = Q K^T MMAs fed.
+        // Order: Q, K0, then for each block kb: K(kb+1), V(kb).  Both rings
+        // are 2-stage, so a V load waits for the PV MMA two blocks back and
+        // its latency stays off the PV critical path.
         if (lane == 0) {
             bool ok = true;
             uint32_t kissued = 0, kpar = 0, vissued = 0, vpar = 0;
@@ -188,40 +201,37 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
                 tma_load_2d(sQ + c * QBOX, &p.map_q, bar(B_Q_FULL), qcol + 64 * c, tok0 + q0);
-            auto load_k = [&](int kb) -> bool {
+            auto load_kv = [&](int kb, bool is_v) -> bool {
                 const int st = kb & 1;
                 const uint32_t ph = (kb >> 1) & 1;
-                if (!mbar_wait(bar(B_K_EMPTY + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns))
-                    return false;
-                mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KT);
+                const int e = is_v ? B_V_EMPTY : B_K_EMPTY, f = is_v ? B_V_FULL : B_K_FULL;
+                if (!mbar_wait(bar(e + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) return false;
+                mbar_arrive_expect_tx(bar(f + st), L::KT);
+                const uint32_t dst = (is_v ? sV : sK) + st * L::KT;
+                const int col = is_v ? vcol : kcol;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sK + st * L::KT + c * KBOX, &p.map_kv, bar(B_K_FULL + st),
-                                kcol + 64 * c, tok0 + kb * KB);
-                kissued |= 1u << st;
-                kpar = (kpar & ~(1u << st)) | (ph << st);
+                    tma_load_2d(dst + c * KBOX, &p.map_kv, bar(f + st), col + 64 * c, tok0 + kb * KB);
+                if (is_v) {
+                    vissued |= 1u << st;
+                    vpar = (vpar & ~(1u << st)) | (ph << st);
+                } else {
+                    kissued |= 1u << st;
+                    kpar = (kpar & ~(1u << st)) | (ph << st);
+                }
                 return true;
             };
-            ok = load_k(0);
+            ok = load_kv(0, false);
             for (int kb = 0; kb < nkb && ok; ++kb) {
-                if (kb + 1 < nkb && !(ok = load_k(kb + 1))) break;
-                const uint32_t ph = kb & 1;
-                if (!mbar_wait(bar(B_V_EMPTY), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar(B_V_FULL), L::KT);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sV + c * KBOX, &p.map_kv, bar(B_V_FULL), vcol + 64 * c, tok0 + kb * KB);
-                vissued = 1;
-                vpar = ph;
+                if (kb + 1 < nkb && !(ok = load_kv(kb + 1, false))) break;
+                ok = load_kv(kb, true);
             }
             if (!ok) {
                 drain_wait(bar(B_Q_FULL), 0);
-                for (int s = 0; s < 2; ++s)
+                for (int s = 0; s < 2; ++s) {
                     if (kissued & (1u << s)) drain_wait(bar(B_K_FULL + s), (kpar >> s) & 1u);
-                if (vissued) drain_wait(bar(B_V_FULL), vpar);
+                    if (vissued & (1u << s)) drain_wait(bar(B_V_FULL + s), (vpar >> s) & 1u);
+                }
             }
         }
     } else if (warp == 1) {
@@ -253,8 +263,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             if (ok) ok = issue_s(0);
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 if (kb + 1 < nkb && !(ok = issue_s(kb + 1))) break;
+                const int vst = kb & 1;
                 if (!mbar_wait(bar(B_P_FULL), kb & 1, abort_flag, p.status, p.timeout_ns) ||
-                    !mbar_wait(bar(B_V_FULL), kb & 1, abort_flag, p.status, p.timeout_ns)) {
+                    !mbar_wait(bar(B_V_FULL + vst), (kb >> 1) & 1, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -262,10 +273,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
                 for (int ks = 0; ks < KB / 16; ++ks) {
                     umma_bf16(tmem + 2 * KB, sdesc_sw128(sP + ks * 32),
-                              sdesc_sw128_mn(sV + ks * 16 * 128, KBOX, 1024), idesc_o,
+                              sdesc_sw128_mn(sV + vst * L::KT + ks * 16 * 128, KBOX, 1024), idesc_o,
                               (kb > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(B_V_EMPTY));
+                umma_commit(bar(B_V_EMPTY + vst));
                 umma_commit(bar(B_P_EMPTY));
             }
             if (ok) {

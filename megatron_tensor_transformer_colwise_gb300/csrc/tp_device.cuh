@@ -19,6 +19,9 @@ namespace tpk {
 // Status word bits (device side).  The host maps a non-zero word to
 // TP_ERR_DEVICE_TIMEOUT.
 constexpr unsigned kStatusTimeout = 1u;
+// A kernel found its shared-memory layout does not fit its allocation and
+// stopped before touching anything.
+constexpr unsigned kStatusLayout = 2u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
