@@ -330,6 +330,16 @@ def run_case(args):
         plan = mk(ffn=K, act="gelu")
         fn = lambda: tp.tp_rowwise_forward(plan, Y, W, None, res, None, Z, stream)
         work = gemm_flops(M, h, K)
+    elif args.case == "packed":
+        # Fused Q, K, V, gate, up projection of a single-stream block with an
+        # MLP ratio of 3 (blocks [1,1,1,3,3] x 3072), 4096 tokens, t = 4.
+        hp, Mp, tpk = 3072, 4096, 4
+        blocks = [hp, hp, hp, 3 * hp, 3 * hp]
+        X = bf((Mp, hp), 1.0, 4010)
+        Wp = bf((sum(blocks), hp), 0.02, 4011)
+        out = torch.empty(Mp, sum(blocks), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: tp.tp_packed_colwise_forward(X, Mp, hp, Wp, blocks, tpk, out, stream)
+        work = gemm_flops(Mp, sum(blocks), hp)
     elif args.case == "attn":
         kvn = max(k // t, 1)
         W = (a // t + 2 * kvn) * d
@@ -575,7 +585,8 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="tokens of the oracle sample per reference step (0 = sized to ~2 min)")
     ap.add_argument("--case", default="layer",
-                    choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce"],
+                    choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
+                             "packed"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
     ap.add_argument("--dominant-traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")

@@ -248,6 +248,36 @@ TP_API int tp_mlp_forward_noalloc(tp_plan_t plan, const tp_bf16* X, const tp_bf1
                                   const tp_bf16* W3, const tp_bf16* W2, const tp_bf16* b2,
                                   const tp_bf16* residual, tp_bf16* Z, void* stream);
 
+/* ------------------------------------------------------------ packed projections */
+
+/* Per-block shard layout of a packed projection: one Linear whose output
+ * rows pack `nblocks` logical blocks of sizes blocks[0..nblocks) (e.g. gate
+ * and up of SwiGLU as [f, f]; Q, K, V, gate, up as [h, h, h, 3h, 3h]).
+ * Every block is sharded on its own ([diff] "Fused projections": plain
+ * colwise slicing would cut across the concatenation; [trf] "패킹 전략":
+ * each rank gets the matching slice of every block), and every block must
+ * divide by t on its own, not only their sum ([diff] "제약 조건 및 검증").
+ * out[(i * nblocks + b) * 2 + {0, 1}] = first packed row and row count of
+ * block b held by shard i; *n = 2 t nblocks.  Host-only.
+ * Errors: TP_ERR_NOT_DIVISIBLE (a block), TP_ERR_INVALID_ARG (nblocks not in
+ * [1, 8], non-positive block, small capacity). */
+TP_API int tp_packed_shard_table(const int64_t* blocks, int32_t nblocks, int32_t t, int32_t* out,
+                                 int64_t cap, int64_t* n);
+
+/* Colwise projection by a packed weight, all shards in one launch:
+ * Y[:, shard block i] = X * (rows of W that shard i holds)^T, shard i's
+ * column block being the concatenation, in block order, of its per-block
+ * slices (width sum_b blocks[b] / t).  X: device [M][h]; W: device
+ * [sum blocks][h]; Y: device [M][sum blocks]; bf16, fp32 accumulation.
+ * Each blocks[b] / t must be a multiple of 64 (TP_ERR_UNSUPPORTED).
+ * A packed SwiGLU gate_up weight W13 [2f][h] needs no copy for the MLP:
+ * pass W1 = W13 and W3 = W13 + f * h to tp_colwise_forward / tp_mlp_forward
+ * (their per-shard row mapping is exactly the per-block sharding); a packed
+ * QKV weight [(a + 2k) d][h] likewise splits into Wq, Wk, Wv by offsets. */
+TP_API int tp_packed_colwise_forward(const tp_bf16* X, int64_t M, int32_t h, const tp_bf16* W,
+                                     const int64_t* blocks, int32_t nblocks, int32_t t, tp_bf16* Y,
+                                     void* stream);
+
 /* ------------------------------------------------------------ attention */
 
 /* Colwise Q/K/V projection, all shards in one launch ([wiki] "셀프 어텐션":

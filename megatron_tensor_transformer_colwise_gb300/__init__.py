@@ -29,7 +29,8 @@ __all__ = [
     "tp_plan_workspace_bytes", "tp_plan_shard_table", "tp_get_device_status", "tp_last_error",
     "tp_reduce_partials", "tp_rmsnorm", "tp_colwise_forward", "tp_rowwise_forward",
     "tp_mlp_forward", "tp_mlp_forward_noalloc", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
-    "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout", "EXPORTED",
+    "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout",
+    "tp_packed_shard_table", "tp_packed_colwise_forward", "EXPORTED",
 ]
 
 TP_OK = 0
@@ -98,6 +99,10 @@ _SIGS = {
     "tp_layer_forward_traced": [_VP, _VP, C.POINTER(TPLayerWeights), _VP, _VP, C.c_size_t, _VP,
                                 C.POINTER(C.c_void_p), C.c_int],
     "tp_selftest_wait_timeout": [_VP, C.c_uint64, _VP],
+    "tp_packed_shard_table": [C.POINTER(C.c_int64), C.c_int32, C.c_int32, C.POINTER(C.c_int32),
+                              C.c_int64, C.POINTER(C.c_int64)],
+    "tp_packed_colwise_forward": [_VP, C.c_int64, C.c_int32, _VP, C.POINTER(C.c_int64), C.c_int32,
+                                  C.c_int32, _VP, _VP],
 }
 EXPORTED = tuple(sorted(list(_SIGS) + ["tp_last_error"]))
 
@@ -303,3 +308,25 @@ def tp_layer_forward_traced(plan: Plan, X, weights, Y, workspace, ws_bytes: int,
 
 def tp_selftest_wait_timeout(plan: Plan, timeout_ns: int, stream=None) -> None:
     _call("tp_selftest_wait_timeout", plan.handle, timeout_ns, _s(stream))
+
+
+def _blocks(blocks):
+    arr = (C.c_int64 * len(blocks))(*[int(b) for b in blocks])
+    return arr, len(blocks)
+
+
+def tp_packed_shard_table(blocks, t: int):
+    """[(first packed row, rows)] per shard and block, flattened."""
+    arr, nb = _blocks(blocks)
+    n = C.c_int64(0)
+    rc = lib().tp_packed_shard_table(arr, nb, t, None, 0, C.byref(n))
+    if rc not in (TP_OK, TP_ERR_INVALID_ARG) or n.value == 0:
+        raise TPError("tp_packed_shard_table", rc, tp_last_error())
+    buf = (C.c_int32 * n.value)()
+    _call("tp_packed_shard_table", arr, nb, t, buf, n.value, C.byref(n))
+    return [buf[i] for i in range(n.value)]
+
+
+def tp_packed_colwise_forward(X, M: int, h: int, W, blocks, t: int, Y, stream=None) -> None:
+    arr, nb = _blocks(blocks)
+    _call("tp_packed_colwise_forward", _p(X), M, h, _p(W), arr, nb, t, _p(Y), _s(stream))

@@ -768,3 +768,91 @@ extern "C" int tp_mlp_forward_noalloc(tp_plan_t plan, const tp_bf16* X, const tp
     if (!fused) return do_reduce(plan, P, b2, residual, Z, plan->h, s);
     return TP_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Packed projections: one Linear packing several logical blocks along its
+// output rows; every block is sharded on its own ("Tensor 병렬성", "Fused
+// projections"; "추론을 위한 텐서 병렬성", "패킹 전략"; each block divisible by
+// t individually, "제약 조건 및 검증").
+namespace {
+
+int check_packed_blocks(const int64_t* blocks, int32_t nblocks, int32_t t) {
+    if (!blocks) return fail(TP_ERR_INVALID_ARG, "blocks is NULL");
+    if (nblocks < 1 || nblocks > tpi::kMaxPackedBlocks)
+        return fail(TP_ERR_INVALID_ARG, "nblocks must be in [1, %d]", tpi::kMaxPackedBlocks);
+    if (t < 1 || t > 64) return fail(TP_ERR_INVALID_ARG, "t must be in [1, 64]");
+    int64_t total = 0;
+    for (int b = 0; b < nblocks; ++b) {
+        if (blocks[b] <= 0) return fail(TP_ERR_INVALID_ARG, "block %d has size %lld", b, (long long)blocks[b]);
+        total += blocks[b];
+    }
+    for (int b = 0; b < nblocks; ++b)
+        if (blocks[b] % t)
+            return fail(TP_ERR_NOT_DIVISIBLE,
+                        "packed block %d (size %lld) does not divide by t = %d (each block must, "
+                        "not only their sum %lld)",
+                        b, (long long)blocks[b], t, (long long)total);
+    if (total > (int64_t)1 << 30) return fail(TP_ERR_UNSUPPORTED, "packed rows above 2^30");
+    return TP_OK;
+}
+
+}  // namespace
+
+extern "C" int tp_packed_shard_table(const int64_t* blocks, int32_t nblocks, int32_t t,
+                                     int32_t* out, int64_t cap, int64_t* n) {
+    if (!n) return fail(TP_ERR_INVALID_ARG, "n is NULL");
+    int rc;
+    if ((rc = check_packed_blocks(blocks, nblocks, t))) return rc;
+    const int64_t cnt = 2LL * t * nblocks;
+    *n = cnt;
+    if (cnt > cap || !out)
+        return fail(TP_ERR_INVALID_ARG, "table needs %lld entries, capacity %lld", (long long)cnt,
+                    (long long)cap);
+    for (int32_t i = 0; i < t; ++i) {
+        int64_t off = 0;
+        for (int32_t b = 0; b < nblocks; ++b) {
+            const int64_t w = blocks[b] / t;
+            out[(i * nblocks + b) * 2 + 0] = static_cast<int32_t>(off + i * w);
+            out[(i * nblocks + b) * 2 + 1] = static_cast<int32_t>(w);
+            off += blocks[b];
+        }
+    }
+    return TP_OK;
+}
+
+extern "C" int tp_packed_colwise_forward(const tp_bf16* X, int64_t M, int32_t h, const tp_bf16* W,
+                                         const int64_t* blocks, int32_t nblocks, int32_t t,
+                                         tp_bf16* Y, void* stream) {
+    int rc;
+    if ((rc = need_ptr(X, "X")) || (rc = need_ptr(W, "W")) || (rc = need_ptr(Y, "Y"))) return rc;
+    if (M < 1 || M > (int64_t)1 << 30) return fail(TP_ERR_INVALID_ARG, "M out of range");
+    if (h < 8 || h % 8) return fail(TP_ERR_INVALID_ARG, "h must be a positive multiple of 8");
+    if ((rc = check_packed_blocks(blocks, nblocks, t))) return rc;
+    tpi::GemmArgs g;
+    g.mode = tpi::GEMM_COL_PACKED;
+    int64_t total = 0, ws = 0;
+    for (int b = 0; b < nblocks; ++b) {
+        const int64_t w = blocks[b] / t;
+        if (w % 64)
+            return fail(TP_ERR_UNSUPPORTED,
+                        "packed block %d gives %lld rows per shard; the GPU path needs multiples of 64",
+                        b, (long long)w);
+        g.pk_w[b] = static_cast<int>(w);
+        g.pk_off[b] = total;
+        total += blocks[b];
+        ws += w;
+    }
+    g.pk_nb = nblocks;
+    g.pk_ws = ws;
+    g.M = M;
+    g.N = total;
+    g.A = X;
+    g.K = h;
+    g.t = t;
+    g.B0 = W;
+    g.B0_rows = total;
+    g.out = Y;
+    g.ldo = total;
+    std::string err;
+    return run(tpi::gemm_launch(g, as_stream(stream), &err), err);
+}

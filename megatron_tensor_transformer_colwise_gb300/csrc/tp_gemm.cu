@@ -84,6 +84,9 @@ struct GemmParams {
     int act;
     int b_rows0;       // rows of B0 (out-of-range chunks read zeros)
     int qkv_ws, qkv_qw, qkv_kvw, kv_heads, head_dim, tp;
+    int pk_nb, pk_ws;
+    int pk_w[tpi::kMaxPackedBlocks];
+    int pk_off[tpi::kMaxPackedBlocks];
     void* out;
     long long ldo;
     long long shard_stride;  // ROW_PARTIAL: elements between shard outputs
@@ -176,6 +179,20 @@ __device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, int first,
                         row[i] = kv0 + (l2 - p.qkv_kvw);
                     }
                 }
+            }
+        } else if (MODE == tpi::GEMM_COL_PACKED) {
+            // Output column -> shard, then the packed block it falls in.
+            const int col = nb * BN + c * B_CHUNK_ROWS;
+            if (col >= p.N) {
+                row[i] = p.b_rows0;  // wholly out of range: zeros
+            } else {
+                const int sh = col / p.pk_ws;
+                int l = col - sh * p.pk_ws, b = 0;
+                while (b + 1 < p.pk_nb && l >= p.pk_w[b]) {
+                    l -= p.pk_w[b];
+                    ++b;
+                }
+                row[i] = p.pk_off[b] + sh * p.pk_w[b] + l;
             }
         } else {
             row[i] = nb * BN + c * B_CHUNK_ROWS;
@@ -393,7 +410,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                         float v[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[g * 8 + e]);
-                        if (MODE == tpi::GEMM_COL_ACT || MODE == tpi::GEMM_COL_QKV) {
+                        if (MODE == tpi::GEMM_COL_ACT || MODE == tpi::GEMM_COL_QKV ||
+                            MODE == tpi::GEMM_COL_PACKED) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] *= rs;
                         }
@@ -672,6 +690,12 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         p.kv_heads = a.kv_heads;
         p.head_dim = a.head_dim;
         p.tp = a.t;
+        p.pk_nb = a.pk_nb;
+        p.pk_ws = static_cast<int>(a.pk_ws);
+        for (int b = 0; b < kMaxPackedBlocks; ++b) {
+            p.pk_w[b] = a.pk_w[b];
+            p.pk_off[b] = static_cast<int>(a.pk_off[b]);
+        }
     }
     // Tiles run in groups of group_m m-tiles sweeping all n-tiles, so a wave
     // of SM-count CTAs shares a few weight (B) tiles across many m-tiles.
@@ -687,6 +711,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         case GEMM_COL_QKV: return launch_mode<GEMM_COL_QKV, CG>(p, grid, stream, err);
         case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED, CG>(p, grid, stream, err);
         case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL, CG>(p, grid, stream, err);
+        case GEMM_COL_PACKED: return launch_mode<GEMM_COL_PACKED, CG>(p, grid, stream, err);
         default:
             if (err) *err = "unknown GEMM mode";
             return TP_ERR_INVALID_ARG;

@@ -15,8 +15,11 @@ enum GemmMode {
     GEMM_COL_SWIGLU = 1,  // colwise SiLU(X W1^T) * (X W3^T), bf16 out
     GEMM_COL_QKV = 2,     // colwise Q|K|V per shard, bf16 out
     GEMM_ROW_FUSED = 3,   // rowwise, shards summed in the accumulator, + bias + residual
-    GEMM_ROW_PARTIAL = 4  // rowwise, one [M][N] partial per shard (fp32 or bf16)
+    GEMM_ROW_PARTIAL = 4, // rowwise, one [M][N] partial per shard (fp32 or bf16)
+    GEMM_COL_PACKED = 5   // colwise from a packed weight, each block sharded on its own
 };
+
+constexpr int kMaxPackedBlocks = 8;
 
 struct GemmArgs {
     int mode = GEMM_COL_ACT;
@@ -37,6 +40,13 @@ struct GemmArgs {
     // KV rows of shard i start at kv_first(i) * d.
     int64_t qkv_ws = 0, qkv_qw = 0, qkv_kvw = 0;
     int kv_heads = 0, head_dim = 0;
+    // Packed blocks (GEMM_COL_PACKED): per-shard width and packed-row offset
+    // of each block; a shard's output slice is the concatenation of its
+    // per-block slices (pk_ws columns wide).
+    int pk_nb = 0;
+    int pk_w[kMaxPackedBlocks] = {0};
+    int64_t pk_off[kMaxPackedBlocks] = {0};
+    int64_t pk_ws = 0;
     // Output.
     void* out = nullptr;
     int64_t ldo = 0;

@@ -61,6 +61,9 @@ def lib():
                                + [_I64, C.POINTER(C.c_int64), _D]),
             "tpo_attention_rows": (C.c_int, [_I64] * 6 + [_D] * 5
                                    + [_I64, C.POINTER(C.c_int64), _D]),
+            "tpo_packed_shard_rows": (C.c_int, [C.POINTER(C.c_int64), _I64, _I64, _I64,
+                                                C.POINTER(C.c_int64)]),
+            "tpo_mlp_packed_gate_up": (C.c_int, [C.c_int] + [_I64] * 4 + [_D] * 4),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -279,3 +282,31 @@ def attention_rows(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, 
                                                           _p(Wk), _p(Wv), _p(Wo), len(r), rp,
                                                           _p(out)))
     return out
+
+
+def packed_shard_rows(blocks: Sequence[int], t: int, i: int) -> np.ndarray:
+    """Rows of a packed weight device i holds under per-block sharding."""
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64))
+    out = np.empty(max(1, int(sum(int(x) // max(t, 1) for x in blocks))), dtype=np.int64)
+    rc = lib().tpo_packed_shard_rows(b.ctypes.data_as(C.POINTER(C.c_int64)), len(b), t, i,
+                                     out.ctypes.data_as(C.POINTER(C.c_int64)))
+    _check("tpo_packed_shard_rows", rc)
+    return out[: sum(int(x) // t for x in blocks)]
+
+
+def packed_check(blocks: Sequence[int], t: int) -> int:
+    """OK, or ERR_NOT_DIVISIBLE when any packed block does not divide by t."""
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64))
+    return lib().tpo_packed_shard_rows(b.ctypes.data_as(C.POINTER(C.c_int64)), len(b), t, 0, None)
+
+
+def mlp_packed_gate_up(per_block: bool, t: int, X, Wgu, W2) -> np.ndarray:
+    """SwiGLU MLP from a packed [gate; up] weight, sharded per block (correct)
+    or by contiguous rows of the packed tensor (the misplacement)."""
+    X, Wgu, W2 = _d(X), _d(Wgu), _d(W2)
+    M, h = X.shape
+    f = Wgu.shape[0] // 2
+    Z = np.empty((M, h))
+    _check("tpo_mlp_packed_gate_up", lib().tpo_mlp_packed_gate_up(
+        1 if per_block else 0, M, h, f, t, _p(X), _p(Wgu), _p(W2), _p(Z)))
+    return Z

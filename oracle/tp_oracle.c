@@ -525,3 +525,64 @@ int tpo_attention_rows(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t
     return layer_rows_impl(batch, seq, h, a, k, d, 0, 0.0, 0, 0, X, Wq, Wk, Wv, Wo, NULL, NULL,
                            NULL, nrows, rows, out_rows);
 }
+
+/* ---------------------------------------------------------------- packed */
+
+/* Packed projections ("Tensor 병렬성", section "Fused projections"; "추론을
+ * 위한 텐서 병렬성", section "패킹 전략"): one Linear whose output rows pack
+ * nb logical blocks of sizes n_0..n_{nb-1} (e.g. gate and up of SwiGLU, or
+ * Q, K, V, gate, up).  Each block is sharded on its own: device i holds rows
+ * [off_b + i n_b / t, off_b + (i+1) n_b / t) of every block b, in block
+ * order.  Every block must divide by t ("제약 조건 및 검증": each packed block
+ * individually, not only their sum).  rows_out receives the packed-weight
+ * row indices device i holds (sum_b n_b / t entries). */
+int tpo_packed_shard_rows(const int64_t* blocks, int64_t nb, int64_t t, int64_t i,
+                          int64_t* rows_out) {
+    if (!blocks || nb <= 0 || t <= 0 || i < 0 || i >= t) return TPO_ERR_INVALID;
+    int64_t off = 0, k = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        if (blocks[b] <= 0) return TPO_ERR_INVALID;
+        if (blocks[b] % t) return TPO_ERR_NOT_DIVISIBLE;
+        const int64_t w = blocks[b] / t;
+        if (rows_out)
+            for (int64_t r = 0; r < w; ++r) rows_out[k + r] = off + i * w + r;
+        k += w;
+        off += blocks[b];
+    }
+    return TPO_OK;
+}
+
+/* SwiGLU MLP from a packed gate_up weight Wgu[2f][h] (gate rows first, then
+ * up rows: blocks [f, f]) and W2[h][f].  per_block != 0: the correct
+ * per-block sharding (device i: gate rows [i f/t, (i+1) f/t) and the same
+ * up rows, i.e. the strided interleave); per_block == 0: the naive
+ * contiguous split of the packed rows ([i 2f/t, (i+1) 2f/t)) followed by
+ * chunk(2) of each device's slice into gate and up -- the misplacement the
+ * pages warn runs but gives a wrong result.  Z = sum_i
+ * (SiLU(X G_i^T) (.) X U_i^T) W2_i^T, with W2_i the columns matching
+ * device i's gate rows. */
+int tpo_mlp_packed_gate_up(int per_block, int64_t M, int64_t h, int64_t f, int64_t t,
+                           const double* X, const double* Wgu, const double* W2, double* Z) {
+    if (M < 0 || h <= 0 || f <= 0 || t <= 0 || !X || !Wgu || !W2 || !Z) return TPO_ERR_INVALID;
+    if (f % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t w = f / t;
+    double* G = (double*)malloc(sizeof(double) * (size_t)(M * w + 1));
+    double* U = (double*)malloc(sizeof(double) * (size_t)(M * w + 1));
+    double* P = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    if (!G || !U || !P) { free(G); free(U); free(P); return TPO_ERR_NOMEM; }
+    for (int64_t e = 0; e < M * h; ++e) Z[e] = 0.0;
+    for (int64_t i = 0; i < t; ++i) {
+        const int64_t g0 = per_block ? i * w : i * 2 * w;       /* first gate row */
+        const int64_t u0 = per_block ? f + i * w : i * 2 * w + w; /* first up row */
+        /* W2 columns matching the gate rows the device holds (for the naive
+         * split this is the column block the device would be given). */
+        const int64_t c0 = per_block ? i * w : (i * 2 * w) % f;
+        tpo_linear(X, h, Wgu + g0 * h, h, M, w, h, G, w);
+        tpo_linear(X, h, Wgu + u0 * h, h, M, w, h, U, w);
+        for (int64_t e = 0; e < M * w; ++e) G[e] = tpo_silu(G[e]) * U[e];
+        tpo_linear(G, w, W2 + c0, f, M, h, w, P, h);
+        for (int64_t e = 0; e < M * h; ++e) Z[e] += P[e];
+    }
+    free(G); free(U); free(P);
+    return TPO_OK;
+}

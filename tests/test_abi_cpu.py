@@ -129,3 +129,28 @@ def test_entry_points_reject_null_plan_without_touching_a_gpu():
     assert L.tp_layer_forward(None, None, None, None, None, 0, None) == tp.TP_ERR_INVALID_ARG
     assert L.tp_reduce_partials(None, 0, 4, 64, 8, None, None, None, None) == tp.TP_ERR_INVALID_ARG
     assert L.tp_plan_create(None, None) == tp.TP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("blocks,t", [([4, 4], 2), ([256, 256], 4), ([192, 192, 192, 576, 576], 3),
+                                      ([64], 1), ([128, 64, 64], 8)])
+def test_packed_shard_table_bit_exact_vs_oracle(blocks, t):
+    if any(b % t for b in blocks):
+        pytest.skip("not divisible")
+    table = tp.tp_packed_shard_table(blocks, t)
+    nb = len(blocks)
+    for i in range(t):
+        rows = []
+        for b in range(nb):
+            first, count = table[(i * nb + b) * 2], table[(i * nb + b) * 2 + 1]
+            rows.extend(range(first, first + count))
+        assert rows == oracle.packed_shard_rows(blocks, t, i).tolist()
+
+
+def test_packed_shard_table_rejects_blocks_not_divisible_individually():
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_packed_shard_table([6, 2], 4)
+    assert e.value.code == tp.TP_ERR_NOT_DIVISIBLE
+    assert "each block" in tp.tp_last_error()
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_packed_shard_table([4] * 9, 2)
+    assert e.value.code == tp.TP_ERR_INVALID_ARG

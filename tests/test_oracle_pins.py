@@ -385,3 +385,44 @@ def test_layer_matches_composed_torch_reference_and_sharded_form():
     rows = [0, 5, 6, 11, 7]
     Yr = oracle.layer_rows(*dims, X, *W, rows)
     assert np.abs(Yr - Y[rows]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- packed projections
+
+def test_packed_shard_rows_match_golden_and_differ_from_contiguous():
+    for line in open(os.path.join(GOLDEN, "packed_gate_up_f4_t2.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        left, right = line.split("|")
+        shard, *rows = (int(v) for v in left.split())
+        contiguous = [int(v) for v in right.split()]
+        got = oracle.packed_shard_rows([4, 4], 2, shard).tolist()
+        assert got == rows
+        assert got != contiguous
+
+
+def test_packed_blocks_must_divide_individually():
+    assert oracle.packed_check([8, 8], 4) == oracle.OK
+    assert oracle.packed_check([6, 2], 4) == oracle.ERR_NOT_DIVISIBLE   # sum 8 divides, blocks do not
+    assert oracle.packed_check([3072, 3072, 3072, 9216, 9216], 4) == oracle.OK
+    assert oracle.packed_check([3072, 3072, 3072, 9216, 9216], 5) == oracle.ERR_NOT_DIVISIBLE
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_packed_gate_up_per_block_equals_unpacked_and_contiguous_does_not(t):
+    torch.manual_seed(21 + t)
+    M, h, f = 5, 16, 32
+    X = torch.randn(M, h, dtype=torch.float64)
+    Wg = torch.randn(f, h, dtype=torch.float64) * 0.5
+    Wu = torch.randn(f, h, dtype=torch.float64) * 0.5
+    W2 = torch.randn(h, f, dtype=torch.float64) * 0.5
+    Wgu = torch.cat([Wg, Wu], 0)
+    ref = oracle.mlp("swiglu", X.numpy(), Wg.numpy(), W2.numpy(), Wu.numpy())
+    good = oracle.mlp_packed_gate_up(True, t, X.numpy(), Wgu.numpy(), W2.numpy())
+    assert np.abs(good - ref).max() <= 1e-12 * np.abs(ref).max()
+    bad = oracle.mlp_packed_gate_up(False, t, X.numpy(), Wgu.numpy(), W2.numpy())
+    if t == 1:
+        assert np.abs(bad - ref).max() <= 1e-12 * np.abs(ref).max()   # nothing to mix at t = 1
+    else:
+        assert np.abs(bad - ref).max() > 1e-2 * np.abs(ref).max()     # runs, but wrong
