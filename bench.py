@@ -340,6 +340,30 @@ def run_case(args):
         out = torch.empty(Mp, sum(blocks), dtype=torch.bfloat16, device="cuda")
         fn = lambda: tp.tp_packed_colwise_forward(X, Mp, hp, Wp, blocks, tpk, out, stream)
         work = gemm_flops(Mp, sum(blocks), hp)
+    elif args.case in ("vocab_logits", "vocab_ce", "embedding"):
+        # Llama-3-sized output layer / embedding: 8192 tokens, h = 4096,
+        # v = 128256, vocab split t = 8.
+        Mv, hv, vv, tv = 8192, 4096, 128256, 8
+        if args.case == "vocab_logits":
+            Hn, Wn = bf((Mv, hv), 1.0, 4100), bf((vv, hv), 0.02, 4101)
+            logits = torch.empty(Mv, vv, dtype=torch.bfloat16, device="cuda")
+            fn = lambda: tp.tp_vocab_logits_forward(Hn, Mv, hv, Wn, vv, tv, logits, stream)
+            work = gemm_flops(Mv, vv, hv)
+        elif args.case == "vocab_ce":
+            logits = bf((Mv, vv), 3.0, 4103)
+            labels = torch.randint(0, vv, (Mv,), dtype=torch.int32, device="cuda")
+            stats = torch.empty(3 * tv * Mv, dtype=torch.float32, device="cuda")
+            loss = torch.empty(Mv, dtype=torch.float32, device="cuda")
+            fn = lambda: tp.tp_vocab_parallel_cross_entropy(logits, Mv, vv, tv, labels, stats, loss,
+                                                            stream)
+            # logits read once; the exchanged statistics and the loss are small
+            work, unit, peak = Mv * vv * 2 + 3 * tv * Mv * 4 * 2 + Mv * 8, "GB/s", peaks["hbm_gbs"]
+        else:
+            E = bf((vv, hv), 1.0, 4104)
+            ids = torch.randint(0, vv, (Mv,), dtype=torch.int32, device="cuda")
+            out = torch.empty(Mv, hv, dtype=torch.bfloat16, device="cuda")
+            fn = lambda: tp.tp_vocab_embedding_forward(ids, Mv, E, vv, hv, tv, out, stream)
+            work, unit, peak = 2 * Mv * hv * 2 + Mv * 4, "GB/s", peaks["hbm_gbs"]
     elif args.case == "attn":
         kvn = max(k // t, 1)
         W = (a // t + 2 * kvn) * d
@@ -586,7 +610,7 @@ def main(argv=None):
                     help="tokens of the oracle sample per reference step (0 = sized to ~2 min)")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
-                             "packed"],
+                             "packed", "vocab_logits", "vocab_ce", "embedding"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
     ap.add_argument("--dominant-traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")

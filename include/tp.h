@@ -278,6 +278,40 @@ TP_API int tp_packed_colwise_forward(const tp_bf16* X, int64_t M, int32_t h, con
                                      const int64_t* blocks, int32_t nblocks, int32_t t, tp_bf16* Y,
                                      void* stream);
 
+/* ------------------------------------------------------------ vocabulary */
+
+/* Vocab-parallel embedding lookup ([wiki] "임베딩과 출력층": the embedding
+ * matrix is split along the vocabulary; [trf] "분할 전략":
+ * EmbeddingParallel(shard_dim=0) all-reduces the partial lookups).  Shard i
+ * holds rows [i v/t, (i+1) v/t) of E; its partial for an id is E[id] if it
+ * owns the id, else zero, so out[m] = E[ids[m]] (a zero row when
+ * ids[m] is outside [0, v): no shard owns it).  ids: device [M] int32;
+ * E: device [v][h] bf16 (nn.Embedding rows); out: device [M][h] bf16.
+ * Errors: TP_ERR_NOT_DIVISIBLE when t does not divide v. */
+TP_API int tp_vocab_embedding_forward(const int32_t* ids, int64_t M, const tp_bf16* E, int64_t v,
+                                      int32_t h, int32_t t, tp_bf16* out, void* stream);
+
+/* Vocab-parallel output projection: logits[M][v] = H W^T with W [v][h]
+ * split by rows (colwise over the vocabulary), all shards in one launch;
+ * shard i's logits are columns [i v/t, (i+1) v/t).  bf16 in and out, fp32
+ * accumulation.  (v / t) % 8 == 0. */
+TP_API int tp_vocab_logits_forward(const tp_bf16* H, int64_t M, int32_t h, const tp_bf16* W,
+                                   int64_t v, int32_t t, tp_bf16* logits, void* stream);
+
+/* Cross-entropy from vocab-sharded logits, exchanging only per-token
+ * statistics ([wiki] "임베딩과 출력층": the max and the sum, b x s values,
+ * instead of the b x s x v logits).  Shard i (columns [i v/t, (i+1) v/t) of
+ * logits) computes m_i = max z, s_i = sum exp(z - m_i) and y_i = z_label if
+ * it owns the label (else 0) into stats[3][t][M] (fp32: the exchanged
+ * values); then loss[m] = log(sum_i s_i exp(m_i - m)) + m - sum_i y_i with
+ * m = max_i m_i.  labels: device [M] int32, -100 = ignored (loss 0), any
+ * other value outside [0, v) gives NaN.  logits: device [M][v] bf16;
+ * stats: device [3 t M] fp32 (caller-owned scratch); loss: device [M] fp32.
+ * (v / t) % 8 == 0. */
+TP_API int tp_vocab_parallel_cross_entropy(const tp_bf16* logits, int64_t M, int64_t v, int32_t t,
+                                           const int32_t* labels, float* stats, float* loss,
+                                           void* stream);
+
 /* ------------------------------------------------------------ attention */
 
 /* Colwise Q/K/V projection, all shards in one launch ([wiki] "셀프 어텐션":

@@ -30,7 +30,8 @@ __all__ = [
     "tp_reduce_partials", "tp_rmsnorm", "tp_colwise_forward", "tp_rowwise_forward",
     "tp_mlp_forward", "tp_mlp_forward_noalloc", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
     "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout",
-    "tp_packed_shard_table", "tp_packed_colwise_forward", "EXPORTED",
+    "tp_packed_shard_table", "tp_packed_colwise_forward", "tp_vocab_embedding_forward",
+    "tp_vocab_logits_forward", "tp_vocab_parallel_cross_entropy", "EXPORTED",
 ]
 
 TP_OK = 0
@@ -103,6 +104,9 @@ _SIGS = {
                               C.c_int64, C.POINTER(C.c_int64)],
     "tp_packed_colwise_forward": [_VP, C.c_int64, C.c_int32, _VP, C.POINTER(C.c_int64), C.c_int32,
                                   C.c_int32, _VP, _VP],
+    "tp_vocab_embedding_forward": [_VP, C.c_int64, _VP, C.c_int64, C.c_int32, C.c_int32, _VP, _VP],
+    "tp_vocab_logits_forward": [_VP, C.c_int64, C.c_int32, _VP, C.c_int64, C.c_int32, _VP, _VP],
+    "tp_vocab_parallel_cross_entropy": [_VP, C.c_int64, C.c_int64, C.c_int32, _VP, _VP, _VP, _VP],
 }
 EXPORTED = tuple(sorted(list(_SIGS) + ["tp_last_error"]))
 
@@ -330,3 +334,17 @@ def tp_packed_shard_table(blocks, t: int):
 def tp_packed_colwise_forward(X, M: int, h: int, W, blocks, t: int, Y, stream=None) -> None:
     arr, nb = _blocks(blocks)
     _call("tp_packed_colwise_forward", _p(X), M, h, _p(W), arr, nb, t, _p(Y), _s(stream))
+
+
+def tp_vocab_embedding_forward(ids, M: int, E, v: int, h: int, t: int, out, stream=None) -> None:
+    _call("tp_vocab_embedding_forward", _p(ids), M, _p(E), v, h, t, _p(out), _s(stream))
+
+
+def tp_vocab_logits_forward(H, M: int, h: int, W, v: int, t: int, logits, stream=None) -> None:
+    _call("tp_vocab_logits_forward", _p(H), M, h, _p(W), v, t, _p(logits), _s(stream))
+
+
+def tp_vocab_parallel_cross_entropy(logits, M: int, v: int, t: int, labels, stats, loss,
+                                    stream=None) -> None:
+    _call("tp_vocab_parallel_cross_entropy", _p(logits), M, v, t, _p(labels), _p(stats), _p(loss),
+          _s(stream))

@@ -856,3 +856,68 @@ extern "C" int tp_packed_colwise_forward(const tp_bf16* X, int64_t M, int32_t h,
     std::string err;
     return run(tpi::gemm_launch(g, as_stream(stream), &err), err);
 }
+
+// ---------------------------------------------------------------------------
+// Vocabulary parallelism ("텐서 병렬화", "임베딩과 출력층").
+namespace {
+
+int check_vocab(int64_t M, int64_t v, int32_t t, int64_t align) {
+    if (M < 0 || M > (int64_t)1 << 31) return fail(TP_ERR_INVALID_ARG, "M out of range");
+    if (t < 1 || t > 64) return fail(TP_ERR_INVALID_ARG, "t must be in [1, 64]");
+    if (v < 1 || v > (int64_t)1 << 31) return fail(TP_ERR_INVALID_ARG, "v out of range");
+    if (v % t) return fail(TP_ERR_NOT_DIVISIBLE, "t = %d does not divide the vocabulary v = %lld", t,
+                           (long long)v);
+    if ((v / t) % align)
+        return fail(TP_ERR_INVALID_ARG, "v / t = %lld must be a multiple of %lld",
+                    (long long)(v / t), (long long)align);
+    return TP_OK;
+}
+
+}  // namespace
+
+extern "C" int tp_vocab_embedding_forward(const int32_t* ids, int64_t M, const tp_bf16* E, int64_t v,
+                                          int32_t h, int32_t t, tp_bf16* out, void* stream) {
+    int rc;
+    if ((rc = need_ptr(ids, "ids")) || (rc = need_ptr(E, "E")) || (rc = need_ptr(out, "out"))) return rc;
+    if ((rc = check_vocab(M, v, t, 1))) return rc;
+    if (h < 8 || h % 8) return fail(TP_ERR_INVALID_ARG, "h must be a positive multiple of 8");
+    std::string err;
+    return run(tpi::vocab_embedding_launch(ids, M, E, v, h, out, as_stream(stream), &err), err);
+}
+
+extern "C" int tp_vocab_logits_forward(const tp_bf16* H, int64_t M, int32_t h, const tp_bf16* W,
+                                       int64_t v, int32_t t, tp_bf16* logits, void* stream) {
+    int rc;
+    if ((rc = need_ptr(H, "H")) || (rc = need_ptr(W, "W")) || (rc = need_ptr(logits, "logits"))) return rc;
+    if ((rc = check_vocab(M, v, t, 8))) return rc;
+    if (M < 1) return fail(TP_ERR_INVALID_ARG, "M must be >= 1");
+    if (h < 8 || h % 8) return fail(TP_ERR_INVALID_ARG, "h must be a positive multiple of 8");
+    // Colwise over the vocabulary: shard i's logits are columns [i v/t,
+    // (i+1) v/t) of one [M][v] result (its slice of W's rows).
+    tpi::GemmArgs g;
+    g.mode = tpi::GEMM_COL_ACT;
+    g.act = TP_ACT_NONE;
+    g.M = M;
+    g.N = v;
+    g.A = H;
+    g.K = h;
+    g.t = t;
+    g.B0 = W;
+    g.B0_rows = v;
+    g.out = logits;
+    g.ldo = v;
+    std::string err;
+    return run(tpi::gemm_launch(g, as_stream(stream), &err), err);
+}
+
+extern "C" int tp_vocab_parallel_cross_entropy(const tp_bf16* logits, int64_t M, int64_t v,
+                                               int32_t t, const int32_t* labels, float* stats,
+                                               float* loss, void* stream) {
+    int rc;
+    if ((rc = need_ptr(logits, "logits")) || (rc = need_ptr(labels, "labels")) ||
+        (rc = need_ptr(stats, "stats")) || (rc = need_ptr(loss, "loss")))
+        return rc;
+    if ((rc = check_vocab(M, v, t, 8))) return rc;
+    std::string err;
+    return run(tpi::vocab_ce_launch(logits, M, v, t, labels, stats, loss, as_stream(stream), &err), err);
+}

@@ -101,6 +101,12 @@ struct AttnArgs {
 };
 int attn_launch(const AttnArgs& a, cudaStream_t stream, std::string* err);
 
+// Vocabulary-parallel embedding and cross-entropy (tp_vocab.cu).
+int vocab_embedding_launch(const int32_t* ids, int64_t M, const void* E, int64_t v, int h, void* out,
+                           cudaStream_t stream, std::string* err);
+int vocab_ce_launch(const void* logits, int64_t M, int64_t v, int t, const int32_t* labels,
+                    float* stats, float* loss, cudaStream_t stream, std::string* err);
+
 // Self test: a kernel that waits on a barrier nobody arrives at.
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,
                             std::string* err);

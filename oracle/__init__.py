@@ -64,6 +64,10 @@ def lib():
             "tpo_packed_shard_rows": (C.c_int, [C.POINTER(C.c_int64), _I64, _I64, _I64,
                                                 C.POINTER(C.c_int64)]),
             "tpo_mlp_packed_gate_up": (C.c_int, [C.c_int] + [_I64] * 4 + [_D] * 4),
+            "tpo_embedding_vocab_parallel": (C.c_int, [_I64] * 4 + [C.POINTER(C.c_int32), _D, _D]),
+            "tpo_cross_entropy": (C.c_int, [_I64, _I64, _D, C.POINTER(C.c_int32), _D]),
+            "tpo_cross_entropy_vocab_parallel": (C.c_int, [_I64] * 3 + [_D, C.POINTER(C.c_int32),
+                                                                        _D, _D]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -310,3 +314,40 @@ def mlp_packed_gate_up(per_block: bool, t: int, X, Wgu, W2) -> np.ndarray:
     _check("tpo_mlp_packed_gate_up", lib().tpo_mlp_packed_gate_up(
         1 if per_block else 0, M, h, f, t, _p(X), _p(Wgu), _p(W2), _p(Z)))
     return Z
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def embedding_vocab_parallel(t: int, ids, E) -> np.ndarray:
+    """Sum over devices of the masked partial lookups of a vocab-split E[v][h]."""
+    ids, E = _i32(ids).ravel(), _d(E)
+    v, h = E.shape
+    out = np.empty((len(ids), h))
+    _check("tpo_embedding_vocab_parallel", lib().tpo_embedding_vocab_parallel(
+        len(ids), v, h, t, ids.ctypes.data_as(C.POINTER(C.c_int32)), _p(E), _p(out)))
+    return out
+
+
+def cross_entropy(logits, labels) -> np.ndarray:
+    """Per-token log-sum-exp minus the label's logit (ignore index -100 -> 0)."""
+    z, lab = _d(logits), _i32(labels).ravel()
+    M, v = z.shape
+    loss = np.empty(M)
+    _check("tpo_cross_entropy", lib().tpo_cross_entropy(
+        M, v, _p(z), lab.ctypes.data_as(C.POINTER(C.c_int32)), _p(loss)))
+    return loss
+
+
+def cross_entropy_vocab_parallel(t: int, logits, labels, want_stats: bool = False):
+    """loss_parallel: per-device (max, sum, target) exchanged, then combined."""
+    z, lab = _d(logits), _i32(labels).ravel()
+    M, v = z.shape
+    loss = np.empty(M)
+    st = np.empty((3, t, M)) if want_stats else None
+    _check("tpo_cross_entropy_vocab_parallel", lib().tpo_cross_entropy_vocab_parallel(
+        M, v, t, _p(z), lab.ctypes.data_as(C.POINTER(C.c_int32)), _p(st), _p(loss)))
+    return (loss, st) if want_stats else loss

@@ -586,3 +586,89 @@ int tpo_mlp_packed_gate_up(int per_block, int64_t M, int64_t h, int64_t f, int64
     free(G); free(U); free(P);
     return TPO_OK;
 }
+
+/* ---------------------------------------------------------------- vocabulary */
+
+/* Vocab-parallel embedding ("텐서 병렬화", section "임베딩과 출력층": the
+ * embedding matrix is split along the vocabulary; "추론을 위한 텐서 병렬성",
+ * "분할 전략": EmbeddingParallel(shard_dim=0) looks up each rank's partial
+ * and all-reduces them).  E[v][h] (nn.Embedding rows); device i holds rows
+ * [i v/t, (i+1) v/t); its partial for token id is E[id] if the id is in its
+ * range, else zeros; out = sum of the t partials (i ascending).  An id
+ * outside [0, v) is in no device's range, so its row is zero. */
+int tpo_embedding_vocab_parallel(int64_t M, int64_t v, int64_t h, int64_t t, const int32_t* ids,
+                                 const double* E, double* out) {
+    if (M < 0 || v <= 0 || h <= 0 || t <= 0 || !ids || !E || !out) return TPO_ERR_INVALID;
+    if (v % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t w = v / t;
+    for (int64_t e = 0; e < M * h; ++e) out[e] = 0.0;
+    for (int64_t i = 0; i < t; ++i)
+        for (int64_t m = 0; m < M; ++m) {
+            const int64_t id = ids[m];
+            if (id < i * w || id >= (i + 1) * w) continue; /* masked: zero partial */
+            for (int64_t j = 0; j < h; ++j) out[m * h + j] += E[id * h + j];
+        }
+    return TPO_OK;
+}
+
+/* Cross-entropy of one row of logits, the plain definition:
+ * loss = log(sum_j exp(z_j)) - z_label, computed with the max subtracted. */
+int tpo_cross_entropy(int64_t M, int64_t v, const double* logits, const int32_t* labels,
+                      double* loss) {
+    if (M < 0 || v <= 0 || !logits || !labels || !loss) return TPO_ERR_INVALID;
+    for (int64_t m = 0; m < M; ++m) {
+        const double* z = logits + m * v;
+        if (labels[m] == -100) { loss[m] = 0.0; continue; } /* ignored position */
+        if (labels[m] < 0 || labels[m] >= v) { loss[m] = NAN; continue; }
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < v; ++j) if (z[j] > mx) mx = z[j];
+        double s = 0.0;
+        for (int64_t j = 0; j < v; ++j) s += exp(z[j] - mx);
+        loss[m] = log(s) + mx - z[labels[m]];
+    }
+    return TPO_OK;
+}
+
+/* loss_parallel ("텐서 병렬화", "임베딩과 출력층": instead of gathering the
+ * b x s x v logits, each device computes the cross-entropy terms from its own
+ * partial logits and only the max and the sum are exchanged, so the traffic
+ * is b x s).  Device i holds logits columns [i v/t, (i+1) v/t) and computes
+ *   m_i = max_j z_j,  s_i = sum_j exp(z_j - m_i),  y_i = z_label if it owns it
+ * The exchange: m = max_i m_i,  s = sum_i s_i exp(m_i - m),  y = sum_i y_i,
+ * and loss = log(s) + m - y.  stats (nullable) receives [3][t][M]
+ * (m_i, s_i, y_i): the only values that cross devices. */
+int tpo_cross_entropy_vocab_parallel(int64_t M, int64_t v, int64_t t, const double* logits,
+                                     const int32_t* labels, double* stats, double* loss) {
+    if (M < 0 || v <= 0 || t <= 0 || !logits || !labels || !loss) return TPO_ERR_INVALID;
+    if (v % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t w = v / t;
+    double* st = (double*)malloc(sizeof(double) * (size_t)(3 * t * M + 1));
+    if (!st) return TPO_ERR_NOMEM;
+    for (int64_t i = 0; i < t; ++i)
+        for (int64_t m = 0; m < M; ++m) {
+            const double* z = logits + m * v + i * w;
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < w; ++j) if (z[j] > mx) mx = z[j];
+            double s = 0.0;
+            for (int64_t j = 0; j < w; ++j) s += exp(z[j] - mx);
+            const int64_t lab = labels[m];
+            st[(0 * t + i) * M + m] = mx;
+            st[(1 * t + i) * M + m] = s;
+            st[(2 * t + i) * M + m] = (lab >= i * w && lab < (i + 1) * w) ? z[lab - i * w] : 0.0;
+        }
+    for (int64_t m = 0; m < M; ++m) {
+        if (labels[m] == -100) { loss[m] = 0.0; continue; }
+        if (labels[m] < 0 || labels[m] >= v) { loss[m] = NAN; continue; }
+        double mx = -INFINITY;
+        for (int64_t i = 0; i < t; ++i) if (st[(0 * t + i) * M + m] > mx) mx = st[(0 * t + i) * M + m];
+        double s = 0.0, y = 0.0;
+        for (int64_t i = 0; i < t; ++i) {
+            s += st[(1 * t + i) * M + m] * exp(st[(0 * t + i) * M + m] - mx);
+            y += st[(2 * t + i) * M + m];
+        }
+        loss[m] = log(s) + mx - y;
+    }
+    if (stats) memcpy(stats, st, sizeof(double) * (size_t)(3 * t * M));
+    free(st);
+    return TPO_OK;
+}

@@ -426,3 +426,58 @@ def test_packed_gate_up_per_block_equals_unpacked_and_contiguous_does_not(t):
         assert np.abs(bad - ref).max() <= 1e-12 * np.abs(ref).max()   # nothing to mix at t = 1
     else:
         assert np.abs(bad - ref).max() > 1e-2 * np.abs(ref).max()     # runs, but wrong
+
+
+# ---------------------------------------------------------------- vocabulary parallelism
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_vocab_parallel_embedding_is_the_gather(t):
+    rng = np.random.default_rng(31 + t)
+    v, h = 64, 12
+    E = rng.normal(size=(v, h))
+    ids = rng.integers(0, v, size=40).astype(np.int32)
+    ids[[3, 7]] = [-1, v]              # no device owns these ids
+    out = oracle.embedding_vocab_parallel(t, ids, E)
+    want = np.where(((ids >= 0) & (ids < v))[:, None], E[np.clip(ids, 0, v - 1)], 0.0)
+    assert np.array_equal(out, want)
+
+
+def test_cross_entropy_matches_torch_and_closed_forms():
+    rng = np.random.default_rng(5)
+    z = rng.normal(size=(9, 40)) * 4
+    lab = rng.integers(0, 40, size=9).astype(np.int32)
+    lab[2] = -100
+    got = oracle.cross_entropy(z, lab)
+    want = F.cross_entropy(torch.tensor(z), torch.tensor(lab, dtype=torch.long),
+                           reduction="none", ignore_index=-100).numpy()
+    assert np.abs(got - want).max() < 1e-12
+    # equal logits: every class has probability 1/v
+    assert np.allclose(oracle.cross_entropy(np.zeros((3, 40)), np.array([0, 5, 39], np.int32)),
+                       np.log(40.0), atol=1e-14)
+    # a huge margin on the label: loss -> 0; on another class: loss -> margin
+    zz = np.zeros((2, 10))
+    zz[0, 3] = 50.0
+    zz[1, 4] = 50.0
+    l2 = oracle.cross_entropy(zz, np.array([3, 3], np.int32))
+    assert l2[0] == pytest.approx(9 * np.exp(-50.0), abs=1e-18)
+    assert l2[1] == pytest.approx(50.0, rel=1e-12)
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 5, 8])
+def test_vocab_parallel_cross_entropy_equals_plain(t):
+    rng = np.random.default_rng(40 + t)
+    M, v = 11, 40
+    z = rng.normal(size=(M, v)) * 6
+    lab = rng.integers(0, v, size=M).astype(np.int32)
+    lab[0] = -100
+    plain = oracle.cross_entropy(z, lab)
+    par, st = oracle.cross_entropy_vocab_parallel(t, z, lab, want_stats=True)
+    assert np.abs(par - plain).max() < 1e-12
+    # Only 3 numbers per token and device cross devices; their max is the row max.
+    assert st.shape == (3, t, M)
+    assert np.array_equal(st[0].max(0), z.max(1))
+    w = v // t
+    owner = lab // w
+    for m in range(1, M):
+        assert st[2, owner[m], m] == z[m, lab[m]]
+        assert np.count_nonzero(st[2, :, m]) <= 1
