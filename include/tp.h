@@ -121,6 +121,9 @@ typedef struct {
     int32_t reduce_mode;   /* TP_REDUCE_*                                     */
     int32_t partial_dtype; /* TP_F32 or TP_BF16 (PARTIALS mode only)          */
     float rms_eps;         /* RMSNorm epsilon (layer only), > 0               */
+    int32_t sequence_parallel; /* 1: layer in/out in the sequence-split layout
+                                  [t][batch][seq/t][h] (needs t | seq and
+                                  TP_REDUCE_PARTIALS); 0: replicated [M][h]   */
 } tp_config;
 
 /* Weights of one layer, all full nn.Linear matrices [out][in] in bf16:
@@ -278,6 +281,30 @@ TP_API int tp_packed_colwise_forward(const tp_bf16* X, int64_t M, int32_t h, con
                                      const int64_t* blocks, int32_t nblocks, int32_t t, tp_bf16* Y,
                                      void* stream);
 
+/* ------------------------------------------------------------ sequence parallelism */
+
+/* Sequence-split layout ([wiki] "시퀀스 병렬화": the norm and dropout regions
+ * are split along the sequence; entering the tensor-parallel region an
+ * all-gather collects the sequence, leaving it a reduce-scatter sums the
+ * partials and splits them along the sequence again, the same traffic as
+ * the all-reduce; [wiki] "PyTorch로 쓰기": SequenceParallel on the norms,
+ * Shard(1) outputs).  A sequence-split tensor is [t][batch][seq/t][h]:
+ * piece i holds positions [i seq/t, (i+1) seq/t) of every sequence.
+ *
+ * All-gather: full[b seq + pos] = sp[piece(pos)][b][pos % (seq/t)].
+ * sp, full: device bf16, [batch seq][h]; t | seq, h % 8 == 0. */
+TP_API int tp_sp_all_gather(const tp_bf16* sp, int32_t batch, int32_t seq, int32_t t, int32_t h,
+                            tp_bf16* full, void* stream);
+
+/* Reduce-scatter of the t shard partials (token order, [t][batch seq][h],
+ * TP_F32 or TP_BF16) into the sequence-split layout, plus the sequence-split
+ * residual: out_sp = sum_i partials[i] (+ residual_sp), fp32 sums in shard
+ * order, bf16 out.  xn_sp (nullable): also RMSNorm(out_sp) with unit gain
+ * and `eps` (the next block's local norm, fused).  h <= 8192. */
+TP_API int tp_sp_reduce_scatter(const void* partials, int partial_dtype, int32_t t, int32_t batch,
+                                int32_t seq, int32_t h, const tp_bf16* residual_sp, tp_bf16* out_sp,
+                                tp_bf16* xn_sp, float eps, void* stream);
+
 /* ------------------------------------------------------------ vocabulary */
 
 /* Vocab-parallel embedding lookup ([wiki] "임베딩과 출력층": the embedding
@@ -341,6 +368,9 @@ TP_API int tp_attn_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, 
 /* One pre-norm layer with two g reductions ([wiki] "통신 연산 f와 g": one
  * all-reduce after attention and one after the MLP; norm and residual
  * replicated):  h1 = x + Attn(RMSNorm(x)),  y = h1 + MLP(RMSNorm(h1)).
+ * With cfg.sequence_parallel = 1, X and Y are in the sequence-split layout
+ * and every g is a reduce-scatter fused with the next local norm, every
+ * block input an all-gather ([wiki] "시퀀스 병렬화").
  * X, Y: device [M][h] bf16 (may not alias).  Requires act == TP_ACT_SWIGLU
  * or a GeLU form (W3 NULL then).  workspace >= tp_plan_workspace_bytes(
  * TP_OP_LAYER); in PARTIALS mode it also holds the [t][M][h] partials. */

@@ -31,7 +31,8 @@ __all__ = [
     "tp_mlp_forward", "tp_mlp_forward_noalloc", "tp_qkv_forward", "tp_attn_core_forward", "tp_attn_forward",
     "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout",
     "tp_packed_shard_table", "tp_packed_colwise_forward", "tp_vocab_embedding_forward",
-    "tp_vocab_logits_forward", "tp_vocab_parallel_cross_entropy", "EXPORTED",
+    "tp_vocab_logits_forward", "tp_vocab_parallel_cross_entropy", "tp_sp_all_gather",
+    "tp_sp_reduce_scatter", "EXPORTED",
 ]
 
 TP_OK = 0
@@ -70,6 +71,7 @@ class TPConfig(C.Structure):
         ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
         ("tp_degree", C.c_int32), ("act", C.c_int32), ("reduce_mode", C.c_int32),
         ("partial_dtype", C.c_int32), ("rms_eps", C.c_float),
+        ("sequence_parallel", C.c_int32),
     ]
 
 
@@ -107,6 +109,9 @@ _SIGS = {
     "tp_vocab_embedding_forward": [_VP, C.c_int64, _VP, C.c_int64, C.c_int32, C.c_int32, _VP, _VP],
     "tp_vocab_logits_forward": [_VP, C.c_int64, C.c_int32, _VP, C.c_int64, C.c_int32, _VP, _VP],
     "tp_vocab_parallel_cross_entropy": [_VP, C.c_int64, C.c_int64, C.c_int32, _VP, _VP, _VP, _VP],
+    "tp_sp_all_gather": [_VP, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _VP, _VP],
+    "tp_sp_reduce_scatter": [_VP, C.c_int, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _VP, _VP, _VP,
+                             C.c_float, _VP],
 }
 EXPORTED = tuple(sorted(list(_SIGS) + ["tp_last_error"]))
 
@@ -167,13 +172,13 @@ def _s(stream) -> Optional[int]:
 def make_config(tokens: int, hidden: int, ffn: int = 0, n_heads: int = 0, n_kv_heads: int = 0,
                 head_dim: int = 0, tp_degree: int = 1, act="gelu", reduce_mode: int = TP_REDUCE_FUSED,
                 partial_dtype: int = TP_F32, rms_eps: float = 1e-5, batch: int = 1,
-                seq: Optional[int] = None) -> TPConfig:
+                seq: Optional[int] = None, sequence_parallel: int = 0) -> TPConfig:
     if isinstance(act, str):
         act = ACT_BY_NAME[act]
     if seq is None:
         seq = tokens // max(batch, 1)
     return TPConfig(tokens, batch, seq, hidden, ffn, n_heads, n_kv_heads, head_dim, tp_degree, act,
-                    reduce_mode, partial_dtype, rms_eps)
+                    reduce_mode, partial_dtype, rms_eps, sequence_parallel)
 
 
 class Plan:
@@ -348,3 +353,13 @@ def tp_vocab_parallel_cross_entropy(logits, M: int, v: int, t: int, labels, stat
                                     stream=None) -> None:
     _call("tp_vocab_parallel_cross_entropy", _p(logits), M, v, t, _p(labels), _p(stats), _p(loss),
           _s(stream))
+
+
+def tp_sp_all_gather(sp, batch: int, seq: int, t: int, h: int, full, stream=None) -> None:
+    _call("tp_sp_all_gather", _p(sp), batch, seq, t, h, _p(full), _s(stream))
+
+
+def tp_sp_reduce_scatter(partials, partial_dtype: int, t: int, batch: int, seq: int, h: int,
+                         residual_sp, out_sp, xn_sp=None, eps: float = 1e-5, stream=None) -> None:
+    _call("tp_sp_reduce_scatter", _p(partials), partial_dtype, t, batch, seq, h, _p(residual_sp),
+          _p(out_sp), _p(xn_sp), eps, _s(stream))

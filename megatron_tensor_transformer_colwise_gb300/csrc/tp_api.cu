@@ -95,6 +95,7 @@ struct Layout {
     size_t h1 = 0;       // [M][h] bf16 (residual stream after attention)
     size_t partials = 0; // [t][M][h] fp32 or bf16 (layer in PARTIALS mode)
     size_t ss = 0;       // 2 x [M] fp32 row sums of squares (layer in FUSED mode)
+    size_t full = 0;     // [M][h] bf16 all-gathered block input (sequence parallel)
 };
 
 size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
@@ -114,6 +115,7 @@ Layout layout_of(const tp_plan_s* p, int op) {
         if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS) {
             L.xn = align_up(M * p->h * 2);
             L.partials = align_up(static_cast<size_t>(p->t) * M * p->h * partial_elem_bytes(p));
+            if (p->cfg.sequence_parallel) L.full = align_up(M * p->h * 2);
         } else {
             L.ss = align_up(2 * M * sizeof(float));  // folded RMSNorm statistics
         }
@@ -121,7 +123,9 @@ Layout layout_of(const tp_plan_s* p, int op) {
     return L;
 }
 
-size_t layout_total(const Layout& L) { return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss; }
+size_t layout_total(const Layout& L) {
+    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full;
+}
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
     const size_t need = layout_total(layout_of(p, op));
@@ -317,6 +321,19 @@ int derive_plan(const tp_config& cfg, tp_plan_s* p) {
                         (long long)c.tokens, c.batch, c.seq);
     }
     if (!(c.rms_eps >= 0.0f)) return fail(TP_ERR_INVALID_ARG, "rms_eps must be >= 0");
+    if (c.sequence_parallel != 0 && c.sequence_parallel != 1)
+        return fail(TP_ERR_INVALID_ARG, "sequence_parallel must be 0 or 1");
+    if (c.sequence_parallel) {
+        if (c.batch < 1 || c.seq < 1 || (int64_t)c.batch * c.seq != c.tokens)
+            return fail(TP_ERR_INVALID_ARG, "sequence parallelism needs tokens == batch x seq");
+        if (c.seq % t)
+            return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide seq %d (sequence split)",
+                        c.tp_degree, c.seq);
+        if (c.reduce_mode != TP_REDUCE_PARTIALS)
+            return fail(TP_ERR_UNSUPPORTED,
+                        "sequence parallelism leaves each block through a reduce-scatter of the "
+                        "partials: use TP_REDUCE_PARTIALS");
+    }
 
     *p = tp_plan_s();
     p->cfg = c;
@@ -612,7 +629,8 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     if (X == Y) return fail(TP_ERR_INVALID_ARG, "X and Y must not alias");
     if ((rc = check_ws(plan, TP_OP_LAYER, workspace, ws_bytes))) return rc;
     const bool fused_mode = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
-    const int need_events = fused_mode ? 7 : 9;
+    const bool sp_mode = plan->cfg.sequence_parallel != 0;
+    const int need_events = fused_mode ? 7 : sp_mode ? 11 : 9;
     if (events) {
         if (n_events < need_events)
             return fail(TP_ERR_INVALID_ARG, "%d events given, %d needed", n_events, need_events);
@@ -632,6 +650,8 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     void* h1 = region(workspace, off); off += L.h1;
     void* P = L.partials ? region(workspace, off) : nullptr; off += L.partials;
     float* ss1 = L.ss ? reinterpret_cast<float*>(region(workspace, off)) : nullptr;
+    off += L.ss;
+    void* full = L.full ? region(workspace, off) : nullptr;
     float* ss2 = ss1 ? ss1 + plan->M : nullptr;
     const float eps = plan->cfg.rms_eps;
     cudaStream_t s = as_stream(stream);
@@ -657,6 +677,40 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
         mark(s);
         // y = h1 + sum_i act(xn A_i) B_i.
         if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s))) return rc;
+        mark(s);
+        return TP_OK;
+    }
+    if (sp_mode) {
+        // Sequence parallel: X, h1 and Y stay split along the sequence; each
+        // block's input is all-gathered after its local norm, and each g is a
+        // reduce-scatter (fused with the next local norm).
+        const int64_t B = plan->cfg.batch, S = plan->cfg.seq;
+        const int T = (int)plan->t, Hd = (int)plan->h, pf = plan->cfg.partial_dtype == TP_F32 ? 1 : 0;
+        mark(s);
+        if ((rc = run(tpi::rmsnorm_launch(X, plan->M, Hd, eps, xn, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = run(tpi::sp_all_gather_launch(xn, B, S, T, Hd, full, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = do_qkv(plan, full, w->Wq, w->Wk, w->Wv, QKV, s))) return rc;
+        mark(s);
+        if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
+        mark(s);
+        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, nullptr, P, nullptr, false, s)))
+            return rc;
+        mark(s);
+        if ((rc = run(tpi::reduce_norm_launch(P, pf, T, plan->M, Hd, X, h1, xn, eps, s, &err, B, S, T), err)))
+            return rc;
+        mark(s);
+        if ((rc = run(tpi::sp_all_gather_launch(xn, B, S, T, Hd, full, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = do_colwise(plan, full, w->W1, w->W3, Yb, s))) return rc;
+        mark(s);
+        if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, nullptr, P, nullptr, false, s)))
+            return rc;
+        mark(s);
+        if ((rc = run(tpi::reduce_norm_launch(P, pf, T, plan->M, Hd, h1, Y, nullptr, eps, s, &err, B, S, T),
+                      err)))
+            return rc;
         mark(s);
         return TP_OK;
     }
@@ -920,4 +974,38 @@ extern "C" int tp_vocab_parallel_cross_entropy(const tp_bf16* logits, int64_t M,
     if ((rc = check_vocab(M, v, t, 8))) return rc;
     std::string err;
     return run(tpi::vocab_ce_launch(logits, M, v, t, labels, stats, loss, as_stream(stream), &err), err);
+}
+
+// ---------------------------------------------------------------------------
+// Sequence parallelism ("텐서 병렬화", "시퀀스 병렬화").
+extern "C" int tp_sp_all_gather(const tp_bf16* sp, int32_t batch, int32_t seq, int32_t t, int32_t h,
+                                tp_bf16* full, void* stream) {
+    int rc;
+    if ((rc = need_ptr(sp, "sp")) || (rc = need_ptr(full, "full"))) return rc;
+    if (batch < 0 || seq < 1 || t < 1 || t > 64) return fail(TP_ERR_INVALID_ARG, "bad batch/seq/t");
+    if (seq % t) return fail(TP_ERR_NOT_DIVISIBLE, "t = %d does not divide seq = %d", t, seq);
+    if (h < 8 || h % 8) return fail(TP_ERR_INVALID_ARG, "h must be a positive multiple of 8");
+    if (sp == full) return fail(TP_ERR_INVALID_ARG, "sp and full must not alias");
+    std::string err;
+    return run(tpi::sp_all_gather_launch(sp, batch, seq, t, h, full, as_stream(stream), &err), err);
+}
+
+extern "C" int tp_sp_reduce_scatter(const void* partials, int partial_dtype, int32_t t, int32_t batch,
+                                    int32_t seq, int32_t h, const tp_bf16* residual_sp, tp_bf16* out_sp,
+                                    tp_bf16* xn_sp, float eps, void* stream) {
+    int rc;
+    if ((rc = need_ptr(partials, "partials")) || (rc = need_ptr(out_sp, "out_sp")) ||
+        (rc = opt_ptr(residual_sp, "residual_sp")) || (rc = opt_ptr(xn_sp, "xn_sp")))
+        return rc;
+    if (partial_dtype != TP_F32 && partial_dtype != TP_BF16)
+        return fail(TP_ERR_INVALID_ARG, "partial_dtype must be TP_F32 or TP_BF16");
+    if (batch < 0 || seq < 1 || t < 1 || t > 64) return fail(TP_ERR_INVALID_ARG, "bad batch/seq/t");
+    if (seq % t) return fail(TP_ERR_NOT_DIVISIBLE, "t = %d does not divide seq = %d", t, seq);
+    if (h < 8 || h % 8 || h > 8192) return fail(TP_ERR_INVALID_ARG, "h must be a multiple of 8 in [8, 8192]");
+    if (!(eps >= 0.0f)) return fail(TP_ERR_INVALID_ARG, "eps must be >= 0");
+    std::string err;
+    const int64_t rows = (int64_t)batch * seq;
+    return run(tpi::reduce_norm_launch(partials, partial_dtype == TP_F32 ? 1 : 0, t, rows, h, residual_sp,
+                                       out_sp, xn_sp, eps, as_stream(stream), &err, batch, seq, t),
+               err);
 }

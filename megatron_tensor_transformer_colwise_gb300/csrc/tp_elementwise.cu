@@ -123,14 +123,30 @@ __global__ void __launch_bounds__(RED_THREADS) reduce_kernel(const void* __restr
 constexpr int ROW_THREADS = 256;
 constexpr int ROW_VEC = 4;  // vectors of 8 per thread -> h <= 8192
 
+// Row of token `row` (= b * seq + pos) in the sequence-split layout
+// [t][batch][seq/t] ("시퀀스 병렬화": device i keeps positions
+// [i seq/t, (i+1) seq/t) of every sequence); identity when sp_t == 0.
+__device__ __forceinline__ long long sp_out_row(long long row, long long sp_batch, long long sp_seq,
+                                                int sp_t) {
+    if (sp_t == 0) return row;
+    const long long w = sp_seq / sp_t;
+    const long long b = row / sp_seq, pos = row - b * sp_seq;
+    return ((pos / w) * sp_batch + b) * w + pos % w;
+}
+
 template <bool HAS_P, bool F32>
 __global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict__ partials, int t,
                                                           long long n, int h,
                                                           const __nv_bfloat16* __restrict__ src,
                                                           __nv_bfloat16* h1_out,
-                                                          __nv_bfloat16* xn_out, float eps) {
+                                                          __nv_bfloat16* xn_out, float eps,
+                                                          long long sp_batch, long long sp_seq,
+                                                          int sp_t) {
     __shared__ float red[ROW_THREADS / 32];
-    const long long row = blockIdx.x;
+    // Partials are read at the token's row; residual and outputs live at its
+    // (possibly sequence-split) output row.
+    const long long prow = blockIdx.x;
+    const long long row = sp_out_row(prow, sp_batch, sp_seq, sp_t);
     const int nv = h >> 3;
     float vals[ROW_VEC][8];
     float ss = 0.0f;
@@ -141,10 +157,11 @@ __global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict
         for (int e = 0; e < 8; ++e) vals[j][e] = 0.0f;
         if (v < nv) {
             const long long e0 = row * h + (long long)v * 8;
+            const long long p0 = prow * h + (long long)v * 8;
             if (HAS_P) {
                 for (int i = 0; i < t; ++i) {
                     if (F32) {
-                        const float* P = reinterpret_cast<const float*>(partials) + i * n + e0;
+                        const float* P = reinterpret_cast<const float*>(partials) + i * n + p0;
                         const uint4 lo = ld_stream(P), hi = ld_stream(P + 4);
                         vals[j][0] += __uint_as_float(lo.x);
                         vals[j][1] += __uint_as_float(lo.y);
@@ -156,7 +173,7 @@ __global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict
                         vals[j][7] += __uint_as_float(hi.w);
                     } else {
                         add_bf16x8(vals[j], ld_stream(reinterpret_cast<const __nv_bfloat16*>(partials) +
-                                                      i * n + e0));
+                                                      i * n + p0));
                     }
                 }
             }
@@ -226,6 +243,21 @@ __global__ void __launch_bounds__(SS_WARPS * 32) row_sumsq_kernel(const __nv_bfl
         ss[row] = t;
         if (zero) zero[row] = 0.0f;
     }
+}
+
+// Sequence-parallel all-gather ("시퀀스 병렬화": entering the tensor-parallel
+// region the sequence pieces are gathered): full[row] = sp[sp_out_row(row)],
+// one warp per row, 16-byte vectors.
+constexpr int AG_WARPS = 8;
+
+__global__ void __launch_bounds__(AG_WARPS * 32) sp_all_gather_kernel(
+    const __nv_bfloat16* __restrict__ sp, long long rows, int h, long long batch, long long seq,
+    int t, __nv_bfloat16* __restrict__ full) {
+    const long long row = static_cast<long long>(blockIdx.x) * AG_WARPS + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint4* src = reinterpret_cast<const uint4*>(sp + sp_out_row(row, batch, seq, t) * h);
+    uint4* dst = reinterpret_cast<uint4*>(full + row * h);
+    for (int c = threadIdx.x & 31; c < (h >> 3); c += 32) dst[c] = src[c];
 }
 
 // Failure-detection self test: wait on a barrier that never completes.
@@ -309,16 +341,18 @@ int reduce_launch(const void* partials, int partial_f32, int t, int64_t n, int h
 
 int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t rows, int h,
                        const void* residual, void* h1, void* xn, float eps, cudaStream_t stream,
-                       std::string* err) {
+                       std::string* err, int64_t sp_batch, int64_t sp_seq, int sp_t) {
     if (rows == 0) return TP_OK;
     const long long n = rows * (long long)h;
     const __nv_bfloat16* r = reinterpret_cast<const __nv_bfloat16*>(residual);
     auto* h1p = reinterpret_cast<__nv_bfloat16*>(h1);
     auto* xnp = reinterpret_cast<__nv_bfloat16*>(xn);
     if (partial_f32)
-        row_kernel<true, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp, eps);
+        row_kernel<true, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp,
+                                                                           eps, sp_batch, sp_seq, sp_t);
     else
-        row_kernel<true, false><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp, eps);
+        row_kernel<true, false><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp,
+                                                                            eps, sp_batch, sp_seq, sp_t);
     return check_launch("reduce+norm kernel", err);
 }
 
@@ -328,7 +362,7 @@ int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaS
     const long long n = rows * (long long)h;
     row_kernel<false, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(
         nullptr, 0, n, h, reinterpret_cast<const __nv_bfloat16*>(x), nullptr,
-        reinterpret_cast<__nv_bfloat16*>(y), eps);
+        reinterpret_cast<__nv_bfloat16*>(y), eps, 0, 0, 0);
     return check_launch("rmsnorm kernel", err);
 }
 
@@ -339,6 +373,16 @@ int row_sumsq_launch(const void* x, int64_t rows, int h, float* ss, float* zero,
     row_sumsq_kernel<<<(unsigned)blocks, SS_WARPS * 32, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(x), rows, h, ss, zero);
     return check_launch("row sum-of-squares kernel", err);
+}
+
+int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int h, void* full,
+                         cudaStream_t stream, std::string* err) {
+    const long long rows = batch * seq;
+    if (rows == 0) return TP_OK;
+    sp_all_gather_kernel<<<(unsigned)((rows + AG_WARPS - 1) / AG_WARPS), AG_WARPS * 32, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
+        reinterpret_cast<__nv_bfloat16*>(full));
+    return check_launch("all-gather kernel", err);
 }
 
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,

@@ -78,9 +78,14 @@ int reduce_launch(const void* partials, int partial_f32, int t, int64_t n, int h
                   std::string* err);
 // Row-wise reduce of the partials plus residual into h1 (bf16), and also
 // xn = RMSNorm(h1) (unit gain) when xn != nullptr.
+// sp_t > 0: residual, h1 and xn live in the sequence-split layout
+// [sp_t][sp_batch][sp_seq / sp_t] (a reduce-scatter); partials in token order.
 int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t rows, int h,
                        const void* residual, void* h1, void* xn, float eps, cudaStream_t stream,
-                       std::string* err);
+                       std::string* err, int64_t sp_batch = 0, int64_t sp_seq = 0, int sp_t = 0);
+// full[b * seq + pos] = sp[row of (b, pos) in [t][batch][seq / t]].
+int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int h, void* full,
+                         cudaStream_t stream, std::string* err);
 int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaStream_t stream,
                    std::string* err);
 // ss[row] = sum_j x[row][j]^2 (fp32 over the bf16 values); zero[row] = 0

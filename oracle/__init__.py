@@ -68,6 +68,10 @@ def lib():
             "tpo_cross_entropy": (C.c_int, [_I64, _I64, _D, C.POINTER(C.c_int32), _D]),
             "tpo_cross_entropy_vocab_parallel": (C.c_int, [_I64] * 3 + [_D, C.POINTER(C.c_int32),
                                                                         _D, _D]),
+            "tpo_sp_row": (_I64, [_I64] * 5),
+            "tpo_sp_all_gather": (C.c_int, [_I64] * 4 + [_D, _D]),
+            "tpo_sp_reduce_scatter": (C.c_int, [_I64] * 4 + [_D, _D]),
+            "tpo_layer_sp": (C.c_int, [_I64] * 8 + [C.c_double] + [_D] * 9),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -351,3 +355,37 @@ def cross_entropy_vocab_parallel(t: int, logits, labels, want_stats: bool = Fals
     _check("tpo_cross_entropy_vocab_parallel", lib().tpo_cross_entropy_vocab_parallel(
         M, v, t, _p(z), lab.ctypes.data_as(C.POINTER(C.c_int32)), _p(st), _p(loss)))
     return (loss, st) if want_stats else loss
+
+
+def sp_row(batch: int, seq: int, t: int, b: int, pos: int) -> int:
+    """Row of token (b, pos) in the sequence-split layout [t][batch][s/t]."""
+    return lib().tpo_sp_row(batch, seq, t, b, pos)
+
+
+def sp_all_gather(batch: int, seq: int, t: int, sp) -> np.ndarray:
+    sp = _d(sp)
+    h = sp.shape[1]
+    full = np.empty_like(sp)
+    _check("tpo_sp_all_gather", lib().tpo_sp_all_gather(batch, seq, t, h, _p(sp), _p(full)))
+    return full
+
+
+def sp_reduce_scatter(batch: int, seq: int, t: int, partials) -> np.ndarray:
+    P = _d(partials)
+    h = P.shape[-1]
+    out = np.empty((batch * seq, h))
+    _check("tpo_sp_reduce_scatter", lib().tpo_sp_reduce_scatter(batch, seq, t, h, _p(P), _p(out)))
+    return out
+
+
+def layer_sp(batch: int, seq: int, a: int, k: int, d: int, t: int, X_sp, Wq, Wk, Wv, Wo, W1, W3,
+             W2, eps: float = 1e-5) -> np.ndarray:
+    """Sequence-parallel pre-norm layer; X_sp and the result in [t][batch][s/t][h]."""
+    X, Wq, Wk, Wv, Wo, W1, W3, W2 = map(_d, (X_sp, Wq, Wk, Wv, Wo, W1, W3, W2))
+    M, h = X.shape
+    f = W1.shape[0]
+    Y = np.empty((M, h))
+    _check("tpo_layer_sp", lib().tpo_layer_sp(batch, seq, h, a, k, d, f, t, float(eps), _p(X),
+                                              _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(W1), _p(W3),
+                                              _p(W2), _p(Y)))
+    return Y

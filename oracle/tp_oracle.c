@@ -672,3 +672,85 @@ int tpo_cross_entropy_vocab_parallel(int64_t M, int64_t v, int64_t t, const doub
     free(st);
     return TPO_OK;
 }
+
+/* ---------------------------------------------------------------- sequence parallel */
+
+/* Sequence parallelism ("텐서 병렬화", section "시퀀스 병렬화"): the norm
+ * and dropout regions are split along the sequence into t pieces, each
+ * device keeping its own piece; entering the tensor-parallel region an
+ * all-gather collects the sequence, leaving it a reduce-scatter sums the
+ * partials and splits them along the sequence again (the same traffic as the
+ * all-reduce).  Layout of the sequence-split tensors: [t][batch][s/t][h],
+ * device i holding positions [i s/t, (i+1) s/t) of every sequence.
+ * Row of token (b, pos) in that layout: */
+int64_t tpo_sp_row(int64_t batch, int64_t seq, int64_t t, int64_t b, int64_t pos) {
+    const int64_t w = seq / t;
+    return ((pos / w) * batch + b) * w + pos % w;
+}
+
+/* All-gather: full[b s + pos] = sp[tpo_sp_row(b, pos)]. */
+int tpo_sp_all_gather(int64_t batch, int64_t seq, int64_t t, int64_t h, const double* sp,
+                      double* full) {
+    if (batch < 0 || seq <= 0 || t <= 0 || h <= 0 || (seq % t)) return TPO_ERR_INVALID;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t pos = 0; pos < seq; ++pos)
+            memcpy(full + (b * seq + pos) * h, sp + tpo_sp_row(batch, seq, t, b, pos) * h,
+                   sizeof(double) * (size_t)h);
+    return TPO_OK;
+}
+
+/* Reduce-scatter of t partials [t][batch seq][h] (full token order) into the
+ * sequence-split layout: device i receives sum_j partials[j] at its own
+ * positions (j ascending). */
+int tpo_sp_reduce_scatter(int64_t batch, int64_t seq, int64_t t, int64_t h, const double* partials,
+                          double* sp) {
+    if (batch < 0 || seq <= 0 || t <= 0 || h <= 0 || (seq % t)) return TPO_ERR_INVALID;
+    const int64_t M = batch * seq;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t pos = 0; pos < seq; ++pos) {
+            double* dst = sp + tpo_sp_row(batch, seq, t, b, pos) * h;
+            for (int64_t c = 0; c < h; ++c) {
+                double s = 0.0;
+                for (int64_t j = 0; j < t; ++j) s += partials[(j * M + b * seq + pos) * h + c];
+                dst[c] = s;
+            }
+        }
+    return TPO_OK;
+}
+
+/* One pre-norm layer in the sequence-parallel form, step by step: X_sp and
+ * Y_sp in the sequence-split layout.
+ *   xn_sp = RMSNorm(x_sp) on each device's piece; xn = all-gather(xn_sp)
+ *   attention block (head-sharded) -> partials; a_sp = reduce-scatter
+ *   h1_sp = x_sp + a_sp; hn_sp = RMSNorm(h1_sp); hn = all-gather(hn_sp)
+ *   MLP (sharded SwiGLU) -> partials; m_sp = reduce-scatter; y_sp = h1_sp + m_sp */
+int tpo_layer_sp(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                 int64_t f, int64_t t, double eps, const double* X_sp, const double* Wq,
+                 const double* Wk, const double* Wv, const double* Wo, const double* W1,
+                 const double* W3, const double* W2, double* Y_sp) {
+    int rc = tpo_plan_check(h, f, a, k, d, t);
+    if (rc) return rc;
+    if (seq % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t M = batch * seq;
+    double* n_sp = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    double* full = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    double* P = (double*)malloc(sizeof(double) * (size_t)(t * M * h + 1));
+    double* h1 = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)(M * h + 1));
+    if (!n_sp || !full || !P || !h1 || !tmp) { rc = TPO_ERR_NOMEM; goto done; }
+    tpo_rmsnorm(M, h, eps, X_sp, n_sp);                      /* row-local: any layout */
+    tpo_sp_all_gather(batch, seq, t, h, n_sp, full);
+    rc = tpo_attention_sharded(batch, seq, h, a, k, d, t, full, Wq, Wk, Wv, Wo, P, tmp);
+    if (rc) goto done;
+    tpo_sp_reduce_scatter(batch, seq, t, h, P, tmp);
+    for (int64_t e = 0; e < M * h; ++e) h1[e] = X_sp[e] + tmp[e];
+    tpo_rmsnorm(M, h, eps, h1, n_sp);
+    tpo_sp_all_gather(batch, seq, t, h, n_sp, full);
+    rc = tpo_mlp_sharded(TPO_ACT_SWIGLU, M, h, f, t, full, W1, W3, W2, P, tmp);
+    if (rc) goto done;
+    tpo_sp_reduce_scatter(batch, seq, t, h, P, tmp);
+    for (int64_t e = 0; e < M * h; ++e) Y_sp[e] = h1[e] + tmp[e];
+done:
+    free(n_sp); free(full); free(P); free(h1); free(tmp);
+    return rc;
+}

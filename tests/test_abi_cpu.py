@@ -154,3 +154,15 @@ def test_packed_shard_table_rejects_blocks_not_divisible_individually():
     with pytest.raises(tp.TPError) as e:
         tp.tp_packed_shard_table([4] * 9, 2)
     assert e.value.code == tp.TP_ERR_INVALID_ARG
+
+
+def test_sequence_parallel_config_rules():
+    ok = cfg(tokens=64, batch=2, seq=32, tp_degree=4, reduce_mode=tp.TP_REDUCE_PARTIALS,
+             sequence_parallel=1)
+    assert tp.tp_config_check(ok) == tp.TP_OK, tp.tp_last_error()
+    bad_seq = cfg(tokens=60, batch=2, seq=30, tp_degree=4, reduce_mode=tp.TP_REDUCE_PARTIALS,
+                  sequence_parallel=1, ffn=256)
+    assert tp.tp_config_check(bad_seq) == tp.TP_ERR_NOT_DIVISIBLE
+    fused = cfg(tokens=64, batch=2, seq=32, tp_degree=4, sequence_parallel=1)
+    assert tp.tp_config_check(fused) == tp.TP_ERR_UNSUPPORTED
+    assert "reduce-scatter" in tp.tp_last_error()

@@ -481,3 +481,43 @@ def test_vocab_parallel_cross_entropy_equals_plain(t):
     for m in range(1, M):
         assert st[2, owner[m], m] == z[m, lab[m]]
         assert np.count_nonzero(st[2, :, m]) <= 1
+
+
+# ---------------------------------------------------------------- sequence parallelism
+
+def test_sp_layout_matches_golden():
+    for line in open(os.path.join(GOLDEN, "sp_layout_b2_s4_t2.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            b, pos, row = (int(v) for v in line.split())
+            assert oracle.sp_row(2, 4, 2, b, pos) == row
+
+
+@pytest.mark.parametrize("batch,seq,t", [(2, 4, 2), (3, 8, 4), (1, 6, 3), (2, 8, 1)])
+def test_sp_all_gather_inverts_the_split_and_reduce_scatter_sums(batch, seq, t):
+    rng = np.random.default_rng(batch * 100 + seq * 10 + t)
+    h = 5
+    full = rng.normal(size=(batch * seq, h))
+    sp = np.empty_like(full)
+    for b in range(batch):
+        for pos in range(seq):
+            sp[oracle.sp_row(batch, seq, t, b, pos)] = full[b * seq + pos]
+    assert np.array_equal(oracle.sp_all_gather(batch, seq, t, sp), full)
+    P = rng.integers(-9, 10, size=(t, batch * seq, h)).astype(np.float64)
+    red = oracle.sp_reduce_scatter(batch, seq, t, P)
+    S = P.sum(0)
+    for b in range(batch):
+        for pos in range(seq):
+            assert np.array_equal(red[oracle.sp_row(batch, seq, t, b, pos)], S[b * seq + pos])
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_sp_layer_equals_replicated_layer_in_the_split_layout(t):
+    dims, X, W = _small_layer(7, batch=2, seq=8, h=16, a=4, k=2, d=4, f=32)
+    batch, seq, a, k, d = dims
+    Y = oracle.layer(*dims, t, X, *W, sharded=True)
+    perm = [oracle.sp_row(batch, seq, t, b, pos) for b in range(batch) for pos in range(seq)]
+    X_sp = np.empty_like(X.numpy())
+    X_sp[perm] = X.numpy()
+    Y_sp = oracle.layer_sp(batch, seq, a, k, d, t, X_sp, *W)
+    assert np.abs(Y_sp[perm] - Y).max() < 1e-12
