@@ -72,6 +72,8 @@ def lib():
             "tpo_sp_all_gather": (C.c_int, [_I64] * 4 + [_D, _D]),
             "tpo_sp_reduce_scatter": (C.c_int, [_I64] * 4 + [_D, _D]),
             "tpo_layer_sp": (C.c_int, [_I64] * 8 + [C.c_double] + [_D] * 9),
+            "tpo_mlp_backward": (C.c_int, [C.c_int] + [_I64] * 3 + [_D] * 10),
+            "tpo_mlp_backward_sharded": (C.c_int, [C.c_int] + [_I64] * 4 + [_D] * 11),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -389,3 +391,28 @@ def layer_sp(batch: int, seq: int, a: int, k: int, d: int, t: int, X_sp, Wq, Wk,
                                               _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(W1), _p(W3),
                                               _p(W2), _p(Y)))
     return Y
+
+
+def mlp_backward(act: str, X, W1, W2, dZ, W3=None, t: int = 0, want_partials: bool = False):
+    """Gradients (dX, dW1, dW3, dW2, db2) of the MLP given dZ (db2: of a bias
+    added once to Z); t > 0 uses the literal t-device form (g backward =
+    identity, f backward = all-reduce)."""
+    X, W1, W2, dZ, W3 = map(_d, (X, W1, W2, dZ, W3))
+    M, h = X.shape
+    f = W1.shape[0]
+    dX = np.empty((M, h))
+    dW1 = np.empty((f, h))
+    dW3 = np.empty((f, h)) if act == "swiglu" else None
+    dW2 = np.empty((h, f))
+    db2 = np.empty(h)
+    if t:
+        P = np.empty((t, M, h)) if want_partials else None
+        _check("tpo_mlp_backward_sharded", lib().tpo_mlp_backward_sharded(
+            ACT[act], M, h, f, t, _p(X), _p(W1), _p(W3), _p(W2), _p(dZ), _p(P), _p(dX), _p(dW1),
+            _p(dW3), _p(dW2), _p(db2)))
+        out = (dX, dW1, dW3, dW2, db2)
+        return out + (P,) if want_partials else out
+    _check("tpo_mlp_backward", lib().tpo_mlp_backward(
+        ACT[act], M, h, f, _p(X), _p(W1), _p(W3), _p(W2), _p(dZ), _p(dX), _p(dW1), _p(dW3), _p(dW2),
+        _p(db2)))
+    return dX, dW1, dW3, dW2, db2

@@ -754,3 +754,144 @@ done:
     free(n_sp); free(full); free(P); free(h1); free(tmp);
     return rc;
 }
+
+/* ---------------------------------------------------------------- backward */
+
+/* d act(u) / du for the MLP activations. */
+static double act_grad(int act, double u) {
+    if (act == TPO_ACT_GELU_ERF)  /* Phi(u) + u phi(u) */
+        return 0.5 * (1.0 + erf(u / sqrt(2.0))) + u * exp(-0.5 * u * u) / sqrt(2.0 * 3.14159265358979323846);
+    if (act == TPO_ACT_GELU_TANH) {
+        const double c = sqrt(2.0 / 3.14159265358979323846), a = 0.044715;
+        const double th = tanh(c * (u + a * u * u * u));
+        return 0.5 * (1.0 + th) + 0.5 * u * (1.0 - th * th) * c * (1.0 + 3.0 * a * u * u);
+    }
+    if (act == TPO_ACT_SWIGLU) {  /* d SiLU / du = s (1 + u (1 - s)), s = sigmoid(u) */
+        const double s = 1.0 / (1.0 + exp(-u));
+        return s * (1.0 + u * (1.0 - s));
+    }
+    return 1.0;
+}
+
+/* Backward of the MLP at its plain definition, given dZ = dL/dZ:
+ *   U = X W1^T, G = X W3^T (SwiGLU), H = act(U) or SiLU(U) (.) G, Z = H W2^T
+ *   dH = dZ W2;  dU = dH (.) act'(U)  [SwiGLU: dU = dH (.) G (.) SiLU'(U),
+ *   dG = dH (.) SiLU(U)];  dX = dU W1 (+ dG W3);  dW2 = dZ^T H;
+ *   dW1 = dU^T X;  dW3 = dG^T X;  and, for a bias b2 added to Z once,
+ *   db2 = sum over rows of dZ.
+ * dW3 may be NULL unless SwiGLU; db2 may be NULL. */
+int tpo_mlp_backward(int act, int64_t M, int64_t h, int64_t f, const double* X, const double* W1,
+                     const double* W3, const double* W2, const double* dZ, double* dX, double* dW1,
+                     double* dW3, double* dW2, double* db2) {
+    if (M <= 0 || h <= 0 || f <= 0 || !X || !W1 || !W2 || !dZ || !dX || !dW1 || !dW2)
+        return TPO_ERR_INVALID;
+    const int swiglu = act == TPO_ACT_SWIGLU;
+    if (swiglu && (!W3 || !dW3)) return TPO_ERR_INVALID;
+    double* U = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    double* G = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    double* H = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    double* dH = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    double* dU = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    double* dG = (double*)malloc(sizeof(double) * (size_t)(M * f));
+    int rc = TPO_OK;
+    if (!U || !G || !H || !dH || !dU || !dG) { rc = TPO_ERR_NOMEM; goto done; }
+    tpo_linear(X, h, W1, h, M, f, h, U, f);
+    if (swiglu) tpo_linear(X, h, W3, h, M, f, h, G, f);
+    for (int64_t e = 0; e < M * f; ++e) H[e] = swiglu ? tpo_silu(U[e]) * G[e] : act_scalar(act, U[e]);
+    if (db2)
+        for (int64_t j = 0; j < h; ++j) {
+            double s = 0.0;
+            for (int64_t m = 0; m < M; ++m) s += dZ[m * h + j];
+            db2[j] = s;
+        }
+    /* dH[m][n] = sum_j dZ[m][j] W2[j][n] */
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < f; ++n) {
+            double s = 0.0;
+            for (int64_t j = 0; j < h; ++j) s += dZ[m * h + j] * W2[j * f + n];
+            dH[m * f + n] = s;
+        }
+    for (int64_t e = 0; e < M * f; ++e) {
+        if (swiglu) {
+            dU[e] = dH[e] * G[e] * act_grad(TPO_ACT_SWIGLU, U[e]);
+            dG[e] = dH[e] * tpo_silu(U[e]);
+        } else {
+            dU[e] = dH[e] * act_grad(act, U[e]);
+        }
+    }
+    /* dX[m][j] = sum_n dU[m][n] W1[n][j] (+ dG[m][n] W3[n][j]) */
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < h; ++j) {
+            double s = 0.0;
+            for (int64_t n = 0; n < f; ++n) {
+                s += dU[m * f + n] * W1[n * h + j];
+                if (swiglu) s += dG[m * f + n] * W3[n * h + j];
+            }
+            dX[m * h + j] = s;
+        }
+    /* dW2[j][n] = sum_m dZ[m][j] H[m][n];  dW1[n][j] = sum_m dU[m][n] X[m][j] */
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < h; ++j)
+        for (int64_t n = 0; n < f; ++n) {
+            double s = 0.0;
+            for (int64_t m = 0; m < M; ++m) s += dZ[m * h + j] * H[m * f + n];
+            dW2[j * f + n] = s;
+        }
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < f; ++n)
+        for (int64_t j = 0; j < h; ++j) {
+            double s = 0.0, s3 = 0.0;
+            for (int64_t m = 0; m < M; ++m) {
+                s += dU[m * f + n] * X[m * h + j];
+                if (swiglu) s3 += dG[m * f + n] * X[m * h + j];
+            }
+            dW1[n * h + j] = s;
+            if (swiglu) dW3[n * h + j] = s3;
+        }
+done:
+    free(U); free(G); free(H); free(dH); free(dU); free(dG);
+    return rc;
+}
+
+/* The same backward in the literal t-device form ("통신 연산 f와 g"): g's
+ * backward is the identity, so every device receives the same dZ; device i
+ * computes its own slices dW2[:, block i], dW1[block i, :] (and dW3) and a
+ * partial dX_i = dU_i W1_i (+ dG_i W3_i); f's backward is the all-reduce
+ * dX = sum_i dX_i (i ascending).  dX_partials (nullable): [t][M][h]. */
+int tpo_mlp_backward_sharded(int act, int64_t M, int64_t h, int64_t f, int64_t t, const double* X,
+                             const double* W1, const double* W3, const double* W2, const double* dZ,
+                             double* dX_partials, double* dX, double* dW1, double* dW3, double* dW2,
+                             double* db2) {
+    if (t <= 0 || f % t) return TPO_ERR_NOT_DIVISIBLE;
+    const int64_t w = f / t;
+    const int swiglu = act == TPO_ACT_SWIGLU;
+    double* W1i = (double*)malloc(sizeof(double) * (size_t)(w * h));
+    double* W3i = (double*)malloc(sizeof(double) * (size_t)(w * h));
+    double* W2i = (double*)malloc(sizeof(double) * (size_t)(h * w));
+    double* dXi = (double*)malloc(sizeof(double) * (size_t)(M * h));
+    double* dW1i = (double*)malloc(sizeof(double) * (size_t)(w * h));
+    double* dW3i = (double*)malloc(sizeof(double) * (size_t)(w * h));
+    double* dW2i = (double*)malloc(sizeof(double) * (size_t)(h * w));
+    int rc = TPO_OK;
+    if (!W1i || !W3i || !W2i || !dXi || !dW1i || !dW3i || !dW2i) { rc = TPO_ERR_NOMEM; goto done; }
+    for (int64_t e = 0; e < M * h; ++e) dX[e] = 0.0;
+    for (int64_t i = 0; i < t; ++i) {
+        memcpy(W1i, W1 + i * w * h, sizeof(double) * (size_t)(w * h));
+        if (swiglu) memcpy(W3i, W3 + i * w * h, sizeof(double) * (size_t)(w * h));
+        for (int64_t j = 0; j < h; ++j) memcpy(W2i + j * w, W2 + j * f + i * w, sizeof(double) * (size_t)w);
+        /* the bias is added once after g's sum: its gradient is taken once */
+        rc = tpo_mlp_backward(act, M, h, w, X, W1i, swiglu ? W3i : NULL, W2i, dZ, dXi, dW1i,
+                              swiglu ? dW3i : NULL, dW2i, i == 0 ? db2 : NULL);
+        if (rc) goto done;
+        for (int64_t e = 0; e < M * h; ++e) dX[e] += dXi[e];
+        if (dX_partials) memcpy(dX_partials + i * M * h, dXi, sizeof(double) * (size_t)(M * h));
+        memcpy(dW1 + i * w * h, dW1i, sizeof(double) * (size_t)(w * h));
+        if (swiglu) memcpy(dW3 + i * w * h, dW3i, sizeof(double) * (size_t)(w * h));
+        for (int64_t j = 0; j < h; ++j) memcpy(dW2 + j * f + i * w, dW2i + j * w, sizeof(double) * (size_t)w);
+    }
+done:
+    free(W1i); free(W3i); free(W2i); free(dXi); free(dW1i); free(dW3i); free(dW2i);
+    return rc;
+}

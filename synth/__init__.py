@@ -139,3 +139,10 @@ def workload_inputs(shape: Shape, seed_base: Optional[int] = None,
             std = 1.0 if name == "X" else WEIGHT_STD
             out[name] = normal_bf16(dims[name], std, base + j)
     return out
+
+
+def grad_output(shape: Shape, seed_base: Optional[int] = None) -> torch.Tensor:
+    """Upstream gradient dL/dZ for a block's backward: [tokens][hidden] bf16,
+    N(0, 1), seeded after the workload's own tensors."""
+    base = 1000 * shape.index if seed_base is None else seed_base
+    return normal_bf16((shape.tokens, shape.hidden), 1.0, base + len(TENSOR_ORDER))

@@ -521,3 +521,82 @@ def test_sp_layer_equals_replicated_layer_in_the_split_layout(t):
     X_sp[perm] = X.numpy()
     Y_sp = oracle.layer_sp(batch, seq, a, k, d, t, X_sp, *W)
     assert np.abs(Y_sp[perm] - Y).max() < 1e-12
+
+
+# ---------------------------------------------------------------- backward
+
+def _autograd_mlp(act, X, W1, W2, W3, dZ, b2):
+    X, W1, W2, b2 = (v.clone().requires_grad_(True) for v in (X, W1, W2, b2))
+    W3 = W3.clone().requires_grad_(True) if act == "swiglu" else None
+    U = X @ W1.T
+    if act == "gelu":
+        H = F.gelu(U)
+    elif act == "gelu_tanh":
+        H = F.gelu(U, approximate="tanh")
+    elif act == "swiglu":
+        H = F.silu(U) * (X @ W3.T)
+    else:
+        H = U
+    Z = H @ W2.T + b2
+    Z.backward(dZ)
+    return X.grad, W1.grad, (W3.grad if W3 is not None else None), W2.grad, b2.grad
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "none"])
+def test_mlp_backward_matches_torch_autograd(act):
+    g = torch.Generator().manual_seed(61)
+    M, h, f = 7, 12, 24
+    X = torch.randn(M, h, generator=g, dtype=torch.float64)
+    W1 = torch.randn(f, h, generator=g, dtype=torch.float64) * 0.4
+    W3 = torch.randn(f, h, generator=g, dtype=torch.float64) * 0.4
+    W2 = torch.randn(h, f, generator=g, dtype=torch.float64) * 0.4
+    dZ = torch.randn(M, h, generator=g, dtype=torch.float64)
+    b2 = torch.randn(h, generator=g, dtype=torch.float64)
+    want = _autograd_mlp(act, X, W1, W2, W3, dZ, b2)
+    got = oracle.mlp_backward(act, X, W1, W2, dZ, W3 if act == "swiglu" else None)
+    for name, a, b in zip(("dX", "dW1", "dW3", "dW2", "db2"), got, want):
+        if b is None:
+            continue
+        assert np.abs(a - b.numpy()).max() < 1e-12 * max(1.0, np.abs(b.numpy()).max()), name
+
+
+def test_mlp_backward_central_differences():
+    # d(sum dZ * Z)/dW1[n][j] by central differences of the oracle's forward.
+    g = torch.Generator().manual_seed(62)
+    M, h, f = 3, 4, 8
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    W1 = (torch.randn(f, h, generator=g, dtype=torch.float64) * 0.5).numpy()
+    W3 = (torch.randn(f, h, generator=g, dtype=torch.float64) * 0.5).numpy()
+    W2 = (torch.randn(h, f, generator=g, dtype=torch.float64) * 0.5).numpy()
+    dZ = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    _, dW1, dW3, _, _ = oracle.mlp_backward("swiglu", X, W1, W2, dZ, W3)
+    eps = 1e-6
+    for (n, j) in [(0, 0), (3, 2), (7, 3)]:
+        for W, dW in ((W1, dW1), (W3, dW3)):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[n, j] += eps
+            Wm[n, j] -= eps
+            args_p = (X, Wp, W2, W3) if W is W1 else (X, W1, W2, Wp)
+            args_m = (X, Wm, W2, W3) if W is W1 else (X, W1, W2, Wm)
+            Lp = (oracle.mlp("swiglu", *args_p) * dZ).sum()
+            Lm = (oracle.mlp("swiglu", *args_m) * dZ).sum()
+            assert (Lp - Lm) / (2 * eps) == pytest.approx(dW[n, j], rel=1e-6, abs=1e-9)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_mlp_backward_sharded_equals_plain(act, t):
+    g = torch.Generator().manual_seed(63 + t)
+    M, h, f = 6, 8, 32
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    W1 = (torch.randn(f, h, generator=g, dtype=torch.float64) * 0.4).numpy()
+    W3 = (torch.randn(f, h, generator=g, dtype=torch.float64) * 0.4).numpy()
+    W2 = (torch.randn(h, f, generator=g, dtype=torch.float64) * 0.4).numpy()
+    dZ = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    w3 = W3 if act == "swiglu" else None
+    plain = oracle.mlp_backward(act, X, W1, W2, dZ, w3)
+    *shard, P = oracle.mlp_backward(act, X, W1, W2, dZ, w3, t=t, want_partials=True)
+    for a, b in zip(plain, shard):
+        if a is not None:
+            assert np.abs(a - b).max() < 1e-12 * max(1.0, np.abs(a).max())
+    assert np.abs(P.sum(0) - plain[0]).max() < 1e-12   # f backward: dX = sum of the t partials
