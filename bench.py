@@ -73,6 +73,19 @@ def layer_kernel_bytes(s: Shape):
     return {"row_sumsq_x": 2.0 * s.tokens * s.hidden}
 
 
+def mlp_backward_kernel_flops(M, h, f, glu=True):
+    """Algorithmic FLOPs of the MLP backward's GEMMs, in launch order: dH =
+    dZ W2 (+ activation gradient), dX = [dU | dG] [W1 ; W3] (f's all-reduce
+    in the K loop), dW2 = dZ^T H, [dW1 ; dW3] = [dU | dG]^T X."""
+    wu = (2 if glu else 1) * f
+    return [
+        ("bwd_dh_gemm+act_grad", gemm_flops(M, f, h)),
+        ("bwd_dx_gemm+f", gemm_flops(M, h, wu)),
+        ("bwd_dw2_gemm", gemm_flops(h, f, M)),
+        ("bwd_dw13_gemm", gemm_flops(wu, h, M)),
+    ]
+
+
 def layer_flops(s: Shape):
     return sum(v for _, v in layer_kernel_flops(s))
 
@@ -380,6 +393,33 @@ def run_case(args):
         wd = {kk: vv for kk, vv in d.items() if kk != "X"}
         fn = lambda: tp.tp_layer_forward(plan, d["X"], wd, Yl, wsb, nws, stream)
         work = layer_flops(s)
+    elif args.case in ("mlp_backward", "mlp_backward_recompute"):
+        # Backward of the layer's MLP (8192 tokens, h 4096, f 14336, SwiGLU,
+        # t 8): the pre-activations saved by the forward, or recomputed.
+        # --tokens shrinks M for a profiler capture.
+        if args.tokens:
+            M = args.tokens
+            mk = lambda **kw: tp.Plan(tp.make_config(tokens=M, hidden=h, tp_degree=t, **kw))
+        X, W1, W3 = bf((M, h), 1.0, 4000), bf((f, h), 0.02, 4001), bf((f, h), 0.02, 4002)
+        W2, dZ = bf((h, f), 0.02, 4007), bf((M, h), 1.0, 4012)
+        plan = mk(ffn=f, act="swiglu")
+        nf = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_MLP)
+        fws = torch.empty(nf, dtype=torch.uint8, device="cuda")
+        Z = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+        UG = torch.empty(M, 2 * f, dtype=torch.bfloat16, device="cuda")
+        tp.tp_mlp_forward_train(plan, X, W1, W3, W2, None, None, None, Z, UG, fws, nf, stream)
+        del fws
+        if args.case == "mlp_backward_recompute":
+            UG = None
+        nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_MLP_BACKWARD)
+        wsb = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        dX = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+        dW1, dW3 = (torch.empty(f, h, dtype=torch.float32, device="cuda") for _ in range(2))
+        dW2 = torch.empty(h, f, dtype=torch.float32, device="cuda")
+        db2 = torch.empty(h, dtype=torch.float32, device="cuda")
+        fn = lambda: tp.tp_mlp_backward(plan, X, W1, W3, W2, dZ, UG, dX, dW1, dW3, dW2, db2, False,
+                                        wsb, nws, stream)
+        work = sum(v for _, v in mlp_backward_kernel_flops(M, h, f))
     elif args.case == "attn":
         kvn = max(k // t, 1)
         W = (a // t + 2 * kvn) * d
@@ -627,8 +667,10 @@ def main(argv=None):
     ap.add_argument("--case", default="layer",
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
                              "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer",
-                             "partials_layer"],
+                             "partials_layer", "mlp_backward", "mlp_backward_recompute"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="mlp_backward cases: tokens (0 = the layer's 8192), for small captures")
     ap.add_argument("--dominant-traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args(argv)

@@ -86,7 +86,7 @@ enum { TP_REDUCE_FUSED = 0, TP_REDUCE_PARTIALS = 1 };
 enum { TP_F32 = 0, TP_BF16 = 1 };
 
 /* Operations whose workspace size tp_plan_workspace_bytes reports. */
-enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2 };
+enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2, TP_OP_MLP_BACKWARD = 3 };
 
 /* Index tables tp_plan_shard_table exports (int32, row-major):
  *  FFN_SHARDS  [t][2]: first column of shard i in the ffn dimension, width f/t
@@ -250,6 +250,45 @@ TP_API int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, c
 TP_API int tp_mlp_forward_noalloc(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1,
                                   const tp_bf16* W3, const tp_bf16* W2, const tp_bf16* b2,
                                   const tp_bf16* residual, tp_bf16* Z, void* stream);
+
+/* tp_mlp_forward that also saves what its backward needs: the
+ * pre-activations UG, bf16, [M][f] U = X W1^T for GeLU / none, [M][2f] for
+ * SwiGLU (U at columns [0, f), G = X W3^T at [f, 2f)); shard i's slice of
+ * U (and G) is its column block i of width f/t, the layout of the colwise
+ * output.  Everything else as tp_mlp_forward.  UG: device, 16-byte
+ * aligned, not aliasing the other buffers. */
+TP_API int tp_mlp_forward_train(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1,
+                                const tp_bf16* W3, const tp_bf16* W2, const tp_bf16* b2,
+                                const tp_bf16* residual, void* partials, tp_bf16* Z, tp_bf16* UG,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward of the sharded MLP ([wiki] "통신 연산 f와 g": g, at the block's
+ * output, is the identity in the backward pass, so every shard receives
+ * the same dZ; f, at its input, becomes the all-reduce of the shards'
+ * partial input gradients).  With dZ = dL/dZ [M][h]:
+ *   dH_i  = dZ W2_i                                  (W2_i: columns of shard i)
+ *   dU_i  = dH_i (.) act'(U_i);  SwiGLU: dU_i = dH_i (.) G_i (.) SiLU'(U_i),
+ *           dG_i = dH_i (.) SiLU(U_i)
+ *   dX    = sum_i dU_i W1_i (+ dG_i W3_i)           (f's all-reduce; the sum
+ *           over i runs inside one accumulator, as the FUSED forward's g)
+ *   dW1_i = dU_i^T X,  dW3_i = dG_i^T X,  dW2_i = dZ^T H_i,  db2 = sum_m dZ[m]
+ * where H_i = act(U_i) (SwiGLU: SiLU(U_i) (.) G_i) and W1_i, W3_i are the row
+ * blocks of shard i.  Any residual added in the forward passes dZ through
+ * unchanged; it is the caller's.
+ * X [M][h], W1, W3 [f][h], W2 [h][f], dZ [M][h]: device bf16 as in
+ * tp_mlp_forward.  UG: the pre-activations tp_mlp_forward_train saved, or
+ * NULL to recompute them here (one more colwise GEMM).
+ * dX: device [M][h] bf16.  dW1, dW3: device [f][h] fp32 (dW3 must be NULL
+ * unless act is SwiGLU), dW2: [h][f] fp32, db2: [h] fp32 or NULL.  With
+ * accumulate != 0 the weight gradients are added to what the buffers hold
+ * (gradient accumulation over micro-batches); else they are overwritten.
+ * Workspace: tp_plan_workspace_bytes(TP_OP_MLP_BACKWARD) bytes, device.
+ * SwiGLU needs f to be a multiple of 64 (TP_ERR_UNSUPPORTED otherwise);
+ * the reduce mode and partial dtype of the plan do not apply. */
+TP_API int tp_mlp_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                           const tp_bf16* W2, const tp_bf16* dZ, const tp_bf16* UG, tp_bf16* dX,
+                           float* dW1, float* dW3, float* dW2, float* db2, int accumulate,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------ packed projections */
 

@@ -96,6 +96,9 @@ struct Layout {
     size_t partials = 0; // [t][M][h] fp32 or bf16 (layer in PARTIALS mode)
     size_t ss = 0;       // 2 x [M] fp32 row sums of squares (layer in FUSED mode)
     size_t full = 0;     // [M][h] bf16 all-gathered block input (sequence parallel)
+    size_t ug = 0;       // MLP backward: recomputed pre-activations [M][f or 2f] bf16
+    size_t dug = 0;      // MLP backward: dU (| dG) [M][f or 2f] bf16
+    size_t hact = 0;     // MLP backward: activations H [M][f] bf16
 };
 
 size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
@@ -109,6 +112,12 @@ Layout layout_of(const tp_plan_s* p, int op) {
             L.qkv = align_up(M * p->t * p->qkv_w * 2);
             L.o = align_up(M * p->a * p->d * 2);
         }
+    }
+    if (op == TP_OP_MLP_BACKWARD && p->has_mlp) {
+        const size_t wu = (p->cfg.act == TP_ACT_SWIGLU ? 2 : 1) * static_cast<size_t>(p->f);
+        L.ug = align_up(M * wu * 2);
+        L.dug = align_up(M * wu * 2);
+        L.hact = align_up(M * p->f * 2);
     }
     if (op == TP_OP_LAYER) {
         L.h1 = align_up(M * p->h * 2);
@@ -124,7 +133,7 @@ Layout layout_of(const tp_plan_s* p, int op) {
 }
 
 size_t layout_total(const Layout& L) {
-    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full;
+    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact;
 }
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
@@ -145,7 +154,7 @@ int run(int rc, const std::string& err) {
 // ---- building blocks (arguments already validated) ----
 
 int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3, void* Y,
-               cudaStream_t s, const float* row_ss = nullptr) {
+               cudaStream_t s, const float* row_ss = nullptr, void* UG = nullptr) {
     tpi::GemmArgs g;
     g.mode = (p->cfg.act == TP_ACT_SWIGLU) ? tpi::GEMM_COL_SWIGLU : tpi::GEMM_COL_ACT;
     g.act = p->cfg.act;
@@ -162,6 +171,9 @@ int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3
     }
     g.out = Y;
     g.ldo = p->f;
+    g.aux_out = UG;  // pre-activations U (| G), saved for the backward pass
+    g.ldaux = (p->cfg.act == TP_ACT_SWIGLU ? 2 : 1) * p->f;
+    g.n_half = p->f;
     g.row_ss = row_ss;
     g.inv_h = 1.0f / static_cast<float>(p->h);
     g.eps = p->cfg.rms_eps;
@@ -409,7 +421,7 @@ int tp_plan_destroy(tp_plan_t plan) {
 
 int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes) {
     if (!plan || !bytes) return fail(TP_ERR_INVALID_ARG, "plan and bytes must be non-NULL");
-    if (op < TP_OP_MLP || op > TP_OP_LAYER) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
+    if (op < TP_OP_MLP || op > TP_OP_MLP_BACKWARD) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
     *bytes = layout_total(layout_of(plan, op));
     return TP_OK;
 }
@@ -534,15 +546,17 @@ int tp_rowwise_forward(tp_plan_t plan, const tp_bf16* Y, const tp_bf16* W2, cons
                       as_stream(stream));
 }
 
-int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
-                   const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
-                   tp_bf16* Z, void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+int mlp_forward_impl(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                     const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
+                     tp_bf16* Z, tp_bf16* UG, void* workspace, size_t ws_bytes, void* stream) {
     if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
     if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
     int rc;
     if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(W1, "W1")) ||
         (rc = need_ptr(W2, "W2")) || (rc = need_ptr(Z, "Z")) || (rc = opt_ptr(b2, "b2")) ||
-        (rc = opt_ptr(residual, "residual")))
+        (rc = opt_ptr(residual, "residual")) || (rc = opt_ptr(UG, "UG")))
         return rc;
     if (plan->cfg.act == TP_ACT_SWIGLU) {
         if ((rc = need_ptr(W3, "W3 (SwiGLU)"))) return rc;
@@ -554,9 +568,137 @@ int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp
     if ((rc = check_ws(plan, TP_OP_MLP, workspace, ws_bytes))) return rc;
     cudaStream_t s = as_stream(stream);
     void* Y = workspace;
-    if ((rc = do_colwise(plan, X, W1, W3, Y, s))) return rc;
+    if ((rc = do_colwise(plan, X, W1, W3, Y, s, nullptr, UG))) return rc;
     if ((rc = do_rowwise(plan, Y, plan->fw, W2, plan->h, b2, residual, partials, Z, fused, s))) return rc;
     if (!fused) return do_reduce(plan, partials, b2, residual, Z, plan->h, s);
+    return TP_OK;
+}
+
+}  // namespace
+
+int tp_mlp_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                   const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual, void* partials,
+                   tp_bf16* Z, void* workspace, size_t ws_bytes, void* stream) {
+    return mlp_forward_impl(plan, X, W1, W3, W2, b2, residual, partials, Z, nullptr, workspace,
+                            ws_bytes, stream);
+}
+
+int tp_mlp_forward_train(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                         const tp_bf16* W2, const tp_bf16* b2, const tp_bf16* residual,
+                         void* partials, tp_bf16* Z, tp_bf16* UG, void* workspace, size_t ws_bytes,
+                         void* stream) {
+    if (!UG) return fail(TP_ERR_INVALID_ARG, "UG is NULL");
+    return mlp_forward_impl(plan, X, W1, W3, W2, b2, residual, partials, Z, UG, workspace,
+                            ws_bytes, stream);
+}
+
+int tp_mlp_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const tp_bf16* W3,
+                    const tp_bf16* W2, const tp_bf16* dZ, const tp_bf16* UG, tp_bf16* dX,
+                    float* dW1, float* dW3, float* dW2, float* db2, int accumulate, void* workspace,
+                    size_t ws_bytes, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_mlp) return fail(TP_ERR_INVALID_ARG, "the plan has no MLP (ffn == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(W1, "W1")) ||
+        (rc = need_ptr(W2, "W2")) || (rc = need_ptr(dZ, "dZ")) || (rc = opt_ptr(UG, "UG")) ||
+        (rc = need_ptr(dX, "dX")) || (rc = need_ptr(dW1, "dW1")) || (rc = need_ptr(dW2, "dW2")) ||
+        (rc = opt_ptr(db2, "db2")))
+        return rc;
+    const bool glu = plan->cfg.act == TP_ACT_SWIGLU;
+    if (glu) {
+        if ((rc = need_ptr(W3, "W3 (SwiGLU)")) || (rc = need_ptr(dW3, "dW3 (SwiGLU)"))) return rc;
+        if (plan->f % 64 != 0)
+            return fail(TP_ERR_UNSUPPORTED, "the SwiGLU backward needs ffn %% 64 == 0 (ffn = %lld)",
+                        static_cast<long long>(plan->f));
+    } else if (W3 || dW3) {
+        return fail(TP_ERR_INVALID_ARG, "W3 and dW3 must be NULL unless act is TP_ACT_SWIGLU");
+    }
+    if ((rc = check_ws(plan, TP_OP_MLP_BACKWARD, workspace, ws_bytes))) return rc;
+    const Layout L = layout_of(plan, TP_OP_MLP_BACKWARD);
+    void* ug_ws = region(workspace, 0);
+    void* dug = region(workspace, L.ug);
+    void* hact = region(workspace, L.ug + L.dug);
+    cudaStream_t s = as_stream(stream);
+    const int64_t M = plan->M, h = plan->h, f = plan->f, wu = (glu ? 2 : 1) * f;
+    std::string err;
+    // Pre-activations: the caller's, or recomputed together with H.
+    const void* ug = UG;
+    if (!UG) {
+        if ((rc = do_colwise(plan, X, W1, W3, hact, s, nullptr, ug_ws))) return rc;
+        ug = ug_ws;
+    }
+    {  // dH = dZ W2 (g backward: the same dZ for every shard), then dU (| dG), H.
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_BWD_ACT;
+        g.act = plan->cfg.act;
+        g.M = M;
+        g.N = f;
+        g.K = h;
+        g.A = dZ;
+        g.B0 = W2;
+        g.aux = ug;
+        g.ldaux = wu;
+        g.n_half = f;
+        g.out = dug;
+        g.ldo = wu;
+        g.out2 = UG ? hact : nullptr;  // recomputation already wrote H
+        g.ldo2 = f;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // dX = [dU | dG] [W1 ; W3]: f's all-reduce as the K loop over all shards.
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_NN;
+        g.M = M;
+        g.N = h;
+        g.K = wu;
+        g.A = dug;
+        g.B0 = W1;
+        g.B1 = glu ? W3 : nullptr;
+        g.k_split = f;
+        g.out = dX;
+        g.ldo = h;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // dW2 = dZ^T H (shard i: columns i f/t .. of dW2).
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_TN;
+        g.M = h;
+        g.N = f;
+        g.K = M;
+        g.A = dZ;
+        g.lda = h;
+        g.B0 = hact;
+        g.out = dW2;
+        g.ldo = f;
+        g.accumulate = accumulate ? 1 : 0;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // [dW1 ; dW3] = [dU | dG]^T X (shard i: rows i f/t .. of each).
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_TN;
+        g.M = wu;
+        g.N = h;
+        g.K = M;
+        g.A = dug;
+        g.lda = wu;
+        g.B0 = X;
+        g.out = dW1;
+        g.ldo = h;
+        g.out2 = glu ? dW3 : nullptr;
+        g.ldo2 = h;
+        g.row_split = f;
+        g.accumulate = accumulate ? 1 : 0;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    if (db2) return run(tpi::colsum_launch(dZ, M, static_cast<int>(h), db2, accumulate, s, &err), err);
     return TP_OK;
 }
 

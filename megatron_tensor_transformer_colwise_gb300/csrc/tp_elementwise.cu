@@ -290,6 +290,64 @@ int check_launch(const char* what, std::string* err) {
     return TP_OK;
 }
 
+// Column sums of a bf16 [rows][h] matrix into fp32 (the bias gradient
+// db = sum over tokens of dZ), deterministic: block (CS_X, CS_Y) owns
+// CS_X * 8 columns over all rows; thread (x, y) adds rows y, y + CS_Y, ...
+// in order, then a fixed-shape tree over y in shared memory.  No atomics,
+// so repeated calls give identical bits.
+constexpr int CS_X = 4, CS_Y = 128;
+
+__global__ void __launch_bounds__(CS_X * CS_Y) colsum_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            long long rows, int h,
+                                                            float* __restrict__ out, int accumulate) {
+    __shared__ float part[CS_Y][CS_X * 8 + 1];
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int col = (blockIdx.x * CS_X + tx) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (col < h) {
+        long long r = ty;
+        for (; r + 3 * CS_Y < rows; r += 4 * CS_Y) {
+            uint4 u[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u[k] = *reinterpret_cast<const uint4*>(x + (r + k * CS_Y) * h + col);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16x2(w[e]);
+                    acc[2 * e] += f.x;
+                    acc[2 * e + 1] += f.y;
+                }
+            }
+        }
+        for (; r < rows; r += CS_Y) {
+            const uint4 u = *reinterpret_cast<const uint4*>(x + r * h + col);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16x2(w[e]);
+                acc[2 * e] += f.x;
+                acc[2 * e + 1] += f.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[ty][tx * 8 + e] = acc[e];
+    __syncthreads();
+    for (int sh = CS_Y / 2; sh > 0; sh >>= 1) {
+        if (ty < sh) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part[ty][tx * 8 + e] += part[ty + sh][tx * 8 + e];
+        }
+        __syncthreads();
+    }
+    if (ty == 0 && col < h) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[col + e] = (accumulate ? out[col + e] : 0.f) + part[0][tx * 8 + e];
+    }
+}
+
 }  // namespace
 
 namespace tpi {
@@ -383,6 +441,15 @@ int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int 
         reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
         reinterpret_cast<__nv_bfloat16*>(full));
     return check_launch("all-gather kernel", err);
+}
+
+int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate,
+                  cudaStream_t stream, std::string* err) {
+    if (h == 0) return TP_OK;
+    const unsigned gx = static_cast<unsigned>((h / 8 + CS_X - 1) / CS_X);
+    colsum_kernel<<<gx, dim3(CS_X, CS_Y), 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                                      rows, h, out, accumulate);
+    return check_launch("column-sum kernel", err);
 }
 
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,

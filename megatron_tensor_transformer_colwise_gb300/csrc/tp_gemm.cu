@@ -9,14 +9,16 @@
 // rowwise).
 //
 // One kernel template, one CTA per SM (persistent), CTAs in pairs
-// (clusters of 2) that share a 256 x 256 output tile, 6 warps per CTA:
+// (clusters of 2) that share a 256 x 256 output tile, 6 or 10 warps per CTA:
 //   warp 0      TMA producer (one lane): this CTA's 128 rows of A and half of
 //               the tile's 256 B rows into a 6-stage ring (32 KB stages);
 //               completion is counted on the pair leader's barriers
 //   warp 1      TMEM owner; in the leader CTA also the MMA issuer (one lane):
 //               256x256x16 bf16 UMMAs (tcgen05 cta_group::2) that read both
 //               CTAs' shared memory and accumulate 128 rows in each CTA's TMEM
-//   warps 2..5  epilogue: TMEM -> registers -> fused op -> global
+//   warps 2..   epilogue: TMEM -> registers -> fused op -> global (4 warps,
+//               one per TMEM lane quadrant; 8 for the activation-gradient
+//               epilogue, two per quadrant on halves of the tile's columns)
 // The accumulator is double-buffered in TMEM (2 x 256 fp32 columns) so the
 // epilogue of tile n overlaps the main loop of tile n+1.  Splitting B over
 // the pair halves each SM's shared-memory operand traffic per FLOP.
@@ -55,21 +57,43 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_CHUNK_ROWS = 64;
 constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
 constexpr int TMEM_COLS = 2 * BN;               // 512
-constexpr int NUM_THREADS = 192;
+// Epilogue warps per CTA: one per TMEM lane quadrant, or two, each taking
+// half of the tile's columns, where the epilogue of a tile (the activation
+// gradient with its loads and three stores) would otherwise outlast the
+// next tile's main loop.
+#ifndef TP_GEMM_EPI_WARPS_FWD
+#define TP_GEMM_EPI_WARPS_FWD 4
+#endif
+template <int MODE>
+__host__ __device__ constexpr int epi_warps() {
+    return MODE == tpi::GEMM_BWD_ACT ? 8 : TP_GEMM_EPI_WARPS_FWD;
+}
+template <int MODE>
+__host__ __device__ constexpr int num_threads() {
+    return 64 + 32 * epi_warps<MODE>();
+}
 
 // CG = CTAs per tile.  CG = 1: a 128 x 256 tile per CTA, 4 stages of 48 KB.
 // CG = 2: a 256 x 256 tile per CTA pair (cta_group::2): each CTA loads its
 // 128 rows of A and half of the 256 B rows, 6 stages of 32 KB, and the
 // pair's leader issues 256 x 256 x 16 UMMAs that read both CTAs' shared
 // memory and write 128 accumulator rows into each CTA's TMEM.
-template <int CG>
+//
+// GEMM_BWD_ACT stages its three outputs through shared memory (one 32 x 32
+// bf16 box per output and epilogue warp, 64-byte swizzle) and writes them
+// with TMA stores; it runs one ring stage fewer to make room.
+constexpr int EPI_BOX = 32;                        // rows and columns of an output box
+constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;  // 2 KB
+template <int MODE, int CG>
 struct Cfg {
     static constexpr int B_BYTES = (BN / CG) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr bool STAGED_OUT = MODE == tpi::GEMM_BWD_ACT;
+    static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : 6);
     static constexpr int CHUNKS = (BN / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
+    static constexpr int EPI_BYTES = STAGED_OUT ? 8 * 3 * EPI_BOX_BYTES : 0;  // 8 warps x 3 boxes
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TILE_M = BM * CG;
 };
 
@@ -97,9 +121,31 @@ struct GemmParams {
     const float* row_ss;  // colwise: scale row by rsqrt(row_ss * inv_h + eps)
     float* ss_out;        // ROW_FUSED: += sum of squares of the row's bf16 outputs
     float inv_h, eps;
+    // Backward modes (see tpi::GemmArgs).
+    const __nv_bfloat16* aux;  // BWD_ACT: saved pre-activations U (| G)
+    __nv_bfloat16* aux_out;    // COL_ACT / COL_SWIGLU: pre-activations out
+    long long ldaux, n_half;
+    void* out2;
+    long long ldo2;
+    int k_split;    // GEMM_NN: first K row read from mapB[1]
+    int row_split;  // GEMM_TN: first output row written to out2
+    int accumulate;
+    CUtensorMap mapO[3];  // BWD_ACT: TMA-store maps of dU, dG, H (64-byte swizzle)
     unsigned* status;
     unsigned long long timeout_ns;
 };
+
+// Which operands a mode reads MN-major (M or N index contiguous in global
+// memory, [K][M] / [K][N]); the others are K-major ([M][K] / [N][K]).
+template <int MODE>
+struct Major {
+    static constexpr bool A_MN = MODE == tpi::GEMM_TN;
+    static constexpr bool B_MN =
+        MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_NN || MODE == tpi::GEMM_TN;
+};
+// An MN-major operand tile is stored as 64-element (128-byte) MN blocks of
+// BK = 64 swizzled K rows each, MN_BLOCK_BYTES apart.
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // 8 KB
 
 __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& s, int& mb,
                                             int& nb) {
@@ -126,6 +172,72 @@ __device__ __forceinline__ float act_apply(int act, float v) {
     if (act == TP_ACT_GELU_TANH)
         return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * (v + 0.044715f * v * v * v)));
     return v;
+}
+
+// Backward of the MLP nonlinearity at one element: from the pre-activation
+// u (and the SwiGLU up value g) and dh = dL/dH, the gradients du (and dg)
+// and the forward value hv = H.
+//   SwiGLU  H = SiLU(u) g:  du = dh g s (1 + u (1 - s)), s = sigmoid(u);
+//           dg = dh SiLU(u)
+//   GeLU    H = u Phi(u):   du = dh (Phi(u) + u phi(u))
+//   GeLU (tanh form) H = u/2 (1 + T), T = tanh(c (u + a u^3)):
+//           du = dh (1/2 (1 + T) + u/2 (1 - T^2) c (1 + 3 a u^2))
+template <int ACT>
+__device__ __forceinline__ void act_backward(float u, float g, float dh, float& du, float& dg,
+                                             float& hv) {
+    dg = 0.0f;
+    if (ACT == TP_ACT_SWIGLU) {
+        // Fast-math sigmoid (the results are rounded to bf16).
+        const float s = __fdividef(1.0f, 1.0f + __expf(-u));
+        const float silu = u * s;
+        hv = silu * g;
+        dg = dh * silu;
+        du = dh * g * (s * (1.0f + u * (1.0f - s)));
+    } else if (ACT == TP_ACT_GELU_ERF) {
+        const float cdf = 0.5f * (1.0f + erff(u * 0.70710678118654752f));
+        const float pdf = 0.39894228040143268f * expf(-0.5f * u * u);
+        hv = u * cdf;
+        du = dh * (cdf + u * pdf);
+    } else if (ACT == TP_ACT_GELU_TANH) {
+        const float c = 0.79788456080286536f, a = 0.044715f;
+        const float th = tanhf(c * (u + a * u * u * u));
+        hv = 0.5f * u * (1.0f + th);
+        du = dh * (0.5f * (1.0f + th) + 0.5f * u * (1.0f - th * th) * c * (1.0f + 3.0f * a * u * u));
+    } else {
+        hv = u;
+        du = dh;
+    }
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// U (and G) of one 32-column chunk of an epilogue row (BWD_ACT): four
+// 16-byte loads each, zeros outside the matrix.
+__device__ __forceinline__ void load_ug_chunk(const GemmParams& p, const __nv_bfloat16* ug, bool row_ok,
+                                              bool glu, int col0, uint4 (&u)[4], uint4 (&g)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int col = col0 + e * 8;
+        const bool ok = row_ok && col < p.N;
+        u[e] = ok ? ld_nc_v4(ug + col) : make_uint4(0, 0, 0, 0);
+        g[e] = (ok && glu) ? ld_nc_v4(ug + p.n_half + col) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float (&x)[8]) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(a[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
 }
 
 __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -203,7 +315,7 @@ __device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, int first,
 template <int MODE, int CG>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                               uint32_t rank, volatile int* abort_flag) {
-    using C = Cfg<CG>;
+    using C = Cfg<MODE, CG>;
     constexpr bool ROW = (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
@@ -239,6 +351,21 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                         const int r = c < 0 ? arow : nb * BN + cc * B_CHUNK_ROWS;
                         if (CG == 2) tma_load_3d_pair(dst, map, full_l, kc, shard, r);
                         else tma_load_3d(dst, map, full_l, kc, shard, r);
+                    } else if (c < 0 && Major<MODE>::A_MN) {
+                        // [K][M] source: the CTA's 128 A rows as two 64-wide blocks.
+#pragma unroll
+                        for (int e = 0; e < BM / 64; ++e) {
+                            if (CG == 2)
+                                tma_load_2d_pair(dst + e * MN_BLOCK_BYTES, &p.mapA, full_l, arow + 64 * e, kc);
+                            else tma_load_2d(dst + e * MN_BLOCK_BYTES, &p.mapA, full_l, arow + 64 * e, kc);
+                        }
+                    } else if (c >= 0 && Major<MODE>::B_MN) {
+                        // [K][N] source; GEMM_NN takes K rows >= k_split from B1.
+                        const bool hi = MODE == tpi::GEMM_NN && kc >= p.k_split;
+                        const CUtensorMap* map = hi ? &p.mapB[1] : &p.mapB[0];
+                        const int kk = hi ? kc - p.k_split : kc;
+                        if (CG == 2) tma_load_2d_pair(dst, map, full_l, brow[c < 0 ? 0 : c], kk);
+                        else tma_load_2d(dst, map, full_l, brow[c < 0 ? 0 : c], kk);
                     } else {
                         const CUtensorMap* map = c < 0 ? &p.mapA : bmap[c < 0 ? 0 : c];
                         const int r = c < 0 ? arow : brow[c < 0 ? 0 : c];
@@ -263,11 +390,18 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
     }
 }
 
-template <int CG>
+template <int MODE, int CG>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                          uint32_t tmem_base, volatile int* abort_flag) {
-    using C = Cfg<CG>;
-    constexpr uint32_t idesc = idesc_bf16_f32(BM * CG, BN);
+    using C = Cfg<MODE, CG>;
+    constexpr bool AMN = Major<MODE>::A_MN, BMN = Major<MODE>::B_MN;
+    // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
+    constexpr uint32_t idesc =
+        idesc_bf16_f32(BM * CG, BN) | (AMN ? (1u << 15) : 0u) | (BMN ? (1u << 16) : 0u);
+    // Per UMMA (K = 16): a K-major operand advances 32 bytes inside its
+    // swizzle row (2 in descriptor units), an MN-major one 16 K rows of
+    // 128 bytes (128 units).
+    constexpr uint64_t a_step = AMN ? 128u : 2u, b_step = BMN ? 128u : 2u;
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     const int kblocks = p.k_shards * p.kb_per_shard;
@@ -289,14 +423,16 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
             }
             tc_fence_after();
             const uint32_t a_addr = base + stage * C::STAGE_BYTES;
-            const uint64_t adesc = sdesc_sw128(a_addr);
-            const uint64_t bdesc = sdesc_sw128(a_addr + A_BYTES);
+            const uint64_t adesc = AMN ? sdesc_sw128_mn(a_addr, MN_BLOCK_BYTES, 1024)
+                                       : sdesc_sw128(a_addr);
+            const uint64_t bdesc = BMN ? sdesc_sw128_mn(a_addr + A_BYTES, MN_BLOCK_BYTES, 1024)
+                                       : sdesc_sw128(a_addr + A_BYTES);
 #pragma unroll
             for (int j = 0; j < BK / UK; ++j) {
-                // +32 bytes along K inside the 128-byte swizzle row.
                 const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-                if (CG == 2) umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, accum);
-                else umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc, accum);
+                const uint64_t ad = adesc + a_step * j, bd = bdesc + b_step * j;
+                if (CG == 2) umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+                else umma_bf16(d_tmem, ad, bd, idesc, accum);
             }
             // Frees the smem stage (of both CTAs) when these UMMAs finish.
             if (CG == 2) umma_commit_pair(empty, 0x3);
@@ -322,12 +458,91 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
     }
 }
 
+// Epilogue of GEMM_BWD_ACT for one warp's CPW 32-column chunks of a tile:
+// dH from TMEM, U (and G) from the prefetch ring (chunks c and c + 1 already
+// requested; each chunk requests c + 2).  dU, dG and H of a chunk go to the
+// warp's three 32 x 32 boxes in shared memory, stored in the 64-byte swizzle
+// (16-byte piece j of row r at r * 64 + (j ^ ((r >> 1) & 3)) * 16, which
+// also keeps the 32 rows' writes free of bank conflicts), and leave by TMA
+// stores (whole rows per request; rows and columns outside the matrices are
+// clipped by the tensor maps).  row0: first global row of the warp's box.
+template <int ACT, int CPW>
+__device__ __forceinline__ void bwd_act_tile(const GemmParams& p, const __nv_bfloat16* ug, bool row_ok,
+                                             int row0, int nb, int cb, uint32_t t0, uint32_t sbuf,
+                                             uint4 (&n1u)[4], uint4 (&n1g)[4], uint4 (&n2u)[4],
+                                             uint4 (&n2g)[4]) {
+    constexpr bool glu = ACT == TP_ACT_SWIGLU;
+    const int lane = threadIdx.x & 31;
+    const bool want_h = p.out2 != nullptr;
+    const bool box_ok = row0 < p.M;  // warp-uniform
+    const uint32_t srow = sbuf + static_cast<uint32_t>(lane) * (EPI_BOX * 2);
+    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int cc = 0; cc < CPW; ++cc) {  // kept rolled: instruction-cache footprint
+        const int c = cb + cc;
+        const int col0 = nb * BN + c * 32;
+        if (col0 >= p.N) break;  // warp-uniform
+        uint4 cu[4], cg[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            cu[e] = n1u[e];
+            cg[e] = n1g[e];
+            n1u[e] = n2u[e];
+            n1g[e] = n2g[e];
+        }
+        // The loads of chunk c + 2 are in flight during this chunk's math.
+        if (cc + 2 < CPW) load_ug_chunk(p, ug, row_ok, glu, col0 + 64, n2u, n2g);
+        __syncwarp();
+        tmem_ld32(t0 + c * 32, r);  // dH
+        tmem_ld_wait();
+        // The boxes may be rewritten once the previous chunk's stores have
+        // read them.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float uu[8], gg[8];
+            unpack8(cu[g], uu);
+            unpack8(cg[g], gg);
+            uint32_t wu[4], wg[4], wh[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float du0, dg0, h0, du1, dg1, h1;
+                act_backward<ACT>(uu[2 * e], gg[2 * e], __uint_as_float(r[g * 8 + 2 * e]), du0, dg0, h0);
+                act_backward<ACT>(uu[2 * e + 1], gg[2 * e + 1], __uint_as_float(r[g * 8 + 2 * e + 1]),
+                                  du1, dg1, h1);
+                wu[e] = pack_bf16x2(du0, du1);
+                wg[e] = pack_bf16x2(dg0, dg1);
+                wh[e] = pack_bf16x2(h0, h1);
+            }
+            const uint32_t off = (static_cast<uint32_t>(g) ^ sw) << 4;
+            st_shared_v4(srow + off, wu[0], wu[1], wu[2], wu[3]);
+            if (glu) st_shared_v4(srow + EPI_BOX_BYTES + off, wg[0], wg[1], wg[2], wg[3]);
+            if (want_h) st_shared_v4(srow + 2 * EPI_BOX_BYTES + off, wh[0], wh[1], wh[2], wh[3]);
+        }
+        fence_proxy_async_smem();  // visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && box_ok) {
+            tma_store_2d(&p.mapO[0], sbuf, col0, row0);
+            if (glu) tma_store_2d(&p.mapO[1], sbuf + EPI_BOX_BYTES, col0, row0);
+            if (want_h) tma_store_2d(&p.mapO[2], sbuf + 2 * EPI_BOX_BYTES, col0, row0);
+            bulk_commit_group();
+        }
+    }
+}
+
 template <int MODE, int CG>
-__device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t tmem_base,
-                                              uint32_t rank, volatile int* abort_flag) {
-    using C = Cfg<CG>;
+__device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t epi0,
+                                              uint32_t tmem_base, uint32_t rank, volatile int* abort_flag) {
+    using C = Cfg<MODE, CG>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    constexpr int EPI_WARPS = epi_warps<MODE>();
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns (8 warps)
+    constexpr int CPW = (BN / 32) / (EPI_WARPS / 4);        // 32-column chunks per warp
+    constexpr int CPW_GLU = (BN / 64) / (EPI_WARPS / 4);    // SwiGLU: output chunks per warp
+    const int cb = half * CPW, cb_glu = half * CPW_GLU;
     uint32_t acc = 0, acc_phase = 0;
     const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
     for (int tile = cid; tile < p.num_tiles; tile += ncl) {
@@ -335,12 +550,23 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         decode_tile(p, tile, s_grid, mb, nb);
         const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
         const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
+        const int row = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
+        const bool row_ok = row < p.M;
+        // BWD_ACT: the saved pre-activations of the warp's first two chunks
+        // are fetched while the accumulator is still being computed; each
+        // chunk then prefetches the one two ahead.
+        const bool glu = p.act == TP_ACT_SWIGLU;
+        const __nv_bfloat16* ug =
+            MODE == tpi::GEMM_BWD_ACT ? p.aux + static_cast<long long>(row_ok ? row : 0) * p.ldaux : nullptr;
+        uint4 n1u[4], n1g[4], n2u[4], n2g[4];
+        if (MODE == tpi::GEMM_BWD_ACT) {
+            load_ug_chunk(p, ug, row_ok, glu, nb * BN + cb * 32, n1u, n1g);
+            load_ug_chunk(p, ug, row_ok, glu, nb * BN + cb * 32 + 32, n2u, n2g);
+        }
         const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status, p.timeout_ns);
         __syncwarp();
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
-        const int row = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
-        const bool row_ok = row < p.M;
         // Folded RMSNorm of the A rows (colwise modes): per-row scale.
         float rs = 1.0f;
         if (MODE != tpi::GEMM_ROW_FUSED && MODE != tpi::GEMM_ROW_PARTIAL && p.row_ss && row_ok)
@@ -348,10 +574,28 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         float ssq = 0.0f;
         const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
         uint32_t r[32];
-        if (MODE == tpi::GEMM_COL_SWIGLU) {
+        if (MODE == tpi::GEMM_BWD_ACT) {
+            // One branch-free chunk loop per activation, chosen once per tile.
+            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const uint32_t sbuf = epi0 + static_cast<uint32_t>(warp - 2) * 3 * EPI_BOX_BYTES;
+            switch (p.act) {
+                case TP_ACT_SWIGLU:
+                    bwd_act_tile<TP_ACT_SWIGLU, CPW>(p, ug, row_ok, row0, nb, cb, t0, sbuf, n1u, n1g, n2u, n2g);
+                    break;
+                case TP_ACT_GELU_ERF:
+                    bwd_act_tile<TP_ACT_GELU_ERF, CPW>(p, ug, row_ok, row0, nb, cb, t0, sbuf, n1u, n1g, n2u, n2g);
+                    break;
+                case TP_ACT_GELU_TANH:
+                    bwd_act_tile<TP_ACT_GELU_TANH, CPW>(p, ug, row_ok, row0, nb, cb, t0, sbuf, n1u, n1g, n2u, n2g);
+                    break;
+                default:
+                    bwd_act_tile<TP_ACT_NONE, CPW>(p, ug, row_ok, row0, nb, cb, t0, sbuf, n1u, n1g, n2u, n2g);
+                    break;
+            }
+        } else if (MODE == tpi::GEMM_COL_SWIGLU) {
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
-            for (int c = 0; c < (BN / 2) / 32; ++c) {
+            for (int c = cb_glu; c < cb_glu + CPW_GLU; ++c) {
                 if (nb * (BN / 2) + c * 32 >= p.N) break;  // warp-uniform
                 uint32_t u[32];
                 __syncwarp();
@@ -364,7 +608,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                     for (int g = 0; g < 4; ++g) {
                         const int col = col0 + g * 8;
                         if (col < p.N) {
-                            uint32_t w[4];
+                            uint32_t w[4], pg[4], pu[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float g0 = __uint_as_float(r[g * 8 + 2 * e]) * rs;
@@ -374,16 +618,23 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                                 const float h0 = g0 / (1.0f + expf(-g0)) * u0;
                                 const float h1 = g1 / (1.0f + expf(-g1)) * u1;
                                 w[e] = pack_bf16x2(h0, h1);
+                                pg[e] = pack_bf16x2(g0, g1);
+                                pu[e] = pack_bf16x2(u0, u1);
                             }
                             st_v4(out + static_cast<long long>(row) * p.ldo + col, w[0], w[1],
                                   w[2], w[3]);
+                            if (p.aux_out) {  // pre-activations for the backward pass
+                                __nv_bfloat16* a = p.aux_out + static_cast<long long>(row) * p.ldaux;
+                                st_v4(a + col, pg[0], pg[1], pg[2], pg[3]);
+                                st_v4(a + p.n_half + col, pu[0], pu[1], pu[2], pu[3]);
+                            }
                         }
                     }
                 }
             }
         } else {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = cb; c < cb + CPW; ++c) {
                 const int col0 = nb * BN + c * 32;
                 if (col0 >= p.N) break;  // warp-uniform
                 __syncwarp();
@@ -398,6 +649,26 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                         const int col = col0 + g * 4;
                         if (col < p.N)
                             st_v4(out + col, r[g * 4], r[g * 4 + 1], r[g * 4 + 2], r[g * 4 + 3]);
+                    }
+                } else if (MODE == tpi::GEMM_TN) {
+                    float* out = row < p.row_split
+                                     ? reinterpret_cast<float*>(p.out) + static_cast<long long>(row) * p.ldo
+                                     : reinterpret_cast<float*>(p.out2) +
+                                           static_cast<long long>(row - p.row_split) * p.ldo2;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int col = col0 + g * 4;
+                        if (col >= p.N) continue;
+                        float4 v = make_float4(__uint_as_float(r[g * 4]), __uint_as_float(r[g * 4 + 1]),
+                                               __uint_as_float(r[g * 4 + 2]), __uint_as_float(r[g * 4 + 3]));
+                        if (p.accumulate) {
+                            const float4 o = *reinterpret_cast<const float4*>(out + col);
+                            v.x += o.x;
+                            v.y += o.y;
+                            v.z += o.z;
+                            v.w += o.w;
+                        }
+                        *reinterpret_cast<float4*>(out + col) = v;
                     }
                 } else {
                     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -416,6 +687,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                             for (int e = 0; e < 8; ++e) v[e] *= rs;
                         }
                         if (MODE == tpi::GEMM_COL_ACT) {
+                            if (p.aux_out)  // pre-activations for the backward pass
+                                st_v4(p.aux_out + static_cast<long long>(row) * p.ldaux + col,
+                                      pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
                         }
@@ -470,18 +745,24 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }
+    // Staged outputs: every TMA store has completed before the CTA moves on
+    // (its shared memory stays valid until then).
+    if (C::STAGED_OUT && lane == 0) bulk_wait_group0();
+    __syncwarp();
 }
 
 template <int MODE, int CG>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = Cfg<CG>;
+__global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
+    constexpr int EPI_WARPS = epi_warps<MODE>();
+    using C = Cfg<MODE, CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(gbase + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 5));
+    const uint32_t epi0 = base + C::STAGES * C::STAGE_BYTES;  // staged output boxes
+    const uint32_t bar0 = epi0 + C::EPI_BYTES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES +
+                                                      8 * (2 * C::STAGES + 5));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -493,8 +774,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_co
         }
         mbar_init(bar0 + 8 * (2 * C::STAGES + 0), 1);       // tmem full x2: one commit
         mbar_init(bar0 + 8 * (2 * C::STAGES + 1), 1);
-        mbar_init(bar0 + 8 * (2 * C::STAGES + 2), 4 * CG);  // tmem empty x2: epilogue warps
-        mbar_init(bar0 + 8 * (2 * C::STAGES + 3), 4 * CG);
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 2), EPI_WARPS * CG);  // tmem empty x2: epilogue warps
+        mbar_init(bar0 + 8 * (2 * C::STAGES + 3), EPI_WARPS * CG);
         mbar_init(bar0 + 8 * (2 * C::STAGES + 4), 1);       // drain
         *abort_flag = 0;
         fence_barrier_init();
@@ -502,7 +783,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_co
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.mapA);
         tma_prefetch_desc(&p.mapB[0]);
-        if (MODE == tpi::GEMM_COL_SWIGLU || MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[1]);
+        if (MODE == tpi::GEMM_COL_SWIGLU || MODE == tpi::GEMM_COL_QKV || MODE == tpi::GEMM_NN)
+            tma_prefetch_desc(&p.mapB[1]);
         if (MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[2]);
     }
     if (warp == 1) {
@@ -524,9 +806,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tp_gemm_kernel(const __grid_co
     if (warp == 0) {
         if (lane == 0) producer_loop<MODE, CG>(p, base, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) mma_loop<CG>(p, base, bar0, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) mma_loop<MODE, CG>(p, base, bar0, tmem_base, abort_flag);
     } else {
-        epilogue_loop<MODE, CG>(p, bar0, tmem_base, rank, abort_flag);
+        epilogue_loop<MODE, CG>(p, bar0, epi0, tmem_base, rank, abort_flag);
     }
     __syncwarp();
     tc_fence_before();
@@ -565,7 +847,8 @@ EncodeTiledFn encode_fn(std::string* err) {
 // bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
 // bytes for dims 1.., box innermost first.
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box, std::string* err) {
+              const uint64_t* strides, const uint32_t* box, std::string* err,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn(err);
     if (!fn) return false;
     cuuint64_t d[3], s[2];
@@ -576,7 +859,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     }
     for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, s, b, e,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         if (err) *err = "cuTensorMapEncodeTiled failed with code " + std::to_string((int)r);
@@ -593,7 +876,7 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<CG>::SMEM);
+                                             Cfg<MODE, CG>::SMEM);
         if (e != cudaSuccess) {
             if (err) *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return TP_ERR_CUDA;
@@ -603,8 +886,8 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
+    cfg.blockDim = dim3(num_threads<MODE>(), 1, 1);
+    cfg.dynamicSmemBytes = Cfg<MODE, CG>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -646,10 +929,20 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     p.ss_out = a.ss_out;
     p.inv_h = a.inv_h;
     p.eps = a.eps;
+    p.aux = reinterpret_cast<const __nv_bfloat16*>(a.aux);
+    p.aux_out = reinterpret_cast<__nv_bfloat16*>(a.aux_out);
+    p.ldaux = a.ldaux;
+    p.n_half = a.n_half;
+    p.out2 = a.out2;
+    p.ldo2 = a.ldo2;
+    p.k_split = static_cast<int>(a.k_split);
+    p.row_split = static_cast<int>(a.row_split);
+    p.accumulate = a.accumulate;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     constexpr int CG = kPairTiles;
-    p.m_tiles = static_cast<int>((a.M + Cfg<CG>::TILE_M - 1) / Cfg<CG>::TILE_M);
+    constexpr int TILE_M = BM * CG;
+    p.m_tiles = static_cast<int>((a.M + TILE_M - 1) / TILE_M);
     const int bn_out = (a.mode == GEMM_COL_SWIGLU) ? BN / 2 : BN;
     p.n_tiles = static_cast<int>((a.N + bn_out - 1) / bn_out);
     p.grid_shards = (a.mode == GEMM_ROW_PARTIAL) ? a.t : 1;
@@ -665,6 +958,62 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         const uint64_t dB[3] = {(uint64_t)a.Ks, (uint64_t)a.t, (uint64_t)a.N};
         const uint32_t bB[3] = {BK, 1, B_CHUNK_ROWS};
         if (!make_map(&p.mapB[0], a.B0, 3, dB, sA, bB, err)) return TP_ERR_CUDA;
+    } else if (a.mode == GEMM_BWD_ACT || a.mode == GEMM_NN || a.mode == GEMM_TN) {
+        p.kb_per_shard = static_cast<int>((a.K + BK - 1) / BK);
+        p.k_shards = 1;
+        const uint32_t box_mn[2] = {64, BK};  // 64 MN elements x 64 K rows
+        if (a.mode == GEMM_TN) {
+            // A stored [K][lda]: (M, K) view.
+            const int64_t lda = a.lda ? a.lda : a.M;
+            const uint64_t dA[2] = {(uint64_t)a.M, (uint64_t)a.K};
+            const uint64_t sA[1] = {(uint64_t)lda * 2};
+            if (!make_map(&p.mapA, a.A, 2, dA, sA, box_mn, err)) return TP_ERR_CUDA;
+        } else {
+            const int64_t lda = a.lda ? a.lda : a.K;
+            const uint64_t dA[2] = {(uint64_t)a.K, (uint64_t)a.M};
+            const uint64_t sA[1] = {(uint64_t)lda * 2};
+            const uint32_t bA[2] = {BK, BM};
+            if (!make_map(&p.mapA, a.A, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
+        }
+        // B stored [K rows][N]: (N, K rows) views; GEMM_NN splits K rows at
+        // k_split between B0 and B1 (k_split a multiple of BK).
+        const int64_t split = (a.mode == GEMM_NN && a.B1) ? a.k_split : a.K;
+        if (split % BK != 0 && split != a.K) {
+            if (err) *err = "K split of the NN GEMM is not a multiple of 64";
+            return TP_ERR_INVALID_ARG;
+        }
+        p.k_split = static_cast<int>(split);
+        const uint64_t sB[1] = {(uint64_t)a.N * 2};
+        const uint64_t dB0[2] = {(uint64_t)a.N, (uint64_t)split};
+        if (!make_map(&p.mapB[0], a.B0, 2, dB0, sB, box_mn, err)) return TP_ERR_CUDA;
+        if (split < a.K) {
+            const uint64_t dB1[2] = {(uint64_t)a.N, (uint64_t)(a.K - split)};
+            if (!make_map(&p.mapB[1], a.B1, 2, dB1, sB, box_mn, err)) return TP_ERR_CUDA;
+        } else {
+            p.mapB[1] = p.mapB[0];
+        }
+        p.mapB[2] = p.mapB[0];
+        p.row_split = static_cast<int>(a.mode == GEMM_TN && a.out2 ? a.row_split : a.M);
+        if (a.mode == GEMM_BWD_ACT) {
+            // Output boxes of 32 x 32 bf16, 64-byte swizzle: dU = out[:, :N],
+            // dG = out[:, n_half : n_half + N] (SwiGLU), H = out2.
+            const uint32_t box_o[2] = {EPI_BOX, EPI_BOX};
+            const uint64_t dO[2] = {(uint64_t)a.N, (uint64_t)a.M};
+            const uint64_t sO[1] = {(uint64_t)a.ldo * 2};
+            const char* base = static_cast<const char*>(a.out);
+            if (!make_map(&p.mapO[0], base, 2, dO, sO, box_o, err, CU_TENSOR_MAP_SWIZZLE_64B))
+                return TP_ERR_CUDA;
+            p.mapO[1] = p.mapO[0];
+            if (a.act == TP_ACT_SWIGLU &&
+                !make_map(&p.mapO[1], base + a.n_half * 2, 2, dO, sO, box_o, err, CU_TENSOR_MAP_SWIZZLE_64B))
+                return TP_ERR_CUDA;
+            p.mapO[2] = p.mapO[0];
+            if (a.out2) {
+                const uint64_t sH[1] = {(uint64_t)a.ldo2 * 2};
+                if (!make_map(&p.mapO[2], a.out2, 2, dO, sH, box_o, err, CU_TENSOR_MAP_SWIZZLE_64B))
+                    return TP_ERR_CUDA;
+            }
+        }
     } else {
         p.kb_per_shard = static_cast<int>((a.K + BK - 1) / BK);
         p.k_shards = 1;
@@ -712,6 +1061,9 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED, CG>(p, grid, stream, err);
         case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL, CG>(p, grid, stream, err);
         case GEMM_COL_PACKED: return launch_mode<GEMM_COL_PACKED, CG>(p, grid, stream, err);
+        case GEMM_BWD_ACT: return launch_mode<GEMM_BWD_ACT, CG>(p, grid, stream, err);
+        case GEMM_NN: return launch_mode<GEMM_NN, CG>(p, grid, stream, err);
+        case GEMM_TN: return launch_mode<GEMM_TN, CG>(p, grid, stream, err);
         default:
             if (err) *err = "unknown GEMM mode";
             return TP_ERR_INVALID_ARG;

@@ -16,7 +16,12 @@ enum GemmMode {
     GEMM_COL_QKV = 2,     // colwise Q|K|V per shard, bf16 out
     GEMM_ROW_FUSED = 3,   // rowwise, shards summed in the accumulator, + bias + residual
     GEMM_ROW_PARTIAL = 4, // rowwise, one [M][N] partial per shard (fp32 or bf16)
-    GEMM_COL_PACKED = 5   // colwise from a packed weight, each block sharded on its own
+    GEMM_COL_PACKED = 5,  // colwise from a packed weight, each block sharded on its own
+    // Backward GEMMs (operands read in their stored layout; "MN-major" =
+    // the operand's M or N index is the contiguous one):
+    GEMM_BWD_ACT = 6,     // dH = dZ W2 (B MN-major), epilogue: dU, dG, H from saved U, G
+    GEMM_NN = 7,          // A K-major, B MN-major [K][N] (K rows split over B0 / B1)
+    GEMM_TN = 8           // A and B MN-major ([K][M], [K][N]), fp32 out split by rows
 };
 
 constexpr int kMaxPackedBlocks = 8;
@@ -61,6 +66,26 @@ struct GemmArgs {
     const float* row_ss = nullptr;
     float* ss_out = nullptr;
     float inv_h = 0.0f, eps = 0.0f;
+    // Backward modes.
+    //  GEMM_BWD_ACT: aux = saved pre-activations [M][ldaux] (U at column n,
+    //    G at n_half + n for SwiGLU); out = dU (dG at n_half + n), ldo;
+    //    out2 = H [M][ldo2] (nullable).  A = dZ [M][K], B0 = W2 [K][N].
+    //  GEMM_NN: A [M][lda] K-major; B0 = [k_split][N], B1 = [K - k_split][N]
+    //    (nullable when k_split == K), MN-major; bf16 out.
+    //  GEMM_TN: A [K][M] and B0 [K][N], both MN-major; fp32 out [M][N];
+    //    rows >= row_split go to out2 (row - row_split); accumulate adds.
+    //  COL_ACT / COL_SWIGLU: aux_out (nullable) also receives the
+    //    pre-activations (U, and G at n_half + n), ld ldaux.
+    int64_t lda = 0;  // 0: K (K-major) or M (MN-major)
+    const void* aux = nullptr;
+    void* aux_out = nullptr;
+    int64_t ldaux = 0;
+    int64_t n_half = 0;
+    void* out2 = nullptr;
+    int64_t ldo2 = 0;
+    int64_t k_split = 0;
+    int64_t row_split = 0;
+    int accumulate = 0;
     unsigned* status = nullptr;
     uint64_t timeout_ns = 2000000000ull;
 };
@@ -111,6 +136,10 @@ int vocab_embedding_launch(const int32_t* ids, int64_t M, const void* E, int64_t
                            cudaStream_t stream, std::string* err);
 int vocab_ce_launch(const void* logits, int64_t M, int64_t v, int t, const int32_t* labels,
                     float* stats, float* loss, cudaStream_t stream, std::string* err);
+
+// out[j] (+)= sum_r x[r][j] for a bf16 [rows][h] x (h % 8 == 0), fp32 out.
+int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate,
+                  cudaStream_t stream, std::string* err);
 
 // Self test: a kernel that waits on a barrier nobody arrives at.
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,
