@@ -73,6 +73,9 @@ def lib():
             "tpo_sp_reduce_scatter": (C.c_int, [_I64] * 4 + [_D, _D]),
             "tpo_layer_sp": (C.c_int, [_I64] * 8 + [C.c_double] + [_D] * 9),
             "tpo_mlp_backward": (C.c_int, [C.c_int] + [_I64] * 3 + [_D] * 10),
+            "tpo_attention_core_backward": (C.c_int, [_I64] * 5 + [_D, _I64, _D, _D, _I64, _D, _I64, _D, _D, _D]),
+            "tpo_attention_backward": (C.c_int, [_I64] * 6 + [_D] * 11),
+            "tpo_attention_backward_sharded": (C.c_int, [_I64] * 7 + [_D] * 12),
             "tpo_mlp_backward_sharded": (C.c_int, [C.c_int] + [_I64] * 4 + [_D] * 11),
         }
         for name, (res, args) in sig.items():
@@ -416,3 +419,37 @@ def mlp_backward(act: str, X, W1, W2, dZ, W3=None, t: int = 0, want_partials: bo
         ACT[act], M, h, f, _p(X), _p(W1), _p(W3), _p(W2), _p(dZ), _p(dX), _p(dW1), _p(dW3), _p(dW2),
         _p(db2)))
     return dX, dW1, dW3, dW2, db2
+
+
+def attention_core_backward(batch: int, seq: int, a: int, k: int, Q, K, V, dO):
+    """(dQ, dK, dV) of the causal GQA attention core; Q, dO [M][a d], K, V [M][k d]."""
+    Q, K, V, dO = map(_d, (Q, K, V, dO))
+    d = Q.shape[1] // a
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(K), np.empty_like(V)
+    _check("tpo_attention_core_backward", lib().tpo_attention_core_backward(
+        batch, seq, a, k, d, _p(Q), Q.shape[1], _p(K), _p(V), K.shape[1], _p(dO), dO.shape[1],
+        _p(dQ), _p(dK), _p(dV)))
+    return dQ, dK, dV
+
+
+def attention_backward(batch: int, seq: int, a: int, k: int, X, Wq, Wk, Wv, Wo, dOut, t: int = 0,
+                       want_partials: bool = False):
+    """(dX, dWq, dWk, dWv, dWo) of the attention block given dOut; t > 0 uses
+    the literal t-device form (same dOut per device, dX = sum of partials,
+    replicated KV-head gradients summed)."""
+    X, Wq, Wk, Wv, Wo, dOut = map(_d, (X, Wq, Wk, Wv, Wo, dOut))
+    M, h = X.shape
+    d = Wq.shape[0] // a
+    dX = np.empty((M, h))
+    dWq, dWk, dWv, dWo = (np.empty_like(w) for w in (Wq, Wk, Wv, Wo))
+    if t:
+        P = np.empty((t, M, h)) if want_partials else None
+        _check("tpo_attention_backward_sharded", lib().tpo_attention_backward_sharded(
+            batch, seq, h, a, k, d, t, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(dOut), _p(P),
+            _p(dX), _p(dWq), _p(dWk), _p(dWv), _p(dWo)))
+        out = (dX, dWq, dWk, dWv, dWo)
+        return out + (P,) if want_partials else out
+    _check("tpo_attention_backward", lib().tpo_attention_backward(
+        batch, seq, h, a, k, d, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(dOut), _p(dX), _p(dWq),
+        _p(dWk), _p(dWv), _p(dWo)))
+    return dX, dWq, dWk, dWv, dWo

@@ -895,3 +895,198 @@ done:
     free(W1i); free(W3i); free(W2i); free(dXi); free(dW1i); free(dW3i); free(dW2i);
     return rc;
 }
+
+/* ---------------------------------------------------------------- attention backward */
+
+/* C[M][N] = A[M][K] B[K][N] (plain row-major, no transposes). */
+static void matmul_nn(const double* A, const double* B, int64_t M, int64_t K, int64_t N, double* C) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t q = 0; q < K; ++q) s += A[m * K + q] * B[q * N + n];
+            C[m * N + n] = s;
+        }
+}
+
+/* C[M][N] (+)= A[K][M]^T B[K][N]. */
+static void matmul_tn(const double* A, const double* B, int64_t K, int64_t M, int64_t N, double* C,
+                      int accumulate) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t q = 0; q < K; ++q) s += A[q * M + m] * B[q * N + n];
+            C[m * N + n] = accumulate ? C[m * N + n] + s : s;
+        }
+}
+
+/* Backward of one causal attention row (query p of its sequence), by the
+ * chain rule through the row's softmax: with s_r = q.K_r / sqrt d and
+ * P = softmax(s) over r <= p, o = sum_r P_r V_r, and the upstream dout:
+ *   dP_r = dout . V_r,  D = sum_r P_r dP_r (= dout . o),
+ *   dS_r = P_r (dP_r - D),
+ *   dq   = sum_r dS_r K_r / sqrt d,   dK_r += dS_r q / sqrt d,
+ *   dV_r += P_r dout.
+ * dq[d] is written; dK and dV rows (stride ld) are accumulated. */
+static void attend_row_backward(const double* q, const double* K, const double* V, int64_t ld,
+                                int64_t p, int64_t d, const double* dout, double* P, double* dP,
+                                double* dq, double* dK, double* dV) {
+    const double scale = 1.0 / sqrt((double)d);
+    double mx = -INFINITY;
+    for (int64_t r = 0; r <= p; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += q[c] * K[r * ld + c];
+        P[r] = acc * scale;
+        if (P[r] > mx) mx = P[r];
+    }
+    double sum = 0.0;
+    for (int64_t r = 0; r <= p; ++r) { P[r] = exp(P[r] - mx); sum += P[r]; }
+    double D = 0.0;
+    for (int64_t r = 0; r <= p; ++r) {
+        P[r] /= sum;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += dout[c] * V[r * ld + c];
+        dP[r] = acc;
+        D += P[r] * acc;
+    }
+    for (int64_t c = 0; c < d; ++c) dq[c] = 0.0;
+    for (int64_t r = 0; r <= p; ++r) {
+        const double ds = P[r] * (dP[r] - D);
+        for (int64_t c = 0; c < d; ++c) {
+            dq[c] += ds * K[r * ld + c] * scale;
+            dK[r * ld + c] += ds * q[c] * scale;
+            dV[r * ld + c] += P[r] * dout[c];
+        }
+    }
+}
+
+/* Backward of the attention core (layout of tpo_attention_core): given
+ * dO[M][a d] (stride lddo), writes dQ (stride ldq) and dK, dV (stride ldkv).
+ * The gradient of a KV head sums over every query head that reads it (GQA).
+ * Parallel over (sequence, KV head): each task owns its dK/dV rows. */
+int tpo_attention_core_backward(int64_t batch, int64_t seq, int64_t a, int64_t k, int64_t d,
+                                const double* Q, int64_t ldq, const double* K, const double* V,
+                                int64_t ldkv, const double* dO, int64_t lddo, double* dQ,
+                                double* dK, double* dV) {
+    if (batch < 0 || seq < 0 || a <= 0 || k <= 0 || d <= 0 || a % k) return TPO_ERR_INVALID;
+    for (int64_t m = 0; m < batch * seq; ++m)
+        for (int64_t c = 0; c < k * d; ++c) dK[m * ldkv + c] = dV[m * ldkv + c] = 0.0;
+#pragma omp parallel
+    {
+        double* P = (double*)malloc(sizeof(double) * (size_t)(seq + 1));
+        double* dP = (double*)malloc(sizeof(double) * (size_t)(seq + 1));
+#pragma omp for schedule(dynamic, 1) collapse(2)
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t g = 0; g < k; ++g) {
+                const int64_t r0 = b * seq;
+                for (int64_t j = 0; j < a; ++j) {
+                    if (tpo_q_head_kv(a, k, j) != g) continue;
+                    for (int64_t p = 0; p < seq; ++p)
+                        attend_row_backward(Q + (r0 + p) * ldq + j * d, K + r0 * ldkv + g * d,
+                                            V + r0 * ldkv + g * d, ldkv, p, d,
+                                            dO + (r0 + p) * lddo + j * d, P, dP,
+                                            dQ + (r0 + p) * ldq + j * d, dK + r0 * ldkv + g * d,
+                                            dV + r0 * ldkv + g * d);
+                }
+            }
+        free(P);
+        free(dP);
+    }
+    return TPO_OK;
+}
+
+/* Backward of the unsharded attention block of tpo_attention, given
+ * dOut = dL/dout [M][h]:
+ *   dO = dOut Wo,  dWo = dOut^T O,  (dQ, dK, dV) = core backward,
+ *   dWq = dQ^T X,  dWk = dK^T X,  dWv = dV^T X,
+ *   dX = dQ Wq + dK Wk + dV Wv. */
+int tpo_attention_backward(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                           const double* X, const double* Wq, const double* Wk, const double* Wv,
+                           const double* Wo, const double* dOut, double* dX, double* dWq,
+                           double* dWk, double* dWv, double* dWo) {
+    if (batch < 0 || seq < 0 || h <= 0 || a <= 0 || k <= 0 || d <= 0 || a % k) return TPO_ERR_INVALID;
+    const int64_t M = batch * seq, qw = a * d, kw = k * d;
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * M * qw + 4 * M * kw + M * h + 1));
+    if (!buf) return TPO_ERR_NOMEM;
+    double *Q = buf, *O = Q + M * qw, *dO = O + M * qw, *dQ = dO + M * qw;
+    double *Kx = dQ + M * qw, *Vx = Kx + M * kw, *dK = Vx + M * kw, *dV = dK + M * kw;
+    double* t1 = dV + M * kw;
+    tpo_linear(X, h, Wq, h, M, qw, h, Q, qw);
+    tpo_linear(X, h, Wk, h, M, kw, h, Kx, kw);
+    tpo_linear(X, h, Wv, h, M, kw, h, Vx, kw);
+    tpo_attention_core(batch, seq, a, k, d, Q, qw, Kx, Vx, kw, O, qw);
+    matmul_nn(dOut, Wo, M, h, qw, dO);
+    matmul_tn(dOut, O, M, h, qw, dWo, 0);
+    tpo_attention_core_backward(batch, seq, a, k, d, Q, qw, Kx, Vx, kw, dO, qw, dQ, dK, dV);
+    matmul_tn(dQ, X, M, qw, h, dWq, 0);
+    matmul_tn(dK, X, M, kw, h, dWk, 0);
+    matmul_tn(dV, X, M, kw, h, dWv, 0);
+    matmul_nn(dQ, Wq, M, qw, h, dX);
+    matmul_nn(dK, Wk, M, kw, h, t1);
+    for (int64_t e = 0; e < M * h; ++e) dX[e] += t1[e];
+    matmul_nn(dV, Wv, M, kw, h, t1);
+    for (int64_t e = 0; e < M * h; ++e) dX[e] += t1[e];
+    free(buf);
+    return TPO_OK;
+}
+
+/* The same backward in the literal t-device form ("통신 연산 f와 g" with
+ * the head split of "셀프 어텐션"): device i receives the same dOut (g's
+ * backward is the identity), back-propagates through its column block of Wo,
+ * its query heads and the KV heads it holds (its own, or a replica), and
+ * keeps the gradients of its weight slices; a replicated KV head's weight
+ * gradient is the sum over the devices holding it; f's backward is
+ * dX = sum_i dX_i (i ascending).  dX_partials (nullable): [t][M][h]. */
+int tpo_attention_backward_sharded(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k,
+                                   int64_t d, int64_t t, const double* X, const double* Wq,
+                                   const double* Wk, const double* Wv, const double* Wo,
+                                   const double* dOut, double* dX_partials, double* dX, double* dWq,
+                                   double* dWk, double* dWv, double* dWo) {
+    int rc = tpo_plan_check(h, 0, a, k, d, t);
+    if (rc) return rc;
+    const int64_t M = batch * seq, ap = a / t, kvn = tpo_shard_kv_count(k, t);
+    const int64_t qw = ap * d, kw = kvn * d, ad = a * d;
+    const size_t n = (size_t)(4 * M * qw + 4 * M * kw + 2 * M * h + qw * h + qw * h + 2 * kw * h + 1);
+    double* buf = (double*)malloc(sizeof(double) * n);
+    if (!buf) return TPO_ERR_NOMEM;
+    double *Q = buf, *O = Q + M * qw, *dO = O + M * qw, *dQ = dO + M * qw;
+    double *Kx = dQ + M * qw, *Vx = Kx + M * kw, *dK = Vx + M * kw, *dV = dK + M * kw;
+    double *dXi = dV + M * kw, *t1 = dXi + M * h;
+    double *Woi = t1 + M * h, *dWoi = Woi + qw * h, *dWki = dWoi + qw * h, *dWvi = dWki + kw * h;
+    for (int64_t e = 0; e < M * h; ++e) dX[e] = 0.0;
+    for (int64_t e = 0; e < k * d * h; ++e) dWk[e] = dWv[e] = 0.0;
+    for (int64_t i = 0; i < t; ++i) {
+        const int64_t kv0 = tpo_shard_kv_first(k, t, i);
+        const double* Wqi = Wq + i * qw * h;
+        const double* Wki = Wk + kv0 * d * h;
+        const double* Wvi = Wv + kv0 * d * h;
+        /* columns [i qw, (i+1) qw) of Wo, as a [h][qw] matrix */
+        for (int64_t j = 0; j < h; ++j) memcpy(Woi + j * qw, Wo + j * ad + i * qw, sizeof(double) * (size_t)qw);
+        tpo_linear(X, h, Wqi, h, M, qw, h, Q, qw);
+        tpo_linear(X, h, Wki, h, M, kw, h, Kx, kw);
+        tpo_linear(X, h, Wvi, h, M, kw, h, Vx, kw);
+        /* local heads: local query head jl reads local KV slot jl / (ap / kvn) */
+        tpo_attention_core(batch, seq, ap, kvn, d, Q, qw, Kx, Vx, kw, O, qw);
+        matmul_nn(dOut, Woi, M, h, qw, dO);
+        matmul_tn(dOut, O, M, h, qw, dWoi, 0);
+        for (int64_t j = 0; j < h; ++j) memcpy(dWo + j * ad + i * qw, dWoi + j * qw, sizeof(double) * (size_t)qw);
+        tpo_attention_core_backward(batch, seq, ap, kvn, d, Q, qw, Kx, Vx, kw, dO, qw, dQ, dK, dV);
+        matmul_tn(dQ, X, M, qw, h, dWq + i * qw * h, 0);
+        matmul_tn(dK, X, M, kw, h, dWki, 0);
+        matmul_tn(dV, X, M, kw, h, dWvi, 0);
+        for (int64_t e = 0; e < kw * h; ++e) {
+            dWk[kv0 * d * h + e] += dWki[e];
+            dWv[kv0 * d * h + e] += dWvi[e];
+        }
+        matmul_nn(dQ, Wqi, M, qw, h, dXi);
+        matmul_nn(dK, Wki, M, kw, h, t1);
+        for (int64_t e = 0; e < M * h; ++e) dXi[e] += t1[e];
+        matmul_nn(dV, Wvi, M, kw, h, t1);
+        for (int64_t e = 0; e < M * h; ++e) dXi[e] += t1[e];
+        for (int64_t e = 0; e < M * h; ++e) dX[e] += dXi[e];
+        if (dX_partials) memcpy(dX_partials + i * M * h, dXi, sizeof(double) * (size_t)(M * h));
+    }
+    free(buf);
+    return TPO_OK;
+}

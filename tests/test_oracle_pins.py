@@ -600,3 +600,78 @@ def test_mlp_backward_sharded_equals_plain(act, t):
         if a is not None:
             assert np.abs(a - b).max() < 1e-12 * max(1.0, np.abs(a).max())
     assert np.abs(P.sum(0) - plain[0]).max() < 1e-12   # f backward: dX = sum of the t partials
+
+
+def _torch_attention(batch, seq, a, k, Q, K, V):
+    """Causal GQA attention by torch ops, for autograd pins."""
+    M = batch * seq
+    d = Q.shape[1] // a
+    q = Q.reshape(batch, seq, a, d).transpose(1, 2)                  # b a s d
+    kk = K.reshape(batch, seq, k, d).transpose(1, 2).repeat_interleave(a // k, dim=1)
+    vv = V.reshape(batch, seq, k, d).transpose(1, 2).repeat_interleave(a // k, dim=1)
+    s = q @ kk.transpose(-1, -2) / math.sqrt(d)
+    mask = torch.ones(seq, seq, dtype=torch.bool).triu(1)
+    s = s.masked_fill(mask, float("-inf"))
+    o = torch.softmax(s, dim=-1) @ vv
+    return o.transpose(1, 2).reshape(M, a * d)
+
+
+def test_attention_core_backward_matches_torch_autograd():
+    g = torch.Generator().manual_seed(71)
+    batch, seq, a, k, d = 2, 5, 4, 2, 3
+    M = batch * seq
+    Q, K, V = (torch.randn(M, n * d, generator=g, dtype=torch.float64).requires_grad_(True)
+               for n in (a, k, k))
+    dO = torch.randn(M, a * d, generator=g, dtype=torch.float64)
+    _torch_attention(batch, seq, a, k, Q, K, V).backward(dO)
+    got = oracle.attention_core_backward(batch, seq, a, k, Q.detach(), K.detach(), V.detach(), dO)
+    for name, x, ref in zip(("dQ", "dK", "dV"), got, (Q.grad, K.grad, V.grad)):
+        assert np.abs(x - ref.numpy()).max() < 1e-12, name
+
+
+def test_attention_core_backward_single_position_closed_form():
+    # seq = 1: every query attends only to itself, P = 1, so dS = 0:
+    # dQ = dK = 0 and dV = the sum of dO over the query heads of the group.
+    g = torch.Generator().manual_seed(72)
+    batch, a, k, d = 3, 4, 2, 5
+    Q, K, V = (torch.randn(batch, n * d, generator=g, dtype=torch.float64) for n in (a, k, k))
+    dO = torch.randn(batch, a * d, generator=g, dtype=torch.float64).numpy()
+    dQ, dK, dV = oracle.attention_core_backward(batch, 1, a, k, Q, K, V, dO)
+    assert np.abs(dQ).max() == 0 and np.abs(dK).max() == 0
+    want = dO.reshape(batch, k, a // k, d).sum(2).reshape(batch, k * d)
+    assert np.abs(dV - want).max() < 1e-15
+
+
+def test_attention_block_backward_matches_torch_autograd():
+    g = torch.Generator().manual_seed(73)
+    batch, seq, h, a, k, d = 2, 4, 6, 4, 2, 2
+    M = batch * seq
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).requires_grad_(True)
+    Wq = (torch.randn(a * d, h, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
+    Wk = (torch.randn(k * d, h, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
+    Wv = (torch.randn(k * d, h, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
+    Wo = (torch.randn(h, a * d, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
+    dOut = torch.randn(M, h, generator=g, dtype=torch.float64)
+    out = _torch_attention(batch, seq, a, k, X @ Wq.T, X @ Wk.T, X @ Wv.T) @ Wo.T
+    out.backward(dOut)
+    got = oracle.attention_backward(batch, seq, a, k, *(w.detach() for w in (X, Wq, Wk, Wv, Wo)), dOut)
+    for name, x, ref in zip(("dX", "dWq", "dWk", "dWv", "dWo"), got,
+                            (X.grad, Wq.grad, Wk.grad, Wv.grad, Wo.grad)):
+        assert np.abs(x - ref.numpy()).max() < 1e-12 * max(1.0, ref.abs().max().item()), name
+
+
+@pytest.mark.parametrize("a,k,t", [(4, 2, 2), (4, 2, 4), (4, 4, 2), (8, 2, 4), (4, 1, 2), (2, 1, 1)])
+def test_attention_backward_sharded_equals_plain(a, k, t):
+    # k < t exercises KV replicas: their weight gradients are summed.
+    g = torch.Generator().manual_seed(74 + 10 * a + k + t)
+    batch, seq, h, d = 2, 3, 8, 2
+    M = batch * seq
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    W = [(torch.randn(n, m, generator=g, dtype=torch.float64) * 0.5).numpy()
+         for n, m in ((a * d, h), (k * d, h), (k * d, h), (h, a * d))]
+    dOut = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    plain = oracle.attention_backward(batch, seq, a, k, X, *W, dOut)
+    *shard, P = oracle.attention_backward(batch, seq, a, k, X, *W, dOut, t=t, want_partials=True)
+    for x, y in zip(plain, shard):
+        assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max())
+    assert np.abs(P.sum(0) - plain[0]).max() < 1e-12 * max(1.0, np.abs(plain[0]).max())
