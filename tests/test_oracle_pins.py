@@ -602,7 +602,7 @@ def test_mlp_backward_sharded_equals_plain(act, t):
     assert np.abs(P.sum(0) - plain[0]).max() < 1e-12   # f backward: dX = sum of the t partials
 
 
-def _torch_attention(batch, seq, a, k, Q, K, V):
+def _torch_gqa_attention(batch, seq, a, k, Q, K, V):
     """Causal GQA attention by torch ops, for autograd pins."""
     M = batch * seq
     d = Q.shape[1] // a
@@ -623,7 +623,7 @@ def test_attention_core_backward_matches_torch_autograd():
     Q, K, V = (torch.randn(M, n * d, generator=g, dtype=torch.float64).requires_grad_(True)
                for n in (a, k, k))
     dO = torch.randn(M, a * d, generator=g, dtype=torch.float64)
-    _torch_attention(batch, seq, a, k, Q, K, V).backward(dO)
+    _torch_gqa_attention(batch, seq, a, k, Q, K, V).backward(dO)
     got = oracle.attention_core_backward(batch, seq, a, k, Q.detach(), K.detach(), V.detach(), dO)
     for name, x, ref in zip(("dQ", "dK", "dV"), got, (Q.grad, K.grad, V.grad)):
         assert np.abs(x - ref.numpy()).max() < 1e-12, name
@@ -652,7 +652,7 @@ def test_attention_block_backward_matches_torch_autograd():
     Wv = (torch.randn(k * d, h, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
     Wo = (torch.randn(h, a * d, generator=g, dtype=torch.float64) * 0.5).requires_grad_(True)
     dOut = torch.randn(M, h, generator=g, dtype=torch.float64)
-    out = _torch_attention(batch, seq, a, k, X @ Wq.T, X @ Wk.T, X @ Wv.T) @ Wo.T
+    out = _torch_gqa_attention(batch, seq, a, k, X @ Wq.T, X @ Wk.T, X @ Wv.T) @ Wo.T
     out.backward(dOut)
     got = oracle.attention_backward(batch, seq, a, k, *(w.detach() for w in (X, Wq, Wk, Wv, Wo)), dOut)
     for name, x, ref in zip(("dX", "dWq", "dWk", "dWv", "dWo"), got,
