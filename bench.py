@@ -86,6 +86,20 @@ def mlp_backward_kernel_flops(M, h, f, glu=True):
     ]
 
 
+def attn_backward_kernel_flops(s: Shape):
+    """Algorithmic FLOPs of the attention block's backward, in launch order
+    (the core backward is five matmuls of the forward's two sizes: S and dP
+    recomputed, dV, dK, dQ)."""
+    M, h, a, k, d = s.tokens, s.hidden, s.heads, s.kv_heads, s.head_dim
+    return [
+        ("bwd_do_gemm", gemm_flops(M, a * d, h)),
+        ("bwd_dwo_gemm", gemm_flops(h, a * d, M)),
+        ("attn_bwd_core", 2.5 * attn_core_flops(s)),
+        ("bwd_dx_gemm+f", gemm_flops(M, h, (a + 2 * k) * d)),
+        ("bwd_dwqkv_gemm", gemm_flops((a + 2 * k) * d, h, M)),
+    ]
+
+
 def layer_flops(s: Shape):
     return sum(v for _, v in layer_kernel_flops(s))
 
@@ -420,6 +434,34 @@ def run_case(args):
         fn = lambda: tp.tp_mlp_backward(plan, X, W1, W3, W2, dZ, UG, dX, dW1, dW3, dW2, db2, False,
                                         wsb, nws, stream)
         work = sum(v for _, v in mlp_backward_kernel_flops(M, h, f))
+    elif args.case in ("attn_backward", "attn_backward_recompute"):
+        # Backward of the layer's attention block (4 x 2048 tokens, h 4096,
+        # 32 query / 8 KV heads of 128, t 8), with the forward's QKV, O and
+        # softmax statistics saved, or recomputed.
+        inp = synth.workload_inputs(s)
+        dd = {kk: inp[kk].cuda() for kk in ("X", "Wq", "Wk", "Wv", "Wo")}
+        dOut = bf((M, h), 1.0, 4013)
+        plan = tp.Plan(tp.make_config(tokens=M, hidden=h, n_heads=a, n_kv_heads=k, head_dim=d,
+                                      tp_degree=t, act="none", batch=s.batch, seq=s.seq))
+        qb_, ob_, lb_ = tp.tp_plan_attn_saved_bytes(plan)
+        QKVs = torch.empty(qb_, dtype=torch.uint8, device="cuda")
+        Os = torch.empty(ob_, dtype=torch.uint8, device="cuda")
+        LSEs = torch.empty(lb_, dtype=torch.uint8, device="cuda")
+        outf = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+        tp.tp_attn_forward_train(plan, dd["X"], dd["Wq"], dd["Wk"], dd["Wv"], dd["Wo"], None, None,
+                                 outf, QKVs, Os, LSEs, stream)
+        if args.case == "attn_backward_recompute":
+            QKVs = Os = LSEs = None
+        nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_ATTN_BACKWARD)
+        wsb = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        dX = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+        f32 = dict(dtype=torch.float32, device="cuda")
+        dWq, dWk = torch.empty(a * d, h, **f32), torch.empty(k * d, h, **f32)
+        dWv, dWo = torch.empty(k * d, h, **f32), torch.empty(h, a * d, **f32)
+        fn = lambda: tp.tp_attn_backward(plan, dd["X"], dd["Wq"], dd["Wk"], dd["Wv"], dd["Wo"], dOut,
+                                         QKVs, Os, LSEs, dX, dWq, dWk, dWv, dWo, False, wsb, nws,
+                                         stream)
+        work = sum(v for _, v in attn_backward_kernel_flops(s))
     elif args.case == "attn":
         kvn = max(k // t, 1)
         W = (a // t + 2 * kvn) * d
@@ -667,7 +709,8 @@ def main(argv=None):
     ap.add_argument("--case", default="layer",
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
                              "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer",
-                             "partials_layer", "mlp_backward", "mlp_backward_recompute"],
+                             "partials_layer", "mlp_backward", "mlp_backward_recompute",
+                             "attn_backward", "attn_backward_recompute"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="mlp_backward cases: tokens (0 = the layer's 8192), for small captures")

@@ -86,7 +86,7 @@ enum { TP_REDUCE_FUSED = 0, TP_REDUCE_PARTIALS = 1 };
 enum { TP_F32 = 0, TP_BF16 = 1 };
 
 /* Operations whose workspace size tp_plan_workspace_bytes reports. */
-enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2, TP_OP_MLP_BACKWARD = 3 };
+enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2, TP_OP_MLP_BACKWARD = 3, TP_OP_ATTN_BACKWARD = 4 };
 
 /* Index tables tp_plan_shard_table exports (int32, row-major):
  *  FFN_SHARDS  [t][2]: first column of shard i in the ffn dimension, width f/t
@@ -289,6 +289,49 @@ TP_API int tp_mlp_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, 
                            const tp_bf16* W2, const tp_bf16* dZ, const tp_bf16* UG, tp_bf16* dX,
                            float* dW1, float* dW3, float* dW2, float* db2, int accumulate,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Sizes of what the attention backward reads from its forward: the
+ * shard-blocked QKV buffer ([M][t (a/t + 2 kv_held) d] bf16, as
+ * tp_qkv_forward writes it), the attention output O ([M][a d] bf16) and the
+ * softmax statistics LSE ([a][batch][seq_pad] fp32, seq_pad = seq rounded up
+ * to a multiple of 64; entry (j, b, pos) is the base-2 log of the row's
+ * sum of 2^(s log2(e) / sqrt(d)) over its causal keys, s the raw scores).
+ * Any pointer may be NULL. */
+TP_API int tp_plan_attn_saved_bytes(tp_plan_t plan, size_t* qkv_bytes, size_t* o_bytes, size_t* lse_bytes);
+
+/* tp_attn_forward that keeps what its backward reads: QKV, O and LSE (sizes
+ * from tp_plan_attn_saved_bytes; device, 16-byte aligned, not aliasing).
+ * These replace the forward's workspace; everything else is as in
+ * tp_attn_forward. */
+TP_API int tp_attn_forward_train(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                                 const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* residual,
+                                 void* partials, tp_bf16* out, tp_bf16* QKV, tp_bf16* O, float* LSE,
+                                 void* stream);
+
+/* Backward of the head-sharded attention block ([wiki] "셀프 어텐션" and
+ * "통신 연산 f와 g").  g at the block's output is the identity backward:
+ * every shard receives the same dOut [M][h].  Then
+ *   dO_i  = dOut Wo_i,   dWo_i = dOut^T O_i         (Wo_i: columns of shard i)
+ *   dQ, dK, dV per head by the chain rule through the causal softmax:
+ *           dV = P^T dO, dS = P (.) (dO V^T - rowsum(dO (.) O)),
+ *           dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d);
+ *           a KV head's gradient sums over the query heads that read it,
+ *           which also sums its replicas when k < t
+ *   dX    = sum_i (dQ_i Wq_i + dK_i Wk_i + dV_i Wv_i)  (f's all-reduce; the
+ *           sum over shards runs inside one accumulator)
+ *   dWq = dQ^T X, dWk = dK^T X, dWv = dV^T X.
+ * X, Wq, Wk, Wv, Wo as in tp_attn_forward; dOut [M][h] bf16.  QKV, O, LSE:
+ * from tp_attn_forward_train, or all NULL to recompute them here (the QKV
+ * GEMM and the attention forward run again).  dX: [M][h] bf16.  dWq [a d][h],
+ * dWk, dWv [k d][h], dWo [h][a d]: fp32, overwritten, or added to when
+ * accumulate != 0.  Workspace: tp_plan_workspace_bytes(TP_OP_ATTN_BACKWARD)
+ * bytes (it covers recomputation).  Needs head_dim 128 (TP_ERR_UNSUPPORTED
+ * otherwise); the plan's reduce mode does not apply. */
+TP_API int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                            const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* dOut, const tp_bf16* QKV,
+                            const tp_bf16* O, const float* LSE, tp_bf16* dX, float* dWq, float* dWk,
+                            float* dWv, float* dWo, int accumulate, void* workspace, size_t ws_bytes,
+                            void* stream);
 
 /* ------------------------------------------------------------ packed projections */
 

@@ -22,7 +22,7 @@ __all__ = [
     "TP_ERR_WORKSPACE", "TP_ERR_CUDA", "TP_ERR_DEVICE_TIMEOUT",
     "TP_ACT_GELU_ERF", "TP_ACT_GELU_TANH", "TP_ACT_SWIGLU", "TP_ACT_NONE",
     "TP_REDUCE_FUSED", "TP_REDUCE_PARTIALS", "TP_F32", "TP_BF16",
-    "TP_OP_MLP", "TP_OP_ATTN", "TP_OP_LAYER", "TP_OP_MLP_BACKWARD",
+    "TP_OP_MLP", "TP_OP_ATTN", "TP_OP_LAYER", "TP_OP_MLP_BACKWARD", "TP_OP_ATTN_BACKWARD",
     "TP_TABLE_FFN_SHARDS", "TP_TABLE_Q_HEAD_SHARD", "TP_TABLE_Q_HEAD_KV",
     "TP_TABLE_SHARD_KV", "TP_TABLE_QKV_COLUMNS",
     "tp_plan_create", "tp_plan_destroy", "tp_config_check", "tp_config_shard_table",
@@ -32,7 +32,8 @@ __all__ = [
     "tp_layer_forward", "tp_layer_forward_traced", "tp_selftest_wait_timeout",
     "tp_packed_shard_table", "tp_packed_colwise_forward", "tp_vocab_embedding_forward",
     "tp_vocab_logits_forward", "tp_vocab_parallel_cross_entropy", "tp_sp_all_gather",
-    "tp_sp_reduce_scatter", "tp_mlp_forward_train", "tp_mlp_backward", "EXPORTED",
+    "tp_sp_reduce_scatter", "tp_mlp_forward_train", "tp_mlp_backward", "tp_plan_attn_saved_bytes",
+    "tp_attn_forward_train", "tp_attn_backward", "EXPORTED",
 ]
 
 TP_OK = 0
@@ -46,7 +47,7 @@ TP_ERR_DEVICE_TIMEOUT = 6
 TP_ACT_GELU_ERF, TP_ACT_GELU_TANH, TP_ACT_SWIGLU, TP_ACT_NONE = 0, 1, 2, 3
 TP_REDUCE_FUSED, TP_REDUCE_PARTIALS = 0, 1
 TP_F32, TP_BF16 = 0, 1
-TP_OP_MLP, TP_OP_ATTN, TP_OP_LAYER, TP_OP_MLP_BACKWARD = 0, 1, 2, 3
+TP_OP_MLP, TP_OP_ATTN, TP_OP_LAYER, TP_OP_MLP_BACKWARD, TP_OP_ATTN_BACKWARD = 0, 1, 2, 3, 4
 (TP_TABLE_FFN_SHARDS, TP_TABLE_Q_HEAD_SHARD, TP_TABLE_Q_HEAD_KV, TP_TABLE_SHARD_KV,
  TP_TABLE_QKV_COLUMNS) = range(5)
 
@@ -97,6 +98,9 @@ _SIGS = {
     "tp_mlp_forward_noalloc": [_VP] * 9,
     "tp_mlp_forward_train": [_VP] * 11 + [C.c_size_t, _VP],
     "tp_mlp_backward": [_VP] * 12 + [C.c_int, _VP, C.c_size_t, _VP],
+    "tp_plan_attn_saved_bytes": [_VP] + [C.POINTER(C.c_size_t)] * 3,
+    "tp_attn_forward_train": [_VP] * 13,
+    "tp_attn_backward": [_VP] * 15 + [C.c_int, _VP, C.c_size_t, _VP],
     "tp_qkv_forward": [_VP] * 7,
     "tp_attn_core_forward": [_VP] * 4,
     "tp_attn_forward": [_VP] * 10 + [C.c_size_t, _VP],
@@ -296,6 +300,28 @@ def tp_mlp_backward(plan: Plan, X, W1, W3, W2, dZ, UG, dX, dW1, dW3, dW2, db2, a
     _call("tp_mlp_backward", plan.handle, _p(X), _p(W1), _p(W3), _p(W2), _p(dZ), _p(UG), _p(dX),
           _p(dW1), _p(dW3), _p(dW2), _p(db2), 1 if accumulate else 0, _p(workspace), ws_bytes,
           _s(stream))
+
+
+def tp_plan_attn_saved_bytes(plan: Plan):
+    """(qkv, o, lse) byte sizes of what tp_attn_forward_train saves."""
+    q, o, l = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    _call("tp_plan_attn_saved_bytes", plan.handle, C.byref(q), C.byref(o), C.byref(l))
+    return q.value, o.value, l.value
+
+
+def tp_attn_forward_train(plan: Plan, X, Wq, Wk, Wv, Wo, residual, partials, out, QKV, O, LSE,
+                          stream=None) -> None:
+    """tp_attn_forward that keeps QKV, O and the softmax statistics LSE."""
+    _call("tp_attn_forward_train", plan.handle, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo),
+          _p(residual), _p(partials), _p(out), _p(QKV), _p(O), _p(LSE), _s(stream))
+
+
+def tp_attn_backward(plan: Plan, X, Wq, Wk, Wv, Wo, dOut, QKV, O, LSE, dX, dWq, dWk, dWv, dWo,
+                     accumulate: bool, workspace, ws_bytes: int, stream=None) -> None:
+    """Gradients of the head-sharded attention block (QKV/O/LSE None: recomputed)."""
+    _call("tp_attn_backward", plan.handle, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(dOut),
+          _p(QKV), _p(O), _p(LSE), _p(dX), _p(dWq), _p(dWk), _p(dWv), _p(dWo),
+          1 if accumulate else 0, _p(workspace), ws_bytes, _s(stream))
 
 
 def tp_qkv_forward(plan: Plan, X, Wq, Wk, Wv, QKV, stream=None) -> None:

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libtp.so")
 
-SOURCES = ["tp_api.cu", "tp_gemm.cu", "tp_elementwise.cu", "tp_attn.cu", "tp_vocab.cu"]
+SOURCES = ["tp_api.cu", "tp_gemm.cu", "tp_elementwise.cu", "tp_attn.cu", "tp_attn_bwd.cu", "tp_vocab.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

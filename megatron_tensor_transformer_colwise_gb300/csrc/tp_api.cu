@@ -99,7 +99,16 @@ struct Layout {
     size_t ug = 0;       // MLP backward: recomputed pre-activations [M][f or 2f] bf16
     size_t dug = 0;      // MLP backward: dU (| dG) [M][f or 2f] bf16
     size_t hact = 0;     // MLP backward: activations H [M][f] bf16
+    size_t bdo = 0;      // attention backward: dO [M][a d] bf16
+    size_t bdstat = 0;   // attention backward: D [a][batch][seq_pad] fp32
+    size_t bdq = 0;      // attention backward: dQ accumulator [M][a d] fp32
+    size_t bdqkv = 0;    // attention backward: dQ | dK | dV [M][(a + 2k) d] bf16
+    size_t bqkv = 0;     // attention backward, recomputation: QKV [M][t qkv_w] bf16
+    size_t bo = 0;       // attention backward, recomputation: O [M][a d] bf16
+    size_t blse = 0;     // attention backward, recomputation: LSE [a][batch][seq_pad] fp32
 };
+
+int64_t seq_pad_of(const tp_plan_s* p) { return (p->cfg.seq + 63) / 64 * 64; }
 
 size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
 
@@ -119,6 +128,16 @@ Layout layout_of(const tp_plan_s* p, int op) {
         L.dug = align_up(M * wu * 2);
         L.hact = align_up(M * p->f * 2);
     }
+    if (op == TP_OP_ATTN_BACKWARD && p->has_attn) {
+        const size_t stat = static_cast<size_t>(p->a) * p->cfg.batch * seq_pad_of(p) * 4;
+        L.bdo = align_up(M * p->a * p->d * 2);
+        L.bdstat = align_up(stat);
+        L.bdq = align_up(M * p->a * p->d * 4);
+        L.bdqkv = align_up(M * (p->a + 2 * p->k) * p->d * 2);
+        L.bqkv = align_up(M * p->t * p->qkv_w * 2);
+        L.bo = align_up(M * p->a * p->d * 2);
+        L.blse = align_up(stat);
+    }
     if (op == TP_OP_LAYER) {
         L.h1 = align_up(M * p->h * 2);
         if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS) {
@@ -133,7 +152,8 @@ Layout layout_of(const tp_plan_s* p, int op) {
 }
 
 size_t layout_total(const Layout& L) {
-    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact;
+    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact + L.bdo +
+           L.bdstat + L.bdq + L.bdqkv + L.bqkv + L.bo + L.blse;
 }
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
@@ -255,8 +275,10 @@ int do_qkv(const tp_plan_s* p, const void* X, const void* Wq, const void* Wk, co
     return run(tpi::gemm_launch(g, s, &err), err);
 }
 
-int do_attn_core(const tp_plan_s* p, const void* QKV, void* O, cudaStream_t s) {
+int do_attn_core(const tp_plan_s* p, const void* QKV, void* O, cudaStream_t s, float* lse = nullptr) {
     tpi::AttnArgs a;
+    a.lse = lse;  // base-2 log-sum-exp per (head, sequence, row), for the backward pass
+    a.seq_pad = seq_pad_of(p);
     a.QKV = QKV;
     a.ld_qkv = p->t * p->qkv_w;
     a.shard_w = p->qkv_w;
@@ -421,7 +443,7 @@ int tp_plan_destroy(tp_plan_t plan) {
 
 int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes) {
     if (!plan || !bytes) return fail(TP_ERR_INVALID_ARG, "plan and bytes must be non-NULL");
-    if (op < TP_OP_MLP || op > TP_OP_MLP_BACKWARD) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
+    if (op < TP_OP_MLP || op > TP_OP_ATTN_BACKWARD) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
     *bytes = layout_total(layout_of(plan, op));
     return TP_OK;
 }
@@ -743,6 +765,187 @@ int tp_attn_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const t
     if ((rc = do_rowwise(plan, O, plan->qw, Wo, plan->h, nullptr, residual, partials, out, fused, s)))
         return rc;
     if (!fused) return do_reduce(plan, partials, nullptr, residual, out, plan->h, s);
+    return TP_OK;
+}
+
+int tp_plan_attn_saved_bytes(tp_plan_t plan, size_t* qkv_bytes, size_t* o_bytes, size_t* lse_bytes) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    const size_t M = static_cast<size_t>(plan->M);
+    if (qkv_bytes) *qkv_bytes = M * plan->t * plan->qkv_w * 2;
+    if (o_bytes) *o_bytes = M * plan->a * plan->d * 2;
+    if (lse_bytes) *lse_bytes = static_cast<size_t>(plan->a) * plan->cfg.batch * seq_pad_of(plan) * 4;
+    return TP_OK;
+}
+
+int tp_attn_forward_train(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                          const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* residual, void* partials,
+                          tp_bf16* out, tp_bf16* QKV, tp_bf16* O, float* LSE, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Wq, "Wq")) ||
+        (rc = need_ptr(Wk, "Wk")) || (rc = need_ptr(Wv, "Wv")) || (rc = need_ptr(Wo, "Wo")) ||
+        (rc = need_ptr(out, "out")) || (rc = opt_ptr(residual, "residual")) || (rc = need_ptr(QKV, "QKV")) ||
+        (rc = need_ptr(O, "O")) || (rc = need_ptr(LSE, "LSE")))
+        return rc;
+    const bool fused = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
+    if (!fused && (rc = need_ptr(partials, "partials"))) return rc;
+    cudaStream_t s = as_stream(stream);
+    if ((rc = do_qkv(plan, X, Wq, Wk, Wv, QKV, s))) return rc;
+    if ((rc = do_attn_core(plan, QKV, O, s, LSE))) return rc;
+    if ((rc = do_rowwise(plan, O, plan->qw, Wo, plan->h, nullptr, residual, partials, out, fused, s)))
+        return rc;
+    if (!fused) return do_reduce(plan, partials, nullptr, residual, out, plan->h, s);
+    return TP_OK;
+}
+
+int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
+                     const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* dOut, const tp_bf16* QKV,
+                     const tp_bf16* O, const float* LSE, tp_bf16* dX, float* dWq, float* dWk, float* dWv,
+                     float* dWo, int accumulate, void* workspace, size_t ws_bytes, void* stream) {
+    if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
+    if (plan->d != 128) return fail(TP_ERR_UNSUPPORTED, "the attention backward needs head_dim 128");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Wq, "Wq")) ||
+        (rc = need_ptr(Wk, "Wk")) || (rc = need_ptr(Wv, "Wv")) || (rc = need_ptr(Wo, "Wo")) ||
+        (rc = need_ptr(dOut, "dOut")) || (rc = opt_ptr(QKV, "QKV")) || (rc = opt_ptr(O, "O")) ||
+        (rc = opt_ptr(LSE, "LSE")) || (rc = need_ptr(dX, "dX")) || (rc = need_ptr(dWq, "dWq")) ||
+        (rc = need_ptr(dWk, "dWk")) || (rc = need_ptr(dWv, "dWv")) || (rc = need_ptr(dWo, "dWo")))
+        return rc;
+    const bool saved = QKV != nullptr;
+    if (saved != (O != nullptr) || saved != (LSE != nullptr))
+        return fail(TP_ERR_INVALID_ARG, "QKV, O and LSE must be all saved or all NULL");
+    if ((rc = check_ws(plan, TP_OP_ATTN_BACKWARD, workspace, ws_bytes))) return rc;
+    const Layout L = layout_of(plan, TP_OP_ATTN_BACKWARD);
+    size_t off = 0;
+    void* w_do = region(workspace, off);
+    off += L.bdo;
+    float* w_dstat = reinterpret_cast<float*>(region(workspace, off));
+    off += L.bdstat;
+    float* w_dq = reinterpret_cast<float*>(region(workspace, off));
+    off += L.bdq;
+    void* w_dqkv = region(workspace, off);
+    off += L.bdqkv;
+    void* w_qkv = region(workspace, off);
+    off += L.bqkv;
+    void* w_o = region(workspace, off);
+    off += L.bo;
+    float* w_lse = reinterpret_cast<float*>(region(workspace, off));
+    cudaStream_t s = as_stream(stream);
+    const int64_t M = plan->M, h = plan->h, ad = plan->a * plan->d, kd = plan->k * plan->d;
+    const int64_t wd = ad + 2 * kd;  // dQ | dK | dV columns
+    std::string err;
+    const void* qkv = QKV;
+    const void* o = O;
+    const float* lse = LSE;
+    if (!saved) {  // recompute what the forward would have saved
+        if ((rc = do_qkv(plan, X, Wq, Wk, Wv, w_qkv, s))) return rc;
+        if ((rc = do_attn_core(plan, w_qkv, w_o, s, w_lse))) return rc;
+        qkv = w_qkv;
+        o = w_o;
+        lse = w_lse;
+    }
+    {  // dO = dOut Wo (g's backward: the same dOut for every shard)
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_NN;
+        g.M = M;
+        g.N = ad;
+        g.K = h;
+        g.A = dOut;
+        g.B0 = Wo;
+        g.out = w_do;
+        g.ldo = ad;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // dWo = dOut^T O (shard i: columns of its heads)
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_TN;
+        g.M = h;
+        g.N = ad;
+        g.K = M;
+        g.A = dOut;
+        g.lda = h;
+        g.B0 = o;
+        g.out = dWo;
+        g.ldo = ad;
+        g.accumulate = accumulate ? 1 : 0;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // attention core backward: dQ | dK | dV, KV gradients summed over each group
+        tpi::AttnBwdArgs a;
+        a.QKV = qkv;
+        a.ld_qkv = plan->t * plan->qkv_w;
+        a.shard_w = plan->qkv_w;
+        a.q_w = plan->qw;
+        a.kv_w = plan->kvw;
+        a.dO = w_do;
+        a.O = o;
+        a.ld_do = ad;
+        a.lse = lse;
+        a.dstat = w_dstat;
+        a.seq_pad = seq_pad_of(plan);
+        a.dq = w_dq;
+        a.ld_dq = ad;
+        a.dqkv = w_dqkv;
+        a.ld_dqkv = wd;
+        a.dk_col = ad;
+        a.dv_col = ad + kd;
+        a.batch = plan->cfg.batch;
+        a.seq = plan->cfg.seq;
+        a.heads = static_cast<int>(plan->a);
+        a.kv_heads = static_cast<int>(plan->k);
+        a.head_dim = static_cast<int>(plan->d);
+        a.t = static_cast<int>(plan->t);
+        a.status = plan->status;
+        a.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::attn_bwd_launch(a, s, &err), err))) return rc;
+    }
+    {  // dX = [dQ | dK | dV] [Wq ; Wk ; Wv]: f's all-reduce as the K loop over all shards
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_NN;
+        g.M = M;
+        g.N = h;
+        g.K = wd;
+        g.A = w_dqkv;
+        g.B0 = Wq;
+        g.B1 = Wk;
+        g.B2 = Wv;
+        g.k_split = ad;
+        g.k_split2 = ad + kd;
+        g.out = dX;
+        g.ldo = h;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
+    {  // [dWq ; dWk ; dWv] = [dQ | dK | dV]^T X
+        tpi::GemmArgs g;
+        g.mode = tpi::GEMM_TN;
+        g.M = wd;
+        g.N = h;
+        g.K = M;
+        g.A = w_dqkv;
+        g.lda = wd;
+        g.B0 = X;
+        g.out = dWq;
+        g.ldo = h;
+        g.out2 = dWk;
+        g.ldo2 = h;
+        g.row_split = ad;
+        g.out3 = dWv;
+        g.ldo3 = h;
+        g.row_split2 = ad + kd;
+        g.accumulate = accumulate ? 1 : 0;
+        g.status = plan->status;
+        g.timeout_ns = plan->timeout_ns;
+        if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
+    }
     return TP_OK;
 }
 

@@ -97,6 +97,9 @@ struct AttnParams {
     long long ld_o;
     int seq, heads, kv_heads, t, heads_per_shard, shard_w, q_w, kv_w;
     float scale_log2;  // log2(e) / sqrt(d)
+    float* lse;        // nullable: base-2 log-sum-exp per (head, sequence, row)
+    long long seq_pad;
+    int batch;
     unsigned* status;
     unsigned long long timeout_ns;
 };
@@ -389,6 +392,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
                 const float inv = 1.0f / l_sum;
+                if (p.lse && qpos < p.seq)
+                    p.lse[(static_cast<long long>(j) * p.batch + b) * p.seq_pad + qpos] = m_ref + log2f(l_sum);
                 __nv_bfloat16* orow = p.o + static_cast<long long>(tok0 + qpos) * p.ld_o +
                                       static_cast<long long>(j) * D;
 #pragma unroll 1
@@ -463,6 +468,9 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     p.q_w = static_cast<int>(a.q_w);
     p.kv_w = static_cast<int>(a.kv_w);
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.lse = a.lse;
+    p.seq_pad = a.seq_pad;
+    p.batch = a.batch;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     const int smem = Layout<D>::SMEM;

@@ -1,0 +1,648 @@
+// tp_attn_bwd.cu -- backward of the causal GQA attention core on sm_103a
+// tensor cores (tcgen05 / TMEM), fed by TMA.
+//
+// Source: "텐서 병렬화" (itwiki, Tensor parallelism), sections "셀프 어텐션"
+// (heads are independent, so each shard back-propagates through its own
+// heads with no communication) and "통신 연산 f와 g" (the backward pass).
+// The per-head gradients are the chain rule through each row's softmax:
+// with s = q.k / sqrt(d), P = softmax(s) over the causal keys, O = P V and
+// the upstream dO,
+//   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO (.) O),  dS = P (.) (dP - D),
+//   dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d).
+// P is recomputed from the forward's saved base-2 log-sum-exp per row.
+//
+// Kernels (one call = three launches):
+//   attn_bwd_prep_kernel  D per (head, sequence, row), zero in the padding
+//                         of each sequence to a multiple of 64 rows, and a
+//                         zeroed fp32 dQ accumulator.
+//   attn_bwd_kernel       one CTA per (128-key block, KV head, sequence),
+//                         longest (earliest) key blocks first, 10 warps:
+//     warp 0     TMA: K and V of the key block once; then, per step, Q and
+//                dO of 64 queries of one query head of the group plus their
+//                log-sum-exp and D (3-stage ring).
+//     warp 1     TMEM owner and MMA issuer.  Per step:
+//                  S^T  = K Q^T   and dP^T = V dO^T   (128 x 64, TMEM)
+//                then, once the softmax warps have written P^T and dS^T:
+//                  dV  += P^T dO,  dK += dS^T Q      (128 x d, TMEM, over
+//                                                      the whole group)
+//                  dQ^T = K^T dS^T                    (d x 64, TMEM)
+//                S^T of the next step is issued before the gradients of the
+//                current one, so the tensor core works while the softmax
+//                warps compute.
+//     warps 2-5  one key row per thread: P^T = 2^(S^T log2(e)/sqrt(d) - lse)
+//                under the causal mask, dS^T = P^T (dP^T - D); both to
+//                128-byte-swizzled shared memory as bf16; at the end dV and
+//                dK (times 1/sqrt(d)) to global memory as bf16.
+//     warps 6-9  one head dimension per thread: dQ^T from TMEM, added (times
+//                1/sqrt(d)) to the fp32 accumulator, 32 consecutive floats
+//                per warp instruction.
+//   attn_bwd_dq_cast_kernel  the accumulator to bf16.
+// The gradient of a KV head sums over every query head of its group inside
+// one CTA's TMEM accumulators, so the KV replicas of the t-device form (when
+// there are fewer KV heads than shards) need no extra reduction: the sum
+// over replicas is the sum over the group.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <string>
+
+#include "tp_device.cuh"
+#include "tp_internal.h"
+
+namespace {
+
+using namespace tpk;
+
+constexpr int HD = 128;                        // head dimension this kernel handles
+constexpr int BKEYS = 128;                     // keys per CTA: UMMA M of S^T, dP^T, dV, dK
+constexpr int BQ = 64;                         // queries per step: UMMA N of S^T, dP^T, dQ^T
+constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
+constexpr int NTHREADS = 320;
+constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
+constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
+constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
+constexpr int QT_BYTES = 2 * QBOX_BYTES;       // Q or dO tile: 16 KB
+constexpr int PT_BYTES = BKEYS * BQ * 2;       // P^T or dS^T [128 keys][64 queries]: 16 KB
+constexpr int STAT_BYTES = 2 * BQ * 4;         // log-sum-exp and D of 64 queries
+
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KT_BYTES;
+constexpr int OFF_Q = OFF_V + KT_BYTES;
+constexpr int OFF_DO = OFF_Q + NSTAGE * QT_BYTES;
+constexpr int OFF_PT = OFF_DO + NSTAGE * QT_BYTES;
+constexpr int OFF_DST = OFF_PT + PT_BYTES;
+constexpr int OFF_STAT = OFF_DST + PT_BYTES;
+constexpr int OFF_BAR = OFF_STAT + NSTAGE * STAT_BYTES;
+
+enum {
+    B_KV_FULL = 0,
+    B_Q_FULL = 1,   // x NSTAGE
+    B_Q_EMPTY = 4,  // x NSTAGE: one MMA commit + 4 softmax warps (statistics read)
+    B_S_FULL = 7,
+    B_S_EMPTY = 8,
+    B_P_FULL = 9,
+    B_P_EMPTY = 10,
+    B_DQ_FULL = 11,
+    B_DQ_EMPTY = 12,
+    B_DKV_FULL = 13,
+    B_DRAIN = 14,
+    NUM_BARS = 15
+};
+constexpr int SMEM_BYTES = OFF_BAR + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
+
+// TMEM columns (512 allocated): S^T, dP^T, dQ^T (64 each), dV, dK (128 each).
+constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+
+static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_PT % 1024 == 0 && OFF_DST % 1024 == 0,
+              "swizzled tiles must be 1024-byte aligned");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+struct BwdParams {
+    CUtensorMap map_kv;  // the QKV buffer: dims {ld_qkv, tokens}, box {64, 128}
+    CUtensorMap map_q;   // the same buffer, box {64, 64}
+    CUtensorMap map_do;  // dO [tokens][a d], box {64, 64}
+    const float* lse;    // [a][batch][seq_pad]
+    const float* dstat;  // [a][batch][seq_pad]
+    float* dq;           // [tokens][ld_dq] fp32 accumulator
+    long long ld_dq;
+    __nv_bfloat16* dkv;  // dK of KV head g at columns dk_col + g d, dV at dv_col + g d
+    long long ld_dkv, dk_col, dv_col;
+    long long seq_pad;
+    int seq, batch, heads, kv_heads, t, heads_per_shard, shard_w, q_w, kv_w;
+    float scale, scale_log2;
+    unsigned* status;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 200000000ull) break;  // 200 ms
+    }
+}
+
+// 2^x with the SFU's approximate exp2 (PTX ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One-dimensional bulk copy global -> shared, completing on an mbarrier
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sK = base + OFF_K, sV = base + OFF_V, sQ = base + OFF_Q, sDO = base + OFF_DO,
+                   sPT = base + OFF_PT, sDST = base + OFF_DST, sSTAT = base + OFF_STAT;
+    const float* stat = reinterpret_cast<const float*>(gbase + OFF_STAT);
+    const uint32_t bar0 = base + OFF_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_kb = p.kv_heads * p.batch;
+    const int kb = static_cast<int>(blockIdx.x) / per_kb;  // ascending: the longest first
+    const int rem = static_cast<int>(blockIdx.x) - kb * per_kb;
+    const int g = rem / p.batch, b = rem - g * p.batch;
+    const int G = p.heads / p.kv_heads;  // query heads of the group
+    const int nqb = (p.seq + BQ - 1) / BQ;
+    const int qb0 = (kb * BKEYS) / BQ;  // causal: earlier query blocks see none of these keys
+    const int nq = nqb - qb0;
+    const int n_it = G * nq;
+    const int tok0 = b * p.seq;
+    const int k0 = kb * BKEYS;
+    // KV head g in the shard-blocked QKV buffer: its shard (the first that
+    // holds it when it is replicated) and its slot there.
+    int sh, slot;
+    if (p.kv_heads >= p.t) {
+        const int per = p.kv_heads / p.t;
+        sh = g / per;
+        slot = g - sh * per;
+    } else {
+        sh = g * (p.t / p.kv_heads);
+        slot = 0;
+    }
+    const int kcol = sh * p.shard_w + p.q_w + slot * HD;
+    const int vcol = kcol + p.kv_w;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_KV_FULL), 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(bar(B_Q_FULL + s), 1);
+            mbar_init(bar(B_Q_EMPTY + s), 1 + 4);
+        }
+        mbar_init(bar(B_S_FULL), 1);
+        mbar_init(bar(B_S_EMPTY), 4);
+        mbar_init(bar(B_P_FULL), 4);
+        mbar_init(bar(B_P_EMPTY), 1);
+        mbar_init(bar(B_DQ_FULL), 1);
+        mbar_init(bar(B_DQ_EMPTY), 4);
+        mbar_init(bar(B_DKV_FULL), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.map_kv);
+        tma_prefetch_desc(&p.map_q);
+        tma_prefetch_desc(&p.map_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t issued = 0, ipar = 0;
+            mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * KT_BYTES);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tma_load_2d(sK + c * KBOX_BYTES, &p.map_kv, bar(B_KV_FULL), kcol + 64 * c, tok0 + k0);
+                tma_load_2d(sV + c * KBOX_BYTES, &p.map_kv, bar(B_KV_FULL), vcol + 64 * c, tok0 + k0);
+            }
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % NSTAGE;
+                const uint32_t use = static_cast<uint32_t>(it / NSTAGE);
+                if (!mbar_wait(bar(B_Q_EMPTY + st), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int jj = it / nq, qb = qb0 + (it - jj * nq);
+                const int j = g * G + jj;
+                const int shj = j / p.heads_per_shard;
+                const int qcol = shj * p.shard_w + (j - shj * p.heads_per_shard) * HD;
+                const int row = tok0 + qb * BQ;
+                mbar_arrive_expect_tx(bar(B_Q_FULL + st), 2 * QT_BYTES + STAT_BYTES);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tma_load_2d(sQ + st * QT_BYTES + c * QBOX_BYTES, &p.map_q, bar(B_Q_FULL + st),
+                                qcol + 64 * c, row);
+                    tma_load_2d(sDO + st * QT_BYTES + c * QBOX_BYTES, &p.map_do, bar(B_Q_FULL + st),
+                                j * HD + 64 * c, row);
+                }
+                const long long srow = (static_cast<long long>(j) * p.batch + b) * p.seq_pad + qb * BQ;
+                bulk_load_1d(sSTAT + st * STAT_BYTES, p.lse + srow, BQ * 4, bar(B_Q_FULL + st));
+                bulk_load_1d(sSTAT + st * STAT_BYTES + BQ * 4, p.dstat + srow, BQ * 4, bar(B_Q_FULL + st));
+                issued |= 1u << st;
+                ipar = (ipar & ~(1u << st)) | ((use & 1u) << st);
+            }
+            if (!ok) {
+                drain_wait(bar(B_KV_FULL), 0);
+                for (int s = 0; s < NSTAGE; ++s)
+                    if (issued & (1u << s)) drain_wait(bar(B_Q_FULL + s), (ipar >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            // S^T, dP^T: M 128 keys, N 64 queries, both operands K-major (K = d).
+            constexpr uint32_t id_s = idesc_bf16_f32(BKEYS, BQ);
+            // dV, dK: M 128 keys, N d; A = P^T / dS^T K-major (K = queries),
+            // B = dO / Q read MN-major from their [query][d] tiles.
+            constexpr uint32_t id_kv = idesc_bf16_f32(BKEYS, HD) | (1u << 16);
+            // dQ^T: M d, N 64 queries, K = keys; A = K read MN-major from its
+            // [key][d] tile, B = dS^T read MN-major from its [key][query] tile.
+            constexpr uint32_t id_q = idesc_bf16_f32(HD, BQ) | (1u << 15) | (1u << 16);
+            bool ok = mbar_wait(bar(B_KV_FULL), 0, abort_flag, p.status, p.timeout_ns);
+            auto issue_s = [&](int it) -> bool {
+                const int st = it % NSTAGE;
+                if (!mbar_wait(bar(B_Q_FULL + st), static_cast<uint32_t>(it / NSTAGE) & 1u, abort_flag,
+                               p.status, p.timeout_ns))
+                    return false;
+                if (!mbar_wait(bar(B_S_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
+                               p.timeout_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < HD / 16; ++ks) {
+                    const uint32_t a_off = (ks >> 2) * KBOX_BYTES + (ks & 3) * 32;
+                    const uint32_t b_off = (ks >> 2) * QBOX_BYTES + (ks & 3) * 32;
+                    umma_bf16(tmem + COL_S, sdesc_sw128(sK + a_off), sdesc_sw128(q + b_off), id_s,
+                              ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < HD / 16; ++ks) {
+                    const uint32_t a_off = (ks >> 2) * KBOX_BYTES + (ks & 3) * 32;
+                    const uint32_t b_off = (ks >> 2) * QBOX_BYTES + (ks & 3) * 32;
+                    umma_bf16(tmem + COL_DP, sdesc_sw128(sV + a_off), sdesc_sw128(dO + b_off), id_s,
+                              ks > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(B_S_FULL));
+                return true;
+            };
+            auto issue_grad = [&](int it) -> bool {
+                const int st = it % NSTAGE;
+                if (!mbar_wait(bar(B_P_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
+                               p.timeout_ns))
+                    return false;
+                if (!mbar_wait(bar(B_DQ_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
+                               p.timeout_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries per UMMA
+                    umma_bf16(tmem + COL_DV, sdesc_sw128(sPT + ks * 32),
+                              sdesc_sw128_mn(dO + ks * 2048, QBOX_BYTES, 1024), id_kv,
+                              (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    umma_bf16(tmem + COL_DK, sdesc_sw128(sDST + ks * 32),
+                              sdesc_sw128_mn(q + ks * 2048, QBOX_BYTES, 1024), id_kv,
+                              (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys per UMMA
+                    umma_bf16(tmem + COL_DQ, sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
+                              sdesc_sw128_mn(sDST + ks * 2048, KBOX_BYTES, 1024), id_q, ks > 0 ? 1u : 0u);
+                umma_commit(bar(B_P_EMPTY));
+                umma_commit(bar(B_DQ_FULL));
+                umma_commit(bar(B_Q_EMPTY + st));
+                return true;
+            };
+            for (int it = 0; it < n_it && ok; ++it) {
+                ok = issue_s(it);
+                if (ok && it > 0) ok = issue_grad(it - 1);
+            }
+            if (ok && n_it > 0) ok = issue_grad(n_it - 1);
+            if (ok) {
+                umma_commit(bar(B_DKV_FULL));
+            } else {
+                umma_commit(bar(B_DRAIN));
+                drain_wait(bar(B_DRAIN), 0);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ softmax gradient
+        const int q4 = warp & 3;  // TMEM lane quadrant
+        const int r = q4 * 32 + lane;
+        const int kpos = k0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int st = it % NSTAGE;
+            const int jj = it / nq, qb = qb0 + (it - jj * nq);
+            bool got = mbar_wait(bar(B_S_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
+                                 p.timeout_ns);
+            // The statistics in the stage were written by TMA: observe their
+            // barrier too.
+            got = got && mbar_wait(bar(B_Q_FULL + st), static_cast<uint32_t>(it / NSTAGE) & 1u, abort_flag,
+                                   p.status, p.timeout_ns);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* lse = stat + st * (STAT_BYTES / 4);
+            const float* dd = lse + BQ;
+            uint32_t pk[BQ / 2], sk[BQ / 2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tmem + lane_off + COL_S + h2 * 32, sv);
+                tmem_ld32(tmem + lane_off + COL_DP + h2 * 32, dp);
+                tmem_ld_wait();
+                if (h2 == 1) {  // S^T and dP^T are in registers: TMEM may be rewritten
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_S_EMPTY));
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pv[2], gv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int cq = h2 * 32 + c + e;
+                        const int qpos = qb * BQ + cq;
+                        const bool valid = kpos <= qpos && qpos < p.seq;
+                        const float pp = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lse[cq]));
+                        pv[e] = valid ? pp : 0.0f;
+                        gv[e] = valid ? pp * (__uint_as_float(dp[c + e]) - dd[cq]) : 0.0f;
+                    }
+                    pk[(h2 * 32 + c) / 2] = pack_bf16x2(pv[0], pv[1]);
+                    sk[(h2 * 32 + c) / 2] = pack_bf16x2(gv[0], gv[1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_Q_EMPTY + st));  // statistics read
+            // The previous step's gradient MMAs are done with P^T and dS^T.
+            const bool got2 = mbar_wait(bar(B_P_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag,
+                                        p.status, p.timeout_ns);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got2)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // Row r (a key) of P^T and dS^T: 64 queries = one 128-byte row;
+            // 16-byte chunk c of the row sits at chunk c ^ (r % 8).
+#pragma unroll
+            for (int c8 = 0; c8 < BQ / 8; ++c8) {
+                const uint32_t off = static_cast<uint32_t>(r) * 128 + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4);
+                st_shared_v4(sPT + off, pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                st_shared_v4(sDST + off, sk[4 * c8], sk[4 * c8 + 1], sk[4 * c8 + 2], sk[4 * c8 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+        }
+        if (ok) {
+            const bool got = mbar_wait(bar(B_DKV_FULL), 0, abort_flag, p.status, p.timeout_ns);
+            __syncwarp();
+            if (__all_sync(0xffffffffu, got)) {
+                tc_fence_after();
+                const bool row_ok = kpos < p.seq;
+                __nv_bfloat16* drow = p.dkv + static_cast<long long>(tok0 + (row_ok ? kpos : 0)) * p.ld_dkv;
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+                    const float mul = which ? p.scale : 1.0f;
+                    __nv_bfloat16* dst = drow + (which ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD;
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c * 32, v);
+                        tmem_ld_wait();
+                        if (row_ok) {
+#pragma unroll
+                            for (int g8 = 0; g8 < 4; ++g8) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    w[e] = pack_bf16x2(__uint_as_float(v[g8 * 8 + 2 * e]) * mul,
+                                                       __uint_as_float(v[g8 * 8 + 2 * e + 1]) * mul);
+                                *reinterpret_cast<uint4*>(dst + c * 32 + g8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ dQ accumulation
+        const int q4 = warp & 3;
+        const int dim = q4 * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        for (int it = 0; it < n_it; ++it) {
+            const bool got = mbar_wait(bar(B_DQ_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
+                                       p.timeout_ns);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_off + COL_DQ, v0);
+            tmem_ld32(tmem + lane_off + COL_DQ + 32, v1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+            const int jj = it / nq, qb = qb0 + (it - jj * nq);
+            const int j = g * G + jj;
+            const int q0 = qb * BQ;
+            float* dst = p.dq + static_cast<long long>(tok0 + q0) * p.ld_dq + static_cast<long long>(j) * HD + dim;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (q0 + c < p.seq) atomicAdd(dst + static_cast<long long>(c) * p.ld_dq, __uint_as_float(v0[c]) * p.scale);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (q0 + 32 + c < p.seq)
+                    atomicAdd(dst + static_cast<long long>(32 + c) * p.ld_dq, __uint_as_float(v1[c]) * p.scale);
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// D[(j batch + b) seq_pad + pos] = sum_c dO[row][j d + c] O[row][j d + c]
+// (0 for pos >= seq), and dQ accumulator row segment [j d, j d + d) = 0.
+// One warp per (head, sequence, padded position).
+constexpr int PREP_WARPS = 8;
+
+__global__ void __launch_bounds__(PREP_WARPS * 32) attn_bwd_prep_kernel(
+    const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O, long long ld, int heads,
+    int d, int batch, int seq, long long seq_pad, float* __restrict__ dstat, float* __restrict__ dq,
+    long long ld_dq) {
+    const long long idx = static_cast<long long>(blockIdx.x) * PREP_WARPS + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const long long total = static_cast<long long>(heads) * batch * seq_pad;
+    if (idx >= total) return;
+    const long long per_head = static_cast<long long>(batch) * seq_pad;
+    const int j = static_cast<int>(idx / per_head);
+    const long long r = idx - j * per_head;
+    const int b = static_cast<int>(r / seq_pad);
+    const int pos = static_cast<int>(r - static_cast<long long>(b) * seq_pad);
+    float acc = 0.0f;
+    if (pos < seq) {
+        const long long row = static_cast<long long>(b) * seq + pos;
+        const __nv_bfloat16* a = dO + row * ld + static_cast<long long>(j) * d;
+        const __nv_bfloat16* o = O + row * ld + static_cast<long long>(j) * d;
+        for (int c = lane * 2; c < d; c += 64) {
+            const float2 x = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(a + c));
+            const float2 y = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(o + c));
+            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+        float* z = dq + row * ld_dq + static_cast<long long>(j) * d;
+        for (int c = lane * 4; c < d; c += 128) *reinterpret_cast<float4*>(z + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) dstat[idx] = acc;
+}
+
+// out[row][c] = bf16(acc[row][c]) for c < n (n % 8 == 0).
+__global__ void attn_bwd_dq_cast_kernel(const float* __restrict__ acc, long long ld_acc, long long rows,
+                                        int n, __nv_bfloat16* __restrict__ out, long long ld_out) {
+    const long long per_row = n / 8;
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * per_row) return;
+    const long long row = i / per_row;
+    const int c = static_cast<int>(i - row * per_row) * 8;
+    const float4 a = *reinterpret_cast<const float4*>(acc + row * ld_acc + c);
+    const float4 bq = *reinterpret_cast<const float4*>(acc + row * ld_acc + c + 4);
+    *reinterpret_cast<uint4*>(out + row * ld_out + c) =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(bq.x, bq.y), pack_bf16x2(bq.z, bq.w));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool encode_2d(EncodeTiledFn encode, CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+               uint64_t ld, uint32_t box_rows, std::string* err) {
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (err) *err = "cuTensorMapEncodeTiled (attention backward) failed: " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+int check(const char* what, std::string* err) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        if (err) *err = std::string(what) + ": " + cudaGetErrorString(e);
+        return TP_ERR_CUDA;
+    }
+    return TP_OK;
+}
+
+}  // namespace
+
+namespace tpi {
+
+int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err) {
+    if (a.batch == 0 || a.seq == 0) return TP_OK;
+    if (a.head_dim != HD) {
+        if (err) *err = "the attention backward supports head_dim 128";
+        return TP_ERR_UNSUPPORTED;
+    }
+    const long long tokens = static_cast<long long>(a.batch) * a.seq;
+    // 1. D and a zeroed dQ accumulator.
+    {
+        const long long total = static_cast<long long>(a.heads) * a.batch * a.seq_pad;
+        const long long blocks = (total + PREP_WARPS - 1) / PREP_WARPS;
+        attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), PREP_WARPS * 32, 0, stream>>>(
+            reinterpret_cast<const __nv_bfloat16*>(a.dO), reinterpret_cast<const __nv_bfloat16*>(a.O),
+            a.ld_do, a.heads, HD, a.batch, a.seq, a.seq_pad, a.dstat, a.dq, a.ld_dq);
+        int rc = check("attention backward prep kernel", err);
+        if (rc) return rc;
+    }
+    // 2. The tensor-core kernel.
+    {
+        BwdParams p;
+        memset(&p, 0, sizeof(p));
+        void* fn_ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn_ptr, 12000, cudaEnableDefault,
+                                             &qr) != cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess || !fn_ptr) {
+            if (err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+            return TP_ERR_CUDA;
+        }
+        EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(fn_ptr);
+        if (!encode_2d(encode, &p.map_kv, a.QKV, a.ld_qkv, tokens, a.ld_qkv, BKEYS, err) ||
+            !encode_2d(encode, &p.map_q, a.QKV, a.ld_qkv, tokens, a.ld_qkv, BQ, err) ||
+            !encode_2d(encode, &p.map_do, a.dO, static_cast<uint64_t>(a.heads) * HD, tokens, a.ld_do, BQ, err))
+            return TP_ERR_CUDA;
+        p.lse = a.lse;
+        p.dstat = a.dstat;
+        p.dq = a.dq;
+        p.ld_dq = a.ld_dq;
+        p.dkv = reinterpret_cast<__nv_bfloat16*>(a.dqkv);
+        p.ld_dkv = a.ld_dqkv;
+        p.dk_col = a.dk_col;
+        p.dv_col = a.dv_col;
+        p.seq_pad = a.seq_pad;
+        p.seq = a.seq;
+        p.batch = a.batch;
+        p.heads = a.heads;
+        p.kv_heads = a.kv_heads;
+        p.t = a.t;
+        p.heads_per_shard = a.heads / a.t;
+        p.shard_w = static_cast<int>(a.shard_w);
+        p.q_w = static_cast<int>(a.q_w);
+        p.kv_w = static_cast<int>(a.kv_w);
+        p.scale = 1.0f / sqrtf(static_cast<float>(HD));
+        p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+        p.status = a.status;
+        p.timeout_ns = a.timeout_ns;
+        static bool configured[64] = {false};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 64 && !configured[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 SMEM_BYTES);
+            if (e != cudaSuccess) {
+                if (err) *err = std::string("cudaFuncSetAttribute(attention backward): ") + cudaGetErrorString(e);
+                return TP_ERR_CUDA;
+            }
+            configured[dev] = true;
+        }
+        const unsigned grid = static_cast<unsigned>(((a.seq + BKEYS - 1) / BKEYS) * a.kv_heads * a.batch);
+        attn_bwd_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
+        int rc = check("attention backward kernel", err);
+        if (rc) return rc;
+    }
+    // 3. dQ to bf16.
+    {
+        const long long n = static_cast<long long>(a.heads) * HD;
+        const long long items = tokens * (n / 8);
+        attn_bwd_dq_cast_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
+            a.dq, a.ld_dq, tokens, static_cast<int>(n), reinterpret_cast<__nv_bfloat16*>(a.dqkv), a.ld_dqkv);
+        return check("attention backward dQ cast kernel", err);
+    }
+}
+
+}  // namespace tpi

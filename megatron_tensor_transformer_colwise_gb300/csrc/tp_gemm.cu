@@ -127,8 +127,10 @@ struct GemmParams {
     long long ldaux, n_half;
     void* out2;
     long long ldo2;
-    int k_split;    // GEMM_NN: first K row read from mapB[1]
-    int row_split;  // GEMM_TN: first output row written to out2
+    int k_split, k_split2;      // GEMM_NN: first K rows read from mapB[1], mapB[2]
+    int row_split, row_split2;  // GEMM_TN: first output rows written to out2, out3
+    void* out3;
+    long long ldo3;
     int accumulate;
     CUtensorMap mapO[3];  // BWD_ACT: TMA-store maps of dU, dG, H (64-byte swizzle)
     unsigned* status;
@@ -360,10 +362,12 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                             else tma_load_2d(dst + e * MN_BLOCK_BYTES, &p.mapA, full_l, arow + 64 * e, kc);
                         }
                     } else if (c >= 0 && Major<MODE>::B_MN) {
-                        // [K][N] source; GEMM_NN takes K rows >= k_split from B1.
+                        // [K][N] source; GEMM_NN takes K rows >= k_split from B1
+                        // and >= k_split2 from B2.
+                        const bool hi2 = MODE == tpi::GEMM_NN && kc >= p.k_split2;
                         const bool hi = MODE == tpi::GEMM_NN && kc >= p.k_split;
-                        const CUtensorMap* map = hi ? &p.mapB[1] : &p.mapB[0];
-                        const int kk = hi ? kc - p.k_split : kc;
+                        const CUtensorMap* map = hi2 ? &p.mapB[2] : (hi ? &p.mapB[1] : &p.mapB[0]);
+                        const int kk = hi2 ? kc - p.k_split2 : (hi ? kc - p.k_split : kc);
                         if (CG == 2) tma_load_2d_pair(dst, map, full_l, brow[c < 0 ? 0 : c], kk);
                         else tma_load_2d(dst, map, full_l, brow[c < 0 ? 0 : c], kk);
                     } else {
@@ -653,8 +657,11 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                 } else if (MODE == tpi::GEMM_TN) {
                     float* out = row < p.row_split
                                      ? reinterpret_cast<float*>(p.out) + static_cast<long long>(row) * p.ldo
-                                     : reinterpret_cast<float*>(p.out2) +
-                                           static_cast<long long>(row - p.row_split) * p.ldo2;
+                                 : row < p.row_split2
+                                     ? reinterpret_cast<float*>(p.out2) +
+                                           static_cast<long long>(row - p.row_split) * p.ldo2
+                                     : reinterpret_cast<float*>(p.out3) +
+                                           static_cast<long long>(row - p.row_split2) * p.ldo3;
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
                         const int col = col0 + g * 4;
@@ -785,7 +792,7 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
         tma_prefetch_desc(&p.mapB[0]);
         if (MODE == tpi::GEMM_COL_SWIGLU || MODE == tpi::GEMM_COL_QKV || MODE == tpi::GEMM_NN)
             tma_prefetch_desc(&p.mapB[1]);
-        if (MODE == tpi::GEMM_COL_QKV) tma_prefetch_desc(&p.mapB[2]);
+        if (MODE == tpi::GEMM_COL_QKV || MODE == tpi::GEMM_NN) tma_prefetch_desc(&p.mapB[2]);
     }
     if (warp == 1) {
         if (CG == 2) {
@@ -976,24 +983,32 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
             if (!make_map(&p.mapA, a.A, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
         }
         // B stored [K rows][N]: (N, K rows) views; GEMM_NN splits K rows at
-        // k_split between B0 and B1 (k_split a multiple of BK).
+        // k_split and k_split2 between B0, B1 and B2 (multiples of BK).
         const int64_t split = (a.mode == GEMM_NN && a.B1) ? a.k_split : a.K;
-        if (split % BK != 0 && split != a.K) {
-            if (err) *err = "K split of the NN GEMM is not a multiple of 64";
+        const int64_t split2 = (a.mode == GEMM_NN && a.B1 && a.B2) ? a.k_split2 : a.K;
+        if ((split % BK != 0 && split != a.K) || (split2 % BK != 0 && split2 != a.K) || split2 < split) {
+            if (err) *err = "K splits of the NN GEMM must be ordered multiples of 64";
             return TP_ERR_INVALID_ARG;
         }
         p.k_split = static_cast<int>(split);
+        p.k_split2 = static_cast<int>(split2);
         const uint64_t sB[1] = {(uint64_t)a.N * 2};
         const uint64_t dB0[2] = {(uint64_t)a.N, (uint64_t)split};
         if (!make_map(&p.mapB[0], a.B0, 2, dB0, sB, box_mn, err)) return TP_ERR_CUDA;
-        if (split < a.K) {
-            const uint64_t dB1[2] = {(uint64_t)a.N, (uint64_t)(a.K - split)};
-            if (!make_map(&p.mapB[1], a.B1, 2, dB1, sB, box_mn, err)) return TP_ERR_CUDA;
-        } else {
-            p.mapB[1] = p.mapB[0];
-        }
+        p.mapB[1] = p.mapB[0];
         p.mapB[2] = p.mapB[0];
+        if (split < split2) {
+            const uint64_t dB1[2] = {(uint64_t)a.N, (uint64_t)(split2 - split)};
+            if (!make_map(&p.mapB[1], a.B1, 2, dB1, sB, box_mn, err)) return TP_ERR_CUDA;
+        }
+        if (split2 < a.K) {
+            const uint64_t dB2[2] = {(uint64_t)a.N, (uint64_t)(a.K - split2)};
+            if (!make_map(&p.mapB[2], a.B2, 2, dB2, sB, box_mn, err)) return TP_ERR_CUDA;
+        }
         p.row_split = static_cast<int>(a.mode == GEMM_TN && a.out2 ? a.row_split : a.M);
+        p.row_split2 = static_cast<int>(a.mode == GEMM_TN && a.out2 && a.out3 ? a.row_split2 : a.M);
+        p.out3 = a.out3;
+        p.ldo3 = a.ldo3;
         if (a.mode == GEMM_BWD_ACT) {
             // Output boxes of 32 x 32 bf16, 64-byte swizzle: dU = out[:, :N],
             // dG = out[:, n_half : n_half + N] (SwiGLU), H = out2.

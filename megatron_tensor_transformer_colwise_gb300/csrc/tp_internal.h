@@ -70,10 +70,12 @@ struct GemmArgs {
     //  GEMM_BWD_ACT: aux = saved pre-activations [M][ldaux] (U at column n,
     //    G at n_half + n for SwiGLU); out = dU (dG at n_half + n), ldo;
     //    out2 = H [M][ldo2] (nullable).  A = dZ [M][K], B0 = W2 [K][N].
-    //  GEMM_NN: A [M][lda] K-major; B0 = [k_split][N], B1 = [K - k_split][N]
-    //    (nullable when k_split == K), MN-major; bf16 out.
+    //  GEMM_NN: A [M][lda] K-major; B0 = [k_split][N], B1 = [k_split2 -
+    //    k_split][N], B2 = [K - k_split2][N] (nullable when their K range is
+    //    empty), MN-major; bf16 out.
     //  GEMM_TN: A [K][M] and B0 [K][N], both MN-major; fp32 out [M][N];
-    //    rows >= row_split go to out2 (row - row_split); accumulate adds.
+    //    rows in [row_split, row_split2) go to out2 (row - row_split), rows
+    //    >= row_split2 to out3 (row - row_split2); accumulate adds.
     //  COL_ACT / COL_SWIGLU: aux_out (nullable) also receives the
     //    pre-activations (U, and G at n_half + n), ld ldaux.
     int64_t lda = 0;  // 0: K (K-major) or M (MN-major)
@@ -83,8 +85,10 @@ struct GemmArgs {
     int64_t n_half = 0;
     void* out2 = nullptr;
     int64_t ldo2 = 0;
-    int64_t k_split = 0;
-    int64_t row_split = 0;
+    int64_t k_split = 0, k_split2 = 0;
+    void* out3 = nullptr;
+    int64_t ldo3 = 0;
+    int64_t row_split = 0, row_split2 = 0;
     int accumulate = 0;
     unsigned* status = nullptr;
     uint64_t timeout_ns = 2000000000ull;
@@ -126,10 +130,38 @@ struct AttnArgs {
     void* O = nullptr;
     int64_t ld_o = 0;
     int batch = 0, seq = 0, heads = 0, kv_heads = 0, head_dim = 0, t = 1;
+    // Softmax statistics for the backward pass (nullable): lse[(j * batch +
+    // b) * seq_pad + pos] = log2 of the row's sum of 2^(s / sqrt(d) * log2 e),
+    // i.e. the base-2 log-sum-exp of the scaled scores, for pos < seq.
+    float* lse = nullptr;
+    int64_t seq_pad = 0;
     unsigned* status = nullptr;
     uint64_t timeout_ns = 2000000000ull;
 };
 int attn_launch(const AttnArgs& a, cudaStream_t stream, std::string* err);
+
+// Attention core backward (tp_attn_bwd.cu), head_dim 128: three launches
+// (statistics D and a zeroed dQ accumulator; the tcgen05 kernel; dQ to bf16).
+struct AttnBwdArgs {
+    const void* QKV = nullptr;  // the forward's shard-blocked Q | K | V buffer
+    int64_t ld_qkv = 0;
+    int64_t shard_w = 0, q_w = 0, kv_w = 0;
+    const void* dO = nullptr;   // [tokens][a d] bf16, row stride ld_do (also O's)
+    const void* O = nullptr;
+    int64_t ld_do = 0;
+    const float* lse = nullptr; // [a][batch][seq_pad], from the forward
+    float* dstat = nullptr;     // [a][batch][seq_pad] scratch (D)
+    int64_t seq_pad = 0;        // seq rounded up to a multiple of 64
+    float* dq = nullptr;        // [tokens][ld_dq] fp32 scratch
+    int64_t ld_dq = 0;
+    void* dqkv = nullptr;       // bf16 out: dQ at columns [0, a d), dK of KV head g at
+    int64_t ld_dqkv = 0;        // dk_col + g d, dV at dv_col + g d
+    int64_t dk_col = 0, dv_col = 0;
+    int batch = 0, seq = 0, heads = 0, kv_heads = 0, head_dim = 0, t = 1;
+    unsigned* status = nullptr;
+    uint64_t timeout_ns = 2000000000ull;
+};
+int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err);
 
 // Vocabulary-parallel embedding and cross-entropy (tp_vocab.cu).
 int vocab_embedding_launch(const int32_t* ids, int64_t M, const void* E, int64_t v, int h, void* out,

@@ -453,3 +453,19 @@ def attention_backward(batch: int, seq: int, a: int, k: int, X, Wq, Wk, Wv, Wo, 
         batch, seq, h, a, k, d, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(dOut), _p(dX), _p(dWq),
         _p(dWk), _p(dWv), _p(dWo)))
     return dX, dWq, dWk, dWv, dWo
+
+
+def attention_backward_composed(batch: int, seq: int, a: int, k: int, X, Wq, Wk, Wv, Wo, dOut):
+    """The plain attention-block backward of tpo_attention_backward, composed
+    for large sizes: the projections are library matmuls (numpy, fp64) and
+    the attention core forward and backward are the C oracle's.  Same
+    definition, same order of steps; returns (dX, dWq, dWk, dWv, dWo)."""
+    X, Wq, Wk, Wv, Wo, dOut = map(_d, (X, Wq, Wk, Wv, Wo, dOut))
+    d = Wq.shape[0] // a
+    Q, K, V = X @ Wq.T, X @ Wk.T, X @ Wv.T
+    O = attention_core(batch, seq, a, k, d, Q, K, V)
+    dO = dOut @ Wo
+    dWo = dOut.T @ O
+    dQ, dK, dV = attention_core_backward(batch, seq, a, k, Q, K, V, dO)
+    dX = dQ @ Wq + dK @ Wk + dV @ Wv
+    return dX, dQ.T @ X, dK.T @ X, dV.T @ X, dWo

@@ -27,6 +27,23 @@ def test_header_declares_the_boundary():
     assert tuple(names) == tp.EXPORTED   # binding covers exactly the header
 
 
+def declared_arg_counts():
+    """Number of parameters of every TP_API declaration in tp.h."""
+    src = open(os.path.join(ROOT, "include", "tp.h")).read()
+    out = {}
+    for m in re.finditer(r"^TP_API\s+[\w\s\*]+?\b(tp_\w+)\s*\(([^)]*)\)", src, flags=re.M):
+        params = " ".join(m.group(2).split())
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_header():
+    counts = declared_arg_counts()
+    assert set(counts) == set(tp.EXPORTED)
+    for name, args in tp._SIGS.items():
+        assert len(args) == counts[name], f"{name}: binding {len(args)} args, header {counts[name]}"
+
+
 def test_library_exports_every_declared_symbol():
     L = tp.lib()
     for name in declared_functions():

@@ -675,3 +675,19 @@ def test_attention_backward_sharded_equals_plain(a, k, t):
     for x, y in zip(plain, shard):
         assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max())
     assert np.abs(P.sum(0) - plain[0]).max() < 1e-12 * max(1.0, np.abs(plain[0]).max())
+
+
+def test_attention_backward_composed_equals_c_form():
+    # The large-size composition (numpy projections + C attention core) is
+    # the same definition as the all-C block backward.
+    g = torch.Generator().manual_seed(81)
+    batch, seq, h, a, k, d = 2, 6, 8, 4, 2, 3
+    M = batch * seq
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    W = [(torch.randn(n, m, generator=g, dtype=torch.float64) * 0.5).numpy()
+         for n, m in ((a * d, h), (k * d, h), (k * d, h), (h, a * d))]
+    dOut = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    a1 = oracle.attention_backward(batch, seq, a, k, X, *W, dOut)
+    a2 = oracle.attention_backward_composed(batch, seq, a, k, X, *W, dOut)
+    for x, y in zip(a1, a2):
+        assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max())
