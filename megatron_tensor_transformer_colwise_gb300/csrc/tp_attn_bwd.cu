@@ -16,10 +16,10 @@
 //                         of each sequence to a multiple of 64 rows, and a
 //                         zeroed fp32 dQ accumulator.
 //   attn_bwd_kernel       one CTA per (128-key block, KV head, sequence),
-//                         longest (earliest) key blocks first, 10 warps:
+//                         longest (earliest) key blocks first, 14 warps:
 //     warp 0     TMA: K and V of the key block once; then, per step, Q and
 //                dO of 64 queries of one query head of the group plus their
-//                log-sum-exp and D (3-stage ring).
+//                log-sum-exp and D (2-stage ring).
 //     warp 1     TMEM owner and MMA issuer.  Per step:
 //                  S^T  = K Q^T   and dP^T = V dO^T   (128 x 64, TMEM)
 //                then, once the softmax warps have written P^T and dS^T:
@@ -29,13 +29,14 @@
 //                S^T of the next step is issued before the gradients of the
 //                current one, so the tensor core works while the softmax
 //                warps compute.
-//     warps 2-5  one key row per thread: P^T = 2^(S^T log2(e)/sqrt(d) - lse)
+//     warps 2-9  one key row and 32 of the 64 queries per thread (two warps
+//                per TMEM lane quadrant): P^T = 2^(S^T log2(e)/sqrt(d) - lse)
 //                under the causal mask, dS^T = P^T (dP^T - D); both to
 //                128-byte-swizzled shared memory as bf16; at the end dV and
 //                dK (times 1/sqrt(d)) to global memory as bf16.
-//     warps 6-9  one head dimension per thread: dQ^T from TMEM, added (times
-//                1/sqrt(d)) to the fp32 accumulator, 32 consecutive floats
-//                per warp instruction.
+//     warps 10-13 one head dimension per thread: dQ^T from TMEM (times
+//                1/sqrt(d)) to a [64 queries][32 d] fp32 box in shared memory,
+//                added to the fp32 accumulator by one TMA reduce-add per step.
 //   attn_bwd_dq_cast_kernel  the accumulator to bf16.
 // The gradient of a KV head sums over every query head of its group inside
 // one CTA's TMEM accumulators, so the KV replicas of the t-device form (when
@@ -59,13 +60,15 @@ constexpr int HD = 128;                        // head dimension this kernel han
 constexpr int BKEYS = 128;                     // keys per CTA: UMMA M of S^T, dP^T, dV, dK
 constexpr int BQ = 64;                         // queries per step: UMMA N of S^T, dP^T, dQ^T
 constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
-constexpr int NTHREADS = 320;
+constexpr int SM_WARPS = 8;                    // softmax-gradient warps: 2 per TMEM lane quadrant
+constexpr int NTHREADS = 32 * (2 + SM_WARPS + 4);
 constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
 constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
 constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
 constexpr int QT_BYTES = 2 * QBOX_BYTES;       // Q or dO tile: 16 KB
 constexpr int PT_BYTES = BKEYS * BQ * 2;       // P^T or dS^T [128 keys][64 queries]: 16 KB
 constexpr int STAT_BYTES = 2 * BQ * 4;         // log-sum-exp and D of 64 queries
+constexpr int DQ_BOX_BYTES = BQ * 32 * 4;      // one dQ warp's [64 queries][32 d] fp32: 8 KB
 
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KT_BYTES;
@@ -74,35 +77,43 @@ constexpr int OFF_DO = OFF_Q + NSTAGE * QT_BYTES;
 constexpr int OFF_PT = OFF_DO + NSTAGE * QT_BYTES;
 constexpr int OFF_DST = OFF_PT + PT_BYTES;
 constexpr int OFF_STAT = OFF_DST + PT_BYTES;
-constexpr int OFF_BAR = OFF_STAT + NSTAGE * STAT_BYTES;
+constexpr int OFF_DQ = OFF_STAT + NSTAGE * STAT_BYTES;
+constexpr int OFF_BAR = OFF_DQ + 4 * DQ_BOX_BYTES;
 
-enum {
-    B_KV_FULL = 0,
-    B_Q_FULL = 1,   // x NSTAGE
-    B_Q_EMPTY = 4,  // x NSTAGE: one MMA commit + 4 softmax warps (statistics read)
-    B_S_FULL = 7,
-    B_S_EMPTY = 8,
-    B_P_FULL = 9,
-    B_P_EMPTY = 10,
-    B_DQ_FULL = 11,
-    B_DQ_EMPTY = 12,
-    B_DKV_FULL = 13,
-    B_DRAIN = 14,
-    NUM_BARS = 15
-};
-constexpr int SMEM_BYTES = OFF_BAR + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
+constexpr int B_KV_FULL = 0;
+constexpr int B_Q_FULL = 1;                  // x NSTAGE
+constexpr int B_Q_EMPTY = B_Q_FULL + NSTAGE; // x NSTAGE: one MMA commit + the softmax warps
+constexpr int B_S_FULL = B_Q_EMPTY + NSTAGE;
+constexpr int B_S_EMPTY = B_S_FULL + 1;
+constexpr int B_P_FULL = B_S_EMPTY + 1;
+constexpr int B_P_EMPTY = B_P_FULL + 1;
+constexpr int B_DQ_FULL = B_P_EMPTY + 1;   // x2 (dQ^T double-buffered in TMEM)
+constexpr int B_DQ_EMPTY = B_DQ_FULL + 2;  // x2
+constexpr int B_DKV_FULL = B_DQ_EMPTY + 2;
+constexpr int B_DRAIN = B_DKV_FULL + 1;
+constexpr int NUM_BARS = B_DRAIN + 1;
+// The data fill all but a few bytes of the 227 KB a CTA may use, leaving no
+// room to align the dynamic shared-memory base to 1024 bytes ourselves; the
+// kernel checks at run time that the base is aligned (it is when the kernel
+// has no static shared memory) and otherwise stops with an error flag,
+// touching nothing.
+constexpr int DATA_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
+constexpr int SMEM_BYTES = DATA_BYTES + 128 <= 232448 ? DATA_BYTES + 128 : 232448;
 
-// TMEM columns (512 allocated): S^T, dP^T, dQ^T (64 each), dV, dK (128 each).
-constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+// TMEM columns (512 allocated): S^T, dP^T (64 each), dQ^T x2 (64 each), dV,
+// dK (128 each).
+constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ0 = 384, COL_DQ1 = 448;
 
 static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_PT % 1024 == 0 && OFF_DST % 1024 == 0,
               "swizzled tiles must be 1024-byte aligned");
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(OFF_DQ % 128 == 0, "TMA boxes must be 128-byte aligned");
+static_assert(DATA_BYTES <= 232448, "shared memory");
 
 struct BwdParams {
     CUtensorMap map_kv;  // the QKV buffer: dims {ld_qkv, tokens}, box {64, 128}
     CUtensorMap map_q;   // the same buffer, box {64, 64}
     CUtensorMap map_do;  // dO [tokens][a d], box {64, 64}
+    CUtensorMap map_dq;  // fp32 dQ accumulator [tokens][a d], box {32, 64}, reduce-add target
     const float* lse;    // [a][batch][seq_pad]
     const float* dstat;  // [a][batch][seq_pad]
     float* dq;           // [tokens][ld_dq] fp32 accumulator
@@ -153,6 +164,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+    if (base - raw + static_cast<uint32_t>(DATA_BYTES) > static_cast<uint32_t>(SMEM_BYTES)) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusLayout);
+        return;  // the aligned layout does not fit: nothing was touched
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_kb = p.kv_heads * p.batch;
     const int kb = static_cast<int>(blockIdx.x) / per_kb;  // ascending: the longest first
@@ -183,14 +198,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(bar(B_KV_FULL), 1);
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(B_Q_FULL + s), 1);
-            mbar_init(bar(B_Q_EMPTY + s), 1 + 4);
+            mbar_init(bar(B_Q_EMPTY + s), 1 + SM_WARPS);
         }
         mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_S_EMPTY), 4);
-        mbar_init(bar(B_P_FULL), 4);
+        mbar_init(bar(B_S_EMPTY), SM_WARPS);
+        mbar_init(bar(B_P_FULL), SM_WARPS);
         mbar_init(bar(B_P_EMPTY), 1);
-        mbar_init(bar(B_DQ_FULL), 1);
-        mbar_init(bar(B_DQ_EMPTY), 4);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_DQ_FULL + s), 1);
+            mbar_init(bar(B_DQ_EMPTY + s), 4);
+        }
         mbar_init(bar(B_DKV_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -200,6 +217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         tma_prefetch_desc(&p.map_kv);
         tma_prefetch_desc(&p.map_q);
         tma_prefetch_desc(&p.map_do);
+        tma_prefetch_desc(&p.map_dq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -297,8 +315,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 if (!mbar_wait(bar(B_P_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
                                p.timeout_ns))
                     return false;
-                if (!mbar_wait(bar(B_DQ_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
-                               p.timeout_ns))
+                const int qbuf = it & 1;
+                if (!mbar_wait(bar(B_DQ_EMPTY + qbuf), (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, abort_flag,
+                               p.status, p.timeout_ns))
                     return false;
                 tc_fence_after();
                 const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
@@ -314,10 +333,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                               (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys per UMMA
-                    umma_bf16(tmem + COL_DQ, sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
+                    umma_bf16(tmem + (qbuf ? COL_DQ1 : COL_DQ0), sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
                               sdesc_sw128_mn(sDST + ks * 2048, KBOX_BYTES, 1024), id_q, ks > 0 ? 1u : 0u);
                 umma_commit(bar(B_P_EMPTY));
-                umma_commit(bar(B_DQ_FULL));
+                umma_commit(bar(B_DQ_FULL + qbuf));
                 umma_commit(bar(B_Q_EMPTY + st));
                 return true;
             };
@@ -333,9 +352,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 drain_wait(bar(B_DRAIN), 0);
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + SM_WARPS) {
         // ------------------------------------------------------------ softmax gradient
-        const int q4 = warp & 3;  // TMEM lane quadrant
+        // Two warps per TMEM lane quadrant: key row r, query columns
+        // [32 hh, 32 hh + 32).
+        const int q4 = warp & 3;
+        const int hh = (warp - 2) >> 2;
         const int r = q4 * 32 + lane;
         const int kpos = k0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -355,35 +377,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            const float* lse = stat + st * (STAT_BYTES / 4);
-            const float* dd = lse + BQ;
-            uint32_t pk[BQ / 2], sk[BQ / 2];
+            uint32_t sv[32], dp[32];
+            tmem_ld32(tmem + lane_off + COL_S + hh * 32, sv);
+            tmem_ld32(tmem + lane_off + COL_DP + hh * 32, dp);
+            tmem_ld_wait();
+            // This warp's 32 log-sum-exp and D values: broadcast 16-byte reads
+            // of the stage (released only after the math).
+            const float4* lse4 = reinterpret_cast<const float4*>(stat + st * (STAT_BYTES / 4) + hh * 32);
+            const float4* dd4 = lse4 + BQ / 4;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_EMPTY));  // S^T, dP^T are in registers
+            uint32_t pk[16], sk[16];
+            const int qbase = qb * BQ + hh * 32;
+            // Blocks wholly below the diagonal and inside the sequence need no mask.
+            const bool unmasked = qb * BQ >= k0 + BKEYS - 1 && qb * BQ + BQ <= p.seq;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tmem + lane_off + COL_S + h2 * 32, sv);
-                tmem_ld32(tmem + lane_off + COL_DP + h2 * 32, dp);
-                tmem_ld_wait();
-                if (h2 == 1) {  // S^T and dP^T are in registers: TMEM may be rewritten
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_S_EMPTY));
+            for (int v = 0; v < 8; ++v) {
+                const float4 l4 = lse4[v], d4 = dd4[v];
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                float pv[4], gv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * v + e;
+                    const float pp = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[e]));
+                    const float gg = pp * (__uint_as_float(dp[c]) - dv[e]);
+                    const int qpos = qbase + c;
+                    const bool valid = unmasked || (kpos <= qpos && qpos < p.seq);
+                    pv[e] = valid ? pp : 0.0f;
+                    gv[e] = valid ? gg : 0.0f;
                 }
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float pv[2], gv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cq = h2 * 32 + c + e;
-                        const int qpos = qb * BQ + cq;
-                        const bool valid = kpos <= qpos && qpos < p.seq;
-                        const float pp = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lse[cq]));
-                        pv[e] = valid ? pp : 0.0f;
-                        gv[e] = valid ? pp * (__uint_as_float(dp[c + e]) - dd[cq]) : 0.0f;
-                    }
-                    pk[(h2 * 32 + c) / 2] = pack_bf16x2(pv[0], pv[1]);
-                    sk[(h2 * 32 + c) / 2] = pack_bf16x2(gv[0], gv[1]);
-                }
+                pk[2 * v] = pack_bf16x2(pv[0], pv[1]);
+                pk[2 * v + 1] = pack_bf16x2(pv[2], pv[3]);
+                sk[2 * v] = pack_bf16x2(gv[0], gv[1]);
+                sk[2 * v + 1] = pack_bf16x2(gv[2], gv[3]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_EMPTY + st));  // statistics read
@@ -399,8 +426,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             // Row r (a key) of P^T and dS^T: 64 queries = one 128-byte row;
             // 16-byte chunk c of the row sits at chunk c ^ (r % 8).
 #pragma unroll
-            for (int c8 = 0; c8 < BQ / 8; ++c8) {
-                const uint32_t off = static_cast<uint32_t>(r) * 128 + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4);
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const uint32_t chunk = static_cast<uint32_t>(hh * 4 + c8) ^ static_cast<uint32_t>(r & 7);
+                const uint32_t off = static_cast<uint32_t>(r) * 128 + (chunk << 4);
                 st_shared_v4(sPT + off, pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
                 st_shared_v4(sDST + off, sk[4 * c8], sk[4 * c8 + 1], sk[4 * c8 + 2], sk[4 * c8 + 3]);
             }
@@ -414,27 +442,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             __syncwarp();
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
+                // hh = 0 writes the row's dV, hh = 1 its dK (times 1/sqrt(d)).
                 const bool row_ok = kpos < p.seq;
-                __nv_bfloat16* drow = p.dkv + static_cast<long long>(tok0 + (row_ok ? kpos : 0)) * p.ld_dkv;
+                const float mul = hh ? p.scale : 1.0f;
+                __nv_bfloat16* dst = p.dkv + static_cast<long long>(tok0 + (row_ok ? kpos : 0)) * p.ld_dkv +
+                                     (hh ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD;
 #pragma unroll 1
-                for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
-                    const float mul = which ? p.scale : 1.0f;
-                    __nv_bfloat16* dst = drow + (which ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD;
-#pragma unroll 1
-                    for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c * 32, v);
-                        tmem_ld_wait();
-                        if (row_ok) {
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + (hh ? COL_DK : COL_DV) + c * 32, v);
+                    tmem_ld_wait();
+                    if (row_ok) {
 #pragma unroll
-                            for (int g8 = 0; g8 < 4; ++g8) {
-                                uint32_t w[4];
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            uint32_t w[4];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    w[e] = pack_bf16x2(__uint_as_float(v[g8 * 8 + 2 * e]) * mul,
-                                                       __uint_as_float(v[g8 * 8 + 2 * e + 1]) * mul);
-                                *reinterpret_cast<uint4*>(dst + c * 32 + g8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-                            }
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(v[g8 * 8 + 2 * e]) * mul,
+                                                   __uint_as_float(v[g8 * 8 + 2 * e + 1]) * mul);
+                            *reinterpret_cast<uint4*>(dst + c * 32 + g8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
@@ -442,34 +468,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------------------ dQ accumulation
+        // Each warp owns 32 head dimensions: its [64 queries][32 d] slice of
+        // dQ^T goes (times 1/sqrt(d)) to a row-major fp32 box in shared
+        // memory, which one TMA reduce-add adds to the accumulator.
         const int q4 = warp & 3;
-        const int dim = q4 * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        const uint32_t sdq = base + OFF_DQ + static_cast<uint32_t>(warp - 2 - SM_WARPS) * DQ_BOX_BYTES;
         for (int it = 0; it < n_it; ++it) {
-            const bool got = mbar_wait(bar(B_DQ_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
-                                       p.timeout_ns);
+            const int qbuf = it & 1;
+            const bool got = mbar_wait(bar(B_DQ_FULL + qbuf), static_cast<uint32_t>(it >> 1) & 1u, abort_flag,
+                                       p.status, p.timeout_ns);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
+            const uint32_t col = qbuf ? COL_DQ1 : COL_DQ0;
             uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_off + COL_DQ, v0);
-            tmem_ld32(tmem + lane_off + COL_DQ + 32, v1);
+            tmem_ld32(tmem + lane_off + col, v0);
+            tmem_ld32(tmem + lane_off + col + 32, v1);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+            if (lane == 0) {
+                mbar_arrive(bar(B_DQ_EMPTY + qbuf));
+                bulk_wait_group_read0();  // the previous box has been read
+            }
+            __syncwarp();
             const int jj = it / nq, qb = qb0 + (it - jj * nq);
             const int j = g * G + jj;
-            const int q0 = qb * BQ;
-            float* dst = p.dq + static_cast<long long>(tok0 + q0) * p.ld_dq + static_cast<long long>(j) * HD + dim;
+            // Row c of the box = query c; lane = dimension: 128 contiguous bytes per row.
+#pragma unroll
+            for (int c = 0; c < 32; ++c) st_shared_f32(sdq + c * 128 + lane * 4, __uint_as_float(v0[c]) * p.scale);
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-                if (q0 + c < p.seq) atomicAdd(dst + static_cast<long long>(c) * p.ld_dq, __uint_as_float(v0[c]) * p.scale);
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (q0 + 32 + c < p.seq)
-                    atomicAdd(dst + static_cast<long long>(32 + c) * p.ld_dq, __uint_as_float(v1[c]) * p.scale);
+                st_shared_f32(sdq + (32 + c) * 128 + lane * 4, __uint_as_float(v1[c]) * p.scale);
+            fence_proxy_async_smem();
+            __syncwarp();
+            // Columns of queries past the sequence are exactly zero (dS is
+            // masked there), so the box may overlap the next sequence's rows.
+            if (lane == 0) {
+                tma_reduce_add_2d(&p.map_dq, sdq, j * HD + q4 * 32, tok0 + qb * BQ);
+                bulk_commit_group();
+            }
         }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
     __syncwarp();
     tc_fence_before();
@@ -592,6 +634,19 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
             return TP_ERR_CUDA;
         }
         EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(fn_ptr);
+        {
+            cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.heads) * HD, static_cast<cuuint64_t>(tokens)};
+            cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.ld_dq) * 4};
+            cuuint32_t box[2] = {32, BQ};
+            cuuint32_t estr[2] = {1, 1};
+            CUresult r = encode(&p.map_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dq, dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                if (err) *err = "cuTensorMapEncodeTiled (dQ accumulator) failed: " + std::to_string((int)r);
+                return TP_ERR_CUDA;
+            }
+        }
         if (!encode_2d(encode, &p.map_kv, a.QKV, a.ld_qkv, tokens, a.ld_qkv, BKEYS, err) ||
             !encode_2d(encode, &p.map_q, a.QKV, a.ld_qkv, tokens, a.ld_qkv, BQ, err) ||
             !encode_2d(encode, &p.map_do, a.dO, static_cast<uint64_t>(a.heads) * HD, tokens, a.ld_do, BQ, err))
