@@ -81,17 +81,22 @@ __host__ __device__ constexpr int num_threads() {
 //
 // GEMM_BWD_ACT stages its three outputs through shared memory (one 32 x 32
 // bf16 box per output and epilogue warp, 64-byte swizzle) and writes them
-// with TMA stores; it runs one ring stage fewer to make room.
+// with TMA stores; it runs one ring stage fewer to make room.  GEMM_TN
+// stages its fp32 output the same way (two 32 x 32 fp32 boxes per epilogue
+// warp, alternating, 128-byte swizzle), written by TMA stores or, when
+// accumulating, TMA reduce-adds.
 constexpr int EPI_BOX = 32;                        // rows and columns of an output box
 constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;  // 2 KB
 template <int MODE, int CG>
 struct Cfg {
     static constexpr int B_BYTES = (BN / CG) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr bool STAGED_OUT = MODE == tpi::GEMM_BWD_ACT;
+    static constexpr bool STAGED_OUT = MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_TN;
     static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : 6);
     static constexpr int CHUNKS = (BN / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
-    static constexpr int EPI_BYTES = STAGED_OUT ? 8 * 3 * EPI_BOX_BYTES : 0;  // 8 warps x 3 boxes
+    static constexpr int EPI_BYTES = MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
+                                     : MODE == tpi::GEMM_TN    ? 4 * 2 * 2 * EPI_BOX_BYTES  // 4 warps x 2 fp32 boxes
+                                                               : 0;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TILE_M = BM * CG;
@@ -596,6 +601,40 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                     bwd_act_tile<TP_ACT_NONE, CPW>(p, ug, row_ok, row0, nb, cb, t0, sbuf, n1u, n1g, n2u, n2g);
                     break;
             }
+        } else if (MODE == tpi::GEMM_TN) {
+            // fp32 output through two alternating 32 x 32 boxes per warp
+            // (128-byte swizzle: 16-byte piece j of row r at r * 128 +
+            // (j ^ (r % 8)) * 16); one TMA store, or reduce-add when
+            // accumulating, per 32-column chunk.  The warp's 32 rows lie in
+            // one output (row splits are multiples of 32).
+            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const bool box_ok = row0 < p.M;
+            const int which = row0 >= p.row_split2 ? 2 : (row0 >= p.row_split ? 1 : 0);
+            const int ybase = row0 - (which == 2 ? p.row_split2 : (which == 1 ? p.row_split : 0));
+            const uint32_t sw_base = epi0 + static_cast<uint32_t>(warp - 2) * 4 * EPI_BOX_BYTES;
+            const uint32_t srow = static_cast<uint32_t>(lane) * 128;
+#pragma unroll 1
+            for (int c = cb; c < cb + CPW; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N) break;  // warp-uniform
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);
+                tmem_ld_wait();
+                const uint32_t buf = sw_base + static_cast<uint32_t>(c & 1) * 2 * EPI_BOX_BYTES;
+                if (lane == 0) bulk_wait_group_read1();  // this box's previous store has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(buf + srow + ((static_cast<uint32_t>(j) ^ (lane & 7)) << 4), r[4 * j],
+                                 r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && box_ok) {
+                    if (p.accumulate) tma_reduce_add_2d(&p.mapO[which], buf, col0, ybase);
+                    else tma_store_2d(&p.mapO[which], buf, col0, ybase);
+                    bulk_commit_group();
+                }
+            }
         } else if (MODE == tpi::GEMM_COL_SWIGLU) {
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
@@ -653,29 +692,6 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                         const int col = col0 + g * 4;
                         if (col < p.N)
                             st_v4(out + col, r[g * 4], r[g * 4 + 1], r[g * 4 + 2], r[g * 4 + 3]);
-                    }
-                } else if (MODE == tpi::GEMM_TN) {
-                    float* out = row < p.row_split
-                                     ? reinterpret_cast<float*>(p.out) + static_cast<long long>(row) * p.ldo
-                                 : row < p.row_split2
-                                     ? reinterpret_cast<float*>(p.out2) +
-                                           static_cast<long long>(row - p.row_split) * p.ldo2
-                                     : reinterpret_cast<float*>(p.out3) +
-                                           static_cast<long long>(row - p.row_split2) * p.ldo3;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const int col = col0 + g * 4;
-                        if (col >= p.N) continue;
-                        float4 v = make_float4(__uint_as_float(r[g * 4]), __uint_as_float(r[g * 4 + 1]),
-                                               __uint_as_float(r[g * 4 + 2]), __uint_as_float(r[g * 4 + 3]));
-                        if (p.accumulate) {
-                            const float4 o = *reinterpret_cast<const float4*>(out + col);
-                            v.x += o.x;
-                            v.y += o.y;
-                            v.z += o.z;
-                            v.w += o.w;
-                        }
-                        *reinterpret_cast<float4*>(out + col) = v;
                     }
                 } else {
                     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -855,7 +871,8 @@ EncodeTiledFn encode_fn(std::string* err) {
 // bytes for dims 1.., box innermost first.
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box, std::string* err,
-              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn fn = encode_fn(err);
     if (!fn) return false;
     cuuint64_t d[3], s[2];
@@ -865,7 +882,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
         b[i] = box[i];
     }
     for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, s, b, e,
+    CUresult r = fn(m, dtype, rank, const_cast<void*>(ptr), d, s, b, e,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -1009,6 +1026,28 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         p.row_split2 = static_cast<int>(a.mode == GEMM_TN && a.out2 && a.out3 ? a.row_split2 : a.M);
         p.out3 = a.out3;
         p.ldo3 = a.ldo3;
+        if (a.mode == GEMM_TN) {
+            // fp32 output boxes of 32 x 32, 128-byte swizzle: out rows [0,
+            // row_split), out2 rows [row_split, row_split2), out3 the rest.
+            if ((p.row_split < a.M && p.row_split % EPI_BOX) || (p.row_split2 < a.M && p.row_split2 % EPI_BOX)) {
+                if (err) *err = "TN row splits must be multiples of 32";
+                return TP_ERR_INVALID_ARG;
+            }
+            const uint32_t box_o[2] = {EPI_BOX, EPI_BOX};
+            void* outs[3] = {a.out, a.out2, a.out3};
+            const int64_t lds[3] = {a.ldo, a.ldo2, a.ldo3};
+            const int64_t r0[3] = {0, p.row_split, p.row_split2};
+            const int64_t r1[3] = {p.row_split, p.row_split2, a.M};
+            for (int o = 0; o < 3; ++o) {
+                p.mapO[o] = p.mapO[0];
+                if (r1[o] <= r0[o] || !outs[o]) continue;
+                const uint64_t dO[2] = {(uint64_t)a.N, (uint64_t)(r1[o] - r0[o])};
+                const uint64_t sO[1] = {(uint64_t)lds[o] * 4};
+                if (!make_map(&p.mapO[o], outs[o], 2, dO, sO, box_o, err, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+                    return TP_ERR_CUDA;
+            }
+        }
         if (a.mode == GEMM_BWD_ACT) {
             // Output boxes of 32 x 32 bf16, 64-byte swizzle: dU = out[:, :N],
             // dG = out[:, n_half : n_half + N] (SwiGLU), H = out2.
