@@ -73,6 +73,8 @@ def lib():
             "tpo_sp_reduce_scatter": (C.c_int, [_I64] * 4 + [_D, _D]),
             "tpo_layer_sp": (C.c_int, [_I64] * 8 + [C.c_double] + [_D] * 9),
             "tpo_mlp_backward": (C.c_int, [C.c_int] + [_I64] * 3 + [_D] * 10),
+            "tpo_rmsnorm_backward": (C.c_int, [_I64, _I64, C.c_double, _D, _D, _D]),
+            "tpo_layer_backward": (C.c_int, [_I64] * 7 + [C.c_double] + [_D] * 17),
             "tpo_attention_core_backward": (C.c_int, [_I64] * 5 + [_D, _I64, _D, _D, _I64, _D, _I64, _D, _D, _D]),
             "tpo_attention_backward": (C.c_int, [_I64] * 6 + [_D] * 11),
             "tpo_attention_backward_sharded": (C.c_int, [_I64] * 7 + [_D] * 12),
@@ -469,3 +471,47 @@ def attention_backward_composed(batch: int, seq: int, a: int, k: int, X, Wq, Wk,
     dQ, dK, dV = attention_core_backward(batch, seq, a, k, Q, K, V, dO)
     dX = dQ @ Wq + dK @ Wk + dV @ Wv
     return dX, dQ.T @ X, dK.T @ X, dV.T @ X, dWo
+
+
+def rmsnorm_backward(x, g, eps: float = 1e-5) -> np.ndarray:
+    """dL/dx of the unit-gain RMSNorm at x for the upstream g."""
+    x, g = _d(x), _d(g)
+    out = np.zeros_like(x)
+    _check("tpo_rmsnorm_backward", lib().tpo_rmsnorm_backward(x.shape[0], x.shape[1], eps, _p(x), _p(g), _p(out)))
+    return out
+
+
+def layer_backward(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo, W1, W3, W2, dY,
+                   eps: float = 1e-5):
+    """(dX, dWq, dWk, dWv, dWo, dW1, dW3, dW2) of the pre-norm SwiGLU layer."""
+    X, Wq, Wk, Wv, Wo, W1, W3, W2, dY = map(_d, (X, Wq, Wk, Wv, Wo, W1, W3, W2, dY))
+    M, h = X.shape
+    f = W1.shape[0]
+    outs = [np.empty((M, h))] + [np.empty_like(w) for w in (Wq, Wk, Wv, Wo, W1, W3, W2)]
+    _check("tpo_layer_backward", lib().tpo_layer_backward(
+        batch, seq, h, a, k, d, f, eps, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(W1), _p(W3), _p(W2),
+        _p(dY), *(_p(o) for o in outs)))
+    return tuple(outs)
+
+
+def layer_backward_composed(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo, W1, W3,
+                            W2, dY, eps: float = 1e-5):
+    """tpo_layer_backward's steps for large sizes: numpy matmuls for the
+    projections and the MLP, the C oracle for the attention core and the norms."""
+    X, Wq, Wk, Wv, Wo, W1, W3, W2, dY = map(_d, (X, Wq, Wk, Wv, Wo, W1, W3, W2, dY))
+    xn1 = rmsnorm(X, eps)
+    Q, K, V = xn1 @ Wq.T, xn1 @ Wk.T, xn1 @ Wv.T
+    h1 = X + attention_core(batch, seq, a, k, d, Q, K, V) @ Wo.T
+    xn2 = rmsnorm(h1, eps)
+    U, G = xn2 @ W1.T, xn2 @ W3.T
+    s = 1.0 / (1.0 + np.exp(-U))
+    H = U * s * G
+    dH = dY @ W2
+    dU = dH * G * s * (1.0 + U * (1.0 - s))
+    dG = dH * U * s
+    dxn2 = dU @ W1 + dG @ W3
+    grads_mlp = (dU.T @ xn2, dG.T @ xn2, dY.T @ H)
+    dh1 = dY + rmsnorm_backward(h1, dxn2, eps)
+    dxn1, dWq, dWk, dWv, dWo = attention_backward_composed(batch, seq, a, k, xn1, Wq, Wk, Wv, Wo, dh1)
+    dX = dh1 + rmsnorm_backward(X, dxn1, eps)
+    return (dX, dWq, dWk, dWv, dWo) + grads_mlp

@@ -1090,3 +1090,64 @@ int tpo_attention_backward_sharded(int64_t batch, int64_t seq, int64_t h, int64_
     free(buf);
     return TPO_OK;
 }
+
+/* ---------------------------------------------------------------- layer backward */
+
+/* Backward of the unit-gain RMSNorm y = x r, r = 1 / sqrt(mean_j x_j^2 + eps),
+ * per row, added to out: with g = dL/dy,
+ *   dL/dx_i = r g_i - x_i r^3 (sum_j g_j x_j) / h. */
+int tpo_rmsnorm_backward(int64_t M, int64_t h, double eps, const double* x, const double* g,
+                         double* out) {
+    if (M < 0 || h <= 0) return TPO_ERR_INVALID;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const double* xr = x + m * h;
+        const double* gr = g + m * h;
+        double ss = 0.0, dot = 0.0;
+        for (int64_t j = 0; j < h; ++j) {
+            ss += xr[j] * xr[j];
+            dot += gr[j] * xr[j];
+        }
+        const double r = 1.0 / sqrt(ss / (double)h + eps);
+        for (int64_t j = 0; j < h; ++j) out[m * h + j] += r * gr[j] - xr[j] * r * r * r * dot / (double)h;
+    }
+    return TPO_OK;
+}
+
+/* Backward of the layer of tpo_layer (pre-norm, SwiGLU MLP), given dY:
+ *   forward: xn1 = rms(X), h1 = X + Attn(xn1), xn2 = rms(h1), Y = h1 + MLP(xn2)
+ *   dh1 = dY + rms'(h1)^T (MLP backward of dY at xn2)
+ *   dX  = dh1 + rms'(X)^T (attention backward of dh1 at xn1)
+ * with the weight gradients of both blocks.  The blocks' own backward passes
+ * are the plain (unsharded) definitions, which the t-device forms equal. */
+int tpo_layer_backward(int64_t batch, int64_t seq, int64_t h, int64_t a, int64_t k, int64_t d,
+                       int64_t f, double eps, const double* X, const double* Wq, const double* Wk,
+                       const double* Wv, const double* Wo, const double* W1, const double* W3,
+                       const double* W2, const double* dY, double* dX, double* dWq, double* dWk,
+                       double* dWv, double* dWo, double* dW1, double* dW3, double* dW2) {
+    if (batch < 0 || seq < 0 || h <= 0 || a <= 0 || k <= 0 || d <= 0 || f <= 0 || a % k) return TPO_ERR_INVALID;
+    const int64_t M = batch * seq;
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(6 * M * h + 1));
+    if (!buf) return TPO_ERR_NOMEM;
+    double *xn1 = buf, *h1 = xn1 + M * h, *xn2 = h1 + M * h, *dxn = xn2 + M * h, *dh1 = dxn + M * h;
+    double* at = dh1 + M * h;
+    int rc;
+    tpo_rmsnorm(M, h, eps, X, xn1);
+    rc = tpo_attention(batch, seq, h, a, k, d, xn1, Wq, Wk, Wv, Wo, NULL, at);
+    if (!rc) {
+        for (int64_t e = 0; e < M * h; ++e) h1[e] = X[e] + at[e];
+        tpo_rmsnorm(M, h, eps, h1, xn2);
+        rc = tpo_mlp_backward(TPO_ACT_SWIGLU, M, h, f, xn2, W1, W3, W2, dY, dxn, dW1, dW3, dW2, NULL);
+    }
+    if (!rc) {
+        memcpy(dh1, dY, sizeof(double) * (size_t)(M * h));
+        tpo_rmsnorm_backward(M, h, eps, h1, dxn, dh1);
+        rc = tpo_attention_backward(batch, seq, h, a, k, d, xn1, Wq, Wk, Wv, Wo, dh1, dxn, dWq, dWk, dWv, dWo);
+    }
+    if (!rc) {
+        memcpy(dX, dh1, sizeof(double) * (size_t)(M * h));
+        tpo_rmsnorm_backward(M, h, eps, X, dxn, dX);
+    }
+    free(buf);
+    return rc;
+}

@@ -691,3 +691,40 @@ def test_attention_backward_composed_equals_c_form():
     a2 = oracle.attention_backward_composed(batch, seq, a, k, X, *W, dOut)
     for x, y in zip(a1, a2):
         assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max())
+
+
+def test_rmsnorm_backward_matches_torch_autograd():
+    g = torch.Generator().manual_seed(91)
+    x = torch.randn(5, 12, generator=g, dtype=torch.float64).requires_grad_(True)
+    up = torch.randn(5, 12, generator=g, dtype=torch.float64)
+    y = x * torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + 1e-5)
+    y.backward(up)
+    got = oracle.rmsnorm_backward(x.detach(), up)
+    assert np.abs(got - x.grad.numpy()).max() < 1e-13
+
+
+def _torch_layer(batch, seq, a, k, X, Wq, Wk, Wv, Wo, W1, W3, W2, eps=1e-5):
+    rms = lambda v: v * torch.rsqrt(v.pow(2).mean(-1, keepdim=True) + eps)
+    xn1 = rms(X)
+    h1 = X + _torch_gqa_attention(batch, seq, a, k, xn1 @ Wq.T, xn1 @ Wk.T, xn1 @ Wv.T) @ Wo.T
+    xn2 = rms(h1)
+    return h1 + (F.silu(xn2 @ W1.T) * (xn2 @ W3.T)) @ W2.T
+
+
+def test_layer_backward_matches_torch_autograd():
+    g = torch.Generator().manual_seed(92)
+    batch, seq, h, a, k, d, f = 2, 5, 8, 4, 2, 2, 16
+    M = batch * seq
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).requires_grad_(True)
+    shapes = [(a * d, h), (k * d, h), (k * d, h), (h, a * d), (f, h), (f, h), (h, f)]
+    W = [(torch.randn(*s, generator=g, dtype=torch.float64) * 0.4).requires_grad_(True) for s in shapes]
+    dY = torch.randn(M, h, generator=g, dtype=torch.float64)
+    _torch_layer(batch, seq, a, k, X, *W).backward(dY)
+    got = oracle.layer_backward(batch, seq, a, k, d, X.detach(), *(w.detach() for w in W), dY)
+    want = [X.grad] + [w.grad for w in W]
+    names = ["dX", "dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"]
+    for n, x, ref in zip(names, got, want):
+        assert np.abs(x - ref.numpy()).max() < 1e-11 * max(1.0, ref.abs().max().item()), n
+    comp = oracle.layer_backward_composed(batch, seq, a, k, d, X.detach(), *(w.detach() for w in W), dY)
+    for n, x, y in zip(names, got, comp):
+        assert np.abs(x - y).max() < 1e-11 * max(1.0, np.abs(x).max()), n + " (composed)"
