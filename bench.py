@@ -462,6 +462,23 @@ def run_case(args):
                                          QKVs, Os, LSEs, dX, dWq, dWk, dWv, dWo, False, wsb, nws,
                                          stream)
         work = sum(v for _, v in attn_backward_kernel_flops(s))
+    elif args.case == "layer_backward":
+        # The layer's training step minus its output: tp_layer_backward
+        # recomputes the forward (state kept) and runs the whole backward.
+        inp = synth.workload_inputs(s)
+        wd = {kk: vv.cuda() for kk, vv in inp.items() if kk != "X"}
+        Xd, dY = inp["X"].cuda(), bf((M, h), 1.0, 4014)
+        plan = tp.Plan(tp.make_config(tokens=M, hidden=h, ffn=f, n_heads=a, n_kv_heads=k, head_dim=d,
+                                      tp_degree=t, act=s.act, batch=s.batch, seq=s.seq))
+        nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_LAYER_BACKWARD)
+        wsb = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        dX = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
+        grads = {"d" + kk: torch.empty(tuple(vv.shape), dtype=torch.float32, device="cuda")
+                 for kk, vv in wd.items()}
+        fn = lambda: tp.tp_layer_backward(plan, Xd, wd, dY, dX, grads, False, wsb, nws, stream)
+        # forward (recomputed) + both blocks' backward passes
+        work = (layer_flops(s) + sum(v for _, v in mlp_backward_kernel_flops(M, h, f))
+                + sum(v for _, v in attn_backward_kernel_flops(s)))
     elif args.case == "attn":
         kvn = max(k // t, 1)
         W = (a // t + 2 * kvn) * d
@@ -710,7 +727,7 @@ def main(argv=None):
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
                              "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer",
                              "partials_layer", "mlp_backward", "mlp_backward_recompute",
-                             "attn_backward", "attn_backward_recompute"],
+                             "attn_backward", "attn_backward_recompute", "layer_backward"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="mlp_backward cases: tokens (0 = the layer's 8192), for small captures")

@@ -86,7 +86,14 @@ enum { TP_REDUCE_FUSED = 0, TP_REDUCE_PARTIALS = 1 };
 enum { TP_F32 = 0, TP_BF16 = 1 };
 
 /* Operations whose workspace size tp_plan_workspace_bytes reports. */
-enum { TP_OP_MLP = 0, TP_OP_ATTN = 1, TP_OP_LAYER = 2, TP_OP_MLP_BACKWARD = 3, TP_OP_ATTN_BACKWARD = 4 };
+enum {
+    TP_OP_MLP = 0,
+    TP_OP_ATTN = 1,
+    TP_OP_LAYER = 2,
+    TP_OP_MLP_BACKWARD = 3,
+    TP_OP_ATTN_BACKWARD = 4,
+    TP_OP_LAYER_BACKWARD = 5
+};
 
 /* Index tables tp_plan_shard_table exports (int32, row-major):
  *  FFN_SHARDS  [t][2]: first column of shard i in the ffn dimension, width f/t
@@ -131,6 +138,12 @@ typedef struct {
 typedef struct {
     const tp_bf16 *Wq, *Wk, *Wv, *Wo, *W1, *W3, *W2;
 } tp_layer_weights;
+
+/* fp32 weight gradients of one layer, shaped as the weights
+ * (dW3 NULL unless the MLP is SwiGLU). */
+typedef struct {
+    float *dWq, *dWk, *dWv, *dWo, *dW1, *dW3, *dW2;
+} tp_layer_grads;
 
 /* ------------------------------------------------------------ plan */
 
@@ -332,6 +345,25 @@ TP_API int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq,
                             const tp_bf16* O, const float* LSE, tp_bf16* dX, float* dWq, float* dWk,
                             float* dWv, float* dWo, int accumulate, void* workspace, size_t ws_bytes,
                             void* stream);
+
+/* Backward of one pre-norm layer (the layer of tp_layer_forward), a whole
+ * training step but the output: the forward is recomputed with what its
+ * backward reads saved in the workspace, then
+ *   MLP block backward at xn2 = RMSNorm(h1) with dZ = dY  ->  dxn2
+ *   dh1 = dY + RMSNorm'(h1)^T dxn2                       (residual + norm)
+ *   attention block backward at xn1 = RMSNorm(X), dOut = dh1  ->  dxn1
+ *   dX  = dh1 + RMSNorm'(X)^T dxn1
+ * where the blocks' backward passes are those of tp_mlp_backward and
+ * tp_attn_backward (g backward identity, f backward the sum of the shards'
+ * partial input gradients) and RMSNorm has unit gain.  X, dY, dX: device
+ * [M][h] bf16 (dX may not alias X or dY); w: the layer's weights; grads: fp32
+ * weight gradients, overwritten or, with accumulate != 0, added to.
+ * Workspace: tp_plan_workspace_bytes(TP_OP_LAYER_BACKWARD).  Needs an
+ * attention head_dim of 128, no sequence parallelism, hidden <= 8192, and
+ * for SwiGLU f % 64 == 0 (TP_ERR_UNSUPPORTED otherwise). */
+TP_API int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, const tp_bf16* dY,
+                             tp_bf16* dX, const tp_layer_grads* grads, int accumulate, void* workspace,
+                             size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------ packed projections */
 

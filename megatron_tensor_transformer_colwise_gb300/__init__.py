@@ -23,6 +23,7 @@ __all__ = [
     "TP_ACT_GELU_ERF", "TP_ACT_GELU_TANH", "TP_ACT_SWIGLU", "TP_ACT_NONE",
     "TP_REDUCE_FUSED", "TP_REDUCE_PARTIALS", "TP_F32", "TP_BF16",
     "TP_OP_MLP", "TP_OP_ATTN", "TP_OP_LAYER", "TP_OP_MLP_BACKWARD", "TP_OP_ATTN_BACKWARD",
+    "TP_OP_LAYER_BACKWARD", "TPLayerGrads",
     "TP_TABLE_FFN_SHARDS", "TP_TABLE_Q_HEAD_SHARD", "TP_TABLE_Q_HEAD_KV",
     "TP_TABLE_SHARD_KV", "TP_TABLE_QKV_COLUMNS",
     "tp_plan_create", "tp_plan_destroy", "tp_config_check", "tp_config_shard_table",
@@ -33,7 +34,7 @@ __all__ = [
     "tp_packed_shard_table", "tp_packed_colwise_forward", "tp_vocab_embedding_forward",
     "tp_vocab_logits_forward", "tp_vocab_parallel_cross_entropy", "tp_sp_all_gather",
     "tp_sp_reduce_scatter", "tp_mlp_forward_train", "tp_mlp_backward", "tp_plan_attn_saved_bytes",
-    "tp_attn_forward_train", "tp_attn_backward", "EXPORTED",
+    "tp_attn_forward_train", "tp_attn_backward", "tp_layer_backward", "EXPORTED",
 ]
 
 TP_OK = 0
@@ -47,7 +48,8 @@ TP_ERR_DEVICE_TIMEOUT = 6
 TP_ACT_GELU_ERF, TP_ACT_GELU_TANH, TP_ACT_SWIGLU, TP_ACT_NONE = 0, 1, 2, 3
 TP_REDUCE_FUSED, TP_REDUCE_PARTIALS = 0, 1
 TP_F32, TP_BF16 = 0, 1
-TP_OP_MLP, TP_OP_ATTN, TP_OP_LAYER, TP_OP_MLP_BACKWARD, TP_OP_ATTN_BACKWARD = 0, 1, 2, 3, 4
+(TP_OP_MLP, TP_OP_ATTN, TP_OP_LAYER, TP_OP_MLP_BACKWARD, TP_OP_ATTN_BACKWARD,
+ TP_OP_LAYER_BACKWARD) = range(6)
 (TP_TABLE_FFN_SHARDS, TP_TABLE_Q_HEAD_SHARD, TP_TABLE_Q_HEAD_KV, TP_TABLE_SHARD_KV,
  TP_TABLE_QKV_COLUMNS) = range(5)
 
@@ -80,6 +82,10 @@ class TPLayerWeights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")]
 
 
+class TPLayerGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2")]
+
+
 _VP = C.c_void_p
 _SIGS = {
     "tp_plan_create": [C.POINTER(TPConfig), C.POINTER(C.c_void_p)],
@@ -101,6 +107,7 @@ _SIGS = {
     "tp_plan_attn_saved_bytes": [_VP] + [C.POINTER(C.c_size_t)] * 3,
     "tp_attn_forward_train": [_VP] * 13,
     "tp_attn_backward": [_VP] * 15 + [C.c_int, _VP, C.c_size_t, _VP],
+    "tp_layer_backward": [_VP] * 6 + [C.c_int, _VP, C.c_size_t, _VP],
     "tp_qkv_forward": [_VP] * 7,
     "tp_attn_core_forward": [_VP] * 4,
     "tp_attn_forward": [_VP] * 10 + [C.c_size_t, _VP],
@@ -343,6 +350,16 @@ def tp_layer_forward(plan: Plan, X, weights: dict, Y, workspace, ws_bytes: int,
     w = TPLayerWeights(*[_p(weights.get(k)) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")])
     _call("tp_layer_forward", plan.handle, _p(X), C.byref(w), _p(Y), _p(workspace), ws_bytes,
           _s(stream))
+
+
+def tp_layer_backward(plan: Plan, X, weights: dict, dY, dX, grads: dict, accumulate: bool, workspace,
+                      ws_bytes: int, stream=None) -> None:
+    """Backward of the pre-norm layer (forward recomputed): dX and the fp32
+    weight gradients in ``grads`` (keys dWq, dWk, dWv, dWo, dW1, dW3, dW2)."""
+    w = TPLayerWeights(*[_p(weights.get(k)) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")])
+    g = TPLayerGrads(*[_p(grads.get(k)) for k in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2")])
+    _call("tp_layer_backward", plan.handle, _p(X), C.byref(w), _p(dY), _p(dX), C.byref(g),
+          1 if accumulate else 0, _p(workspace), ws_bytes, _s(stream))
 
 
 def layer_weights(weights: dict) -> TPLayerWeights:

@@ -17,6 +17,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <algorithm>
 #include <string>
 
 #include "tp.h"
@@ -106,9 +107,17 @@ struct Layout {
     size_t bqkv = 0;     // attention backward, recomputation: QKV [M][t qkv_w] bf16
     size_t bo = 0;       // attention backward, recomputation: O [M][a d] bf16
     size_t blse = 0;     // attention backward, recomputation: LSE [a][batch][seq_pad] fp32
+    // Layer backward: the recomputed forward's saved state, the gradient
+    // stream, and one region the block backward passes use in turn.
+    size_t lxn1 = 0, lh1 = 0, lxn2 = 0, ldxn = 0, ldh1 = 0;  // [M][h] bf16 each
+    size_t lqkv = 0, lo = 0, llse = 0;                       // attention state
+    size_t lug = 0;                                          // MLP pre-activations
+    size_t lshared = 0;  // max(MLP backward, attention backward workspaces, [M][f] bf16)
 };
 
 int64_t seq_pad_of(const tp_plan_s* p) { return (p->cfg.seq + 63) / 64 * 64; }
+
+size_t layout_total(const Layout& L);
 
 size_t partial_elem_bytes(const tp_plan_s* p) { return p->cfg.partial_dtype == TP_BF16 ? 2 : 4; }
 
@@ -138,6 +147,17 @@ Layout layout_of(const tp_plan_s* p, int op) {
         L.bo = align_up(M * p->a * p->d * 2);
         L.blse = align_up(stat);
     }
+    if (op == TP_OP_LAYER_BACKWARD && p->has_attn && p->has_mlp) {
+        const size_t act = align_up(M * p->h * 2);
+        L.lxn1 = L.lh1 = L.lxn2 = L.ldxn = L.ldh1 = act;
+        L.lqkv = align_up(M * p->t * p->qkv_w * 2);
+        L.lo = align_up(M * p->a * p->d * 2);
+        L.llse = align_up(static_cast<size_t>(p->a) * p->cfg.batch * seq_pad_of(p) * 4);
+        L.lug = align_up(M * (p->cfg.act == TP_ACT_SWIGLU ? 2 : 1) * static_cast<size_t>(p->f) * 2);
+        const size_t mb = layout_total(layout_of(p, TP_OP_MLP_BACKWARD));
+        const size_t ab = layout_total(layout_of(p, TP_OP_ATTN_BACKWARD));
+        L.lshared = std::max(std::max(mb, ab), align_up(M * p->f * 2));
+    }
     if (op == TP_OP_LAYER) {
         L.h1 = align_up(M * p->h * 2);
         if (p->cfg.reduce_mode == TP_REDUCE_PARTIALS) {
@@ -153,7 +173,8 @@ Layout layout_of(const tp_plan_s* p, int op) {
 
 size_t layout_total(const Layout& L) {
     return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact + L.bdo +
-           L.bdstat + L.bdq + L.bdqkv + L.bqkv + L.bo + L.blse;
+           L.bdstat + L.bdq + L.bdqkv + L.bqkv + L.bo + L.blse + L.lxn1 + L.lh1 + L.lxn2 + L.ldxn + L.ldh1 +
+           L.lqkv + L.lo + L.llse + L.lug + L.lshared;
 }
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
@@ -443,7 +464,7 @@ int tp_plan_destroy(tp_plan_t plan) {
 
 int tp_plan_workspace_bytes(tp_plan_t plan, int op, size_t* bytes) {
     if (!plan || !bytes) return fail(TP_ERR_INVALID_ARG, "plan and bytes must be non-NULL");
-    if (op < TP_OP_MLP || op > TP_OP_ATTN_BACKWARD) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
+    if (op < TP_OP_MLP || op > TP_OP_LAYER_BACKWARD) return fail(TP_ERR_INVALID_ARG, "unknown op %d", op);
     *bytes = layout_total(layout_of(plan, op));
     return TP_OK;
 }
@@ -947,6 +968,64 @@ int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const 
         if ((rc = run(tpi::gemm_launch(g, s, &err), err))) return rc;
     }
     return TP_OK;
+}
+
+int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, const tp_bf16* dY,
+                      tp_bf16* dX, const tp_layer_grads* grads, int accumulate, void* workspace,
+                      size_t ws_bytes, void* stream) {
+    if (!plan || !w || !grads) return fail(TP_ERR_INVALID_ARG, "plan, weights and grads must be non-NULL");
+    if (!plan->has_attn || !plan->has_mlp)
+        return fail(TP_ERR_INVALID_ARG, "a layer needs both attention (n_heads > 0) and an MLP (ffn > 0)");
+    if (plan->cfg.sequence_parallel)
+        return fail(TP_ERR_UNSUPPORTED, "the layer backward does not support sequence parallelism");
+    if (plan->h > 8192) return fail(TP_ERR_UNSUPPORTED, "layer RMSNorm supports hidden <= 8192");
+    int rc;
+    if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(dY, "dY")) ||
+        (rc = need_ptr(dX, "dX")))
+        return rc;
+    if (dX == X || dX == dY) return fail(TP_ERR_INVALID_ARG, "dX may not alias X or dY");
+    if ((rc = check_ws(plan, TP_OP_LAYER_BACKWARD, workspace, ws_bytes))) return rc;
+    const Layout L = layout_of(plan, TP_OP_LAYER_BACKWARD);
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        void* r = region(workspace, off);
+        off += n;
+        return r;
+    };
+    void* xn1 = take(L.lxn1);
+    void* h1 = take(L.lh1);
+    void* xn2 = take(L.lxn2);
+    void* dxn = take(L.ldxn);
+    void* dh1 = take(L.ldh1);
+    void* qkv = take(L.lqkv);
+    void* o = take(L.lo);
+    float* lse = reinterpret_cast<float*>(take(L.llse));
+    void* ug = take(L.lug);
+    void* shared = take(L.lshared);
+    cudaStream_t s = as_stream(stream);
+    const float eps = plan->cfg.rms_eps;
+    const int H = static_cast<int>(plan->h);
+    std::string err;
+    // Forward, keeping what the backward reads.
+    if ((rc = run(tpi::rmsnorm_launch(X, plan->M, H, eps, xn1, s, &err), err))) return rc;
+    if ((rc = do_qkv(plan, xn1, w->Wq, w->Wk, w->Wv, qkv, s))) return rc;
+    if ((rc = do_attn_core(plan, qkv, o, s, lse))) return rc;
+    if ((rc = do_rowwise(plan, o, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s))) return rc;
+    if ((rc = run(tpi::rmsnorm_launch(h1, plan->M, H, eps, xn2, s, &err), err))) return rc;
+    if ((rc = do_colwise(plan, xn2, w->W1, w->W3, shared, s, nullptr, ug))) return rc;
+    // MLP block, then the norm and the residual: dh1 = dY + RMSNorm'(h1)^T dxn2.
+    if ((rc = tp_mlp_backward(plan, static_cast<const tp_bf16*>(xn2), w->W1, w->W3, w->W2, dY,
+                              static_cast<const tp_bf16*>(ug), static_cast<tp_bf16*>(dxn), grads->dW1,
+                              grads->dW3, grads->dW2, nullptr, accumulate, shared, L.lshared, stream)))
+        return rc;
+    if ((rc = run(tpi::rmsnorm_bwd_launch(h1, dxn, dY, plan->M, H, eps, dh1, s, &err), err))) return rc;
+    // Attention block, then dX = dh1 + RMSNorm'(X)^T dxn1.
+    if ((rc = tp_attn_backward(plan, static_cast<const tp_bf16*>(xn1), w->Wq, w->Wk, w->Wv, w->Wo,
+                               static_cast<const tp_bf16*>(dh1), static_cast<const tp_bf16*>(qkv),
+                               static_cast<const tp_bf16*>(o), lse, static_cast<tp_bf16*>(dxn), grads->dWq,
+                               grads->dWk, grads->dWv, grads->dWo, accumulate, shared, L.lshared, stream)))
+        return rc;
+    return run(tpi::rmsnorm_bwd_launch(X, dxn, dh1, plan->M, H, eps, dX, s, &err), err);
 }
 
 int tp_layer_forward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, tp_bf16* Y,

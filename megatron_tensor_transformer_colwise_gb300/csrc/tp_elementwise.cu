@@ -290,6 +290,84 @@ int check_launch(const char* what, std::string* err) {
     return TP_OK;
 }
 
+// Backward of the unit-gain RMSNorm, plus a residual gradient, per row:
+//   out = res + r g - x r^3 (sum_j g_j x_j) / h,  r = 1 / sqrt(mean_j x_j^2 + eps)
+// (bf16 in and out, fp32 arithmetic).  One CTA of RB_THREADS per row; each
+// thread keeps VPT 8-element vectors of x and g in registers.
+constexpr int RB_THREADS = 128;
+
+template <int VPT>
+__global__ void __launch_bounds__(RB_THREADS) rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                const __nv_bfloat16* __restrict__ g,
+                                                                const __nv_bfloat16* __restrict__ res,
+                                                                int h, float eps,
+                                                                __nv_bfloat16* __restrict__ out) {
+    __shared__ float red[2][RB_THREADS / 32];
+    const long long row = blockIdx.x;
+    const int nv = h / 8;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * h);
+    const uint4* gr = reinterpret_cast<const uint4*>(g + row * h);
+    float xv[VPT][8], gv[VPT][8];
+    float ss = 0.0f, dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * RB_THREADS;
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (v < nv) {
+            a = xr[v];
+            b = gr[v];
+        }
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = unpack_bf16x2(aw[e]), fb = unpack_bf16x2(bw[e]);
+            xv[i][2 * e] = fa.x;
+            xv[i][2 * e + 1] = fa.y;
+            gv[i][2 * e] = fb.x;
+            gv[i][2 * e + 1] = fb.y;
+            ss = fmaf(fa.x, fa.x, fmaf(fa.y, fa.y, ss));
+            dot = fmaf(fb.x, fa.x, fmaf(fb.y, fa.y, dot));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = ss;
+        red[1][threadIdx.x >> 5] = dot;
+    }
+    __syncthreads();
+    ss = 0.0f;
+    dot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < RB_THREADS / 32; ++w) {
+        ss += red[0][w];
+        dot += red[1][w];
+    }
+    const float inv_h = 1.0f / static_cast<float>(h);
+    const float r = rsqrtf(ss * inv_h + eps);
+    const float coef = r * r * r * dot * inv_h;
+    const uint4* rr = reinterpret_cast<const uint4*>(res + row * h);
+    uint4* orow = reinterpret_cast<uint4*>(out + row * h);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * RB_THREADS;
+        if (v >= nv) continue;
+        const uint4 c = rr[v];
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fc = unpack_bf16x2(cw[e]);
+            w[e] = pack_bf16x2(fc.x + r * gv[i][2 * e] - xv[i][2 * e] * coef,
+                               fc.y + r * gv[i][2 * e + 1] - xv[i][2 * e + 1] * coef);
+        }
+        orow[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // Column sums of a bf16 [rows][h] matrix into fp32 (the bias gradient
 // db = sum over tokens of dZ), deterministic: block (CS_X, CS_Y) owns
 // CS_X * 8 columns over all rows; thread (x, y) adds rows y, y + CS_Y, ...
@@ -441,6 +519,26 @@ int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int 
         reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
         reinterpret_cast<__nv_bfloat16*>(full));
     return check_launch("all-gather kernel", err);
+}
+
+int rmsnorm_bwd_launch(const void* x, const void* g, const void* res, int64_t rows, int h, float eps,
+                       void* out, cudaStream_t stream, std::string* err) {
+    if (rows == 0) return TP_OK;
+    const int nv = h / 8;
+    const __nv_bfloat16* X = reinterpret_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* G = reinterpret_cast<const __nv_bfloat16*>(g);
+    const __nv_bfloat16* R = reinterpret_cast<const __nv_bfloat16*>(res);
+    __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(out);
+    const unsigned grid = static_cast<unsigned>(rows);
+    if (nv <= RB_THREADS) rmsnorm_bwd_kernel<1><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
+    else if (nv <= 2 * RB_THREADS) rmsnorm_bwd_kernel<2><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
+    else if (nv <= 4 * RB_THREADS) rmsnorm_bwd_kernel<4><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
+    else if (nv <= 8 * RB_THREADS) rmsnorm_bwd_kernel<8><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
+    else {
+        if (err) *err = "RMSNorm backward supports hidden <= 8192";
+        return TP_ERR_UNSUPPORTED;
+    }
+    return check_launch("RMSNorm backward kernel", err);
 }
 
 int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate,

@@ -169,6 +169,10 @@ int vocab_embedding_launch(const int32_t* ids, int64_t M, const void* E, int64_t
 int vocab_ce_launch(const void* logits, int64_t M, int64_t v, int t, const int32_t* labels,
                     float* stats, float* loss, cudaStream_t stream, std::string* err);
 
+// out = res + RMSNorm'(x)^T g per row (unit gain; bf16 [rows][h], h % 8 == 0,
+// h <= 8192); out may alias res.
+int rmsnorm_bwd_launch(const void* x, const void* g, const void* res, int64_t rows, int h, float eps,
+                       void* out, cudaStream_t stream, std::string* err);
 // out[j] (+)= sum_r x[r][j] for a bf16 [rows][h] x (h % 8 == 0), fp32 out.
 int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate,
                   cudaStream_t stream, std::string* err);
