@@ -18,13 +18,17 @@
 //               K one block ahead) from the shard-blocked QKV buffer.
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 64, fp32, two
 //               TMEM buffers so S of block j+1 is computed while the softmax
-//               works on block j), then O += P V (V used as an MN-major
-//               operand straight from its [key][d] layout).
+//               works on block j), then O += P V with P read from TMEM
+//               (tcgen05.mma with the A operand in tensor memory) and V used
+//               as an MN-major operand straight from its [key][d] layout.
 //   warps 2..5  one query row per thread (TMEM lane = row): read the S row,
-//               apply the causal mask, online softmax with exp2, write P
-//               (bf16) to 128-byte-swizzled shared memory for the PV MMA,
+//               apply the causal mask, online softmax with exp2, write P as
+//               bf16 over the first half of the same S buffer (tcgen05.st),
 //               rescale the O row in TMEM when its reference maximum moves,
 //               and finally write O / l as bf16.
+// A buffer is reused for S of block j+2 after the PV of block j, which reads
+// its P, in the tensor core's issue order; the softmax warps wait for that
+// PV to complete only when they rescale O in place.
 // The reference maximum of a row only moves when the block maximum exceeds
 // it by more than 2^8 (in the exp2 domain), so most blocks need no O
 // rescale; P then stays below 256, well inside bf16 and fp32 range.
@@ -47,19 +51,17 @@ constexpr int KB = 64;   // keys per block (UMMA N of S, UMMA K of PV)
 constexpr int NTHREADS = 192;
 constexpr int QBOX = QB * 128;  // TMA box of Q: 128 rows x 64 bf16 (16 KB)
 constexpr int KBOX = KB * 128;  // TMA box of K or V: 64 rows x 64 bf16 (8 KB)
-constexpr int P_BYTES = QB * KB * 2;       // 16 KB: one 128-byte-swizzle column
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 of the allowed growth of P
 
 enum {
     B_Q_FULL = 0,
-    B_K_FULL = 1,   // x2 (K ring)
-    B_K_EMPTY = 3,  // x2
-    B_V_FULL = 5,   // x2 (V ring)
-    B_V_EMPTY = 7,  // x2
-    B_S_FULL = 9,   // x2 (S buffers in TMEM)
-    B_S_EMPTY = 11, // x2
+    B_K_FULL = 1,    // x2 (K ring)
+    B_K_EMPTY = 3,   // x2
+    B_V_FULL = 5,    // x2 (V ring)
+    B_V_EMPTY = 7,   // x2
+    B_S_FULL = 9,    // x2 (S / P buffers in TMEM)
+    B_PV_DONE = 11,  // x2: the PV MMA that read P from buffer i has completed
     B_P_FULL = 13,
-    B_P_EMPTY = 14,
     B_O_FULL = 15,
     B_DRAIN = 16,
     NUM_BARS = 17
@@ -70,12 +72,10 @@ enum {
 constexpr int TWO_CTA_SMEM = 115712;
 
 // Shared memory of one CTA (two CTAs share an SM):
-//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | P [128][64] | barriers
-// At d = 128 the data fills 114,840 of the 115,712 bytes two CTAs may each
-// use, leaving 872 bytes to align the data to 1024 bytes; the kernel checks
-// at run time that its layout fits the allocation (it does when the dynamic
-// shared-memory base is 1024-byte aligned) and otherwise stops with an
-// error flag, touching nothing.
+//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | barriers
+// (P lives in TMEM, over the first half of its S buffer).  The kernel checks
+// at run time that its 1024-aligned layout fits the allocation and
+// otherwise stops with an error flag, touching nothing.
 template <int D>
 struct Layout {
     static constexpr int QT = QB * D * 2;
@@ -83,8 +83,7 @@ struct Layout {
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = QT;
     static constexpr int V_OFF = K_OFF + 2 * KT;
-    static constexpr int P_OFF = V_OFF + 2 * KT;
-    static constexpr int BAR_OFF = P_OFF + P_BYTES;
+    static constexpr int BAR_OFF = V_OFF + 2 * KT;
     static constexpr int DATA = BAR_OFF + 8 * NUM_BARS + 16;
     static constexpr int SMEM = DATA + 1024 <= TWO_CTA_SMEM ? DATA + 1024 : TWO_CTA_SMEM;
     static constexpr int TMEM_COLS = 2 * KB + D <= 256 ? 256 : 512;  // S0 | S1 | O
@@ -127,8 +126,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + L::Q_OFF, sK = base + L::K_OFF, sV = base + L::V_OFF,
-                   sP = base + L::P_OFF;
+    const uint32_t sQ = base + L::Q_OFF, sK = base + L::K_OFF, sV = base + L::V_OFF;
     const uint32_t bar0 = base + L::BAR_OFF;
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::BAR_OFF + 8 * NUM_BARS);
@@ -162,12 +160,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_S_EMPTY + s), 4);
+            mbar_init(bar(B_PV_DONE + s), 1);
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         mbar_init(bar(B_P_FULL), 4);
-        mbar_init(bar(B_P_EMPTY), 1);
         mbar_init(bar(B_O_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -240,8 +237,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             auto issue_s = [&](int kb) -> bool {
                 const int st = kb & 1;
                 const uint32_t use = static_cast<uint32_t>(kb >> 1);
-                if (!mbar_wait(bar(B_S_EMPTY + st), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
-                    return false;
+                // Buffer st held S and then P of block kb - 2.  Its PV was
+                // issued earlier by this thread, and tcgen05.mma operations
+                // from one thread execute in issue order, so this S cannot
+                // overwrite P before that PV has read it.
                 if (!mbar_wait(bar(B_K_FULL + st), use & 1u, abort_flag, p.status, p.timeout_ns))
                     return false;
                 tc_fence_after();
@@ -267,14 +266,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                     break;
                 }
                 tc_fence_after();
+                // P of block kb: bf16 in the first KB/2 columns of S buffer
+                // kb & 1, 16 keys (8 columns) per UMMA.
 #pragma unroll
                 for (int ks = 0; ks < KB / 16; ++ks) {
-                    umma_bf16(tmem + 2 * KB, sdesc_sw128(sP + ks * 32),
-                              sdesc_sw128_mn(sV + vst * L::KT + ks * 16 * 128, KBOX, 1024), idesc_o,
-                              (kb > 0 || ks > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + 2 * KB, tmem + (kb & 1) * KB + ks * 8,
+                                 sdesc_sw128_mn(sV + vst * L::KT + ks * 16 * 128, KBOX, 1024), idesc_o,
+                                 (kb > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(B_V_EMPTY + vst));
-                umma_commit(bar(B_P_EMPTY));
+                umma_commit(bar(B_PV_DONE + (kb & 1)));
             }
             if (ok) {
                 umma_commit(bar(B_O_FULL));
@@ -306,9 +307,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             for (int c = 0; c < KB / 32; ++c)
                 tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
             tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + st));
 
             const int k0 = kb * KB;
             if (k0 + KB - 1 > q0 || k0 + KB > p.seq) {
@@ -352,15 +350,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l_sum = l_sum * alpha + sum;
 
-            // PV of the previous block must be done: O is stable, P is free.
-            const bool got2 = mbar_wait(bar(B_P_EMPTY), (kb & 1) ^ 1, abort_flag, p.status, p.timeout_ns);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, got2)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
             if (__any_sync(0xffffffffu, rescale)) {
+                // O is rescaled in place: the PV of the previous block must be done.
+                const int pb = kb - 1;
+                const bool got2 = mbar_wait(bar(B_PV_DONE + (pb & 1)), static_cast<uint32_t>(pb >> 1) & 1u,
+                                            abort_flag, p.status, p.timeout_ns);
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, got2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -373,15 +373,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 }
                 tmem_st_wait();
             }
-            // P row r: 64 keys = one 128-byte row of a 128-byte-swizzle
-            // column; 16-byte chunk c of the row sits at chunk c ^ (r % 8).
-#pragma unroll
-            for (int c8 = 0; c8 < KB / 8; ++c8) {
-                const uint32_t chunk = static_cast<uint32_t>(c8 ^ (r & 7));
-                st_shared_v4(sP + r * 128 + (chunk << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
-                             pk[4 * c8 + 3]);
-            }
-            fence_proxy_async_smem();
+            // P row r over its S row in TMEM: 64 keys as 32 packed columns.
+            tmem_st32(tmem + lane_off + st * KB, pk);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL));
