@@ -313,6 +313,18 @@ def run_reference(args):
     return 0
 
 
+def run_blocks(args):
+    """The configurations' blocks alone (the ``blocks`` object of the bench
+    line), for profiling."""
+    import torch
+    import megatron_tensor_transformer_colwise_gb300 as tp
+    torch.cuda.set_device(0)
+    peaks, _ = load_peaks()
+    print(json.dumps(time_blocks(tp, torch, torch.device("cuda", 0), torch.cuda.current_stream(), peaks,
+                                 reps=args.steps)))
+    return 0
+
+
 def run_case(args):
     """Single-kernel loops on the layer's shapes, for profiling one kernel:
     w13 (colwise W1/W3 + SwiGLU), qkv (colwise QKV), gelu (colwise GeLU, same
@@ -512,6 +524,60 @@ def run_case(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def time_blocks(tp, torch, device, stream, peaks, reps=20):
+    """The configurations' blocks through the C ABI (FUSED g), each iteration
+    timed alone after an L2 flush (two of the three fit in L2): the GPT-style
+    GeLU MLP, the Llama-3-8B-shaped SwiGLU MLP and the batch-1 attention block.
+    Returns {name: {...}} with TFLOP/s against the measured bf16 burst peak
+    (kernels timed alone)."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > 129 MB L2
+    out = {}
+    for name in ("gpt_mlp", "llama_mlp", "attn"):
+        s = SHAPES[name]
+        inp = {k: v.to(device) for k, v in synth.workload_inputs(s).items()}
+        M, h = s.tokens, s.hidden
+        plan = tp.Plan(tp.make_config(tokens=M, hidden=h, ffn=s.ffn, n_heads=s.heads,
+                                      n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp,
+                                      act=s.act, batch=s.batch, seq=s.seq))
+        Z = torch.empty(M, h, dtype=torch.bfloat16, device=device)
+        if s.ffn:
+            nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_MLP)
+            ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device)
+            W3 = inp.get("W3")
+            fn = lambda: tp.tp_mlp_forward(plan, inp["X"], inp["W1"], W3, inp["W2"], None, None, None,
+                                           Z, ws, nws, stream)
+            flops = gemm_flops(M, (2 if s.act == "swiglu" else 1) * s.ffn, h) + gemm_flops(M, h, s.ffn)
+            desc = f"tp_mlp_forward: {M} tokens, h={h}, ffn={s.ffn}, {s.act}, t={s.tp}, FUSED g"
+        else:
+            nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_ATTN)
+            ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device)
+            fn = lambda: tp.tp_attn_forward(plan, inp["X"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"],
+                                            None, None, Z, ws, nws, stream)
+            a, k, dh = s.heads, s.kv_heads, s.head_dim
+            flops = gemm_flops(M, (a + 2 * k) * dh, h) + attn_core_flops(s) + gemm_flops(M, h, a * dh)
+            desc = (f"tp_attn_forward: batch {s.batch} x seq {s.seq}, h={h}, {a} q / {k} kv heads "
+                    f"d={dh}, t={s.tp}, FUSED g")
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert tp.tp_get_device_status(plan) == tp.TP_OK, tp.tp_last_error()
+        us = sum(e0.elapsed_time(e1) for e0, e1 in evs) / reps * 1e3
+        tfl = flops / (us / 1e6) / 1e12
+        out[name] = {"workload": desc, "us": us, "tflops": tfl, "frac_bf16": tfl / peaks["bf16_tflops"],
+                     "gflop": flops / 1e9, "l2": "L2 flushed before every timed iteration"}
+        del inp, ws, Z
+    del flush
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -636,6 +702,10 @@ def run_ours(args):
                    "l2": "inputs 1.07 GB > 129 MB L2"}
     del P
 
+    # The configurations' blocks on their own (the MLP configurations are
+    # what the sharded-MLP share of the tensor-core peak is quoted on).
+    blocks = time_blocks(tp, torch, device, stream, peaks)
+
     # End to end through the C ABI with host buffers (pinned): every step
     # copies its X in and its Y out.  Copies run on their own streams with
     # double-buffered device X / Y, so step k+1's input copy and step k-1's
@@ -695,6 +765,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (436 MB of weights per step)"},
         "roofline": roofline,
         "reduce": reduce_line,
+        "blocks": blocks,
         "kernels": kernels,
         "e2e": e2e,
         "clocks": clocks,
@@ -727,7 +798,7 @@ def main(argv=None):
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
                              "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer",
                              "partials_layer", "mlp_backward", "mlp_backward_recompute",
-                             "attn_backward", "attn_backward_recompute", "layer_backward"],
+                             "attn_backward", "attn_backward_recompute", "layer_backward", "blocks"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="mlp_backward cases: tokens (0 = the layer's 8192), for small captures")
@@ -738,6 +809,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.case == "blocks":
+        return run_blocks(args)
     if args.case != "layer":
         return run_case(args)
     return run_ours(args)
