@@ -54,7 +54,7 @@ extern "C" {
 #define TP_OK 0
 #define TP_ERR_INVALID_ARG 1    /* null / negative / misaligned / bad enum   */
 #define TP_ERR_NOT_DIVISIBLE 2  /* t does not divide f or a; bad (k, t) pair */
-#define TP_ERR_UNSUPPORTED 3    /* a combination this build does not provide */
+#define TP_ERR_UNSUPPORTED 3    /* a combination the library does not provide */
 #define TP_ERR_WORKSPACE 4      /* workspace missing or smaller than needed   */
 #define TP_ERR_CUDA 5           /* a CUDA runtime / driver call failed        */
 #define TP_ERR_DEVICE_TIMEOUT 6 /* a bounded device-side wait gave up         */

@@ -346,7 +346,7 @@ int derive_plan(const tp_config& cfg, tp_plan_s* p) {
     if (c.reduce_mode == TP_REDUCE_FUSED && c.partial_dtype != TP_F32)
         return fail(TP_ERR_UNSUPPORTED, "bf16 partials only exist in TP_REDUCE_PARTIALS mode");
     const int64_t t = c.tp_degree;
-    // The pages' divisibility rules first, then this build's alignment rules.
+    // The pages' divisibility rules first, then the kernels' alignment rules.
     if (c.ffn > 0 && c.ffn % t)
         return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide ffn %d", c.tp_degree, c.ffn);
     if (c.n_heads > 0) {
