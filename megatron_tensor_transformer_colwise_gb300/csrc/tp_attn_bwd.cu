@@ -19,21 +19,26 @@
 //                         longest (earliest) key blocks first, 14 warps:
 //     warp 0     TMA: K and V of the key block once; then, per step, Q and
 //                dO of 64 queries of one query head of the group plus their
-//                log-sum-exp and D (2-stage ring).
+//                log-sum-exp and D (3-stage ring).
 //     warp 1     TMEM owner and MMA issuer.  Per step:
 //                  S^T  = K Q^T   and dP^T = V dO^T   (128 x 64, TMEM)
 //                then, once the softmax warps have written P^T and dS^T:
-//                  dV  += P^T dO,  dK += dS^T Q      (128 x d, TMEM, over
+//                  dV  += P^T dO  (P^T read from TMEM),
+//                  dK  += dS^T Q                      (128 x d, TMEM, over
 //                                                      the whole group)
 //                  dQ^T = K^T dS^T                    (d x 64, TMEM)
 //                S^T of the next step is issued before the gradients of the
 //                current one, so the tensor core works while the softmax
-//                warps compute.
+//                warps compute; P^T (TMEM) and dS^T (shared memory) are
+//                double-buffered, so step i's stores need only step i-2's
+//                gradient MMAs to be done.
 //     warps 2-9  one key row and 32 of the 64 queries per thread (two warps
 //                per TMEM lane quadrant): P^T = 2^(S^T log2(e)/sqrt(d) - lse)
-//                under the causal mask, dS^T = P^T (dP^T - D); both to
-//                128-byte-swizzled shared memory as bf16; at the end dV and
-//                dK (times 1/sqrt(d)) to global memory as bf16.
+//                under the causal mask, dS^T = P^T (dP^T - D); P^T to TMEM,
+//                dS^T to 128-byte-swizzled shared memory, both bf16; at the
+//                end dV and dK (times 1/sqrt(d)) to global memory as bf16.
+//                No row maximum is needed (the log-sum-exp is given), so the
+//                row splits across warps with no exchange.
 //     warps 10-13 one head dimension per thread: dQ^T from TMEM (times
 //                1/sqrt(d)) to a [64 queries][32 d] fp32 box in shared memory,
 //                added to the fp32 accumulator by one TMA reduce-add per step.
@@ -60,13 +65,17 @@ constexpr int HD = 128;                        // head dimension this kernel han
 constexpr int BKEYS = 128;                     // keys per CTA: UMMA M of S^T, dP^T, dV, dK
 constexpr int BQ = 64;                         // queries per step: UMMA N of S^T, dP^T, dQ^T
 constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
-constexpr int SM_WARPS = 8;                    // softmax-gradient warps: 2 per TMEM lane quadrant
+// Softmax-gradient warps: 2 per TMEM lane quadrant.  (Measured at the layer
+// shape: 8 warps 416 us, 16 warps with 16 columns each 474 us.)
+constexpr int SM_WARPS = 8;
+constexpr int SM_PARTS = SM_WARPS / 4;         // column parts of a key row
+constexpr int CPW = BQ / SM_PARTS;             // query columns per softmax warp
 constexpr int NTHREADS = 32 * (2 + SM_WARPS + 4);
 constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
 constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
 constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
 constexpr int QT_BYTES = 2 * QBOX_BYTES;       // Q or dO tile: 16 KB
-constexpr int PT_BYTES = BKEYS * BQ * 2;       // P^T or dS^T [128 keys][64 queries]: 16 KB
+constexpr int PT_BYTES = BKEYS * BQ * 2;       // dS^T [128 keys][64 queries]: 16 KB
 constexpr int STAT_BYTES = 2 * BQ * 4;         // log-sum-exp and D of 64 queries
 constexpr int DQ_BOX_BYTES = BQ * 32 * 4;      // one dQ warp's [64 queries][32 d] fp32: 8 KB
 
@@ -74,9 +83,8 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KT_BYTES;
 constexpr int OFF_Q = OFF_V + KT_BYTES;
 constexpr int OFF_DO = OFF_Q + NSTAGE * QT_BYTES;
-constexpr int OFF_PT = OFF_DO + NSTAGE * QT_BYTES;
-constexpr int OFF_DST = OFF_PT + PT_BYTES;
-constexpr int OFF_STAT = OFF_DST + PT_BYTES;
+constexpr int OFF_DST = OFF_DO + NSTAGE * QT_BYTES;  // dS^T x2
+constexpr int OFF_STAT = OFF_DST + 2 * PT_BYTES;
 constexpr int OFF_DQ = OFF_STAT + NSTAGE * STAT_BYTES;
 constexpr int OFF_BAR = OFF_DQ + 4 * DQ_BOX_BYTES;
 
@@ -85,11 +93,11 @@ constexpr int B_Q_FULL = 1;                  // x NSTAGE
 constexpr int B_Q_EMPTY = B_Q_FULL + NSTAGE; // x NSTAGE: one MMA commit + the softmax warps
 constexpr int B_S_FULL = B_Q_EMPTY + NSTAGE;
 constexpr int B_S_EMPTY = B_S_FULL + 1;
-constexpr int B_P_FULL = B_S_EMPTY + 1;
-constexpr int B_P_EMPTY = B_P_FULL + 1;
-constexpr int B_DQ_FULL = B_P_EMPTY + 1;   // x2 (dQ^T double-buffered in TMEM)
-constexpr int B_DQ_EMPTY = B_DQ_FULL + 2;  // x2
-constexpr int B_DKV_FULL = B_DQ_EMPTY + 2;
+constexpr int B_P_FULL = B_S_EMPTY + 1;   // x2 (P^T in TMEM and dS^T in shared memory, double-buffered)
+constexpr int B_P_EMPTY = B_P_FULL + 2;   // x2
+constexpr int B_DQ_FULL = B_P_EMPTY + 2;
+constexpr int B_DQ_EMPTY = B_DQ_FULL + 1;
+constexpr int B_DKV_FULL = B_DQ_EMPTY + 1;
 constexpr int B_DRAIN = B_DKV_FULL + 1;
 constexpr int NUM_BARS = B_DRAIN + 1;
 // The data fill all but a few bytes of the 227 KB a CTA may use, leaving no
@@ -100,11 +108,12 @@ constexpr int NUM_BARS = B_DRAIN + 1;
 constexpr int DATA_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
 constexpr int SMEM_BYTES = DATA_BYTES + 128 <= 232448 ? DATA_BYTES + 128 : 232448;
 
-// TMEM columns (512 allocated): S^T, dP^T (64 each), dQ^T x2 (64 each), dV,
-// dK (128 each).
-constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ0 = 384, COL_DQ1 = 448;
+// TMEM columns (512 allocated): S^T, dP^T (64 each), dV, dK (128 each), dQ^T
+// (64), and P^T x2 as bf16 (32 packed columns each: the A operand of dV).
+constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ = 384, COL_PT0 = 448,
+                   COL_PT1 = 480;
 
-static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_PT % 1024 == 0 && OFF_DST % 1024 == 0,
+static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DST % 1024 == 0 && PT_BYTES % 1024 == 0,
               "swizzled tiles must be 1024-byte aligned");
 static_assert(OFF_DQ % 128 == 0, "TMA boxes must be 128-byte aligned");
 static_assert(DATA_BYTES <= 232448, "shared memory");
@@ -151,13 +160,19 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
         : "memory");
 }
 
+// TMEM loads / stores of one warp's columns, by register-array width.
+__device__ __forceinline__ void ld_cols(uint32_t a, uint32_t (&r)[32]) { tmem_ld32(a, r); }
+__device__ __forceinline__ void ld_cols(uint32_t a, uint32_t (&r)[16]) { tmem_ld16(a, r); }
+__device__ __forceinline__ void st_cols(uint32_t a, const uint32_t (&r)[16]) { tmem_st16(a, r); }
+__device__ __forceinline__ void st_cols(uint32_t a, const uint32_t (&r)[8]) { tmem_st8(a, r); }
+
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t sK = base + OFF_K, sV = base + OFF_V, sQ = base + OFF_Q, sDO = base + OFF_DO,
-                   sPT = base + OFF_PT, sDST = base + OFF_DST, sSTAT = base + OFF_STAT;
+                   sDST = base + OFF_DST, sSTAT = base + OFF_STAT;
     const float* stat = reinterpret_cast<const float*>(gbase + OFF_STAT);
     const uint32_t bar0 = base + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -202,12 +217,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         }
         mbar_init(bar(B_S_FULL), 1);
         mbar_init(bar(B_S_EMPTY), SM_WARPS);
-        mbar_init(bar(B_P_FULL), SM_WARPS);
-        mbar_init(bar(B_P_EMPTY), 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_DQ_FULL + s), 1);
-            mbar_init(bar(B_DQ_EMPTY + s), 4);
+            mbar_init(bar(B_P_FULL + s), SM_WARPS);
+            mbar_init(bar(B_P_EMPTY + s), 1);
         }
+        mbar_init(bar(B_DQ_FULL), 1);
+        mbar_init(bar(B_DQ_EMPTY), 4);
         mbar_init(bar(B_DKV_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -312,31 +327,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             };
             auto issue_grad = [&](int it) -> bool {
                 const int st = it % NSTAGE;
-                if (!mbar_wait(bar(B_P_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
+                const int pb = it & 1;  // P^T / dS^T buffer
+                if (!mbar_wait(bar(B_P_FULL + pb), static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status,
                                p.timeout_ns))
                     return false;
-                const int qbuf = it & 1;
-                if (!mbar_wait(bar(B_DQ_EMPTY + qbuf), (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, abort_flag,
-                               p.status, p.timeout_ns))
+                if (!mbar_wait(bar(B_DQ_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
+                               p.timeout_ns))
                     return false;
                 tc_fence_after();
                 const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
+                const uint32_t dst = sDST + pb * PT_BYTES;
+                const uint32_t pt = tmem + (pb ? COL_PT1 : COL_PT0);
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries per UMMA
-                    umma_bf16(tmem + COL_DV, sdesc_sw128(sPT + ks * 32),
-                              sdesc_sw128_mn(dO + ks * 2048, QBOX_BYTES, 1024), id_kv,
-                              (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries (8 packed columns) per UMMA
+                    umma_bf16_ts(tmem + COL_DV, pt + ks * 8, sdesc_sw128_mn(dO + ks * 2048, QBOX_BYTES, 1024),
+                                 id_kv, (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)
-                    umma_bf16(tmem + COL_DK, sdesc_sw128(sDST + ks * 32),
+                    umma_bf16(tmem + COL_DK, sdesc_sw128(dst + ks * 32),
                               sdesc_sw128_mn(q + ks * 2048, QBOX_BYTES, 1024), id_kv,
                               (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys per UMMA
-                    umma_bf16(tmem + (qbuf ? COL_DQ1 : COL_DQ0), sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
-                              sdesc_sw128_mn(sDST + ks * 2048, KBOX_BYTES, 1024), id_q, ks > 0 ? 1u : 0u);
-                umma_commit(bar(B_P_EMPTY));
-                umma_commit(bar(B_DQ_FULL + qbuf));
+                    umma_bf16(tmem + COL_DQ, sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
+                              sdesc_sw128_mn(dst + ks * 2048, KBOX_BYTES, 1024), id_q, ks > 0 ? 1u : 0u);
+                umma_commit(bar(B_P_EMPTY + pb));
+                umma_commit(bar(B_DQ_FULL));
                 umma_commit(bar(B_Q_EMPTY + st));
                 return true;
             };
@@ -354,8 +370,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         }
     } else if (warp < 2 + SM_WARPS) {
         // ------------------------------------------------------------ softmax gradient
-        // Two warps per TMEM lane quadrant: key row r, query columns
-        // [32 hh, 32 hh + 32).
+        // SM_PARTS warps per TMEM lane quadrant: key row r, query columns
+        // [CPW hh, CPW hh + CPW).
         const int q4 = warp & 3;
         const int hh = (warp - 2) >> 2;
         const int r = q4 * 32 + lane;
@@ -377,23 +393,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            uint32_t sv[32], dp[32];
-            tmem_ld32(tmem + lane_off + COL_S + hh * 32, sv);
-            tmem_ld32(tmem + lane_off + COL_DP + hh * 32, dp);
+            uint32_t sv[CPW], dp[CPW];
+            ld_cols(tmem + lane_off + COL_S + hh * CPW, sv);
+            ld_cols(tmem + lane_off + COL_DP + hh * CPW, dp);
             tmem_ld_wait();
-            // This warp's 32 log-sum-exp and D values: broadcast 16-byte reads
+            // This warp's log-sum-exp and D values: broadcast 16-byte reads
             // of the stage (released only after the math).
-            const float4* lse4 = reinterpret_cast<const float4*>(stat + st * (STAT_BYTES / 4) + hh * 32);
+            const float4* lse4 = reinterpret_cast<const float4*>(stat + st * (STAT_BYTES / 4) + hh * CPW);
             const float4* dd4 = lse4 + BQ / 4;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_S_EMPTY));  // S^T, dP^T are in registers
-            uint32_t pk[16], sk[16];
-            const int qbase = qb * BQ + hh * 32;
+            uint32_t pk[CPW / 2], sk[CPW / 2];
+            const int qbase = qb * BQ + hh * CPW;
             // Blocks wholly below the diagonal and inside the sequence need no mask.
             const bool unmasked = qb * BQ >= k0 + BKEYS - 1 && qb * BQ + BQ <= p.seq;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
+            for (int v = 0; v < CPW / 4; ++v) {
                 const float4 l4 = lse4[v], d4 = dd4[v];
                 const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
                 float pv[4], gv[4];
@@ -414,43 +430,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_EMPTY + st));  // statistics read
-            // The previous step's gradient MMAs are done with P^T and dS^T.
-            const bool got2 = mbar_wait(bar(B_P_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag,
-                                        p.status, p.timeout_ns);
+            // The gradient MMAs of step it - 2 are done with this P^T / dS^T buffer.
+            const int pb = it & 1;
+            const bool got2 = mbar_wait(bar(B_P_EMPTY + pb), (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u,
+                                        abort_flag, p.status, p.timeout_ns);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got2)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // Row r (a key) of P^T and dS^T: 64 queries = one 128-byte row;
-            // 16-byte chunk c of the row sits at chunk c ^ (r % 8).
+            // P^T row r (a key), this warp's CPW queries: CPW / 2 packed
+            // columns of the TMEM buffer.  dS^T row r: 64 queries = one
+            // 128-byte row of shared memory, 16-byte chunk c at chunk c ^ (r % 8).
+            st_cols(tmem + lane_off + (pb ? COL_PT1 : COL_PT0) + hh * (CPW / 2), pk);
+            const uint32_t dst = sDST + pb * PT_BYTES;
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                const uint32_t chunk = static_cast<uint32_t>(hh * 4 + c8) ^ static_cast<uint32_t>(r & 7);
+            for (int c8 = 0; c8 < CPW / 8; ++c8) {
+                const uint32_t chunk = static_cast<uint32_t>(hh * (CPW / 8) + c8) ^ static_cast<uint32_t>(r & 7);
                 const uint32_t off = static_cast<uint32_t>(r) * 128 + (chunk << 4);
-                st_shared_v4(sPT + off, pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-                st_shared_v4(sDST + off, sk[4 * c8], sk[4 * c8 + 1], sk[4 * c8 + 2], sk[4 * c8 + 3]);
+                st_shared_v4(dst + off, sk[4 * c8], sk[4 * c8 + 1], sk[4 * c8 + 2], sk[4 * c8 + 3]);
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + pb));
         }
         if (ok) {
             const bool got = mbar_wait(bar(B_DKV_FULL), 0, abort_flag, p.status, p.timeout_ns);
             __syncwarp();
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
-                // hh = 0 writes the row's dV, hh = 1 its dK (times 1/sqrt(d)).
+                // The first half of the parts writes the row's dV, the second
+                // its dK (times 1/sqrt(d)), each part HD / (SM_PARTS / 2) columns.
+                constexpr int HALF = SM_PARTS / 2, SPAN = HD / HALF;
+                const int which = hh / HALF, c0 = (hh % HALF) * SPAN;
                 const bool row_ok = kpos < p.seq;
-                const float mul = hh ? p.scale : 1.0f;
+                const float mul = which ? p.scale : 1.0f;
                 __nv_bfloat16* dst = p.dkv + static_cast<long long>(tok0 + (row_ok ? kpos : 0)) * p.ld_dkv +
-                                     (hh ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD;
+                                     (which ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD + c0;
 #pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = 0; c < SPAN / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + (hh ? COL_DK : COL_DV) + c * 32, v);
+                    tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c0 + c * 32, v);
                     tmem_ld_wait();
                     if (row_ok) {
 #pragma unroll
@@ -475,32 +498,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t sdq = base + OFF_DQ + static_cast<uint32_t>(warp - 2 - SM_WARPS) * DQ_BOX_BYTES;
         for (int it = 0; it < n_it; ++it) {
-            const int qbuf = it & 1;
-            const bool got = mbar_wait(bar(B_DQ_FULL + qbuf), static_cast<uint32_t>(it >> 1) & 1u, abort_flag,
-                                       p.status, p.timeout_ns);
+            const bool got = mbar_wait(bar(B_DQ_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
+                                       p.timeout_ns);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            const uint32_t col = qbuf ? COL_DQ1 : COL_DQ0;
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_off + col, v0);
-            tmem_ld32(tmem + lane_off + col + 32, v1);
-            tmem_ld_wait();
-            tc_fence_before();
+            if (lane == 0) bulk_wait_group_read0();  // the previous box has been read
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_DQ_EMPTY + qbuf));
-                bulk_wait_group_read0();  // the previous box has been read
+            // Row c of the box = query c; lane = dimension: 128 contiguous bytes
+            // per row.  Two 32-query halves keep 32 values in registers.
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + COL_DQ + half * 32, v);
+                tmem_ld_wait();
+                if (half == 1) {  // dQ^T is in registers and shared memory: TMEM may be rewritten
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    st_shared_f32(sdq + (half * 32 + c) * 128 + lane * 4, __uint_as_float(v[c]) * p.scale);
             }
-            __syncwarp();
             const int jj = it / nq, qb = qb0 + (it - jj * nq);
             const int j = g * G + jj;
-            // Row c of the box = query c; lane = dimension: 128 contiguous bytes per row.
-#pragma unroll
-            for (int c = 0; c < 32; ++c) st_shared_f32(sdq + c * 128 + lane * 4, __uint_as_float(v0[c]) * p.scale);
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                st_shared_f32(sdq + (32 + c) * 128 + lane * 4, __uint_as_float(v1[c]) * p.scale);
             fence_proxy_async_smem();
             __syncwarp();
             // Columns of queries past the sequence are exactly zero (dS is
