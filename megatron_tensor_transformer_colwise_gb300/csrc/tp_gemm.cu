@@ -18,10 +18,14 @@
 //               CTAs' shared memory and accumulate 128 rows in each CTA's TMEM
 //   warps 2..   epilogue: TMEM -> registers -> fused op -> global (4 warps,
 //               one per TMEM lane quadrant; 8 for the activation-gradient
-//               epilogue, two per quadrant on halves of the tile's columns)
+//               and GeLU epilogues, two per quadrant on halves of the tile's
+//               columns)
 // The accumulator is double-buffered in TMEM (2 x 256 fp32 columns) so the
 // epilogue of tile n overlaps the main loop of tile n+1.  Splitting B over
 // the pair halves each SM's shared-memory operand traffic per FLOP.
+// Rowwise problems that fit in one wave of 256 x 128 tiles use those
+// instead (UMMA N = 128, 8 stages of 24 KB, 2 x 128 TMEM columns), so that
+// twice as many SMs share a short output.
 //
 // Shards are grid/loop indices, not devices: a colwise output tile may span
 // shard boundaries (the output is the concatenation of the shards' slices);
@@ -56,17 +60,18 @@ constexpr int UK = 16;              // K of one kind::f16 UMMA
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_CHUNK_ROWS = 64;
 constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
-constexpr int TMEM_COLS = 2 * BN;               // 512
 // Epilogue warps per CTA: one per TMEM lane quadrant, or two, each taking
-// half of the tile's columns, where the epilogue of a tile (the activation
-// gradient with its loads and three stores) would otherwise outlast the
-// next tile's main loop.
+// half of the tile's columns, where the epilogue of a tile would otherwise
+// outlast the next tile's main loop: the activation gradient with its loads
+// and three stores, and the GeLU epilogue of short-K problems (measured on
+// GB300: the 2048 x 4096 x 1024 GeLU GEMM in 22.9 us with 8 warps, 24.8 us
+// with 4).
 #ifndef TP_GEMM_EPI_WARPS_FWD
 #define TP_GEMM_EPI_WARPS_FWD 4
 #endif
 template <int MODE>
 __host__ __device__ constexpr int epi_warps() {
-    return MODE == tpi::GEMM_BWD_ACT ? 8 : TP_GEMM_EPI_WARPS_FWD;
+    return (MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : TP_GEMM_EPI_WARPS_FWD;
 }
 template <int MODE>
 __host__ __device__ constexpr int num_threads() {
@@ -87,13 +92,14 @@ __host__ __device__ constexpr int num_threads() {
 // accumulating, TMA reduce-adds.
 constexpr int EPI_BOX = 32;                        // rows and columns of an output box
 constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;  // 2 KB
-template <int MODE, int CG>
+template <int MODE, int CG, int BNT = BN>
 struct Cfg {
-    static constexpr int B_BYTES = (BN / CG) * BK * 2;
+    static constexpr int B_BYTES = (BNT / CG) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr bool STAGED_OUT = MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_TN;
-    static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : 6);
-    static constexpr int CHUNKS = (BN / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
+    static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : (BNT == BN ? 6 : 8));
+    static constexpr int CHUNKS = (BNT / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
+    static constexpr int TMEM_COLS = 2 * BNT;                  // two accumulators
     static constexpr int EPI_BYTES = MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
                                      : MODE == tpi::GEMM_TN    ? 4 * 2 * 2 * EPI_BOX_BYTES  // 4 warps x 2 fp32 boxes
                                                                : 0;
@@ -174,42 +180,86 @@ __device__ __forceinline__ int kv_first(int k, int t, int i) {
     return (k >= t) ? i * (k / t) : (i * k) / t;
 }
 
-__device__ __forceinline__ float act_apply(int act, float v) {
-    if (act == TP_ACT_GELU_ERF) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
-    if (act == TP_ACT_GELU_TANH)
-        return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * (v + 0.044715f * v * v * v)));
+// 2^x and 1/x on the SFU (PTX ex2.approx.ftz / rcp.approx.ftz: relative
+// error about 2^-22 and 1 ulp; 2^-inf = +0, 1/inf = +0).  The activations
+// below are rounded to bf16 (8 significant bits) right after, so these are
+// far below the output's resolution.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Upper tail of the standard normal CDF: q(u) = (1 - erf(|u| / sqrt2)) / 2,
+// with erf from Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26: for y >= 0, erf(y) = 1 - t (a1 + t (a2 + t (a3 + t (a4 +
+// t a5)))) exp(-y^2) + e(y), t = 1 / (1 + p y), |e(y)| <= 1.5e-7.  So Phi(u)
+// = 1 - q for u >= 0 and q for u < 0, and e = exp(-u^2 / 2) is returned
+// for the GeLU derivative's density term.
+__device__ __forceinline__ float normal_tail(float u, float& e) {
+    constexpr float P = 0.3275911f * 0.70710678118654752f;  // p / sqrt2 (y = |u| / sqrt2)
+    constexpr float A1 = 0.5f * 0.254829592f, A2 = 0.5f * -0.284496736f, A3 = 0.5f * 1.421413741f;
+    constexpr float A4 = 0.5f * -1.453152027f, A5 = 0.5f * 1.061405429f;
+    const float t = rcp_approx(fmaf(P, fabsf(u), 1.0f));
+    e = ex2_approx(u * u * (-0.5f * kLog2e));
+    return t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, A5, A4), A3), A2), A1) * e;
+}
+
+// GeLU, exact (erf) form: u Phi(u).
+__device__ __forceinline__ float gelu_erf(float u) {
+    float e;
+    const float q = normal_tail(u, e);
+    return u * (u >= 0.0f ? 1.0f - q : q);
+}
+
+// GeLU, tanh form: u (1 + tanh(z)) / 2 with z = sqrt(2/pi) (u + 0.044715
+// u^3), through (1 + tanh(z)) / 2 = 1 / (1 + exp(-2 z)).
+constexpr float kGeluC = 0.79788456080286536f, kGeluA = 0.044715f;
+__device__ __forceinline__ float gelu_tanh_sigma(float u) {
+    const float z = kGeluC * u * fmaf(kGeluA * u, u, 1.0f);
+    return rcp_approx(1.0f + ex2_approx(-2.0f * kLog2e * z));
+}
+
+// SiLU(u) = u sigmoid(u) = u / (1 + exp(-u)).
+__device__ __forceinline__ float silu(float u) { return u * rcp_approx(1.0f + ex2_approx(-kLog2e * u)); }
+
+template <int ACT>
+__device__ __forceinline__ float act_apply(float v) {
+    if (ACT == TP_ACT_GELU_ERF) return gelu_erf(v);
+    if (ACT == TP_ACT_GELU_TANH) return v * gelu_tanh_sigma(v);
     return v;
 }
 
-// Backward of the MLP nonlinearity at one element: from the pre-activation
-// u (and the SwiGLU up value g) and dh = dL/dH, the gradients du (and dg)
-// and the forward value hv = H.
-//   SwiGLU  H = SiLU(u) g:  du = dh g s (1 + u (1 - s)), s = sigmoid(u);
-//           dg = dh SiLU(u)
-//   GeLU    H = u Phi(u):   du = dh (Phi(u) + u phi(u))
-//   GeLU (tanh form) H = u/2 (1 + T), T = tanh(c (u + a u^3)):
-//           du = dh (1/2 (1 + T) + u/2 (1 - T^2) c (1 + 3 a u^2))
 template <int ACT>
 __device__ __forceinline__ void act_backward(float u, float g, float dh, float& du, float& dg,
                                              float& hv) {
     dg = 0.0f;
     if (ACT == TP_ACT_SWIGLU) {
-        // Fast-math sigmoid (the results are rounded to bf16).
-        const float s = __fdividef(1.0f, 1.0f + __expf(-u));
-        const float silu = u * s;
-        hv = silu * g;
-        dg = dh * silu;
+        const float s = rcp_approx(1.0f + ex2_approx(-kLog2e * u));  // sigmoid(u)
+        const float su = u * s;
+        hv = su * g;
+        dg = dh * su;
         du = dh * g * (s * (1.0f + u * (1.0f - s)));
     } else if (ACT == TP_ACT_GELU_ERF) {
-        const float cdf = 0.5f * (1.0f + erff(u * 0.70710678118654752f));
-        const float pdf = 0.39894228040143268f * expf(-0.5f * u * u);
+        float e;  // exp(-u^2 / 2)
+        const float q = normal_tail(u, e);
+        const float cdf = u >= 0.0f ? 1.0f - q : q;
+        const float pdf = 0.39894228040143268f * e;  // 1 / sqrt(2 pi)
         hv = u * cdf;
         du = dh * (cdf + u * pdf);
     } else if (ACT == TP_ACT_GELU_TANH) {
-        const float c = 0.79788456080286536f, a = 0.044715f;
-        const float th = tanhf(c * (u + a * u * u * u));
-        hv = 0.5f * u * (1.0f + th);
-        du = dh * (0.5f * (1.0f + th) + 0.5f * u * (1.0f - th * th) * c * (1.0f + 3.0f * a * u * u));
+        // sigma = (1 + tanh z) / 2; d/du [u sigma] = sigma + u 2 sigma (1 -
+        // sigma) dz/du, dz/du = c (1 + 3 a u^2).
+        const float sg = gelu_tanh_sigma(u);
+        hv = u * sg;
+        du = dh * (sg + u * 2.0f * sg * (1.0f - sg) * kGeluC * fmaf(3.0f * kGeluA * u, u, 1.0f));
     } else {
         hv = u;
         du = dh;
@@ -319,10 +369,10 @@ __device__ __forceinline__ void b_boxes(const GemmParams& p, int nb, int first,
     }
 }
 
-template <int MODE, int CG>
+template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                               uint32_t rank, volatile int* abort_flag) {
-    using C = Cfg<MODE, CG>;
+    using C = Cfg<MODE, CG, BNT>;
     constexpr bool ROW = (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
@@ -355,7 +405,7 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                     const uint32_t dst = c < 0 ? a_dst : b_dst + c * B_CHUNK_BYTES;
                     if (ROW) {
                         const CUtensorMap* map = c < 0 ? &p.mapA : &p.mapB[0];
-                        const int r = c < 0 ? arow : nb * BN + cc * B_CHUNK_ROWS;
+                        const int r = c < 0 ? arow : nb * BNT + cc * B_CHUNK_ROWS;
                         if (CG == 2) tma_load_3d_pair(dst, map, full_l, kc, shard, r);
                         else tma_load_3d(dst, map, full_l, kc, shard, r);
                     } else if (c < 0 && Major<MODE>::A_MN) {
@@ -399,14 +449,14 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
     }
 }
 
-template <int MODE, int CG>
+template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                          uint32_t tmem_base, volatile int* abort_flag) {
-    using C = Cfg<MODE, CG>;
+    using C = Cfg<MODE, CG, BNT>;
     constexpr bool AMN = Major<MODE>::A_MN, BMN = Major<MODE>::B_MN;
     // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
     constexpr uint32_t idesc =
-        idesc_bf16_f32(BM * CG, BN) | (AMN ? (1u << 15) : 0u) | (BMN ? (1u << 16) : 0u);
+        idesc_bf16_f32(BM * CG, BNT) | (AMN ? (1u << 15) : 0u) | (BMN ? (1u << 16) : 0u);
     // Per UMMA (K = 16): a K-major operand advances 32 bytes inside its
     // swizzle row (2 in descriptor units), an MN-major one 16 K rows of
     // 128 bytes (128 units).
@@ -423,7 +473,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
             break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * BNT;
         for (int kb = 0; kb < kblocks; ++kb) {
             const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
             if (!mbar_wait(full, phase, abort_flag, p.status, p.timeout_ns)) {
@@ -541,15 +591,104 @@ __device__ __forceinline__ void bwd_act_tile(const GemmParams& p, const __nv_bfl
     }
 }
 
-template <int MODE, int CG>
+// Epilogue of the column- and row-parallel forward modes for one warp's CPW
+// 32-column chunks of a tile (row: this thread's global row; rs: the folded
+// RMSNorm scale of colwise rows; ssq accumulates the squares of the stored
+// values when the rowwise GEMM feeds the next norm).
+template <int MODE, int ACT, int CPW, int BNT>
+__device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int cb, int nb, int s_grid, int row,
+                                         bool row_ok, float rs, float& ssq) {
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = cb; c < cb + CPW; ++c) {
+        const int col0 = nb * BNT + c * 32;
+        if (col0 >= p.N) break;  // warp-uniform
+        __syncwarp();
+        tmem_ld32(t0 + c * 32, r);
+        tmem_ld_wait();
+        if (!row_ok) {
+        } else if (MODE == tpi::GEMM_ROW_PARTIAL && p.out_f32) {
+            float* out = reinterpret_cast<float*>(p.out) + s_grid * p.shard_stride +
+                         static_cast<long long>(row) * p.ldo;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int col = col0 + g * 4;
+                if (col < p.N)
+                    st_v4(out + col, r[g * 4], r[g * 4 + 1], r[g * 4 + 2], r[g * 4 + 3]);
+            }
+        } else {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+            if (MODE == tpi::GEMM_ROW_PARTIAL) out += s_grid * p.shard_stride;
+            out += static_cast<long long>(row) * p.ldo;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int col = col0 + g * 8;
+                if (col >= p.N) continue;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[g * 8 + e]);
+                if (MODE == tpi::GEMM_COL_ACT || MODE == tpi::GEMM_COL_QKV ||
+                    MODE == tpi::GEMM_COL_PACKED) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] *= rs;
+                }
+                if (MODE == tpi::GEMM_COL_ACT) {
+                    if (p.aux_out)  // pre-activations for the backward pass
+                        st_v4(p.aux_out + static_cast<long long>(row) * p.ldaux + col,
+                              pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = act_apply<ACT>(v[e]);
+                }
+                if (MODE == tpi::GEMM_ROW_FUSED) {
+                    if (p.bias) {
+                        const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col);
+                        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(bw[e]);
+                            v[2 * e] += f.x;
+                            v[2 * e + 1] += f.y;
+                        }
+                    }
+                    if (p.residual) {
+                        const uint4 rr = *reinterpret_cast<const uint4*>(
+                            p.residual + static_cast<long long>(row) * p.ldr + col);
+                        const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(rw[e]);
+                            v[2 * e] += f.x;
+                            v[2 * e + 1] += f.y;
+                        }
+                    }
+                }
+                const uint32_t w0 = pack_bf16x2(v[0], v[1]), w1 = pack_bf16x2(v[2], v[3]);
+                const uint32_t w2 = pack_bf16x2(v[4], v[5]), w3 = pack_bf16x2(v[6], v[7]);
+                st_v4(out + col, w0, w1, w2, w3);
+                if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out) {
+                    // The next norm reads the stored (bf16) values.
+                    const uint32_t ws[4] = {w0, w1, w2, w3};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_bf16x2(ws[e]);
+                        ssq = fmaf(f.x, f.x, fmaf(f.y, f.y, ssq));
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t epi0,
                                               uint32_t tmem_base, uint32_t rank, volatile int* abort_flag) {
-    using C = Cfg<MODE, CG>;
+    using C = Cfg<MODE, CG, BNT>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     constexpr int EPI_WARPS = epi_warps<MODE>();
     const int half = (warp - 2) >> 2;  // which half of the tile's columns (8 warps)
-    constexpr int CPW = (BN / 32) / (EPI_WARPS / 4);        // 32-column chunks per warp
+    constexpr int CPW = (BNT / 32) / (EPI_WARPS / 4);       // 32-column chunks per warp
     constexpr int CPW_GLU = (BN / 64) / (EPI_WARPS / 4);    // SwiGLU: output chunks per warp
     const int cb = half * CPW, cb_glu = half * CPW_GLU;
     uint32_t acc = 0, acc_phase = 0;
@@ -581,7 +720,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         if (MODE != tpi::GEMM_ROW_FUSED && MODE != tpi::GEMM_ROW_PARTIAL && p.row_ss && row_ok)
             rs = rsqrtf(p.row_ss[row] * p.inv_h + p.eps);
         float ssq = 0.0f;
-        const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t t0 = tmem_base + acc * BNT + (static_cast<uint32_t>(q * 32) << 16);
         uint32_t r[32];
         if (MODE == tpi::GEMM_BWD_ACT) {
             // One branch-free chunk loop per activation, chosen once per tile.
@@ -658,8 +797,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                                 const float g1 = __uint_as_float(r[g * 8 + 2 * e + 1]) * rs;
                                 const float u0 = __uint_as_float(u[g * 8 + 2 * e]) * rs;
                                 const float u1 = __uint_as_float(u[g * 8 + 2 * e + 1]) * rs;
-                                const float h0 = g0 / (1.0f + expf(-g0)) * u0;
-                                const float h1 = g1 / (1.0f + expf(-g1)) * u1;
+                                const float h0 = silu(g0) * u0;
+                                const float h1 = silu(g1) * u1;
                                 w[e] = pack_bf16x2(h0, h1);
                                 pg[e] = pack_bf16x2(g0, g1);
                                 pu[e] = pack_bf16x2(u0, u1);
@@ -675,86 +814,21 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                     }
                 }
             }
-        } else {
-#pragma unroll 1
-            for (int c = cb; c < cb + CPW; ++c) {
-                const int col0 = nb * BN + c * 32;
-                if (col0 >= p.N) break;  // warp-uniform
-                __syncwarp();
-                tmem_ld32(t0 + c * 32, r);
-                tmem_ld_wait();
-                if (!row_ok) {
-                } else if (MODE == tpi::GEMM_ROW_PARTIAL && p.out_f32) {
-                    float* out = reinterpret_cast<float*>(p.out) + s_grid * p.shard_stride +
-                                 static_cast<long long>(row) * p.ldo;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const int col = col0 + g * 4;
-                        if (col < p.N)
-                            st_v4(out + col, r[g * 4], r[g * 4 + 1], r[g * 4 + 2], r[g * 4 + 3]);
-                    }
-                } else {
-                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-                    if (MODE == tpi::GEMM_ROW_PARTIAL) out += s_grid * p.shard_stride;
-                    out += static_cast<long long>(row) * p.ldo;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = col0 + g * 8;
-                        if (col >= p.N) continue;
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[g * 8 + e]);
-                        if (MODE == tpi::GEMM_COL_ACT || MODE == tpi::GEMM_COL_QKV ||
-                            MODE == tpi::GEMM_COL_PACKED) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] *= rs;
-                        }
-                        if (MODE == tpi::GEMM_COL_ACT) {
-                            if (p.aux_out)  // pre-activations for the backward pass
-                                st_v4(p.aux_out + static_cast<long long>(row) * p.ldaux + col,
-                                      pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
-                        }
-                        if (MODE == tpi::GEMM_ROW_FUSED) {
-                            if (p.bias) {
-                                const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col);
-                                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 f = unpack_bf16x2(bw[e]);
-                                    v[2 * e] += f.x;
-                                    v[2 * e + 1] += f.y;
-                                }
-                            }
-                            if (p.residual) {
-                                const uint4 rr = *reinterpret_cast<const uint4*>(
-                                    p.residual + static_cast<long long>(row) * p.ldr + col);
-                                const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 f = unpack_bf16x2(rw[e]);
-                                    v[2 * e] += f.x;
-                                    v[2 * e + 1] += f.y;
-                                }
-                            }
-                        }
-                        const uint32_t w0 = pack_bf16x2(v[0], v[1]), w1 = pack_bf16x2(v[2], v[3]);
-                        const uint32_t w2 = pack_bf16x2(v[4], v[5]), w3 = pack_bf16x2(v[6], v[7]);
-                        st_v4(out + col, w0, w1, w2, w3);
-                        if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out) {
-                            // The next norm reads the stored (bf16) values.
-                            const uint32_t ws[4] = {w0, w1, w2, w3};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_bf16x2(ws[e]);
-                                ssq = fmaf(f.x, f.x, fmaf(f.y, f.y, ssq));
-                            }
-                        }
-                    }
-                }
+        } else if (MODE == tpi::GEMM_COL_ACT) {
+            // One branch-free chunk loop per activation, chosen once per tile.
+            switch (p.act) {
+                case TP_ACT_GELU_ERF:
+                    std_tile<MODE, TP_ACT_GELU_ERF, CPW, BNT>(p, t0, cb, nb, s_grid, row, row_ok, rs, ssq);
+                    break;
+                case TP_ACT_GELU_TANH:
+                    std_tile<MODE, TP_ACT_GELU_TANH, CPW, BNT>(p, t0, cb, nb, s_grid, row, row_ok, rs, ssq);
+                    break;
+                default:
+                    std_tile<MODE, TP_ACT_NONE, CPW, BNT>(p, t0, cb, nb, s_grid, row, row_ok, rs, ssq);
+                    break;
             }
+        } else {
+            std_tile<MODE, TP_ACT_NONE, CPW, BNT>(p, t0, cb, nb, s_grid, row, row_ok, rs, ssq);
         }
         if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out && row_ok) atomicAdd(p.ss_out + row, ssq);
         tc_fence_before();
@@ -774,10 +848,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
     __syncwarp();
 }
 
-template <int MODE, int CG>
+template <int MODE, int CG, int BNT>
 __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr int EPI_WARPS = epi_warps<MODE>();
-    using C = Cfg<MODE, CG>;
+    using C = Cfg<MODE, CG, BNT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -812,10 +886,10 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     }
     if (warp == 1) {
         if (CG == 2) {
-            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
             tmem_relinquish_pair();
         } else {
-            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
             tmem_relinquish();
         }
     }
@@ -827,11 +901,11 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop<MODE, CG>(p, base, bar0, rank, abort_flag);
+        if (lane == 0) producer_loop<MODE, CG, BNT>(p, base, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) mma_loop<MODE, CG>(p, base, bar0, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
     } else {
-        epilogue_loop<MODE, CG>(p, bar0, epi0, tmem_base, rank, abort_flag);
+        epilogue_loop<MODE, CG, BNT>(p, bar0, epi0, tmem_base, rank, abort_flag);
     }
     __syncwarp();
     tc_fence_before();
@@ -840,8 +914,8 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     if (CG == 2) cluster_sync_all();
     tc_fence_after();
     if (warp == 1) {
-        if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
-        else tmem_dealloc(tmem_base, TMEM_COLS);
+        if (CG == 2) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -892,15 +966,15 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     return true;
 }
 
-template <int MODE, int CG>
+template <int MODE, int CG, int BNT = BN>
 int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string* err) {
-    auto kern = tp_gemm_kernel<MODE, CG>;
+    auto kern = tp_gemm_kernel<MODE, CG, BNT>;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<MODE, CG>::SMEM);
+                                             Cfg<MODE, CG, BNT>::SMEM);
         if (e != cudaSuccess) {
             if (err) *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return TP_ERR_CUDA;
@@ -911,7 +985,7 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(num_threads<MODE>(), 1, 1);
-    cfg.dynamicSmemBytes = Cfg<MODE, CG>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<MODE, CG, BNT>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -935,6 +1009,8 @@ namespace tpi {
 
 // CTAs per output tile (1: 128 x 256 per CTA; 2: 256 x 256 per CTA pair).
 constexpr int kPairTiles = TP_GEMM_CTA_PAIR;
+// Output columns of the narrow rowwise tile (UMMA N = 128).
+constexpr int kNarrowBN = 128;
 
 int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     GemmParams p;
@@ -970,6 +1046,17 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     const int bn_out = (a.mode == GEMM_COL_SWIGLU) ? BN / 2 : BN;
     p.n_tiles = static_cast<int>((a.N + bn_out - 1) / bn_out);
     p.grid_shards = (a.mode == GEMM_ROW_PARTIAL) ? a.t : 1;
+    // Rowwise GEMMs of small problems (few output tiles, long K) take
+    // 128-column tiles when those still fit in one wave: twice the CTAs
+    // busy, each tile half as long.
+    bool narrow = false;
+    if (row) {
+        const long long units = std::max(1, device_sm_count() / CG);
+        const long long n_narrow = (a.N + kNarrowBN - 1) / kNarrowBN;
+        const long long thin = static_cast<long long>(p.grid_shards) * p.m_tiles * n_narrow;
+        narrow = n_narrow > p.n_tiles && thin <= units;
+        if (narrow) p.n_tiles = static_cast<int>(n_narrow);
+    }
     p.shard_stride = a.M * a.ldo;
     if (row) {
         p.kb_per_shard = static_cast<int>((a.Ks + BK - 1) / BK);
@@ -1112,8 +1199,12 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         case GEMM_COL_ACT: return launch_mode<GEMM_COL_ACT, CG>(p, grid, stream, err);
         case GEMM_COL_SWIGLU: return launch_mode<GEMM_COL_SWIGLU, CG>(p, grid, stream, err);
         case GEMM_COL_QKV: return launch_mode<GEMM_COL_QKV, CG>(p, grid, stream, err);
-        case GEMM_ROW_FUSED: return launch_mode<GEMM_ROW_FUSED, CG>(p, grid, stream, err);
-        case GEMM_ROW_PARTIAL: return launch_mode<GEMM_ROW_PARTIAL, CG>(p, grid, stream, err);
+        case GEMM_ROW_FUSED:
+            return narrow ? launch_mode<GEMM_ROW_FUSED, CG, kNarrowBN>(p, grid, stream, err)
+                          : launch_mode<GEMM_ROW_FUSED, CG>(p, grid, stream, err);
+        case GEMM_ROW_PARTIAL:
+            return narrow ? launch_mode<GEMM_ROW_PARTIAL, CG, kNarrowBN>(p, grid, stream, err)
+                          : launch_mode<GEMM_ROW_PARTIAL, CG>(p, grid, stream, err);
         case GEMM_COL_PACKED: return launch_mode<GEMM_COL_PACKED, CG>(p, grid, stream, err);
         case GEMM_BWD_ACT: return launch_mode<GEMM_BWD_ACT, CG>(p, grid, stream, err);
         case GEMM_NN: return launch_mode<GEMM_NN, CG>(p, grid, stream, err);

@@ -123,11 +123,48 @@ def test_colwise_activation_within_tolerance(act):
     assert_close(host64(Y), ref, what=f"colwise {act}")
 
 
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu"])
+def test_colwise_activation_pointwise_accuracy(act):
+    # X = I: every pre-activation is exactly one bf16 weight (N(0, 3^2),
+    # so both tails are covered), and every output is act(u) rounded once
+    # to bf16.  It must lie within half a bf16 ulp of the exact value plus
+    # the activation's own error in fp32 (the erf form is good to 7e-8 |u|
+    # in exact arithmetic; the SFU exp2 and reciprocal add a few fp32 ulps).
+    M = K = 256
+    f, t = 512, 4
+    X = torch.eye(M, dtype=torch.bfloat16)
+    W1 = synth.normal_bf16((f, K), 3.0, 9001)
+    W3 = synth.normal_bf16((f, K), 3.0, 9002) if act == "swiglu" else None
+    cfg = tp.make_config(tokens=M, hidden=K, ffn=f, tp_degree=t, act=act)
+    plan = tp.Plan(cfg)
+    Y = torch.empty(M, f, dtype=torch.bfloat16, device="cuda")
+    tp.tp_colwise_forward(plan, dev(X), dev(W1), dev(W3) if W3 is not None else None, Y)
+    sync_ok(plan)
+    U = host64(W1).T  # U[m][n] = W1[n][m]
+    fn = {"gelu": oracle.gelu_erf, "gelu_tanh": oracle.gelu_tanh, "swiglu": oracle.silu}[act]
+    ref = np.vectorize(fn)(U)
+    if act == "swiglu":
+        ref = ref * host64(W3).T
+    got = host64(Y)
+    mag = np.abs(ref)
+    ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.where(mag > 0, mag, 1.0))) - 7), 0.0)
+    bound = 0.5 * ulp + 1e-6 * mag + 4e-7 * np.abs(U)
+    excess = np.abs(got - ref) - bound
+    i = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, f"{act}: u={U[i]} got {got[i]} ref {ref[i]}"
+
+
 # ---------------------------------------------------------------- rowwise
 
+# SMALL_MLP runs the narrow (128-column) rowwise tiles, which a problem of
+# at most one wave of them gets; the ragged 2500 x 1000 one has more tiles
+# and runs the 256-column tiles.
+ROW_SHAPES = [SMALL_MLP, Shape("row_wide", 1, 2500, 1000, ffn=800, tp=4, act="gelu", index=15)]
+
+
 @pytest.mark.parametrize("mode", [tp.TP_REDUCE_FUSED, tp.TP_REDUCE_PARTIALS])
-def test_rowwise_integer_bit_exact(mode):
-    s = SMALL_MLP
+@pytest.mark.parametrize("s", ROW_SHAPES, ids=["narrow", "wide_ragged"])
+def test_rowwise_integer_bit_exact(s, mode):
     t, M, h, f = s.tp, s.tokens, s.hidden, s.ffn
     Y = synth.integer_bf16((M, f), -2, 2, 31)
     W2 = synth.integer_bf16((h, f), -2, 2, 32)
