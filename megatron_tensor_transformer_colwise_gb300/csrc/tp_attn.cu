@@ -11,24 +11,29 @@
 // (key position <= query position) within each sequence, fp32 softmax with
 // a running maximum subtracted, no dropout, no rotary embedding.
 //
-// One CTA per (128 query rows, query head, sequence), 6 warps, two CTAs
+// One CTA per (128 query rows, query head, sequence), 7 warps, two CTAs
 // resident per SM (256 TMEM columns and ~97 KB of shared memory each), so
 // one CTA's softmax overlaps the other's tensor-core work:
 //   warp 0      TMA: Q once, then K and V blocks of 64 keys (2-stage rings,
 //               K one block ahead) from the shard-blocked QKV buffer.
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T (128 x 64, fp32, two
-//               TMEM buffers so S of block j+1 is computed while the softmax
-//               works on block j), then O += P V with P read from TMEM
-//               (tcgen05.mma with the A operand in tensor memory) and V used
-//               as an MN-major operand straight from its [key][d] layout.
-//   warps 2..5  one query row per thread (TMEM lane = row): read the S row,
+//   warp 1      TMEM owner and S issuer: S = Q K^T (128 x 64, fp32, two TMEM
+//               buffers so S of block j+1 is computed while the softmax works
+//               on block j).
+//   warp 2      PV issuer: O += P V with P read from TMEM (tcgen05.mma with
+//               the A operand in tensor memory) and V used as an MN-major
+//               operand straight from its [key][d] layout.
+//               A thread issues one tcgen05.mma about every 100 cycles
+//               whatever its size (measured on GB300), while an S or PV step
+//               here is 30 to 60 cycles of math, so the two products have
+//               an issuing thread each.
+//   warps 3..6  one query row per thread (TMEM lane = row): read the S row,
 //               apply the causal mask, online softmax with exp2, write P as
 //               bf16 over the first half of the same S buffer (tcgen05.st),
 //               rescale the O row in TMEM when its reference maximum moves,
 //               and finally write O / l as bf16.
-// A buffer is reused for S of block j+2 after the PV of block j, which reads
-// its P, in the tensor core's issue order; the softmax warps wait for that
-// PV to complete only when they rescale O in place.
+// A buffer is reused for S of block j+2 once the PV of block j, which reads
+// its P, has completed; the softmax warps wait for the previous PV to
+// complete only when they rescale O in place.
 // The reference maximum of a row only moves when the block maximum exceeds
 // it by more than 2^8 (in the exp2 domain), so most blocks need no O
 // rescale; P then stays below 256, well inside bf16 and fp32 range.
@@ -48,7 +53,7 @@ using namespace tpk;
 
 constexpr int QB = 128;  // query rows per CTA (UMMA M, TMEM lanes)
 constexpr int KB = 64;   // keys per block (UMMA N of S, UMMA K of PV)
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;
 constexpr int QBOX = QB * 128;  // TMA box of Q: 128 rows x 64 bf16 (16 KB)
 constexpr int KBOX = KB * 128;  // TMA box of K or V: 64 rows x 64 bf16 (8 KB)
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 of the allowed growth of P
@@ -63,8 +68,8 @@ enum {
     B_PV_DONE = 11,  // x2: the PV MMA that read P from buffer i has completed
     B_P_FULL = 13,
     B_O_FULL = 15,
-    B_DRAIN = 16,
-    NUM_BARS = 17
+    B_DRAIN = 16,    // x2: one per issuing thread
+    NUM_BARS = 18
 };
 
 // Per-CTA dynamic shared memory when two CTAs share an SM: (228 KB - 2 x
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         mbar_init(bar(B_P_FULL), 4);
         mbar_init(bar(B_O_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_DRAIN + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -229,36 +235,47 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+        // ---------------------------------------------------------- S issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(QB, KB);
-            constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(QB, D);
             bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, p.status, p.timeout_ns);
-            auto issue_s = [&](int kb) -> bool {
+            for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int st = kb & 1;
-                const uint32_t use = static_cast<uint32_t>(kb >> 1);
-                // Buffer st held S and then P of block kb - 2.  Its PV was
-                // issued earlier by this thread, and tcgen05.mma operations
-                // from one thread execute in issue order, so this S cannot
-                // overwrite P before that PV has read it.
-                if (!mbar_wait(bar(B_K_FULL + st), use & 1u, abort_flag, p.status, p.timeout_ns))
-                    return false;
+                // Buffer st held S and then P of block kb - 2: its PV must
+                // have read that P before this S overwrites it.
+                if (kb >= 2 && !mbar_wait(bar(B_PV_DONE + st), static_cast<uint32_t>((kb - 2) >> 1) & 1u, abort_flag,
+                                          p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(bar(B_K_FULL + st), static_cast<uint32_t>(kb >> 1) & 1u, abort_flag, p.status,
+                               p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + st * KB;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t a_off = (ks >> 2) * QBOX + (ks & 3) * 32;
                     const uint32_t b_off = (ks >> 2) * KBOX + (ks & 3) * 32;
-                    umma_bf16(d_tmem, sdesc_sw128(sQ + a_off), sdesc_sw128(sK + st * L::KT + b_off),
-                              idesc_s, ks > 0 ? 1u : 0u);
+                    umma_bf16(d_tmem, sdesc_sw128(sQ + a_off), sdesc_sw128(sK + st * L::KT + b_off), idesc_s,
+                              ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_K_EMPTY + st));
                 umma_commit(bar(B_S_FULL + st));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
+            }
+            if (!ok) {
+                umma_commit(bar(B_DRAIN));
+                drain_wait(bar(B_DRAIN), 0);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- PV issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(QB, D);
+            bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
-                if (kb + 1 < nkb && !(ok = issue_s(kb + 1))) break;
                 const int vst = kb & 1;
                 if (!mbar_wait(bar(B_P_FULL), kb & 1, abort_flag, p.status, p.timeout_ns) ||
                     !mbar_wait(bar(B_V_FULL + vst), (kb >> 1) & 1, abort_flag, p.status, p.timeout_ns)) {
@@ -280,8 +297,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             if (ok) {
                 umma_commit(bar(B_O_FULL));
             } else {
-                umma_commit(bar(B_DRAIN));
-                drain_wait(bar(B_DRAIN), 0);
+                umma_commit(bar(B_DRAIN + 1));
+                drain_wait(bar(B_DRAIN + 1), 0);
             }
         }
     } else {
