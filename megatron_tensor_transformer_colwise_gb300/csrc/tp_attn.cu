@@ -238,6 +238,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         // ---------------------------------------------------------- S issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(QB, KB);
+            // Descriptors built once: a step adds its constant offset (in
+            // 16-byte units) to the start-address field.
+            const uint64_t qdesc = sdesc_sw128(sQ);
+            const uint64_t kdesc0 = sdesc_sw128(sK), kdesc1 = sdesc_sw128(sK + L::KT);
             bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, p.status, p.timeout_ns);
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int st = kb & 1;
@@ -255,12 +259,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + st * KB;
+                const uint64_t kdesc = st ? kdesc1 : kdesc0;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t a_off = (ks >> 2) * QBOX + (ks & 3) * 32;
-                    const uint32_t b_off = (ks >> 2) * KBOX + (ks & 3) * 32;
-                    umma_bf16(d_tmem, sdesc_sw128(sQ + a_off), sdesc_sw128(sK + st * L::KT + b_off), idesc_s,
-                              ks > 0 ? 1u : 0u);
+                    constexpr uint32_t unit = 16;
+                    const uint32_t a_off = ((ks >> 2) * QBOX + (ks & 3) * 32) / unit;
+                    const uint32_t b_off = ((ks >> 2) * KBOX + (ks & 3) * 32) / unit;
+                    umma_bf16(d_tmem, qdesc + a_off, kdesc + b_off, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_K_EMPTY + st));
                 umma_commit(bar(B_S_FULL + st));
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         // ---------------------------------------------------------- PV issuer
         if (lane == 0) {
             constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(QB, D);
+            const uint64_t vdesc0 = sdesc_sw128_mn(sV, KBOX, 1024), vdesc1 = sdesc_sw128_mn(sV + L::KT, KBOX, 1024);
             bool ok = true;
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int vst = kb & 1;
@@ -285,12 +291,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 tc_fence_after();
                 // P of block kb: bf16 in the first KB/2 columns of S buffer
                 // kb & 1, 16 keys (8 columns) per UMMA.
+                const uint64_t vdesc = vst ? vdesc1 : vdesc0;
+                const uint32_t pcol = tmem + (kb & 1) * KB;
+                const uint32_t acc0 = kb > 0 ? 1u : 0u;
 #pragma unroll
-                for (int ks = 0; ks < KB / 16; ++ks) {
-                    umma_bf16_ts(tmem + 2 * KB, tmem + (kb & 1) * KB + ks * 8,
-                                 sdesc_sw128_mn(sV + vst * L::KT + ks * 16 * 128, KBOX, 1024), idesc_o,
-                                 (kb > 0 || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < KB / 16; ++ks)
+                    umma_bf16_ts(tmem + 2 * KB, pcol + ks * 8, vdesc + (ks * 16 * 128) / 16, idesc_o, ks > 0 ? 1u : acc0);
                 umma_commit(bar(B_V_EMPTY + vst));
                 umma_commit(bar(B_PV_DONE + (kb & 1)));
             }
