@@ -16,22 +16,25 @@
 //                         of each sequence to a multiple of 64 rows, and a
 //                         zeroed fp32 dQ accumulator.
 //   attn_bwd_kernel       one CTA per (128-key block, KV head, sequence),
-//                         longest (earliest) key blocks first, 14 warps:
+//                         longest (earliest) key blocks first, 15 warps:
 //     warp 0     TMA: K and V of the key block once; then, per step, Q and
 //                dO of 64 queries of one query head of the group plus their
 //                log-sum-exp and D (3-stage ring).
-//     warp 1     TMEM owner and MMA issuer.  Per step:
+//     warp 1     TMEM owner and issuer of, per step,
 //                  S^T  = K Q^T   and dP^T = V dO^T   (128 x 64, TMEM)
-//                then, once the softmax warps have written P^T and dS^T:
+//     warp 14    issuer of the gradient products, once the softmax warps
+//                have written P^T and dS^T:
 //                  dV  += P^T dO  (P^T read from TMEM),
 //                  dK  += dS^T Q                      (128 x d, TMEM, over
 //                                                      the whole group)
 //                  dQ^T = K^T dS^T                    (d x 64, TMEM)
-//                S^T of the next step is issued before the gradients of the
-//                current one, so the tensor core works while the softmax
-//                warps compute; P^T (TMEM) and dS^T (shared memory) are
-//                double-buffered, so step i's stores need only step i-2's
-//                gradient MMAs to be done.
+//                A thread issues one tcgen05.mma about every 100 cycles
+//                whatever its size (measured on GB300), and a step is 32 of
+//                them, so the two groups have an issuing thread each: S^T of
+//                the next step is computed while the softmax warps and the
+//                gradient products work on the current one.  P^T (TMEM) and
+//                dS^T (shared memory) are double-buffered, so step i's stores
+//                need only step i-2's gradient MMAs to be done.
 //     warps 2-9  one key row and 32 of the 64 queries per thread (two warps
 //                per TMEM lane quadrant): P^T = 2^(S^T log2(e)/sqrt(d) - lse)
 //                under the causal mask, dS^T = P^T (dP^T - D); P^T to TMEM,
@@ -53,6 +56,7 @@
 
 #include <cstring>
 #include <string>
+#include <type_traits>
 
 #include "tp_device.cuh"
 #include "tp_internal.h"
@@ -70,7 +74,8 @@ constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
 constexpr int SM_WARPS = 8;
 constexpr int SM_PARTS = SM_WARPS / 4;         // column parts of a key row
 constexpr int CPW = BQ / SM_PARTS;             // query columns per softmax warp
-constexpr int NTHREADS = 32 * (2 + SM_WARPS + 4);
+constexpr int GRAD_WARP = 2 + SM_WARPS + 4;   // issuer of dV, dK, dQ^T
+constexpr int NTHREADS = 32 * (GRAD_WARP + 1);
 constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
 constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
 constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
@@ -98,8 +103,8 @@ constexpr int B_P_EMPTY = B_P_FULL + 2;   // x2
 constexpr int B_DQ_FULL = B_P_EMPTY + 2;
 constexpr int B_DQ_EMPTY = B_DQ_FULL + 1;
 constexpr int B_DKV_FULL = B_DQ_EMPTY + 1;
-constexpr int B_DRAIN = B_DKV_FULL + 1;
-constexpr int NUM_BARS = B_DRAIN + 1;
+constexpr int B_DRAIN = B_DKV_FULL + 1;      // x2: one per issuing thread
+constexpr int NUM_BARS = B_DRAIN + 2;
 // The data fill all but a few bytes of the 227 KB a CTA may use, leaving no
 // room to align the dynamic shared-memory base to 1024 bytes ourselves; the
 // kernel checks at run time that the base is aligned (it is when the kernel
@@ -225,6 +230,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(bar(B_DQ_EMPTY), 4);
         mbar_init(bar(B_DKV_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_DRAIN + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -286,8 +292,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                     if (issued & (1u << s)) drain_wait(bar(B_Q_FULL + s), (ipar >> s) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == GRAD_WARP) {
+        // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
             // S^T, dP^T: M 128 keys, N 64 queries, both operands K-major (K = d).
             constexpr uint32_t id_s = idesc_bf16_f32(BKEYS, BQ);
@@ -298,6 +304,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             // [key][d] tile, B = dS^T read MN-major from its [key][query] tile.
             constexpr uint32_t id_q = idesc_bf16_f32(HD, BQ) | (1u << 15) | (1u << 16);
             bool ok = mbar_wait(bar(B_KV_FULL), 0, abort_flag, p.status, p.timeout_ns);
+            // Descriptors built once; a step adds its constant offset (in
+            // 16-byte units) to the start-address field.
+            constexpr uint32_t U = 16;
+            const uint64_t kd = sdesc_sw128(sK), vd = sdesc_sw128(sV);
+            const uint64_t qd = sdesc_sw128(sQ), dod = sdesc_sw128(sDO);
+            const uint64_t qm = sdesc_sw128_mn(sQ, QBOX_BYTES, 1024), dom = sdesc_sw128_mn(sDO, QBOX_BYTES, 1024);
+            const uint64_t km = sdesc_sw128_mn(sK, KBOX_BYTES, 1024);
+            const uint64_t dstd = sdesc_sw128(sDST), dstm = sdesc_sw128_mn(sDST, KBOX_BYTES, 1024);
             auto issue_s = [&](int it) -> bool {
                 const int st = it % NSTAGE;
                 if (!mbar_wait(bar(B_Q_FULL + st), static_cast<uint32_t>(it / NSTAGE) & 1u, abort_flag,
@@ -307,20 +321,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                                p.timeout_ns))
                     return false;
                 tc_fence_after();
-                const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
+                const uint32_t so = static_cast<uint32_t>(st) * (QT_BYTES / U);
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ++ks) {
-                    const uint32_t a_off = (ks >> 2) * KBOX_BYTES + (ks & 3) * 32;
-                    const uint32_t b_off = (ks >> 2) * QBOX_BYTES + (ks & 3) * 32;
-                    umma_bf16(tmem + COL_S, sdesc_sw128(sK + a_off), sdesc_sw128(q + b_off), id_s,
-                              ks > 0 ? 1u : 0u);
+                    const uint32_t a_off = ((ks >> 2) * KBOX_BYTES + (ks & 3) * 32) / U;
+                    const uint32_t b_off = ((ks >> 2) * QBOX_BYTES + (ks & 3) * 32) / U;
+                    umma_bf16(tmem + COL_S, kd + a_off, qd + so + b_off, id_s, ks > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ++ks) {
-                    const uint32_t a_off = (ks >> 2) * KBOX_BYTES + (ks & 3) * 32;
-                    const uint32_t b_off = (ks >> 2) * QBOX_BYTES + (ks & 3) * 32;
-                    umma_bf16(tmem + COL_DP, sdesc_sw128(sV + a_off), sdesc_sw128(dO + b_off), id_s,
-                              ks > 0 ? 1u : 0u);
+                    const uint32_t a_off = ((ks >> 2) * KBOX_BYTES + (ks & 3) * 32) / U;
+                    const uint32_t b_off = ((ks >> 2) * QBOX_BYTES + (ks & 3) * 32) / U;
+                    umma_bf16(tmem + COL_DP, vd + a_off, dod + so + b_off, id_s, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_S_FULL));
                 return true;
@@ -331,41 +343,47 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 if (!mbar_wait(bar(B_P_FULL + pb), static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.status,
                                p.timeout_ns))
                     return false;
+                tc_fence_after();
+                const uint32_t so = static_cast<uint32_t>(st) * (QT_BYTES / U);
+                const uint32_t po = static_cast<uint32_t>(pb) * (PT_BYTES / U);
+                const uint32_t pt = tmem + (pb ? COL_PT1 : COL_PT0);
+                const uint32_t acc = it > 0 ? 1u : 0u;
+                // dV and dK first: they do not touch dQ^T's TMEM, so they go
+                // out while the dQ warps may still be reading the previous one.
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries (8 packed columns) per UMMA
+                    umma_bf16_ts(tmem + COL_DV, pt + ks * 8, dom + so + (ks * 2048) / U, id_kv, ks > 0 ? 1u : acc);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    umma_bf16(tmem + COL_DK, dstd + po + (ks * 32) / U, qm + so + (ks * 2048) / U, id_kv,
+                              ks > 0 ? 1u : acc);
                 if (!mbar_wait(bar(B_DQ_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
                                p.timeout_ns))
                     return false;
                 tc_fence_after();
-                const uint32_t q = sQ + st * QT_BYTES, dO = sDO + st * QT_BYTES;
-                const uint32_t dst = sDST + pb * PT_BYTES;
-                const uint32_t pt = tmem + (pb ? COL_PT1 : COL_PT0);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries (8 packed columns) per UMMA
-                    umma_bf16_ts(tmem + COL_DV, pt + ks * 8, sdesc_sw128_mn(dO + ks * 2048, QBOX_BYTES, 1024),
-                                 id_kv, (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    umma_bf16(tmem + COL_DK, sdesc_sw128(dst + ks * 32),
-                              sdesc_sw128_mn(q + ks * 2048, QBOX_BYTES, 1024), id_kv,
-                              (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BKEYS / 16; ++ks)  // 16 keys per UMMA
-                    umma_bf16(tmem + COL_DQ, sdesc_sw128_mn(sK + ks * 2048, KBOX_BYTES, 1024),
-                              sdesc_sw128_mn(dst + ks * 2048, KBOX_BYTES, 1024), id_q, ks > 0 ? 1u : 0u);
+                    umma_bf16(tmem + COL_DQ, km + (ks * 2048) / U, dstm + po + (ks * 2048) / U, id_q,
+                              ks > 0 ? 1u : 0u);
                 umma_commit(bar(B_P_EMPTY + pb));
                 umma_commit(bar(B_DQ_FULL));
                 umma_commit(bar(B_Q_EMPTY + st));
                 return true;
             };
-            for (int it = 0; it < n_it && ok; ++it) {
-                ok = issue_s(it);
-                if (ok && it > 0) ok = issue_grad(it - 1);
-            }
-            if (ok && n_it > 0) ok = issue_grad(n_it - 1);
-            if (ok) {
-                umma_commit(bar(B_DKV_FULL));
+            if (warp == 1) {
+                for (int it = 0; it < n_it && ok; ++it) ok = issue_s(it);
+                if (!ok) {
+                    umma_commit(bar(B_DRAIN));
+                    drain_wait(bar(B_DRAIN), 0);
+                }
             } else {
-                umma_commit(bar(B_DRAIN));
-                drain_wait(bar(B_DRAIN), 0);
+                for (int it = 0; it < n_it && ok; ++it) ok = issue_grad(it);
+                if (ok) {
+                    umma_commit(bar(B_DKV_FULL));
+                } else {
+                    umma_commit(bar(B_DRAIN + 1));
+                    drain_wait(bar(B_DRAIN + 1), 0);
+                }
             }
         }
     } else if (warp < 2 + SM_WARPS) {
@@ -406,28 +424,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(bar(B_S_EMPTY));  // S^T, dP^T are in registers
             uint32_t pk[CPW / 2], sk[CPW / 2];
             const int qbase = qb * BQ + hh * CPW;
+            // P^T and dS^T of the warp's CPW queries, masked or not (the mask
+            // test per element costs as much as the rest of the math, so the
+            // blocks that need none take a loop without it).
+            auto grad_cols = [&](auto masked) {
+#pragma unroll
+                for (int v = 0; v < CPW / 4; ++v) {
+                    const float4 l4 = lse4[v], d4 = dd4[v];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], gv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * v + e;
+                        float pp = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[e]));
+                        if (decltype(masked)::value) {
+                            const int qpos = qbase + c;
+                            if (!(kpos <= qpos && qpos < p.seq)) pp = 0.0f;
+                        }
+                        pv[e] = pp;
+                        gv[e] = pp * (__uint_as_float(dp[c]) - dv[e]);
+                    }
+                    pk[2 * v] = pack_bf16x2(pv[0], pv[1]);
+                    pk[2 * v + 1] = pack_bf16x2(pv[2], pv[3]);
+                    sk[2 * v] = pack_bf16x2(gv[0], gv[1]);
+                    sk[2 * v + 1] = pack_bf16x2(gv[2], gv[3]);
+                }
+            };
             // Blocks wholly below the diagonal and inside the sequence need no mask.
             const bool unmasked = qb * BQ >= k0 + BKEYS - 1 && qb * BQ + BQ <= p.seq;
-#pragma unroll
-            for (int v = 0; v < CPW / 4; ++v) {
-                const float4 l4 = lse4[v], d4 = dd4[v];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                float pv[4], gv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 4 * v + e;
-                    const float pp = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[e]));
-                    const float gg = pp * (__uint_as_float(dp[c]) - dv[e]);
-                    const int qpos = qbase + c;
-                    const bool valid = unmasked || (kpos <= qpos && qpos < p.seq);
-                    pv[e] = valid ? pp : 0.0f;
-                    gv[e] = valid ? gg : 0.0f;
-                }
-                pk[2 * v] = pack_bf16x2(pv[0], pv[1]);
-                pk[2 * v + 1] = pack_bf16x2(pv[2], pv[3]);
-                sk[2 * v] = pack_bf16x2(gv[0], gv[1]);
-                sk[2 * v + 1] = pack_bf16x2(gv[2], gv[3]);
-            }
+            if (unmasked) grad_cols(std::false_type{});
+            else grad_cols(std::true_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_EMPTY + st));  // statistics read
             // The gradient MMAs of step it - 2 are done with this P^T / dS^T buffer.
@@ -490,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             }
         }
     } else {
-        // ------------------------------------------------------------ dQ accumulation
+        // ------------------------------------------------------------ dQ accumulation (warps 10-13)
         // Each warp owns 32 head dimensions: its [64 queries][32 d] slice of
         // dQ^T goes (times 1/sqrt(d)) to a row-major fp32 box in shared
         // memory, which one TMA reduce-add adds to the accumulator.
