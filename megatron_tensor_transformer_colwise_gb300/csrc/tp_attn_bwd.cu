@@ -14,7 +14,7 @@
 // Kernels (one call = three launches):
 //   attn_bwd_prep_kernel  D per (head, sequence, row), zero in the padding
 //                         of each sequence to a multiple of 64 rows, and a
-//                         zeroed fp32 dQ accumulator.
+//                         zeroed fp32 dQ accumulator (one CTA per token row).
 //   attn_bwd_kernel       one CTA per (128-key block, KV head, sequence),
 //                         longest (earliest) key blocks first, 15 warps:
 //     warp 0     TMA: K and V of the key block once; then, per step, Q and
@@ -571,37 +571,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
 // D[(j batch + b) seq_pad + pos] = sum_c dO[row][j d + c] O[row][j d + c]
 // (0 for pos >= seq), and dQ accumulator row segment [j d, j d + d) = 0.
 // One warp per (head, sequence, padded position).
-constexpr int PREP_WARPS = 8;
+// D = rowsum(dO (.) O) per (head, sequence, position) and the zeroed fp32 dQ
+// accumulator.  One CTA per token row of a sequence padded to seq_pad (all
+// heads of the row, 16-byte loads): a head's HD = 128 values are 16 chunks
+// of 8, summed across a half-warp.  Padding positions get D = 0.
+constexpr int PREP_THREADS = 256;
+constexpr int PREP_MAX_HEADS = 1024;
 
-__global__ void __launch_bounds__(PREP_WARPS * 32) attn_bwd_prep_kernel(
+__global__ void __launch_bounds__(PREP_THREADS) attn_bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O, long long ld, int heads,
-    int d, int batch, int seq, long long seq_pad, float* __restrict__ dstat, float* __restrict__ dq,
-    long long ld_dq) {
-    const long long idx = static_cast<long long>(blockIdx.x) * PREP_WARPS + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const long long total = static_cast<long long>(heads) * batch * seq_pad;
-    if (idx >= total) return;
-    const long long per_head = static_cast<long long>(batch) * seq_pad;
-    const int j = static_cast<int>(idx / per_head);
-    const long long r = idx - j * per_head;
-    const int b = static_cast<int>(r / seq_pad);
-    const int pos = static_cast<int>(r - static_cast<long long>(b) * seq_pad);
-    float acc = 0.0f;
-    if (pos < seq) {
-        const long long row = static_cast<long long>(b) * seq + pos;
-        const __nv_bfloat16* a = dO + row * ld + static_cast<long long>(j) * d;
-        const __nv_bfloat16* o = O + row * ld + static_cast<long long>(j) * d;
-        for (int c = lane * 2; c < d; c += 64) {
-            const float2 x = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(a + c));
-            const float2 y = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(o + c));
-            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-        }
-        float* z = dq + row * ld_dq + static_cast<long long>(j) * d;
-        for (int c = lane * 4; c < d; c += 128) *reinterpret_cast<float4*>(z + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    int batch, int seq, long long seq_pad, float* __restrict__ dstat, float* __restrict__ dq, long long ld_dq) {
+    __shared__ float dsum[PREP_MAX_HEADS];
+    const long long rb = blockIdx.x;
+    const int b = static_cast<int>(rb / seq_pad);
+    const int pos = static_cast<int>(rb - static_cast<long long>(b) * seq_pad);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const bool real = pos < seq;
+    const long long row = static_cast<long long>(b) * seq + pos;
+    const int nchunk = heads * (HD / 8);
+    if (real) {
+        const __nv_bfloat16* a = dO + row * ld;
+        const __nv_bfloat16* o = O + row * ld;
+        for (int c0 = 0; c0 < nchunk; c0 += PREP_THREADS) {
+            const int c = c0 + tid;
+            float acc = 0.0f;
+            if (c < nchunk) {
+                const uint4 x = __ldg(reinterpret_cast<const uint4*>(a + static_cast<long long>(c) * 8));
+                const uint4 y = __ldg(reinterpret_cast<const uint4*>(o + static_cast<long long>(c) * 8));
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) dstat[idx] = acc;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 u = unpack_bf16x2(xs[e]), v = unpack_bf16x2(ys[e]);
+                    acc = fmaf(u.x, v.x, fmaf(u.y, v.y, acc));
+                }
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if ((lane & 15) == 0 && c < nchunk) dsum[c / (HD / 8)] = acc;
+        }
+        float4* z = reinterpret_cast<float4*>(dq + row * ld_dq);
+        for (int e = tid; e < heads * (HD / 4); e += PREP_THREADS) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    for (int j = tid; j < heads; j += PREP_THREADS)
+        dstat[(static_cast<long long>(j) * batch + b) * seq_pad + pos] = real ? dsum[j] : 0.0f;
 }
 
 // out[row][c] = bf16(acc[row][c]) for c < n (n % 8 == 0).
@@ -661,11 +674,14 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
     const long long tokens = static_cast<long long>(a.batch) * a.seq;
     // 1. D and a zeroed dQ accumulator.
     {
-        const long long total = static_cast<long long>(a.heads) * a.batch * a.seq_pad;
-        const long long blocks = (total + PREP_WARPS - 1) / PREP_WARPS;
-        attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), PREP_WARPS * 32, 0, stream>>>(
+        if (a.heads > PREP_MAX_HEADS) {
+            if (err) *err = "the attention backward supports at most 1024 query heads";
+            return TP_ERR_UNSUPPORTED;
+        }
+        const long long blocks = static_cast<long long>(a.batch) * a.seq_pad;
+        attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), PREP_THREADS, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16*>(a.dO), reinterpret_cast<const __nv_bfloat16*>(a.O),
-            a.ld_do, a.heads, HD, a.batch, a.seq, a.seq_pad, a.dstat, a.dq, a.ld_dq);
+            a.ld_do, a.heads, a.batch, a.seq, a.seq_pad, a.dstat, a.dq, a.ld_dq);
         int rc = check("attention backward prep kernel", err);
         if (rc) return rc;
     }
