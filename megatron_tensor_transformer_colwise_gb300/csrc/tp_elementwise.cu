@@ -227,15 +227,26 @@ __global__ void __launch_bounds__(SS_WARPS * 32) row_sumsq_kernel(const __nv_bfl
     if (row >= rows) return;
     const __nv_bfloat16* xr = x + row * h;
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int v = lane; v < (h >> 3); v += 32) {
-        const uint4 u = *reinterpret_cast<const uint4*>(xr + v * 8);  // kept in L2 for the GEMM
+    auto add = [&](const uint4& u) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = unpack_bf16x2(w[e]);
             acc[e] = fmaf(f.x, f.x, fmaf(f.y, f.y, acc[e]));
         }
+    };
+    // Four 16-byte loads in flight per lane (plain loads: the rows stay in
+    // L2 for the GEMM that follows).
+    const int nv = h >> 3;
+    int v = lane;
+    for (; v + 96 < nv; v += 128) {
+        uint4 u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) u[k] = *reinterpret_cast<const uint4*>(xr + (v + 32 * k) * 8);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) add(u[k]);
     }
+    for (; v < nv; v += 32) add(*reinterpret_cast<const uint4*>(xr + v * 8));
     float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
