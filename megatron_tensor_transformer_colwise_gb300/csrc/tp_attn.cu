@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <string>
 
@@ -66,10 +67,12 @@ enum {
     B_V_EMPTY = 7,   // x2
     B_S_FULL = 9,    // x2 (S / P buffers in TMEM)
     B_PV_DONE = 11,  // x2: the PV MMA that read P from buffer i has completed
-    B_P_FULL = 13,
+    B_P_FULL = 13,   // x2 (per S buffer): its 4 softmax warps wrote P
     B_O_FULL = 15,
     B_DRAIN = 16,    // x2: one per issuing thread
-    NUM_BARS = 18
+    B_Q_EMPTY = 18,  // the item's S products are done with Q
+    B_O_EMPTY = 19,  // the item's epilogue has read O (4 softmax warps)
+    NUM_BARS = 20
 };
 
 // Per-CTA dynamic shared memory when two CTAs share an SM: (228 KB - 2 x
@@ -124,6 +127,42 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 
+// One work item: 128 query rows (tile qb) of query head j in sequence b.
+// Items are numbered longest first: item w has tile nqb - 1 - w / (heads *
+// batch), so each round of gridDim.x items has rows of one length.
+struct Item {
+    int q0, nkb, tok0, j, b;
+    int qcol, kcol, vcol;
+};
+
+template <int D>
+__device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
+    const int nqb = (p.seq + QB - 1) / QB;
+    const int hb = p.heads * p.batch;
+    const int qi = w / hb;
+    const int r = w - qi * hb;
+    Item x;
+    x.j = r % p.heads;
+    x.b = r / p.heads;
+    const int qb = nqb - 1 - qi;
+    const int shard = x.j / p.heads_per_shard;
+    const int jl = x.j - shard * p.heads_per_shard;
+    const int g = x.j / (p.heads / p.kv_heads);
+    const int kv0 = (p.kv_heads >= p.t) ? shard * (p.kv_heads / p.t) : (shard * p.kv_heads) / p.t;
+    x.qcol = shard * p.shard_w + jl * D;
+    x.kcol = shard * p.shard_w + p.q_w + (g - kv0) * D;
+    x.vcol = x.kcol + p.kv_w;
+    x.tok0 = x.b * p.seq;
+    x.q0 = qb * QB;
+    // causal: keys 0 .. q0+127, and never past the sequence
+    x.nkb = min((x.q0 + QB + KB - 1) / KB, (p.seq + KB - 1) / KB);
+    return x;
+}
+
+// Persistent: CTA c takes items c, c + gridDim.x, ...  Every role walks the
+// same item list; K/V ring stages, S buffers and their barrier phases run on
+// one block count across items, so the next item's Q and first K/V blocks
+// load while the current item finishes.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_constant__ AttnParams p) {
     using L = Layout<D>;
@@ -142,25 +181,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         return;  // the aligned layout does not fit: nothing was touched
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nqb = (p.seq + QB - 1) / QB;
-    const int qb = nqb - 1 - static_cast<int>(blockIdx.x);  // longest rows first
-    const int j = blockIdx.y;
-    const int b = blockIdx.z;
-    const int shard = j / p.heads_per_shard;
-    const int jl = j - shard * p.heads_per_shard;
-    const int g = j / (p.heads / p.kv_heads);
-    const int kv0 = (p.kv_heads >= p.t) ? shard * (p.kv_heads / p.t) : (shard * p.kv_heads) / p.t;
-    const int gl = g - kv0;
-    const int qcol = shard * p.shard_w + jl * D;
-    const int kcol = shard * p.shard_w + p.q_w + gl * D;
-    const int vcol = kcol + p.kv_w;
-    const int tok0 = b * p.seq;
-    const int q0 = qb * QB;
-    // causal: keys 0 .. q0+127, and never past the sequence
-    const int nkb = min((q0 + QB + KB - 1) / KB, (p.seq + KB - 1) / KB);
+    const int n_items = ((p.seq + QB - 1) / QB) * p.heads * p.batch;
+    const int w0 = static_cast<int>(blockIdx.x), dw = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q_FULL), 1);
+        mbar_init(bar(B_Q_EMPTY), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
@@ -169,8 +195,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
+        // One P_FULL per S buffer: a warp a block ahead of the others
+        // arrives on the other barrier, never on the phase they complete.
         mbar_init(bar(B_P_FULL), 4);
+        mbar_init(bar(B_P_FULL + 1), 4);
         mbar_init(bar(B_O_FULL), 1);
+        mbar_init(bar(B_O_EMPTY), 4);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_DRAIN + 1), 1);
         *abort_flag = 0;
@@ -191,27 +221,26 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // Order: Q, K0, then for each block kb: K(kb+1), V(kb).  Both rings
-        // are 2-stage, so a V load waits for the PV MMA two blocks back and
-        // its latency stays off the PV critical path.
+        // Per item: Q (once the previous item's S products are done with
+        // it), K0, then for each block kb: K(kb+1), V(kb).  Both rings are
+        // 2-stage, so a V load waits for the PV MMA two blocks back and its
+        // latency stays off the PV critical path.
         if (lane == 0) {
-            bool ok = true;
-            uint32_t kissued = 0, kpar = 0, vissued = 0, vpar = 0;
-            mbar_arrive_expect_tx(bar(B_Q_FULL), L::QT);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_2d(sQ + c * QBOX, &p.map_q, bar(B_Q_FULL), qcol + 64 * c, tok0 + q0);
-            auto load_kv = [&](int kb, bool is_v) -> bool {
-                const int st = kb & 1;
-                const uint32_t ph = (kb >> 1) & 1;
+            bool ok = true, q_issued = false;
+            uint32_t kissued = 0, kpar = 0, vissued = 0, vpar = 0, qpar = 0;
+            int gb = 0;  // blocks of earlier items
+            auto load_kv = [&](const Item& x, int kb, bool is_v) -> bool {
+                const int n = gb + kb;  // ring position
+                const int st = n & 1;
+                const uint32_t ph = static_cast<uint32_t>(n >> 1) & 1u;
                 const int e = is_v ? B_V_EMPTY : B_K_EMPTY, f = is_v ? B_V_FULL : B_K_FULL;
                 if (!mbar_wait(bar(e + st), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) return false;
                 mbar_arrive_expect_tx(bar(f + st), L::KT);
                 const uint32_t dst = (is_v ? sV : sK) + st * L::KT;
-                const int col = is_v ? vcol : kcol;
+                const int col = is_v ? x.vcol : x.kcol;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(dst + c * KBOX, &p.map_kv, bar(f + st), col + 64 * c, tok0 + kb * KB);
+                    tma_load_2d(dst + c * KBOX, &p.map_kv, bar(f + st), col + 64 * c, x.tok0 + kb * KB);
                 if (is_v) {
                     vissued |= 1u << st;
                     vpar = (vpar & ~(1u << st)) | (ph << st);
@@ -221,13 +250,29 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 }
                 return true;
             };
-            ok = load_kv(0, false);
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-                if (kb + 1 < nkb && !(ok = load_kv(kb + 1, false))) break;
-                ok = load_kv(kb, true);
+            int li = 0;
+            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+                const Item x = item_of<D>(p, w);
+                if (li > 0 && !mbar_wait(bar(B_Q_EMPTY), static_cast<uint32_t>(li - 1) & 1u, abort_flag, p.status,
+                                         p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_Q_FULL), L::QT);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(sQ + c * QBOX, &p.map_q, bar(B_Q_FULL), x.qcol + 64 * c, x.tok0 + x.q0);
+                q_issued = true;
+                qpar = static_cast<uint32_t>(li) & 1u;
+                ok = load_kv(x, 0, false);
+                for (int kb = 0; kb < x.nkb && ok; ++kb) {
+                    if (kb + 1 < x.nkb && !(ok = load_kv(x, kb + 1, false))) break;
+                    ok = load_kv(x, kb, true);
+                }
+                gb += x.nkb;
             }
             if (!ok) {
-                drain_wait(bar(B_Q_FULL), 0);
+                if (q_issued) drain_wait(bar(B_Q_FULL), qpar);
                 for (int s = 0; s < 2; ++s) {
                     if (kissued & (1u << s)) drain_wait(bar(B_K_FULL + s), (kpar >> s) & 1u);
                     if (vissued & (1u << s)) drain_wait(bar(B_V_FULL + s), (vpar >> s) & 1u);
@@ -242,33 +287,43 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             // 16-byte units) to the start-address field.
             const uint64_t qdesc = sdesc_sw128(sQ);
             const uint64_t kdesc0 = sdesc_sw128(sK), kdesc1 = sdesc_sw128(sK + L::KT);
-            bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, p.status, p.timeout_ns);
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-                const int st = kb & 1;
-                // Buffer st held S and then P of block kb - 2: its PV must
-                // have read that P before this S overwrites it.
-                if (kb >= 2 && !mbar_wait(bar(B_PV_DONE + st), static_cast<uint32_t>((kb - 2) >> 1) & 1u, abort_flag,
-                                          p.status, p.timeout_ns)) {
+            bool ok = true;
+            int gb = 0, li = 0;
+            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+                const int nkb = item_of<D>(p, w).nkb;
+                if (!mbar_wait(bar(B_Q_FULL), static_cast<uint32_t>(li) & 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(bar(B_K_FULL + st), static_cast<uint32_t>(kb >> 1) & 1u, abort_flag, p.status,
-                               p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + st * KB;
-                const uint64_t kdesc = st ? kdesc1 : kdesc0;
+                for (int kb = 0; kb < nkb && ok; ++kb, ++gb) {
+                    const int st = gb & 1;
+                    // Buffer st held S and then P of block gb - 2: its PV must
+                    // have read that P before this S overwrites it.
+                    if (gb >= 2 && !mbar_wait(bar(B_PV_DONE + st), static_cast<uint32_t>((gb - 2) >> 1) & 1u,
+                                              abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(bar(B_K_FULL + st), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag, p.status,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + st * KB;
+                    const uint64_t kdesc = st ? kdesc1 : kdesc0;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    constexpr uint32_t unit = 16;
-                    const uint32_t a_off = ((ks >> 2) * QBOX + (ks & 3) * 32) / unit;
-                    const uint32_t b_off = ((ks >> 2) * KBOX + (ks & 3) * 32) / unit;
-                    umma_bf16(d_tmem, qdesc + a_off, kdesc + b_off, idesc_s, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        constexpr uint32_t unit = 16;
+                        const uint32_t a_off = ((ks >> 2) * QBOX + (ks & 3) * 32) / unit;
+                        const uint32_t b_off = ((ks >> 2) * KBOX + (ks & 3) * 32) / unit;
+                        umma_bf16(d_tmem, qdesc + a_off, kdesc + b_off, idesc_s, ks > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(B_K_EMPTY + st));
+                    umma_commit(bar(B_S_FULL + st));
                 }
-                umma_commit(bar(B_K_EMPTY + st));
-                umma_commit(bar(B_S_FULL + st));
+                // Q may be reloaded once this item's S products are done.
+                if (ok) umma_commit(bar(B_Q_EMPTY));
             }
             if (!ok) {
                 umma_commit(bar(B_DRAIN));
@@ -281,28 +336,42 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(QB, D);
             const uint64_t vdesc0 = sdesc_sw128_mn(sV, KBOX, 1024), vdesc1 = sdesc_sw128_mn(sV + L::KT, KBOX, 1024);
             bool ok = true;
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-                const int vst = kb & 1;
-                if (!mbar_wait(bar(B_P_FULL), kb & 1, abort_flag, p.status, p.timeout_ns) ||
-                    !mbar_wait(bar(B_V_FULL + vst), (kb >> 1) & 1, abort_flag, p.status, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // P of block kb: bf16 in the first KB/2 columns of S buffer
-                // kb & 1, 16 keys (8 columns) per UMMA.
-                const uint64_t vdesc = vst ? vdesc1 : vdesc0;
-                const uint32_t pcol = tmem + (kb & 1) * KB;
-                const uint32_t acc0 = kb > 0 ? 1u : 0u;
+            int gb = 0, li = 0;
+            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+                const int nkb = item_of<D>(p, w).nkb;
+                for (int kb = 0; kb < nkb && ok; ++kb, ++gb) {
+                    const int vst = gb & 1;
+                    if (!mbar_wait(bar(B_P_FULL + vst), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag, p.status,
+                                   p.timeout_ns) ||
+                        !mbar_wait(bar(B_V_FULL + vst), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag, p.status,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // The first PV of an item overwrites O: the previous
+                    // item's epilogue must have read it.
+                    if (kb == 0 && li > 0 &&
+                        !mbar_wait(bar(B_O_EMPTY), static_cast<uint32_t>(li - 1) & 1u, abort_flag, p.status,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // P of block gb: bf16 in the first KB/2 columns of S buffer
+                    // gb & 1, 16 keys (8 columns) per UMMA.
+                    const uint64_t vdesc = vst ? vdesc1 : vdesc0;
+                    const uint32_t pcol = tmem + vst * KB;
+                    const uint32_t acc0 = kb > 0 ? 1u : 0u;
 #pragma unroll
-                for (int ks = 0; ks < KB / 16; ++ks)
-                    umma_bf16_ts(tmem + 2 * KB, pcol + ks * 8, vdesc + (ks * 16 * 128) / 16, idesc_o, ks > 0 ? 1u : acc0);
-                umma_commit(bar(B_V_EMPTY + vst));
-                umma_commit(bar(B_PV_DONE + (kb & 1)));
+                    for (int ks = 0; ks < KB / 16; ++ks)
+                        umma_bf16_ts(tmem + 2 * KB, pcol + ks * 8, vdesc + (ks * 16 * 128) / 16, idesc_o,
+                                     ks > 0 ? 1u : acc0);
+                    umma_commit(bar(B_V_EMPTY + vst));
+                    umma_commit(bar(B_PV_DONE + vst));
+                }
+                if (ok) umma_commit(bar(B_O_FULL));
             }
-            if (ok) {
-                umma_commit(bar(B_O_FULL));
-            } else {
+            if (!ok) {
                 umma_commit(bar(B_DRAIN + 1));
                 drain_wait(bar(B_DRAIN + 1), 0);
             }
@@ -311,13 +380,104 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         // ---------------------------------------------------------- softmax / epilogue
         const int q = warp & 3;  // TMEM lane quadrant
         const int r = q * 32 + lane;
-        const int qpos = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        float m_ref = -INFINITY, l_sum = 0.0f;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb & 1;
-            const bool got = mbar_wait(bar(B_S_FULL + st), (kb >> 1) & 1, abort_flag, p.status,
+        int gb = 0, li = 0;
+        for (int w = w0; w < n_items && ok; w += dw, ++li) {
+            const Item x = item_of<D>(p, w);
+            const int q0 = x.q0;
+            const int qpos = q0 + r;
+            float m_ref = -INFINITY, l_sum = 0.0f;
+            for (int kb = 0; kb < x.nkb; ++kb, ++gb) {
+                const int st = gb & 1;
+                const bool got = mbar_wait(bar(B_S_FULL + st), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag,
+                                           p.status, p.timeout_ns);
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[KB];
+#pragma unroll
+                for (int c = 0; c < KB / 32; ++c)
+                    tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+                tmem_ld_wait();
+
+                const int k0 = kb * KB;
+                if (k0 + KB - 1 > q0 || k0 + KB > p.seq) {
+#pragma unroll
+                    for (int c = 0; c < KB; ++c) {
+                        const int key = k0 + c;
+                        if (key > qpos || key >= p.seq) s[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // Row max with 8 independent chains (one softmax warp per SM
+                // sub-partition and CTA leaves little to hide a serial chain).
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+#pragma unroll
+                for (int c = 8; c < KB; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[c + e]));
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mxs = mx * p.scale_log2;
+                float alpha = 1.0f;
+                bool rescale = false;
+                if (mxs > m_ref + RESCALE_THRESHOLD) {
+                    alpha = exp2f(m_ref - mxs);  // 0 on the first block
+                    m_ref = mxs;
+                    rescale = kb > 0;
+                }
+                float sum8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
+                uint32_t pk[KB / 2];
+#pragma unroll
+                for (int c = 0; c < KB / 2; ++c) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
+                    sum8[c & 7] += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                l_sum = l_sum * alpha + sum;
+
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O is rescaled in place: the PV of the previous block must be done.
+                    const int pb = gb - 1;
+                    const bool got2 = mbar_wait(bar(B_PV_DONE + (pb & 1)), static_cast<uint32_t>(pb >> 1) & 1u,
+                                                abort_flag, p.status, p.timeout_ns);
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, got2)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        const uint32_t ta = tmem + lane_off + 2 * KB + c * 32;
+                        tmem_ld32(ta, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(ta, o);
+                    }
+                    tmem_st_wait();
+                }
+                // P row r over its S row in TMEM: 64 keys as 32 packed columns.
+                tmem_st32(tmem + lane_off + st * KB, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + st));
+            }
+            if (!ok) break;
+            const bool got = mbar_wait(bar(B_O_FULL), static_cast<uint32_t>(li) & 1u, abort_flag, p.status,
                                        p.timeout_ns);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) {
@@ -325,113 +485,33 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 break;
             }
             tc_fence_after();
-            uint32_t s[KB];
-#pragma unroll
-            for (int c = 0; c < KB / 32; ++c)
-                tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-            tmem_ld_wait();
-
-            const int k0 = kb * KB;
-            if (k0 + KB - 1 > q0 || k0 + KB > p.seq) {
-#pragma unroll
-                for (int c = 0; c < KB; ++c) {
-                    const int key = k0 + c;
-                    if (key > qpos || key >= p.seq) s[c] = __float_as_uint(-INFINITY);
-                }
-            }
-            // Row max with 8 independent chains (one softmax warp per SM
-            // sub-partition and CTA leaves little to hide a serial chain).
-            float mx8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
-#pragma unroll
-            for (int c = 8; c < KB; c += 8)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[c + e]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float mxs = mx * p.scale_log2;
-            float alpha = 1.0f;
-            bool rescale = false;
-            if (mxs > m_ref + RESCALE_THRESHOLD) {
-                alpha = exp2f(m_ref - mxs);  // 0 on the first block
-                m_ref = mxs;
-                rescale = kb > 0;
-            }
-            float sum8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
-            uint32_t pk[KB / 2];
-#pragma unroll
-            for (int c = 0; c < KB / 2; ++c) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
-                sum8[c & 7] += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-            l_sum = l_sum * alpha + sum;
-
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O is rescaled in place: the PV of the previous block must be done.
-                const int pb = kb - 1;
-                const bool got2 = mbar_wait(bar(B_PV_DONE + (pb & 1)), static_cast<uint32_t>(pb >> 1) & 1u,
-                                            abort_flag, p.status, p.timeout_ns);
-                __syncwarp();
-                if (!__all_sync(0xffffffffu, got2)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            const float inv = 1.0f / l_sum;
+            if (p.lse && qpos < p.seq)
+                p.lse[(static_cast<long long>(x.j) * p.batch + x.b) * p.seq_pad + qpos] = m_ref + log2f(l_sum);
+            __nv_bfloat16* orow = p.o + static_cast<long long>(x.tok0 + qpos) * p.ld_o +
+                                  static_cast<long long>(x.j) * D;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    const uint32_t ta = tmem + lane_off + 2 * KB + c * 32;
-                    tmem_ld32(ta, o);
-                    tmem_ld_wait();
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + 2 * KB + c * 32, o);
+                tmem_ld_wait();
+                if (qpos < p.seq) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(ta, o);
-                }
-                tmem_st_wait();
-            }
-            // P row r over its S row in TMEM: 64 keys as 32 packed columns.
-            tmem_st32(tmem + lane_off + st * KB, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL));
-        }
-        if (ok) {
-            const bool got = mbar_wait(bar(B_O_FULL), 0, abort_flag, p.status, p.timeout_ns);
-            __syncwarp();
-            if (__all_sync(0xffffffffu, got)) {
-                tc_fence_after();
-                const float inv = 1.0f / l_sum;
-                if (p.lse && qpos < p.seq)
-                    p.lse[(static_cast<long long>(j) * p.batch + b) * p.seq_pad + qpos] = m_ref + log2f(l_sum);
-                __nv_bfloat16* orow = p.o + static_cast<long long>(tok0 + qpos) * p.ld_o +
-                                      static_cast<long long>(j) * D;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + 2 * KB + c * 32, o);
-                    tmem_ld_wait();
-                    if (qpos < p.seq) {
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        uint32_t wv[4];
 #pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * inv,
-                                                   __uint_as_float(o[g8 * 8 + 2 * e + 1]) * inv);
-                            *reinterpret_cast<uint4*>(orow + c * 32 + g8 * 8) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[g8 * 8 + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + g8 * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
             }
+            // O is in registers and written: the next item's first PV may
+            // overwrite it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
         }
     }
     __syncwarp();
@@ -502,7 +582,11 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
         }
         configured[dev] = true;
     }
-    dim3 grid((a.seq + QB - 1) / QB, a.heads, a.batch);
+    // Persistent grid: two CTAs per SM, or fewer when there are fewer items.
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+    const long long n_items = static_cast<long long>((a.seq + QB - 1) / QB) * a.heads * a.batch;
+    dim3 grid(static_cast<unsigned>(std::min<long long>(n_items, 2LL * sms)), 1, 1);
     attn_tc_kernel<D><<<grid, NTHREADS, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
