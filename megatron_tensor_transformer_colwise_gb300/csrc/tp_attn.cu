@@ -11,9 +11,11 @@
 // (key position <= query position) within each sequence, fp32 softmax with
 // a running maximum subtracted, no dropout, no rotary embedding.
 //
-// One CTA per (128 query rows, query head, sequence), 7 warps, two CTAs
-// resident per SM (256 TMEM columns and ~97 KB of shared memory each), so
-// one CTA's softmax overlaps the other's tensor-core work:
+// Work item: 128 query rows of one query head and sequence.  A persistent
+// grid of two CTAs per SM (7 warps, 256 TMEM columns and ~97 KB of shared
+// memory each) walks the items longest first, so one CTA's softmax overlaps
+// the other's tensor-core work and the next item's loads overlap the
+// current item's last blocks:
 //   warp 0      TMA: Q once, then K and V blocks of 64 keys (2-stage rings,
 //               K one block ahead) from the shard-blocked QKV buffer.
 //   warp 1      TMEM owner and S issuer: S = Q K^T (128 x 64, fp32, two TMEM
