@@ -165,7 +165,9 @@ Layout layout_of(const tp_plan_s* p, int op) {
             L.partials = align_up(static_cast<size_t>(p->t) * M * p->h * partial_elem_bytes(p));
             if (p->cfg.sequence_parallel) L.full = align_up(M * p->h * 2);
         } else {
-            L.ss = align_up(2 * M * sizeof(float));  // folded RMSNorm statistics
+            // Folded RMSNorm statistics: x's row sums of squares, then h1's
+            // per 128-column slice of the o_proj output.
+            L.ss = align_up((1 + (p->h + 127) / 128) * M * sizeof(float));
         }
     }
     return L;
@@ -195,7 +197,7 @@ int run(int rc, const std::string& err) {
 // ---- building blocks (arguments already validated) ----
 
 int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3, void* Y,
-               cudaStream_t s, const float* row_ss = nullptr, void* UG = nullptr) {
+               cudaStream_t s, const float* row_ss = nullptr, void* UG = nullptr, int row_ss_parts = 1) {
     tpi::GemmArgs g;
     g.mode = (p->cfg.act == TP_ACT_SWIGLU) ? tpi::GEMM_COL_SWIGLU : tpi::GEMM_COL_ACT;
     g.act = p->cfg.act;
@@ -216,6 +218,7 @@ int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3
     g.ldaux = (p->cfg.act == TP_ACT_SWIGLU ? 2 : 1) * p->f;
     g.n_half = p->f;
     g.row_ss = row_ss;
+    g.row_ss_parts = row_ss_parts;
     g.inv_h = 1.0f / static_cast<float>(p->h);
     g.eps = p->cfg.rms_eps;
     g.status = p->status;
@@ -1084,10 +1087,10 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
         // RMSNorm is folded into the GEMMs: a unit-gain norm is a per-row
         // scale, so RMSNorm(x) W^T = rsqrt(mean(x^2) + eps) * (x W^T).  The
         // row statistic of x comes from one read-only pass, that of h1 from
-        // the o_proj epilogue (which also clears nothing: ss2 is zeroed by
-        // the first pass).
+        // the o_proj epilogue as one partial per 128-column slice, summed
+        // in a fixed order by the W1/W3 GEMM.
         mark(s);
-        if ((rc = run(tpi::row_sumsq_launch(X, plan->M, (int)plan->h, ss1, ss2, s, &err), err))) return rc;
+        if ((rc = run(tpi::row_sumsq_launch(X, plan->M, (int)plan->h, ss1, nullptr, s, &err), err))) return rc;
         mark(s);
         if ((rc = do_qkv(plan, X, w->Wq, w->Wk, w->Wv, QKV, s, ss1))) return rc;
         mark(s);
@@ -1097,7 +1100,8 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
         if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s, ss2)))
             return rc;
         mark(s);
-        if ((rc = do_colwise(plan, h1, w->W1, w->W3, Yb, s, ss2))) return rc;
+        if ((rc = do_colwise(plan, h1, w->W1, w->W3, Yb, s, ss2, nullptr, static_cast<int>((plan->h + 127) / 128))))
+            return rc;
         mark(s);
         // y = h1 + sum_i act(xn A_i) B_i.
         if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s))) return rc;

@@ -129,8 +129,9 @@ struct GemmParams {
     const __nv_bfloat16* bias;
     const __nv_bfloat16* residual;
     long long ldr;
-    const float* row_ss;  // colwise: scale row by rsqrt(row_ss * inv_h + eps)
-    float* ss_out;        // ROW_FUSED: += sum of squares of the row's bf16 outputs
+    const float* row_ss;  // colwise: scale row by rsqrt(sum of row_ss_parts partials * inv_h + eps)
+    int row_ss_parts;     // partials of row_ss, M apart
+    float* ss_out;        // ROW_FUSED: sum of squares of the row's bf16 outputs per 128-column slice
     float inv_h, eps;
     // Backward modes (see tpi::GemmArgs).
     const __nv_bfloat16* aux;  // BWD_ACT: saved pre-activations U (| G)
@@ -677,6 +678,13 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
                 }
             }
         }
+        // The row's sum of squares over each 128-column slice goes out once,
+        // when the slice's last chunk is done.
+        if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out && ((c & 3) == 3 || col0 + 32 >= p.N || c + 1 == cb + CPW)) {
+            const int slice = col0 >> 7;
+            if (row_ok) p.ss_out[static_cast<long long>(slice) * p.M + row] = ssq;
+            ssq = 0.0f;
+        }
     }
 }
 
@@ -717,8 +725,11 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         tc_fence_after();
         // Folded RMSNorm of the A rows (colwise modes): per-row scale.
         float rs = 1.0f;
-        if (MODE != tpi::GEMM_ROW_FUSED && MODE != tpi::GEMM_ROW_PARTIAL && p.row_ss && row_ok)
-            rs = rsqrtf(p.row_ss[row] * p.inv_h + p.eps);
+        if (MODE != tpi::GEMM_ROW_FUSED && MODE != tpi::GEMM_ROW_PARTIAL && p.row_ss && row_ok) {
+            float ss = 0.0f;
+            for (int i = 0; i < p.row_ss_parts; ++i) ss += p.row_ss[static_cast<long long>(i) * p.M + row];
+            rs = rsqrtf(ss * p.inv_h + p.eps);
+        }
         float ssq = 0.0f;
         const uint32_t t0 = tmem_base + acc * BNT + (static_cast<uint32_t>(q * 32) << 16);
         uint32_t r[32];
@@ -830,7 +841,6 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         } else {
             std_tile<MODE, TP_ACT_NONE, CPW, BNT>(p, t0, cb, nb, s_grid, row, row_ok, rs, ssq);
         }
-        if (MODE == tpi::GEMM_ROW_FUSED && p.ss_out && row_ok) atomicAdd(p.ss_out + row, ssq);
         tc_fence_before();
         __syncwarp();
         // Release the accumulator: the leader's MMA waits for the epilogue
@@ -1026,6 +1036,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     p.residual = reinterpret_cast<const __nv_bfloat16*>(a.residual);
     p.ldr = a.ldr;
     p.row_ss = a.row_ss;
+    p.row_ss_parts = a.row_ss_parts > 0 ? a.row_ss_parts : 1;
     p.ss_out = a.ss_out;
     p.inv_h = a.inv_h;
     p.eps = a.eps;

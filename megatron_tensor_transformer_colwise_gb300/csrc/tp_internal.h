@@ -60,10 +60,14 @@ struct GemmArgs {
     const void* residual = nullptr;
     int64_t ldr = 0;
     // RMSNorm folded into the GEMMs (unit gain): colwise modes scale each
-    // accumulator row by rsqrt(row_ss[row] * inv_h + eps) when row_ss is set;
-    // GEMM_ROW_FUSED adds the sum of squares of each output row's bf16
-    // values to ss_out[row] when ss_out is set.
+    // accumulator row by rsqrt(sum_i row_ss[i M + row] * inv_h + eps) over
+    // i < row_ss_parts when row_ss is set; GEMM_ROW_FUSED writes the sum of
+    // squares of each output row's bf16 values over each 128-column slice s
+    // to ss_out[s M + row] when ss_out is set (ceil(N / 128) slices, each
+    // written once: the statistic is summed in a fixed order, so the layer
+    // is bit-reproducible).
     const float* row_ss = nullptr;
+    int row_ss_parts = 1;
     float* ss_out = nullptr;
     float inv_h = 0.0f, eps = 0.0f;
     // Backward modes.

@@ -179,6 +179,18 @@ def test_small_layer_full_output(mode):
     assert_close(Y - X, ref - X, tol=5e-2, what="layer minus residual")
 
 
+@pytest.mark.parametrize("s", [Shape("l_det", 2, 300, 640, ffn=1280, heads=10, kv_heads=2, head_dim=64, tp=2,
+                                     act="swiglu", index=27), SHAPES["layer"]], ids=["small", "full"])
+def test_layer_forward_is_bit_reproducible(s):
+    # Every sum on the path runs in a fixed order (the folded norm's row
+    # statistics are per-slice partials summed by the consumer, not atomics),
+    # so two runs give the same bits.
+    inp = synth.workload_inputs(s)
+    Y1 = run_layer(s, inp, tp.TP_REDUCE_FUSED)
+    Y2 = run_layer(s, inp, tp.TP_REDUCE_FUSED)
+    assert np.array_equal(Y1, Y2)
+
+
 def test_full_size_layer_sampled_rows():
     s = SHAPES["layer"]
     inp = synth.workload_inputs(s)
