@@ -191,6 +191,33 @@ def test_layer_forward_is_bit_reproducible(s):
     assert np.array_equal(Y1, Y2)
 
 
+def test_layer_forward_replays_from_a_cuda_graph():
+    # The library launches only on the caller's stream, so the layer can be
+    # captured once and replayed; the replay gives the eager result's bits.
+    s = Shape("l_graph", 2, 128, 256, ffn=512, heads=4, kv_heads=2, head_dim=64, tp=2, act="swiglu",
+              index=28)
+    inp = synth.workload_inputs(s)
+    plan = plan_for(s)
+    ws, nws = workspace(plan, tp.TP_OP_LAYER)
+    Xd = dev(inp["X"])
+    wd = {k: dev(v) for k, v in inp.items() if k != "X"}
+    Y = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        tp.tp_layer_forward(plan, Xd, wd, Y, ws, nws, side)
+    torch.cuda.synchronize()
+    eager = Y.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        tp.tp_layer_forward(plan, Xd, wd, Y, ws, nws, side)
+    Y.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        g.replay()
+    sync_ok(plan)
+    assert torch.equal(Y.view(torch.int16), eager.view(torch.int16))
+
+
 def test_full_size_layer_sampled_rows():
     s = SHAPES["layer"]
     inp = synth.workload_inputs(s)
