@@ -16,14 +16,15 @@
 //                         of each sequence to a multiple of 64 rows, and a
 //                         zeroed fp32 dQ accumulator (one CTA per token row).
 //   attn_bwd_kernel       one CTA per (128-key block, KV head, sequence),
-//                         longest (earliest) key blocks first, 15 warps:
+//                         longest (earliest) key blocks first, 16 warps:
 //     warp 0     TMA: K and V of the key block once; then, per step, Q and
 //                dO of 64 queries of one query head of the group plus their
 //                log-sum-exp and D (3-stage ring).
 //     warp 1     TMEM owner and issuer of, per step,
 //                  S^T  = K Q^T   and dP^T = V dO^T   (128 x 64, TMEM)
-//     warp 14    issuer of the gradient products, once the softmax warps
-//                have written P^T and dS^T:
+//     warps 14, 15  issuers of the gradient products, once the softmax
+//                warps have written P^T and dS^T (warp 14 the first two,
+//                warp 15 dQ^T once the dQ warps have drained the last one):
 //                  dV  += P^T dO  (P^T read from TMEM),
 //                  dK  += dS^T Q                      (128 x d, TMEM, over
 //                                                      the whole group)
@@ -74,8 +75,9 @@ constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
 constexpr int SM_WARPS = 8;
 constexpr int SM_PARTS = SM_WARPS / 4;         // column parts of a key row
 constexpr int CPW = BQ / SM_PARTS;             // query columns per softmax warp
-constexpr int GRAD_WARP = 2 + SM_WARPS + 4;   // issuer of dV, dK, dQ^T
-constexpr int NTHREADS = 32 * (GRAD_WARP + 1);
+constexpr int GRAD_WARP = 2 + SM_WARPS + 4;   // issuer of dV, dK
+constexpr int DQ_WARP = GRAD_WARP + 1;         // issuer of dQ^T
+constexpr int NTHREADS = 32 * (DQ_WARP + 1);
 constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
 constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
 constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
@@ -103,8 +105,8 @@ constexpr int B_P_EMPTY = B_P_FULL + 2;   // x2
 constexpr int B_DQ_FULL = B_P_EMPTY + 2;
 constexpr int B_DQ_EMPTY = B_DQ_FULL + 1;
 constexpr int B_DKV_FULL = B_DQ_EMPTY + 1;
-constexpr int B_DRAIN = B_DKV_FULL + 1;      // x2: one per issuing thread
-constexpr int NUM_BARS = B_DRAIN + 2;
+constexpr int B_DRAIN = B_DKV_FULL + 1;      // x3: one per issuing thread
+constexpr int NUM_BARS = B_DRAIN + 3;
 // The data fill all but a few bytes of the 227 KB a CTA may use, leaving no
 // room to align the dynamic shared-memory base to 1024 bytes ourselves; the
 // kernel checks at run time that the base is aligned (it is when the kernel
@@ -224,13 +226,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(bar(B_S_EMPTY), SM_WARPS);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_P_FULL + s), SM_WARPS);
-            mbar_init(bar(B_P_EMPTY + s), 1);
+            mbar_init(bar(B_P_EMPTY + s), 2);  // the dV/dK and the dQ^T issuers' commits
         }
         mbar_init(bar(B_DQ_FULL), 1);
         mbar_init(bar(B_DQ_EMPTY), 4);
         mbar_init(bar(B_DKV_FULL), 1);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_DRAIN + 1), 1);
+        mbar_init(bar(B_DRAIN + 2), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                     if (issued & (1u << s)) drain_wait(bar(B_Q_FULL + s), (ipar >> s) & 1u);
             }
         }
-    } else if (warp == 1 || warp == GRAD_WARP) {
+    } else if (warp == 1 || warp == GRAD_WARP || warp == DQ_WARP) {
         // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
             // S^T, dP^T: M 128 keys, N 64 queries, both operands K-major (K = d).
@@ -348,15 +351,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 const uint32_t po = static_cast<uint32_t>(pb) * (PT_BYTES / U);
                 const uint32_t pt = tmem + (pb ? COL_PT1 : COL_PT0);
                 const uint32_t acc = it > 0 ? 1u : 0u;
-                // dV and dK first: they do not touch dQ^T's TMEM, so they go
-                // out while the dQ warps may still be reading the previous one.
+                if (warp == GRAD_WARP) {
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries (8 packed columns) per UMMA
-                    umma_bf16_ts(tmem + COL_DV, pt + ks * 8, dom + so + (ks * 2048) / U, id_kv, ks > 0 ? 1u : acc);
+                    for (int ks = 0; ks < BQ / 16; ++ks)  // 16 queries (8 packed columns) per UMMA
+                        umma_bf16_ts(tmem + COL_DV, pt + ks * 8, dom + so + (ks * 2048) / U, id_kv,
+                                     ks > 0 ? 1u : acc);
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    umma_bf16(tmem + COL_DK, dstd + po + (ks * 32) / U, qm + so + (ks * 2048) / U, id_kv,
-                              ks > 0 ? 1u : acc);
+                    for (int ks = 0; ks < BQ / 16; ++ks)
+                        umma_bf16(tmem + COL_DK, dstd + po + (ks * 32) / U, qm + so + (ks * 2048) / U, id_kv,
+                                  ks > 0 ? 1u : acc);
+                    umma_commit(bar(B_P_EMPTY + pb));
+                    umma_commit(bar(B_Q_EMPTY + st));  // Q and dO are read by dK and dV
+                    return true;
+                }
+                // dQ^T (warp DQ_WARP) once the dQ warps have drained the previous one.
                 if (!mbar_wait(bar(B_DQ_EMPTY), (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag, p.status,
                                p.timeout_ns))
                     return false;
@@ -367,7 +375,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                               ks > 0 ? 1u : 0u);
                 umma_commit(bar(B_P_EMPTY + pb));
                 umma_commit(bar(B_DQ_FULL));
-                umma_commit(bar(B_Q_EMPTY + st));
                 return true;
             };
             if (warp == 1) {
@@ -379,10 +386,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             } else {
                 for (int it = 0; it < n_it && ok; ++it) ok = issue_grad(it);
                 if (ok) {
-                    umma_commit(bar(B_DKV_FULL));
+                    if (warp == GRAD_WARP) umma_commit(bar(B_DKV_FULL));
                 } else {
-                    umma_commit(bar(B_DRAIN + 1));
-                    drain_wait(bar(B_DRAIN + 1), 0);
+                    const uint32_t dr = bar(warp == GRAD_WARP ? B_DRAIN + 1 : B_DRAIN + 2);
+                    umma_commit(dr);
+                    drain_wait(dr, 0);
                 }
             }
         }
