@@ -403,16 +403,19 @@ def run_case(args):
             out = torch.empty(Mv, hv, dtype=torch.bfloat16, device="cuda")
             fn = lambda: tp.tp_vocab_embedding_forward(ids, Mv, E, vv, hv, tv, out, stream)
             work, unit, peak = 2 * Mv * hv * 2 + Mv * 4, "GB/s", peaks["hbm_gbs"]
-    elif args.case in ("sp_layer", "partials_layer"):
-        # The layer with the g reductions through HBM partials: sequence
-        # parallel (reduce-scatter exits, all-gather entries, sequence-split
-        # residual stream) or replicated (all-reduce exits).
+    elif args.case in ("sp_layer", "sp_layer_partials", "partials_layer"):
+        # The sequence-parallel layer (all-gather entries, reduce-scatter
+        # exits, sequence-split residual stream) with g in the accumulator
+        # (sp_layer) or through HBM partials (sp_layer_partials), and the
+        # replicated layer with HBM partials (partials_layer).
         inp = synth.workload_inputs(s)
         d = {k: v.cuda() for k, v in inp.items()}
+        fused = args.case == "sp_layer"
         plan = tp.Plan(tp.make_config(tokens=M, hidden=h, ffn=f, n_heads=a, n_kv_heads=k,
                                       head_dim=s.head_dim, tp_degree=t, act=s.act,
-                                      batch=s.batch, seq=s.seq, reduce_mode=tp.TP_REDUCE_PARTIALS,
-                                      sequence_parallel=1 if args.case == "sp_layer" else 0))
+                                      batch=s.batch, seq=s.seq,
+                                      reduce_mode=tp.TP_REDUCE_FUSED if fused else tp.TP_REDUCE_PARTIALS,
+                                      sequence_parallel=0 if args.case == "partials_layer" else 1))
         nws = tp.tp_plan_workspace_bytes(plan, tp.TP_OP_LAYER)
         wsb = torch.empty(nws, dtype=torch.uint8, device="cuda")
         Yl = torch.empty(M, h, dtype=torch.bfloat16, device="cuda")
@@ -796,7 +799,7 @@ def main(argv=None):
                     help="tokens of the oracle sample per reference step (0 = sized to ~2 min)")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "w13", "qkv", "gelu", "o_proj", "w2", "attn", "reduce",
-                             "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer",
+                             "packed", "vocab_logits", "vocab_ce", "embedding", "sp_layer", "sp_layer_partials",
                              "partials_layer", "mlp_backward", "mlp_backward_recompute",
                              "attn_backward", "attn_backward_recompute", "layer_backward", "blocks"],
                     help="layer = the benchmark step; others = one kernel alone (profiling)")

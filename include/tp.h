@@ -129,8 +129,8 @@ typedef struct {
     int32_t partial_dtype; /* TP_F32 or TP_BF16 (PARTIALS mode only)          */
     float rms_eps;         /* RMSNorm epsilon (layer only), > 0               */
     int32_t sequence_parallel; /* 1: layer in/out in the sequence-split layout
-                                  [t][batch][seq/t][h] (needs t | seq and
-                                  TP_REDUCE_PARTIALS); 0: replicated [M][h]   */
+                                  [t][batch][seq/t][h] (needs t | seq);
+                                  0: replicated [M][h]                        */
 } tp_config;
 
 /* Weights of one layer, all full nn.Linear matrices [out][in] in bf16:
@@ -482,9 +482,12 @@ TP_API int tp_attn_forward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, 
 /* One pre-norm layer with two g reductions ([wiki] "통신 연산 f와 g": one
  * all-reduce after attention and one after the MLP; norm and residual
  * replicated):  h1 = x + Attn(RMSNorm(x)),  y = h1 + MLP(RMSNorm(h1)).
- * With cfg.sequence_parallel = 1, X and Y are in the sequence-split layout
- * and every g is a reduce-scatter fused with the next local norm, every
- * block input an all-gather ([wiki] "시퀀스 병렬화").
+ * With cfg.sequence_parallel = 1, X and Y are in the sequence-split layout,
+ * every block input is an all-gather and every g a reduce-scatter ([wiki]
+ * "시퀀스 병렬화").  In PARTIALS mode the reduce-scatter sums the [t][M][h]
+ * partials and fuses the next local norm; in FUSED mode it is the rowwise
+ * GEMM's sum over shards in the accumulator, written with the residual into
+ * the split layout, and the norms are folded into the colwise GEMMs.
  * X, Y: device [M][h] bf16 (may not alias).  Requires act == TP_ACT_SWIGLU
  * or a GeLU form (W3 NULL then).  workspace >= tp_plan_workspace_bytes(
  * TP_OP_LAYER); in PARTIALS mode it also holds the [t][M][h] partials. */

@@ -168,6 +168,8 @@ Layout layout_of(const tp_plan_s* p, int op) {
             // Folded RMSNorm statistics: x's row sums of squares, then h1's
             // per 128-column slice of the o_proj output.
             L.ss = align_up((1 + (p->h + 127) / 128) * M * sizeof(float));
+            // Sequence parallel: the gathered (token-order) copy of x or h1.
+            if (p->cfg.sequence_parallel) L.full = align_up(M * p->h * 2);
         }
     }
     return L;
@@ -231,7 +233,7 @@ int do_colwise(const tp_plan_s* p, const void* X, const void* W1, const void* W3
 // accumulator, + bias + residual, bf16 out) or per-shard partials.
 int do_rowwise(const tp_plan_s* p, const void* A, int64_t Ks, const void* B, int64_t N,
                const void* bias, const void* residual, void* partials, void* out, bool fused,
-               cudaStream_t s, float* ss_out = nullptr) {
+               cudaStream_t s, float* ss_out = nullptr, bool sp_rows = false) {
     tpi::GemmArgs g;
     g.mode = fused ? tpi::GEMM_ROW_FUSED : tpi::GEMM_ROW_PARTIAL;
     g.M = p->M;
@@ -248,6 +250,11 @@ int do_rowwise(const tp_plan_s* p, const void* A, int64_t Ks, const void* B, int
         g.residual = residual;
         g.ldr = N;
         g.ss_out = ss_out;
+        if (sp_rows) {  // output and residual in the sequence-split layout
+            g.sp_batch = p->cfg.batch;
+            g.sp_seq = p->cfg.seq;
+            g.sp_t = static_cast<int>(p->t);
+        }
     } else {
         g.out = partials;
         g.ldo = N;
@@ -387,10 +394,6 @@ int derive_plan(const tp_config& cfg, tp_plan_s* p) {
         if (c.seq % t)
             return fail(TP_ERR_NOT_DIVISIBLE, "tp_degree %d does not divide seq %d (sequence split)",
                         c.tp_degree, c.seq);
-        if (c.reduce_mode != TP_REDUCE_PARTIALS)
-            return fail(TP_ERR_UNSUPPORTED,
-                        "sequence parallelism leaves each block through a reduce-scatter of the "
-                        "partials: use TP_REDUCE_PARTIALS");
     }
 
     *p = tp_plan_s();
@@ -1057,7 +1060,7 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     if ((rc = check_ws(plan, TP_OP_LAYER, workspace, ws_bytes))) return rc;
     const bool fused_mode = plan->cfg.reduce_mode == TP_REDUCE_FUSED;
     const bool sp_mode = plan->cfg.sequence_parallel != 0;
-    const int need_events = fused_mode ? 7 : sp_mode ? 11 : 9;
+    const int need_events = fused_mode ? (sp_mode ? 9 : 7) : sp_mode ? 11 : 9;
     if (events) {
         if (n_events < need_events)
             return fail(TP_ERR_INVALID_ARG, "%d events given, %d needed", n_events, need_events);
@@ -1083,6 +1086,37 @@ int tp_layer_forward_traced(tp_plan_t plan, const tp_bf16* X, const tp_layer_wei
     const float eps = plan->cfg.rms_eps;
     cudaStream_t s = as_stream(stream);
     std::string err;
+    if (fused_mode && sp_mode) {
+        // Sequence parallel with g in the accumulator: X, h1 and Y stay in the
+        // sequence-split layout.  Each block's input is gathered into token
+        // order; its norm is folded into the colwise GEMM as in the
+        // replicated layer; the reduce-scatter is the rowwise GEMM's sum over
+        // shards in TMEM, written (with the residual) straight into the split
+        // layout, so no partials go through HBM.
+        const int64_t B = plan->cfg.batch, S = plan->cfg.seq;
+        const int T = (int)plan->t, Hd = (int)plan->h;
+        mark(s);
+        if ((rc = run(tpi::sp_all_gather_launch(X, B, S, T, Hd, full, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = run(tpi::row_sumsq_launch(full, plan->M, Hd, ss1, nullptr, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = do_qkv(plan, full, w->Wq, w->Wk, w->Wv, QKV, s, ss1))) return rc;
+        mark(s);
+        if ((rc = do_attn_core(plan, QKV, O, s))) return rc;
+        mark(s);
+        if ((rc = do_rowwise(plan, O, plan->qw, w->Wo, plan->h, nullptr, X, nullptr, h1, true, s, ss2, true)))
+            return rc;
+        mark(s);
+        if ((rc = run(tpi::sp_all_gather_launch(h1, B, S, T, Hd, full, s, &err), err))) return rc;
+        mark(s);
+        if ((rc = do_colwise(plan, full, w->W1, w->W3, Yb, s, ss2, nullptr, static_cast<int>((plan->h + 127) / 128))))
+            return rc;
+        mark(s);
+        if ((rc = do_rowwise(plan, Yb, plan->fw, w->W2, plan->h, nullptr, h1, nullptr, Y, true, s, nullptr, true)))
+            return rc;
+        mark(s);
+        return TP_OK;
+    }
     if (fused_mode) {
         // RMSNorm is folded into the GEMMs: a unit-gain norm is a per-row
         // scale, so RMSNorm(x) W^T = rsqrt(mean(x^2) + eps) * (x W^T).  The

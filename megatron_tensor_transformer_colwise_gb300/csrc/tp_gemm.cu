@@ -132,6 +132,8 @@ struct GemmParams {
     const float* row_ss;  // colwise: scale row by rsqrt(sum of row_ss_parts partials * inv_h + eps)
     int row_ss_parts;     // partials of row_ss, M apart
     float* ss_out;        // ROW_FUSED: sum of squares of the row's bf16 outputs per 128-column slice
+    long long sp_batch, sp_seq;  // ROW_FUSED: output / residual rows in the sequence-split layout
+    int sp_t;                    // (0: token order)
     float inv_h, eps;
     // Backward modes (see tpi::GemmArgs).
     const __nv_bfloat16* aux;  // BWD_ACT: saved pre-activations U (| G)
@@ -620,7 +622,15 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
         } else {
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
             if (MODE == tpi::GEMM_ROW_PARTIAL) out += s_grid * p.shard_stride;
-            out += static_cast<long long>(row) * p.ldo;
+            // Output (and residual) row: the token's row in the sequence-split
+            // layout when the layer is sequence parallel.
+            long long orow = row;
+            if (MODE == tpi::GEMM_ROW_FUSED && p.sp_t > 0) {
+                const long long w = p.sp_seq / p.sp_t;
+                const long long b = row / p.sp_seq, pos = row - b * p.sp_seq;
+                orow = ((pos / w) * p.sp_batch + b) * w + pos % w;
+            }
+            out += orow * p.ldo;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 const int col = col0 + g * 8;
@@ -653,8 +663,7 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
                         }
                     }
                     if (p.residual) {
-                        const uint4 rr = *reinterpret_cast<const uint4*>(
-                            p.residual + static_cast<long long>(row) * p.ldr + col);
+                        const uint4 rr = *reinterpret_cast<const uint4*>(p.residual + orow * p.ldr + col);
                         const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -1037,6 +1046,9 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     p.ldr = a.ldr;
     p.row_ss = a.row_ss;
     p.row_ss_parts = a.row_ss_parts > 0 ? a.row_ss_parts : 1;
+    p.sp_batch = a.sp_batch;
+    p.sp_seq = a.sp_seq;
+    p.sp_t = (a.mode == GEMM_ROW_FUSED && a.sp_t > 0 && a.sp_seq > 0 && a.sp_seq % a.sp_t == 0) ? a.sp_t : 0;
     p.ss_out = a.ss_out;
     p.inv_h = a.inv_h;
     p.eps = a.eps;

@@ -69,6 +69,12 @@ struct GemmArgs {
     const float* row_ss = nullptr;
     int row_ss_parts = 1;
     float* ss_out = nullptr;
+    // GEMM_ROW_FUSED in a sequence-parallel layer: output and residual rows
+    // live in the sequence-split layout [t][batch][seq/t] (token b seq + pos
+    // at row ((pos / w) batch + b) w + pos % w, w = seq / t); ss_out stays in
+    // token order.  sp_t == 0: token order.
+    int64_t sp_batch = 0, sp_seq = 0;
+    int sp_t = 0;
     float inv_h = 0.0f, eps = 0.0f;
     // Backward modes.
     //  GEMM_BWD_ACT: aux = saved pre-activations [M][ldaux] (U at column n,

@@ -180,6 +180,8 @@ def test_sequence_parallel_config_rules():
     bad_seq = cfg(tokens=60, batch=2, seq=30, tp_degree=4, reduce_mode=tp.TP_REDUCE_PARTIALS,
                   sequence_parallel=1, ffn=256)
     assert tp.tp_config_check(bad_seq) == tp.TP_ERR_NOT_DIVISIBLE
+    # FUSED mode: the reduce-scatter happens in the rowwise GEMM's accumulator.
     fused = cfg(tokens=64, batch=2, seq=32, tp_degree=4, sequence_parallel=1)
-    assert tp.tp_config_check(fused) == tp.TP_ERR_UNSUPPORTED
-    assert "reduce-scatter" in tp.tp_last_error()
+    assert tp.tp_config_check(fused) == tp.TP_OK, tp.tp_last_error()
+    bad_tokens = cfg(tokens=64, batch=2, seq=16, tp_degree=4, sequence_parallel=1)
+    assert tp.tp_config_check(bad_tokens) == tp.TP_ERR_INVALID_ARG

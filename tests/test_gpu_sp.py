@@ -42,11 +42,13 @@ def test_reduce_scatter_integer_bit_exact_and_fused_norm(dtype):
     assert_close(host64(xn), oracle.rmsnorm(host64(out), 1e-5), tol=1e-2, what="fused local norm")
 
 
-def _run_sp_layer(s, inp):
+SP_MODES = [tp.TP_REDUCE_PARTIALS, tp.TP_REDUCE_FUSED]
+
+
+def _run_sp_layer(s, inp, mode=tp.TP_REDUCE_PARTIALS):
     cfg = tp.make_config(tokens=s.tokens, hidden=s.hidden, ffn=s.ffn, n_heads=s.heads,
                          n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp, act=s.act,
-                         reduce_mode=tp.TP_REDUCE_PARTIALS, batch=s.batch, seq=s.seq,
-                         sequence_parallel=1)
+                         reduce_mode=mode, batch=s.batch, seq=s.seq, sequence_parallel=1)
     plan = tp.Plan(cfg)
     ws, nws = workspace(plan, tp.TP_OP_LAYER)
     perm = _perm(s.batch, s.seq, s.tp)
@@ -58,21 +60,25 @@ def _run_sp_layer(s, inp):
     return X_sp, host64(Y_sp), perm
 
 
-def test_small_sequence_parallel_layer():
+# FUSED mode: the reduce-scatter is the rowwise GEMM's sum over shards in
+# TMEM, written into the split layout; PARTIALS mode sums the partials.
+@pytest.mark.parametrize("mode", SP_MODES, ids=["partials", "fused"])
+def test_small_sequence_parallel_layer(mode):
     s = Shape("sp", 2, 128, 256, ffn=768, heads=8, kv_heads=2, head_dim=64, tp=4, act="swiglu",
               index=27)
     inp = synth.workload_inputs(s)
-    X_sp, Y_sp, perm = _run_sp_layer(s, inp)
+    X_sp, Y_sp, perm = _run_sp_layer(s, inp, mode)
     ref = oracle.layer_sp(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, s.tp, host64(X_sp),
                           *(host64(inp[n]) for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")))
     assert_close(Y_sp, ref, what="sequence-parallel layer")
     assert_close(Y_sp - host64(X_sp), ref - host64(X_sp), tol=5e-2, what="SP layer minus residual")
 
 
-def test_full_size_sequence_parallel_layer_sampled_rows():
+@pytest.mark.parametrize("mode", SP_MODES, ids=["partials", "fused"])
+def test_full_size_sequence_parallel_layer_sampled_rows(mode):
     s = SHAPES["layer"]
     inp = synth.workload_inputs(s)
-    X_sp, Y_sp, perm = _run_sp_layer(s, inp)
+    X_sp, Y_sp, perm = _run_sp_layer(s, inp, mode)
     rows = [0, 5, 300, 2 * s.seq + 1, 3 * s.seq + 1100, s.seq - 1]
     ref = oracle.layer_rows(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim,
                             *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")),
