@@ -129,6 +129,42 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 
+// Two fp32 values in one 64-bit register pair for the packed FP32
+// instructions (fma.rn.f32x2, add.rn.f32x2: each half rounds as the scalar
+// instruction does), which halve the softmax's instruction count.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// Maximum of three (PTX max.f32 with three sources).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Bring a box of a tensor map into L2 without writing shared memory.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // One work item: 128 query rows (tile qb) of query head j in sequence b.
 // Items are numbered longest first: item w has tile nqb - 1 - w / (heads *
 // batch), so each round of gridDim.x items has rows of one length.
@@ -255,6 +291,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             int li = 0;
             for (int w = w0; w < n_items && ok; w += dw, ++li) {
                 const Item x = item_of<D>(p, w);
+                // The next item's Q is read from HBM for the first time: start
+                // that read now, so its TMA load later hits L2.
+                if (w + dw < n_items) {
+                    const Item y = item_of<D>(p, w + dw);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(&p.map_q, y.qcol + 64 * c, y.tok0 + y.q0);
+                }
                 if (li > 0 && !mbar_wait(bar(B_Q_EMPTY), static_cast<uint32_t>(li - 1) & 1u, abort_flag, p.status,
                                          p.timeout_ns)) {
                     ok = false;
@@ -406,25 +449,28 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                     tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
                 tmem_ld_wait();
 
+                // Keys k0 + c with c > lim are masked: later than the query
+                // (causal) or past the sequence end.
                 const int k0 = kb * KB;
-                if (k0 + KB - 1 > q0 || k0 + KB > p.seq) {
+                const int lim = min(qpos, p.seq - 1) - k0;
+                if (lim < KB - 1) {
 #pragma unroll
-                    for (int c = 0; c < KB; ++c) {
-                        const int key = k0 + c;
-                        if (key > qpos || key >= p.seq) s[c] = __float_as_uint(-INFINITY);
-                    }
+                    for (int c = 0; c < KB; ++c)
+                        if (c > lim) s[c] = __float_as_uint(-INFINITY);
                 }
-                // Row max with 8 independent chains (one softmax warp per SM
-                // sub-partition and CTA leaves little to hide a serial chain).
+                // Row max with 8 independent chains of three-way maxima (one
+                // softmax warp per SM sub-partition and CTA leaves little to
+                // hide a serial chain).
                 float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[8 + e]));
 #pragma unroll
-                for (int c = 8; c < KB; c += 8)
+                for (int c = 16; c < KB; c += 16)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(s[c + e]));
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    for (int e = 0; e < 8; ++e)
+                        mx8[e] = max3(mx8[e], __uint_as_float(s[c + e]), __uint_as_float(s[c + 8 + e]));
+                const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
+                                      fmaxf(mx8[6], mx8[7]));
                 const float mxs = mx * p.scale_log2;
                 float alpha = 1.0f;
                 bool rescale = false;
@@ -433,17 +479,24 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                     m_ref = mxs;
                     rescale = kb > 0;
                 }
-                float sum8[8];
+                const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t neg2 = f2_pack(-m_ref, -m_ref);
+                uint64_t acc[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
+                for (int e = 0; e < 4; ++e) acc[e] = f2_pack(0.0f, 0.0f);
                 uint32_t pk[KB / 2];
 #pragma unroll
                 for (int c = 0; c < KB / 2; ++c) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -m_ref));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -m_ref));
-                    sum8[c & 7] += p0 + p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, neg2),
+                              x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
+                float sum8[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(acc[e], sum8[2 * e], sum8[2 * e + 1]);
                 const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
                                   ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
                 l_sum = l_sum * alpha + sum;

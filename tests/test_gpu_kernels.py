@@ -234,12 +234,16 @@ def test_qkv_integer_bit_exact(a, k, t, d):
     assert np.array_equal(bf16_bits(QKV), oracle.round_bf16_bits(ref).reshape(ref.shape))
 
 
-# The last case has 1024 work items (query tiles x heads x sequences), over
-# three times as many as the kernel's persistent grid holds on GB300, so
-# every CTA runs several items back to back.
+# The (8, 512, 32, 8, 8) case has 1024 work items (query tiles x heads x
+# sequences) and (8, 512, 24, 8, 8) 768, over twice as many as the kernel's
+# persistent grid holds on GB300, so every CTA runs several items back to
+# back; (6, 1000, 16, 4, 4) adds a ragged last query tile and key block to
+# that, and (1, 1, ...) is a one-token sequence.
 @pytest.mark.parametrize("batch,seq,a,k,t,d", [(2, 200, 8, 2, 4, 64), (1, 130, 4, 4, 2, 128),
                                                (3, 64, 8, 1, 8, 128), (1, 1, 4, 2, 2, 64),
-                                               (2, 257, 16, 8, 8, 128), (8, 512, 32, 8, 8, 128)])
+                                               (2, 257, 16, 8, 8, 128), (8, 512, 32, 8, 8, 128),
+                                               (4, 700, 8, 2, 2, 128), (6, 1000, 16, 4, 4, 128),
+                                               (8, 512, 24, 8, 8, 128), (1, 1, 4, 2, 2, 128)])
 def test_attention_core_vs_oracle(batch, seq, a, k, t, d):
     s = Shape("ac", batch, seq, 64, heads=a, kv_heads=k, head_dim=d, tp=t, act="none", index=15)
     plan = plan_for(s)
