@@ -212,7 +212,7 @@ def profiled_traffic(kernel_name: str):
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as fh:
             entry = json.load(fh)[kernel_name]
         h = hashlib.sha256()
-        for f in ("tp_gemm.cu", "tp_device.cuh"):
+        for f in ("tp_gemm.cu", "tp_device.cuh", "tp_packed.cuh"):
             with open(os.path.join(ROOT, "megatron_tensor_transformer_colwise_gb300", "csrc", f), "rb") as fh:
                 h.update(fh.read())
         if h.hexdigest()[:16] != entry["source_sha256_16"]:

@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The next kernel may start its prologue on SMs this grid leaves; this
+    // one touches global memory only once the previous kernel is done.
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -615,8 +619,8 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
     const long long n_items = static_cast<long long>((a.seq + QB - 1) / QB) * a.heads * a.batch;
     dim3 grid(static_cast<unsigned>(std::min<long long>(n_items, 2LL * sms)), 1, 1);
-    attn_tc_kernel<D><<<grid, NTHREADS, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = tpi::launch_pdl(attn_tc_kernel<D>, grid, dim3(NTHREADS), smem, stream, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (err) *err = std::string("attention launch: ") + cudaGetErrorString(e);
         return TP_ERR_CUDA;

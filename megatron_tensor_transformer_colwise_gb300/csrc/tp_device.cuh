@@ -337,6 +337,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t m, uint32_t n
     return idesc_bf16_f32(m, n) | (1u << 16);
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+
+// A kernel launched with cudaLaunchAttributeProgrammaticStreamSerialization
+// may start while the previous kernel of its stream is still running, once
+// every CTA of that kernel has called pdl_trigger() or exited.  pdl_wait()
+// returns when the previous kernel has completed and its memory operations
+// are visible, so it comes before the kernel touches global memory; without
+// the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------ CTA pairs (clusters of 2)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

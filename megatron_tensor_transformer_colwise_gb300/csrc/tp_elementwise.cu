@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(RED_THREADS) reduce_kernel(const void* __restr
                                                              const __nv_bfloat16* __restrict__ bias,
                                                              const __nv_bfloat16* __restrict__ residual,
                                                              __nv_bfloat16* out) {
+    pdl_trigger();
+    pdl_wait();
     const int tt = T ? T : t;
     const long long nvec = n >> 3;
     for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(ROW_THREADS) row_kernel(const void* __restrict
                                                           __nv_bfloat16* xn_out, float eps,
                                                           long long sp_batch, long long sp_seq,
                                                           int sp_t) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[ROW_THREADS / 32];
     // Partials are read at the token's row; residual and outputs live at its
     // (possibly sequence-split) output row.
@@ -222,6 +226,8 @@ constexpr int SS_WARPS = 8;
 __global__ void __launch_bounds__(SS_WARPS * 32) row_sumsq_kernel(const __nv_bfloat16* __restrict__ x,
                                                                   long long rows, int h, float* ss,
                                                                   float* zero) {
+    pdl_trigger();
+    pdl_wait();
     const long long row = static_cast<long long>(blockIdx.x) * SS_WARPS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -264,6 +270,8 @@ constexpr int AG_WARPS = 8;
 __global__ void __launch_bounds__(AG_WARPS * 32) sp_all_gather_kernel(
     const __nv_bfloat16* __restrict__ sp, long long rows, int h, long long batch, long long seq,
     int t, __nv_bfloat16* __restrict__ full) {
+    pdl_trigger();
+    pdl_wait();
     const long long row = static_cast<long long>(blockIdx.x) * AG_WARPS + (threadIdx.x >> 5);
     if (row >= rows) return;
     const uint4* src = reinterpret_cast<const uint4*>(sp + sp_out_row(row, batch, seq, t) * h);
@@ -464,7 +472,7 @@ int reduce_launch(const void* partials, int partial_f32, int t, int64_t n, int h
     const __nv_bfloat16* r = reinterpret_cast<const __nv_bfloat16*>(residual);
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
 #define TP_RED(TT, FF) \
-    reduce_kernel<TT, FF><<<(unsigned)blocks, RED_THREADS, 0, stream>>>(partials, t, n, h, b, r, o)
+    launch_pdl(reduce_kernel<TT, FF>, dim3((unsigned)blocks), dim3(RED_THREADS), 0, stream, partials, t, n, h, b, r, o)
     if (partial_f32) {
         switch (t) {
             case 1: TP_RED(1, true); break;
@@ -495,11 +503,11 @@ int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t row
     auto* h1p = reinterpret_cast<__nv_bfloat16*>(h1);
     auto* xnp = reinterpret_cast<__nv_bfloat16*>(xn);
     if (partial_f32)
-        row_kernel<true, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp,
-                                                                           eps, sp_batch, sp_seq, sp_t);
+        launch_pdl(row_kernel<true, true>, dim3((unsigned)rows), dim3(ROW_THREADS), 0, stream, partials, t, n, h,
+                   r, h1p, xnp, eps, sp_batch, sp_seq, sp_t);
     else
-        row_kernel<true, false><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(partials, t, n, h, r, h1p, xnp,
-                                                                            eps, sp_batch, sp_seq, sp_t);
+        launch_pdl(row_kernel<true, false>, dim3((unsigned)rows), dim3(ROW_THREADS), 0, stream, partials, t, n,
+                   h, r, h1p, xnp, eps, sp_batch, sp_seq, sp_t);
     return check_launch("reduce+norm kernel", err);
 }
 
@@ -507,9 +515,9 @@ int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaS
                    std::string* err) {
     if (rows == 0) return TP_OK;
     const long long n = rows * (long long)h;
-    row_kernel<false, true><<<(unsigned)rows, ROW_THREADS, 0, stream>>>(
-        nullptr, 0, n, h, reinterpret_cast<const __nv_bfloat16*>(x), nullptr,
-        reinterpret_cast<__nv_bfloat16*>(y), eps, 0, 0, 0);
+    launch_pdl(row_kernel<false, true>, dim3((unsigned)rows), dim3(ROW_THREADS), 0, stream,
+               static_cast<const void*>(nullptr), 0, n, h, reinterpret_cast<const __nv_bfloat16*>(x),
+               static_cast<__nv_bfloat16*>(nullptr), reinterpret_cast<__nv_bfloat16*>(y), eps, 0LL, 0LL, 0);
     return check_launch("rmsnorm kernel", err);
 }
 
@@ -517,8 +525,8 @@ int row_sumsq_launch(const void* x, int64_t rows, int h, float* ss, float* zero,
                      cudaStream_t stream, std::string* err) {
     if (rows == 0) return TP_OK;
     const long long blocks = (rows + SS_WARPS - 1) / SS_WARPS;
-    row_sumsq_kernel<<<(unsigned)blocks, SS_WARPS * 32, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), rows, h, ss, zero);
+    launch_pdl(row_sumsq_kernel, dim3((unsigned)blocks), dim3(SS_WARPS * 32), 0, stream,
+               reinterpret_cast<const __nv_bfloat16*>(x), rows, h, ss, zero);
     return check_launch("row sum-of-squares kernel", err);
 }
 
@@ -526,9 +534,9 @@ int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int 
                          cudaStream_t stream, std::string* err) {
     const long long rows = batch * seq;
     if (rows == 0) return TP_OK;
-    sp_all_gather_kernel<<<(unsigned)((rows + AG_WARPS - 1) / AG_WARPS), AG_WARPS * 32, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
-        reinterpret_cast<__nv_bfloat16*>(full));
+    launch_pdl(sp_all_gather_kernel, dim3((unsigned)((rows + AG_WARPS - 1) / AG_WARPS)), dim3(AG_WARPS * 32), 0,
+               stream, reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
+               reinterpret_cast<__nv_bfloat16*>(full));
     return check_launch("all-gather kernel", err);
 }
 

@@ -44,6 +44,7 @@
 
 #include "tp_device.cuh"
 #include "tp_internal.h"
+#include "tp_packed.cuh"
 
 #ifndef TP_GEMM_CTA_PAIR
 #define TP_GEMM_CTA_PAIR 2
@@ -97,11 +98,16 @@ struct Cfg {
     static constexpr int B_BYTES = (BNT / CG) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr bool STAGED_OUT = MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_TN;
+    // GEMM_COL_ACT stages its bf16 output through two alternating 32 x 32
+    // boxes per epilogue warp (64-byte swizzle) when the output allows a
+    // TMA map; the six ring stages still fit beside them.
+    static constexpr bool COL_STAGED = MODE == tpi::GEMM_COL_ACT && CG == 2 && BNT == BN;
     static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : (BNT == BN ? 6 : 8));
     static constexpr int CHUNKS = (BNT / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
     static constexpr int TMEM_COLS = 2 * BNT;                  // two accumulators
     static constexpr int EPI_BYTES = MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
                                      : MODE == tpi::GEMM_TN    ? 4 * 2 * 2 * EPI_BOX_BYTES  // 4 warps x 2 fp32 boxes
+                                     : COL_STAGED              ? 8 * 2 * EPI_BOX_BYTES      // 8 warps x 2 boxes
                                                                : 0;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -146,6 +152,7 @@ struct GemmParams {
     void* out3;
     long long ldo3;
     int accumulate;
+    int o_staged;  // GEMM_COL_ACT: out written through mapO[0] by TMA stores
     CUtensorMap mapO[3];  // BWD_ACT: TMA-store maps of dU, dG, H (64-byte swizzle)
     unsigned* status;
     unsigned long long timeout_ns;
@@ -238,6 +245,34 @@ __device__ __forceinline__ float act_apply(float v) {
     if (ACT == TP_ACT_GELU_ERF) return gelu_erf(v);
     if (ACT == TP_ACT_GELU_TANH) return v * gelu_tanh_sigma(v);
     return v;
+}
+
+// act_apply of two values with packed FP32 arithmetic (GeLU: the same
+// operations in the same order as gelu_erf and gelu_tanh_sigma, each lane
+// rounded as the scalar instruction, so the results are the same bits).
+template <int ACT>
+__device__ __forceinline__ void act_apply2(float u0, float u1, float& h0, float& h1) {
+    if (ACT == TP_ACT_GELU_ERF) {
+        constexpr float P = 0.3275911f * 0.70710678118654752f;
+        constexpr float A1 = 0.5f * 0.254829592f, A2 = 0.5f * -0.284496736f, A3 = 0.5f * 1.421413741f;
+        constexpr float A4 = 0.5f * -1.453152027f, A5 = 0.5f * 1.061405429f;
+        const uint64_t U = f2_pack(u0, u1);
+        float d0, d1, s0, s1;
+        f2_unpack(f2_fma(f2_pack(P, P), f2_pack(fabsf(u0), fabsf(u1)), f2_pack(1.0f, 1.0f)), d0, d1);
+        f2_unpack(f2_mul(f2_mul(U, U), f2_pack(-0.5f * kLog2e, -0.5f * kLog2e)), s0, s1);
+        const uint64_t T = f2_pack(rcp_approx(d0), rcp_approx(d1));
+        const uint64_t E = f2_pack(ex2_approx(s0), ex2_approx(s1));
+        uint64_t poly = f2_fma(T, f2_pack(A5, A5), f2_pack(A4, A4));
+        poly = f2_fma(T, poly, f2_pack(A3, A3));
+        poly = f2_fma(T, poly, f2_pack(A2, A2));
+        poly = f2_fma(T, poly, f2_pack(A1, A1));
+        float q0, q1;
+        f2_unpack(f2_mul(f2_mul(T, poly), E), q0, q1);
+        f2_unpack(f2_mul(U, f2_pack(u0 >= 0.0f ? 1.0f - q0 : q0, u1 >= 0.0f ? 1.0f - q1 : q1)), h0, h1);
+    } else {
+        h0 = act_apply<ACT>(u0);
+        h1 = act_apply<ACT>(u1);
+    }
 }
 
 template <int ACT>
@@ -594,6 +629,59 @@ __device__ __forceinline__ void bwd_act_tile(const GemmParams& p, const __nv_bfl
     }
 }
 
+// GEMM_COL_ACT epilogue through shared memory: per 32-column chunk the warp
+// writes its 32 rows x 32 columns as bf16 into one of its two boxes (64-byte
+// swizzle: 16-byte piece g of row l at l * 64 + (g ^ ((l / 2) % 4)) * 16)
+// and lane 0 issues one TMA store of the box; rows and columns past the
+// output are clipped by the map.  A box is rewritten once the store two
+// chunks back has read it.  row0: first global row of the warp's box.
+template <int ACT, int CPW, int BNT>
+__device__ __forceinline__ void col_act_tile_staged(const GemmParams& p, uint32_t t0, int cb, int nb, int row,
+                                                    bool row_ok, int row0, float rs, uint32_t sbuf) {
+    const int lane = threadIdx.x & 31;
+    const bool box_ok = row0 < p.M;  // warp-uniform
+    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+    const uint64_t rs2 = f2_pack(rs, rs);
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = cb; c < cb + CPW; ++c) {
+        const int col0 = nb * BNT + c * 32;
+        if (col0 >= p.N) break;  // warp-uniform
+        __syncwarp();
+        tmem_ld32(t0 + c * 32, r);
+        tmem_ld_wait();
+        const uint32_t box = sbuf + static_cast<uint32_t>(c & 1) * EPI_BOX_BYTES;
+        const uint32_t srow = box + static_cast<uint32_t>(lane) * 64;
+        if (lane == 0) bulk_wait_group_read1();  // this box's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[g * 8 + 2 * e]), __uint_as_float(r[g * 8 + 2 * e + 1])), rs2),
+                          v[2 * e], v[2 * e + 1]);
+            if (p.aux_out && row_ok && col0 + g * 8 < p.N)  // pre-activations for the backward pass
+                st_v4(p.aux_out + static_cast<long long>(row) * p.ldaux + col0 + g * 8, pack_bf16x2(v[0], v[1]),
+                      pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float h0, h1;
+                act_apply2<ACT>(v[2 * e], v[2 * e + 1], h0, h1);
+                w[e] = pack_bf16x2(h0, h1);
+            }
+            st_shared_v4(srow + ((static_cast<uint32_t>(g) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();  // visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && box_ok) {
+            tma_store_2d(&p.mapO[0], box, col0, row0);
+            bulk_commit_group();
+        }
+    }
+}
+
 // Epilogue of the column- and row-parallel forward modes for one warp's CPW
 // 32-column chunks of a tile (row: this thread's global row; rs: the folded
 // RMSNorm scale of colwise rows; ssq accumulates the squares of the stored
@@ -834,6 +922,20 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                     }
                 }
             }
+        } else if (MODE == tpi::GEMM_COL_ACT && C::COL_STAGED && p.o_staged) {
+            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const uint32_t sbuf = epi0 + static_cast<uint32_t>(warp - 2) * 2 * EPI_BOX_BYTES;
+            switch (p.act) {
+                case TP_ACT_GELU_ERF:
+                    col_act_tile_staged<TP_ACT_GELU_ERF, CPW, BNT>(p, t0, cb, nb, row, row_ok, row0, rs, sbuf);
+                    break;
+                case TP_ACT_GELU_TANH:
+                    col_act_tile_staged<TP_ACT_GELU_TANH, CPW, BNT>(p, t0, cb, nb, row, row_ok, row0, rs, sbuf);
+                    break;
+                default:
+                    col_act_tile_staged<TP_ACT_NONE, CPW, BNT>(p, t0, cb, nb, row, row_ok, row0, rs, sbuf);
+                    break;
+            }
         } else if (MODE == tpi::GEMM_COL_ACT) {
             // One branch-free chunk loop per activation, chosen once per tile.
             switch (p.act) {
@@ -863,7 +965,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
     }
     // Staged outputs: every TMA store has completed before the CTA moves on
     // (its shared memory stays valid until then).
-    if (C::STAGED_OUT && lane == 0) bulk_wait_group0();
+    if ((C::STAGED_OUT || C::COL_STAGED) && lane == 0) bulk_wait_group0();
     __syncwarp();
 }
 
@@ -918,6 +1020,10 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     if (CG == 2) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The next kernel may start its prologue on SMs this grid leaves; this
+    // one touches global memory only once the previous kernel is done.
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) producer_loop<MODE, CG, BNT>(p, base, bar0, rank, abort_flag);
@@ -1006,13 +1112,14 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     cfg.blockDim = dim3(num_threads<MODE>(), 1, 1);
     cfg.dynamicSmemBytes = Cfg<MODE, CG, BNT>::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    tpi::pdl_attribute(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -1197,6 +1304,17 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
             if (!make_map(&p.mapB[i], bs[i], 2, dB, sA, bB, err)) return TP_ERR_CUDA;
         }
         p.b_rows0 = static_cast<int>(a.B0_rows);
+        if (a.mode == GEMM_COL_ACT && kPairTiles == 2 && a.ldo % 8 == 0 &&
+            (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0) {
+            // Output boxes of 32 x 32 bf16, 64-byte swizzle (rows and columns
+            // past the output are clipped).
+            const uint32_t box_o[2] = {EPI_BOX, EPI_BOX};
+            const uint64_t dO[2] = {(uint64_t)a.N, (uint64_t)a.M};
+            const uint64_t sO[1] = {(uint64_t)a.ldo * 2};
+            if (!make_map(&p.mapO[0], a.out, 2, dO, sO, box_o, err, CU_TENSOR_MAP_SWIZZLE_64B))
+                return TP_ERR_CUDA;
+            p.o_staged = 1;
+        }
         p.qkv_ws = static_cast<int>(a.qkv_ws);
         p.qkv_qw = static_cast<int>(a.qkv_qw);
         p.qkv_kvw = static_cast<int>(a.qkv_kvw);

@@ -4,10 +4,35 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <string>
 
 namespace tpi {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes (its prologue overlaps that
+// kernel's tail).  Every kernel launched this way calls pdl_wait() before it
+// touches global memory.
+inline void pdl_attribute(cudaLaunchAttribute& a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    pdl_attribute(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Kinds of GEMM the tcgen05 kernel implements.  D[m][n] = sum_k A[m][k] B[n][k].
 enum GemmMode {

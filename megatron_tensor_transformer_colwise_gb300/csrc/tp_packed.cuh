@@ -1,13 +1,14 @@
 // tp_packed.cuh -- packed two-lane FP32 arithmetic and a three-way maximum
-// for the attention forward's per-row softmax math (sm_100 family PTX).
+// for per-element epilogue math: the attention forward's softmax and the
+// colwise GEMM's activation (sm_100 family PTX).
 #pragma once
 #include <cstdint>
 
 namespace tpk {
 
 // Two fp32 values in one 64-bit register pair for the packed FP32
-// instructions (fma.rn.f32x2, add.rn.f32x2: each half rounds as the
-// scalar instruction does), which halve the instruction count of per-element math.
+// instructions (fma/add/mul.rn.f32x2: each half rounds as the scalar
+// instruction does), which halve the instruction count of per-element math.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -24,6 +25,11 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 // Maximum of three (PTX max.f32 with three sources).
