@@ -251,6 +251,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The next kernel may start its prologue on SMs this grid leaves; this
+    // one touches global memory only once the previous kernel is done.
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -589,6 +593,8 @@ constexpr int PREP_MAX_HEADS = 1024;
 __global__ void __launch_bounds__(PREP_THREADS) attn_bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O, long long ld, int heads,
     int batch, int seq, long long seq_pad, float* __restrict__ dstat, float* __restrict__ dq, long long ld_dq) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float dsum[PREP_MAX_HEADS];
     const long long rb = blockIdx.x;
     const int b = static_cast<int>(rb / seq_pad);
@@ -628,6 +634,8 @@ __global__ void __launch_bounds__(PREP_THREADS) attn_bwd_prep_kernel(
 // out[row][c] = bf16(acc[row][c]) for c < n (n % 8 == 0).
 __global__ void attn_bwd_dq_cast_kernel(const float* __restrict__ acc, long long ld_acc, long long rows,
                                         int n, __nv_bfloat16* __restrict__ out, long long ld_out) {
+    pdl_trigger();
+    pdl_wait();
     const long long per_row = n / 8;
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= rows * per_row) return;
@@ -687,6 +695,10 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
             return TP_ERR_UNSUPPORTED;
         }
         const long long blocks = static_cast<long long>(a.batch) * a.seq_pad;
+        // Plain launches: with programmatic dependent launch the three
+        // kernels measured 0.6% slower (1187 vs 1180 us per block backward
+        // on one GB300), the many small CTAs of the next kernel waiting
+        // beside the last wave.  Their griddepcontrol calls are then no-ops.
         attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), PREP_THREADS, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16*>(a.dO), reinterpret_cast<const __nv_bfloat16*>(a.O),
             a.ld_do, a.heads, a.batch, a.seq, a.seq_pad, a.dstat, a.dq, a.ld_dq);

@@ -321,6 +321,8 @@ __global__ void __launch_bounds__(RB_THREADS) rmsnorm_bwd_kernel(const __nv_bflo
                                                                 const __nv_bfloat16* __restrict__ res,
                                                                 int h, float eps,
                                                                 __nv_bfloat16* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[2][RB_THREADS / 32];
     const long long row = blockIdx.x;
     const int nv = h / 8;
@@ -397,6 +399,8 @@ constexpr int CS_X = 4, CS_Y = 128;
 __global__ void __launch_bounds__(CS_X * CS_Y) colsum_kernel(const __nv_bfloat16* __restrict__ x,
                                                             long long rows, int h,
                                                             float* __restrict__ out, int accumulate) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float part[CS_Y][CS_X * 8 + 1];
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int col = (blockIdx.x * CS_X + tx) * 8;
@@ -549,10 +553,13 @@ int rmsnorm_bwd_launch(const void* x, const void* g, const void* res, int64_t ro
     const __nv_bfloat16* R = reinterpret_cast<const __nv_bfloat16*>(res);
     __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(out);
     const unsigned grid = static_cast<unsigned>(rows);
-    if (nv <= RB_THREADS) rmsnorm_bwd_kernel<1><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
-    else if (nv <= 2 * RB_THREADS) rmsnorm_bwd_kernel<2><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
-    else if (nv <= 4 * RB_THREADS) rmsnorm_bwd_kernel<4><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
-    else if (nv <= 8 * RB_THREADS) rmsnorm_bwd_kernel<8><<<grid, RB_THREADS, 0, stream>>>(X, G, R, h, eps, O);
+    if (nv <= RB_THREADS) launch_pdl(rmsnorm_bwd_kernel<1>, dim3(grid), dim3(RB_THREADS), 0, stream, X, G, R, h, eps, O);
+    else if (nv <= 2 * RB_THREADS)
+        launch_pdl(rmsnorm_bwd_kernel<2>, dim3(grid), dim3(RB_THREADS), 0, stream, X, G, R, h, eps, O);
+    else if (nv <= 4 * RB_THREADS)
+        launch_pdl(rmsnorm_bwd_kernel<4>, dim3(grid), dim3(RB_THREADS), 0, stream, X, G, R, h, eps, O);
+    else if (nv <= 8 * RB_THREADS)
+        launch_pdl(rmsnorm_bwd_kernel<8>, dim3(grid), dim3(RB_THREADS), 0, stream, X, G, R, h, eps, O);
     else {
         if (err) *err = "RMSNorm backward supports hidden <= 8192";
         return TP_ERR_UNSUPPORTED;
@@ -564,8 +571,8 @@ int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate
                   cudaStream_t stream, std::string* err) {
     if (h == 0) return TP_OK;
     const unsigned gx = static_cast<unsigned>((h / 8 + CS_X - 1) / CS_X);
-    colsum_kernel<<<gx, dim3(CS_X, CS_Y), 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x),
-                                                      rows, h, out, accumulate);
+    launch_pdl(colsum_kernel, dim3(gx), dim3(CS_X, CS_Y), 0, stream, reinterpret_cast<const __nv_bfloat16*>(x),
+               static_cast<long long>(rows), h, out, accumulate);
     return check_launch("column-sum kernel", err);
 }
 

@@ -54,6 +54,8 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 __global__ void __launch_bounds__(EMB_WARPS * 32) vocab_embedding_kernel(
     const int32_t* __restrict__ ids, long long M, const __nv_bfloat16* __restrict__ E, long long v,
     int h, __nv_bfloat16* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     const long long m = static_cast<long long>(blockIdx.x) * EMB_WARPS + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (m >= M) return;
@@ -79,6 +81,8 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
 __global__ void __launch_bounds__(CE_THREADS) ce_shard_stats_kernel(
     const __nv_bfloat16* __restrict__ logits, long long M, long long v, int t,
     const int32_t* __restrict__ labels, float* __restrict__ stats) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ MS red[CE_THREADS / 32];
     const long long m = blockIdx.x;
     const int i = blockIdx.y;
@@ -125,6 +129,8 @@ __global__ void __launch_bounds__(CE_THREADS) ce_shard_stats_kernel(
 // One thread per token: combine the t shards' (max, sum, target).
 __global__ void ce_combine_kernel(const float* __restrict__ stats, long long M, long long v, int t,
                                   const int32_t* __restrict__ labels, float* __restrict__ loss) {
+    pdl_trigger();
+    pdl_wait();
     const long long m = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (m >= M) return;
     const long long lab = labels[m];
@@ -163,8 +169,9 @@ int vocab_embedding_launch(const int32_t* ids, int64_t M, const void* E, int64_t
                            cudaStream_t stream, std::string* err) {
     if (M == 0) return TP_OK;
     const long long blocks = (M + EMB_WARPS - 1) / EMB_WARPS;
-    vocab_embedding_kernel<<<(unsigned)blocks, EMB_WARPS * 32, 0, stream>>>(
-        ids, M, reinterpret_cast<const __nv_bfloat16*>(E), v, h, reinterpret_cast<__nv_bfloat16*>(out));
+    launch_pdl(vocab_embedding_kernel, dim3((unsigned)blocks), dim3(EMB_WARPS * 32), 0, stream, ids,
+               static_cast<long long>(M), reinterpret_cast<const __nv_bfloat16*>(E), static_cast<long long>(v), h,
+               reinterpret_cast<__nv_bfloat16*>(out));
     return check("embedding kernel", err);
 }
 
@@ -172,11 +179,14 @@ int vocab_ce_launch(const void* logits, int64_t M, int64_t v, int t, const int32
                     float* stats, float* loss, cudaStream_t stream, std::string* err) {
     if (M == 0) return TP_OK;
     dim3 grid((unsigned)M, (unsigned)t);
-    ce_shard_stats_kernel<<<grid, CE_THREADS, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(logits), M, v, t, labels, stats);
+    launch_pdl(ce_shard_stats_kernel, grid, dim3(CE_THREADS), 0, stream,
+               reinterpret_cast<const __nv_bfloat16*>(logits), static_cast<long long>(M), static_cast<long long>(v), t,
+               labels, stats);
     int rc = check("cross-entropy statistics kernel", err);
     if (rc) return rc;
-    ce_combine_kernel<<<(unsigned)((M + 255) / 256), 256, 0, stream>>>(stats, M, v, t, labels, loss);
+    launch_pdl(ce_combine_kernel, dim3((unsigned)((M + 255) / 256)), dim3(256), 0, stream,
+               static_cast<const float*>(stats), static_cast<long long>(M), static_cast<long long>(v), t, labels,
+               loss);
     return check("cross-entropy combine kernel", err);
 }
 
