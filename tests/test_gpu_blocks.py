@@ -191,6 +191,38 @@ def test_layer_forward_is_bit_reproducible(s):
     assert np.array_equal(Y1, Y2)
 
 
+def test_layer_chain_without_syncs_matches_synced_chain():
+    # Eight full-size layer steps, each step's output the next step's input,
+    # sharing one workspace.  Launched back to back on one stream, the next
+    # kernel may start its prologue under the previous kernel's tail
+    # (programmatic dependent launch); every kernel touches global memory
+    # only after the previous one has completed.  The same chain with a
+    # synchronize after every step must give the same bits.
+    s = SHAPES["layer"]
+    inp = synth.workload_inputs(s)
+    plan = plan_for(s)
+    ws, nws = workspace(plan, tp.TP_OP_LAYER)
+    wd = {k: dev(v) for k, v in inp.items() if k != "X"}
+    steps = 8
+
+    def chain(sync_each):
+        xs = [dev(inp["X"])]
+        for _ in range(steps):
+            y = torch.empty(s.tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+            tp.tp_layer_forward(plan, xs[-1], wd, y, ws, nws)
+            if sync_each:
+                torch.cuda.synchronize()
+            xs.append(y)
+        sync_ok(plan)
+        return xs[1:]
+
+    free = chain(False)
+    synced = chain(True)
+    for k in range(steps):
+        assert torch.equal(free[k].view(torch.int16), synced[k].view(torch.int16)), f"step {k}"
+    assert torch.isfinite(free[-1].float()).all()
+
+
 def test_layer_forward_replays_from_a_cuda_graph():
     # The library launches only on the caller's stream, so the layer can be
     # captured once and replayed; the replay gives the eager result's bits.
