@@ -83,10 +83,12 @@ enum {
 constexpr int TWO_CTA_SMEM = 115712;
 
 // Shared memory of one CTA (two CTAs share an SM):
-//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | barriers
+//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | O staging | barriers
 // (P lives in TMEM, over the first half of its S buffer).  The kernel checks
 // at run time that its 1024-aligned layout fits the allocation and
 // otherwise stops with an error flag, touching nothing.
+constexpr int STG_BOX = 32 * 64;  // 32 rows x 32 bf16 (64-byte swizzle)
+
 template <int D>
 struct Layout {
     static constexpr int QT = QB * D * 2;
@@ -94,7 +96,8 @@ struct Layout {
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = QT;
     static constexpr int V_OFF = K_OFF + 2 * KT;
-    static constexpr int BAR_OFF = V_OFF + 2 * KT;
+    static constexpr int STG_OFF = V_OFF + 2 * KT;  // O staging: one 32 x 32 bf16 box per softmax warp
+    static constexpr int BAR_OFF = STG_OFF + 4 * STG_BOX;
     static constexpr int DATA = BAR_OFF + 8 * NUM_BARS + 16;
     static constexpr int SMEM = DATA + 1024 <= TWO_CTA_SMEM ? DATA + 1024 : TWO_CTA_SMEM;
     static constexpr int TMEM_COLS = 2 * KB + D <= 256 ? 256 : 512;  // S0 | S1 | O
@@ -103,6 +106,9 @@ struct Layout {
 struct AttnParams {
     CUtensorMap map_q;   // the QKV buffer: dims {t * W, tokens}, box {64, 128}
     CUtensorMap map_kv;  // the same buffer, box {64, 64}
+    CUtensorMap map_o;   // O as {ld_o, seq, batch}, box {32, 32, 1}, 64-byte swizzle; rows
+                         // past a sequence's end are outside it and not written
+    int o_tma;           // 1: O leaves by TMA stores through map_o
     __nv_bfloat16* o;
     long long ld_o;
     int seq, heads, kv_heads, t, heads_per_shard, shard_w, q_w, kv_w;
@@ -129,6 +135,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+
+// Tiled TMA store of a 3-D box (elements outside the map are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 
 // Bring a box of a tensor map into L2 without writing shared memory.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
@@ -522,12 +537,38 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 p.lse[(static_cast<long long>(x.j) * p.batch + x.b) * p.seq_pad + qpos] = m_ref + log2f(l_sum);
             __nv_bfloat16* orow = p.o + static_cast<long long>(x.tok0 + qpos) * p.ld_o +
                                   static_cast<long long>(x.j) * D;
+            // O / l as bf16, 32 columns at a time.  With a TMA map the warp
+            // writes its 32 rows into its shared-memory box (16-byte piece u
+            // of row l at l * 64 + (u ^ ((l / 2) % 4)) * 16) and lane 0
+            // stores the box; otherwise each thread stores its row.
+            const int row0 = q0 + q * 32;
+            const uint32_t box = base + L::STG_OFF + static_cast<uint32_t>(q) * STG_BOX;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_off + 2 * KB + c * 32, o);
                 tmem_ld_wait();
-                if (qpos < p.seq) {
+                if (p.o_tma) {
+                    if (lane == 0) bulk_wait_group_read0();  // the box's previous store has read it
+                    __syncwarp();
+                    const uint32_t srow = box + static_cast<uint32_t>(lane) * 64u;
+                    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[u * 8 + 2 * e + 1]) * inv);
+                        st_shared_v4(srow + ((static_cast<uint32_t>(u) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
+                    }
+                    fence_proxy_async_smem();  // visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.seq) {
+                        tma_store_3d(&p.map_o, box, x.j * D + c * 32, row0, x.b);
+                        bulk_commit_group();
+                    }
+                } else if (qpos < p.seq) {
 #pragma unroll
                     for (int g8 = 0; g8 < 4; ++g8) {
                         uint32_t wv[4];
@@ -539,12 +580,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                     }
                 }
             }
-            // O is in registers and written: the next item's first PV may
+            // O has been read from TMEM: the next item's first PV may
             // overwrite it.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
         }
+        // The O stores must have completed before the CTA exits.
+        if (lane == 0) bulk_wait_group0();
     }
     __syncwarp();
     tc_fence_before();
@@ -585,6 +628,24 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
             if (err) *err = "cuTensorMapEncodeTiled (attention QKV) failed: " + std::to_string((int)r);
             return TP_ERR_CUDA;
         }
+    }
+    // O as {columns, position, sequence} for the TMA stores of the epilogue
+    // (16-byte aligned base and row stride); otherwise per-thread stores.
+    if (a.ld_o % 8 == 0 && (reinterpret_cast<uintptr_t>(a.O) & 15u) == 0) {
+        cuuint64_t odims[3] = {static_cast<cuuint64_t>(a.ld_o), static_cast<cuuint64_t>(a.seq),
+                               static_cast<cuuint64_t>(a.batch)};
+        cuuint64_t ostr[2] = {static_cast<cuuint64_t>(a.ld_o) * 2,
+                              static_cast<cuuint64_t>(a.ld_o) * 2 * static_cast<cuuint64_t>(a.seq)};
+        cuuint32_t obox[3] = {32, 32, 1};
+        cuuint32_t oestr[3] = {1, 1, 1};
+        CUresult r = encode(&p.map_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.O, odims, ostr, obox, oestr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            if (err) *err = "cuTensorMapEncodeTiled (attention O) failed: " + std::to_string((int)r);
+            return TP_ERR_CUDA;
+        }
+        p.o_tma = 1;
     }
     p.o = reinterpret_cast<__nv_bfloat16*>(a.O);
     p.ld_o = a.ld_o;
