@@ -185,8 +185,16 @@ __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
     return x;
 }
 
-// Persistent: CTA c takes items c, c + gridDim.x, ...  Every role walks the
-// same item list; K/V ring stages, S buffers and their barrier phases run on
+// The k-th item of CTA c in a grid of g CTAs: rounds of g items, taken
+// left to right in even rounds and right to left in odd ones, so the CTA
+// that took a round's longest item takes the next round's shortest.  Item
+// lengths fall with the index; a plain c, c + g, ... order gives CTA 0 the
+// longest item of every round (one sequence of 2048 tokens, 512 items on
+// 304 CTAs: 46 key blocks for CTA 0 against 28.6 on average).
+__device__ __forceinline__ int item_at(int k, int c, int g) { return k * g + ((k & 1) ? g - 1 - c : c); }
+
+// Persistent: CTA c takes items item_at(0, c), item_at(1, c), ...  Every
+// role walks the same item list; K/V ring stages, S buffers and their barrier phases run on
 // one block count across items, so the next item's Q and first K/V blocks
 // load while the current item finishes.
 template <int D>
@@ -281,12 +289,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 return true;
             };
             int li = 0;
-            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+            for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
                 const Item x = item_of<D>(p, w);
                 // The next item's Q is read from HBM for the first time: start
                 // that read now, so its TMA load later hits L2.
-                if (w + dw < n_items) {
-                    const Item y = item_of<D>(p, w + dw);
+                if (item_at(li + 1, w0, dw) < n_items) {
+                    const Item y = item_of<D>(p, item_at(li + 1, w0, dw));
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(&p.map_q, y.qcol + 64 * c, y.tok0 + y.q0);
                 }
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             const uint64_t kdesc0 = sdesc_sw128(sK), kdesc1 = sdesc_sw128(sK + L::KT);
             bool ok = true;
             int gb = 0, li = 0;
-            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+            for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
                 const int nkb = item_of<D>(p, w).nkb;
                 if (!mbar_wait(bar(B_Q_FULL), static_cast<uint32_t>(li) & 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             const uint64_t vdesc0 = sdesc_sw128_mn(sV, KBOX, 1024), vdesc1 = sdesc_sw128_mn(sV + L::KT, KBOX, 1024);
             bool ok = true;
             int gb = 0, li = 0;
-            for (int w = w0; w < n_items && ok; w += dw, ++li) {
+            for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
                 const int nkb = item_of<D>(p, w).nkb;
                 for (int kb = 0; kb < nkb && ok; ++kb, ++gb) {
                     const int vst = gb & 1;
@@ -420,7 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         bool ok = true;
         int gb = 0, li = 0;
-        for (int w = w0; w < n_items && ok; w += dw, ++li) {
+        for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
             const Item x = item_of<D>(p, w);
             const int q0 = x.q0;
             const int qpos = q0 + r;
