@@ -12,12 +12,14 @@
 // a running maximum subtracted, no dropout, no rotary embedding.
 //
 // Work item: 128 query rows of one query head and sequence.  A persistent
-// grid of two CTAs per SM (7 warps, 256 TMEM columns and ~97 KB of shared
-// memory each) walks the items longest first, so one CTA's softmax overlaps
-// the other's tensor-core work and the next item's loads overlap the
-// current item's last blocks:
+// grid of two CTAs per SM (7 warps, 256 TMEM columns and ~105 KB of shared
+// memory each) walks the items longest first, in rounds of alternating
+// direction (item_at), so one CTA's softmax overlaps the other's
+// tensor-core work and the next item's loads overlap the current item's
+// last blocks:
 //   warp 0      TMA: Q once, then K and V blocks of 64 keys (2-stage rings,
-//               K one block ahead) from the shard-blocked QKV buffer.
+//               K one block ahead) from the shard-blocked QKV buffer; an L2
+//               prefetch of the next item's Q.
 //   warp 1      TMEM owner and S issuer: S = Q K^T (128 x 64, fp32, two TMEM
 //               buffers so S of block j+1 is computed while the softmax works
 //               on block j).
@@ -32,7 +34,8 @@
 //               apply the causal mask, online softmax with exp2, write P as
 //               bf16 over the first half of the same S buffer (tcgen05.st),
 //               rescale the O row in TMEM when its reference maximum moves,
-//               and finally write O / l as bf16.
+//               and finally write O / l as bf16 through a per-warp shared-
+//               memory box and a TMA store.
 // A buffer is reused for S of block j+2 once the PV of block j, which reads
 // its P, has completed; the softmax warps wait for the previous PV to
 // complete only when they rescale O in place.
