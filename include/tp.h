@@ -33,7 +33,14 @@
  *    library allocates device memory only in tp_plan_create (a 256-byte
  *    status word) and never frees caller memory.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
- *    only enqueue work; nothing synchronises implicitly.
+ *    only enqueue work; nothing synchronises implicitly.  The library's
+ *    kernels use programmatic dependent launch: a kernel may start its
+ *    prologue while the previous kernel of the stream is finishing, and
+ *    touches global memory only once that kernel has completed.  Stream
+ *    order therefore holds as usual for the caller's work.  A caller kernel
+ *    that is itself launched with programmatic stream serialization right
+ *    after one of the library's must execute griddepcontrol.wait before it
+ *    reads the library's outputs.
  *  - Every call returns TP_OK or a TP_ERR_* code, and on error launches
  *    nothing ([diff] "한계": an error instead of a silent fallback;
  *    "제약 조건 및 검증": checks happen before any weight is touched).
