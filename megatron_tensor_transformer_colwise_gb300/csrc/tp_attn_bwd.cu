@@ -130,6 +130,8 @@ struct BwdParams {
     CUtensorMap map_q;   // the same buffer, box {64, 64}
     CUtensorMap map_do;  // dO [tokens][a d], box {64, 64}
     CUtensorMap map_dq;  // fp32 dQ accumulator [tokens][a d], box {32, 64}, reduce-add target
+    CUtensorMap map_dkv; // dK | dV as {ld_dkv, seq, batch}, box {32, 32, 1}, 64-byte swizzle
+    int dkv_tma;         // 1: dK and dV leave by TMA stores through map_dkv
     const float* lse;    // [a][batch][seq_pad]
     const float* dstat;  // [a][batch][seq_pad]
     float* dq;           // [tokens][ld_dq] fp32 accumulator
@@ -148,6 +150,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > 200000000ull) break;  // 200 ms
     }
+}
+
+// Tiled TMA store of a 3-D box (elements outside the map are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 // 2^x with the SFU's approximate exp2 (PTX ex2.approx.ftz.f32).
@@ -508,12 +519,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 const float mul = which ? p.scale : 1.0f;
                 __nv_bfloat16* dst = p.dkv + static_cast<long long>(tok0 + (row_ok ? kpos : 0)) * p.ld_dkv +
                                      (which ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD + c0;
+                // With a TMA map the warp stages its 32 rows x 32 columns in a
+                // 2 KB box (64-byte swizzle) over the Q ring, which no product
+                // reads any more (all of them have completed), and lane 0
+                // stores the box; rows past the sequence end fall outside the
+                // map.  Otherwise each thread stores its row.
+                const int krow0 = k0 + q4 * 32;
+                const uint32_t box = base + OFF_Q + static_cast<uint32_t>(warp - 2) * 2048u;
+                const int col_base = static_cast<int>((which ? p.dk_col : p.dv_col) + static_cast<long long>(g) * HD) + c0;
 #pragma unroll 1
                 for (int c = 0; c < SPAN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c0 + c * 32, v);
                     tmem_ld_wait();
-                    if (row_ok) {
+                    if (p.dkv_tma) {
+                        if (lane == 0) bulk_wait_group_read0();  // the box's previous store has read it
+                        __syncwarp();
+                        const uint32_t srow = box + static_cast<uint32_t>(lane) * 64u;
+                        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(v[g8 * 8 + 2 * e]) * mul,
+                                                   __uint_as_float(v[g8 * 8 + 2 * e + 1]) * mul);
+                            st_shared_v4(srow + ((static_cast<uint32_t>(g8) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                        }
+                        fence_proxy_async_smem();  // visible to the TMA engine
+                        __syncwarp();
+                        if (lane == 0 && krow0 < p.seq) {
+                            tma_store_3d(&p.map_dkv, box, col_base + c * 32, krow0, b);
+                            bulk_commit_group();
+                        }
+                    } else if (row_ok) {
 #pragma unroll
                         for (int g8 = 0; g8 < 4; ++g8) {
                             uint32_t w[4];
@@ -527,6 +566,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 }
             }
         }
+        // The dK / dV stores must have completed before the CTA exits.
+        if (lane == 0) bulk_wait_group0();
     } else {
         // ------------------------------------------------------------ dQ accumulation (warps 10-13)
         // Each warp owns 32 head dimensions: its [64 queries][32 d] slice of
@@ -741,6 +782,26 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
         p.ld_dq = a.ld_dq;
         p.dkv = reinterpret_cast<__nv_bfloat16*>(a.dqkv);
         p.ld_dkv = a.ld_dqkv;
+        // dK and dV as {columns, position, sequence} for the TMA stores of
+        // the epilogue (16-byte aligned base and row stride, column offsets
+        // multiples of 8); otherwise per-thread stores.
+        if (a.ld_dqkv % 8 == 0 && a.dk_col % 8 == 0 && a.dv_col % 8 == 0 &&
+            (reinterpret_cast<uintptr_t>(a.dqkv) & 15u) == 0) {
+            cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.ld_dqkv), static_cast<cuuint64_t>(a.seq),
+                                  static_cast<cuuint64_t>(a.batch)};
+            cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_dqkv) * 2,
+                                     static_cast<cuuint64_t>(a.ld_dqkv) * 2 * static_cast<cuuint64_t>(a.seq)};
+            cuuint32_t box[3] = {32, 32, 1};
+            cuuint32_t estr[3] = {1, 1, 1};
+            CUresult r = encode(&p.map_dkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dqkv, dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                if (err) *err = "cuTensorMapEncodeTiled (dK / dV) failed: " + std::to_string((int)r);
+                return TP_ERR_CUDA;
+            }
+            p.dkv_tma = 1;
+        }
         p.dk_col = a.dk_col;
         p.dv_col = a.dv_col;
         p.seq_pad = a.seq_pad;
