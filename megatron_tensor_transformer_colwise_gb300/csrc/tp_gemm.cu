@@ -66,13 +66,13 @@ constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
 // outlast the next tile's main loop: the activation gradient with its loads
 // and three stores, and the GeLU epilogue of short-K problems (measured on
 // GB300: the 2048 x 4096 x 1024 GeLU GEMM in 22.9 us with 8 warps, 24.8 us
-// with 4).
-#ifndef TP_GEMM_EPI_WARPS_FWD
-#define TP_GEMM_EPI_WARPS_FWD 4
-#endif
+// with 4).  The other forward modes keep 4: with 8 the layer step took
+// 2.170 ms against 2.127 ms (W1/W3 1036 against 1011 us), and 4 keeps one
+// warp per 128-column slice of a narrow rowwise tile, whose sum of squares
+// it writes whole.
 template <int MODE>
 __host__ __device__ constexpr int epi_warps() {
-    return (MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : TP_GEMM_EPI_WARPS_FWD;
+    return (MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : 4;
 }
 template <int MODE>
 __host__ __device__ constexpr int num_threads() {
