@@ -40,6 +40,16 @@ from synth import SHAPES, Shape  # noqa: E402
 METRIC = ("sharded-MLP/attn TFLOP/s & % BF16 peak; partial-reduce GB/s & % HBM (1×GB300)")
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Context denominators: the vendor's dense BF16 figure (no 2:4 sparsity) and
+# the tensor rate per SM and clock that tcgen05 kind::f16 issues at (a
+# 128 x 256 x 16 MMA step every 128 cycles: 8192 FLOP per SM per clock).
+SPEC_BF16_TFLOPS = 2250.0
+SPEC_BF16_SOURCE = "NVIDIA GB300 dense BF16, 2.25 PFLOP/s per GPU without sparsity (datasheet)"
+TENSOR_FLOP_PER_SM_CLK = 8192.0
+NOMINAL_HBM_GBS = 8000.0
+# A timed region shorter than this runs at the burst clock (the power cap
+# needs about a second of full load to pull the clock down).
+BURST_REGION_S = 1.0
 
 
 # ------------------------------------------------------------------ work model
@@ -100,6 +110,31 @@ def attn_backward_kernel_flops(s: Shape):
     ]
 
 
+def tensor_roofline(achieved, peaks, peak_src, timed_s, sm_mhz, n_sm):
+    """Fractions of a contraction's achieved TFLOP/s.  `peak`/`frac` use the
+    measured burst peak when the timed region is shorter than BURST_REGION_S
+    and the measured sustained one otherwise; the other fractions are
+    context: both measured peaks, the vendor's dense figure, and the tensor
+    rate at the SM clock sampled during the timed region."""
+    burst = timed_s < BURST_REGION_S
+    key = "bf16_tflops" if burst else "bf16_tflops_sustained"
+    out = {"peak": peaks[key], "frac": achieved / peaks[key],
+           "peak_source": f"{peak_src} {key} (timed region {timed_s:.3f} s: "
+                          f"{'under' if burst else 'over'} {BURST_REGION_S:.0f} s, "
+                          f"{'burst' if burst else 'sustained'} clocks)",
+           "frac_of_burst": achieved / peaks["bf16_tflops"],
+           "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+           "frac_of_spec": achieved / SPEC_BF16_TFLOPS, "spec_peak": SPEC_BF16_TFLOPS,
+           "spec_source": SPEC_BF16_SOURCE}
+    if sm_mhz:
+        at_clock = n_sm * TENSOR_FLOP_PER_SM_CLK * sm_mhz * 1e6 / 1e12
+        out["per_clock"] = {"sm_mhz": sm_mhz, "n_sm": n_sm,
+                            "tensor_peak_at_clock": at_clock,
+                            "frac_at_clock": achieved / at_clock,
+                            "flop_per_sm_clk": TENSOR_FLOP_PER_SM_CLK}
+    return out
+
+
 def layer_flops(s: Shape):
     return sum(v for _, v in layer_kernel_flops(s))
 
@@ -137,7 +172,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", self.gpu_id],
+                 "-lms", "50", "-i", self.gpu_id],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -205,8 +240,9 @@ def gpu_id_for(torch, dev_index: int) -> str:
 
 def profiled_traffic(kernel_name: str):
     """DRAM bytes per launch of `kernel_name` from the committed ncu summary
-    (profiles/dram_traffic.json), or None when the GEMM kernel sources have
-    changed since those counters were taken."""
+    (profiles/dram_traffic.json) with the command that took them and the
+    spread over the recorded captures, or None when the GEMM kernel sources
+    have changed since those counters were taken."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as fh:
@@ -217,7 +253,11 @@ def profiled_traffic(kernel_name: str):
                 h.update(fh.read())
         if h.hexdigest()[:16] != entry["source_sha256_16"]:
             return None
-        return entry["bytes_per_launch"]
+        out = {"bytes_per_launch": entry["bytes_per_launch"], "source": entry.get("command")}
+        if "captures" in entry:
+            vals = [c["bytes_per_launch"] for c in entry["captures"]]
+            out["spread"] = {"captures": len(vals), "min": min(vals), "max": max(vals)}
+        return out
     except Exception:
         return None
 
@@ -575,7 +615,9 @@ def time_blocks(tp, torch, device, stream, peaks, reps=20):
         us = sum(e0.elapsed_time(e1) for e0, e1 in evs) / reps * 1e3
         tfl = flops / (us / 1e6) / 1e12
         out[name] = {"workload": desc, "us": us, "tflops": tfl, "frac_bf16": tfl / peaks["bf16_tflops"],
-                     "gflop": flops / 1e9, "l2": "L2 flushed before every timed iteration"}
+                     "frac_of_spec": tfl / SPEC_BF16_TFLOPS,
+                     "gflop": flops / 1e9, "l2": "L2 flushed before every timed iteration",
+                     "peak_source": "measured bf16_tflops (burst: each block timed alone)"}
         del inp, ws, Z
     del flush
     return out
@@ -658,26 +700,38 @@ def run_ours(args):
     per_kernel = [v / args.steps for v in per_kernel]
     total_k = sum(per_kernel)
     kbytes = layer_kernel_bytes(s)
+    timed_s = ms_local * args.steps / 1e3
+    sm_mhz = clocks.get("sm_mhz") if clocks else None
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
     kernels = []
     for (name, fl), msk in zip(kf, per_kernel):
         row = {"name": name, "us": msk * 1e3, "share": msk / total_k if total_k else None}
         if fl > 0:
             row["tflops"] = fl / (msk / 1e3) / 1e12
-            row["frac_bf16_sustained"] = row["tflops"] / peaks["bf16_tflops_sustained"]
+            rl = tensor_roofline(row["tflops"], peaks, peak_src, timed_s, sm_mhz, n_sm)
+            row["frac_bf16"] = rl["frac"]
+            row["frac_of_spec"] = rl["frac_of_spec"]
+            if "per_clock" in rl:
+                row["frac_at_clock"] = rl["per_clock"]["frac_at_clock"]
         else:
             row["gbs"] = kbytes[name] / (msk / 1e3) / 1e9
             row["frac_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+            row["frac_of_8tbs"] = row["gbs"] / NOMINAL_HBM_GBS
         kernels.append(row)
     dom = max(range(nk), key=lambda i: per_kernel[i])
     dom_name, dom_fl = kf[dom]
     achieved = dom_fl / (per_kernel[dom] / 1e3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)",
-                "algorithmic_flops_per_launch": dom_fl,
-                "traffic": args.dominant_traffic if args.dominant_traffic is not None
-                else profiled_traffic(dom_name)}
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "unit": "TFLOP/s",
+                "algorithmic_flops_per_launch": dom_fl, "us_per_launch": per_kernel[dom] * 1e3}
+    roofline.update(tensor_roofline(achieved, peaks, peak_src, timed_s, sm_mhz, n_sm))
+    if sm_mhz:
+        roofline["us_x_mhz"] = per_kernel[dom] * 1e3 * sm_mhz
+    tr = args.dominant_traffic if args.dominant_traffic is not None else profiled_traffic(dom_name)
+    roofline["traffic"] = tr["bytes_per_launch"] if isinstance(tr, dict) else tr
+    if isinstance(tr, dict):
+        roofline["traffic_source"] = tr.get("source")
+        if "spread" in tr:
+            roofline["traffic_spread"] = tr["spread"]
 
     # The g reduction as a PARTIALS-mode kernel over the layer's partials.
     n = s.tokens * s.hidden
@@ -699,7 +753,7 @@ def run_ours(args):
     red_gbs = rb / (red_us / 1e6) / 1e9
     reduce_line = {"bound": "hbm", "kernel": "tp_reduce_partials (t=8 fp32 partials + residual)",
                    "achieved": red_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": red_gbs / peaks["hbm_gbs"], "frac_of_8tbs": red_gbs / 8000.0,
+                   "frac": red_gbs / peaks["hbm_gbs"], "frac_of_8tbs": red_gbs / NOMINAL_HBM_GBS,
                    "us": red_us, "bytes_per_launch": rb,
                    "peak_source": f"{peak_src} hbm_gbs (kernel timed alone)",
                    "l2": "inputs 1.07 GB > 129 MB L2"}

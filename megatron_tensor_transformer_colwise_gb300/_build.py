@@ -53,6 +53,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
+    # Objects of translation units that are no longer sources would
+    # otherwise linger beside the library.
+    keep = {src.replace(".cu", ".o") for src in SOURCES}
+    for name in os.listdir(OUT_DIR):
+        if name.endswith(".o") and name not in keep:
+            os.remove(os.path.join(OUT_DIR, name))
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))

@@ -515,3 +515,72 @@ def layer_backward_composed(batch: int, seq: int, a: int, k: int, d: int, X, Wq,
     dxn1, dWq, dWk, dWv, dWo = attention_backward_composed(batch, seq, a, k, xn1, Wq, Wk, Wv, Wo, dh1)
     dX = dh1 + rmsnorm_backward(X, dxn1, eps)
     return (dX, dWq, dWk, dWv, dWo) + grads_mlp
+
+
+# ---------------------------------------------------------------- composed forms for full sizes
+#
+# The same definitions as tpo_mlp, tpo_attention, tpo_layer and
+# tpo_mlp_backward, with every matrix product taken by numpy's matmul (a
+# library primitive used as a step) instead of the plain loops, so that the
+# workloads' full sizes (up to 8192 tokens x 14336 ffn) finish in seconds
+# rather than minutes.  The attention core and the norms stay in the C
+# routines.  Each form is pinned to its all-C counterpart at small sizes.
+
+def _act_np(act: str, U, G=None):
+    """The activation step of "MLP" ("텐서 병렬화"), elementwise in fp64."""
+    if act == "gelu":
+        from scipy.special import erf
+        return 0.5 * U * (1.0 + erf(U / np.sqrt(2.0)))
+    if act == "gelu_tanh":
+        c = np.sqrt(2.0 / np.pi)
+        return 0.5 * U * (1.0 + np.tanh(c * (U + 0.044715 * U * U * U)))
+    if act == "swiglu":
+        return U / (1.0 + np.exp(-U)) * G
+    if act == "none":
+        return U
+    raise ValueError(f"unknown activation {act!r}; valid: gelu, gelu_tanh, swiglu, none")
+
+
+def mlp_composed(act: str, X, W1, W2, W3=None) -> np.ndarray:
+    """Unsharded MLP of tpo_mlp ("MLP": Z = act(X W1^T [(.) X W3^T]) W2^T),
+    matrix products by numpy."""
+    X, W1, W2, W3 = _d(X), _d(W1), _d(W2), _d(W3)
+    U = X @ W1.T
+    G = X @ W3.T if act == "swiglu" else None
+    return _act_np(act, U, G) @ W2.T
+
+
+def attention_composed(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo) -> np.ndarray:
+    """Unsharded attention block of tpo_attention ("셀프 어텐션"): projections
+    by numpy, the causal GQA core by tpo_attention_core."""
+    X, Wq, Wk, Wv, Wo = map(_d, (X, Wq, Wk, Wv, Wo))
+    O = attention_core(batch, seq, a, k, d, X @ Wq.T, X @ Wk.T, X @ Wv.T)
+    return O @ Wo.T
+
+
+def layer_composed(batch: int, seq: int, a: int, k: int, d: int, X, Wq, Wk, Wv, Wo, W1, W3, W2,
+                   eps: float = 1e-5, want_h1: bool = False):
+    """Pre-norm layer of tpo_layer ("통신 연산 f와 g": norm and residual
+    replicated): h1 = x + Attn(RMSNorm(x)), y = h1 + SwiGLU-MLP(RMSNorm(h1)).
+    With want_h1, also returns the residual stream h1."""
+    X = _d(X)
+    h1 = X + attention_composed(batch, seq, a, k, d, rmsnorm(X, eps), Wq, Wk, Wv, Wo)
+    Y = h1 + mlp_composed("swiglu", rmsnorm(h1, eps), W1, W2, W3)
+    return (Y, h1) if want_h1 else Y
+
+
+def mlp_backward_composed(X, W1, W2, dZ, W3):
+    """(dX, dW1, dW3, dW2, db2) of the SwiGLU MLP given dZ, the steps of
+    tpo_mlp_backward with the matrix products by numpy:
+      U = X W1^T, G = X W3^T, H = SiLU(U) (.) G, Z = H W2^T (+ b2)
+      dH = dZ W2, dU = dH (.) G (.) SiLU'(U), dG = dH (.) SiLU(U)
+      dX = dU W1 + dG W3, dW1 = dU^T X, dW3 = dG^T X, dW2 = dZ^T H,
+      db2 = sum over tokens of dZ."""
+    X, W1, W2, dZ, W3 = map(_d, (X, W1, W2, dZ, W3))
+    U, G = X @ W1.T, X @ W3.T
+    s = 1.0 / (1.0 + np.exp(-U))
+    H = U * s * G
+    dH = dZ @ W2
+    dU = dH * G * s * (1.0 + U * (1.0 - s))
+    dG = dH * U * s
+    return (dU @ W1 + dG @ W3, dU.T @ X, dG.T @ X, dZ.T @ H, dZ.sum(axis=0))

@@ -8,7 +8,9 @@ import megatron_tensor_transformer_colwise_gb300 as tp
 import oracle
 import synth
 from synth import SHAPES, Shape
-from gpu_util import assert_close, bf16_bits, dev, host64, plan_for, sync_ok, workspace
+import full_refs
+from gpu_util import (assert_close, assert_layer_contribution_close, bf16_bits, dev,
+                      elementwise_excess_fraction, host64, plan_for, report, sync_ok, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,19 +73,27 @@ def test_small_sequence_parallel_layer(mode):
     ref = oracle.layer_sp(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, s.tp, host64(X_sp),
                           *(host64(inp[n]) for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")))
     assert_close(Y_sp, ref, what="sequence-parallel layer")
-    assert_close(Y_sp - host64(X_sp), ref - host64(X_sp), tol=5e-2, what="SP layer minus residual")
+    # The blocks' own contribution, with the residual stream h1 of the same
+    # layer in the split layout (token row r sits at row perm[r]).
+    X = host64(inp["X"])
+    h1 = X + oracle.attention_sharded(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, s.tp,
+                                      oracle.rmsnorm(X),
+                                      *(host64(inp[n]) for n in ("Wq", "Wk", "Wv", "Wo")))
+    h1_sp = np.empty_like(h1)
+    h1_sp[perm] = h1
+    assert_layer_contribution_close(Y_sp, ref, host64(X_sp), h1_sp, what="SP layer contribution")
 
 
 @pytest.mark.parametrize("mode", SP_MODES, ids=["partials", "fused"])
-def test_full_size_sequence_parallel_layer_sampled_rows(mode):
+def test_full_size_sequence_parallel_layer_full_output(mode):
+    # The split layout is a permutation of the token rows, so the SP layer's
+    # output, read back in token order, is the replicated layer's.
     s = SHAPES["layer"]
-    inp = synth.workload_inputs(s)
+    inp, ref, h1 = full_refs.layer_forward()
     X_sp, Y_sp, perm = _run_sp_layer(s, inp, mode)
-    rows = [0, 5, 300, 2 * s.seq + 1, 3 * s.seq + 1100, s.seq - 1]
-    ref = oracle.layer_rows(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim,
-                            *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")),
-                            rows)
-    got = Y_sp[[perm[r] for r in rows]]
-    X = host64(inp["X"])[rows]
-    assert_close(got, ref, what="SP layer sampled rows")
-    assert_close(got - X, ref - X, tol=5e-2, what="SP layer sampled rows minus residual")
+    got = Y_sp[perm]
+    e = assert_close(got, ref, what="SP layer full output")
+    c = assert_layer_contribution_close(got, ref, host64(inp["X"]), h1,
+                                        what="SP layer full output contribution")
+    report(f"sp layer forward ({'fused' if mode == tp.TP_REDUCE_FUSED else 'partials'})", max_rel=e,
+           contribution=c, frac_beyond=elementwise_excess_fraction(got, ref))

@@ -728,3 +728,46 @@ def test_layer_backward_matches_torch_autograd():
     comp = oracle.layer_backward_composed(batch, seq, a, k, d, X.detach(), *(w.detach() for w in W), dY)
     for n, x, y in zip(names, got, comp):
         assert np.abs(x - y).max() < 1e-11 * max(1.0, np.abs(x).max()), n + " (composed)"
+
+
+# ---------------------------------------------------------------- composed forms (full-size checks)
+
+def test_composed_forward_forms_equal_the_c_forms():
+    # The full-size parity tests use the numpy-matmul compositions; at small
+    # sizes they equal the all-C definitions for every activation, the
+    # attention block and the layer (and the layer's residual stream h1).
+    g = torch.Generator().manual_seed(93)
+    batch, seq, h, a, k, d, f = 2, 9, 16, 4, 2, 4, 40
+    M = batch * seq
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    rnd = lambda n, m: (torch.randn(n, m, generator=g, dtype=torch.float64) * 0.4).numpy()
+    W1, W3, W2 = rnd(f, h), rnd(f, h), rnd(h, f)
+    Wq, Wk, Wv, Wo = rnd(a * d, h), rnd(k * d, h), rnd(k * d, h), rnd(h, a * d)
+    for act in ("gelu", "gelu_tanh", "swiglu", "none"):
+        w3 = W3 if act == "swiglu" else None
+        want = oracle.mlp(act, X, W1, W2, w3)
+        got = oracle.mlp_composed(act, X, W1, W2, w3)
+        assert np.abs(got - want).max() < 1e-12 * np.abs(want).max(), act
+    want = oracle.attention(batch, seq, a, k, d, X, Wq, Wk, Wv, Wo)
+    got = oracle.attention_composed(batch, seq, a, k, d, X, Wq, Wk, Wv, Wo)
+    assert np.abs(got - want).max() < 1e-12 * np.abs(want).max()
+    want = oracle.layer(batch, seq, a, k, d, 2, X, Wq, Wk, Wv, Wo, W1, W3, W2)
+    got, h1 = oracle.layer_composed(batch, seq, a, k, d, X, Wq, Wk, Wv, Wo, W1, W3, W2, want_h1=True)
+    assert np.abs(got - want).max() < 1e-12 * np.abs(want).max()
+    h1_want = X + oracle.attention(batch, seq, a, k, d, oracle.rmsnorm(X), Wq, Wk, Wv, Wo)
+    assert np.abs(h1 - h1_want).max() < 1e-12 * np.abs(h1_want).max()
+    with pytest.raises(ValueError):
+        oracle.mlp_composed("relu", X, W1, W2)
+
+
+def test_composed_mlp_backward_equals_c_form():
+    g = torch.Generator().manual_seed(94)
+    M, h, f = 11, 12, 20
+    X = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    rnd = lambda n, m: (torch.randn(n, m, generator=g, dtype=torch.float64) * 0.5).numpy()
+    W1, W3, W2 = rnd(f, h), rnd(f, h), rnd(h, f)
+    dZ = torch.randn(M, h, generator=g, dtype=torch.float64).numpy()
+    want = oracle.mlp_backward("swiglu", X, W1, W2, dZ, W3)
+    got = oracle.mlp_backward_composed(X, W1, W2, dZ, W3)
+    for n, x, y in zip(("dX", "dW1", "dW3", "dW2", "db2"), want, got):
+        assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max()), n

@@ -5,8 +5,9 @@ framework whose memory manager owns the GPU, a plugin with no allocator
 handle, a latency-critical loop that cannot afford cudaMalloc's implicit
 synchronisation): its scratch lives in the library's built-in device array
 instead of a caller workspace.  Checked here through the C ABI against
-tp_mlp_forward (which takes a workspace) on two calls in a row, within the
-parity tolerance of the other tests, in both reduction modes; and a plan
+tp_mlp_forward (which takes a workspace) and against the fp64 oracle on two
+calls in a row, within the parity tolerance of the other tests, in both
+reduction modes; and a plan
 whose scratch does not fit the built-in array is refused before any launch.
 
 This file is collected last so that a run stopping at the first failure has
@@ -17,6 +18,7 @@ import pytest
 import torch
 
 import megatron_tensor_transformer_colwise_gb300 as tp
+import oracle
 import synth
 from synth import SHAPES
 from gpu_util import assert_close, dev, host64, plan_for, sync_ok, workspace
@@ -56,6 +58,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(name, mode):
         assert_close(got, want, what=f"noalloc call {call}")
         # The block's own contribution (without the residual) agrees as well.
         assert_close(got - host64(res), want - host64(res), what=f"noalloc call {call} minus residual")
+        # And both agree with the oracle on the same bf16 inputs.
+        w3 = host64(inp["W3"]) if "W3" in inp else None
+        ref = oracle.mlp(s.act, host64(inp["X"]), host64(inp["W1"]), host64(inp["W2"]), w3)
+        if b2 is not None:
+            ref = ref + host64(b2)[None, :]
+        assert_close(got, ref + host64(res), what=f"noalloc call {call} vs oracle")
 
 
 def test_noalloc_refuses_scratch_beyond_the_builtin_array():
