@@ -35,6 +35,10 @@ struct tp_plan_s {
     int64_t kvw;    // kvn * d
     int64_t qkv_w;  // per-shard width of the QKV buffer: qw + 2 kvw
     bool has_mlp, has_attn;
+    // tp_mlp_forward in FUSED mode with a GeLU (or no) activation on a
+    // problem too small to fill the GPU with two GEMMs: the K pieces of the
+    // one-launch MLP (tpi::mlp_fused_launch); 0 = the two-GEMM path.
+    int mlp_pieces;
     uint64_t timeout_ns;
 };
 
@@ -90,6 +94,8 @@ int64_t kv_first(int64_t k, int64_t t, int64_t i) { return (k >= t) ? i * (k / t
 // Workspace regions of each op, in bytes, in order.
 struct Layout {
     size_t y = 0;        // MLP colwise output [M][f] bf16
+    size_t mpart = 0;    // one-launch MLP: [pieces][M][h] fp32 partials (pieces > 1)
+    size_t mcnt = 0;     // one-launch MLP: tile counters (zeroed by every call)
     size_t qkv = 0;      // [M][t * qkv_w] bf16
     size_t o = 0;        // [M][a d] bf16
     size_t xn = 0;       // [M][h] bf16 (normalised input of a block)
@@ -125,6 +131,10 @@ Layout layout_of(const tp_plan_s* p, int op) {
     Layout L;
     const size_t M = static_cast<size_t>(p->M);
     if (op == TP_OP_MLP || op == TP_OP_LAYER) L.y = p->has_mlp ? align_up(M * p->f * 2) : 0;
+    if (op == TP_OP_MLP && p->mlp_pieces > 0) {
+        if (p->mlp_pieces > 1) L.mpart = align_up(static_cast<size_t>(p->mlp_pieces) * M * p->h * 4);
+        L.mcnt = align_up(static_cast<size_t>(tpi::mlp_fused_counter_words(p->M, p->h, p->f)) * 4);
+    }
     if (op == TP_OP_ATTN || op == TP_OP_LAYER) {
         if (p->has_attn) {
             L.qkv = align_up(M * p->t * p->qkv_w * 2);
@@ -176,7 +186,7 @@ Layout layout_of(const tp_plan_s* p, int op) {
 }
 
 size_t layout_total(const Layout& L) {
-    return L.y + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact + L.bdo +
+    return L.y + L.mpart + L.mcnt + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact + L.bdo +
            L.bdstat + L.bdq + L.bdqkv + L.bqkv + L.bo + L.blse + L.lxn1 + L.lh1 + L.lxn2 + L.ldxn + L.ldh1 +
            L.lqkv + L.lo + L.llse + L.lug + L.lshared;
 }
@@ -418,6 +428,7 @@ int derive_plan(const tp_config& cfg, tp_plan_s* p) {
         p->qkv_w = p->qw + 2 * p->kvw;
     }
     p->timeout_ns = 2000000000ull;  // 2 s per barrier wait
+    p->mlp_pieces = 0;
     return TP_OK;
 }
 
@@ -451,6 +462,8 @@ int tp_plan_create(const tp_config* cfg, tp_plan_t* out) {
     tp_plan_s* p = new (std::nothrow) tp_plan_s(tmp);
     if (!p) return fail(TP_ERR_CUDA, "out of host memory");
     p->device = dev;
+    if (p->has_mlp && p->cfg.reduce_mode == TP_REDUCE_FUSED)
+        p->mlp_pieces = tpi::mlp_fused_pieces(p->M, p->h, p->f, static_cast<int>(p->t), p->cfg.act);
     cudaError_t e = cudaMalloc(&p->status, 256);
     if (e == cudaSuccess) e = cudaMemset(p->status, 0, 256);
     if (e != cudaSuccess) {
@@ -617,6 +630,34 @@ int mlp_forward_impl(tp_plan_t plan, const tp_bf16* X, const tp_bf16* W1, const 
     if ((rc = check_ws(plan, TP_OP_MLP, workspace, ws_bytes))) return rc;
     cudaStream_t s = as_stream(stream);
     void* Y = workspace;
+    if (fused && !UG && plan->mlp_pieces > 0) {
+        // One launch: colwise tiles, then each m-block's rowwise tiles as
+        // soon as their H columns are stored ("MLP": Z = sum_i GeLU(X A_i) B_i).
+        const Layout L = layout_of(plan, TP_OP_MLP);
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        tpi::MlpArgs m;
+        m.act = plan->cfg.act;
+        m.M = plan->M;
+        m.h = plan->h;
+        m.f = plan->f;
+        m.t = static_cast<int>(plan->t);
+        m.pieces = plan->mlp_pieces;
+        m.X = X;
+        m.W1 = W1;
+        m.W2 = W2;
+        m.bias = b2;
+        m.residual = residual;
+        m.Z = Z;
+        m.H = w;
+        m.partials = L.mpart ? reinterpret_cast<float*>(w + L.y) : nullptr;
+        m.counters = reinterpret_cast<unsigned*>(w + L.y + L.mpart);
+        m.status = plan->status;
+        m.timeout_ns = plan->timeout_ns;
+        cudaError_t e = cudaMemsetAsync(m.counters, 0, L.mcnt, s);
+        if (e != cudaSuccess) return fail(TP_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
+        std::string err;
+        return run(tpi::mlp_fused_launch(m, s, &err), err);
+    }
     if ((rc = do_colwise(plan, X, W1, W3, Y, s, nullptr, UG))) return rc;
     if ((rc = do_rowwise(plan, Y, plan->fw, W2, plan->h, b2, residual, partials, Z, fused, s))) return rc;
     if (!fused) return do_reduce(plan, partials, b2, residual, Z, plan->h, s);

@@ -70,9 +70,12 @@ constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
 // 2.170 ms against 2.127 ms (W1/W3 1036 against 1011 us), and 4 keeps one
 // warp per 128-column slice of a narrow rowwise tile, whose sum of squares
 // it writes whole.
+// The fused MLP (GEMM_MLP) runs four per quadrant, each on a quarter of the
+// columns: its tiles are short (16 k-blocks at the GPT-sized shapes) and
+// every one of them has a GeLU or a partial-sum epilogue.
 template <int MODE>
 __host__ __device__ constexpr int epi_warps() {
-    return (MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : 4;
+    return MODE == tpi::GEMM_MLP ? 16 : ((MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : 4);
 }
 template <int MODE>
 __host__ __device__ constexpr int num_threads() {
@@ -102,14 +105,18 @@ struct Cfg {
     // boxes per epilogue warp (64-byte swizzle) when the output allows a
     // TMA map; the six ring stages still fit beside them.
     static constexpr bool COL_STAGED = MODE == tpi::GEMM_COL_ACT && CG == 2 && BNT == BN;
-    static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : (BNT == BN ? 6 : 8));
+    static constexpr int STAGES =
+        CG == 1 ? 4 : ((STAGED_OUT || MODE == tpi::GEMM_MLP) ? 5 : (BNT == BN ? 6 : 8));
     static constexpr int CHUNKS = (BNT / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
     static constexpr int TMEM_COLS = 2 * BNT;                  // two accumulators
-    static constexpr int EPI_BYTES = MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
+    static constexpr int EPI_BYTES = MODE == tpi::GEMM_MLP    ? 16 * 2 * EPI_BOX_BYTES     // 16 warps x 2 boxes
+                                     : MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
                                      : MODE == tpi::GEMM_TN    ? 4 * 2 * 2 * EPI_BOX_BYTES  // 4 warps x 2 fp32 boxes
                                      : COL_STAGED              ? 8 * 2 * EPI_BOX_BYTES      // 8 warps x 2 boxes
                                                                : 0;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
+    // GEMM_MLP adds one mbarrier per output box (TMA loads into the boxes).
+    static constexpr int BOX_BARS = MODE == tpi::GEMM_MLP ? 32 : 0;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16 + 8 * BOX_BARS;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TILE_M = BM * CG;
 };
@@ -154,6 +161,25 @@ struct GemmParams {
     int accumulate;
     int o_staged;  // GEMM_COL_ACT: out written through mapO[0] by TMA stores
     CUtensorMap mapO[3];  // BWD_ACT: TMA-store maps of dU, dG, H (64-byte swizzle)
+    // GEMM_MLP (tpi::MlpArgs): mapA / mapB[0] are X / W1 of the colwise
+    // tiles, out = H (ldo = f); the rowwise tiles read H and W2 as (Ks, t,
+    // rows) and write Z (+ bias + residual, ldr = h).
+    CUtensorMap mapH, mapW2;
+    // Output boxes (32 rows x 64 bytes, 64-byte swizzle): H and Z stores,
+    // residual loads, and the fp32 partials as (h, M, pieces) in 16-column
+    // boxes (stores of the lower pieces, loads by the last one).
+    CUtensorMap mapHs, mapZs, mapRs, mapPs;
+    int mlp_col_units;    // colwise units (m_tiles x n_tiles), first in the unit order
+    int mlp_row_n_tiles;  // 256-column tiles of Z
+    int mlp_pieces;       // K pieces of the rowwise sum
+    int mlp_spp;          // shards per piece
+    int mlp_kb_row;       // k-blocks per shard of the rowwise GEMM
+    int mlp_h;            // columns of Z
+    long long mlp_ks;     // columns of H per shard (f / t)
+    unsigned* mlp_ready;   // [m_tiles][n_tiles]: CTAs that stored their half of a colwise tile
+    unsigned* mlp_pdone;   // [m_tiles][mlp_row_n_tiles][2]: lower pieces stored, per CTA half
+    float* mlp_part;       // [mlp_pieces][M][mlp_h]
+    __nv_bfloat16* mlp_z;  // [M][mlp_h]
     unsigned* status;
     unsigned long long timeout_ns;
 };
@@ -182,6 +208,26 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     const int rr = r - g * group_size;
     mb = first_m + rr % gm;
     nb = rr / gm;
+}
+
+// GEMM_MLP unit u: colwise tiles first (m-major), then the rowwise units of
+// each m-block, piece-major (the first piece reads the first H columns).
+__device__ __forceinline__ void decode_mlp(const GemmParams& p, int u, bool& row, int& mb, int& nb,
+                                           int& piece) {
+    if (u < p.mlp_col_units) {
+        row = false;
+        mb = u / p.n_tiles;
+        nb = u - mb * p.n_tiles;
+        piece = 0;
+        return;
+    }
+    const int r = u - p.mlp_col_units;
+    const int per_m = p.mlp_row_n_tiles * p.mlp_pieces;
+    row = true;
+    mb = r / per_m;
+    const int rem = r - mb * per_m;
+    piece = rem / p.mlp_row_n_tiles;
+    nb = rem - piece * p.mlp_row_n_tiles;
 }
 
 // First KV head held by shard i (k/t own heads when k >= t, else a replica
@@ -487,6 +533,79 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
     }
 }
 
+// Producer of the fused MLP.  A rowwise unit first waits (bounded) until
+// both CTAs of every colwise tile holding its H columns have stored them;
+// its loads then read H through the async proxy.
+template <int CG>
+__device__ __forceinline__ void mlp_producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
+                                                  uint32_t rank, volatile int* abort_flag) {
+    using C = Cfg<tpi::GEMM_MLP, CG, BN>;
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, last_parity = 0;
+    bool ok = true;
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    for (int u = cid; ok && u < p.num_tiles; u += ncl) {
+        bool row;
+        int mb, nb, piece;
+        decode_mlp(p, u, row, mb, nb, piece);
+        const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
+        int s0 = 0, ns = 1, nkb = p.kb_per_shard;
+        if (row) {
+            s0 = piece * p.mlp_spp;
+            ns = p.mlp_spp;
+            nkb = p.mlp_kb_row;
+            const long long c0 = static_cast<long long>(s0) * p.mlp_ks, c1 = c0 + ns * p.mlp_ks;
+            for (int j = static_cast<int>(c0 / BN); ok && j <= static_cast<int>((c1 - 1) / BN); ++j)
+                ok = flag_wait_geq(p.mlp_ready + mb * p.n_tiles + j, CG, abort_flag, p.status, p.timeout_ns);
+            if (!ok) break;
+            fence_proxy_async_global();
+        }
+        for (int sh = s0; ok && sh < s0 + ns; ++sh) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
+                if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
+                const uint32_t full_l = (CG == 2) ? mapa_shared(full, 0) : full;
+                const uint32_t a_dst = base + stage * C::STAGE_BYTES;
+                const uint32_t b_dst = a_dst + A_BYTES;
+                const int kc = kb * BK;
+                if (row) {
+                    if (CG == 2) tma_load_3d_pair(a_dst, &p.mapH, full_l, kc, sh, arow);
+                    else tma_load_3d(a_dst, &p.mapH, full_l, kc, sh, arow);
+                } else {
+                    if (CG == 2) tma_load_2d_pair(a_dst, &p.mapA, full_l, kc, arow);
+                    else tma_load_2d(a_dst, &p.mapA, full_l, kc, arow);
+                }
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    const int brow = nb * BN + (static_cast<int>(rank) * C::CHUNKS + c) * B_CHUNK_ROWS;
+                    const uint32_t dst = b_dst + c * B_CHUNK_BYTES;
+                    if (row) {
+                        if (CG == 2) tma_load_3d_pair(dst, &p.mapW2, full_l, kc, sh, brow);
+                        else tma_load_3d(dst, &p.mapW2, full_l, kc, sh, brow);
+                    } else {
+                        if (CG == 2) tma_load_2d_pair(dst, &p.mapB[0], full_l, kc, brow);
+                        else tma_load_2d(dst, &p.mapB[0], full_l, kc, brow);
+                    }
+                }
+                issued_mask |= 1u << stage;
+                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (!ok && rank == 0) {
+        for (int s = 0; s < C::STAGES; ++s)
+            if (issued_mask & (1u << s)) drain_wait(bar0 + 8 * s, (last_parity >> s) & 1u);
+    }
+}
+
 template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                          uint32_t tmem_base, volatile int* abort_flag) {
@@ -512,7 +631,10 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BNT;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        int nkb = kblocks;
+        if constexpr (MODE == tpi::GEMM_MLP)
+            nkb = tile < p.mlp_col_units ? p.kb_per_shard : p.mlp_spp * p.mlp_kb_row;
+        for (int kb = 0; kb < nkb; ++kb) {
             const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
             if (!mbar_wait(full, phase, abort_flag, p.status, p.timeout_ns)) {
                 ok = false;
@@ -785,6 +907,277 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
     }
 }
 
+// Epilogue of the fused MLP: 16 warps, four per TMEM lane quadrant, each
+// on 64 of the tile's 256 columns (two 32-column chunks).  The accumulator
+// arrives one row per thread (TMEM lane = row).  Global memory is reached
+// only through TMA: each warp owns two 2 KB boxes in shared memory (32 rows
+// x 64 bytes, 64-byte swizzle: 16-byte piece j of row r at r * 64 + (j ^
+// ((r / 2) % 4)) * 16, which keeps the row-per-thread accesses free of
+// bank conflicts), used in turn, each with an mbarrier for loads into it.
+//  - colwise unit: act(accumulator) -> bf16 H by TMA stores; once the
+//    CTA's 16 warps have seen their stores complete, one thread counts the
+//    CTA's half of the tile in mlp_ready.
+//  - rowwise unit of a lower piece (piece < pieces - 1): its fp32 partial
+//    goes out by TMA stores, then the CTA counts itself in mlp_pdone.
+//  - rowwise unit of the last piece: waits (bounded) until the lower
+//    pieces of its tile have stored their partials, loads them by TMA and
+//    sums P_0 + ... + P_(pieces-2) + its own accumulator in that order (so
+//    the result does not depend on which piece finished first), adds bias
+//    and residual, and stores bf16 Z.
+// The 16 warps meet on hardware barrier 1 (bar.sync over 512 threads).
+constexpr uint32_t kMlpEpiBar = 1;
+
+// This thread's 64-byte row (16 words) into / out of a box.
+__device__ __forceinline__ void box_put_row(uint32_t box, int lane, const uint32_t* w) {
+    const uint32_t srow = box + static_cast<uint32_t>(lane) * 64, sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(srow + ((static_cast<uint32_t>(j) ^ sw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+__device__ __forceinline__ void box_get_row(uint32_t box, int lane, uint32_t* w) {
+    const uint32_t srow = box + static_cast<uint32_t>(lane) * 64, sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 v = ld_shared_v4(srow + ((static_cast<uint32_t>(j) ^ sw) << 4));
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+    }
+}
+
+template <int ACT>
+__device__ __forceinline__ void mlp_act_pack(const uint32_t (&r)[32], uint32_t (&w)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        float h0, h1;
+        act_apply2<ACT>(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), h0, h1);
+        w[e] = pack_bf16x2(h0, h1);
+    }
+}
+
+// The warp's two boxes, used in turn.  A box is handed out once the bulk
+// store that last read it has done so: when the newest store group read
+// this box, all groups must have been read; otherwise the newest group read
+// the other box and may still be pending.  All lanes track the same state.
+struct MlpBoxes {
+    uint32_t base, bars, phase, use, newest;  // newest: box of the newest store group (2: none)
+    __device__ __forceinline__ uint32_t next(int lane, uint32_t& bar) {
+        const uint32_t k = use & 1u;
+        ++use;
+        if (lane == 0) {
+            if (newest == k) bulk_wait_group_read0();
+            else bulk_wait_group_read1();
+        }
+        __syncwarp();
+        bar = bars + 8 * k;
+        return base + k * EPI_BOX_BYTES;
+    }
+    // After a bulk store (one commit group) from the box last handed out.
+    __device__ __forceinline__ void stored() { newest = (use - 1) & 1u; }
+    // Wait for the TMA load into the box whose barrier is `bar`.
+    __device__ __forceinline__ bool wait_load(uint32_t bar, volatile int* abort_flag, const GemmParams& p) {
+        const uint32_t k = (bar - bars) >> 3;
+        const bool ok = mbar_wait(bar, (phase >> k) & 1u, abort_flag, p.status, p.timeout_ns);
+        phase ^= 1u << k;
+        return ok;
+    }
+};
+
+template <int CG>
+__device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t epi0, uint32_t tmem_base,
+                                                  uint32_t rank, volatile int* abort_flag) {
+    using C = Cfg<tpi::GEMM_MLP, CG, BN>;
+    constexpr int EPI_WARPS = epi_warps<tpi::GEMM_MLP>();
+    constexpr uint32_t EPI_THREADS = 32 * EPI_WARPS;
+    constexpr int CPW = (BN / 32) / (EPI_WARPS / 4);  // 32-column chunks per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;
+    const int cb = ((warp - 2) >> 2) * CPW;
+    const bool leader = warp == 2 && lane == 0;
+    MlpBoxes bx{epi0 + static_cast<uint32_t>(warp - 2) * 2 * EPI_BOX_BYTES,
+                bar0 + 8 * (2 * C::STAGES + 5) + 16 + 16 * static_cast<uint32_t>(warp - 2), 0u, 0u, 2u};
+    uint32_t acc = 0, acc_phase = 0;
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    for (int u = cid; u < p.num_tiles; u += ncl) {
+        bool rowu;
+        int mb, nb, piece;
+        decode_mlp(p, u, rowu, mb, nb, piece);
+        const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
+        const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
+        const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // the warp's first row
+        const bool box_ok = row0 < p.M;  // warp-uniform
+        const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status, p.timeout_ns);
+        // Every epilogue warp takes the same branch, so none is left waiting
+        // at a barrier below when another has given up.
+        if (!named_bar_and(kMlpEpiBar, EPI_THREADS, got)) break;
+        tc_fence_after();
+        const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+        const int tile_ctr = (mb * p.mlp_row_n_tiles + nb) * 2 + static_cast<int>(rank);
+        uint32_t r[32];
+        if (!rowu) {
+#pragma unroll 1
+            for (int c = cb; c < cb + CPW; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.N) break;  // warp-uniform
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);
+                tmem_ld_wait();
+                uint32_t w[16];
+                switch (p.act) {
+                    case TP_ACT_GELU_ERF: mlp_act_pack<TP_ACT_GELU_ERF>(r, w); break;
+                    case TP_ACT_GELU_TANH: mlp_act_pack<TP_ACT_GELU_TANH>(r, w); break;
+                    default: mlp_act_pack<TP_ACT_NONE>(r, w); break;
+                }
+                uint32_t bar;
+                const uint32_t box = bx.next(lane, bar);
+                box_put_row(box, lane, w);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && box_ok) {
+                    tma_store_2d(&p.mapHs, box, col0, row0);
+                    bulk_commit_group();
+                }
+                if (box_ok) bx.stored();
+            }
+            if (lane == 0) bulk_wait_group0();  // this warp's H stores are in global memory
+            __syncwarp();
+            named_bar_sync(kMlpEpiBar, EPI_THREADS);
+            if (leader) {
+                fence_proxy_async_global();
+                red_release_gpu_add(p.mlp_ready + mb * p.n_tiles + nb, 1u);
+            }
+        } else if (piece < p.mlp_pieces - 1) {
+#pragma unroll 1
+            for (int c = cb; c < cb + CPW; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.mlp_h) break;  // warp-uniform
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t bar;
+                    const uint32_t box = bx.next(lane, bar);
+                    box_put_row(box, lane, r + 16 * hf);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && box_ok) {
+                        tma_store_3d(&p.mapPs, box, col0 + 16 * hf, row0, piece);
+                        bulk_commit_group();
+                    }
+                    if (box_ok) bx.stored();
+                }
+            }
+            if (lane == 0) bulk_wait_group0();
+            __syncwarp();
+            named_bar_sync(kMlpEpiBar, EPI_THREADS);
+            if (leader) {
+                fence_proxy_async_global();
+                red_release_gpu_add(p.mlp_pdone + tile_ctr, 1u);
+            }
+        } else {
+            bool ok = true;
+            if (p.mlp_pieces > 1) {
+                if (leader)
+                    ok = flag_wait_geq(p.mlp_pdone + tile_ctr, static_cast<unsigned>(p.mlp_pieces - 1), abort_flag,
+                                       p.status, p.timeout_ns);
+                ok = named_bar_and(kMlpEpiBar, EPI_THREADS, ok);
+                if (lane == 0) fence_proxy_async_global();  // the partials are read by TMA
+            }
+#pragma unroll 1
+            for (int c = cb; ok && c < cb + CPW; ++c) {
+                const int col0 = nb * BN + c * 32;
+                if (col0 >= p.mlp_h) break;  // warp-uniform
+                __syncwarp();
+                tmem_ld32(t0 + c * 32, r);  // this piece's sum
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+                if (p.mlp_pieces > 1) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float sum[16];
+#pragma unroll 1
+                        for (int j = 0; j < p.mlp_pieces - 1; ++j) {
+                            uint32_t bar;
+                            const uint32_t box = bx.next(lane, bar);
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(bar, EPI_BOX_BYTES);
+                                tma_load_3d(box, &p.mapPs, bar, col0 + 16 * hf, row0, j);
+                            }
+                            ok = bx.wait_load(bar, abort_flag, p) && ok;
+                            uint32_t w[16];
+                            box_get_row(box, lane, w);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                sum[e] = j == 0 ? __uint_as_float(w[e]) : sum[e] + __uint_as_float(w[e]);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[16 * hf + e] = sum[e] + v[16 * hf + e];
+                    }
+                }
+                if (p.bias) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (col0 + 8 * g >= p.mlp_h) continue;
+                        const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col0 + 8 * g);
+                        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(bw[e]);
+                            v[8 * g + 2 * e] += f.x;
+                            v[8 * g + 2 * e + 1] += f.y;
+                        }
+                    }
+                }
+                if (p.residual) {
+                    uint32_t bar;
+                    const uint32_t box = bx.next(lane, bar);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, EPI_BOX_BYTES);
+                        tma_load_2d(box, &p.mapRs, bar, col0, row0);
+                    }
+                    ok = bx.wait_load(bar, abort_flag, p) && ok;
+                    uint32_t w[16];
+                    box_get_row(box, lane, w);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 f = unpack_bf16x2(w[e]);
+                        v[2 * e] += f.x;
+                        v[2 * e + 1] += f.y;
+                    }
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+                uint32_t bar;
+                const uint32_t box = bx.next(lane, bar);
+                box_put_row(box, lane, w);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && box_ok) {
+                    tma_store_2d(&p.mapZs, box, col0, row0);
+                    bulk_commit_group();
+                }
+                if (box_ok) bx.stored();
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (CG == 2) mbar_arrive_cluster(mapa_shared(tempty, 0));
+            else mbar_arrive(tempty);
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    // Every bulk store has completed before the CTA's shared memory goes.
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+}
+
 template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t epi0,
                                               uint32_t tmem_base, uint32_t rank, volatile int* abort_flag) {
@@ -995,12 +1388,18 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
         mbar_init(bar0 + 8 * (2 * C::STAGES + 2), EPI_WARPS * CG);  // tmem empty x2: epilogue warps
         mbar_init(bar0 + 8 * (2 * C::STAGES + 3), EPI_WARPS * CG);
         mbar_init(bar0 + 8 * (2 * C::STAGES + 4), 1);       // drain
+        for (int b = 0; b < C::BOX_BARS; ++b)                // output boxes (GEMM_MLP)
+            mbar_init(bar0 + 8 * (2 * C::STAGES + 5) + 16 + 8 * b, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.mapA);
         tma_prefetch_desc(&p.mapB[0]);
+        if (MODE == tpi::GEMM_MLP) {
+            tma_prefetch_desc(&p.mapH);
+            tma_prefetch_desc(&p.mapW2);
+        }
         if (MODE == tpi::GEMM_COL_SWIGLU || MODE == tpi::GEMM_COL_QKV || MODE == tpi::GEMM_NN)
             tma_prefetch_desc(&p.mapB[1]);
         if (MODE == tpi::GEMM_COL_QKV || MODE == tpi::GEMM_NN) tma_prefetch_desc(&p.mapB[2]);
@@ -1025,12 +1424,22 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     pdl_trigger();
     pdl_wait();
 
-    if (warp == 0) {
-        if (lane == 0) producer_loop<MODE, CG, BNT>(p, base, bar0, rank, abort_flag);
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
+    if constexpr (MODE == tpi::GEMM_MLP) {
+        if (warp == 0) {
+            if (lane == 0) mlp_producer_loop<CG>(p, base, bar0, rank, abort_flag);
+        } else if (warp == 1) {
+            if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
+        } else {
+            mlp_epilogue_loop<CG>(p, bar0, epi0, tmem_base, rank, abort_flag);
+        }
     } else {
-        epilogue_loop<MODE, CG, BNT>(p, bar0, epi0, tmem_base, rank, abort_flag);
+        if (warp == 0) {
+            if (lane == 0) producer_loop<MODE, CG, BNT>(p, base, bar0, rank, abort_flag);
+        } else if (warp == 1) {
+            if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
+        } else {
+            epilogue_loop<MODE, CG, BNT>(p, bar0, epi0, tmem_base, rank, abort_flag);
+        }
     }
     __syncwarp();
     tc_fence_before();
@@ -1354,6 +1763,155 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
             if (err) *err = "unknown GEMM mode";
             return TP_ERR_INVALID_ARG;
     }
+}
+
+// ---- the fused MLP (GEMM_MLP)
+
+namespace {
+
+// Makespan, in k-blocks, of `units` run round-robin over `pairs` pairs in
+// the fused MLP's unit order (colwise units first), with `fix` k-blocks of
+// partial-sum epilogue charged to each rowwise unit when pieces > 1.
+long long mlp_makespan(long long col_units, long long kb_col, long long row_units, long long kb_row_unit,
+                       long long fix, int pairs) {
+    long long worst = 0;
+    for (int q = 0; q < pairs; ++q) {
+        long long tsum = 0;
+        for (long long u = q; u < col_units + row_units; u += pairs)
+            tsum += u < col_units ? kb_col : kb_row_unit + fix;
+        worst = std::max(worst, tsum);
+    }
+    return worst;
+}
+
+}  // namespace
+
+int64_t mlp_fused_counter_words(int64_t M, int64_t h, int64_t f) {
+    const int64_t mt = (M + 2 * BM - 1) / (2 * BM);
+    return mt * ((f + BN - 1) / BN) + mt * ((h + BN - 1) / BN) * 2;
+}
+
+int mlp_fused_pieces(int64_t M, int64_t h, int64_t f, int t, int act) {
+    if (kPairTiles != 2) return 0;
+    if (act != TP_ACT_GELU_ERF && act != TP_ACT_GELU_TANH && act != TP_ACT_NONE) return 0;
+    if (M <= 0 || t <= 0 || f % t || (f / t) % 8 || h % 8) return 0;
+    const int pairs = std::max(1, device_sm_count() / 2);
+    const long long mt = (M + 2 * BM - 1) / (2 * BM);
+    const long long col_units = mt * ((f + BN - 1) / BN);
+    // Two GEMMs of a few waves each leave SMs idle at each kernel's tail and
+    // pay a launch and a pipeline fill each; beyond about three colwise waves
+    // the two-GEMM path is as good and needs no scratch.
+    if (col_units > 3LL * pairs) return 0;
+    const long long kb_col = (h + BK - 1) / BK;
+    const long long kb_shard = (f / t + BK - 1) / BK;
+    const long long row_tiles = mt * ((h + BN - 1) / BN);
+    int best = 0;
+    long long best_cost = 0;
+    for (int pieces = 1; pieces <= t && pieces <= 8; pieces *= 2) {
+        if (t % pieces) continue;
+        // Summing a piece's partial reads one 128 KB fp32 half tile per CTA
+        // per other piece: charged as two k-blocks each.
+        const long long fix = pieces > 1 ? 2LL * (pieces - 1) : 0;
+        const long long cost =
+            mlp_makespan(col_units, kb_col, row_tiles * pieces, (t / pieces) * kb_shard, fix, pairs);
+        if (best == 0 || cost < best_cost) {
+            best = pieces;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
+    constexpr int CG = kPairTiles;
+    static_assert(CG == 2, "the fused MLP runs on CTA pairs");
+    if (a.pieces < 1 || a.t % a.pieces) {
+        if (err) *err = "fused MLP: pieces must divide t";
+        return TP_ERR_INVALID_ARG;
+    }
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const int64_t Ks = a.f / a.t;
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.f);
+    p.act = a.act;
+    p.out = a.H;
+    p.ldo = a.f;
+    p.bias = reinterpret_cast<const __nv_bfloat16*>(a.bias);
+    p.residual = reinterpret_cast<const __nv_bfloat16*>(a.residual);
+    p.ldr = a.h;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.kb_per_shard = static_cast<int>((a.h + BK - 1) / BK);
+    p.k_shards = 1;
+    p.m_tiles = static_cast<int>((a.M + 2 * BM - 1) / (2 * BM));
+    p.n_tiles = static_cast<int>((a.f + BN - 1) / BN);
+    p.grid_shards = 1;
+    p.group_m = 16;
+    p.mlp_col_units = p.m_tiles * p.n_tiles;
+    p.mlp_row_n_tiles = static_cast<int>((a.h + BN - 1) / BN);
+    p.mlp_pieces = a.pieces;
+    p.mlp_spp = a.t / a.pieces;
+    p.mlp_kb_row = static_cast<int>((Ks + BK - 1) / BK);
+    p.mlp_h = static_cast<int>(a.h);
+    p.mlp_ks = Ks;
+    const int64_t ready_words = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    p.mlp_ready = a.counters;
+    p.mlp_pdone = a.counters + ready_words;
+    p.mlp_part = a.partials;
+    p.mlp_z = reinterpret_cast<__nv_bfloat16*>(a.Z);
+    if (a.pieces > 1 && !a.partials) {
+        if (err) *err = "fused MLP: partials buffer missing";
+        return TP_ERR_INVALID_ARG;
+    }
+    // Colwise operands: X [M][h], W1 [f][h].
+    {
+        const uint64_t dA[2] = {(uint64_t)a.h, (uint64_t)a.M};
+        const uint64_t sA[1] = {(uint64_t)a.h * 2};
+        const uint32_t bA[2] = {BK, BM};
+        if (!make_map(&p.mapA, a.X, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
+        const uint64_t dB[2] = {(uint64_t)a.h, (uint64_t)a.f};
+        const uint32_t bB[2] = {BK, B_CHUNK_ROWS};
+        if (!make_map(&p.mapB[0], a.W1, 2, dB, sA, bB, err)) return TP_ERR_CUDA;
+    }
+    // Rowwise operands: H [M][t Ks] and W2 [h][t Ks] seen as (Ks, t, rows).
+    {
+        const uint64_t sK[2] = {(uint64_t)Ks * 2, (uint64_t)a.t * Ks * 2};
+        const uint64_t dH[3] = {(uint64_t)Ks, (uint64_t)a.t, (uint64_t)a.M};
+        const uint32_t bH[3] = {BK, 1, BM};
+        if (!make_map(&p.mapH, a.H, 3, dH, sK, bH, err)) return TP_ERR_CUDA;
+        const uint64_t dW[3] = {(uint64_t)Ks, (uint64_t)a.t, (uint64_t)a.h};
+        const uint32_t bW[3] = {BK, 1, B_CHUNK_ROWS};
+        if (!make_map(&p.mapW2, a.W2, 3, dW, sK, bW, err)) return TP_ERR_CUDA;
+    }
+    // Epilogue boxes: 32 x 32 bf16 (H and Z stores, residual loads) and
+    // 16 x 32 fp32 (partials), 64-byte swizzle; rows and columns past the
+    // matrices are clipped on stores and read as zeros.
+    {
+        const uint32_t box16[2] = {EPI_BOX, EPI_BOX};
+        const uint64_t dHs[2] = {(uint64_t)a.f, (uint64_t)a.M};
+        const uint64_t sHs[1] = {(uint64_t)a.f * 2};
+        if (!make_map(&p.mapHs, a.H, 2, dHs, sHs, box16, err, CU_TENSOR_MAP_SWIZZLE_64B)) return TP_ERR_CUDA;
+        const uint64_t dZ[2] = {(uint64_t)a.h, (uint64_t)a.M};
+        const uint64_t sZ[1] = {(uint64_t)a.h * 2};
+        if (!make_map(&p.mapZs, a.Z, 2, dZ, sZ, box16, err, CU_TENSOR_MAP_SWIZZLE_64B)) return TP_ERR_CUDA;
+        p.mapRs = p.mapZs;
+        if (a.residual && !make_map(&p.mapRs, a.residual, 2, dZ, sZ, box16, err, CU_TENSOR_MAP_SWIZZLE_64B))
+            return TP_ERR_CUDA;
+        p.mapPs = p.mapZs;
+        if (a.pieces > 1) {
+            const uint64_t dP[3] = {(uint64_t)a.h, (uint64_t)a.M, (uint64_t)a.pieces};
+            const uint64_t sP[2] = {(uint64_t)a.h * 4, (uint64_t)a.M * a.h * 4};
+            const uint32_t bP[3] = {16, EPI_BOX, 1};
+            if (!make_map(&p.mapPs, a.partials, 3, dP, sP, bP, err, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+                return TP_ERR_CUDA;
+        }
+    }
+    p.num_tiles = p.mlp_col_units + p.m_tiles * p.mlp_row_n_tiles * p.mlp_pieces;
+    if (p.num_tiles == 0) return TP_OK;
+    const int grid = std::min(p.num_tiles, device_sm_count() / CG) * CG;
+    return launch_mode<GEMM_MLP, CG>(p, grid, stream, err);
 }
 
 }  // namespace tpi

@@ -46,7 +46,8 @@ enum GemmMode {
     // the operand's M or N index is the contiguous one):
     GEMM_BWD_ACT = 6,     // dH = dZ W2 (B MN-major), epilogue: dU, dG, H from saved U, G
     GEMM_NN = 7,          // A K-major, B MN-major [K][N] (K rows split over B0 / B1)
-    GEMM_TN = 8           // A and B MN-major ([K][M], [K][N]), fp32 out split by rows
+    GEMM_TN = 8,          // A and B MN-major ([K][M], [K][N]), fp32 out split by rows
+    GEMM_MLP = 9          // the whole sharded MLP in one persistent launch (see MlpArgs)
 };
 
 constexpr int kMaxPackedBlocks = 8;
@@ -215,6 +216,39 @@ int colsum_launch(const void* x, int64_t rows, int h, float* out, int accumulate
 // Self test: a kernel that waits on a barrier nobody arrives at.
 int selftest_timeout_launch(unsigned* status, uint64_t timeout_ns, cudaStream_t stream,
                             std::string* err);
+
+// The sharded MLP Z = sum_i act(X W1_i^T) W2_i^T (+ bias + residual) in one
+// persistent launch, for problems too small to fill the GPU with the two
+// GEMMs one after the other.  Its work units are the colwise tiles (256 x
+// 256 of H = act(X W1^T), bf16) and then, per 256-row m-block, the rowwise
+// tiles (256 x 256 of Z) in `pieces` K pieces of t / pieces shards each.  A
+// rowwise unit starts once the colwise tiles holding its H columns are
+// stored (per-tile counters); with pieces > 1 each piece writes an fp32
+// partial and the last piece of a tile to arrive sums all of them in piece
+// order (so the result does not depend on the arrival order) and writes Z.
+struct MlpArgs {
+    int act = 0;  // TP_ACT_GELU_ERF, TP_ACT_GELU_TANH or TP_ACT_NONE
+    int64_t M = 0, h = 0, f = 0;
+    int t = 1;
+    int pieces = 1;  // divides t
+    const void* X = nullptr;   // [M][h]
+    const void* W1 = nullptr;  // [f][h]
+    const void* W2 = nullptr;  // [h][f]
+    const void* bias = nullptr;      // [h] or null
+    const void* residual = nullptr;  // [M][h] or null
+    void* Z = nullptr;               // [M][h] bf16
+    void* H = nullptr;               // [M][f] bf16 scratch
+    float* partials = nullptr;       // [pieces][M][h] fp32 scratch (pieces > 1)
+    unsigned* counters = nullptr;    // mlp_fused_counter_words() words, zero at launch
+    unsigned* status = nullptr;
+    uint64_t timeout_ns = 0;
+};
+// K pieces the fused MLP launch would use for this problem on the current
+// device, or 0 when the two-GEMM path suits it better (large problems,
+// SwiGLU).
+int mlp_fused_pieces(int64_t M, int64_t h, int64_t f, int t, int act);
+int64_t mlp_fused_counter_words(int64_t M, int64_t h, int64_t f);
+int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err);
 
 // Device properties cached per device.
 int device_sm_count();
