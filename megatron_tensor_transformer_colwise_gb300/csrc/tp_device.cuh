@@ -511,6 +511,26 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// As tma_load_2d_pair / tma_load_3d_pair, with the box written to the same
+// shared-memory offset in every CTA of `cta_mask` (cluster ranks); each
+// destination's bytes are counted on the barrier at `bar_leader`'s offset in
+// the first CTA of the destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_leader,
+                                                    int32_t c0, int32_t c1, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_leader), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_leader,
+                                                    int32_t c0, int32_t c1, int32_t c2, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_leader), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
+        : "memory");
+}
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask`
 // when the leader's prior tcgen05 ops complete.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {

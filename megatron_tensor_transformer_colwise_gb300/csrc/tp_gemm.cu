@@ -70,16 +70,24 @@ constexpr int B_CHUNK_BYTES = B_CHUNK_ROWS * BK * 2;  // 8 KB
 // 2.170 ms against 2.127 ms (W1/W3 1036 against 1011 us), and 4 keeps one
 // warp per 128-column slice of a narrow rowwise tile, whose sum of squares
 // it writes whole.
-// The fused MLP (GEMM_MLP) runs four per quadrant, each on a quarter of the
-// columns: its tiles are short (16 k-blocks at the GPT-sized shapes) and
-// every one of them has a GeLU or a partial-sum epilogue.
+// The fused MLP (GEMM_MLP) runs two per quadrant as well: its tiles are
+// short (16 k-blocks at the GPT-sized shapes) and every one of them has a
+// GeLU or a partial-sum epilogue.
 template <int MODE>
 __host__ __device__ constexpr int epi_warps() {
-    return MODE == tpi::GEMM_MLP ? 16 : ((MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : 4);
+    return (MODE == tpi::GEMM_MLP || MODE == tpi::GEMM_BWD_ACT || MODE == tpi::GEMM_COL_ACT) ? 8 : 4;
 }
 template <int MODE>
 __host__ __device__ constexpr int num_threads() {
     return 64 + 32 * epi_warps<MODE>();
+}
+// CTAs per cluster.  The fused MLP runs clusters of two CTA pairs that take
+// adjacent n-tiles of one m-block: each A tile is read from L2 once and
+// multicast to both pairs (a quarter less operand traffic per MMA); the
+// other modes run one pair (or one CTA) per cluster.
+template <int MODE, int CG>
+__host__ __device__ constexpr int cluster_ctas() {
+    return MODE == tpi::GEMM_MLP ? 2 * CG : CG;
 }
 
 // CG = CTAs per tile.  CG = 1: a 128 x 256 tile per CTA, 4 stages of 48 KB.
@@ -105,17 +113,16 @@ struct Cfg {
     // boxes per epilogue warp (64-byte swizzle) when the output allows a
     // TMA map; the six ring stages still fit beside them.
     static constexpr bool COL_STAGED = MODE == tpi::GEMM_COL_ACT && CG == 2 && BNT == BN;
-    static constexpr int STAGES =
-        CG == 1 ? 4 : ((STAGED_OUT || MODE == tpi::GEMM_MLP) ? 5 : (BNT == BN ? 6 : 8));
+    static constexpr int STAGES = CG == 1 ? 4 : (STAGED_OUT ? 5 : (BNT == BN ? 6 : 8));
     static constexpr int CHUNKS = (BNT / B_CHUNK_ROWS) / CG;  // B boxes loaded per CTA
     static constexpr int TMEM_COLS = 2 * BNT;                  // two accumulators
-    static constexpr int EPI_BYTES = MODE == tpi::GEMM_MLP    ? 16 * 2 * EPI_BOX_BYTES     // 16 warps x 2 boxes
+    static constexpr int EPI_BYTES = MODE == tpi::GEMM_MLP    ? 8 * 2 * EPI_BOX_BYTES      // 8 warps x 2 boxes
                                      : MODE == tpi::GEMM_BWD_ACT ? 8 * 3 * EPI_BOX_BYTES     // 8 warps x 3 boxes
                                      : MODE == tpi::GEMM_TN    ? 4 * 2 * 2 * EPI_BOX_BYTES  // 4 warps x 2 fp32 boxes
                                      : COL_STAGED              ? 8 * 2 * EPI_BOX_BYTES      // 8 warps x 2 boxes
                                                                : 0;
     // GEMM_MLP adds one mbarrier per output box (TMA loads into the boxes).
-    static constexpr int BOX_BARS = MODE == tpi::GEMM_MLP ? 32 : 0;
+    static constexpr int BOX_BARS = MODE == tpi::GEMM_MLP ? 16 : 0;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16 + 8 * BOX_BARS;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TILE_M = BM * CG;
@@ -176,7 +183,8 @@ struct GemmParams {
     int mlp_kb_row;       // k-blocks per shard of the rowwise GEMM
     int mlp_h;            // columns of Z
     long long mlp_ks;     // columns of H per shard (f / t)
-    unsigned* mlp_ready;   // [m_tiles][n_tiles]: CTAs that stored their half of a colwise tile
+    unsigned* mlp_ready;   // [m_tiles][8]: per K piece, CTAs that stored their half of a colwise
+                           // tile overlapping the piece's H columns
     unsigned* mlp_pdone;   // [m_tiles][mlp_row_n_tiles][2]: lower pieces stored, per CTA half
     float* mlp_part;       // [mlp_pieces][M][mlp_h]
     __nv_bfloat16* mlp_z;  // [M][mlp_h]
@@ -210,24 +218,30 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     nb = rr / gm;
 }
 
-// GEMM_MLP unit u: colwise tiles first (m-major), then the rowwise units of
-// each m-block, piece-major (the first piece reads the first H columns).
-__device__ __forceinline__ void decode_mlp(const GemmParams& p, int u, bool& row, int& mb, int& nb,
+// GEMM_MLP unit u of a cluster: colwise units first (all m-blocks of one
+// n-tile pair, then the next pair: the first H columns of every m-block
+// are done first), then the rowwise units of each m-block, piece-major (the
+// first piece reads the first H columns).  A unit is two adjacent n-tiles of one m-block; pair pc
+// of the cluster takes n-tile 2 n + pc (past the matrix when the count is
+// odd: loads read zeros, stores are skipped).
+__device__ __forceinline__ void decode_mlp(const GemmParams& p, int u, int pc, bool& row, int& mb, int& nb,
                                            int& piece) {
     if (u < p.mlp_col_units) {
         row = false;
-        mb = u / p.n_tiles;
-        nb = u - mb * p.n_tiles;
+        const int nbc = u / p.m_tiles;
+        mb = u - nbc * p.m_tiles;
+        nb = 2 * nbc + pc;
         piece = 0;
         return;
     }
+    const int nrow2 = (p.mlp_row_n_tiles + 1) >> 1;
     const int r = u - p.mlp_col_units;
-    const int per_m = p.mlp_row_n_tiles * p.mlp_pieces;
+    const int per_m = nrow2 * p.mlp_pieces;
     row = true;
     mb = r / per_m;
     const int rem = r - mb * per_m;
-    piece = rem / p.mlp_row_n_tiles;
-    nb = rem - piece * p.mlp_row_n_tiles;
+    piece = rem / nrow2;
+    nb = 2 * (rem - piece * nrow2) + pc;
 }
 
 // First KV head held by shard i (k/t own heads when k >= t, else a replica
@@ -540,67 +554,89 @@ template <int CG>
 __device__ __forceinline__ void mlp_producer_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                                   uint32_t rank, volatile int* abort_flag) {
     using C = Cfg<tpi::GEMM_MLP, CG, BN>;
+    constexpr int CL = cluster_ctas<tpi::GEMM_MLP, CG>();
+    static_assert(CG == 2 && CL == 4, "the fused MLP runs clusters of two CTA pairs");
+    // rank: 0..3 in the cluster; pair pc = rank / 2, prank = rank % 2 in it.
+    const int pc = static_cast<int>(rank >> 1), prank = static_cast<int>(rank & 1u);
+    // Each CTA loads 64 of its 128 A rows (the half pc) into both pairs: the
+    // CTAs of the same rank in the two pairs hold the same A rows.
+    const uint16_t a_mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+    constexpr uint32_t A_HALF = A_BYTES / 2;
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
     bool ok = true;
-    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     for (int u = cid; ok && u < p.num_tiles; u += ncl) {
         bool row;
         int mb, nb, piece;
-        decode_mlp(p, u, row, mb, nb, piece);
-        const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
+        decode_mlp(p, u, pc, row, mb, nb, piece);
+        const int arow = mb * C::TILE_M + prank * BM + pc * (BM / 2);
         int s0 = 0, ns = 1, nkb = p.kb_per_shard;
         if (row) {
             s0 = piece * p.mlp_spp;
             ns = p.mlp_spp;
             nkb = p.mlp_kb_row;
+            // One counter per (m-block, piece): the CTAs of every colwise tile
+            // overlapping the piece's H columns count themselves in it.
+            // (Polling one counter per tile in turn, each an L2 round trip,
+            // saw the last store about 3 us late.)
             const long long c0 = static_cast<long long>(s0) * p.mlp_ks, c1 = c0 + ns * p.mlp_ks;
-            for (int j = static_cast<int>(c0 / BN); ok && j <= static_cast<int>((c1 - 1) / BN); ++j)
-                ok = flag_wait_geq(p.mlp_ready + mb * p.n_tiles + j, CG, abort_flag, p.status, p.timeout_ns);
+            const unsigned tiles = static_cast<unsigned>((c1 - 1) / BN - c0 / BN + 1);
+            ok = flag_wait_geq(p.mlp_ready + mb * 8 + piece, CG * tiles, abort_flag, p.status, p.timeout_ns);
             if (!ok) break;
             fence_proxy_async_global();
         }
-        for (int sh = s0; ok && sh < s0 + ns; ++sh) {
+        // One k-loop per kind of unit, each issuing its loads without a
+        // branch: with the colwise / rowwise choice inside the loop the
+        // loads of a k-block arrived measurably later (a colwise unit's main
+        // loop took 12.8 k cycles against 9.1 k).
+        auto acquire = [&](uint32_t& full_l, uint32_t& a_dst) -> bool {
+            const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
+            // Both pairs have consumed this stage (each pair's MMA commit
+            // arrives on every CTA's empty barrier).
+            if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) return false;
+            if (prank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
+            full_l = mapa_shared(full, rank & ~1u);
+            a_dst = base + stage * C::STAGE_BYTES;
+            return true;
+        };
+        auto advance = [&]() {
+            issued_mask |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        if (!row) {
             for (int kb = 0; kb < nkb; ++kb) {
-                const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
-                if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
-                const uint32_t full_l = (CG == 2) ? mapa_shared(full, 0) : full;
-                const uint32_t a_dst = base + stage * C::STAGE_BYTES;
-                const uint32_t b_dst = a_dst + A_BYTES;
+                uint32_t full_l, a_dst;
+                if (!(ok = acquire(full_l, a_dst))) break;
                 const int kc = kb * BK;
-                if (row) {
-                    if (CG == 2) tma_load_3d_pair(a_dst, &p.mapH, full_l, kc, sh, arow);
-                    else tma_load_3d(a_dst, &p.mapH, full_l, kc, sh, arow);
-                } else {
-                    if (CG == 2) tma_load_2d_pair(a_dst, &p.mapA, full_l, kc, arow);
-                    else tma_load_2d(a_dst, &p.mapA, full_l, kc, arow);
-                }
+                tma_load_2d_pair_mc(a_dst + pc * A_HALF, &p.mapA, full_l, kc, arow, a_mask);
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    const int brow = nb * BN + (static_cast<int>(rank) * C::CHUNKS + c) * B_CHUNK_ROWS;
-                    const uint32_t dst = b_dst + c * B_CHUNK_BYTES;
-                    if (row) {
-                        if (CG == 2) tma_load_3d_pair(dst, &p.mapW2, full_l, kc, sh, brow);
-                        else tma_load_3d(dst, &p.mapW2, full_l, kc, sh, brow);
-                    } else {
-                        if (CG == 2) tma_load_2d_pair(dst, &p.mapB[0], full_l, kc, brow);
-                        else tma_load_2d(dst, &p.mapB[0], full_l, kc, brow);
-                    }
-                }
-                issued_mask |= 1u << stage;
-                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_2d_pair(a_dst + A_BYTES + c * B_CHUNK_BYTES, &p.mapB[0], full_l, kc,
+                                     nb * BN + (prank * C::CHUNKS + c) * B_CHUNK_ROWS);
+                advance();
+            }
+        } else {
+            for (int sh = s0; ok && sh < s0 + ns; ++sh) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    uint32_t full_l, a_dst;
+                    if (!(ok = acquire(full_l, a_dst))) break;
+                    const int kc = kb * BK;
+                    tma_load_3d_pair_mc(a_dst + pc * A_HALF, &p.mapH, full_l, kc, sh, arow, a_mask);
+#pragma unroll
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d_pair(a_dst + A_BYTES + c * B_CHUNK_BYTES, &p.mapW2, full_l, kc, sh,
+                                         nb * BN + (prank * C::CHUNKS + c) * B_CHUNK_ROWS);
+                    advance();
                 }
             }
         }
     }
-    if (!ok && rank == 0) {
+    if (!ok && prank == 0) {
         for (int s = 0; s < C::STAGES; ++s)
             if (issued_mask & (1u << s)) drain_wait(bar0 + 8 * s, (last_parity >> s) & 1u);
     }
@@ -608,7 +644,14 @@ __device__ __forceinline__ void mlp_producer_loop(const GemmParams& p, uint32_t 
 
 template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
-                                         uint32_t tmem_base, volatile int* abort_flag) {
+                                         uint32_t tmem_base, volatile int* abort_flag, uint32_t rank) {
+    constexpr int CL = cluster_ctas<MODE, CG>();
+    // Commit masks (cluster ranks): the accumulator goes to this pair; a
+    // freed stage to every CTA whose stage this pair's MMAs read (with
+    // multicast A, all CTAs of the cluster); the drain to this CTA.
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
+    const uint16_t stage_mask = CL == 4 ? 0xF : pair_mask;
+    const uint16_t self_mask = static_cast<uint16_t>(1u << rank);
     using C = Cfg<MODE, CG, BNT>;
     constexpr bool AMN = Major<MODE>::A_MN, BMN = Major<MODE>::B_MN;
     // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
@@ -621,7 +664,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     const int kblocks = p.k_shards * p.kb_per_shard;
-    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
         const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
         const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
@@ -654,7 +697,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
                 else umma_bf16(d_tmem, ad, bd, idesc, accum);
             }
             // Frees the smem stage (of both CTAs) when these UMMAs finish.
-            if (CG == 2) umma_commit_pair(empty, 0x3);
+            if (CG == 2) umma_commit_pair(empty, stage_mask);
             else umma_commit(empty);
             if (++stage == C::STAGES) {
                 stage = 0;
@@ -663,7 +706,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
         }
         if (!ok) break;
         // Accumulator ready for the epilogue (of both CTAs).
-        if (CG == 2) umma_commit_pair(tfull, 0x3);
+        if (CG == 2) umma_commit_pair(tfull, pair_mask);
         else umma_commit(tfull);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
@@ -671,7 +714,7 @@ __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uin
     if (!ok) {
         // No UMMA may still write TMEM when it is freed.
         const uint32_t drain = bar0 + 8 * (2 * C::STAGES + 4);
-        if (CG == 2) umma_commit_pair(drain, 0x1);
+        if (CG == 2) umma_commit_pair(drain, self_mask);
         else umma_commit(drain);
         drain_wait(drain, 0);
     }
@@ -907,16 +950,17 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
     }
 }
 
-// Epilogue of the fused MLP: 16 warps, four per TMEM lane quadrant, each
-// on 64 of the tile's 256 columns (two 32-column chunks).  The accumulator
+// Epilogue of the fused MLP: 8 warps, two per TMEM lane quadrant, each on
+// 128 of the tile's 256 columns (four 32-column chunks).  The accumulator
 // arrives one row per thread (TMEM lane = row).  Global memory is reached
 // only through TMA: each warp owns two 2 KB boxes in shared memory (32 rows
 // x 64 bytes, 64-byte swizzle: 16-byte piece j of row r at r * 64 + (j ^
 // ((r / 2) % 4)) * 16, which keeps the row-per-thread accesses free of
 // bank conflicts), used in turn, each with an mbarrier for loads into it.
 //  - colwise unit: act(accumulator) -> bf16 H by TMA stores; once the
-//    CTA's 16 warps have seen their stores complete, one thread counts the
-//    CTA's half of the tile in mlp_ready.
+//    CTA's 8 warps have seen their stores complete, one thread counts the
+//    CTA's half of the tile in mlp_ready, once for each K piece whose H
+//    columns the tile overlaps.
 //  - rowwise unit of a lower piece (piece < pieces - 1): its fp32 partial
 //    goes out by TMA stores, then the CTA counts itself in mlp_pdone.
 //  - rowwise unit of the last piece: waits (bounded) until the lower
@@ -924,7 +968,7 @@ __device__ __forceinline__ void std_tile(const GemmParams& p, uint32_t t0, int c
 //    sums P_0 + ... + P_(pieces-2) + its own accumulator in that order (so
 //    the result does not depend on which piece finished first), adds bias
 //    and residual, and stores bf16 Z.
-// The 16 warps meet on hardware barrier 1 (bar.sync over 512 threads).
+// The 8 warps meet on hardware barrier 1 (bar.sync over 256 threads).
 constexpr uint32_t kMlpEpiBar = 1;
 
 // This thread's 64-byte row (16 words) into / out of a box.
@@ -988,6 +1032,8 @@ template <int CG>
 __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t bar0, uint32_t epi0, uint32_t tmem_base,
                                                   uint32_t rank, volatile int* abort_flag) {
     using C = Cfg<tpi::GEMM_MLP, CG, BN>;
+    constexpr int CL = cluster_ctas<tpi::GEMM_MLP, CG>();
+    const int pc = static_cast<int>(rank >> 1), prank = static_cast<int>(rank & 1u);
     constexpr int EPI_WARPS = epi_warps<tpi::GEMM_MLP>();
     constexpr uint32_t EPI_THREADS = 32 * EPI_WARPS;
     constexpr int CPW = (BN / 32) / (EPI_WARPS / 4);  // 32-column chunks per warp
@@ -998,14 +1044,14 @@ __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t 
     MlpBoxes bx{epi0 + static_cast<uint32_t>(warp - 2) * 2 * EPI_BOX_BYTES,
                 bar0 + 8 * (2 * C::STAGES + 5) + 16 + 16 * static_cast<uint32_t>(warp - 2), 0u, 0u, 2u};
     uint32_t acc = 0, acc_phase = 0;
-    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     for (int u = cid; u < p.num_tiles; u += ncl) {
         bool rowu;
         int mb, nb, piece;
-        decode_mlp(p, u, rowu, mb, nb, piece);
+        decode_mlp(p, u, pc, rowu, mb, nb, piece);
         const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
         const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
-        const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // the warp's first row
+        const int row0 = mb * C::TILE_M + prank * BM + q * 32;  // the warp's first row
         const bool box_ok = row0 < p.M;  // warp-uniform
         const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status, p.timeout_ns);
         // Every epilogue warp takes the same branch, so none is left waiting
@@ -1013,7 +1059,8 @@ __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t 
         if (!named_bar_and(kMlpEpiBar, EPI_THREADS, got)) break;
         tc_fence_after();
         const uint32_t t0 = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-        const int tile_ctr = (mb * p.mlp_row_n_tiles + nb) * 2 + static_cast<int>(rank);
+        const int tile_ctr = (mb * p.mlp_row_n_tiles + nb) * 2 + prank;
+        const bool tile_ok = nb < (rowu ? p.mlp_row_n_tiles : p.n_tiles);  // not past the matrix
         uint32_t r[32];
         if (!rowu) {
 #pragma unroll 1
@@ -1043,9 +1090,13 @@ __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t 
             if (lane == 0) bulk_wait_group0();  // this warp's H stores are in global memory
             __syncwarp();
             named_bar_sync(kMlpEpiBar, EPI_THREADS);
-            if (leader) {
+            if (leader && tile_ok) {
                 fence_proxy_async_global();
-                red_release_gpu_add(p.mlp_ready + mb * p.n_tiles + nb, 1u);
+                // Every piece whose H columns this tile overlaps.
+                const long long pw = static_cast<long long>(p.mlp_spp) * p.mlp_ks;
+                const int q0 = static_cast<int>(static_cast<long long>(nb) * BN / pw);
+                const int q1 = static_cast<int>((min(static_cast<long long>(nb + 1) * BN, static_cast<long long>(p.N)) - 1) / pw);
+                for (int q = q0; q <= q1; ++q) red_release_gpu_add(p.mlp_ready + mb * 8 + q, 1u);
             }
         } else if (piece < p.mlp_pieces - 1) {
 #pragma unroll 1
@@ -1072,14 +1123,14 @@ __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t 
             if (lane == 0) bulk_wait_group0();
             __syncwarp();
             named_bar_sync(kMlpEpiBar, EPI_THREADS);
-            if (leader) {
+            if (leader && tile_ok) {
                 fence_proxy_async_global();
                 red_release_gpu_add(p.mlp_pdone + tile_ctr, 1u);
             }
         } else {
             bool ok = true;
             if (p.mlp_pieces > 1) {
-                if (leader)
+                if (leader && tile_ok)
                     ok = flag_wait_geq(p.mlp_pdone + tile_ctr, static_cast<unsigned>(p.mlp_pieces - 1), abort_flag,
                                        p.status, p.timeout_ns);
                 ok = named_bar_and(kMlpEpiBar, EPI_THREADS, ok);
@@ -1167,8 +1218,7 @@ __device__ __forceinline__ void mlp_epilogue_loop(const GemmParams& p, uint32_t 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-            if (CG == 2) mbar_arrive_cluster(mapa_shared(tempty, 0));
-            else mbar_arrive(tempty);
+            mbar_arrive_cluster(mapa_shared(tempty, rank & ~1u));
         }
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
@@ -1377,11 +1427,13 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Rank in the cluster (GEMM_MLP: 0..3, pairs (0, 1) and (2, 3)).
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    constexpr int CL = cluster_ctas<MODE, CG>();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar0 + 8 * s, 1);                // full: leader's arrive + both CTAs' bytes
-            mbar_init(bar0 + 8 * (C::STAGES + s), 1);  // empty: one commit
+            mbar_init(bar0 + 8 * (C::STAGES + s), CL / CG);  // empty: one commit per pair reading it
         }
         mbar_init(bar0 + 8 * (2 * C::STAGES + 0), 1);       // tmem full x2: one commit
         mbar_init(bar0 + 8 * (2 * C::STAGES + 1), 1);
@@ -1428,7 +1480,7 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
         if (warp == 0) {
             if (lane == 0) mlp_producer_loop<CG>(p, base, bar0, rank, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
+            if (lane == 0 && (rank & 1u) == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag, rank);
         } else {
             mlp_epilogue_loop<CG>(p, bar0, epi0, tmem_base, rank, abort_flag);
         }
@@ -1436,7 +1488,7 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
         if (warp == 0) {
             if (lane == 0) producer_loop<MODE, CG, BNT>(p, base, bar0, rank, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0 && rank == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag);
+            if (lane == 0 && (rank & 1u) == 0) mma_loop<MODE, CG, BNT>(p, base, bar0, tmem_base, abort_flag, rank);
         } else {
             epilogue_loop<MODE, CG, BNT>(p, bar0, epi0, tmem_base, rank, abort_flag);
         }
@@ -1523,7 +1575,7 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = cluster_ctas<MODE, CG>();
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     tpi::pdl_attribute(attr[1]);
@@ -1769,7 +1821,42 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
 
 namespace {
 
-// Makespan, in k-blocks, of `units` run round-robin over `pairs` pairs in
+// Clusters of the fused MLP kernel that fit on the current device at once
+// (its persistent grid; every cluster must be resident, since units wait on
+// other units' stores).  0 when the query fails.
+int mlp_max_clusters() {
+    static int counts[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 0;
+    if (!counts[dev]) {
+        constexpr int CG = kPairTiles;
+        auto kern = tp_gemm_kernel<GEMM_MLP, CG, BN>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<GEMM_MLP, CG>::SMEM) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t cfg;
+            memset(&cfg, 0, sizeof(cfg));
+            constexpr int CL = cluster_ctas<GEMM_MLP, CG>();
+            cfg.gridDim = dim3(CL * 64, 1, 1);
+            cfg.blockDim = dim3(num_threads<GEMM_MLP>(), 1, 1);
+            cfg.dynamicSmemBytes = Cfg<GEMM_MLP, CG>::SMEM;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = CL;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        counts[dev] = n > 0 ? n : -1;
+    }
+    return counts[dev] > 0 ? counts[dev] : 0;
+}
+
+// Makespan, in k-blocks, of `units` run round-robin over `pairs` clusters in
 // the fused MLP's unit order (colwise units first), with `fix` k-blocks of
 // partial-sum epilogue charged to each rowwise unit when pieces > 1.
 long long mlp_makespan(long long col_units, long long kb_col, long long row_units, long long kb_row_unit,
@@ -1787,24 +1874,28 @@ long long mlp_makespan(long long col_units, long long kb_col, long long row_unit
 }  // namespace
 
 int64_t mlp_fused_counter_words(int64_t M, int64_t h, int64_t f) {
+    (void)f;
     const int64_t mt = (M + 2 * BM - 1) / (2 * BM);
-    return mt * ((f + BN - 1) / BN) + mt * ((h + BN - 1) / BN) * 2;
+    return mt * 8 + mt * ((h + BN - 1) / BN) * 2;  // ready [mt][8 pieces] | pieces done [mt][tiles][2]
 }
 
 int mlp_fused_pieces(int64_t M, int64_t h, int64_t f, int t, int act) {
     if (kPairTiles != 2) return 0;
     if (act != TP_ACT_GELU_ERF && act != TP_ACT_GELU_TANH && act != TP_ACT_NONE) return 0;
     if (M <= 0 || t <= 0 || f % t || (f / t) % 8 || h % 8) return 0;
-    const int pairs = std::max(1, device_sm_count() / 2);
+    const int clusters = mlp_max_clusters();
+    if (clusters < 1) return 0;
     const long long mt = (M + 2 * BM - 1) / (2 * BM);
-    const long long col_units = mt * ((f + BN - 1) / BN);
+    // Units are two adjacent 256-column tiles of one m-block (one per pair
+    // of a cluster).
+    const long long col_units = mt * (((f + BN - 1) / BN + 1) / 2);
     // Two GEMMs of a few waves each leave SMs idle at each kernel's tail and
     // pay a launch and a pipeline fill each; beyond about three colwise waves
     // the two-GEMM path is as good and needs no scratch.
-    if (col_units > 3LL * pairs) return 0;
+    if (col_units > 3LL * clusters) return 0;
     const long long kb_col = (h + BK - 1) / BK;
     const long long kb_shard = (f / t + BK - 1) / BK;
-    const long long row_tiles = mt * ((h + BN - 1) / BN);
+    const long long row_tiles = mt * (((h + BN - 1) / BN + 1) / 2);
     int best = 0;
     long long best_cost = 0;
     for (int pieces = 1; pieces <= t && pieces <= 8; pieces *= 2) {
@@ -1813,7 +1904,7 @@ int mlp_fused_pieces(int64_t M, int64_t h, int64_t f, int t, int act) {
         // per other piece: charged as two k-blocks each.
         const long long fix = pieces > 1 ? 2LL * (pieces - 1) : 0;
         const long long cost =
-            mlp_makespan(col_units, kb_col, row_tiles * pieces, (t / pieces) * kb_shard, fix, pairs);
+            mlp_makespan(col_units, kb_col, row_tiles * pieces, (t / pieces) * kb_shard, fix, clusters);
         if (best == 0 || cost < best_cost) {
             best = pieces;
             best_cost = cost;
@@ -1825,8 +1916,8 @@ int mlp_fused_pieces(int64_t M, int64_t h, int64_t f, int t, int act) {
 int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
     constexpr int CG = kPairTiles;
     static_assert(CG == 2, "the fused MLP runs on CTA pairs");
-    if (a.pieces < 1 || a.t % a.pieces) {
-        if (err) *err = "fused MLP: pieces must divide t";
+    if (a.pieces < 1 || a.pieces > 8 || a.t % a.pieces) {
+        if (err) *err = "fused MLP: pieces must divide t and be at most 8";
         return TP_ERR_INVALID_ARG;
     }
     GemmParams p;
@@ -1848,14 +1939,14 @@ int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
     p.n_tiles = static_cast<int>((a.f + BN - 1) / BN);
     p.grid_shards = 1;
     p.group_m = 16;
-    p.mlp_col_units = p.m_tiles * p.n_tiles;
     p.mlp_row_n_tiles = static_cast<int>((a.h + BN - 1) / BN);
+    p.mlp_col_units = p.m_tiles * ((p.n_tiles + 1) / 2);
     p.mlp_pieces = a.pieces;
     p.mlp_spp = a.t / a.pieces;
     p.mlp_kb_row = static_cast<int>((Ks + BK - 1) / BK);
     p.mlp_h = static_cast<int>(a.h);
     p.mlp_ks = Ks;
-    const int64_t ready_words = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int64_t ready_words = static_cast<int64_t>(p.m_tiles) * 8;
     p.mlp_ready = a.counters;
     p.mlp_pdone = a.counters + ready_words;
     p.mlp_part = a.partials;
@@ -1864,11 +1955,12 @@ int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
         if (err) *err = "fused MLP: partials buffer missing";
         return TP_ERR_INVALID_ARG;
     }
-    // Colwise operands: X [M][h], W1 [f][h].
+    // Colwise operands: X [M][h] (64-row boxes: each CTA loads half of its
+    // 128 rows and multicasts them to both pairs), W1 [f][h].
     {
         const uint64_t dA[2] = {(uint64_t)a.h, (uint64_t)a.M};
         const uint64_t sA[1] = {(uint64_t)a.h * 2};
-        const uint32_t bA[2] = {BK, BM};
+        const uint32_t bA[2] = {BK, BM / 2};
         if (!make_map(&p.mapA, a.X, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
         const uint64_t dB[2] = {(uint64_t)a.h, (uint64_t)a.f};
         const uint32_t bB[2] = {BK, B_CHUNK_ROWS};
@@ -1878,7 +1970,7 @@ int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
     {
         const uint64_t sK[2] = {(uint64_t)Ks * 2, (uint64_t)a.t * Ks * 2};
         const uint64_t dH[3] = {(uint64_t)Ks, (uint64_t)a.t, (uint64_t)a.M};
-        const uint32_t bH[3] = {BK, 1, BM};
+        const uint32_t bH[3] = {BK, 1, BM / 2};
         if (!make_map(&p.mapH, a.H, 3, dH, sK, bH, err)) return TP_ERR_CUDA;
         const uint64_t dW[3] = {(uint64_t)Ks, (uint64_t)a.t, (uint64_t)a.h};
         const uint32_t bW[3] = {BK, 1, B_CHUNK_ROWS};
@@ -1908,9 +2000,15 @@ int mlp_fused_launch(const MlpArgs& a, cudaStream_t stream, std::string* err) {
                 return TP_ERR_CUDA;
         }
     }
-    p.num_tiles = p.mlp_col_units + p.m_tiles * p.mlp_row_n_tiles * p.mlp_pieces;
+    p.num_tiles = p.mlp_col_units + p.m_tiles * ((p.mlp_row_n_tiles + 1) / 2) * p.mlp_pieces;
     if (p.num_tiles == 0) return TP_OK;
-    const int grid = std::min(p.num_tiles, device_sm_count() / CG) * CG;
+    const int clusters = mlp_max_clusters();
+    if (clusters < 1) {
+        if (err) *err = "fused MLP: no cluster of its kernel fits on this device";
+        return TP_ERR_UNSUPPORTED;
+    }
+    constexpr int CL = cluster_ctas<GEMM_MLP, CG>();
+    const int grid = std::min(p.num_tiles, clusters) * CL;
     return launch_mode<GEMM_MLP, CG>(p, grid, stream, err);
 }
 
