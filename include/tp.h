@@ -345,8 +345,8 @@ TP_API int tp_attn_forward_train(tp_plan_t plan, const tp_bf16* X, const tp_bf16
  * GEMM and the attention forward run again).  dX: [M][h] bf16.  dWq [a d][h],
  * dWk, dWv [k d][h], dWo [h][a d]: fp32, overwritten, or added to when
  * accumulate != 0.  Workspace: tp_plan_workspace_bytes(TP_OP_ATTN_BACKWARD)
- * bytes (it covers recomputation).  Needs head_dim 128 (TP_ERR_UNSUPPORTED
- * otherwise); the plan's reduce mode does not apply. */
+ * bytes (it covers recomputation).  Head dimensions 64 and 128 (the plan's);
+ * the plan's reduce mode does not apply. */
 TP_API int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const tp_bf16* Wk,
                             const tp_bf16* Wv, const tp_bf16* Wo, const tp_bf16* dOut, const tp_bf16* QKV,
                             const tp_bf16* O, const float* LSE, tp_bf16* dX, float* dWq, float* dWk,
@@ -365,9 +365,14 @@ TP_API int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq,
  * partial input gradients) and RMSNorm has unit gain.  X, dY, dX: device
  * [M][h] bf16 (dX may not alias X or dY); w: the layer's weights; grads: fp32
  * weight gradients, overwritten or, with accumulate != 0, added to.
- * Workspace: tp_plan_workspace_bytes(TP_OP_LAYER_BACKWARD).  Needs an
- * attention head_dim of 128, no sequence parallelism, hidden <= 8192, and
- * for SwiGLU f % 64 == 0 (TP_ERR_UNSUPPORTED otherwise). */
+ * Workspace: tp_plan_workspace_bytes(TP_OP_LAYER_BACKWARD).  With a
+ * sequence-parallel plan ([wiki] "시퀀스 병렬화") X, dY and dX are in the
+ * split layout [t][batch][seq/t][h] of tp_layer_forward: the backward of the
+ * forward's all-gathers is a reduce-scatter of the shards' partial input
+ * gradients, whose sum the fused backward GEMMs already hold, so dX is that
+ * sum written into the split layout; the weight gradients are those of the
+ * replicated layer.  Needs hidden <= 8192 and for SwiGLU f % 64 == 0
+ * (TP_ERR_UNSUPPORTED otherwise). */
 TP_API int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, const tp_bf16* dY,
                              tp_bf16* dX, const tp_layer_grads* grads, int accumulate, void* workspace,
                              size_t ws_bytes, void* stream);

@@ -119,6 +119,7 @@ struct Layout {
     size_t lqkv = 0, lo = 0, llse = 0;                       // attention state
     size_t lug = 0;                                          // MLP pre-activations
     size_t lshared = 0;  // max(MLP backward, attention backward workspaces, [M][f] bf16)
+    size_t lspx = 0, lspdy = 0, lspdx = 0;  // sequence parallel: X, dY, dX in token order [M][h] bf16
 };
 
 int64_t seq_pad_of(const tp_plan_s* p) { return (p->cfg.seq + 63) / 64 * 64; }
@@ -167,6 +168,7 @@ Layout layout_of(const tp_plan_s* p, int op) {
         const size_t mb = layout_total(layout_of(p, TP_OP_MLP_BACKWARD));
         const size_t ab = layout_total(layout_of(p, TP_OP_ATTN_BACKWARD));
         L.lshared = std::max(std::max(mb, ab), align_up(M * p->f * 2));
+        if (p->cfg.sequence_parallel) L.lspx = L.lspdy = L.lspdx = act;
     }
     if (op == TP_OP_LAYER) {
         L.h1 = align_up(M * p->h * 2);
@@ -188,7 +190,7 @@ Layout layout_of(const tp_plan_s* p, int op) {
 size_t layout_total(const Layout& L) {
     return L.y + L.mpart + L.mcnt + L.qkv + L.o + L.xn + L.h1 + L.partials + L.ss + L.full + L.ug + L.dug + L.hact + L.bdo +
            L.bdstat + L.bdq + L.bdqkv + L.bqkv + L.bo + L.blse + L.lxn1 + L.lh1 + L.lxn2 + L.ldxn + L.ldh1 +
-           L.lqkv + L.lo + L.llse + L.lug + L.lshared;
+           L.lqkv + L.lo + L.llse + L.lug + L.lshared + L.lspx + L.lspdy + L.lspdx;
 }
 
 int check_ws(const tp_plan_s* p, int op, void* ws, size_t bytes) {
@@ -874,7 +876,6 @@ int tp_attn_backward(tp_plan_t plan, const tp_bf16* X, const tp_bf16* Wq, const 
                      float* dWo, int accumulate, void* workspace, size_t ws_bytes, void* stream) {
     if (!plan) return fail(TP_ERR_INVALID_ARG, "plan is NULL");
     if (!plan->has_attn) return fail(TP_ERR_INVALID_ARG, "the plan has no attention (n_heads == 0)");
-    if (plan->d != 128) return fail(TP_ERR_UNSUPPORTED, "the attention backward needs head_dim 128");
     int rc;
     if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(Wq, "Wq")) ||
         (rc = need_ptr(Wk, "Wk")) || (rc = need_ptr(Wv, "Wv")) || (rc = need_ptr(Wo, "Wo")) ||
@@ -1023,8 +1024,6 @@ int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* 
     if (!plan || !w || !grads) return fail(TP_ERR_INVALID_ARG, "plan, weights and grads must be non-NULL");
     if (!plan->has_attn || !plan->has_mlp)
         return fail(TP_ERR_INVALID_ARG, "a layer needs both attention (n_heads > 0) and an MLP (ffn > 0)");
-    if (plan->cfg.sequence_parallel)
-        return fail(TP_ERR_UNSUPPORTED, "the layer backward does not support sequence parallelism");
     if (plan->h > 8192) return fail(TP_ERR_UNSUPPORTED, "layer RMSNorm supports hidden <= 8192");
     int rc;
     if ((rc = check_device(plan)) || (rc = need_ptr(X, "X")) || (rc = need_ptr(dY, "dY")) ||
@@ -1053,6 +1052,27 @@ int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* 
     const float eps = plan->cfg.rms_eps;
     const int H = static_cast<int>(plan->h);
     std::string err;
+    // Sequence parallel ("시퀀스 병렬화"): X, dY and dX live in the split
+    // layout [t][batch][seq/t].  The forward's all-gathers become the
+    // backward's reduce-scatters and the other way round; on one GPU the
+    // shards' partial input gradients are already summed inside the fused
+    // backward GEMMs, so the layer runs on token-order copies: dY and X are
+    // gathered, and dX is written back into the split layout.  The weight
+    // gradients are the replicated layer's.
+    tp_bf16* dX_sp = nullptr;
+    if (plan->cfg.sequence_parallel) {
+        const int64_t B = plan->cfg.batch, S = plan->cfg.seq;
+        const int T = static_cast<int>(plan->t);
+        void* xf = take(L.lspx);
+        void* dyf = take(L.lspdy);
+        void* dxf = take(L.lspdx);
+        if ((rc = run(tpi::sp_all_gather_launch(X, B, S, T, H, xf, s, &err), err))) return rc;
+        if ((rc = run(tpi::sp_all_gather_launch(dY, B, S, T, H, dyf, s, &err), err))) return rc;
+        X = static_cast<const tp_bf16*>(xf);
+        dY = static_cast<const tp_bf16*>(dyf);
+        dX_sp = dX;
+        dX = static_cast<tp_bf16*>(dxf);
+    }
     // Forward, keeping what the backward reads.
     if ((rc = run(tpi::rmsnorm_launch(X, plan->M, H, eps, xn1, s, &err), err))) return rc;
     if ((rc = do_qkv(plan, xn1, w->Wq, w->Wk, w->Wv, qkv, s))) return rc;
@@ -1072,7 +1092,12 @@ int tp_layer_backward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* 
                                static_cast<const tp_bf16*>(o), lse, static_cast<tp_bf16*>(dxn), grads->dWq,
                                grads->dWk, grads->dWv, grads->dWo, accumulate, shared, L.lshared, stream)))
         return rc;
-    return run(tpi::rmsnorm_bwd_launch(X, dxn, dh1, plan->M, H, eps, dX, s, &err), err);
+    if ((rc = run(tpi::rmsnorm_bwd_launch(X, dxn, dh1, plan->M, H, eps, dX, s, &err), err))) return rc;
+    if (dX_sp)
+        return run(tpi::sp_split_launch(dX, plan->cfg.batch, plan->cfg.seq, static_cast<int>(plan->t), H, dX_sp, s,
+                                        &err),
+                   err);
+    return TP_OK;
 }
 
 int tp_layer_forward(tp_plan_t plan, const tp_bf16* X, const tp_layer_weights* w, tp_bf16* Y,

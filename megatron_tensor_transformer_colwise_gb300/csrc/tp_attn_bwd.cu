@@ -51,6 +51,13 @@
 // one CTA's TMEM accumulators, so the KV replicas of the t-device form (when
 // there are fewer KV heads than shards) need no extra reduction: the sum
 // over replicas is the sum over the group.
+//
+// Head dimensions 64 and 128 (the kernels are templates on d).  At d = 64 the
+// K, V, Q and dO tiles are one 64-column box each, dV and dK have 64 TMEM
+// columns, and dQ^T is still issued with M = 128: its A operand's second
+// 64-row block is the V tile, so TMEM lanes 64-127 hold numbers nobody reads
+// (a row of an MMA's result depends only on the same row of A), and the two
+// dQ warps of those lanes skip their reduce-adds.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -66,7 +73,6 @@ namespace {
 
 using namespace tpk;
 
-constexpr int HD = 128;                        // head dimension this kernel handles
 constexpr int BKEYS = 128;                     // keys per CTA: UMMA M of S^T, dP^T, dV, dK
 constexpr int BQ = 64;                         // queries per step: UMMA N of S^T, dP^T, dQ^T
 constexpr int NSTAGE = 3;                      // Q / dO / statistics ring
@@ -79,21 +85,10 @@ constexpr int GRAD_WARP = 2 + SM_WARPS + 4;   // issuer of dV, dK
 constexpr int DQ_WARP = GRAD_WARP + 1;         // issuer of dQ^T
 constexpr int NTHREADS = 32 * (DQ_WARP + 1);
 constexpr int KBOX_BYTES = BKEYS * 128;        // box {64 d, 128 keys}: 16 KB
-constexpr int KT_BYTES = 2 * KBOX_BYTES;       // K or V tile: 32 KB
 constexpr int QBOX_BYTES = BQ * 128;           // box {64 d, 64 queries}: 8 KB
-constexpr int QT_BYTES = 2 * QBOX_BYTES;       // Q or dO tile: 16 KB
 constexpr int PT_BYTES = BKEYS * BQ * 2;       // dS^T [128 keys][64 queries]: 16 KB
 constexpr int STAT_BYTES = 2 * BQ * 4;         // log-sum-exp and D of 64 queries
 constexpr int DQ_BOX_BYTES = BQ * 32 * 4;      // one dQ warp's [64 queries][32 d] fp32: 8 KB
-
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + KT_BYTES;
-constexpr int OFF_Q = OFF_V + KT_BYTES;
-constexpr int OFF_DO = OFF_Q + NSTAGE * QT_BYTES;
-constexpr int OFF_DST = OFF_DO + NSTAGE * QT_BYTES;  // dS^T x2
-constexpr int OFF_STAT = OFF_DST + 2 * PT_BYTES;
-constexpr int OFF_DQ = OFF_STAT + NSTAGE * STAT_BYTES;
-constexpr int OFF_BAR = OFF_DQ + 4 * DQ_BOX_BYTES;
 
 constexpr int B_KV_FULL = 0;
 constexpr int B_Q_FULL = 1;                  // x NSTAGE
@@ -107,23 +102,40 @@ constexpr int B_DQ_EMPTY = B_DQ_FULL + 1;
 constexpr int B_DKV_FULL = B_DQ_EMPTY + 1;
 constexpr int B_DRAIN = B_DKV_FULL + 1;      // x3: one per issuing thread
 constexpr int NUM_BARS = B_DRAIN + 3;
-// The data fill all but a few bytes of the 227 KB a CTA may use, leaving no
-// room to align the dynamic shared-memory base to 1024 bytes ourselves; the
-// kernel checks at run time that the base is aligned (it is when the kernel
-// has no static shared memory) and otherwise stops with an error flag,
-// touching nothing.
-constexpr int DATA_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
-constexpr int SMEM_BYTES = DATA_BYTES + 128 <= 232448 ? DATA_BYTES + 128 : 232448;
+// Shared-memory layout for head dimension HD.  At HD = 128 the data fill all
+// but a few bytes of the 227 KB a CTA may use, leaving no room to align the
+// dynamic shared-memory base to 1024 bytes ourselves; the kernel checks at
+// run time that the base is aligned (it is when the kernel has no static
+// shared memory) and otherwise stops with an error flag, touching nothing.
+template <int HD_>
+struct BwdLayout {
+    static constexpr int HD = HD_;
+    static constexpr int DBOX = HD / 64;               // 64-column boxes per tile row
+    static constexpr int KT_BYTES = DBOX * KBOX_BYTES;  // K or V tile
+    static constexpr int QT_BYTES = DBOX * QBOX_BYTES;  // Q or dO tile
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KT_BYTES;
+    static constexpr int OFF_Q = OFF_V + KT_BYTES;
+    static constexpr int OFF_DO = OFF_Q + NSTAGE * QT_BYTES;
+    static constexpr int OFF_DST = OFF_DO + NSTAGE * QT_BYTES;  // dS^T x2
+    static constexpr int OFF_STAT = OFF_DST + 2 * PT_BYTES;
+    static constexpr int OFF_DQ = OFF_STAT + NSTAGE * STAT_BYTES;
+    static constexpr int OFF_BAR = OFF_DQ + 4 * DQ_BOX_BYTES;
+    static constexpr int DATA_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
+    // Room to align the base by hand where it fits (it does at both sizes).
+    static constexpr int SMEM_BYTES = DATA_BYTES + 1024 <= 232448 ? DATA_BYTES + 1024 : 232448;
+    static_assert(HD == 64 || HD == 128, "head dimensions 64 and 128");
+    static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DST % 1024 == 0 && PT_BYTES % 1024 == 0,
+                  "swizzled tiles must be 1024-byte aligned");
+    static_assert(OFF_DQ % 128 == 0, "TMA boxes must be 128-byte aligned");
+    static_assert(DATA_BYTES <= 232448, "shared memory");
+};
 
-// TMEM columns (512 allocated): S^T, dP^T (64 each), dV, dK (128 each), dQ^T
-// (64), and P^T x2 as bf16 (32 packed columns each: the A operand of dV).
+// TMEM columns (512 allocated): S^T, dP^T (64 each), dV, dK (d each, at 128
+// and 256), dQ^T (64), and P^T x2 as bf16 (32 packed columns each: the A
+// operand of dV).
 constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ = 384, COL_PT0 = 448,
                    COL_PT1 = 480;
-
-static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DST % 1024 == 0 && PT_BYTES % 1024 == 0,
-              "swizzled tiles must be 1024-byte aligned");
-static_assert(OFF_DQ % 128 == 0, "TMA boxes must be 128-byte aligned");
-static_assert(DATA_BYTES <= 232448, "shared memory");
 
 struct BwdParams {
     CUtensorMap map_kv;  // the QKV buffer: dims {ld_qkv, tokens}, box {64, 128}
@@ -184,7 +196,13 @@ __device__ __forceinline__ void ld_cols(uint32_t a, uint32_t (&r)[16]) { tmem_ld
 __device__ __forceinline__ void st_cols(uint32_t a, const uint32_t (&r)[16]) { tmem_st16(a, r); }
 __device__ __forceinline__ void st_cols(uint32_t a, const uint32_t (&r)[8]) { tmem_st8(a, r); }
 
+template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdLayout<HD>;
+    constexpr int KT_BYTES = L::KT_BYTES, QT_BYTES = L::QT_BYTES, DBOX = L::DBOX;
+    constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_Q = L::OFF_Q, OFF_DO = L::OFF_DO;
+    constexpr int OFF_DST = L::OFF_DST, OFF_STAT = L::OFF_STAT, OFF_DQ = L::OFF_DQ, OFF_BAR = L::OFF_BAR;
+    constexpr int DATA_BYTES = L::DATA_BYTES, SMEM_BYTES = L::SMEM_BYTES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -274,7 +292,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             uint32_t issued = 0, ipar = 0;
             mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * KT_BYTES);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < DBOX; ++c) {
                 tma_load_2d(sK + c * KBOX_BYTES, &p.map_kv, bar(B_KV_FULL), kcol + 64 * c, tok0 + k0);
                 tma_load_2d(sV + c * KBOX_BYTES, &p.map_kv, bar(B_KV_FULL), vcol + 64 * c, tok0 + k0);
             }
@@ -292,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
                 const int row = tok0 + qb * BQ;
                 mbar_arrive_expect_tx(bar(B_Q_FULL + st), 2 * QT_BYTES + STAT_BYTES);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < DBOX; ++c) {
                     tma_load_2d(sQ + st * QT_BYTES + c * QBOX_BYTES, &p.map_q, bar(B_Q_FULL + st),
                                 qcol + 64 * c, row);
                     tma_load_2d(sDO + st * QT_BYTES + c * QBOX_BYTES, &p.map_do, bar(B_Q_FULL + st),
@@ -320,7 +338,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
             constexpr uint32_t id_kv = idesc_bf16_f32(BKEYS, HD) | (1u << 16);
             // dQ^T: M d, N 64 queries, K = keys; A = K read MN-major from its
             // [key][d] tile, B = dS^T read MN-major from its [key][query] tile.
-            constexpr uint32_t id_q = idesc_bf16_f32(HD, BQ) | (1u << 15) | (1u << 16);
+            // M is 128 at d = 64 as well (its second 64-row block of A is the
+            // V tile; those result rows are not read).
+            constexpr uint32_t id_q = idesc_bf16_f32(128, BQ) | (1u << 15) | (1u << 16);
             bool ok = mbar_wait(bar(B_KV_FULL), 0, abort_flag, p.status, p.timeout_ns);
             // Descriptors built once; a step adds its constant offset (in
             // 16-byte units) to the start-address field.
@@ -576,12 +596,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
         const int q4 = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t sdq = base + OFF_DQ + static_cast<uint32_t>(warp - 2 - SM_WARPS) * DQ_BOX_BYTES;
+        const bool dims = q4 * 32 < HD;  // this warp's TMEM lanes hold head dimensions
         for (int it = 0; it < n_it; ++it) {
             const bool got = mbar_wait(bar(B_DQ_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, p.status,
                                        p.timeout_ns);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
+            if (!dims) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+                continue;
+            }
             if (lane == 0) bulk_wait_group_read0();  // the previous box has been read
             __syncwarp();
             // Row c of the box = query c; lane = dimension: 128 contiguous bytes
@@ -626,11 +653,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_kernel(const __grid_cons
 // One warp per (head, sequence, padded position).
 // D = rowsum(dO (.) O) per (head, sequence, position) and the zeroed fp32 dQ
 // accumulator.  One CTA per token row of a sequence padded to seq_pad (all
-// heads of the row, 16-byte loads): a head's HD = 128 values are 16 chunks
-// of 8, summed across a half-warp.  Padding positions get D = 0.
+// heads of the row, 16-byte loads): a head's HD values are HD / 8 chunks of
+// 8, summed across HD / 8 lanes.  Padding positions get D = 0.
 constexpr int PREP_THREADS = 256;
 constexpr int PREP_MAX_HEADS = 1024;
 
+template <int HD>
 __global__ void __launch_bounds__(PREP_THREADS) attn_bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O, long long ld, int heads,
     int batch, int seq, long long seq_pad, float* __restrict__ dstat, float* __restrict__ dq, long long ld_dq) {
@@ -660,9 +688,10 @@ __global__ void __launch_bounds__(PREP_THREADS) attn_bwd_prep_kernel(
                     acc = fmaf(u.x, v.x, fmaf(u.y, v.y, acc));
                 }
             }
+            // A head's HD / 8 chunks sit in HD / 8 consecutive lanes.
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if ((lane & 15) == 0 && c < nchunk) dsum[c / (HD / 8)] = acc;
+            for (int off = HD / 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if ((lane & (HD / 8 - 1)) == 0 && c < nchunk) dsum[c / (HD / 8)] = acc;
         }
         float4* z = reinterpret_cast<float4*>(dq + row * ld_dq);
         for (int e = tid; e < heads * (HD / 4); e += PREP_THREADS) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -718,16 +747,10 @@ int check(const char* what, std::string* err) {
     return TP_OK;
 }
 
-}  // namespace
 
-namespace tpi {
-
-int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err) {
-    if (a.batch == 0 || a.seq == 0) return TP_OK;
-    if (a.head_dim != HD) {
-        if (err) *err = "the attention backward supports head_dim 128";
-        return TP_ERR_UNSUPPORTED;
-    }
+template <int HD>
+int attn_bwd_launch_hd(const tpi::AttnBwdArgs& a, cudaStream_t stream, std::string* err) {
+    constexpr int SMEM_BYTES = BwdLayout<HD>::SMEM_BYTES;
     const long long tokens = static_cast<long long>(a.batch) * a.seq;
     // 1. D and a zeroed dQ accumulator.
     {
@@ -740,7 +763,7 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
         // kernels measured 0.6% slower (1187 vs 1180 us per block backward
         // on one GB300), the many small CTAs of the next kernel waiting
         // beside the last wave.  Their griddepcontrol calls are then no-ops.
-        attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), PREP_THREADS, 0, stream>>>(
+        attn_bwd_prep_kernel<HD><<<static_cast<unsigned>(blocks), PREP_THREADS, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16*>(a.dO), reinterpret_cast<const __nv_bfloat16*>(a.O),
             a.ld_do, a.heads, a.batch, a.seq, a.seq_pad, a.dstat, a.dq, a.ld_dq);
         int rc = check("attention backward prep kernel", err);
@@ -822,7 +845,7 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
         int dev = 0;
         cudaGetDevice(&dev);
         if (dev < 64 && !configured[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  SMEM_BYTES);
             if (e != cudaSuccess) {
                 if (err) *err = std::string("cudaFuncSetAttribute(attention backward): ") + cudaGetErrorString(e);
@@ -831,7 +854,7 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
             configured[dev] = true;
         }
         const unsigned grid = static_cast<unsigned>(((a.seq + BKEYS - 1) / BKEYS) * a.kv_heads * a.batch);
-        attn_bwd_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
+        attn_bwd_kernel<HD><<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
         int rc = check("attention backward kernel", err);
         if (rc) return rc;
     }
@@ -842,6 +865,21 @@ int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err)
         attn_bwd_dq_cast_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
             a.dq, a.ld_dq, tokens, static_cast<int>(n), reinterpret_cast<__nv_bfloat16*>(a.dqkv), a.ld_dqkv);
         return check("attention backward dQ cast kernel", err);
+    }
+}
+
+}  // namespace
+
+namespace tpi {
+
+int attn_bwd_launch(const AttnBwdArgs& a, cudaStream_t stream, std::string* err) {
+    if (a.batch == 0 || a.seq == 0) return TP_OK;
+    switch (a.head_dim) {
+        case 64: return attn_bwd_launch_hd<64>(a, stream, err);
+        case 128: return attn_bwd_launch_hd<128>(a, stream, err);
+        default:
+            if (err) *err = "the attention backward supports head_dim 64 and 128";
+            return TP_ERR_UNSUPPORTED;
     }
 }
 

@@ -279,6 +279,22 @@ __global__ void __launch_bounds__(AG_WARPS * 32) sp_all_gather_kernel(
     for (int c = threadIdx.x & 31; c < (h >> 3); c += 32) dst[c] = src[c];
 }
 
+// The inverse of the all-gather: a token-order tensor into the sequence-split
+// layout, one warp per row, 16-byte vectors.  The sequence-parallel layer's
+// backward uses it as the reduce-scatter of dX, whose sum over the shards the
+// fused backward GEMMs already hold ("텐서 병렬화", "시퀀스 병렬화").
+__global__ void __launch_bounds__(AG_WARPS * 32) sp_split_kernel(
+    const __nv_bfloat16* __restrict__ full, long long rows, int h, long long batch, long long seq,
+    int t, __nv_bfloat16* __restrict__ sp) {
+    pdl_trigger();
+    pdl_wait();
+    const long long row = static_cast<long long>(blockIdx.x) * AG_WARPS + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint4* src = reinterpret_cast<const uint4*>(full + row * h);
+    uint4* dst = reinterpret_cast<uint4*>(sp + sp_out_row(row, batch, seq, t) * h);
+    for (int c = threadIdx.x & 31; c < (h >> 3); c += 32) dst[c] = src[c];
+}
+
 // Failure-detection self test: wait on a barrier that never completes.
 __global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -542,6 +558,16 @@ int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int 
                stream, reinterpret_cast<const __nv_bfloat16*>(sp), rows, h, batch, seq, t,
                reinterpret_cast<__nv_bfloat16*>(full));
     return check_launch("all-gather kernel", err);
+}
+
+int sp_split_launch(const void* full, int64_t batch, int64_t seq, int t, int h, void* sp,
+                    cudaStream_t stream, std::string* err) {
+    const long long rows = batch * seq;
+    if (rows == 0) return TP_OK;
+    launch_pdl(sp_split_kernel, dim3((unsigned)((rows + AG_WARPS - 1) / AG_WARPS)), dim3(AG_WARPS * 32), 0,
+               stream, reinterpret_cast<const __nv_bfloat16*>(full), rows, h, batch, seq, t,
+               reinterpret_cast<__nv_bfloat16*>(sp));
+    return check_launch("split kernel", err);
 }
 
 int rmsnorm_bwd_launch(const void* x, const void* g, const void* res, int64_t rows, int h, float eps,

@@ -151,6 +151,9 @@ int reduce_norm_launch(const void* partials, int partial_f32, int t, int64_t row
 // full[b * seq + pos] = sp[row of (b, pos) in [t][batch][seq / t]].
 int sp_all_gather_launch(const void* sp, int64_t batch, int64_t seq, int t, int h, void* full,
                          cudaStream_t stream, std::string* err);
+// sp[row of (b, pos) in [t][batch][seq / t]] = full[b * seq + pos].
+int sp_split_launch(const void* full, int64_t batch, int64_t seq, int t, int h, void* sp,
+                    cudaStream_t stream, std::string* err);
 int rmsnorm_launch(const void* x, int64_t rows, int h, float eps, void* y, cudaStream_t stream,
                    std::string* err);
 // ss[row] = sum_j x[row][j]^2 (fp32 over the bf16 values); zero[row] = 0

@@ -584,3 +584,30 @@ def mlp_backward_composed(X, W1, W2, dZ, W3):
     dU = dH * G * s * (1.0 + U * (1.0 - s))
     dG = dH * U * s
     return (dU @ W1 + dG @ W3, dU.T @ X, dG.T @ X, dZ.T @ H, dZ.sum(axis=0))
+
+
+def sp_split(batch: int, seq: int, t: int, full) -> np.ndarray:
+    """A token-order tensor [batch seq][h] in the sequence-split layout
+    [t][batch][seq/t][h] (row of token (b, pos) from tpo_sp_row)."""
+    full = _d(full)
+    out = np.empty_like(full)
+    rows = [sp_row(batch, seq, t, b, pos) for b in range(batch) for pos in range(seq)]
+    out[rows] = full
+    return out
+
+
+def layer_sp_backward(batch: int, seq: int, a: int, k: int, d: int, t: int, X_sp, Wq, Wk, Wv, Wo, W1, W3, W2,
+                      dY_sp, eps: float = 1e-5, composed: bool = False):
+    """(dX_sp, dWq, dWk, dWv, dWo, dW1, dW3, dW2) of the sequence-parallel
+    pre-norm layer ("텐서 병렬화", "시퀀스 병렬화"): X_sp, dY_sp and dX_sp in
+    the split layout [t][batch][seq/t][h].  The forward's all-gather of each
+    block's input has a reduce-scatter as its backward and its reduce-scatter
+    an all-gather, so: dY is all-gathered, the layer's backward runs on the
+    token-order tensors (the replicated layer's, whose dX already holds the
+    shards' sum), and dX is scattered into the split layout.  composed: use
+    layer_backward_composed (numpy matrix products) for large sizes."""
+    X = sp_all_gather(batch, seq, t, X_sp)
+    dY = sp_all_gather(batch, seq, t, dY_sp)
+    fn = layer_backward_composed if composed else layer_backward
+    out = fn(batch, seq, a, k, d, X, Wq, Wk, Wv, Wo, W1, W3, W2, dY, eps=eps)
+    return (sp_split(batch, seq, t, out[0]),) + tuple(out[1:])

@@ -26,3 +26,14 @@ def layer_forward():
     Y, h1 = oracle.layer_composed(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, f64(inp["X"]),
                                   *(f64(inp[n]) for n in LAYER_WEIGHTS), want_h1=True)
     return inp, Y, h1
+
+
+@functools.lru_cache(maxsize=None)
+def layer_backward():
+    """(inputs, dY, (dX, dWq, dWk, dWv, dWo, dW1, dW3, dW2)) of the full layer."""
+    s = SHAPES["layer"]
+    inp = synth.workload_inputs(s)
+    dY = synth.grad_output(s)
+    out = oracle.layer_backward_composed(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, f64(inp["X"]),
+                                         *(f64(inp[n]) for n in LAYER_WEIGHTS), f64(dY))
+    return inp, dY, out

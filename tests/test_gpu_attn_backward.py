@@ -4,14 +4,12 @@ fp64 oracle, through the C ABI (tp_attn_forward_train, tp_attn_backward).
 Small shapes compare every output with the oracle's literal t-device form
 (the same dOut to every shard; dX the sum of the shards' partials; a
 replicated KV head's weight gradient the sum over the shards holding it).
-They cover GQA groups of 1 to 4, KV replicas (k < t), ragged sequence
-lengths (not multiples of the 64-query or 128-key blocks), sequences shorter
-than one key block and several batches.  At the full size the bench runs
-(4 x 2048 tokens, h 4096, 32 query / 8 KV heads of 128, t 8), two slices
-the oracle computes on their own are compared: the weight gradients of one
-KV group (that group's heads alone are a smaller attention block with the
-same gradients there), and dX on the rows of one sequence (sequences never
-attend across each other)."""
+They cover head dimensions 64 and 128, GQA groups of 1 to 4, KV replicas
+(k < t), ragged sequence lengths (not multiples of the 64-query or 128-key
+blocks), sequences shorter than one key block and several batches.  At the
+full size the bench runs (4 x 2048 tokens, h 4096, 32 query / 8 KV heads of
+128, t 8) every output is compared with the oracle's composed form (numpy
+projections, the C attention core; pinned equal to the all-C form)."""
 import numpy as np
 import pytest
 import torch
@@ -20,7 +18,8 @@ import megatron_tensor_transformer_colwise_gb300 as tp
 import oracle
 import synth
 from synth import Shape
-from gpu_util import assert_close, dev, host64, plan_for, sync_ok, workspace
+from gpu_util import (assert_close, dev, elementwise_excess_fraction, host64, plan_for, report, sync_ok,
+                      workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,6 +66,11 @@ SMALL = [
     Shape("ab_mha_ragged", 2, 192, 128, heads=2, kv_heads=2, head_dim=128, tp=2, act="none", index=53),
     Shape("ab_short_t8", 3, 40, 256, heads=8, kv_heads=8, head_dim=128, tp=8, act="none", index=54),
     Shape("ab_group4", 1, 384, 512, heads=8, kv_heads=2, head_dim=128, tp=4, act="none", index=55),
+    # head dimension 64
+    Shape("ab_d64_gqa2", 2, 128, 256, heads=8, kv_heads=4, head_dim=64, tp=2, act="none", index=58),
+    Shape("ab_d64_replica_ragged", 1, 200, 256, heads=4, kv_heads=1, head_dim=64, tp=4, act="none", index=59),
+    Shape("ab_d64_group4_multi", 2, 320, 512, heads=16, kv_heads=4, head_dim=64, tp=4, act="none", index=60),
+    Shape("ab_d64_short_t8", 3, 40, 256, heads=8, kv_heads=8, head_dim=64, tp=8, act="none", index=61),
 ]
 
 
@@ -105,7 +109,7 @@ def test_accumulate_adds_to_the_weight_gradients():
     assert_close(host64(got["dX"]), ref["dX"], what="dX with accumulate")
 
 
-def test_saved_state_must_be_all_or_nothing_and_head_dim_128():
+def test_saved_state_must_be_all_or_nothing():
     s = SMALL[0]
     plan = plan_for(s)
     QKV, O, LSE = saved_buffers(plan)
@@ -121,42 +125,34 @@ def test_saved_state_must_be_all_or_nothing_and_head_dim_128():
     with pytest.raises(tp.TPError) as e:
         tp.tp_attn_backward(plan, X, Wq, Wk, Wv, Wo, dOut, QKV, None, LSE, dX, *grads, False, ws, nws)
     assert e.value.code == tp.TP_ERR_INVALID_ARG
-    s64 = Shape("ab_d64", 1, 64, 128, heads=2, kv_heads=2, head_dim=64, tp=2, act="none", index=56)
-    p64 = plan_for(s64)
-    ws64, n64 = workspace(p64, tp.TP_OP_ATTN_BACKWARD)
-    with pytest.raises(tp.TPError) as e:
-        tp.tp_attn_backward(p64, torch.zeros(64, 128, **bf), torch.zeros(128, 128, **bf),
-                            torch.zeros(128, 128, **bf), torch.zeros(128, 128, **bf),
-                            torch.zeros(128, 128, **bf), torch.zeros(64, 128, **bf), None, None, None,
-                            torch.zeros(64, 128, **bf), torch.zeros(128, 128, **f32),
-                            torch.zeros(128, 128, **f32), torch.zeros(128, 128, **f32),
-                            torch.zeros(128, 128, **f32), False, ws64, n64)
-    assert e.value.code == tp.TP_ERR_UNSUPPORTED
     sync_ok(plan)
+
+
+def test_head_dim_64_recomputed_forward_state_gives_the_same_gradients():
+    s = SMALL[7]
+    inp = synth.workload_inputs(s)
+    dOut = synth.grad_output(s)
+    a = run_backward(s, inp, dOut, saved=True)
+    b = run_backward(s, inp, dOut, saved=False)
+    for n in ("dWk", "dWv", "dWo"):
+        assert torch.equal(a[n], b[n]), n
+    for n in ("dX", "dWq"):
+        assert_close(host64(b[n]), host64(a[n]), tol=2e-3, what=n)
 
 
 # The layer's attention block at full size (the configuration the bench times).
 FULL = Shape("ab_full", 4, 2048, 4096, heads=32, kv_heads=8, head_dim=128, tp=8, act="none", index=57)
 
 
-def test_full_size_attention_backward_slices():
+def test_full_size_attention_backward_full_output():
     s = FULL
     inp = synth.workload_inputs(s)
     dOut = synth.grad_output(s)
     got = run_backward(s, inp, dOut)
-    a, k, d = s.heads, s.kv_heads, s.head_dim
-    G = a // k
-    X, Wq, Wk, Wv, Wo = (host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo"))
-    dO64 = host64(dOut)
-    # (1) KV group 0 alone: query heads 0..G-1 and KV head 0.
-    qr = slice(0, G * d)
-    _, rWq, rWk, rWv, rWo = oracle.attention_backward_composed(
-        s.batch, s.seq, G, 1, X, Wq[qr], Wk[:d], Wv[:d], Wo[:, qr], dO64)
-    assert_close(host64(got["dWq"])[qr], rWq, what="full-size dWq, group 0")
-    assert_close(host64(got["dWk"])[:d], rWk, what="full-size dWk, head 0")
-    assert_close(host64(got["dWv"])[:d], rWv, what="full-size dWv, head 0")
-    assert_close(host64(got["dWo"])[:, qr], rWo, what="full-size dWo, group 0")
-    # (2) dX on the rows of the last sequence: that sequence alone.
-    rows = slice((s.batch - 1) * s.seq, s.batch * s.seq)
-    rdX = oracle.attention_backward_composed(1, s.seq, a, k, X[rows], Wq, Wk, Wv, Wo, dO64[rows])[0]
-    assert_close(host64(got["dX"])[rows], rdX, what="full-size dX, last sequence")
+    ref = oracle.attention_backward_composed(s.batch, s.seq, s.heads, s.kv_heads,
+                                             *(host64(inp[n]) for n in ("X", "Wq", "Wk", "Wv", "Wo")),
+                                             host64(dOut))
+    for n, r in zip(("dX", "dWq", "dWk", "dWv", "dWo"), ref):
+        g = host64(got[n])
+        e = assert_close(g, r, what=f"full-size {n}")
+        report(f"attn backward {n}", max_rel=e, frac_beyond=elementwise_excess_fraction(g, r))

@@ -7,7 +7,9 @@ Small layers and the full size the bench runs (4 x 2048 tokens, h 4096,
 f 14336, 32 query / 8 KV heads of 128, t 8) compare every output: dX and
 all seven weight gradients.  At full size the oracle runs in its composed
 form (numpy matrix products, the C attention core and norms; pinned equal to
-the all-C definition)."""
+the all-C definition).  The sequence-parallel layer ("시퀀스 병렬화") takes
+X, dY and dX in the split layout [t][batch][seq/t][h] and is compared with
+oracle.layer_sp_backward."""
 import numpy as np
 import pytest
 import torch
@@ -16,6 +18,7 @@ import megatron_tensor_transformer_colwise_gb300 as tp
 import oracle
 import synth
 from synth import SHAPES, Shape
+import full_refs
 from gpu_util import (assert_close, dev, elementwise_excess_fraction, host64, plan_for, report,
                       sync_ok, workspace)
 
@@ -24,8 +27,14 @@ pytestmark = pytest.mark.gpu
 NAMES = ["dX", "dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"]
 
 
-def run_layer_backward(s, inp, dY, accumulate=False, init=0.0):
-    plan = plan_for(s)
+def sp_plan(s, mode=tp.TP_REDUCE_FUSED):
+    return tp.Plan(tp.make_config(tokens=s.tokens, hidden=s.hidden, ffn=s.ffn, n_heads=s.heads,
+                                  n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp, act=s.act,
+                                  reduce_mode=mode, batch=s.batch, seq=s.seq, sequence_parallel=1))
+
+
+def run_layer_backward(s, inp, dY, accumulate=False, init=0.0, plan=None):
+    plan = plan_for(s) if plan is None else plan
     ws, nws = workspace(plan, tp.TP_OP_LAYER_BACKWARD)
     w = {k: dev(v) for k, v in inp.items() if k != "X"}
     f32 = dict(dtype=torch.float32, device="cuda")
@@ -49,6 +58,7 @@ SMALL = [
           index=61),
     Shape("lb_replica_ragged", 1, 200, 256, ffn=320, heads=4, kv_heads=1, head_dim=128, tp=4,
           act="swiglu", index=62),
+    Shape("lb_d64", 2, 128, 256, ffn=512, heads=8, kv_heads=2, head_dim=64, tp=4, act="swiglu", index=63),
 ]
 
 
@@ -73,29 +83,48 @@ def test_layer_backward_accumulates_weight_gradients():
     assert_close(host64(got["dX"]), ref["dX"], what="dX with accumulate")
 
 
-def test_layer_backward_rejects_sequence_parallel_plans():
+def _split(x, s):
+    """Token-order tensor -> the sequence-split layout (oracle's row map)."""
+    return torch.from_numpy(oracle.sp_split(s.batch, s.seq, s.tp, host64(x))).to(x.dtype)
+
+
+@pytest.mark.parametrize("mode", [tp.TP_REDUCE_PARTIALS, tp.TP_REDUCE_FUSED], ids=["partials", "fused"])
+def test_small_sequence_parallel_layer_backward_full_output(mode):
     s = SMALL[0]
-    cfg = tp.make_config(tokens=s.tokens, hidden=s.hidden, ffn=s.ffn, n_heads=s.heads,
-                         n_kv_heads=s.kv_heads, head_dim=s.head_dim, tp_degree=s.tp, act=s.act,
-                         reduce_mode=tp.TP_REDUCE_PARTIALS, batch=s.batch, seq=s.seq,
-                         sequence_parallel=1)
-    plan = tp.Plan(cfg)
-    bf = dict(dtype=torch.bfloat16, device="cuda")
-    X = torch.zeros(s.tokens, s.hidden, **bf)
-    with pytest.raises(tp.TPError) as e:
-        tp.tp_layer_backward(plan, X, {}, X.clone(), X.clone(), {}, False, None, 0)
-    assert e.value.code in (tp.TP_ERR_UNSUPPORTED, tp.TP_ERR_INVALID_ARG)
+    inp = synth.workload_inputs(s)
+    dY = synth.grad_output(s)
+    X_sp, dY_sp = _split(inp["X"], s), _split(dY, s)
+    got = run_layer_backward(s, dict(inp, X=X_sp), dY_sp, plan=sp_plan(s, mode))
+    args = [host64(inp[k]) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")]
+    ref = dict(zip(NAMES, oracle.layer_sp_backward(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim, s.tp,
+                                                   host64(X_sp), *args, host64(dY_sp))))
+    for n in NAMES:
+        assert_close(host64(got[n]), ref[n], what=f"SP {n}")
+    # dX is the replicated layer's, in the split layout
+    rep = run_layer_backward(s, inp, dY)
+    assert torch.equal(got["dX"].view(torch.int16), _split(rep["dX"], s).view(torch.int16))
 
 
 def test_full_size_layer_backward_full_output():
     s = SHAPES["layer"]
-    inp = synth.workload_inputs(s)
-    dY = synth.grad_output(s)
+    inp, dY, ref = full_refs.layer_backward()
     got = run_layer_backward(s, inp, dY)
-    W = [host64(inp[k]) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")]
-    ref = oracle.layer_backward_composed(s.batch, s.seq, s.heads, s.kv_heads, s.head_dim,
-                                         host64(inp["X"]), *W, host64(dY))
     for n, r in zip(NAMES, ref):
         g = host64(got[n])
         e = assert_close(g, r, what=f"full-size layer {n}")
         report(f"layer backward {n}", max_rel=e, frac_beyond=elementwise_excess_fraction(g, r))
+
+
+def test_full_size_sequence_parallel_layer_backward_full_output():
+    # The split layout only permutes token rows: the reference is the
+    # replicated layer's backward with dX split (oracle.layer_sp_backward's
+    # definition, on the cached full-size result).
+    s = SHAPES["layer"]
+    inp, dY, ref = full_refs.layer_backward()
+    X_sp, dY_sp = _split(inp["X"], s), _split(dY, s)
+    got = run_layer_backward(s, dict(inp, X=X_sp), dY_sp, plan=sp_plan(s))
+    ref = [oracle.sp_split(s.batch, s.seq, s.tp, ref[0])] + list(ref[1:])
+    for n, r in zip(NAMES, ref):
+        g = host64(got[n])
+        e = assert_close(g, r, what=f"full-size SP layer {n}")
+        report(f"sp layer backward {n}", max_rel=e, frac_beyond=elementwise_excess_fraction(g, r))

@@ -771,3 +771,44 @@ def test_composed_mlp_backward_equals_c_form():
     got = oracle.mlp_backward_composed(X, W1, W2, dZ, W3)
     for n, x, y in zip(("dX", "dW1", "dW3", "dW2", "db2"), want, got):
         assert np.abs(x - y).max() < 1e-12 * max(1.0, np.abs(x).max()), n
+
+
+def _torch_to_split(Y, batch, seq, t):
+    """Token-order [batch seq][h] -> sequence-split [t][batch][seq/t][h], by
+    its definition: shard i holds positions [i seq/t, (i+1) seq/t) of every
+    sequence ("시퀀스 병렬화")."""
+    h = Y.shape[1]
+    return Y.reshape(batch, t, seq // t, h).permute(1, 0, 2, 3).reshape(batch * seq, h)
+
+
+def _torch_from_split(Y_sp, batch, seq, t):
+    h = Y_sp.shape[1]
+    return Y_sp.reshape(t, batch, seq // t, h).permute(1, 0, 2, 3).reshape(batch * seq, h)
+
+
+def test_sequence_parallel_layer_backward_matches_torch_autograd():
+    # The split-layout layer: gather X_sp into token order, run the layer,
+    # split the output.  Autograd through that composition gives dX_sp and
+    # the weight gradients; the oracle's form must equal it, and its weight
+    # gradients must equal the replicated layer's.
+    g = torch.Generator().manual_seed(95)
+    batch, seq, t, h, a, k, d, f = 2, 8, 4, 8, 4, 2, 2, 16
+    M = batch * seq
+    X_sp = torch.randn(M, h, generator=g, dtype=torch.float64).requires_grad_(True)
+    shapes = [(a * d, h), (k * d, h), (k * d, h), (h, a * d), (f, h), (f, h), (h, f)]
+    W = [(torch.randn(*s, generator=g, dtype=torch.float64) * 0.4).requires_grad_(True) for s in shapes]
+    dY_sp = torch.randn(M, h, generator=g, dtype=torch.float64)
+    Y_sp = _torch_to_split(_torch_layer(batch, seq, a, k, _torch_from_split(X_sp, batch, seq, t), *W), batch, seq, t)
+    Y_sp.backward(dY_sp)
+    got = oracle.layer_sp_backward(batch, seq, a, k, d, t, X_sp.detach(), *(w.detach() for w in W), dY_sp)
+    want = [X_sp.grad] + [w.grad for w in W]
+    names = ["dX", "dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"]
+    for n, x, ref in zip(names, got, want):
+        assert np.abs(x - ref.numpy()).max() < 1e-11 * max(1.0, ref.abs().max().item()), n
+    # the split of a token-order tensor is the inverse of the all-gather
+    Z = torch.randn(M, h, generator=g, dtype=torch.float64)
+    assert np.array_equal(oracle.sp_split(batch, seq, t, Z), _torch_to_split(Z, batch, seq, t).numpy())
+    comp = oracle.layer_sp_backward(batch, seq, a, k, d, t, X_sp.detach(), *(w.detach() for w in W), dY_sp,
+                                    composed=True)
+    for n, x, y in zip(names, got, comp):
+        assert np.abs(x - y).max() < 1e-11 * max(1.0, np.abs(x).max()), n + " (composed)"
