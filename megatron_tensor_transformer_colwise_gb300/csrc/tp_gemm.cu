@@ -216,6 +216,9 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     const int rr = r - g * group_size;
     mb = first_m + rr % gm;
     nb = rr / gm;
+    // Odd groups sweep the n-tiles backwards: a group starts on the weight
+    // tiles the previous group ended on, which are still in L2.
+    if (g & 1) nb = p.n_tiles - 1 - nb;
 }
 
 // GEMM_MLP unit u of a cluster: colwise units first (all m-blocks of one
