@@ -12,31 +12,33 @@
 // a running maximum subtracted, no dropout, no rotary embedding.
 //
 // Work item: 128 query rows of one query head and sequence.  A persistent
-// grid of two CTAs per SM (7 warps, 256 TMEM columns and ~105 KB of shared
-// memory each) walks the items longest first, in rounds of alternating
-// direction (item_at), so one CTA's softmax overlaps the other's
-// tensor-core work and the next item's loads overlap the current item's
-// last blocks:
-//   warp 0      TMA: Q once, then K and V blocks of 64 keys (2-stage rings,
-//               K one block ahead) from the shard-blocked QKV buffer; an L2
-//               prefetch of the next item's Q.
-//   warp 1      TMEM owner and S issuer: S = Q K^T (128 x 64, fp32, two TMEM
-//               buffers so S of block j+1 is computed while the softmax works
-//               on block j).
+// grid of one CTA per SM (11 warps, all 512 TMEM columns, ~195 KB of shared
+// memory at d = 128) walks the items longest first, in rounds of
+// alternating direction (item_at), and the next item's loads overlap the
+// current item's last blocks:
+//   warp 0      TMA: Q, then K and V blocks of 128 keys (2-stage rings, K one
+//               block ahead) from the shard-blocked QKV buffer; the next
+//               item's Q and first K take the place of K(nkb), and an L2
+//               prefetch of the next item's Q goes out when an item starts.
+//   warp 1      TMEM owner and S issuer: S = Q K^T (128 x 128, fp32) into
+//               three TMEM buffers, so S of blocks j+1 and j+2 is computed
+//               while the softmax works on block j.
 //   warp 2      PV issuer: O += P V with P read from TMEM (tcgen05.mma with
 //               the A operand in tensor memory) and V used as an MN-major
 //               operand straight from its [key][d] layout.
-//               A thread issues one tcgen05.mma about every 100 cycles
-//               whatever its size (measured on GB300), while an S or PV step
-//               here is 30 to 60 cycles of math, so the two products have
-//               an issuing thread each.
-//   warps 3..6  one query row per thread (TMEM lane = row): read the S row,
-//               apply the causal mask, online softmax with exp2, write P as
-//               bf16 over the first half of the same S buffer (tcgen05.st),
-//               rescale the O row in TMEM when its reference maximum moves,
-//               and finally write O / l as bf16 through a per-warp shared-
-//               memory box and a TMA store.
-// A buffer is reused for S of block j+2 once the PV of block j, which reads
+//               One thread issues a 128 x 128 x 16 step about every 70
+//               cycles, about its math time, so the two products have an
+//               issuing thread each and run side by side.
+//   warps 3..10 two warps per TMEM lane quadrant, one query row per thread
+//               (TMEM lane = row), each warp half of a block's keys: read
+//               the S half-row, apply the causal mask, agree on the row
+//               maximum with the other half through shared memory, online
+//               softmax with exp2, write P as bf16 over the first half of
+//               the same S buffer (tcgen05.st), rescale its half of the O
+//               row in TMEM when the row's reference maximum moves.  After
+//               the next item's first block they write O / l as bf16
+//               through per-warp shared-memory boxes and TMA stores.
+// A buffer is reused for S of block j+3 once the PV of block j, which reads
 // its P, has completed; the softmax warps wait for the previous PV to
 // complete only when they rescale O in place.
 // The reference maximum of a row only moves when the block maximum exceeds
@@ -59,11 +61,9 @@ namespace {
 using namespace tpk;
 
 constexpr int QB = 128;  // query rows per CTA (UMMA M, TMEM lanes)
-constexpr int KB = 64;   // keys per block (UMMA N of S, UMMA K of PV)
-constexpr int NTHREADS = 224;
 constexpr int QBOX = QB * 128;  // TMA box of Q: 128 rows x 64 bf16 (16 KB)
-constexpr int KBOX = KB * 128;  // TMA box of K or V: 64 rows x 64 bf16 (8 KB)
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 of the allowed growth of P
+constexpr int MAX_NS = 3;  // S buffers in TMEM, at most
 
 enum {
     B_Q_FULL = 0,
@@ -71,39 +71,59 @@ enum {
     B_K_EMPTY = 3,   // x2
     B_V_FULL = 5,    // x2 (V ring)
     B_V_EMPTY = 7,   // x2
-    B_S_FULL = 9,    // x2 (S / P buffers in TMEM)
-    B_PV_DONE = 11,  // x2: the PV MMA that read P from buffer i has completed
-    B_P_FULL = 13,   // x2 (per S buffer): its 4 softmax warps wrote P
-    B_O_FULL = 15,
-    B_DRAIN = 16,    // x2: one per issuing thread
-    B_Q_EMPTY = 18,  // the item's S products are done with Q
-    B_O_EMPTY = 19,  // the item's epilogue has read O (4 softmax warps)
-    NUM_BARS = 20
+    B_S_FULL = 9,    // x NS (S / P buffers in TMEM)
+    B_PV_DONE = B_S_FULL + MAX_NS,   // x NS: the PV MMA that read P from buffer i has completed
+    B_P_FULL = B_PV_DONE + MAX_NS,   // x NS (per S buffer): its softmax warps wrote P
+    B_O_FULL = B_P_FULL + MAX_NS,
+    B_DRAIN = B_O_FULL + 1,          // x2: one per issuing thread
+    B_Q_EMPTY = B_DRAIN + 2,         // the item's S products are done with Q
+    B_O_EMPTY = B_Q_EMPTY + 1,       // the item's epilogue has read O (all softmax warps)
+    NUM_BARS = B_O_EMPTY + 1
 };
 
 // Per-CTA dynamic shared memory when two CTAs share an SM: (228 KB - 2 x
 // 1 KB reserved) / 2.
 constexpr int TWO_CTA_SMEM = 115712;
 
-// Shared memory of one CTA (two CTAs share an SM):
-//   Q [128][d] | K ring 2 x [64][d] | V ring 2 x [64][d] | O staging | barriers
+// Shared memory of one CTA:
+//   Q [128][d] | K ring 2 x [KB][d] | V ring 2 x [KB][d] | O staging |
+//   row-max / row-sum exchange | barriers
 // (P lives in TMEM, over the first half of its S buffer).  The kernel checks
 // at run time that its 1024-aligned layout fits the allocation and
 // otherwise stops with an error flag, touching nothing.
 constexpr int STG_BOX = 32 * 64;  // 32 rows x 32 bf16 (64-byte swizzle)
 
-template <int D>
+// The kernel's configuration: head dimension D, keys per block KB (UMMA N of
+// S, UMMA K of PV), S buffers in TMEM NS (S of later blocks is computed while
+// the softmax and the PV products of earlier ones run) and CTAs per SM.
+template <int D_, int KB_, int NS_, int CTAS_, int SPLIT_>
 struct Layout {
+    static constexpr int D = D_, KB = KB_, NS = NS_, CTAS = CTAS_;
+    // Softmax warps per TMEM lane quadrant (each takes KB / SPLIT keys of a block).
+    static constexpr int SPLIT = SPLIT_;
+    // Warp 0 TMA, warp 1 S issuer, warp 2 PV issuer, then 4 * SPLIT softmax warps.
+    static constexpr int NTHREADS = 96 + 128 * SPLIT;
+    static constexpr int KBOX = KB * 128;  // TMA box of K or V: KB rows x 64 bf16
     static constexpr int QT = QB * D * 2;
     static constexpr int KT = KB * D * 2;
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = QT;
     static constexpr int V_OFF = K_OFF + 2 * KT;
-    static constexpr int STG_OFF = V_OFF + 2 * KT;  // O staging: one 32 x 32 bf16 box per softmax warp
-    static constexpr int BAR_OFF = STG_OFF + 4 * STG_BOX;
+    // O staging: one 32 x 32 bf16 box per softmax warp and 32 columns of O,
+    // so an item's stores never wait for each other.
+    static constexpr int STG_OFF = V_OFF + 2 * KT;
+    // Row maxima of the two block parities and row sums exchanged between
+    // the softmax warps of a quadrant: [3][SPLIT][128] fp32.
+    static constexpr int XCH_OFF = STG_OFF + 4 * (D / 32) * STG_BOX;
+    static constexpr int BAR_OFF = XCH_OFF + 3 * SPLIT * QB * 4;
     static constexpr int DATA = BAR_OFF + 8 * NUM_BARS + 16;
-    static constexpr int SMEM = DATA + 1024 <= TWO_CTA_SMEM ? DATA + 1024 : TWO_CTA_SMEM;
-    static constexpr int TMEM_COLS = 2 * KB + D <= 256 ? 256 : 512;  // S0 | S1 | O
+    static constexpr int SMEM_CAP = CTAS == 2 ? TWO_CTA_SMEM : 232448;
+    static constexpr int SMEM = DATA + 1024 <= SMEM_CAP ? DATA + 1024 : SMEM_CAP;
+    static constexpr int O_COL = NS * KB;  // TMEM: S_0 | ... | S_(NS-1) | O
+    static constexpr int TMEM_COLS = O_COL + D <= 256 ? 256 : 512;
+    static_assert(NS >= 2 && NS <= MAX_NS && O_COL + D <= 512 && KB % 32 == 0, "configuration");
+    static_assert((SPLIT == 1 || SPLIT == 2) && (KB / SPLIT) % 32 == 0 && (D / SPLIT) % 32 == 0, "split");
+    static_assert(CTAS == 1 || TMEM_COLS <= 256, "two CTAs per SM share its 512 TMEM columns");
 };
 
 struct AttnParams {
@@ -138,7 +158,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-
 // Tiled TMA store of a 3-D box (elements outside the map are not written).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
                                              int32_t c2) {
@@ -164,8 +183,9 @@ struct Item {
     int qcol, kcol, vcol;
 };
 
-template <int D>
+template <class L>
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
+    constexpr int D = L::D, KB = L::KB;
     const int nqb = (p.seq + QB - 1) / QB;
     const int hb = p.heads * p.batch;
     const int qi = w / hb;
@@ -200,9 +220,9 @@ __device__ __forceinline__ int item_at(int k, int c, int g) { return k * g + ((k
 // role walks the same item list; K/V ring stages, S buffers and their barrier phases run on
 // one block count across items, so the next item's Q and first K/V blocks
 // load while the current item finishes.
-template <int D>
-__global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_constant__ AttnParams p) {
-    using L = Layout<D>;
+template <class L>
+__global__ void __launch_bounds__(L::NTHREADS, L::CTAS) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+    constexpr int D = L::D, KB = L::KB, NS = L::NS, KBOX = L::KBOX;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -227,17 +247,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
             mbar_init(bar(B_K_EMPTY + s), 1);
-            mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_PV_DONE + s), 1);
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         // One P_FULL per S buffer: a warp a block ahead of the others
-        // arrives on the other barrier, never on the phase they complete.
-        mbar_init(bar(B_P_FULL), 4);
-        mbar_init(bar(B_P_FULL + 1), 4);
+        // arrives on another barrier, never on the phase they complete.
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(B_S_FULL + s), 1);
+            mbar_init(bar(B_PV_DONE + s), 1);
+            mbar_init(bar(B_P_FULL + s), 4 * L::SPLIT);
+        }
         mbar_init(bar(B_O_FULL), 1);
-        mbar_init(bar(B_O_EMPTY), 4);
+        mbar_init(bar(B_O_EMPTY), 4 * L::SPLIT);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_DRAIN + 1), 1);
         *abort_flag = 0;
@@ -270,8 +291,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             bool ok = true, q_issued = false;
             uint32_t kissued = 0, kpar = 0, vissued = 0, vpar = 0, qpar = 0;
             int gb = 0;  // blocks of earlier items
-            auto load_kv = [&](const Item& x, int kb, bool is_v) -> bool {
-                const int n = gb + kb;  // ring position
+            // K or V block kb of item x, whose first block has ring position g0.
+            auto load_kv = [&](const Item& x, int g0, int kb, bool is_v) -> bool {
+                const int n = g0 + kb;  // ring position
                 const int st = n & 1;
                 const uint32_t ph = static_cast<uint32_t>(n >> 1) & 1u;
                 const int e = is_v ? B_V_EMPTY : B_K_EMPTY, f = is_v ? B_V_FULL : B_K_FULL;
@@ -291,33 +313,51 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                 }
                 return true;
             };
-            int li = 0;
-            for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
-                const Item x = item_of<D>(p, w);
-                // The next item's Q is read from HBM for the first time: start
-                // that read now, so its TMA load later hits L2.
-                if (item_at(li + 1, w0, dw) < n_items) {
-                    const Item y = item_of<D>(p, item_at(li + 1, w0, dw));
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(&p.map_q, y.qcol + 64 * c, y.tok0 + y.q0);
-                }
+            // Q of item number li (once the previous item's S products are done with Q).
+            auto load_q = [&](const Item& x, int li) -> bool {
                 if (li > 0 && !mbar_wait(bar(B_Q_EMPTY), static_cast<uint32_t>(li - 1) & 1u, abort_flag, p.status,
-                                         p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+                                         p.timeout_ns))
+                    return false;
                 mbar_arrive_expect_tx(bar(B_Q_FULL), L::QT);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_2d(sQ + c * QBOX, &p.map_q, bar(B_Q_FULL), x.qcol + 64 * c, x.tok0 + x.q0);
                 q_issued = true;
                 qpar = static_cast<uint32_t>(li) & 1u;
-                ok = load_kv(x, 0, false);
+                return true;
+            };
+            // Per item: for each block kb, K(kb + 1) then V(kb).  In place of
+            // K(nkb) come the next item's Q and K(0), so they load while
+            // the item's last blocks are still in flight rather than after
+            // its last V.
+            int li = 0;
+            bool have = item_at(0, w0, dw) < n_items;
+            Item x{};
+            if (have) {
+                x = item_of<L>(p, item_at(0, w0, dw));
+                ok = load_q(x, 0) && load_kv(x, 0, 0, false);
+            }
+            for (; ok && have; ++li) {
+                const int wn = item_at(li + 1, w0, dw);
+                const bool has_next = wn < n_items;
+                Item y{};
+                if (has_next) {
+                    y = item_of<L>(p, wn);
+                    // The next item's Q is read from HBM for the first time:
+                    // start that read now, so its TMA load later hits L2.
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(&p.map_q, y.qcol + 64 * c, y.tok0 + y.q0);
+                }
                 for (int kb = 0; kb < x.nkb && ok; ++kb) {
-                    if (kb + 1 < x.nkb && !(ok = load_kv(x, kb + 1, false))) break;
-                    ok = load_kv(x, kb, true);
+                    if (kb + 1 < x.nkb)
+                        ok = load_kv(x, gb, kb + 1, false);
+                    else if (has_next)
+                        ok = load_q(y, li + 1) && load_kv(y, gb + x.nkb, 0, false);
+                    if (ok) ok = load_kv(x, gb, kb, true);
                 }
                 gb += x.nkb;
+                x = y;
+                have = has_next;
             }
             if (!ok) {
                 if (q_issued) drain_wait(bar(B_Q_FULL), qpar);
@@ -338,17 +378,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             bool ok = true;
             int gb = 0, li = 0;
             for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
-                const int nkb = item_of<D>(p, w).nkb;
+                const int nkb = item_of<L>(p, w).nkb;
                 if (!mbar_wait(bar(B_Q_FULL), static_cast<uint32_t>(li) & 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 for (int kb = 0; kb < nkb && ok; ++kb, ++gb) {
-                    const int st = gb & 1;
-                    // Buffer st held S and then P of block gb - 2: its PV must
+                    const int st = gb & 1;       // K ring stage
+                    const int sb = gb % NS;      // S buffer
+                    // Buffer sb held S and then P of block gb - NS: its PV must
                     // have read that P before this S overwrites it.
-                    if (gb >= 2 && !mbar_wait(bar(B_PV_DONE + st), static_cast<uint32_t>((gb - 2) >> 1) & 1u,
-                                              abort_flag, p.status, p.timeout_ns)) {
+                    if (gb >= NS && !mbar_wait(bar(B_PV_DONE + sb), static_cast<uint32_t>((gb - NS) / NS) & 1u,
+                                               abort_flag, p.status, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -358,7 +399,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + st * KB;
+                    const uint32_t d_tmem = tmem + sb * KB;
                     const uint64_t kdesc = st ? kdesc1 : kdesc0;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
@@ -368,7 +409,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                         umma_bf16(d_tmem, qdesc + a_off, kdesc + b_off, idesc_s, ks > 0 ? 1u : 0u);
                     }
                     umma_commit(bar(B_K_EMPTY + st));
-                    umma_commit(bar(B_S_FULL + st));
+                    umma_commit(bar(B_S_FULL + sb));
                 }
                 // Q may be reloaded once this item's S products are done.
                 if (ok) umma_commit(bar(B_Q_EMPTY));
@@ -386,10 +427,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             bool ok = true;
             int gb = 0, li = 0;
             for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
-                const int nkb = item_of<D>(p, w).nkb;
+                const int nkb = item_of<L>(p, w).nkb;
                 for (int kb = 0; kb < nkb && ok; ++kb, ++gb) {
-                    const int vst = gb & 1;
-                    if (!mbar_wait(bar(B_P_FULL + vst), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag, p.status,
+                    const int vst = gb & 1;   // V ring stage
+                    const int pb = gb % NS;   // P buffer (the block's S buffer)
+                    if (!mbar_wait(bar(B_P_FULL + pb), static_cast<uint32_t>(gb / NS) & 1u, abort_flag, p.status,
                                    p.timeout_ns) ||
                         !mbar_wait(bar(B_V_FULL + vst), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag, p.status,
                                    p.timeout_ns)) {
@@ -405,17 +447,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    // P of block gb: bf16 in the first KB/2 columns of S buffer
-                    // gb & 1, 16 keys (8 columns) per UMMA.
+                    // P of block gb: bf16 in the first KB/2 columns of its S
+                    // buffer, 16 keys (8 columns) per UMMA.
                     const uint64_t vdesc = vst ? vdesc1 : vdesc0;
-                    const uint32_t pcol = tmem + vst * KB;
+                    const uint32_t pcol = tmem + pb * KB;
                     const uint32_t acc0 = kb > 0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < KB / 16; ++ks)
-                        umma_bf16_ts(tmem + 2 * KB, pcol + ks * 8, vdesc + (ks * 16 * 128) / 16, idesc_o,
+                        umma_bf16_ts(tmem + L::O_COL, pcol + ks * 8, vdesc + (ks * 16 * 128) / 16, idesc_o,
                                      ks > 0 ? 1u : acc0);
                     umma_commit(bar(B_V_EMPTY + vst));
-                    umma_commit(bar(B_PV_DONE + vst));
+                    umma_commit(bar(B_PV_DONE + pb));
                 }
                 if (ok) umma_commit(bar(B_O_FULL));
             }
@@ -426,144 +468,72 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
         }
     } else {
         // ---------------------------------------------------------- softmax / epilogue
+        // SPLIT warps share each TMEM lane quadrant: warp half hf takes key
+        // columns [hf * KC, (hf + 1) * KC) of every block and O columns
+        // [hf * D / SPLIT, (hf + 1) * D / SPLIT).  The two halves of a row
+        // agree on its running maximum through one shared-memory exchange
+        // per block, so both apply the same scale; each keeps its part of
+        // the row sum until the epilogue adds them in a fixed order.
+        constexpr int SPLIT = L::SPLIT, KC = KB / SPLIT, DC = D / SPLIT;
         const int q = warp & 3;  // TMEM lane quadrant
+        const int hf = (warp - 3) >> 2;
         const int r = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        bool ok = true;
-        int gb = 0, li = 0;
-        for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
-            const Item x = item_of<D>(p, w);
-            const int q0 = x.q0;
-            const int qpos = q0 + r;
-            float m_ref = -INFINITY, l_sum = 0.0f;
-            for (int kb = 0; kb < x.nkb; ++kb, ++gb) {
-                const int st = gb & 1;
-                const bool got = mbar_wait(bar(B_S_FULL + st), static_cast<uint32_t>(gb >> 1) & 1u, abort_flag,
-                                           p.status, p.timeout_ns);
+        float* xch = reinterpret_cast<float*>(gbase + L::XCH_OFF);  // [2 parities][SPLIT][128]
+        // Every failure passes through one of these before the warps act on
+        // it, so the two halves of a quadrant always leave together and no
+        // named barrier waits for a warp that has gone.
+        auto pair_all = [&](bool v) -> bool {
+            if constexpr (SPLIT == 1) {
                 __syncwarp();
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint32_t s[KB];
-#pragma unroll
-                for (int c = 0; c < KB / 32; ++c)
-                    tmem_ld32(tmem + lane_off + st * KB + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-                tmem_ld_wait();
-
-                // Keys k0 + c with c > lim are masked: later than the query
-                // (causal) or past the sequence end.
-                const int k0 = kb * KB;
-                const int lim = min(qpos, p.seq - 1) - k0;
-                if (lim < KB - 1) {
-#pragma unroll
-                    for (int c = 0; c < KB; ++c)
-                        if (c > lim) s[c] = __float_as_uint(-INFINITY);
-                }
-                // Row max with 8 independent chains of three-way maxima (one
-                // softmax warp per SM sub-partition and CTA leaves little to
-                // hide a serial chain).
-                float mx8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[8 + e]));
-#pragma unroll
-                for (int c = 16; c < KB; c += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        mx8[e] = max3(mx8[e], __uint_as_float(s[c + e]), __uint_as_float(s[c + 8 + e]));
-                const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
-                                      fmaxf(mx8[6], mx8[7]));
-                const float mxs = mx * p.scale_log2;
-                float alpha = 1.0f;
-                bool rescale = false;
-                if (mxs > m_ref + RESCALE_THRESHOLD) {
-                    alpha = exp2f(m_ref - mxs);  // 0 on the first block
-                    m_ref = mxs;
-                    rescale = kb > 0;
-                }
-                const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
-                const uint64_t neg2 = f2_pack(-m_ref, -m_ref);
-                uint64_t acc[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = f2_pack(0.0f, 0.0f);
-                uint32_t pk[KB / 2];
-#pragma unroll
-                for (int c = 0; c < KB / 2; ++c) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, neg2),
-                              x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
-                    pk[c] = pack_bf16x2(p0, p1);
-                }
-                float sum8[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) f2_unpack(acc[e], sum8[2 * e], sum8[2 * e + 1]);
-                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-                l_sum = l_sum * alpha + sum;
-
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O is rescaled in place: the PV of the previous block must be done.
-                    const int pb = gb - 1;
-                    const bool got2 = mbar_wait(bar(B_PV_DONE + (pb & 1)), static_cast<uint32_t>(pb >> 1) & 1u,
-                                                abort_flag, p.status, p.timeout_ns);
-                    __syncwarp();
-                    if (!__all_sync(0xffffffffu, got2)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        const uint32_t ta = tmem + lane_off + 2 * KB + c * 32;
-                        tmem_ld32(ta, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(ta, o);
-                    }
-                    tmem_st_wait();
-                }
-                // P row r over its S row in TMEM: 64 keys as 32 packed columns.
-                tmem_st32(tmem + lane_off + st * KB, pk);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL + st));
+                return __all_sync(0xffffffffu, v);
+            } else {
+                return named_bar_and(1u + static_cast<uint32_t>(q), 64u, v);
             }
-            if (!ok) break;
-            const bool got = mbar_wait(bar(B_O_FULL), static_cast<uint32_t>(li) & 1u, abort_flag, p.status,
-                                       p.timeout_ns);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
+        };
+        // The epilogue of an item (O / l out of TMEM, through shared memory,
+        // to global memory by TMA stores) runs after the next item's first
+        // block, so the wait for the item's last PV and the stores overlap
+        // that block's tensor-core work.  Returns false, in both halves of
+        // the quadrant, when a wait gave up.
+        auto epilogue = [&](int eq0, int ej, int eb, int eli, float m_e, float l_e, bool bad_e) -> bool {
+            bool got = !bad_e && mbar_wait(bar(B_O_FULL), static_cast<uint32_t>(eli) & 1u, abort_flag, p.status,
+                                           p.timeout_ns);
+            got = __all_sync(0xffffffffu, got);
+            if constexpr (SPLIT > 1) xch[2 * SPLIT * QB + hf * QB + r] = l_e;
+            if (!pair_all(got)) return false;
             tc_fence_after();
-            const float inv = 1.0f / l_sum;
-            if (p.lse && qpos < p.seq)
-                p.lse[(static_cast<long long>(x.j) * p.batch + x.b) * p.seq_pad + qpos] = m_ref + log2f(l_sum);
-            __nv_bfloat16* orow = p.o + static_cast<long long>(x.tok0 + qpos) * p.ld_o +
-                                  static_cast<long long>(x.j) * D;
+            const int qpos = eq0 + r;
+            float l_tot = l_e;
+            if constexpr (SPLIT > 1) {
+                // Fixed order, the same in both halves.
+                l_tot = 0.0f;
+#pragma unroll
+                for (int h2 = 0; h2 < SPLIT; ++h2) l_tot += xch[2 * SPLIT * QB + h2 * QB + r];
+            }
+            const float inv = 1.0f / l_tot;
+            if (hf == 0 && p.lse && qpos < p.seq)
+                p.lse[(static_cast<long long>(ej) * p.batch + eb) * p.seq_pad + qpos] = m_e + log2f(l_tot);
             // O / l as bf16, 32 columns at a time.  With a TMA map the warp
-            // writes its 32 rows into its shared-memory box (16-byte piece u
-            // of row l at l * 64 + (u ^ ((l / 2) % 4)) * 16) and lane 0
-            // stores the box; otherwise each thread stores its row.
-            const int row0 = q0 + q * 32;
-            const uint32_t box = base + L::STG_OFF + static_cast<uint32_t>(q) * STG_BOX;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            // writes its 32 rows into one shared-memory box per 32 columns
+            // (16-byte piece u of row l at l * 64 + (u ^ ((l / 2) % 4)) * 16)
+            // and lane 0 stores the boxes; otherwise each thread stores its
+            // row.
+            if (p.o_tma) {
+                if (lane == 0) bulk_wait_group_read0();  // the previous item's stores have read the boxes
+                __syncwarp();
+            }
+            const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+            const uint32_t box0 = base + L::STG_OFF + static_cast<uint32_t>(q * (D / 32) + hf * (DC / 32)) * STG_BOX;
+            __nv_bfloat16* orow = p.o + (static_cast<long long>(eb) * p.seq + qpos) * p.ld_o +
+                                  static_cast<long long>(ej) * D + hf * DC;
+#pragma unroll
+            for (int c = 0; c < DC / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + 2 * KB + c * 32, o);
+                tmem_ld32(tmem + lane_off + L::O_COL + hf * DC + c * 32, o);
                 tmem_ld_wait();
                 if (p.o_tma) {
-                    if (lane == 0) bulk_wait_group_read0();  // the box's previous store has read it
-                    __syncwarp();
-                    const uint32_t srow = box + static_cast<uint32_t>(lane) * 64u;
-                    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+                    const uint32_t srow = box0 + static_cast<uint32_t>(c) * STG_BOX + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         uint32_t wv[4];
@@ -572,12 +542,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
                             wv[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv,
                                                 __uint_as_float(o[u * 8 + 2 * e + 1]) * inv);
                         st_shared_v4(srow + ((static_cast<uint32_t>(u) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
-                    }
-                    fence_proxy_async_smem();  // visible to the TMA engine
-                    __syncwarp();
-                    if (lane == 0 && row0 < p.seq) {
-                        tma_store_3d(&p.map_o, box, x.j * D + c * 32, row0, x.b);
-                        bulk_commit_group();
                     }
                 } else if (qpos < p.seq) {
 #pragma unroll
@@ -596,7 +560,161 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_tc_kernel(const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
+            if (p.o_tma) {
+                fence_proxy_async_smem();  // the boxes are visible to the TMA engine
+                __syncwarp();
+                const int row0 = eq0 + q * 32;
+                if (lane == 0 && row0 < p.seq) {
+#pragma unroll
+                    for (int c = 0; c < DC / 32; ++c)
+                        tma_store_3d(&p.map_o, box0 + static_cast<uint32_t>(c) * STG_BOX, ej * D + hf * DC + c * 32,
+                                     row0, eb);
+                    bulk_commit_group();
+                }
+            }
+            return true;
+        };
+        bool ok = true;
+        bool pending = false;  // an item whose epilogue has not run yet
+        int pq0 = 0, pj = 0, pb_ = 0, pli = 0;
+        float pm = 0.0f, pl = 0.0f;
+        bool pbad = false;
+        int gb = 0, li = 0;
+        for (int w; ok && (w = item_at(li, w0, dw)) < n_items; ++li) {
+            const Item x = item_of<L>(p, w);
+            const int q0 = x.q0;
+            const int qpos = q0 + r;
+            float m_ref = -INFINITY, l_sum = 0.0f;
+            bool bad = false;  // a wait after this block's exchange gave up
+            for (int kb = 0; kb < x.nkb; ++kb, ++gb) {
+                const int st = gb % NS;  // S buffer
+                bool got = !bad && mbar_wait(bar(B_S_FULL + st), static_cast<uint32_t>(gb / NS) & 1u, abort_flag,
+                                             p.status, p.timeout_ns);
+                got = __all_sync(0xffffffffu, got);
+                uint32_t s[KC];
+                float mxp = -INFINITY;
+                if (got) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < KC / 32; ++c)
+                        tmem_ld32(tmem + lane_off + st * KB + hf * KC + c * 32,
+                                  *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+                    tmem_ld_wait();
+                    // Keys k0 + c with c > lim are masked: later than the
+                    // query (causal) or past the sequence end.
+                    const int k0 = kb * KB + hf * KC;
+                    const int lim = min(qpos, p.seq - 1) - k0;
+                    if (lim < KC - 1) {
+#pragma unroll
+                        for (int c = 0; c < KC; ++c)
+                            if (c > lim) s[c] = __float_as_uint(-INFINITY);
+                    }
+                    // Row max with 8 independent chains of three-way maxima.
+                    float mx8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[8 + e]));
+#pragma unroll
+                    for (int c = 16; c < KC; c += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            mx8[e] = max3(mx8[e], __uint_as_float(s[c + e]), __uint_as_float(s[c + 8 + e]));
+                    mxp = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                    if constexpr (SPLIT > 1) xch[((gb & 1) * SPLIT + hf) * QB + r] = mxp;
+                    tc_fence_before();
+                }
+                // The other half's S columns are in its registers once this
+                // returns, so P may be written over them.
+                if (!pair_all(got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float mx = mxp;
+                if constexpr (SPLIT > 1) mx = fmaxf(mxp, xch[((gb & 1) * SPLIT + (hf ^ 1)) * QB + r]);
+                const float mxs = mx * p.scale_log2;
+                float alpha = 1.0f;
+                bool rescale = false;
+                if (mxs > m_ref + RESCALE_THRESHOLD) {
+                    alpha = exp2f(m_ref - mxs);  // 0 on the first block
+                    m_ref = mxs;
+                    rescale = kb > 0;
+                }
+                const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t neg2 = f2_pack(-m_ref, -m_ref);
+                uint64_t acc[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = f2_pack(0.0f, 0.0f);
+                uint32_t pk[KC / 2];
+#pragma unroll
+                for (int c = 0; c < KC / 2; ++c) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, neg2),
+                              x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                float sum8[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(acc[e], sum8[2 * e], sum8[2 * e + 1]);
+                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                l_sum = l_sum * alpha + sum;
+
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O is rescaled in place: the PV of the previous block must be done.
+                    const int pb = gb - 1;
+                    const bool got2 = mbar_wait(bar(B_PV_DONE + pb % NS), static_cast<uint32_t>(pb / NS) & 1u,
+                                                abort_flag, p.status, p.timeout_ns);
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, got2)) {
+                        bad = true;  // acted on at the next pair_all, with the other half
+                    } else {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < DC / 32; ++c) {
+                            uint32_t o[32];
+                            const uint32_t ta = tmem + lane_off + L::O_COL + hf * DC + c * 32;
+                            tmem_ld32(ta, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(ta, o);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                // P row r over its S row in TMEM: KC keys as KC / 2 packed columns.
+#pragma unroll
+                for (int c = 0; c < KC / 64; ++c)
+                    tmem_st32(tmem + lane_off + st * KB + hf * (KC / 2) + c * 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+                if constexpr (KC % 64 == 32)
+                    tmem_st16(tmem + lane_off + st * KB + hf * (KC / 2) + (KC / 64) * 32,
+                              *reinterpret_cast<const uint32_t(*)[16]>(&pk[(KC / 64) * 32]));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + st));
+                if (kb == 0 && pending) {
+                    if (!epilogue(pq0, pj, pb_, pli, pm, pl, pbad)) {
+                        ok = false;
+                        break;
+                    }
+                    pending = false;
+                }
+            }
+            if (!ok) break;
+            pending = true;
+            pq0 = x.q0;
+            pj = x.j;
+            pb_ = x.b;
+            pli = li;
+            pm = m_ref;
+            pl = l_sum;
+            pbad = bad;
         }
+        if (ok && pending) epilogue(pq0, pj, pb_, pli, pm, pl, pbad);
         // The O stores must have completed before the CTA exits.
         if (lane == 0) bulk_wait_group0();
     }
@@ -612,8 +730,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int D>
+template <class L>
 int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
+    constexpr int D = L::D, KB = L::KB;
     AttnParams p;
     memset(&p, 0, sizeof(p));
     void* fn_ptr = nullptr;
@@ -674,24 +793,24 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     p.batch = a.batch;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
-    const int smem = Layout<D>::SMEM;
+    const int smem = L::SMEM;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             if (err) *err = std::string("cudaFuncSetAttribute(attn): ") + cudaGetErrorString(e);
             return TP_ERR_CUDA;
         }
         configured[dev] = true;
     }
-    // Persistent grid: two CTAs per SM, or fewer when there are fewer items.
+    // Persistent grid: L::CTAS CTAs per SM, or fewer when there are fewer items.
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
     const long long n_items = static_cast<long long>((a.seq + QB - 1) / QB) * a.heads * a.batch;
-    dim3 grid(static_cast<unsigned>(std::min<long long>(n_items, 2LL * sms)), 1, 1);
-    cudaError_t e = tpi::launch_pdl(attn_tc_kernel<D>, grid, dim3(NTHREADS), smem, stream, p);
+    dim3 grid(static_cast<unsigned>(std::min<long long>(n_items, static_cast<long long>(L::CTAS) * sms)), 1, 1);
+    cudaError_t e = tpi::launch_pdl(attn_tc_kernel<L>, grid, dim3(L::NTHREADS), smem, stream, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         if (err) *err = std::string("attention launch: ") + cudaGetErrorString(e);
@@ -706,8 +825,8 @@ namespace tpi {
 
 int attn_launch(const AttnArgs& a, cudaStream_t stream, std::string* err) {
     if (a.batch == 0 || a.seq == 0) return TP_OK;
-    if (a.head_dim == 128) return launch_d<128>(a, stream, err);
-    if (a.head_dim == 64) return launch_d<64>(a, stream, err);
+    if (a.head_dim == 128) return launch_d<Layout<128, 128, 3, 1, 2>>(a, stream, err);
+    if (a.head_dim == 64) return launch_d<Layout<64, 128, 3, 1, 2>>(a, stream, err);
     if (err) *err = "head_dim must be 64 or 128";
     return TP_ERR_UNSUPPORTED;
 }
