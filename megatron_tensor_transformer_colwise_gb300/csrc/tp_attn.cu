@@ -527,11 +527,18 @@ __global__ void __launch_bounds__(L::NTHREADS, L::CTAS) attn_tc_kernel(const __g
             const uint32_t box0 = base + L::STG_OFF + static_cast<uint32_t>(q * (D / 32) + hf * (DC / 32)) * STG_BOX;
             __nv_bfloat16* orow = p.o + (static_cast<long long>(eb) * p.seq + qpos) * p.ld_o +
                                   static_cast<long long>(ej) * D + hf * DC;
+            // This half's O columns, all loads in flight at once; O is
+            // released to the next item's first PV as soon as they land.
+            uint32_t o[DC];
+#pragma unroll
+            for (int c = 0; c < DC / 32; ++c)
+                tmem_ld32(tmem + lane_off + L::O_COL + hf * DC + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
 #pragma unroll
             for (int c = 0; c < DC / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + L::O_COL + hf * DC + c * 32, o);
-                tmem_ld_wait();
                 if (p.o_tma) {
                     const uint32_t srow = box0 + static_cast<uint32_t>(c) * STG_BOX + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
@@ -539,8 +546,8 @@ __global__ void __launch_bounds__(L::NTHREADS, L::CTAS) attn_tc_kernel(const __g
                         uint32_t wv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16x2(__uint_as_float(o[u * 8 + 2 * e]) * inv,
-                                                __uint_as_float(o[u * 8 + 2 * e + 1]) * inv);
+                            wv[e] = pack_bf16x2(__uint_as_float(o[c * 32 + u * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[c * 32 + u * 8 + 2 * e + 1]) * inv);
                         st_shared_v4(srow + ((static_cast<uint32_t>(u) ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
                     }
                 } else if (qpos < p.seq) {
@@ -549,17 +556,12 @@ __global__ void __launch_bounds__(L::NTHREADS, L::CTAS) attn_tc_kernel(const __g
                         uint32_t wv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * inv,
-                                                __uint_as_float(o[g8 * 8 + 2 * e + 1]) * inv);
+                            wv[e] = pack_bf16x2(__uint_as_float(o[c * 32 + g8 * 8 + 2 * e]) * inv,
+                                                __uint_as_float(o[c * 32 + g8 * 8 + 2 * e + 1]) * inv);
                         *reinterpret_cast<uint4*>(orow + c * 32 + g8 * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
             }
-            // O has been read from TMEM: the next item's first PV may
-            // overwrite it.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_O_EMPTY));
             if (p.o_tma) {
                 fence_proxy_async_smem();  // the boxes are visible to the TMA engine
                 __syncwarp();
