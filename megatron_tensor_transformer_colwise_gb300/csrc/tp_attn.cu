@@ -126,6 +126,26 @@ struct Layout {
     static_assert(CTAS == 1 || TMEM_COLS <= 256, "two CTAs per SM share its 512 TMEM columns");
 };
 
+// Division by a run-time constant d with a multiply and a shift
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up method): with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (umulhi(n, m) + n) >> s for
+// every n < 2^31.  Item decoding runs at each item start on the softmax
+// warps' critical path, where a hardware-less integer division costs tens of
+// instructions.
+struct FastDiv {
+    uint32_t m, s;
+};
+FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{0, 0};
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.s) - d)) / d + 1);
+    return f;
+}
+__device__ __forceinline__ int fdiv(int n, FastDiv f) {
+    return static_cast<int>((__umulhi(static_cast<uint32_t>(n), f.m) + static_cast<uint32_t>(n)) >> f.s);
+}
+
 struct AttnParams {
     CUtensorMap map_q;   // the QKV buffer: dims {t * W, tokens}, box {64, 128}
     CUtensorMap map_kv;  // the same buffer, box {64, 64}
@@ -141,6 +161,11 @@ struct AttnParams {
     int batch;
     unsigned* status;
     unsigned long long timeout_ns;
+    // Item decoding: divisors heads * batch, heads, heads per shard, query
+    // heads per KV head and t; query tiles per sequence, key blocks per
+    // sequence and KV heads per shard (when there are at least t).
+    FastDiv f_hb, f_heads, f_hps, f_grp, f_t;
+    int nqb, nkb_seq, kv_per_shard;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -186,25 +211,23 @@ struct Item {
 template <class L>
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
     constexpr int D = L::D, KB = L::KB;
-    const int nqb = (p.seq + QB - 1) / QB;
-    const int hb = p.heads * p.batch;
-    const int qi = w / hb;
-    const int r = w - qi * hb;
+    const int qi = fdiv(w, p.f_hb);
+    const int r = w - qi * (p.heads * p.batch);
     Item x;
-    x.j = r % p.heads;
-    x.b = r / p.heads;
-    const int qb = nqb - 1 - qi;
-    const int shard = x.j / p.heads_per_shard;
+    x.b = fdiv(r, p.f_heads);
+    x.j = r - x.b * p.heads;
+    const int qb = p.nqb - 1 - qi;
+    const int shard = fdiv(x.j, p.f_hps);
     const int jl = x.j - shard * p.heads_per_shard;
-    const int g = x.j / (p.heads / p.kv_heads);
-    const int kv0 = (p.kv_heads >= p.t) ? shard * (p.kv_heads / p.t) : (shard * p.kv_heads) / p.t;
+    const int g = fdiv(x.j, p.f_grp);
+    const int kv0 = (p.kv_heads >= p.t) ? shard * p.kv_per_shard : fdiv(shard * p.kv_heads, p.f_t);
     x.qcol = shard * p.shard_w + jl * D;
     x.kcol = shard * p.shard_w + p.q_w + (g - kv0) * D;
     x.vcol = x.kcol + p.kv_w;
     x.tok0 = x.b * p.seq;
     x.q0 = qb * QB;
     // causal: keys 0 .. q0+127, and never past the sequence
-    x.nkb = min((x.q0 + QB + KB - 1) / KB, (p.seq + KB - 1) / KB);
+    x.nkb = min((x.q0 + QB + KB - 1) / KB, p.nkb_seq);
     return x;
 }
 
@@ -238,7 +261,7 @@ __global__ void __launch_bounds__(L::NTHREADS, L::CTAS) attn_tc_kernel(const __g
         return;  // the aligned layout does not fit: nothing was touched
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = ((p.seq + QB - 1) / QB) * p.heads * p.batch;
+    const int n_items = p.nqb * p.heads * p.batch;
     const int w0 = static_cast<int>(blockIdx.x), dw = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
@@ -795,6 +818,14 @@ int launch_d(const tpi::AttnArgs& a, cudaStream_t stream, std::string* err) {
     p.batch = a.batch;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
+    p.f_hb = make_fastdiv(static_cast<uint32_t>(a.heads * a.batch));
+    p.f_heads = make_fastdiv(static_cast<uint32_t>(a.heads));
+    p.f_hps = make_fastdiv(static_cast<uint32_t>(p.heads_per_shard));
+    p.f_grp = make_fastdiv(static_cast<uint32_t>(a.heads / a.kv_heads));
+    p.f_t = make_fastdiv(static_cast<uint32_t>(a.t));
+    p.nqb = (a.seq + QB - 1) / QB;
+    p.nkb_seq = (a.seq + KB - 1) / KB;
+    p.kv_per_shard = a.kv_heads / a.t;
     const int smem = L::SMEM;
     static bool configured[64] = {false};
     int dev = 0;
