@@ -85,9 +85,20 @@ __host__ __device__ constexpr int num_threads() {
 // adjacent n-tiles of one m-block: each A tile is read from L2 once and
 // multicast to both pairs (a quarter less operand traffic per MMA); the
 // other modes run one pair (or one CTA) per cluster.
-template <int MODE, int CG>
+// The QKV GEMM runs the same clusters on its 256-column tiles: a cluster
+// unit is two adjacent n-tiles of one m-block, one per pair, and each A
+// tile is read from L2 once for both pairs (multicast).  Clusters of four
+// fit on 144 of GB300's 152 SMs; QKV's 768 tiles take 11 rounds either way,
+// so the lighter L2 load is a net gain there (224 -> 219 us), while the
+// W1/W3 and rowwise GEMMs would gain rounds (47.2 -> 49.8 and 6.7 -> 7.1)
+// and ran no faster (W1/W3) or slower (W2 506 -> 560 us).
+template <int MODE>
+__host__ __device__ constexpr bool mc_mode() {
+    return MODE == tpi::GEMM_COL_QKV;
+}
+template <int MODE, int CG, int BNT = BN>
 __host__ __device__ constexpr int cluster_ctas() {
-    return MODE == tpi::GEMM_MLP ? 2 * CG : CG;
+    return (MODE == tpi::GEMM_MLP || (mc_mode<MODE>() && CG == 2 && BNT == BN)) ? 2 * CG : CG;
 }
 
 // CG = CTAs per tile.  CG = 1: a 128 x 256 tile per CTA, 4 stages of 48 KB.
@@ -135,6 +146,7 @@ struct GemmParams {
     int kb_per_shard;  // k-blocks of BK per shard (colwise: per whole K)
     int k_shards;      // shards walked inside the K loop (ROW_FUSED: t)
     int m_tiles, n_tiles, grid_shards, num_tiles;
+    int n_dec;  // n-columns of the decode grid: n_tiles, or pairs of n-tiles for cluster units
     int group_m;       // m-tiles per rasterisation group (weight-tile reuse in L2)
     int act;
     int b_rows0;       // rows of B0 (out-of-range chunks read zeros)
@@ -206,10 +218,10 @@ constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // 8 KB
 
 __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& s, int& mb,
                                             int& nb) {
-    const int per_shard = p.m_tiles * p.n_tiles;
+    const int per_shard = p.m_tiles * p.n_dec;
     s = tile / per_shard;
     const int r = tile - s * per_shard;
-    const int group_size = p.group_m * p.n_tiles;
+    const int group_size = p.group_m * p.n_dec;
     const int g = r / group_size;
     const int first_m = g * p.group_m;
     const int gm = min(p.m_tiles - first_m, p.group_m);
@@ -218,7 +230,7 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     nb = rr / gm;
     // Odd groups sweep the n-tiles backwards: a group starts on the weight
     // tiles the previous group ended on, which are still in L2.
-    if (g & 1) nb = p.n_tiles - 1 - nb;
+    if (g & 1) nb = p.n_dec - 1 - nb;
 }
 
 // GEMM_MLP unit u of a cluster: colwise units first (all m-blocks of one
@@ -475,36 +487,51 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
                                               uint32_t rank, volatile int* abort_flag) {
     using C = Cfg<MODE, CG, BNT>;
     constexpr bool ROW = (MODE == tpi::GEMM_ROW_FUSED || MODE == tpi::GEMM_ROW_PARTIAL);
+    constexpr int CL = cluster_ctas<MODE, CG, BNT>();
+    // Clusters of two pairs (MC): pair pc = rank / 2 takes n-tile 2 n + pc of
+    // a unit; each CTA loads 64 of its 128 A rows (the half pc) into its own
+    // stage and, by multicast, into the same-rank CTA of the other pair.
+    constexpr bool MC = CL == 2 * CG;
+    const int pc = MC ? static_cast<int>(rank >> 1) : 0;
+    const uint32_t prank = MC ? (rank & 1u) : rank;
+    const uint16_t a_mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+    constexpr uint32_t A_HALF = A_BYTES / 2;
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;
     bool ok = true;
-    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
         int s_grid, mb, nb;
         decode_tile(p, tile, s_grid, mb, nb);
-        const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
+        if (MC) nb = 2 * nb + pc;  // past the matrix when n_tiles is odd: B reads zeros
+        const int arow = mb * C::TILE_M + static_cast<int>(prank) * BM + (MC ? pc * (BM / 2) : 0);
         const CUtensorMap* bmap[C::CHUNKS];
         int brow[C::CHUNKS];
-        if (!ROW) b_boxes<MODE, C::CHUNKS>(p, nb, static_cast<int>(rank) * C::CHUNKS, bmap, brow);
+        if (!ROW) b_boxes<MODE, C::CHUNKS>(p, nb, static_cast<int>(prank) * C::CHUNKS, bmap, brow);
         for (int ks = 0; ok && ks < p.k_shards; ++ks) {
             const int shard = (MODE == tpi::GEMM_ROW_PARTIAL) ? s_grid : ks;
             for (int kb = 0; kb < p.kb_per_shard; ++kb) {
                 const uint32_t full = bar0 + 8 * stage, empty = bar0 + 8 * (C::STAGES + stage);
+                // MC: both pairs have consumed this stage (each pair's MMA
+                // commit arrives on every CTA's empty barrier).
                 if (!mbar_wait(empty, phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 // The leader's full barrier counts the bytes of both CTAs.
-                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
-                const uint32_t full_l = (CG == 2) ? mapa_shared(full, 0) : full;
+                if (prank == 0) mbar_arrive_expect_tx(full, CG * C::STAGE_BYTES);
+                const uint32_t full_l = (CG == 2) ? mapa_shared(full, rank & ~1u) : full;
                 const uint32_t a_dst = base + stage * C::STAGE_BYTES;
                 const uint32_t b_dst = a_dst + A_BYTES;
                 const int kc = kb * BK;
 #pragma unroll
                 for (int c = -1; c < C::CHUNKS; ++c) {
-                    const int cc = static_cast<int>(rank) * C::CHUNKS + c;  // B box of the tile
+                    const int cc = static_cast<int>(prank) * C::CHUNKS + c;  // B box of the tile
                     const uint32_t dst = c < 0 ? a_dst : b_dst + c * B_CHUNK_BYTES;
-                    if (ROW) {
+                    if (MC && c < 0) {
+                        if (ROW) tma_load_3d_pair_mc(a_dst + pc * A_HALF, &p.mapA, full_l, kc, shard, arow, a_mask);
+                        else tma_load_2d_pair_mc(a_dst + pc * A_HALF, &p.mapA, full_l, kc, arow, a_mask);
+                    } else if (ROW) {
                         const CUtensorMap* map = c < 0 ? &p.mapA : &p.mapB[0];
                         const int r = c < 0 ? arow : nb * BNT + cc * B_CHUNK_ROWS;
                         if (CG == 2) tma_load_3d_pair(dst, map, full_l, kc, shard, r);
@@ -542,7 +569,7 @@ __device__ __forceinline__ void producer_loop(const GemmParams& p, uint32_t base
             }
         }
     }
-    if (!ok && rank == 0) {
+    if (!ok && prank == 0) {
         // Let every copy of the pair land before the CTAs exit (the leader's
         // full barriers count both CTAs' bytes).
         for (int s = 0; s < C::STAGES; ++s)
@@ -648,7 +675,7 @@ __device__ __forceinline__ void mlp_producer_loop(const GemmParams& p, uint32_t 
 template <int MODE, int CG, int BNT>
 __device__ __forceinline__ void mma_loop(const GemmParams& p, uint32_t base, uint32_t bar0,
                                          uint32_t tmem_base, volatile int* abort_flag, uint32_t rank) {
-    constexpr int CL = cluster_ctas<MODE, CG>();
+    constexpr int CL = cluster_ctas<MODE, CG, BNT>();
     // Commit masks (cluster ranks): the accumulator goes to this pair; a
     // freed stage to every CTA whose stage this pair's MMAs read (with
     // multicast A, all CTAs of the cluster); the drain to this CTA.
@@ -1243,13 +1270,18 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
     constexpr int CPW_GLU = (BN / 64) / (EPI_WARPS / 4);    // SwiGLU: output chunks per warp
     const int cb = half * CPW, cb_glu = half * CPW_GLU;
     uint32_t acc = 0, acc_phase = 0;
-    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
+    constexpr int CL = cluster_ctas<MODE, CG, BNT>();
+    constexpr bool MC = CL == 2 * CG;  // clusters of two pairs: pair pc takes n-tile 2 n + pc
+    const int pc = MC ? static_cast<int>(rank >> 1) : 0;
+    const uint32_t prank = MC ? (rank & 1u) : rank;
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     for (int tile = cid; tile < p.num_tiles; tile += ncl) {
         int s_grid, mb, nb;
         decode_tile(p, tile, s_grid, mb, nb);
+        if (MC) nb = 2 * nb + pc;  // past the matrix when n_tiles is odd: the column checks store nothing
         const uint32_t tfull = bar0 + 8 * (2 * C::STAGES + acc);
         const uint32_t tempty = bar0 + 8 * (2 * C::STAGES + 2 + acc);
-        const int row = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
+        const int row = mb * C::TILE_M + static_cast<int>(prank) * BM + q * 32 + lane;
         const bool row_ok = row < p.M;
         // BWD_ACT: the saved pre-activations of the warp's first two chunks
         // are fetched while the accumulator is still being computed; each
@@ -1278,7 +1310,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         uint32_t r[32];
         if (MODE == tpi::GEMM_BWD_ACT) {
             // One branch-free chunk loop per activation, chosen once per tile.
-            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const int row0 = mb * C::TILE_M + static_cast<int>(prank) * BM + q * 32;
             const uint32_t sbuf = epi0 + static_cast<uint32_t>(warp - 2) * 3 * EPI_BOX_BYTES;
             switch (p.act) {
                 case TP_ACT_SWIGLU:
@@ -1300,7 +1332,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
             // (j ^ (r % 8)) * 16); one TMA store, or reduce-add when
             // accumulating, per 32-column chunk.  The warp's 32 rows lie in
             // one output (row splits are multiples of 32).
-            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const int row0 = mb * C::TILE_M + static_cast<int>(prank) * BM + q * 32;
             const bool box_ok = row0 < p.M;
             const int which = row0 >= p.row_split2 ? 2 : (row0 >= p.row_split ? 1 : 0);
             const int ybase = row0 - (which == 2 ? p.row_split2 : (which == 1 ? p.row_split : 0));
@@ -1369,7 +1401,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
                 }
             }
         } else if (MODE == tpi::GEMM_COL_ACT && C::COL_STAGED && p.o_staged) {
-            const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+            const int row0 = mb * C::TILE_M + static_cast<int>(prank) * BM + q * 32;
             const uint32_t sbuf = epi0 + static_cast<uint32_t>(warp - 2) * 2 * EPI_BOX_BYTES;
             switch (p.act) {
                 case TP_ACT_GELU_ERF:
@@ -1403,7 +1435,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmParams& p, uint32_t bar0
         // Release the accumulator: the leader's MMA waits for the epilogue
         // warps of both CTAs.
         if (lane == 0) {
-            if (CG == 2) mbar_arrive_cluster(mapa_shared(tempty, 0));
+            if (CG == 2) mbar_arrive_cluster(mapa_shared(tempty, rank & ~1u));
             else mbar_arrive(tempty);
         }
         acc ^= 1u;
@@ -1432,7 +1464,7 @@ __global__ void __launch_bounds__(num_threads<MODE>(), 1) tp_gemm_kernel(const _
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Rank in the cluster (GEMM_MLP: 0..3, pairs (0, 1) and (2, 3)).
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    constexpr int CL = cluster_ctas<MODE, CG>();
+    constexpr int CL = cluster_ctas<MODE, CG, BNT>();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar0 + 8 * s, 1);                // full: leader's arrive + both CTAs' bytes
@@ -1578,7 +1610,7 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster_ctas<MODE, CG>();
+    attr[0].val.clusterDim.x = cluster_ctas<MODE, CG, BNT>();
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     tpi::pdl_attribute(attr[1]);
@@ -1591,6 +1623,41 @@ int launch_mode(const GemmParams& p, int grid, cudaStream_t stream, std::string*
         return TP_ERR_CUDA;
     }
     return TP_OK;
+}
+
+// Clusters of four CTAs of the wide-tile kernel of MODE that fit on the
+// current device at once (0 when the query fails).
+template <int MODE>
+int max_clusters() {
+    static int counts[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 0;
+    if (!counts[dev]) {
+        constexpr int CG = TP_GEMM_CTA_PAIR;
+        constexpr int CL = cluster_ctas<MODE, CG, BN>();
+        auto kern = tp_gemm_kernel<MODE, CG, BN>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MODE, CG, BN>::SMEM) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t cfg;
+            memset(&cfg, 0, sizeof(cfg));
+            cfg.gridDim = dim3(CL * 64, 1, 1);
+            cfg.blockDim = dim3(num_threads<MODE>(), 1, 1);
+            cfg.dynamicSmemBytes = Cfg<MODE, CG, BN>::SMEM;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = CL;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        counts[dev] = n > 0 ? n : -1;
+    }
+    return counts[dev] > 0 ? counts[dev] : 0;
 }
 
 }  // namespace
@@ -1652,13 +1719,16 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         if (narrow) p.n_tiles = static_cast<int>(n_narrow);
     }
     p.shard_stride = a.M * a.ldo;
+    // Clusters of two pairs with multicast A halves (see mc_mode).
+    const bool mc = a.mode == GEMM_COL_QKV && kPairTiles == 2;
+    const uint32_t a_rows = mc ? BM / 2 : BM;  // A box rows a CTA loads
     if (row) {
         p.kb_per_shard = static_cast<int>((a.Ks + BK - 1) / BK);
         p.k_shards = (a.mode == GEMM_ROW_FUSED) ? a.t : 1;
         // A: [M][t*Ks] seen as (Ks, t, M); B: [N][t*Ks] seen as (Ks, t, N).
         const uint64_t dA[3] = {(uint64_t)a.Ks, (uint64_t)a.t, (uint64_t)a.M};
         const uint64_t sA[2] = {(uint64_t)a.Ks * 2, (uint64_t)a.t * a.Ks * 2};
-        const uint32_t bA[3] = {BK, 1, BM};
+        const uint32_t bA[3] = {BK, 1, a_rows};
         if (!make_map(&p.mapA, a.A, 3, dA, sA, bA, err)) return TP_ERR_CUDA;
         const uint64_t dB[3] = {(uint64_t)a.Ks, (uint64_t)a.t, (uint64_t)a.N};
         const uint32_t bB[3] = {BK, 1, B_CHUNK_ROWS};
@@ -1754,7 +1824,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
         p.k_shards = 1;
         const uint64_t dA[2] = {(uint64_t)a.K, (uint64_t)a.M};
         const uint64_t sA[1] = {(uint64_t)a.K * 2};
-        const uint32_t bA[2] = {BK, BM};
+        const uint32_t bA[2] = {BK, a_rows};
         if (!make_map(&p.mapA, a.A, 2, dA, sA, bA, err)) return TP_ERR_CUDA;
         const void* bs[3] = {a.B0, a.B1, a.B2};
         const int64_t rows[3] = {a.B0_rows, a.B1_rows, a.B2_rows};
@@ -1797,9 +1867,19 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     // Measured on GB300 at the layer's shapes with 256-row pair tiles: 16
     // is best (W1/W3 2005 TFLOP/s vs 1941 at 32 and 1884 at 4).
     p.group_m = 16;
-    p.num_tiles = p.grid_shards * p.m_tiles * p.n_tiles;
+    p.n_dec = mc ? (p.n_tiles + 1) / 2 : p.n_tiles;
+    p.num_tiles = p.grid_shards * p.m_tiles * p.n_dec;  // tiles, or cluster units of two tiles
     if (p.num_tiles == 0) return TP_OK;
-    const int grid = std::min(p.num_tiles, device_sm_count() / CG) * CG;
+    int grid = std::min(p.num_tiles, device_sm_count() / CG) * CG;
+    if (mc) {
+        // Every cluster resident at once: as many as fit (144 SMs on GB300).
+        const int clusters = max_clusters<GEMM_COL_QKV>();
+        if (clusters < 1) {
+            if (err) *err = "no cluster of four CTAs fits on this device";
+            return TP_ERR_CUDA;
+        }
+        grid = std::min(p.num_tiles, clusters) * 2 * CG;
+    }
     switch (a.mode) {
         case GEMM_COL_ACT: return launch_mode<GEMM_COL_ACT, CG>(p, grid, stream, err);
         case GEMM_COL_SWIGLU: return launch_mode<GEMM_COL_SWIGLU, CG>(p, grid, stream, err);
