@@ -220,7 +220,11 @@ def _qkv_ref(s, inp):
     return np.concatenate(blocks, axis=1)
 
 
-@pytest.mark.parametrize("a,k,t,d", [(8, 2, 4, 64), (8, 8, 4, 128), (4, 1, 4, 128), (8, 4, 2, 64)])
+# The QKV GEMM runs clusters of two CTA pairs over pairs of 256-column
+# tiles; (6, 2, 2, 64) and (4, 4, 4, 64) have an odd tile count (3, ragged),
+# so one pair's tile of the last unit lies past the matrix.
+@pytest.mark.parametrize("a,k,t,d", [(8, 2, 4, 64), (8, 8, 4, 128), (4, 1, 4, 128), (8, 4, 2, 64),
+                                     (6, 2, 2, 64), (4, 4, 4, 64)])
 def test_qkv_integer_bit_exact(a, k, t, d):
     s = Shape("q", 2, 150, 192, heads=a, kv_heads=k, head_dim=d, tp=t, act="none", index=14)
     inp = synth.workload_inputs(s, integer=(-2, 2))
