@@ -160,8 +160,9 @@ def run_layer(s, inp, mode):
     return host64(Y)
 
 
-# h = 200 leaves a partial last k-block in the GEMMs over h (zero-filled
-# columns), which the QKV GEMM's in-kernel row statistics of x must ignore.
+# h = 200 leaves a partial last k-block in the GEMMs over h (their loads past
+# column 200 read zeros) and a row of 25 16-byte vectors for the pass that
+# takes the row statistics of x (FUSED folds the norm into the GEMMs).
 @pytest.mark.parametrize("s", [Shape("l", 2, 140, 256, ffn=768, heads=8, kv_heads=2, head_dim=64, tp=4,
                                      act="swiglu", index=26),
                                Shape("l_ragged_k", 2, 130, 200, ffn=384, heads=4, kv_heads=2, head_dim=64,
