@@ -1,6 +1,6 @@
 """Compile the C oracle into oracle/_build/libtp_oracle.so with gcc.
 
-Test infrastructure: building the checker is not using it.  Plain C11 with
+Test infrastructure: the library never links or calls it.  Plain C11 with
 OpenMP; no architecture-specific flags, so the same source builds on x86_64
 and aarch64 hosts.
 """
