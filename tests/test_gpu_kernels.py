@@ -242,12 +242,16 @@ def test_qkv_integer_bit_exact(a, k, t, d):
 # sequences) and (8, 512, 24, 8, 8) 768, over twice as many as the kernel's
 # persistent grid holds on GB300, so every CTA runs several items back to
 # back; (6, 1000, 16, 4, 4) adds a ragged last query tile and key block to
-# that, and (1, 1, ...) is a one-token sequence.
+# that, and (1, 1, ...) is a one-token sequence.  The 8192- and 5000-token
+# sequences give items of up to 64 key blocks (the layer's have 16), so the
+# K/V rings and S buffers wrap many times within one item; 5000 also ends
+# in a ragged tile at d = 64.
 @pytest.mark.parametrize("batch,seq,a,k,t,d", [(2, 200, 8, 2, 4, 64), (1, 130, 4, 4, 2, 128),
                                                (3, 64, 8, 1, 8, 128), (1, 1, 4, 2, 2, 64),
                                                (2, 257, 16, 8, 8, 128), (8, 512, 32, 8, 8, 128),
                                                (4, 700, 8, 2, 2, 128), (6, 1000, 16, 4, 4, 128),
-                                               (8, 512, 24, 8, 8, 128), (1, 1, 4, 2, 2, 128)])
+                                               (8, 512, 24, 8, 8, 128), (1, 1, 4, 2, 2, 128),
+                                               (1, 8192, 4, 1, 2, 128), (1, 5000, 4, 2, 2, 64)])
 def test_attention_core_vs_oracle(batch, seq, a, k, t, d):
     s = Shape("ac", batch, seq, 64, heads=a, kv_heads=k, head_dim=d, tp=t, act="none", index=15)
     plan = plan_for(s)
