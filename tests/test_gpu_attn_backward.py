@@ -84,6 +84,25 @@ def test_small_attention_backward_full_output(s):
         assert_close(host64(got[n]), ref[n], what=f"{s.name} {n}")
 
 
+# Long sequences: a 128-key block's CTA loops over up to 64 causal 64-query
+# blocks per query head (the full-size case has 32), and 3000 tokens end in
+# ragged query and key blocks at d = 64.
+LONG = [
+    Shape("ab_long_seq", 1, 4096, 256, heads=4, kv_heads=1, head_dim=128, tp=2, act="none", index=66),
+    Shape("ab_d64_long_seq_ragged", 1, 3000, 256, heads=4, kv_heads=2, head_dim=64, tp=2, act="none", index=67),
+]
+
+
+@pytest.mark.parametrize("s", LONG, ids=[s.name for s in LONG])
+def test_long_sequence_attention_backward_full_output(s):
+    inp = synth.workload_inputs(s)
+    dOut = synth.grad_output(s)
+    got = run_backward(s, inp, dOut)
+    ref = oracle_grads(s, inp, dOut)
+    for n in ("dX", "dWq", "dWk", "dWv", "dWo"):
+        assert_close(host64(got[n]), ref[n], what=f"{s.name} {n}")
+
+
 def test_recomputed_forward_state_gives_the_same_gradients():
     # With QKV, O and LSE recomputed the inputs of every kernel are the same
     # values; only the order of the fp32 dQ additions differs.
