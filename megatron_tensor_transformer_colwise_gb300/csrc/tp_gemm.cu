@@ -1865,11 +1865,15 @@ int gemm_launch(const GemmArgs& a, cudaStream_t stream, std::string* err) {
     // Tiles run in groups of group_m m-tiles sweeping all n-tiles, so a wave
     // of SM-count CTAs shares a few weight (B) tiles across many m-tiles.
     // Measured on GB300 at the layer's shapes with 256-row pair tiles: 16
-    // is best for the colwise GEMMs (W1/W3 2005 TFLOP/s vs 1941 at 32 and
-    // 1884 at 4), 8 for the rowwise ones, whose A panels (all shards' K)
-    // are longer: W2 509-510 us against 516-525 us at 16, and 1.06 GB of
-    // DRAM reads per launch against 1.27 GB.
-    p.group_m = (a.mode == GEMM_ROW_FUSED || a.mode == GEMM_ROW_PARTIAL) ? 8 : 16;
+    // is best for the forward colwise GEMMs (W1/W3 2005 TFLOP/s vs 1941 at
+    // 32 and 1884 at 4; 930 us vs 934-947 us at 8 and 12), 8 for the
+    // rowwise ones, whose A panels (all shards' K) are longer (W2 509-510 us
+    // against 516-525 us at 16, and 1.06 GB of DRAM reads per launch
+    // against 1.27 GB), and 8 for the backward GEMMs (MLP backward
+    // 3180-3220 us against 3237-3281 us at 16).
+    const bool colwise_fwd = a.mode == GEMM_COL_ACT || a.mode == GEMM_COL_SWIGLU || a.mode == GEMM_COL_QKV ||
+                             a.mode == GEMM_COL_PACKED;
+    p.group_m = colwise_fwd ? 16 : 8;
     p.n_dec = mc ? (p.n_tiles + 1) / 2 : p.n_tiles;
     p.num_tiles = p.grid_shards * p.m_tiles * p.n_dec;  // tiles, or cluster units of two tiles
     if (p.num_tiles == 0) return TP_OK;
